@@ -1,0 +1,247 @@
+"""CPU oracle for the paged speculative-verification step -- TEST INFRASTRUCTURE.
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may import
+this package.  The library itself never does: it has no CPU fallback.
+
+The arithmetic lives in ``svpa_oracle.c`` (plain C, fp64, OpenMP); this module
+compiles it with gcc on first use and wraps it with numpy arrays.  It shares
+no code with the CUDA library.
+
+Parity status of each function (what pins it is in ``tests/test_oracle_*.py``):
+  paged_verify_attn    pinned (library SDPA special case, brute force,
+                       closed forms, block-permutation invariance, FP8 decode
+                       table)
+  spec_accept          pinned (Monte-Carlo output distribution = P, mean
+                       accepted length = E[K] formula, special cases)
+  spec_accept_tree     pinned (reduces to spec_accept on a chain; Monte-Carlo
+                       distribution of the first emitted token = P[root])
+  block_table_commit   pinned (hand-worked example, conservation invariants,
+                       tree compaction moves the path's K/V bytes)
+  expected_accepted, speedup
+                       pinned (the worked example: alpha >= 0.85, r ~ 0.08
+                       gives eta >= 2.8)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "svpa_oracle.c")
+_LIB = os.path.join(_HERE, "libsvpa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle (gcc, OpenMP, no FMA contraction); return the .so path."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+               "-ffp-contract=off", "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+            lib.oracle_paged_verify_attn.argtypes = [I] * 9 + [D] + [P] * 10 + [I]
+            lib.oracle_paged_verify_attn.restype = I
+            lib.oracle_spec_accept.argtypes = [I, I, I] + [P] * 9 + [I]
+            lib.oracle_spec_accept.restype = I
+            lib.oracle_spec_accept_tree.argtypes = [I, I, I] + [P] * 10 + [I]
+            lib.oracle_spec_accept_tree.restype = I
+            lib.oracle_block_table_commit.argtypes = [I] * 5 + [P] * 7 + [I, P, P, I, I, I]
+            lib.oracle_block_table_commit.restype = I
+            lib.oracle_tree_max_depth.argtypes = [P, I]
+            lib.oracle_tree_max_depth.restype = I
+            lib.oracle_expected_accepted.argtypes = [P, I]
+            lib.oracle_expected_accepted.restype = D
+            lib.oracle_speedup.argtypes = [D, I, D]
+            lib.oracle_speedup.restype = D
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_double.restype = D
+            lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_double.restype = D
+            lib.oracle_max_threads.argtypes = []
+            lib.oracle_max_threads.restype = I
+            _lib = lib
+    return _lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _c(a, dtype):
+    """Contiguous numpy array of ``a`` as ``dtype`` (accepts torch CPU tensors).
+
+    bf16 tensors become their uint16 bit patterns and FP8 tensors their bytes.
+    """
+    if a is None:
+        return None
+    if hasattr(a, "detach"):
+        import torch
+        t = a.detach().cpu().contiguous()
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16)
+        elif t.dtype.itemsize == 1 and t.dtype.is_floating_point:
+            t = t.view(torch.uint8)
+        a = t.numpy()
+    a = np.asarray(a)
+    dt = np.dtype(dtype)
+    if a.dtype != dt and a.dtype.itemsize == dt.itemsize and dt.kind == "u" and a.dtype.kind in "iu":
+        a = a.view(dt)
+    return np.ascontiguousarray(a, dtype=dt)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def max_threads() -> int:
+    return _load().oracle_max_threads()
+
+
+def bf16_to_double(bits: int) -> float:
+    return _load().oracle_bf16_to_double(int(bits))
+
+
+def e4m3_to_double(byte: int) -> float:
+    return _load().oracle_e4m3_to_double(int(byte))
+
+
+def paged_verify_attn(q_bits, k_pool, v_pool, block_table, context_lens, *,
+                      num_kv_heads, sm_scale, kv_fp8=False, k_scale=None,
+                      v_scale=None, ancestor_mask=None, nthreads=0):
+    """fp64 masked attention of each sequence's n_q queries over its paged history.
+
+    q_bits: uint16 bf16 bits [B, n_q, Hq, D]; k_pool/v_pool: uint16 bf16 bits or
+    uint8 E4M3 bytes [num_blocks, Hkv, BS, D]; block_table int32 [B, max_blocks];
+    context_lens int32 [B]; ancestor_mask uint64 [n_q] or None (causal).
+    Returns (out fp64 [B, n_q, Hq, D], lse fp64 [B, n_q, Hq]).
+    """
+    lib = _load()
+    q = _c(q_bits, np.uint16)
+    kp = _c(k_pool, np.uint8 if kv_fp8 else np.uint16)
+    vp = _c(v_pool, np.uint8 if kv_fp8 else np.uint16)
+    bt = _c(block_table, np.int32)
+    cl = _c(context_lens, np.int32)
+    ks = _c(k_scale, np.float32)
+    vs = _c(v_scale, np.float32)
+    am = _c(ancestor_mask, np.uint64)
+    B, n_q, Hq, D = q.shape
+    num_blocks, Hkv, BS, D2 = kp.shape
+    assert D2 == D and Hkv == num_kv_heads
+    out = np.zeros((B, n_q, Hq, D), np.float64)
+    lse = np.zeros((B, n_q, Hq), np.float64)
+    rc = lib.oracle_paged_verify_attn(B, n_q, Hq, Hkv, D, BS, bt.shape[1], num_blocks,
+                                      int(bool(kv_fp8)), float(sm_scale), _ptr(q),
+                                      _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt),
+                                      _ptr(cl), _ptr(am), _ptr(out), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise OracleError(f"oracle_paged_verify_attn failed with status {rc}")
+    return out, lse
+
+
+def spec_accept(p_probs, q_probs, draft_tokens, u_accept, u_sample, nthreads=0):
+    """Linear rejection sampler. Returns (accepted_len, out_tokens, near_boundary, dist)."""
+    lib = _load()
+    P = _c(p_probs, np.float32)
+    Q = _c(q_probs, np.float32)
+    x = _c(draft_tokens, np.int32)
+    ua = _c(u_accept, np.float32)
+    us = _c(u_sample, np.float32)
+    B, g1, V = P.shape
+    gamma = g1 - 1
+    assert Q.shape == (B, gamma, V) and x.shape == (B, gamma)
+    k = np.zeros(B, np.int32)
+    out = np.zeros((B, gamma + 1), np.int32)
+    near = np.zeros(B, np.uint8)
+    dist = np.zeros(B, np.float64)
+    rc = lib.oracle_spec_accept(B, gamma, V, _ptr(P), _ptr(Q), _ptr(x), _ptr(ua), _ptr(us),
+                                _ptr(k), _ptr(out), _ptr(near), _ptr(dist), int(nthreads))
+    if rc != 0:
+        raise OracleError(f"oracle_spec_accept failed with status {rc}")
+    return k, out, near.astype(bool), dist
+
+
+def tree_max_depth(parent) -> int:
+    par = _c(parent, np.int32)
+    return _load().oracle_tree_max_depth(_ptr(par), par.shape[0])
+
+
+def spec_accept_tree(parent, p_probs, q_probs, node_tokens, u_accept, u_sample, nthreads=0):
+    """Tree rejection sampler. Returns (accepted_len, path_nodes, out_tokens, near)."""
+    lib = _load()
+    par = _c(parent, np.int32)
+    P = _c(p_probs, np.float32)
+    Q = _c(q_probs, np.float32)
+    tok = _c(node_tokens, np.int32)
+    ua = _c(u_accept, np.float32)
+    us = _c(u_sample, np.float32)
+    B, n_nodes, V = P.shape
+    W = tree_max_depth(par) + 1
+    k = np.zeros(B, np.int32)
+    path = np.zeros((B, W), np.int32)
+    out = np.zeros((B, W), np.int32)
+    near = np.zeros(B, np.uint8)
+    rc = lib.oracle_spec_accept_tree(B, n_nodes, V, _ptr(par), _ptr(P), _ptr(Q), _ptr(tok),
+                                     _ptr(ua), _ptr(us), _ptr(k), _ptr(path), _ptr(out),
+                                     _ptr(near), int(nthreads))
+    if rc != 0:
+        raise OracleError(f"oracle_spec_accept_tree failed with status {rc}")
+    return k, path, out, near.astype(bool)
+
+
+def block_table_commit(block_table, context_lens, accepted_len, refcount, free_stack,
+                       free_top, *, n_q, block_size=16, path_nodes=None, k_pool=None,
+                       v_pool=None):
+    """Commit/rollback on copies of the inputs; returns the updated copies.
+
+    Returns dict(block_table, context_lens, refcount, free_stack, free_top,
+    k_pool, v_pool) -- pools only when path_nodes is given (tree compaction).
+    """
+    lib = _load()
+    bt = _c(block_table, np.int32).copy()
+    cl = _c(context_lens, np.int32).copy()
+    k = _c(accepted_len, np.int32)
+    rcnt = _c(refcount, np.int32).copy()
+    fs = _c(free_stack, np.int32).copy()
+    ft = np.array([int(free_top)], np.int32)
+    B, max_blocks = bt.shape
+    num_blocks = rcnt.shape[0]
+    path = _c(path_nodes, np.int32)
+    kp = vp = None
+    Hkv = D = eb = 0
+    if path is not None:
+        kp = np.ascontiguousarray(np.asarray(k_pool)).copy()
+        vp = np.ascontiguousarray(np.asarray(v_pool)).copy()
+        _, Hkv, _, D = kp.shape
+        eb = kp.dtype.itemsize
+    rc = lib.oracle_block_table_commit(B, n_q, block_size, max_blocks, num_blocks, _ptr(bt),
+                                       _ptr(cl), _ptr(k), _ptr(rcnt), _ptr(fs), _ptr(ft),
+                                       _ptr(path), 0 if path is None else path.shape[1],
+                                       _ptr(kp), _ptr(vp), Hkv, D, eb)
+    if rc != 0:
+        raise OracleError(f"oracle_block_table_commit failed with status {rc}")
+    return dict(block_table=bt, context_lens=cl, refcount=rcnt, free_stack=fs,
+                free_top=int(ft[0]), k_pool=kp, v_pool=vp)
+
+
+def expected_accepted(alpha) -> float:
+    a = np.ascontiguousarray(np.asarray(alpha, np.float64))
+    return _load().oracle_expected_accepted(_ptr(a), a.shape[0])
+
+
+def speedup(expected_k: float, gamma: int, r: float) -> float:
+    return _load().oracle_speedup(float(expected_k), int(gamma), float(r))

@@ -1,0 +1,537 @@
+/*
+ * svpa_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously-correct CPU restatement of the verification step of
+ * speculative decoding over a paged KV cache.  It exists to check the CUDA
+ * library; nothing in the product path may link or call it.  It shares no
+ * code, header or constant with the CUDA sources.
+ *
+ * Precision: every attention quantity is fp64, computed from the stored bf16
+ * or FP8-E4M3 bits.  The draft/target acceptance test is the one fp32 step (a
+ * single rounded fp32 multiply u*Q compared with P); residual sums and CDFs
+ * are fp64.  Compile with -ffp-contract=off so that no multiply-add is fused.
+ *
+ * Sources (page title, section / equation):
+ *  - "The Sub-Millisecond Speculative Decoding Meltdown" (atozofsoftwareengineering
+ *    blog), section "Speculative Decoding Mechanics & The K-Token Penalty",
+ *    equation A_speculative = Softmax((Q K^T + M_tree)/sqrt(d_k)) V; section
+ *    "Triton CUDA Fused Speculative Tree-Verification Kernel" (block-table
+ *    lookup per page, K/V cache layout [blocks, heads, block_size, dim],
+ *    per-block per-head K/V scales); section "Custom FP8 Quantized Memory
+ *    Block Layout" (e4m3 pages with per-block scale factors).
+ *  - "LOW-LATENCY INFERENCE: SPECULATIVE DECODING & PAGING" (innvotechnologies),
+ *    section "Verification Acceptance Probabilities and Speedup Math"
+ *    (alpha_i = min(1, P(x_i)/Q(x_i)), E[K], eta) and the architecture diagram
+ *    (commit to block table on accept; discard KV blocks and resample on reject).
+ *  - "Speculative Decoding & KV-Cache PagedAttention in Enterprise LLM Serving"
+ *    (paurushmuley.com), PagedKVCacheManager: reference counts, release of a
+ *    block to the free pool when its count reaches zero, block size 16.
+ *  - "Speculative Decoding and KV-Cache Compression" (futurestack.online),
+ *    section 2.2/2.3 (exact target distribution; the bundle's K/V is present
+ *    before any acceptance decision).
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *  resample from normalise(max(0, P_k - Q_k)); bonus token from P at position
+ *  gamma when every draft is accepted; inverse-CDF pick = first t whose
+ *  cumulative mass exceeds u*S (strict); accept iff fp32(u*Q) <= P; a draw
+ *  within 1e-6 of a CDF boundary is flagged; new committed length after the
+ *  step = L + k + 1; tree acceptance by recursive residual rejection over a
+ *  node's children in index order.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_ERR_ARG 1
+#define ORC_ERR_BAD_BLOCK 5
+#define ORC_ERR_OUT_OF_BLOCKS 4
+
+/* ------------------------------------------------------------------ */
+/* Number formats                                                      */
+/* ------------------------------------------------------------------ */
+
+/* bf16 is the upper half of an IEEE binary32. */
+double oracle_bf16_to_double(uint16_t bits) {
+    uint32_t w = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* OCP 8-bit floating point, E4M3 ("fn") variant: 1 sign bit, 4 exponent bits
+ * with bias 7, 3 mantissa bits; exponent field 0 is subnormal
+ * (m/8 * 2^(1-7)); there is no infinity; S.1111.111 is NaN; the largest
+ * finite magnitude is S.1111.110 = 1.75 * 2^8 = 448. */
+double oracle_e4m3_to_double(uint8_t byte) {
+    int s = (byte >> 7) & 1;
+    int e = (byte >> 3) & 15;
+    int m = byte & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, 1 - 7);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+static int set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+    return omp_get_max_threads();
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------ */
+/* paged verification attention                                        */
+/* ------------------------------------------------------------------ */
+
+/*
+ * For every sequence b, query j (0..n_q-1) and query head h:
+ *   the queries sit at positions L_b .. L_b+n_q-1 (their K/V are already in
+ *   the pool); the positions present are p < T_b = L_b + n_q;
+ *   K[p], V[p] come from physical block block_table[b][p / BS], slot p % BS;
+ *   FP8 pools decode each byte and multiply by the (block, kv head) scale;
+ *   query j sees every p < L_b, and a speculative slot p = L_b + i (i < n_q)
+ *   when i is an ancestor of j or j itself (bit i of ancestor_mask[j]);
+ *   with no mask, i <= j (causal);
+ *   s_p = (q_j . K[p]) * sm_scale;  w = softmax over the visible p;
+ *   out[b][j][h] = sum_p w_p V[p];  lse = log(sum_p exp(s_p)).
+ * The kv head of query head h is h / (Hq / Hkv).
+ * Inputs: q bf16 bits [B, n_q, Hq, D]; k_pool, v_pool [num_blocks, Hkv, BS, D]
+ * of bf16 bits (kv_fp8 == 0) or E4M3 bytes (kv_fp8 != 0); k_scale, v_scale
+ * fp32 [num_blocks, Hkv] (FP8 only); block_table int32 [B, max_blocks];
+ * context_lens int32 [B]; ancestor_mask uint64 [n_q] or NULL.
+ * Outputs: out fp64 [B, n_q, Hq, D]; lse fp64 [B, n_q, Hq] (may be NULL).
+ */
+int oracle_paged_verify_attn(int B, int n_q, int Hq, int Hkv, int D, int BS,
+                             int max_blocks, int num_blocks, int kv_fp8,
+                             double sm_scale, const uint16_t *q,
+                             const void *k_pool, const void *v_pool,
+                             const float *k_scale, const float *v_scale,
+                             const int32_t *block_table,
+                             const int32_t *context_lens,
+                             const uint64_t *ancestor_mask, double *out,
+                             double *lse, int nthreads) {
+    if (B < 0 || n_q < 1 || n_q > 64 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 ||
+        D < 1 || BS < 1 || max_blocks < 1 || num_blocks < 1)
+        return ORC_ERR_ARG;
+    if (kv_fp8 && (!k_scale || !v_scale)) return ORC_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        long T = (long)context_lens[b] + n_q;
+        if (context_lens[b] < 0 || (T + BS - 1) / BS > max_blocks) return ORC_ERR_ARG;
+        for (long i = 0; i < (T + BS - 1) / BS; ++i) {
+            int32_t blk = block_table[(long)b * max_blocks + i];
+            if (blk < 0 || blk >= num_blocks) return ORC_ERR_BAD_BLOCK;
+        }
+    }
+    const int G = Hq / Hkv;
+    set_threads(nthreads);
+    long units = (long)B * Hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long unit = 0; unit < units; ++unit) {
+        int b = (int)(unit / Hkv), g = (int)(unit % Hkv);
+        long L = context_lens[b];
+        long T = L + n_q;
+        /* 1. gather this (sequence, kv head)'s history into contiguous fp64 */
+        double *K = (double *)malloc(sizeof(double) * (size_t)(T * D + 1));
+        double *V = (double *)malloc(sizeof(double) * (size_t)(T * D + 1));
+        double *s = (double *)malloc(sizeof(double) * (size_t)(T + 1));
+        for (long p = 0; p < T; ++p) {
+            int32_t blk = block_table[(long)b * max_blocks + p / BS];
+            long slot = p % BS;
+            long base = (((long)blk * Hkv + g) * BS + slot) * D;
+            for (int d = 0; d < D; ++d) {
+                if (kv_fp8) {
+                    const uint8_t *kp = (const uint8_t *)k_pool;
+                    const uint8_t *vp = (const uint8_t *)v_pool;
+                    K[p * D + d] = oracle_e4m3_to_double(kp[base + d]) *
+                                   (double)k_scale[(long)blk * Hkv + g];
+                    V[p * D + d] = oracle_e4m3_to_double(vp[base + d]) *
+                                   (double)v_scale[(long)blk * Hkv + g];
+                } else {
+                    const uint16_t *kp = (const uint16_t *)k_pool;
+                    const uint16_t *vp = (const uint16_t *)v_pool;
+                    K[p * D + d] = oracle_bf16_to_double(kp[base + d]);
+                    V[p * D + d] = oracle_bf16_to_double(vp[base + d]);
+                }
+            }
+        }
+        /* 2. textbook masked softmax(q K^T * scale) V for each query row */
+        for (int gi = 0; gi < G; ++gi) {
+            int h = g * G + gi;
+            for (int j = 0; j < n_q; ++j) {
+                const uint16_t *qv = q + (((long)b * n_q + j) * Hq + h) * D;
+                double mx = -INFINITY;
+                for (long p = 0; p < T; ++p) {
+                    int visible;
+                    if (p < L) {
+                        visible = 1;
+                    } else {
+                        long i = p - L;
+                        if (ancestor_mask)
+                            visible = (int)((ancestor_mask[j] >> i) & 1ull);
+                        else
+                            visible = i <= j;
+                    }
+                    if (!visible) {
+                        s[p] = -INFINITY;
+                        continue;
+                    }
+                    double acc = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        acc += oracle_bf16_to_double(qv[d]) * K[p * D + d];
+                    s[p] = acc * sm_scale;
+                    if (s[p] > mx) mx = s[p];
+                }
+                double sum = 0.0;
+                for (long p = 0; p < T; ++p)
+                    if (s[p] != -INFINITY) sum += exp(s[p] - mx);
+                double *o = out + (((long)b * n_q + j) * Hq + h) * D;
+                for (int d = 0; d < D; ++d) o[d] = 0.0;
+                for (long p = 0; p < T; ++p) {
+                    if (s[p] == -INFINITY) continue;
+                    double w = exp(s[p] - mx) / sum;
+                    for (int d = 0; d < D; ++d) o[d] += w * V[p * D + d];
+                }
+                if (lse) lse[((long)b * n_q + j) * Hq + h] = mx + log(sum);
+            }
+        }
+        free(K);
+        free(V);
+        free(s);
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* rejection sampler                                                   */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Inverse-CDF draw from unnormalised non-negative weights r[0..V-1]:
+ * S = sum r; the token is the first t whose running sum C_t exceeds u*S.
+ * *near is set when some C_t/S lies within 1e-6 of u (a draw that fp32 and
+ * fp64 arithmetic may resolve differently).  Returns -1 when S == 0.
+ */
+static int32_t draw_inverse_cdf(const double *r, int V, double u, uint8_t *near,
+                                double *dist) {
+    double S = 0.0;
+    for (int t = 0; t < V; ++t) S += r[t];
+    if (!(S > 0.0)) return -1;
+    double target = u * S;
+    double C = 0.0, best = INFINITY;
+    int32_t tok = -1;
+    for (int t = 0; t < V; ++t) {
+        C += r[t];
+        double dd = fabs(C / S - u);
+        if (dd < best) best = dd;
+        if (tok < 0 && C > target) tok = t;
+    }
+    if (tok < 0) {
+        /* u*S >= S can only come from rounding: take the last token with mass */
+        for (int t = V - 1; t >= 0; --t)
+            if (r[t] > 0.0) { tok = t; break; }
+    }
+    if (near) *near = best < 1e-6;
+    if (dist) *dist = best;
+    return tok;
+}
+
+/* The draft/target acceptance test alpha_i = min(1, P/Q) realised with one
+ * uniform: accept iff u*Q <= P, the product rounded once to fp32. */
+static int accept_test(float u, float qx, float px) {
+    volatile float a = u * qx; /* one rounded fp32 multiply, never fused */
+    return a <= px;
+}
+
+/*
+ * Linear speculative sampler, one row per sequence.
+ * P fp32 [B, gamma+1, V] target distributions at the gamma+1 query positions;
+ * Q fp32 [B, gamma, V] draft distributions; x int32 [B, gamma] draft tokens;
+ * u_acc fp32 [B, gamma]; u_s fp32 [B].
+ * Outputs accepted_len [B] (k), out_tokens [B, gamma+1] (x_0..x_{k-1}, then
+ * the correction or bonus token, then -1), near [B] (1 when the final draw
+ * was within 1e-6 of a CDF boundary), dist [B] (that distance; may be NULL).
+ */
+int oracle_spec_accept(int B, int gamma, int V, const float *P, const float *Q,
+                       const int32_t *x, const float *u_acc, const float *u_s,
+                       int32_t *accepted_len, int32_t *out_tokens, uint8_t *near,
+                       double *dist, int nthreads) {
+    if (B < 0 || gamma < 1 || V < 1) return ORC_ERR_ARG;
+    for (long i = 0; i < (long)B * gamma; ++i)
+        if (x[i] < 0 || x[i] >= V) return ORC_ERR_ARG;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int b = 0; b < B; ++b) {
+        const float *Pb = P + (long)b * (gamma + 1) * V;
+        const float *Qb = Q + (long)b * gamma * V;
+        int k = gamma;
+        for (int i = 0; i < gamma; ++i) {
+            int32_t xi = x[(long)b * gamma + i];
+            if (!accept_test(u_acc[(long)b * gamma + i], Qb[(long)i * V + xi],
+                             Pb[(long)i * V + xi])) {
+                k = i;
+                break;
+            }
+        }
+        double *r = (double *)malloc(sizeof(double) * (size_t)V);
+        int32_t tok;
+        uint8_t nb = 0;
+        double dd = INFINITY;
+        if (k < gamma) {
+            for (int t = 0; t < V; ++t) {
+                double diff = (double)Pb[(long)k * V + t] - (double)Qb[(long)k * V + t];
+                r[t] = diff > 0.0 ? diff : 0.0;
+            }
+            tok = draw_inverse_cdf(r, V, (double)u_s[b], &nb, &dd);
+            if (tok < 0) { /* empty residual: fall back to the target row */
+                for (int t = 0; t < V; ++t) r[t] = (double)Pb[(long)k * V + t];
+                tok = draw_inverse_cdf(r, V, (double)u_s[b], &nb, &dd);
+            }
+        } else {
+            for (int t = 0; t < V; ++t) r[t] = (double)Pb[(long)gamma * V + t];
+            tok = draw_inverse_cdf(r, V, (double)u_s[b], &nb, &dd);
+        }
+        free(r);
+        accepted_len[b] = k;
+        int32_t *o = out_tokens + (long)b * (gamma + 1);
+        for (int i = 0; i <= gamma; ++i)
+            o[i] = i < k ? x[(long)b * gamma + i] : (i == k ? tok : -1);
+        if (near) near[b] = nb;
+        if (dist) dist[b] = dd;
+    }
+    return ORC_OK;
+}
+
+/* Tree helpers: a node is internal when some node names it as parent; its
+ * draft row in Q is its rank among internal nodes in node order. */
+static int tree_depth_of(const int32_t *parent, int n, int node) {
+    int d = 0;
+    while (node > 0) { node = parent[node]; ++d; }
+    return d;
+}
+
+int oracle_tree_max_depth(const int32_t *parent, int n_nodes) {
+    int md = 0;
+    for (int i = 0; i < n_nodes; ++i) {
+        int d = tree_depth_of(parent, n_nodes, i);
+        if (d > md) md = d;
+    }
+    return md;
+}
+
+/*
+ * Tree speculative sampler (recursive residual rejection over the children of
+ * a node, children tested in index order; reduces to the linear sampler when
+ * every node has one child).  Unnormalised residual R with mass Z:
+ *   at a node: R = P[node], Z = 1;
+ *   child c (token x_c): accept iff u_acc[c]*Q[node](x_c)*Z <= R(x_c)
+ *     -- for the first child (Z = 1, R = P) this is the fp32 test u*Q <= P;
+ *        later children use fp64;
+ *   on reject: R <- max(0, R - Z*Q[node]), Z <- sum R;
+ *   if a child is accepted: descend to it; if none: draw from R with u_s;
+ *   at a leaf (all of its ancestors accepted): draw a bonus from P[leaf].
+ * parent int32 [n_nodes] (parent[0] = -1, parent[i] < i); P fp32
+ * [B, n_nodes, V]; Q fp32 [B, n_internal, V]; node_tokens int32 [B, n_nodes];
+ * u_acc fp32 [B, n_nodes] (entry c is used for child c's test); u_s fp32 [B].
+ * Outputs: accepted_len [B]; path_nodes [B, max_depth+1] (root, the accepted
+ * nodes, then -1); out_tokens [B, max_depth+1]; near [B] set when any
+ * fp64-vs-fp32 sensitive decision (a later-child test or the final draw) fell
+ * within 1e-6 (in normalised units) of its threshold.
+ */
+int oracle_spec_accept_tree(int B, int n_nodes, int V, const int32_t *parent,
+                            const float *P, const float *Q,
+                            const int32_t *node_tokens, const float *u_acc,
+                            const float *u_s, int32_t *accepted_len,
+                            int32_t *path_nodes, int32_t *out_tokens,
+                            uint8_t *near, int nthreads) {
+    if (B < 0 || n_nodes < 1 || n_nodes > 64 || V < 1 || parent[0] != -1)
+        return ORC_ERR_ARG;
+    for (int i = 1; i < n_nodes; ++i)
+        if (parent[i] < 0 || parent[i] >= i) return ORC_ERR_ARG;
+    int *qrow = (int *)malloc(sizeof(int) * (size_t)n_nodes);
+    int n_internal = 0;
+    for (int i = 0; i < n_nodes; ++i) {
+        int has_child = 0;
+        for (int c = i + 1; c < n_nodes; ++c) has_child |= parent[c] == i;
+        qrow[i] = has_child ? n_internal++ : -1;
+    }
+    const int W = oracle_tree_max_depth(parent, n_nodes) + 1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        double *R = (double *)malloc(sizeof(double) * (size_t)V);
+        int32_t *path = path_nodes + (long)b * W;
+        int32_t *outt = out_tokens + (long)b * W;
+        const int32_t *tok = node_tokens + (long)b * n_nodes;
+        for (int i = 0; i < W; ++i) path[i] = outt[i] = -1;
+        path[0] = 0;
+        int node = 0, depth = 0;
+        uint8_t nb = 0;
+        int32_t final_tok = -1;
+        for (;;) {
+            const float *Pn = P + ((long)b * n_nodes + node) * V;
+            if (qrow[node] < 0) { /* leaf reached: bonus from its target row */
+                for (int t = 0; t < V; ++t) R[t] = (double)Pn[t];
+                uint8_t nn = 0;
+                final_tok = draw_inverse_cdf(R, V, (double)u_s[b], &nn, NULL);
+                nb |= nn;
+                break;
+            }
+            const float *Qn = Q + ((long)b * n_internal + qrow[node]) * V;
+            for (int t = 0; t < V; ++t) R[t] = (double)Pn[t];
+            double Z = 1.0;
+            int accepted = -1, tested = 0;
+            for (int c = node + 1; c < n_nodes; ++c) {
+                if (parent[c] != node) continue;
+                int32_t xc = tok[c];
+                int ok;
+                if (tested == 0) {
+                    ok = accept_test(u_acc[(long)b * n_nodes + c], Qn[xc], Pn[xc]);
+                } else {
+                    double lhs = (double)u_acc[(long)b * n_nodes + c] * (double)Qn[xc] * Z;
+                    ok = lhs <= R[xc];
+                    if (Z > 0.0 && fabs(lhs - R[xc]) / Z < 1e-6) nb = 1;
+                }
+                ++tested;
+                if (ok) { accepted = c; break; }
+                double Znew = 0.0;
+                for (int t = 0; t < V; ++t) {
+                    double v = R[t] - Z * (double)Qn[t];
+                    R[t] = v > 0.0 ? v : 0.0;
+                    Znew += R[t];
+                }
+                Z = Znew;
+            }
+            if (accepted >= 0) {
+                ++depth;
+                path[depth] = accepted;
+                outt[depth - 1] = tok[accepted];
+                node = accepted;
+                continue;
+            }
+            uint8_t nn = 0;
+            final_tok = draw_inverse_cdf(R, V, (double)u_s[b], &nn, NULL);
+            if (final_tok < 0) { /* empty residual: fall back to the target row */
+                for (int t = 0; t < V; ++t) R[t] = (double)Pn[t];
+                final_tok = draw_inverse_cdf(R, V, (double)u_s[b], &nn, NULL);
+            }
+            nb |= nn;
+            break;
+        }
+        accepted_len[b] = depth;
+        outt[depth] = final_tok;
+        if (near) near[b] = nb;
+        free(R);
+    }
+    free(qrow);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* block-table commit / rollback                                       */
+/* ------------------------------------------------------------------ */
+
+/*
+ * For each sequence b with committed length L and k = accepted_len[b]:
+ *  - tree (path_nodes != NULL, row width path_w): for d = 1..k, in increasing
+ *    d, copy the K and V rows (all kv heads) of speculative slot
+ *    L + path_nodes[b][d] to slot L + d;
+ *  - the new length is L + k + 1 (the last committed token and the k accepted
+ *    drafts have K/V; the correction/bonus token gets its K/V next step);
+ *  - logical blocks i with ceil(new/BS) <= i < ceil((L+n_q)/BS) are dropped:
+ *    the table entry becomes -1 and the block's reference count falls by one;
+ *    a block whose count reaches 0 is pushed on the free stack.
+ * Sequences are processed in order b = 0..B-1 and blocks in increasing i, so
+ * the free-stack order here is one valid order among many.
+ * elem_bytes is 2 (bf16) or 1 (FP8); the pool layout is
+ * [num_blocks, Hkv, BS, D].
+ */
+int oracle_block_table_commit(int B, int n_q, int BS, int max_blocks,
+                              int num_blocks, int32_t *block_table,
+                              int32_t *context_lens, const int32_t *accepted_len,
+                              int32_t *refcount, int32_t *free_stack,
+                              int32_t *free_top, const int32_t *path_nodes,
+                              int path_w, void *k_pool, void *v_pool, int Hkv,
+                              int D, int elem_bytes) {
+    if (B < 0 || n_q < 1 || BS < 1 || max_blocks < 1 || num_blocks < 1)
+        return ORC_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        long L = context_lens[b];
+        int k = accepted_len[b];
+        long T = L + n_q;
+        if (L < 0 || k < 0 || k >= n_q || (T + BS - 1) / BS > max_blocks)
+            return ORC_ERR_ARG;
+        if (path_nodes) {
+            if (path_w < k + 1) return ORC_ERR_ARG;
+            size_t row = (size_t)D * (size_t)elem_bytes;
+            for (int d = 1; d <= k; ++d) {
+                long src = L + path_nodes[(long)b * path_w + d];
+                long dst = L + d;
+                if (src < dst || src >= T) return ORC_ERR_ARG;
+                int32_t sb = block_table[(long)b * max_blocks + src / BS];
+                int32_t db = block_table[(long)b * max_blocks + dst / BS];
+                if (sb < 0 || sb >= num_blocks || db < 0 || db >= num_blocks)
+                    return ORC_ERR_BAD_BLOCK;
+                for (int g = 0; g < Hkv; ++g) {
+                    size_t so = ((((size_t)sb * Hkv + g) * BS) + src % BS) * row;
+                    size_t dof = ((((size_t)db * Hkv + g) * BS) + dst % BS) * row;
+                    memmove((char *)k_pool + dof, (char *)k_pool + so, row);
+                    memmove((char *)v_pool + dof, (char *)v_pool + so, row);
+                }
+            }
+        }
+        long new_len = L + k + 1;
+        long keep = (new_len + BS - 1) / BS;
+        long had = (T + BS - 1) / BS;
+        for (long i = keep; i < had; ++i) {
+            int32_t *e = &block_table[(long)b * max_blocks + i];
+            int32_t blk = *e;
+            if (blk < 0 || blk >= num_blocks) return ORC_ERR_BAD_BLOCK;
+            *e = -1;
+            refcount[blk] -= 1;
+            if (refcount[blk] == 0) {
+                if (*free_top >= num_blocks) return ORC_ERR_OUT_OF_BLOCKS;
+                free_stack[(*free_top)++] = blk;
+            }
+        }
+        context_lens[b] = (int32_t)new_len;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* speed-up model                                                      */
+/* ------------------------------------------------------------------ */
+
+/* E[K] = sum_{i=1}^{gamma} prod_{j=1}^{i} alpha_j */
+double oracle_expected_accepted(const double *alpha, int gamma) {
+    double total = 0.0, prod = 1.0;
+    for (int i = 0; i < gamma; ++i) {
+        prod *= alpha[i];
+        total += prod;
+    }
+    return total;
+}
+
+/* eta = (E[K] + 1) / (gamma * r + 1), r = t_draft / t_target */
+double oracle_speedup(double expected_accepted, int gamma, double r) {
+    return (expected_accepted + 1.0) / ((double)gamma * r + 1.0);
+}
