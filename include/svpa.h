@@ -1,0 +1,285 @@
+/*
+ * svpa.h -- C ABI of libsvpa.so: the target-model verification step of
+ * speculative decoding over a paged KV cache, on one NVIDIA GB300 (sm_103a).
+ *
+ * Three operations, called in this order once per verification step:
+ *
+ *   svpa_paged_verify_attn   the n_q verification queries of every sequence
+ *                            (the last committed token plus the gamma drafts,
+ *                            or the nodes of a draft tree) attend over the
+ *                            sequence's K/V history, fetched page by page
+ *                            through its block table.
+ *   svpa_spec_accept         draft/target rejection sampling over the gamma
+ *   svpa_spec_accept_tree    drafts (or along a draft tree): accepted count,
+ *                            accepted tokens and the correction/bonus token.
+ *   svpa_block_table_commit  commit the accepted tokens and roll back the
+ *                            rest: new lengths, dropped pages returned to the
+ *                            free stack when their reference count reaches 0.
+ *
+ * Conventions shared by every entry point
+ *  - Every pointer argument is a DEVICE pointer unless its comment says HOST.
+ *    The caller owns and allocates all memory; the library allocates nothing.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *    void*; NULL = the legacy default stream).  Arguments are validated on the
+ *    host before anything is enqueued; a non-OK status means nothing ran.
+ *  - Faults found on the device (a block id outside the pool, a free-stack
+ *    overflow, a wait that ran out of time) are OR-ed into the caller's
+ *    `error_flag` word (int32, device, zero before the call) as SVPA_DEVERR_*
+ *    bits; kernels never trap.  svpa_check_error() synchronises the stream,
+ *    reads the word and maps it to a status.
+ *  - Calls that share buffers are not thread safe; order them on one stream.
+ *  - Output of an operation whose error_flag came back non-zero is undefined.
+ */
+#ifndef SVPA_H
+#define SVPA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum svpa_status {
+    SVPA_OK = 0,
+    SVPA_ERR_INVALID_ARG = 1,   /* null pointer, bad size or shape            */
+    SVPA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim)  */
+    SVPA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed          */
+    SVPA_ERR_OUT_OF_BLOCKS = 4, /* the free stack overflowed (device)        */
+    SVPA_ERR_BAD_BLOCK = 5,     /* a block id outside [0, num_blocks) (device)*/
+    SVPA_ERR_WORKSPACE = 6,     /* workspace missing or too small             */
+    SVPA_ERR_TIMEOUT = 7        /* a device-side wait gave up (device)        */
+} svpa_status;
+
+/* bits of the device error word */
+#define SVPA_DEVERR_BAD_BLOCK 1
+#define SVPA_DEVERR_TIMEOUT 2
+#define SVPA_DEVERR_FREE_OVERFLOW 4
+#define SVPA_DEVERR_BAD_VALUE 8 /* an out-of-range length, count or token id */
+
+/* K/V page element types */
+#define SVPA_KV_BF16 0
+#define SVPA_KV_FP8_E4M3 1
+
+/*
+ * Geometry of one paged-attention call.
+ *
+ * Source: "The Sub-Millisecond Speculative Decoding Meltdown", section
+ * "Triton CUDA Fused Speculative Tree-Verification Kernel" (argument list:
+ * query [B, H, K, D], K/V cache [blocks, heads, block_size, dim], K/V scales
+ * [blocks, heads], block tables [B, pages per sequence], sm_scale); the
+ * query/output layout here is [B, n_q, Hq, D] and kv heads are grouped
+ * (query head h reads kv head h / (Hq / Hkv)).
+ */
+typedef struct svpa_attn_params {
+    int32_t batch;              /* B >= 0                                     */
+    int32_t n_q;                /* queries per sequence, 1..64 (gamma + 1, or
+                                   the number of draft-tree nodes incl. root)  */
+    int32_t num_q_heads;        /* Hq                                         */
+    int32_t num_kv_heads;       /* Hkv, Hq % Hkv == 0, Hq / Hkv * n_q <= 128  */
+    int32_t head_dim;           /* D: 64 or 128                               */
+    int32_t block_size;         /* tokens per page: 16                        */
+    int32_t max_blocks_per_seq; /* row stride of block_table                  */
+    int32_t num_blocks;         /* physical pages in the pool                 */
+    int32_t kv_dtype;           /* SVPA_KV_BF16 or SVPA_KV_FP8_E4M3           */
+    float sm_scale;             /* softmax scale, normally 1/sqrt(D)          */
+    int32_t split_pages;        /* pages per KV split; 0 = chosen by library  */
+} svpa_attn_params;
+
+/* Bytes of workspace svpa_paged_verify_attn needs for `p` (split-KV partial
+ * results and per-(sequence, kv head) tickets).  The workspace must be
+ * zero-filled once before its first use; every completed call leaves its
+ * ticket words at zero again. */
+svpa_status svpa_attn_workspace_size(const svpa_attn_params *p, size_t *bytes);
+
+/*
+ * Paged verification attention.
+ *
+ * Computes, for sequence b, query j and query head h,
+ *   out[b][j][h] = softmax_p( q[b][j][h] . K[p] * sm_scale  over visible p ) . V
+ * where the sequence's committed history has context_lens[b] = L_b tokens,
+ * the n_q queries occupy positions L_b .. L_b + n_q - 1 (their K/V are
+ * already written to the pool), position p lives in physical page
+ * block_table[b][p / 16] at slot p % 16, and query j sees every p < L_b plus
+ * the speculative slot L_b + i when bit i of ancestor_mask[j] is set
+ * (causal when ancestor_mask is NULL: i <= j).
+ *
+ * Sources: "The Sub-Millisecond Speculative Decoding Meltdown", section
+ * "Speculative Decoding Mechanics & The K-Token Penalty" (A = Softmax((Q K^T +
+ * M_tree)/sqrt(d_k)) V with a tree mask) and section "Custom FP8 Quantized
+ * Memory Block Layout" (e4m3 pages with per-block K and V scales);
+ * "Speculative Decoding and KV-Cache Compression", section 2.3 (the bundle's
+ * K/V are present before any acceptance decision).
+ *
+ *  q            bf16 [B, n_q, Hq, D]
+ *  k_pool,
+ *  v_pool       [num_blocks, Hkv, 16, D], bf16 or FP8-E4M3 (OCP "fn"
+ *               encoding); 16-byte aligned
+ *  k_scale,
+ *  v_scale      fp32 [num_blocks, Hkv] (FP8 only; NULL for bf16): the real
+ *               value of a stored byte x is e4m3(x) * scale[block][kv head]
+ *  block_table  int32 [B, max_blocks_per_seq]; entries past a sequence's last
+ *               page are ignored
+ *  context_lens int32 [B], committed history L_b >= 0 with
+ *               ceil((L_b + n_q) / 16) <= max_blocks_per_seq
+ *  ancestor_mask HOST uint64 [n_q] or NULL (causal)
+ *  out          bf16 [B, n_q, Hq, D] (written)
+ *  lse          fp32 [B, n_q, Hq] natural-log sum of exp(scores), or NULL
+ *  workspace    device scratch of at least svpa_attn_workspace_size() bytes
+ * Accumulation is fp32; the contraction runs on the tensor cores.
+ */
+svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q,
+                                   const void *k_pool, const void *v_pool,
+                                   const float *k_scale, const float *v_scale,
+                                   const int32_t *block_table,
+                                   const int32_t *context_lens,
+                                   const uint64_t *ancestor_mask, void *out,
+                                   float *lse, void *workspace,
+                                   size_t workspace_bytes, int32_t *error_flag,
+                                   void *stream);
+
+/* Bytes of workspace the samplers need for `batch` rows of `vocab` tokens
+ * (per-chunk residual sums and per-row tickets).  Zero-fill once before the
+ * first use; completed calls leave the tickets at zero. */
+svpa_status svpa_spec_accept_workspace_size(int32_t batch, int32_t vocab,
+                                            size_t *bytes);
+
+/*
+ * Linear draft/target rejection sampler, one row per sequence.
+ *
+ * For i = 0 .. gamma-1 draft x_i is accepted iff u_accept[i] * Q_i(x_i) <=
+ * P_i(x_i), the product rounded once to fp32 (no fused multiply-add) -- the
+ * realisation of alpha_i = min(1, P(x_i)/Q(x_i)); k = the first rejected
+ * index, or gamma.  If k < gamma the emitted token is drawn from the residual
+ * r = max(0, P_k - Q_k) (from P_k if r is all zero), else a bonus token is
+ * drawn from P_gamma: the token is the first t whose running sum of r exceeds
+ * u_sample * sum(r).
+ *
+ * Sources: "LOW-LATENCY INFERENCE: SPECULATIVE DECODING & PAGING", section
+ * "Verification Acceptance Probabilities and Speedup Math" (alpha_i) and its
+ * architecture diagram ("Rejection Recovery (Resample)"); "Speculative
+ * Decoding & KV-Cache PagedAttention in Enterprise LLM Serving", the
+ * draft-verify pipeline figure (k accepted drafts plus one sampled correction
+ * token); the residual distribution is the one that makes the output follow P
+ * exactly ("Speculative Decoding and KV-Cache Compression", section 2.1).
+ *
+ *  p_probs      fp32 [B, gamma+1, V] target distributions (rows sum to ~1)
+ *  q_probs      fp32 [B, gamma, V]   draft distributions
+ *  draft_tokens int32 [B, gamma], each in [0, V)
+ *  u_accept     fp32 [B, gamma] uniforms in [0, 1)
+ *  u_sample     fp32 [B] uniforms in [0, 1)
+ *  accepted_len int32 [B] (written) k in 0..gamma
+ *  out_tokens   int32 [B, gamma+1] (written): x_0..x_{k-1}, the correction or
+ *               bonus token, then -1
+ *  near_boundary uint8 [B] or NULL: 1 when u_sample lay within 1e-6 of a
+ *               boundary of the fp32 cumulative sum (a draw whose token fp32
+ *               and exact arithmetic may resolve differently)
+ *  gamma 1..32, V >= 1.
+ */
+svpa_status svpa_spec_accept(int32_t batch, int32_t gamma, int32_t vocab,
+                             const float *p_probs, const float *q_probs,
+                             const int32_t *draft_tokens,
+                             const float *u_accept, const float *u_sample,
+                             int32_t *accepted_len, int32_t *out_tokens,
+                             uint8_t *near_boundary, void *workspace,
+                             size_t workspace_bytes, int32_t *error_flag,
+                             void *stream);
+
+/*
+ * Draft-tree rejection sampler (recursive residual rejection over the
+ * children of a node, in index order; identical to svpa_spec_accept on a
+ * chain).  At a node: R = P[node], Z = 1; child c with token x_c is accepted
+ * iff u_accept[c] * Q[node](x_c) * Z <= R(x_c) (for the first child this is
+ * the fp32 test of svpa_spec_accept); on rejection R <- max(0, R - Z*Q[node])
+ * and Z <- sum(R).  The walk descends into an accepted child; when every child
+ * is rejected the correction token is drawn from R, and at a leaf a bonus
+ * token is drawn from P[leaf], both with u_sample.
+ *
+ * Sources: "The Sub-Millisecond Speculative Decoding Meltdown" (draft trees
+ * verified in one pass: "Tree-Attention Verification", "Draft Tree Rejection
+ * Cascades"); the per-token rule of "LOW-LATENCY INFERENCE: SPECULATIVE
+ * DECODING & PAGING".  The pages do not spell out the multi-child rule; this
+ * is the recursive form that keeps the output distributed as P.
+ *
+ *  parent       HOST int32 [n_nodes]: parent[0] = -1, 0 <= parent[i] < i
+ *  p_probs      fp32 [B, n_nodes, V]   target distribution at every node
+ *  q_probs      fp32 [B, n_internal, V] draft distribution of the children of
+ *               each internal node (a node with a child), in node order
+ *  node_tokens  int32 [B, n_nodes] (entry 0 unused)
+ *  u_accept     fp32 [B, n_nodes] (entry c drives child c's test)
+ *  u_sample     fp32 [B]
+ *  accepted_len int32 [B]; path_nodes int32 [B, W]; out_tokens int32 [B, W]
+ *               with W = tree depth + 1: the root, the accepted nodes, -1...;
+ *               the accepted tokens, the correction/bonus token, -1...
+ *  near_boundary uint8 [B] or NULL: a later-child test or the final draw fell
+ *               within 1e-6 (normalised units) of its threshold.
+ *  n_nodes 1..64.
+ */
+svpa_status svpa_spec_accept_tree(int32_t batch, int32_t n_nodes, int32_t vocab,
+                                  const int32_t *parent, const float *p_probs,
+                                  const float *q_probs,
+                                  const int32_t *node_tokens,
+                                  const float *u_accept, const float *u_sample,
+                                  int32_t *accepted_len, int32_t *path_nodes,
+                                  int32_t *out_tokens, uint8_t *near_boundary,
+                                  void *workspace, size_t workspace_bytes,
+                                  int32_t *error_flag, void *stream);
+
+/*
+ * Commit the accepted tokens of every sequence and roll back the rest.
+ *
+ * With L = context_lens[b] and k = accepted_len[b] (0 <= k < n_q):
+ *  - tree (path_nodes != NULL): for d = 1..k the K and V rows (all kv heads)
+ *    of speculative slot L + path_nodes[b][d] are copied to slot L + d, so the
+ *    accepted path becomes a linear continuation of the history;
+ *  - context_lens[b] becomes L + k + 1 (the last committed token and the k
+ *    accepted drafts; the correction/bonus token is written next step);
+ *  - logical pages i with ceil((L+k+1)/16) <= i < ceil((L+n_q)/16) are
+ *    dropped: block_table[b][i] = -1 and refcount[block] -= 1; a block whose
+ *    count reaches 0 is pushed on the free stack (free_stack[(*free_top)++]).
+ * The order of pushes within one call is unspecified.
+ *
+ * Sources: "LOW-LATENCY INFERENCE: SPECULATIVE DECODING & PAGING",
+ * architecture diagram (commit to the KV-cache block table; discard the KV
+ * blocks of rejected tokens; rollback through block tables); "Speculative
+ * Decoding & KV-Cache PagedAttention in Enterprise LLM Serving",
+ * PagedKVCacheManager (reference counts, shared prefix blocks, release to the
+ * free pool at count zero, block size 16).
+ *
+ *  block_table  int32 [B, max_blocks_per_seq] (in/out)
+ *  context_lens int32 [B] (in/out)
+ *  accepted_len int32 [B]
+ *  refcount     int32 [num_blocks] (in/out)
+ *  free_stack   int32 [num_blocks] (in/out), free_top int32 [1] (in/out)
+ *  path_nodes   int32 [B, path_width] or NULL (linear)
+ *  k_pool, v_pool  the pools (only read/written for a tree; bf16 only)
+ */
+svpa_status svpa_block_table_commit(int32_t batch, int32_t n_q,
+                                    int32_t block_size,
+                                    int32_t max_blocks_per_seq,
+                                    int32_t num_blocks, int32_t *block_table,
+                                    int32_t *context_lens,
+                                    const int32_t *accepted_len,
+                                    int32_t *refcount, int32_t *free_stack,
+                                    int32_t *free_top,
+                                    const int32_t *path_nodes,
+                                    int32_t path_width, void *k_pool,
+                                    void *v_pool, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t kv_dtype,
+                                    int32_t *error_flag, void *stream);
+
+/* Synchronise `stream`, read the device error word and map it to a status
+ * (SVPA_OK when it is zero).  Does not clear the word. */
+svpa_status svpa_check_error(const int32_t *error_flag, void *stream);
+
+/* Static description of a status code. */
+const char *svpa_status_string(svpa_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t svpa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SVPA_H */

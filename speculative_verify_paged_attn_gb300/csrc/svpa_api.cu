@@ -1,0 +1,362 @@
+// svpa_api.cu -- the C ABI of libsvpa.so: host-side validation, workspace
+// layout, split-size choice, tensor-map encoding and kernel launches.  No
+// function here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/svpa.h"
+#include "svpa_internal.h"
+
+namespace svpa {
+int spec_accept_chunks(int vocab);
+int attn_pick_stages(int head_dim, bool fp8, int M, int split_pages);
+}  // namespace svpa
+
+using namespace svpa;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+struct AttnPlan {
+    int M, split_pages, max_splits;
+    size_t off_ml, off_acc, bytes;
+};
+
+svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
+    if (!p) return SVPA_ERR_INVALID_ARG;
+    if (p->batch < 0 || p->n_q < 1 || p->n_q > kMaxNq || p->num_q_heads < 1 || p->num_kv_heads < 1 ||
+        p->num_q_heads % p->num_kv_heads != 0 || p->block_size != kBlockSize || p->max_blocks_per_seq < 1 ||
+        p->num_blocks < 1 || !(p->sm_scale > 0.f) || !std::isfinite(p->sm_scale) || p->split_pages < 0)
+        return SVPA_ERR_INVALID_ARG;
+    if (p->kv_dtype != SVPA_KV_BF16 && p->kv_dtype != SVPA_KV_FP8_E4M3) return SVPA_ERR_INVALID_ARG;
+    if (p->head_dim != 64 && p->head_dim != 128) return SVPA_ERR_UNSUPPORTED;
+    if (p->kv_dtype == SVPA_KV_FP8_E4M3 && p->head_dim != 128) return SVPA_ERR_UNSUPPORTED;
+    const int G = p->num_q_heads / p->num_kv_heads;
+    const long long M = (long long)G * p->n_q;
+    if (M > kMaxRows) return SVPA_ERR_UNSUPPORTED;
+    pl->M = (int)M;
+    const int D = p->head_dim;
+    const int eb = p->kv_dtype == SVPA_KV_FP8_E4M3 ? 1 : 2;
+    int sp = p->split_pages;
+    if (sp == 0) {
+        const double units = (double)std::max(1, p->batch) * p->num_kv_heads;
+        const double per = units * p->max_blocks_per_seq / (16.0 * sm_count());
+        int pw = 16;
+        while (pw * 2 <= per && pw < 1024) pw *= 2;
+        // keep the split partials under ~5% of the split's K/V bytes
+        const double page_bytes = 2.0 * kBlockSize * D * eb;
+        const double partial_bytes = (double)M * (D + 2) * 4;
+        int min_pages = (int)std::ceil(20.0 * partial_bytes / page_bytes);
+        min_pages = (min_pages + 15) / 16 * 16;
+        sp = std::max(pw, min_pages);
+    }
+    sp = std::min(sp, 4096);
+    pl->split_pages = sp;
+    pl->max_splits = (p->max_blocks_per_seq + sp - 1) / sp;
+    const size_t units = (size_t)p->batch * p->num_kv_heads;
+    size_t off = align_up(units * sizeof(int32_t));
+    pl->off_ml = off;
+    if (pl->max_splits > 1) {
+        off += align_up(units * pl->max_splits * M * 2 * sizeof(float));
+        pl->off_acc = off;
+        off += align_up(units * pl->max_splits * M * D * sizeof(float));
+    } else {
+        pl->off_acc = off;
+    }
+    pl->bytes = std::max<size_t>(off, kAlign);
+    return SVPA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+svpa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SVPA_OK : SVPA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *svpa_status_string(svpa_status s) {
+    switch (s) {
+        case SVPA_OK: return "ok";
+        case SVPA_ERR_INVALID_ARG: return "invalid argument";
+        case SVPA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case SVPA_ERR_CUDA: return "CUDA error";
+        case SVPA_ERR_OUT_OF_BLOCKS: return "free block stack overflow";
+        case SVPA_ERR_BAD_BLOCK: return "block id outside the pool";
+        case SVPA_ERR_WORKSPACE: return "workspace missing or too small";
+        case SVPA_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+int32_t svpa_version(void) { return 100; }
+
+svpa_status svpa_attn_workspace_size(const svpa_attn_params *p, size_t *bytes) {
+    if (!bytes) return SVPA_ERR_INVALID_ARG;
+    AttnPlan pl;
+    const svpa_status s = plan_attn(p, &pl);
+    if (s != SVPA_OK) return s;
+    *bytes = pl.bytes;
+    return SVPA_OK;
+}
+
+svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, const void *k_pool,
+                                   const void *v_pool, const float *k_scale, const float *v_scale,
+                                   const int32_t *block_table, const int32_t *context_lens,
+                                   const uint64_t *ancestor_mask, void *out, float *lse, void *workspace,
+                                   size_t workspace_bytes, int32_t *error_flag, void *stream) {
+    AttnPlan pl;
+    svpa_status s = plan_attn(p, &pl);
+    if (s != SVPA_OK) return s;
+    if (p->batch == 0) return SVPA_OK;
+    if (p->batch > 65535) return SVPA_ERR_UNSUPPORTED;
+    const bool fp8 = p->kv_dtype == SVPA_KV_FP8_E4M3;
+    if (!q || !k_pool || !v_pool || !block_table || !context_lens || !out || !error_flag)
+        return SVPA_ERR_INVALID_ARG;
+    if (fp8 && (!k_scale || !v_scale)) return SVPA_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(q) || !aligned16(out)) return SVPA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < pl.bytes || !aligned16(workspace)) return SVPA_ERR_WORKSPACE;
+    if (ancestor_mask) {
+        for (int j = 0; j < p->n_q; ++j) {
+            // a query always sees itself, never a later slot
+            if (!((ancestor_mask[j] >> j) & 1ull)) return SVPA_ERR_INVALID_ARG;
+            if (j + 1 < 64 && (ancestor_mask[j] >> (j + 1)) != 0ull) return SVPA_ERR_INVALID_ARG;
+        }
+    }
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return SVPA_ERR_CUDA;
+
+    const int D = p->head_dim;
+    const int eb = fp8 ? 1 : 2;
+    AttnMaps maps;
+    memset(&maps, 0, sizeof maps);
+    const cuuint64_t dims[4] = {(cuuint64_t)(fp8 ? 128 : 64), 16, (cuuint64_t)p->num_kv_heads,
+                                (cuuint64_t)p->num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * eb, (cuuint64_t)16 * D * eb,
+                                   (cuuint64_t)p->num_kv_heads * 16 * D * eb};
+    const cuuint32_t box[4] = {(cuuint32_t)(fp8 ? 128 : 64), 16, 1, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int slabs = (D * eb) / 128;
+    for (int sl = 0; sl < 2; ++sl) {
+        const int use = sl < slabs ? sl : 0;
+        char *kb = (char *)const_cast<void *>(k_pool) + use * 128;
+        char *vb = (char *)const_cast<void *>(v_pool) + use * 128;
+        if (enc(&maps.k[sl], dt, 4, kb, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return SVPA_ERR_CUDA;
+        if (enc(&maps.v[sl], dt, 4, vb, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return SVPA_ERR_CUDA;
+    }
+
+    AttnArgs a;
+    memset(&a, 0, sizeof a);
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.block_table = block_table;
+    a.context_lens = context_lens;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.lse = lse;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.tickets = reinterpret_cast<int32_t *>(ws);
+    a.part_ml = reinterpret_cast<float *>(ws + pl.off_ml);
+    a.part_acc = reinterpret_cast<float *>(ws + pl.off_acc);
+    a.err = error_flag;
+    a.B = p->batch;
+    a.n_q = p->n_q;
+    a.Hq = p->num_q_heads;
+    a.Hkv = p->num_kv_heads;
+    a.G = p->num_q_heads / p->num_kv_heads;
+    a.M = pl.M;
+    a.max_blocks = p->max_blocks_per_seq;
+    a.num_blocks = p->num_blocks;
+    a.split_pages = pl.split_pages;
+    a.max_splits = pl.max_splits;
+    a.scale_log2 = p->sm_scale * 1.4426950408889634f;
+    for (int j = 0; j < p->n_q; ++j)
+        a.anc[j] = ancestor_mask ? ancestor_mask[j] : ((j == 63) ? ~0ull : ((1ull << (j + 1)) - 1ull));
+    a.n_stages = attn_pick_stages(D, fp8, pl.M, pl.split_pages);
+    if (a.n_stages <= 0) return SVPA_ERR_CUDA;
+    return from_cuda(launch_paged_verify_attn(maps, a, D, fp8, static_cast<cudaStream_t>(stream)));
+}
+
+svpa_status svpa_spec_accept_workspace_size(int32_t batch, int32_t vocab, size_t *bytes) {
+    if (!bytes || batch < 0 || vocab < 1) return SVPA_ERR_INVALID_ARG;
+    const size_t nc = (size_t)spec_accept_chunks(vocab);
+    *bytes = align_up((size_t)batch * sizeof(int32_t)) + align_up((size_t)batch * nc * sizeof(double));
+    *bytes = std::max<size_t>(*bytes, kAlign);
+    return SVPA_OK;
+}
+
+svpa_status svpa_spec_accept(int32_t batch, int32_t gamma, int32_t vocab, const float *p_probs,
+                             const float *q_probs, const int32_t *draft_tokens, const float *u_accept,
+                             const float *u_sample, int32_t *accepted_len, int32_t *out_tokens,
+                             uint8_t *near_boundary, void *workspace, size_t workspace_bytes,
+                             int32_t *error_flag, void *stream) {
+    if (batch < 0 || gamma < 1 || gamma > 32 || vocab < 1) return SVPA_ERR_INVALID_ARG;
+    if (spec_accept_chunks(vocab) > 65535) return SVPA_ERR_UNSUPPORTED;
+    if (batch == 0) return SVPA_OK;
+    if (!p_probs || !q_probs || !draft_tokens || !u_accept || !u_sample || !accepted_len || !out_tokens ||
+        !error_flag)
+        return SVPA_ERR_INVALID_ARG;
+    size_t need;
+    svpa_spec_accept_workspace_size(batch, vocab, &need);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return SVPA_ERR_WORKSPACE;
+    AcceptArgs a;
+    memset(&a, 0, sizeof a);
+    a.p = p_probs;
+    a.q = q_probs;
+    a.tokens = draft_tokens;
+    a.u_acc = u_accept;
+    a.u_s = u_sample;
+    a.accepted_len = accepted_len;
+    a.out_tokens = out_tokens;
+    a.near = near_boundary;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.tickets = reinterpret_cast<int32_t *>(ws);
+    a.chunk_sum = reinterpret_cast<double *>(ws + align_up((size_t)batch * sizeof(int32_t)));
+    a.err = error_flag;
+    a.B = batch;
+    a.gamma = gamma;
+    a.V = vocab;
+    return from_cuda(launch_spec_accept(a, static_cast<cudaStream_t>(stream)));
+}
+
+svpa_status svpa_spec_accept_tree(int32_t batch, int32_t n_nodes, int32_t vocab, const int32_t *parent,
+                                  const float *p_probs, const float *q_probs, const int32_t *node_tokens,
+                                  const float *u_accept, const float *u_sample, int32_t *accepted_len,
+                                  int32_t *path_nodes, int32_t *out_tokens, uint8_t *near_boundary,
+                                  void *workspace, size_t workspace_bytes, int32_t *error_flag, void *stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    if (batch < 0 || n_nodes < 1 || n_nodes > kMaxNq || vocab < 1 || !parent) return SVPA_ERR_INVALID_ARG;
+    if (vocab > 55000) return SVPA_ERR_UNSUPPORTED;  // residual row held in shared memory
+    if (parent[0] != -1) return SVPA_ERR_INVALID_ARG;
+    for (int i = 1; i < n_nodes; ++i)
+        if (parent[i] < 0 || parent[i] >= i) return SVPA_ERR_INVALID_ARG;
+    if (batch == 0) return SVPA_OK;
+    if (!p_probs || !q_probs || !node_tokens || !u_accept || !u_sample || !accepted_len || !path_nodes ||
+        !out_tokens || !error_flag)
+        return SVPA_ERR_INVALID_ARG;
+    TreeArgs a;
+    memset(&a, 0, sizeof a);
+    int depth_max = 0, n_internal = 0;
+    for (int i = 0; i < n_nodes; ++i) {
+        int d = 0;
+        for (int x = i; x > 0; x = parent[x]) ++d;
+        depth_max = std::max(depth_max, d);
+        bool has_child = false;
+        for (int c = i + 1; c < n_nodes; ++c) has_child |= parent[c] == i;
+        a.qrow[i] = has_child ? (int8_t)n_internal++ : (int8_t)-1;
+        a.parent[i] = (int8_t)parent[i];
+    }
+    a.p = p_probs;
+    a.q = q_probs;
+    a.tokens = node_tokens;
+    a.u_acc = u_accept;
+    a.u_s = u_sample;
+    a.accepted_len = accepted_len;
+    a.path_nodes = path_nodes;
+    a.out_tokens = out_tokens;
+    a.near = near_boundary;
+    a.err = error_flag;
+    a.B = batch;
+    a.n_nodes = n_nodes;
+    a.V = vocab;
+    a.width = depth_max + 1;
+    a.n_internal = n_internal;
+    return from_cuda(launch_spec_accept_tree(a, static_cast<cudaStream_t>(stream)));
+}
+
+svpa_status svpa_block_table_commit(int32_t batch, int32_t n_q, int32_t block_size, int32_t max_blocks_per_seq,
+                                    int32_t num_blocks, int32_t *block_table, int32_t *context_lens,
+                                    const int32_t *accepted_len, int32_t *refcount, int32_t *free_stack,
+                                    int32_t *free_top, const int32_t *path_nodes, int32_t path_width,
+                                    void *k_pool, void *v_pool, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t kv_dtype, int32_t *error_flag, void *stream) {
+    if (batch < 0 || n_q < 1 || n_q > kMaxNq || block_size != kBlockSize || max_blocks_per_seq < 1 ||
+        num_blocks < 1)
+        return SVPA_ERR_INVALID_ARG;
+    if (batch == 0) return SVPA_OK;
+    if (!block_table || !context_lens || !accepted_len || !refcount || !free_stack || !free_top || !error_flag)
+        return SVPA_ERR_INVALID_ARG;
+    CommitArgs a;
+    memset(&a, 0, sizeof a);
+    if (path_nodes) {
+        if (kv_dtype != SVPA_KV_BF16) return SVPA_ERR_UNSUPPORTED;  // per-page FP8 scales differ
+        if (!k_pool || !v_pool || path_width < 1 || num_kv_heads < 1 || (head_dim != 64 && head_dim != 128))
+            return SVPA_ERR_INVALID_ARG;
+        if (!aligned16(k_pool) || !aligned16(v_pool)) return SVPA_ERR_INVALID_ARG;
+        a.row_bytes = head_dim * 2;
+    }
+    a.block_table = block_table;
+    a.context_lens = context_lens;
+    a.accepted_len = accepted_len;
+    a.refcount = refcount;
+    a.free_stack = free_stack;
+    a.free_top = free_top;
+    a.path_nodes = path_nodes;
+    a.k_pool = static_cast<uint8_t *>(k_pool);
+    a.v_pool = static_cast<uint8_t *>(v_pool);
+    a.err = error_flag;
+    a.B = batch;
+    a.n_q = n_q;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.path_width = path_width;
+    a.Hkv = num_kv_heads;
+    return from_cuda(launch_block_table_commit(a, static_cast<cudaStream_t>(stream)));
+}
+
+svpa_status svpa_check_error(const int32_t *error_flag, void *stream) {
+    if (!error_flag) return SVPA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SVPA_ERR_CUDA;
+    int32_t v = 0;
+    if (cudaMemcpy(&v, error_flag, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SVPA_ERR_CUDA;
+    if (v == 0) return SVPA_OK;
+    if (v & SVPA_DEVERR_BAD_BLOCK) return SVPA_ERR_BAD_BLOCK;
+    if (v & SVPA_DEVERR_FREE_OVERFLOW) return SVPA_ERR_OUT_OF_BLOCKS;
+    if (v & SVPA_DEVERR_TIMEOUT) return SVPA_ERR_TIMEOUT;
+    return SVPA_ERR_INVALID_ARG;
+}
+
+}  // extern "C"

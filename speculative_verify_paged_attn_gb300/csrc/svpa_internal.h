@@ -1,0 +1,97 @@
+// svpa_internal.h -- host/device argument structs and launch entry points
+// shared between the C-ABI layer (svpa_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/svpa.h"
+
+namespace svpa {
+
+constexpr int kBlockSize = 16;   // tokens per page
+constexpr int kMaxNq = 64;       // queries per sequence (one 64-bit mask row each)
+constexpr int kMaxRows = 128;    // GQA group size x queries handled by one CTA
+
+// Arguments of the paged verification attention kernel (passed by value).
+struct AttnArgs {
+    const __nv_bfloat16 *q;
+    const float *k_scale;
+    const float *v_scale;
+    const int32_t *block_table;
+    const int32_t *context_lens;
+    __nv_bfloat16 *out;
+    float *lse;
+    float *part_acc;      // [B*Hkv, max_splits, M, D]
+    float *part_ml;       // [B*Hkv, max_splits, M, 2]  (running max in log2 units, sum)
+    int32_t *tickets;     // [B*Hkv]
+    int32_t *err;
+    int32_t B, n_q, Hq, Hkv, G, M;
+    int32_t max_blocks, num_blocks, split_pages, max_splits, n_stages;
+    float scale_log2;     // sm_scale * log2(e)
+    unsigned long long anc[kMaxNq];  // visibility of speculative slots per query
+};
+
+struct AttnMaps {
+    CUtensorMap k[2];     // 128-byte column slabs of the K pages
+    CUtensorMap v[2];
+};
+
+// Launch the attention kernel matching (head_dim, fp8, row tiles).
+cudaError_t launch_paged_verify_attn(const AttnMaps &maps, const AttnArgs &a, int head_dim,
+                                     bool fp8, cudaStream_t stream);
+size_t attn_smem_bytes(int head_dim, bool fp8, int n_stages, int split_pages);
+int attn_pick_stages(int head_dim, bool fp8, int M, int split_pages);
+
+// Rejection sampler.
+struct AcceptArgs {
+    const float *p;
+    const float *q;
+    const int32_t *tokens;
+    const float *u_acc;
+    const float *u_s;
+    int32_t *accepted_len;
+    int32_t *out_tokens;
+    uint8_t *near;
+    double *chunk_sum;    // [B, n_chunks]
+    int32_t *tickets;     // [B]
+    int32_t *err;
+    int32_t B, gamma, V, chunk, n_chunks;
+};
+cudaError_t launch_spec_accept(const AcceptArgs &a, cudaStream_t stream);
+
+struct TreeArgs {
+    const float *p;
+    const float *q;
+    const int32_t *tokens;
+    const float *u_acc;
+    const float *u_s;
+    int32_t *accepted_len;
+    int32_t *path_nodes;
+    int32_t *out_tokens;
+    uint8_t *near;
+    int32_t *err;
+    int32_t B, n_nodes, V, width, n_internal;
+    int8_t parent[kMaxNq];
+    int8_t qrow[kMaxNq];
+};
+cudaError_t launch_spec_accept_tree(const TreeArgs &a, cudaStream_t stream);
+
+struct CommitArgs {
+    int32_t *block_table;
+    int32_t *context_lens;
+    const int32_t *accepted_len;
+    int32_t *refcount;
+    int32_t *free_stack;
+    int32_t *free_top;
+    const int32_t *path_nodes;
+    uint8_t *k_pool;
+    uint8_t *v_pool;
+    int32_t *err;
+    int32_t B, n_q, max_blocks, num_blocks, path_width, Hkv, row_bytes;
+};
+cudaError_t launch_block_table_commit(const CommitArgs &a, cudaStream_t stream);
+
+}  // namespace svpa

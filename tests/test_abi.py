@@ -1,0 +1,84 @@
+"""The C-ABI library builds, loads and exports every entry point the header
+declares; host-side validation answers without touching a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_verify_paged_attn_gb300 import build, svpa
+    build.build()
+    return svpa.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "svpa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(svpa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    from speculative_verify_paged_attn_gb300 import svpa
+    for code in range(8):
+        assert svpa.status_string(code)
+    assert svpa.version() >= 100
+
+
+def test_workspace_size_and_validation(lib):
+    from speculative_verify_paged_attn_gb300 import svpa
+    p = svpa.attn_params(64, 6, 64, 8, 128, 2049, 100000, split_pages=256)
+    n = svpa.attn_workspace_size(p)
+    # tickets + (max, sum) + accumulators for 9 splits of 48 rows
+    assert n >= 64 * 8 * 9 * 48 * (128 + 2) * 4
+    for bad in [dict(head_dim=96), dict(num_kv_heads=5), dict(n_q=65)]:
+        kw = dict(batch=2, n_q=5, num_q_heads=4, num_kv_heads=4, head_dim=64,
+                  max_blocks_per_seq=8, num_blocks=16, split_pages=4)
+        kw.update(bad)
+        with pytest.raises(svpa.SvpaError):
+            svpa.attn_workspace_size(svpa.attn_params(**kw))
+    # GQA rows per CTA beyond 128 are not supported
+    with pytest.raises(svpa.SvpaError) as e:
+        svpa.attn_workspace_size(svpa.attn_params(1, 17, 64, 8, 128, 8, 16, split_pages=4))
+    assert e.value.status == 2
+
+
+def test_null_pointers_rejected_before_launch(lib):
+    from speculative_verify_paged_attn_gb300 import svpa
+    p = svpa.attn_params(2, 5, 4, 4, 64, 8, 16, split_pages=4)
+    st = lib.svpa_paged_verify_attn(ctypes.byref(p), *([None] * 11), 0, None, None)
+    assert st == 1
+    st = lib.svpa_spec_accept(2, 4, 1000, *([None] * 10), 0, None, None)
+    assert st == 1
+    st = lib.svpa_spec_accept(2, 0, 1000, *([None] * 10), 0, None, None)
+    assert st == 1
+    st = lib.svpa_block_table_commit(2, 5, 16, 8, 16, *([None] * 7), 0, None, None, 4, 64, 0, None, None)
+    assert st == 1
+    # empty batch is a no-op
+    p0 = svpa.attn_params(0, 5, 4, 4, 64, 8, 16, split_pages=4)
+    assert lib.svpa_paged_verify_attn(ctypes.byref(p0), *([None] * 11), 0, None, None) == 0
+
+
+def test_tree_topology_validated(lib):
+    par = (ctypes.c_int32 * 3)(-1, 0, 2)   # node 2 names itself as parent
+    st = lib.svpa_spec_accept_tree(1, 3, 10, ctypes.cast(par, ctypes.c_void_p), *([None] * 10),
+                                   0, None, None)
+    assert st == 1
+
+
+def test_library_is_not_the_oracle(lib):
+    # the product library must not link or contain the CPU oracle
+    from speculative_verify_paged_attn_gb300 import svpa
+    data = open(svpa.LIB_PATH, "rb").read()
+    assert b"oracle_" not in data

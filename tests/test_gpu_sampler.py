@@ -1,0 +1,155 @@
+"""GPU parity of svpa_spec_accept / svpa_spec_accept_tree against the oracle.
+
+Accepted lengths must be bit-exact everywhere (the acceptance test is one
+rounded fp32 product on both sides).  Emitted tokens must be bit-exact on
+every row whose final draw the oracle does not flag as within 1e-6 of a CDF
+boundary; flagged rows are counted and must stay rare.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_verify_paged_attn_gb300 import svpa
+from speculative_verify_paged_attn_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def run_linear(s):
+    B, g1, V = s.p.shape
+    d = {k: getattr(s, k).to(DEV) for k in ("p", "q", "tokens", "u_accept", "u_sample")}
+    k = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+    toks = torch.full((B, g1), -7, dtype=torch.int32, device=DEV)
+    near = torch.zeros(B, dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(svpa.spec_accept_workspace_size(B, V), dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for _ in range(2):  # second call checks the self-cleaning tickets
+        svpa.spec_accept(d["p"], d["q"], d["tokens"], d["u_accept"], d["u_sample"], k, toks,
+                         workspace=ws, error_flag=err, near_boundary=near)
+    assert svpa.check_error(err) == 0
+    return k.cpu().numpy(), toks.cpu().numpy(), near.cpu().numpy().astype(bool)
+
+
+def check_linear(s, max_near_frac=0.01):
+    k, toks, gnear = run_linear(s)
+    rk, rt, rnear, _ = oracle.spec_accept(s.p.cpu(), s.q.cpu(), s.tokens.cpu(), s.u_accept.cpu(),
+                                          s.u_sample.cpu())
+    assert np.array_equal(k, rk)
+    ok = ~rnear
+    assert np.array_equal(toks[ok], rt[ok])
+    assert rnear.mean() <= max_near_frac
+    # flagged rows: the accepted prefix still matches exactly
+    for b in np.where(rnear)[0]:
+        assert np.array_equal(toks[b, :k[b]], rt[b, :k[b]])
+    return k
+
+
+@pytest.mark.parametrize("name", ["tiny", "7b", "70b"])
+def test_linear_parity(name):
+    wl = W.WORKLOADS[name]
+    s = W.make_sampler(wl, W.SEEDS[name], device="cpu")
+    check_linear(s)
+
+
+def test_linear_fp8_workload_shape():
+    wl = W.WORKLOADS["fp8"]
+    s = W.make_sampler(wl, W.SEEDS["fp8"], device="cpu")
+    check_linear(s)
+
+
+def test_linear_many_rows_small_vocab():
+    wl = W.WORKLOADS["7b"].scaled(batch=3000, vocab=257, gamma=6)
+    s = W.make_sampler(wl, 44, device="cpu")
+    k = check_linear(s)
+    assert 0 < (k == wl.gamma).mean() < 1 and (k == 0).any()
+
+
+def test_linear_all_accept_and_all_reject():
+    wl = W.WORKLOADS["7b"].scaled(batch=8, vocab=5000)
+    s = W.make_sampler(wl, 45, device="cpu")
+    # P == Q: everything accepted, bonus from P_gamma
+    s.q = s.p[:, :wl.gamma].clone()
+    k, toks, _ = run_linear(s)
+    assert np.all(k == wl.gamma)
+    check_linear(s)
+    # draft token impossible under P: rejected at 0
+    s2 = W.make_sampler(wl, 46, device="cpu")
+    x = s2.tokens[:, 0].long()
+    s2.p[torch.arange(8), 0, x] = 0.0
+    k, _, _ = run_linear(s2)
+    assert np.all(k == 0)
+    check_linear(s2)
+
+
+def test_linear_uniform_edges():
+    wl = W.WORKLOADS["7b"].scaled(batch=16, vocab=4099)
+    s = W.make_sampler(wl, 47, device="cpu")
+    s.u_sample[:4] = 0.0
+    s.u_sample[4:8] = torch.nextafter(torch.tensor(1.0), torch.tensor(0.0))
+    s.u_accept[8:12] = 0.0
+    check_linear(s)
+
+
+@pytest.mark.parametrize("batch", [4, 128])
+def test_tree_parity(batch):
+    wl = W.WORKLOADS["tree"].scaled(batch=batch)
+    s = W.make_sampler(wl, W.SEEDS["tree"], device="cpu")
+    parent = wl.parent
+    B, n, V = s.p.shape
+    W_ = oracle.tree_max_depth(np.array(parent, np.int32)) + 1
+    k = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+    path = torch.full((B, W_), -7, dtype=torch.int32, device=DEV)
+    toks = torch.full((B, W_), -7, dtype=torch.int32, device=DEV)
+    near = torch.zeros(B, dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    svpa.spec_accept_tree(parent, s.p.to(DEV), s.q.to(DEV), s.tokens.to(DEV), s.u_accept.to(DEV),
+                          s.u_sample.to(DEV), k, path, toks, error_flag=err, near_boundary=near)
+    assert svpa.check_error(err) == 0
+    rk, rpath, rtoks, rnear = oracle.spec_accept_tree(np.array(parent, np.int32), s.p, s.q, s.tokens,
+                                                      s.u_accept, s.u_sample)
+    ok = ~rnear
+    assert rnear.mean() <= 0.02
+    assert np.array_equal(k.cpu().numpy()[ok], rk[ok])
+    assert np.array_equal(path.cpu().numpy()[ok], rpath[ok])
+    assert np.array_equal(toks.cpu().numpy()[ok], rtoks[ok])
+
+
+def test_tree_chain_matches_linear_kernel():
+    wl = W.WORKLOADS["7b"].scaled(batch=64, vocab=3000, gamma=4)
+    s = W.make_sampler(wl, 48, device="cpu")
+    k, toks, _ = run_linear(s)
+    B = 64
+    parent = [-1, 0, 1, 2, 3]
+    tok = torch.cat([torch.zeros(B, 1, dtype=torch.int32), s.tokens], 1)
+    ua = torch.cat([torch.zeros(B, 1), s.u_accept], 1)
+    kt = torch.empty(B, dtype=torch.int32, device=DEV)
+    path = torch.empty((B, 5), dtype=torch.int32, device=DEV)
+    outt = torch.empty((B, 5), dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    svpa.spec_accept_tree(parent, s.p.to(DEV), s.q.to(DEV), tok.to(DEV), ua.to(DEV),
+                          s.u_sample.to(DEV), kt, path, outt, error_flag=err)
+    assert svpa.check_error(err) == 0
+    assert np.array_equal(kt.cpu().numpy(), k)
+    assert np.array_equal(outt.cpu().numpy(), toks)
+
+
+def test_gpu_output_distribution_equals_target():
+    # Monte-Carlo on the GPU path: first emitted token ~ P_0
+    from scipy import stats
+    rng = np.random.default_rng(17)
+    B, gamma, V = 100_000, 2, 8
+    logits = rng.normal(0, 1.5, size=(gamma + 1, V))
+    P = np.exp(logits) / np.exp(logits).sum(-1, keepdims=True)
+    ql = rng.normal(0, 1.5, size=(gamma, V))
+    Q = np.exp(ql) / np.exp(ql).sum(-1, keepdims=True)
+    P32 = torch.tensor(np.broadcast_to(P, (B, gamma + 1, V)).copy(), dtype=torch.float32)
+    Q32 = torch.tensor(np.broadcast_to(Q, (B, gamma, V)).copy(), dtype=torch.float32)
+    cdf = np.cumsum(Q, -1)
+    x = torch.tensor((rng.random((B, gamma, 1)) >= cdf[None]).sum(-1), dtype=torch.int32)
+    s = W.SamplerInputs(p=P32, q=Q32, tokens=x, u_accept=torch.tensor(rng.random((B, gamma)), dtype=torch.float32),
+                        u_sample=torch.tensor(rng.random(B), dtype=torch.float32))
+    k, toks, _ = run_linear(s)
+    obs = np.bincount(toks[:, 0], minlength=V)
+    assert stats.chisquare(obs, P[0] / P[0].sum() * B).pvalue > 1e-4
