@@ -84,6 +84,9 @@ typedef struct svpa_attn_params {
     int32_t kv_dtype;           /* SVPA_KV_BF16 or SVPA_KV_FP8_E4M3           */
     float sm_scale;             /* softmax scale, normally 1/sqrt(D)          */
     int32_t split_pages;        /* pages per KV split; 0 = chosen by library  */
+    int32_t variant;            /* 0 = chosen by library; 1 = warp-level MMA
+                                   kernel; 2 = tcgen05/TMEM kernel (bf16,
+                                   head_dim 128)                               */
 } svpa_attn_params;
 
 /* Bytes of workspace svpa_paged_verify_attn needs for `p` (split-KV partial

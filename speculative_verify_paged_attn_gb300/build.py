@@ -22,6 +22,7 @@ COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler",
 SOURCES = {
     "svpa_api.cu": [],
     "paged_verify_attn.cu": [],
+    "paged_verify_attn_tc.cu": [],
     "spec_accept.cu": ["-fmad=false"],
     "block_table_commit.cu": [],
 }

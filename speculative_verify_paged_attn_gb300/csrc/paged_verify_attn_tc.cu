@@ -1,0 +1,535 @@
+// paged_verify_attn_tc.cu -- paged verification attention on the 5th-generation
+// tensor cores (tcgen05 + TMEM) for sm_103a, used when one kv head carries
+// many query rows (grouped-query models, draft trees: G * n_q up to 128).
+//
+// Same computation as paged_verify_attn.cu ("The Sub-Millisecond Speculative
+// Decoding Meltdown", section "Speculative Decoding Mechanics & The K-Token
+// Penalty": A = softmax(Q K^T * scale + M_tree) V over a paged K/V history;
+// "Triton CUDA Fused Speculative Tree-Verification Kernel": per-page block
+// lookup, K/V cache [blocks, heads, 16, dim], running max / sum).
+//
+// Work unit = (sequence, kv head, KV split); persistent CTAs, one per SM.
+// Warp roles:
+//   warp 0     producer: takes units from an atomic counter, streams blocks of
+//              4 pages (64 tokens) of K and V -- and each unit's query tile --
+//              with tiled TMA copies (128-byte swizzle) into a 3-stage ring;
+//              missing pages of a unit's last block are fetched at an
+//              out-of-range block coordinate, which the copy fills with zeros;
+//   warp 1     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T
+//              (M 128, N 64, K 128) into one of two TMEM S buffers, looking one
+//              block ahead, and O += P_j V_j (M 128, N 128, K 64) into one of
+//              two TMEM O buffers (one per unit in flight);
+//   warps 2-5  softmax + epilogue, one thread per query row (TMEM lane): S row
+//              from TMEM, mask, online softmax with a lazy reference maximum
+//              (O in TMEM is rescaled only when a row maximum grows by more
+//              than 2^8), P row as bf16 into shared memory for the PV MMA;
+//              at a unit's end, O row from TMEM to the output (or a split
+//              partial, merged by the last split's CTA with a log-sum-exp).
+// All waits are bounded; nothing spins forever.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "svpa_device.cuh"
+#include "svpa_internal.h"
+
+namespace svpa {
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kPagesPerBlock = 4;
+constexpr int kNB = kPagesPerBlock * 16;       // tokens per block
+constexpr int kRows = 128;                      // MMA M
+constexpr int kKSlab = kNB * 128;               // one 128-byte column slab of a K (or V) block
+constexpr int kKVTile = 2 * kKSlab;             // K (or V) block, 128 columns
+constexpr int kStage = 2 * kKVTile;             // K block then V block
+constexpr int kQSlab = kRows * 128;
+constexpr int kQBuf = 2 * kQSlab;
+constexpr int kPBuf = kRows * 128;              // 128 rows x 64 bf16
+constexpr int kStages = 3;
+constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kBarSoftmax = 1;
+constexpr float kRescaleLog2 = 8.f;             // rescale O when a maximum grows by > 2^8
+
+// TMEM columns: O[0] 0..127, O[1] 128..255, S[0] 256..319, S[1] 320..383
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 0, kTmemS = 256;
+
+constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagEnd = 4;
+
+struct BlockMeta {
+    int32_t b, h, split, pos0, ntok, L, nsplit, flags, qb;
+    int32_t pad[3];
+};
+
+struct Smem {
+    uint8_t q[2][kQBuf];                 // 2 x 32 KB, 1024-aligned
+    uint8_t stage[kStages][kStage];      // 3 x 32 KB
+    uint8_t p[2][kPBuf];                 // 2 x 16 KB
+    uint64_t kv_full[kStages], kv_empty[kStages];
+    uint64_t q_empty[2];
+    uint64_t s_full[2], s_empty[2];
+    uint64_t p_full[2], p_empty[2];
+    uint64_t o_full[2], o_empty[2];
+    BlockMeta meta[kStages];
+    uint32_t tmem_base;
+    int32_t last;
+};
+
+__device__ __forceinline__ uint32_t par_of(int idx) { return (uint32_t)((idx >> 1) & 1); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    pva_tc_kernel(const __grid_constant__ CUtensorMap mk0, const __grid_constant__ CUtensorMap mk1,
+                  const __grid_constant__ CUtensorMap mv0, const __grid_constant__ CUtensorMap mv1,
+                  const __grid_constant__ CUtensorMap mq0, const __grid_constant__ CUtensorMap mq1,
+                  const __grid_constant__ AttnArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm.kv_full[i], 1);
+            mbar_init(&sm.kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.q_empty[i], 1);
+            mbar_init(&sm.s_full[i], 1);
+            mbar_init(&sm.s_empty[i], 4);
+            mbar_init(&sm.p_full[i], 4);
+            mbar_init(&sm.p_empty[i], 1);
+            mbar_init(&sm.o_full[i], 1);
+            mbar_init(&sm.o_empty[i], 4);
+        }
+        fence_mbar_init();
+    }
+    // query rows past M are never written by the copies: keep them zero
+    for (int x = threadIdx.x; x < 2 * kQBuf / 16; x += blockDim.x)
+        reinterpret_cast<uint4 *>(&sm.q[0][0])[x] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == 0) {
+        // ================================================= producer
+        const uint64_t pol = policy_evict_first();
+        if (lane == 0) {
+            prefetch_tensormap(&mk0);
+            prefetch_tensormap(&mk1);
+            prefetch_tensormap(&mv0);
+            prefetch_tensormap(&mv1);
+            prefetch_tensormap(&mq0);
+            prefetch_tensormap(&mq1);
+        }
+        int st = 0, issued = 0, units = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        const uint32_t qbytes = (uint32_t)(a.M * 128 * 2);
+        while (ok) {
+            int u = 0;
+            if (lane == 0) u = atomicAdd(&a.sched[0], 1);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (u >= a.total_units) break;
+            const int bh = u / a.max_splits, split = u - bh * a.max_splits;
+            const int b = bh / a.Hkv, h = bh - b * a.Hkv;
+            const int L = __ldg(a.context_lens + b);
+            const int npages = (L + a.n_q + kBlockSize - 1) / kBlockSize;
+            if (L < 0 || npages > a.max_blocks) {
+                if (lane == 0 && split == 0 && h == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                continue;
+            }
+            const int nsplit = (npages + a.split_pages - 1) / a.split_pages;
+            if (split >= nsplit) continue;
+            const int page0 = split * a.split_pages;
+            const int n = min(a.split_pages, npages - page0);
+            const int nblk = (n + kPagesPerBlock - 1) / kPagesPerBlock;
+            const int qb = units & 1;
+            const int32_t *bt = a.block_table + (size_t)b * a.max_blocks + page0;
+            for (int i0 = 0; i0 < n && ok; i0 += 32) {
+                int blk = a.num_blocks;  // out of range: zero-filled page
+                if (i0 + lane < n) {
+                    blk = __ldg(bt + i0 + lane);
+                    if (blk < 0 || blk >= a.num_blocks) {
+                        raise_error(a.err, SVPA_DEVERR_BAD_BLOCK);
+                        blk = 0;
+                    }
+                }
+                const int cnt = min(32, n - i0);
+                for (int j0 = 0; j0 < cnt; j0 += kPagesPerBlock) {
+                    int ids[kPagesPerBlock];
+#pragma unroll
+                    for (int p = 0; p < kPagesPerBlock; ++p) {
+                        ids[p] = __shfl_sync(0xffffffffu, blk, (j0 + p) & 31);
+                        if (j0 + p >= cnt) ids[p] = a.num_blocks;
+                    }
+                    if (lane == 0) {
+                        const int bi = (i0 + j0) / kPagesPerBlock;  // block index in the unit
+                        if (issued >= kStages) ok = mbar_wait(&sm.kv_empty[st], ph ^ 1u, a.err);
+                        if (ok && bi == 0 && units >= 2) ok = mbar_wait(&sm.q_empty[qb], par_of(units) ^ 1u, a.err);
+                        if (ok) {
+                            BlockMeta &m = sm.meta[st];
+                            m.b = b; m.h = h; m.split = split; m.L = L; m.nsplit = nsplit; m.qb = qb;
+                            m.pos0 = (page0 + i0 + j0) * kBlockSize;
+                            m.ntok = min(kPagesPerBlock, n - (i0 + j0)) * kBlockSize;
+                            m.flags = (bi == 0 ? kFlagFirst : 0) | (bi == nblk - 1 ? kFlagLast : 0);
+                            mbar_arrive_expect_tx(&sm.kv_full[st], kStage + (bi == 0 ? qbytes : 0u));
+                            if (bi == 0) {
+                                tma_load_4d(&sm.q[qb][0], &mq0, 0, h * a.G, 0, b, &sm.kv_full[st], pol);
+                                tma_load_4d(&sm.q[qb][kQSlab], &mq1, 0, h * a.G, 0, b, &sm.kv_full[st], pol);
+                            }
+                            uint8_t *sk = sm.stage[st];
+                            uint8_t *sv = sk + kKVTile;
+#pragma unroll
+                            for (int p = 0; p < kPagesPerBlock; ++p) {
+                                tma_load_4d(sk + p * 2048, &mk0, 0, 0, h, ids[p], &sm.kv_full[st], pol);
+                                tma_load_4d(sk + kKSlab + p * 2048, &mk1, 0, 0, h, ids[p], &sm.kv_full[st], pol);
+                                tma_load_4d(sv + p * 2048, &mv0, 0, 0, h, ids[p], &sm.kv_full[st], pol);
+                                tma_load_4d(sv + kKSlab + p * 2048, &mv1, 0, 0, h, ids[p], &sm.kv_full[st], pol);
+                            }
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+                    if (!ok) break;
+                    ++issued;
+                    if (++st == kStages) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            ++units;
+        }
+        if (lane == 0) {
+            if (ok && issued >= kStages) ok = mbar_wait(&sm.kv_empty[st], ph ^ 1u, a.err);
+            if (ok) {
+                sm.meta[st].flags = kFlagEnd;
+                mbar_arrive(&sm.kv_full[st]);
+            }
+            // wait (bounded) for the copies still in flight; the stage reused
+            // by the end marker had completed before its empty barrier passed
+            const int first = issued >= kStages ? issued - kStages + 1 : 0;
+            for (int i = first; i < issued && ok; ++i)
+                ok = mbar_wait(&sm.kv_full[i % kStages], (uint32_t)((i / kStages) & 1), a.err);
+            __threadfence();
+            const int done = atomicAdd(&a.sched[1], 1);
+            if (done == (int)gridDim.x - 1) {
+                a.sched[0] = 0;
+                a.sched[1] = 0;
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================= MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = umma_idesc_bf16(kRows, kNB, false);
+            constexpr uint32_t idPV = umma_idesc_bf16(kRows, kD, true);
+            const uint32_t qaddr[2] = {smem_u32(&sm.q[0][0]), smem_u32(&sm.q[1][0])};
+            bool ok = true;
+            int j = 0;          // block index (all units)
+            int st = 0;         // ring stage of block j
+            uint32_t ph = 0;    // ring phase of block j
+            int unit = -1;      // unit index of block j
+            // fetch block j's stage; issue S_j (or forward the end marker)
+            auto issue_s = [&](int jj, int stj, uint32_t phj, int &unit_jj, BlockMeta &m) -> bool {
+                if (!mbar_wait(&sm.kv_full[stj], phj, a.err)) return false;
+                m = sm.meta[stj];
+                if (jj >= 2 && !mbar_wait(&sm.s_empty[jj & 1], par_of(jj) ^ 1u, a.err)) return false;
+                if (m.flags & kFlagEnd) {
+                    mbar_arrive(&sm.s_full[jj & 1]);
+                    return true;
+                }
+                if (m.flags & kFlagFirst) ++unit_jj;
+                tc_fence_after();
+                const uint32_t qa = qaddr[m.qb];
+                const uint32_t ka = smem_u32(sm.stage[stj]);
+                const uint32_t dS = tmem + kTmemS + (uint32_t)(jj & 1) * kNB;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint64_t ad = umma_desc_sw128(qa + (kk >> 2) * kQSlab + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = umma_desc_sw128(ka + (kk >> 2) * kKSlab + (kk & 3) * 32, 16, 1024);
+                    umma_bf16(dS, ad, bd, idS, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&sm.s_full[jj & 1]);
+                if (m.flags & kFlagLast) umma_commit(&sm.q_empty[m.qb]);
+                return true;
+            };
+            BlockMeta cur, nxt;
+            int unit_next = unit;
+            ok = issue_s(0, st, ph, unit_next, cur);
+            unit = unit_next;
+            while (ok && !(cur.flags & kFlagEnd)) {
+                // look ahead: S of block j+1 while the softmax works on block j
+                const int st1 = st + 1 == kStages ? 0 : st + 1;
+                const uint32_t ph1 = st + 1 == kStages ? ph ^ 1u : ph;
+                int unit1 = unit;
+                ok = issue_s(j + 1, st1, ph1, unit1, nxt);
+                if (!ok) break;
+                // O += P_j V_j once the softmax has written P_j
+                if (!mbar_wait(&sm.p_full[j & 1], par_of(j), a.err)) break;
+                const int ob = unit & 1;
+                if ((cur.flags & kFlagFirst) && unit >= 2 &&
+                    !mbar_wait(&sm.o_empty[ob], par_of(unit) ^ 1u, a.err))
+                    break;
+                tc_fence_after();
+                const uint32_t pa = smem_u32(&sm.p[j & 1][0]);
+                const uint32_t va = smem_u32(sm.stage[st]) + kKVTile;
+                const uint32_t dO = tmem + kTmemO + (uint32_t)ob * kD;
+#pragma unroll
+                for (int kt = 0; kt < kNB / 16; ++kt) {
+                    const uint64_t ad = umma_desc_sw128(pa + kt * 32, 16, 1024);
+                    const uint64_t bd = umma_desc_sw128(va + kt * 2048, kKSlab, 1024);
+                    umma_bf16(dO, ad, bd, idPV, ((cur.flags & kFlagFirst) && kt == 0) ? 0u : 1u);
+                }
+                umma_commit(&sm.kv_empty[st]);
+                umma_commit(&sm.p_empty[j & 1]);
+                if (cur.flags & kFlagLast) umma_commit(&sm.o_full[ob]);
+                ++j;
+                st = st1;
+                ph = ph1;
+                unit = unit1;
+                cur = nxt;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================================================= softmax + epilogue
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;          // query row == TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int G = a.G;
+        const bool live = r < a.M;
+        const int jq = live ? r / G : 0;
+        const unsigned long long anc = live ? a.anc[jq] : 0ull;
+        float m_ref = -CUDART_INF_F, l_run = 0.f;
+        int j = 0, unit = -1;
+        while (true) {
+            if (!mbar_wait(&sm.s_full[j & 1], par_of(j), a.err)) break;
+            const BlockMeta md = sm.meta[j % kStages];
+            if (md.flags & kFlagEnd) break;
+            if (md.flags & kFlagFirst) {
+                ++unit;
+                m_ref = -CUDART_INF_F;
+                l_run = 0.f;
+            }
+            tc_fence_after();
+            float s[kNB];
+            {
+                uint32_t raw[32];
+                const uint32_t sa = tmem + kTmemS + (uint32_t)(j & 1) * kNB + lane_off;
+                tmem_ld32(sa, raw);
+                tmem_ld_wait();
+#pragma unroll
+                for (int t = 0; t < 32; ++t) s[t] = __uint_as_float(raw[t]);
+                tmem_ld32(sa + 32, raw);
+                tmem_ld_wait();
+#pragma unroll
+                for (int t = 0; t < 32; ++t) s[32 + t] = __uint_as_float(raw[t]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.s_empty[j & 1]);
+
+            const int L = md.L, T = L + a.n_q;
+            float mx = -CUDART_INF_F;
+            const bool need_mask = md.pos0 + kNB > L || md.ntok < kNB;
+#pragma unroll
+            for (int t = 0; t < kNB; ++t) {
+                float v = s[t] * a.scale_log2;
+                if (need_mask) {
+                    const int p = md.pos0 + t;
+                    const int si = p - L;
+                    const bool vis = t < md.ntok && (si < 0 || (si < a.n_q && ((anc >> si) & 1ull)));
+                    if (!vis) v = -CUDART_INF_F;
+                }
+                s[t] = v;
+                mx = fmaxf(mx, v);
+            }
+            float alpha = 1.f;
+            bool rescale = false;
+            if (mx > m_ref + kRescaleLog2 || (m_ref == -CUDART_INF_F && mx != -CUDART_INF_F)) {
+                alpha = exp2f(m_ref - mx);  // 0 when m_ref is -inf
+                m_ref = mx;
+                rescale = !(md.flags & kFlagFirst) && l_run > 0.f;
+                l_run *= alpha;
+            }
+            const float msafe = m_ref == -CUDART_INF_F ? 0.f : m_ref;
+            // P_j goes to the buffer PV_{j-2} read
+            if (j >= 2) mbar_wait(&sm.p_empty[j & 1], par_of(j) ^ 1u, a.err);
+            uint8_t *prow = &sm.p[j & 1][0] + r * 128;
+            float lsum = 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < kNB / 8; ++c8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = live ? exp2f(s[c8 * 8 + 2 * e] - msafe) : 0.f;
+                    const float p1 = live ? exp2f(s[c8 * 8 + 2 * e + 1] - msafe) : 0.f;
+                    lsum += p0 + p1;
+                    w[e] = pack_bf16x2(p0, p1);
+                }
+                *reinterpret_cast<uint4 *>(prow + ((c8 ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            l_run += lsum;
+            // V rows past the sequence's last token may hold anything
+            if (md.pos0 + md.ntok > T) {
+                const int t0 = T - md.pos0;
+                const int nz = (md.ntok - t0) * 2 * 8;
+                uint8_t *sv = sm.stage[j % kStages] + kKVTile;
+                for (int z = threadIdx.x - 64; z < nz; z += kSoftmaxThreads) {
+                    const int row = t0 + z / 16, rem = z % 16;
+                    *reinterpret_cast<uint4 *>(sv + (rem >> 3) * kKSlab + row * 128 + ((rem & 7) << 4)) =
+                        make_uint4(0, 0, 0, 0);
+                }
+            }
+            // TMEM loads and stores are warp-collective: the whole warp takes
+            // the rescale path when any of its rows needs it (factor 1 elsewhere)
+            if (__any_sync(0xffffffffu, rescale)) {
+                const float f = rescale ? alpha : 1.f;
+                // O (TMEM) holds P_{<j} V; PV_{j-1} must have landed first
+                mbar_wait(&sm.p_empty[(j - 1) & 1], par_of(j - 1), a.err);
+                tc_fence_after();
+                const uint32_t oa = tmem + kTmemO + (uint32_t)(unit & 1) * kD + lane_off;
+#pragma unroll
+                for (int c = 0; c < kD / 32; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(oa + c * 32, raw);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) raw[t] = __float_as_uint(__uint_as_float(raw[t]) * f);
+                    tmem_st32(oa + c * 32, raw);
+                }
+                tmem_st_wait();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.p_full[j & 1]);
+
+            if (md.flags & kFlagLast) {
+                // ---- unit epilogue: O row from TMEM
+                const int ob = unit & 1;
+                mbar_wait(&sm.o_full[ob], par_of(unit), a.err);
+                tc_fence_after();
+                const uint32_t oa = tmem + kTmemO + (uint32_t)ob * kD + lane_off;
+                float o[kD];
+#pragma unroll
+                for (int c = 0; c < kD / 32; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(oa + c * 32, raw);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) o[c * 32 + t] = __uint_as_float(raw[t]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.o_empty[ob]);
+                const int b = md.b, h = md.h;
+                if (md.nsplit == 1) {
+                    if (live) {
+                        const int gi = r - jq * G;
+                        const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
+                        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                        uint4 *orow = reinterpret_cast<uint4 *>(a.out + od * kD);
+#pragma unroll
+                        for (int c8 = 0; c8 < kD / 8; ++c8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(o[c8 * 8 + 0] * inv, o[c8 * 8 + 1] * inv);
+                            v.y = pack_bf16x2(o[c8 * 8 + 2] * inv, o[c8 * 8 + 3] * inv);
+                            v.z = pack_bf16x2(o[c8 * 8 + 4] * inv, o[c8 * 8 + 5] * inv);
+                            v.w = pack_bf16x2(o[c8 * 8 + 6] * inv, o[c8 * 8 + 7] * inv);
+                            orow[c8] = v;
+                        }
+                        if (a.lse) a.lse[od] = (m_ref + log2f(l_run)) * 0.69314718055994530942f;
+                    }
+                } else {
+                    const int u2 = b * a.Hkv + h;
+                    if (live) {
+                        const size_t pr = ((size_t)u2 * a.max_splits + md.split) * a.M + r;
+                        float4 *prow4 = reinterpret_cast<float4 *>(a.part_acc + pr * kD);
+#pragma unroll
+                        for (int c4 = 0; c4 < kD / 4; ++c4)
+                            prow4[c4] = make_float4(o[c4 * 4], o[c4 * 4 + 1], o[c4 * 4 + 2], o[c4 * 4 + 3]);
+                        a.part_ml[pr * 2] = m_ref;
+                        a.part_ml[pr * 2 + 1] = l_run;
+                    }
+                    __threadfence();
+                    named_barrier_sync(kBarSoftmax, kSoftmaxThreads);
+                    if (threadIdx.x == 64) {
+                        const int t = atomicAdd(&a.tickets[u2], 1);
+                        sm.last = (t == md.nsplit - 1);
+                        if (sm.last) a.tickets[u2] = 0;
+                    }
+                    named_barrier_sync(kBarSoftmax, kSoftmaxThreads);
+                    const int last = sm.last;
+                    named_barrier_sync(kBarSoftmax, kSoftmaxThreads);
+                    if (last && live) {
+                        __threadfence();
+                        const size_t base = (size_t)u2 * a.max_splits * a.M + r;
+                        float mx2 = -CUDART_INF_F;
+                        for (int s2 = 0; s2 < md.nsplit; ++s2)
+                            mx2 = fmaxf(mx2, __ldcg(&a.part_ml[(base + (size_t)s2 * a.M) * 2]));
+                        const float ms2 = mx2 == -CUDART_INF_F ? 0.f : mx2;
+                        float l2 = 0.f;
+#pragma unroll
+                        for (int d = 0; d < kD; ++d) o[d] = 0.f;
+                        for (int s2 = 0; s2 < md.nsplit; ++s2) {
+                            const size_t pr = base + (size_t)s2 * a.M;
+                            const float w = exp2f(__ldcg(&a.part_ml[pr * 2]) - ms2);
+                            l2 += w * __ldcg(&a.part_ml[pr * 2 + 1]);
+                            const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + pr * kD);
+#pragma unroll
+                            for (int c4 = 0; c4 < kD / 4; ++c4) {
+                                const float4 v = __ldcg(src + c4);
+                                o[c4 * 4] += w * v.x;
+                                o[c4 * 4 + 1] += w * v.y;
+                                o[c4 * 4 + 2] += w * v.z;
+                                o[c4 * 4 + 3] += w * v.w;
+                            }
+                        }
+                        const int gi = r - jq * G;
+                        const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
+                        const float inv = l2 > 0.f ? 1.f / l2 : 0.f;
+                        uint4 *orow = reinterpret_cast<uint4 *>(a.out + od * kD);
+#pragma unroll
+                        for (int c8 = 0; c8 < kD / 8; ++c8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(o[c8 * 8 + 0] * inv, o[c8 * 8 + 1] * inv);
+                            v.y = pack_bf16x2(o[c8 * 8 + 2] * inv, o[c8 * 8 + 3] * inv);
+                            v.z = pack_bf16x2(o[c8 * 8 + 4] * inv, o[c8 * 8 + 5] * inv);
+                            v.w = pack_bf16x2(o[c8 * 8 + 6] * inv, o[c8 * 8 + 7] * inv);
+                            orow[c8] = v;
+                        }
+                        if (a.lse) a.lse[od] = (mx2 + log2f(l2)) * 0.69314718055994530942f;
+                    }
+                }
+            }
+            ++j;
+        }
+    }
+    // every TMEM user is done (the MMA issuer's last operations were waited
+    // on by the softmax warps through o_full) before the owner frees it
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+size_t attn_tc_smem_bytes() { return sizeof(Smem) + 1024; }
+
+cudaError_t launch_paged_verify_attn_tc(const AttnMaps &m, const AttnArgs &a, int grid, cudaStream_t st) {
+    const size_t smem = attn_tc_smem_bytes();
+    cudaError_t e = cudaFuncSetAttribute(pva_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    pva_tc_kernel<<<grid, kThreads, smem, st>>>(m.k[0], m.k[1], m.v[0], m.v[1], m.q[0], m.q[1], a);
+    return cudaGetLastError();
+}
+
+}  // namespace svpa

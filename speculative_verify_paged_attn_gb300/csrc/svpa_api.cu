@@ -15,7 +15,6 @@
 
 namespace svpa {
 int spec_accept_chunks(int vocab);
-int attn_pick_stages(int head_dim, bool fp8, int M, int split_pages);
 }  // namespace svpa
 
 using namespace svpa;
@@ -63,6 +62,8 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
         p->num_blocks < 1 || !(p->sm_scale > 0.f) || !std::isfinite(p->sm_scale) || p->split_pages < 0)
         return SVPA_ERR_INVALID_ARG;
     if (p->kv_dtype != SVPA_KV_BF16 && p->kv_dtype != SVPA_KV_FP8_E4M3) return SVPA_ERR_INVALID_ARG;
+    if (p->variant < 0 || p->variant > 2) return SVPA_ERR_INVALID_ARG;
+    if (p->variant == 2 && (p->head_dim != 128 || p->kv_dtype != SVPA_KV_BF16)) return SVPA_ERR_UNSUPPORTED;
     if (p->head_dim != 64 && p->head_dim != 128) return SVPA_ERR_UNSUPPORTED;
     if (p->kv_dtype == SVPA_KV_FP8_E4M3 && p->head_dim != 128) return SVPA_ERR_UNSUPPORTED;
     const int G = p->num_q_heads / p->num_kv_heads;
@@ -88,7 +89,8 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     pl->split_pages = sp;
     pl->max_splits = (p->max_blocks_per_seq + sp - 1) / sp;
     const size_t units = (size_t)p->batch * p->num_kv_heads;
-    size_t off = align_up(units * sizeof(int32_t));
+    // [scheduler counters][tickets][split (max, sum)][split accumulators]
+    size_t off = kAlign + align_up(units * sizeof(int32_t));
     pl->off_ml = off;
     if (pl->max_splits > 1) {
         off += align_up(units * pl->max_splits * M * 2 * sizeof(float));
@@ -186,6 +188,23 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
             return SVPA_ERR_CUDA;
     }
 
+    {
+        // queries [B, n_q, Hq, D] bf16: box = (64 columns, G heads, n_q queries, 1)
+        const int G = p->num_q_heads / p->num_kv_heads;
+        const cuuint64_t qd[4] = {64, (cuuint64_t)p->num_q_heads, (cuuint64_t)p->n_q, (cuuint64_t)p->batch};
+        const cuuint64_t qs[3] = {(cuuint64_t)D * 2, (cuuint64_t)p->num_q_heads * D * 2,
+                                  (cuuint64_t)p->n_q * p->num_q_heads * D * 2};
+        const cuuint32_t qbox[4] = {64, (cuuint32_t)G, (cuuint32_t)p->n_q, 1};
+        const int qslabs = D * 2 / 128;
+        for (int sl = 0; sl < 2; ++sl) {
+            char *qb = (char *)const_cast<void *>(q) + (sl < qslabs ? sl : 0) * 128;
+            if (enc(&maps.q[sl], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, qb, qd, qs, qbox, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return SVPA_ERR_CUDA;
+        }
+    }
+
     AttnArgs a;
     memset(&a, 0, sizeof a);
     a.q = static_cast<const __nv_bfloat16 *>(q);
@@ -196,7 +215,8 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.lse = lse;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    a.tickets = reinterpret_cast<int32_t *>(ws);
+    a.sched = reinterpret_cast<int32_t *>(ws);
+    a.tickets = reinterpret_cast<int32_t *>(ws + kAlign);
     a.part_ml = reinterpret_cast<float *>(ws + pl.off_ml);
     a.part_acc = reinterpret_cast<float *>(ws + pl.off_acc);
     a.err = error_flag;
@@ -213,9 +233,18 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
     a.scale_log2 = p->sm_scale * 1.4426950408889634f;
     for (int j = 0; j < p->n_q; ++j)
         a.anc[j] = ancestor_mask ? ancestor_mask[j] : ((j == 63) ? ~0ull : ((1ull << (j + 1)) - 1ull));
-    a.n_stages = attn_pick_stages(D, fp8, pl.M, pl.split_pages);
-    if (a.n_stages <= 0) return SVPA_ERR_CUDA;
-    return from_cuda(launch_paged_verify_attn(maps, a, D, fp8, static_cast<cudaStream_t>(stream)));
+    a.total_units = p->batch * p->num_kv_heads * pl.max_splits;
+    const bool use_tc = p->variant == 2 || (p->variant == 0 && D == 128 && !fp8 && pl.M > 16);
+    if (use_tc) {
+        const int grid = std::max(1, std::min(sm_count(), a.total_units));
+        return from_cuda(launch_paged_verify_attn_tc(maps, a, grid, static_cast<cudaStream_t>(stream)));
+    }
+    AttnLaunch lp;
+    if (attn_plan_launch(D, fp8, pl.M, &lp) != cudaSuccess) return SVPA_ERR_CUDA;
+    a.n_stages = lp.n_stages;
+    const long long slots = (long long)lp.ctas_per_sm * sm_count();
+    const int grid = (int)std::max(1LL, std::min<long long>(slots, a.total_units));
+    return from_cuda(launch_paged_verify_attn(maps, a, D, fp8, grid, lp.smem, static_cast<cudaStream_t>(stream)));
 }
 
 svpa_status svpa_spec_accept_workspace_size(int32_t batch, int32_t vocab, size_t *bytes) {

@@ -27,9 +27,10 @@ struct AttnArgs {
     float *part_acc;      // [B*Hkv, max_splits, M, D]
     float *part_ml;       // [B*Hkv, max_splits, M, 2]  (running max in log2 units, sum)
     int32_t *tickets;     // [B*Hkv]
+    int32_t *sched;       // [2]: next work unit, CTAs finished (both back to 0 after a call)
     int32_t *err;
     int32_t B, n_q, Hq, Hkv, G, M;
-    int32_t max_blocks, num_blocks, split_pages, max_splits, n_stages;
+    int32_t max_blocks, num_blocks, split_pages, max_splits, n_stages, total_units;
     float scale_log2;     // sm_scale * log2(e)
     unsigned long long anc[kMaxNq];  // visibility of speculative slots per query
 };
@@ -37,13 +38,23 @@ struct AttnArgs {
 struct AttnMaps {
     CUtensorMap k[2];     // 128-byte column slabs of the K pages
     CUtensorMap v[2];
+    CUtensorMap q[2];     // 128-byte column slabs of the queries of one (sequence, kv head)
+};
+
+struct AttnLaunch {
+    int n_stages;
+    int ctas_per_sm;
+    size_t smem;
 };
 
 // Launch the attention kernel matching (head_dim, fp8, row tiles).
 cudaError_t launch_paged_verify_attn(const AttnMaps &maps, const AttnArgs &a, int head_dim,
-                                     bool fp8, cudaStream_t stream);
-size_t attn_smem_bytes(int head_dim, bool fp8, int n_stages, int split_pages);
-int attn_pick_stages(int head_dim, bool fp8, int M, int split_pages);
+                                     bool fp8, int grid, size_t smem, cudaStream_t stream);
+// Stage count, resident CTAs per SM and dynamic shared memory for a shape.
+cudaError_t attn_plan_launch(int head_dim, bool fp8, int M, AttnLaunch *out);
+// tcgen05 / TMEM variant (bf16 pages, head_dim 128, one CTA per SM).
+cudaError_t launch_paged_verify_attn_tc(const AttnMaps &maps, const AttnArgs &a, int grid,
+                                        cudaStream_t stream);
 
 // Rejection sampler.
 struct AcceptArgs {

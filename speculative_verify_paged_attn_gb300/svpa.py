@@ -41,7 +41,8 @@ class AttnParams(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
-                ("sm_scale", ctypes.c_float), ("split_pages", ctypes.c_int32)]
+                ("sm_scale", ctypes.c_float), ("split_pages", ctypes.c_int32),
+                ("variant", ctypes.c_int32)]
 
 
 _lib = None
@@ -89,11 +90,15 @@ def _check(status: int, what: str):
         raise SvpaError(status, what)
 
 
+VARIANT_AUTO, VARIANT_MMA, VARIANT_TCGEN05 = 0, 1, 2
+
+
 def attn_params(batch, n_q, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_blocks,
-                kv_fp8=False, sm_scale=None, split_pages=0, block_size=16) -> AttnParams:
+                kv_fp8=False, sm_scale=None, split_pages=0, block_size=16, variant=0) -> AttnParams:
     return AttnParams(batch, n_q, num_q_heads, num_kv_heads, head_dim, block_size,
                       max_blocks_per_seq, num_blocks, SVPA_KV_FP8_E4M3 if kv_fp8 else SVPA_KV_BF16,
-                      1.0 / math.sqrt(head_dim) if sm_scale is None else sm_scale, split_pages)
+                      1.0 / math.sqrt(head_dim) if sm_scale is None else sm_scale, split_pages,
+                      variant)
 
 
 def attn_workspace_size(params: AttnParams) -> int:

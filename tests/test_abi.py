@@ -59,9 +59,9 @@ def test_null_pointers_rejected_before_launch(lib):
     p = svpa.attn_params(2, 5, 4, 4, 64, 8, 16, split_pages=4)
     st = lib.svpa_paged_verify_attn(ctypes.byref(p), *([None] * 11), 0, None, None)
     assert st == 1
-    st = lib.svpa_spec_accept(2, 4, 1000, *([None] * 10), 0, None, None)
+    st = lib.svpa_spec_accept(2, 4, 1000, *([None] * 9), 0, None, None)
     assert st == 1
-    st = lib.svpa_spec_accept(2, 0, 1000, *([None] * 10), 0, None, None)
+    st = lib.svpa_spec_accept(2, 0, 1000, *([None] * 9), 0, None, None)
     assert st == 1
     st = lib.svpa_block_table_commit(2, 5, 16, 8, 16, *([None] * 7), 0, None, None, 4, 64, 0, None, None)
     assert st == 1
