@@ -39,6 +39,7 @@ from speculative_verify_paged_attn_gb300 import workloads as W  # noqa: E402
 METRIC = "paged verify-attn KV GB/s (% of GB300 HBM peak); spec_accept rows/s"
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ["speculative_verify_paged_attn_gb300/csrc/paged_verify_attn.cu",
+                  "speculative_verify_paged_attn_gb300/csrc/paged_verify_attn_tc.cu",
                   "speculative_verify_paged_attn_gb300/csrc/svpa_device.cuh"]
 
 
@@ -317,6 +318,8 @@ def main():
     ap.add_argument("--config", default="7b", choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="svpa", choices=["svpa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller cases for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -331,6 +334,8 @@ def main():
     torch.cuda.set_device(dev)
     svpa.load()
     wl = W.WORKLOADS[args.config]
+    if args.batch:
+        wl = wl.scaled(batch=args.batch)
     seed = W.SEEDS[args.config] + 7 * rank
     st = Step(wl, seed, dev)
     stream = torch.cuda.current_stream()

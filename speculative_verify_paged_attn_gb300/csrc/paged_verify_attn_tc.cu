@@ -42,11 +42,12 @@ constexpr int kNB = kPagesPerBlock * 16;       // tokens per block
 constexpr int kRows = 128;                      // MMA M
 constexpr int kKSlab = kNB * 128;               // one 128-byte column slab of a K (or V) block
 constexpr int kKVTile = 2 * kKSlab;             // K (or V) block, 128 columns
-constexpr int kStage = 2 * kKVTile;             // K block then V block
 constexpr int kQSlab = kRows * 128;
 constexpr int kQBuf = 2 * kQSlab;
 constexpr int kPBuf = kRows * 128;              // 128 rows x 64 bf16
-constexpr int kStages = 3;
+constexpr int kNK = 4;                          // K ring (freed once S_j is computed)
+constexpr int kNV = 4;                          // V ring (freed once PV_j is computed)
+constexpr int kNMeta = 8;                       // block descriptors in flight
 constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kBarSoftmax = 1;
@@ -65,14 +66,16 @@ struct BlockMeta {
 
 struct Smem {
     uint8_t q[2][kQBuf];                 // 2 x 32 KB, 1024-aligned
-    uint8_t stage[kStages][kStage];      // 3 x 32 KB
+    uint8_t kbuf[kNK][kKVTile];          // 4 x 16 KB
+    uint8_t vbuf[kNV][kKVTile];          // 4 x 16 KB
     uint8_t p[2][kPBuf];                 // 2 x 16 KB
-    uint64_t kv_full[kStages], kv_empty[kStages];
+    uint64_t k_full[kNK], k_empty[kNK];
+    uint64_t v_full[kNV], v_empty[kNV];
     uint64_t q_empty[2];
     uint64_t s_full[2], s_empty[2];
     uint64_t p_full[2], p_empty[2];
     uint64_t o_full[2], o_empty[2];
-    BlockMeta meta[kStages];
+    BlockMeta meta[kNMeta];
     uint32_t tmem_base;
     int32_t last;
 };
@@ -89,9 +92,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&sm.kv_full[i], 1);
-            mbar_init(&sm.kv_empty[i], 1);
+        for (int i = 0; i < kNK; ++i) {
+            mbar_init(&sm.k_full[i], 1);
+            mbar_init(&sm.k_empty[i], 1);
+        }
+        for (int i = 0; i < kNV; ++i) {
+            mbar_init(&sm.v_full[i], 1);
+            mbar_init(&sm.v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.q_empty[i], 1);
@@ -128,10 +135,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&mq0);
             prefetch_tensormap(&mq1);
         }
-        int st = 0, issued = 0, units = 0;
-        uint32_t ph = 0;
+        int jk = 0, jv = 0, units = 0;      // K blocks issued, V blocks issued, units started (warp-uniform)
         bool ok = true;
+        bool have_prev = false;             // a block whose V still has to be issued
+        int prev_id = 0, prev_h = 0;        // lanes 0..3: page `lane` of that block
         const uint32_t qbytes = (uint32_t)(a.M * 128 * 2);
+        // V of block jv, one block behind K so that K can run ahead; lanes 0..3
+        // issue one page each
+        auto issue_v = [&]() -> bool {
+            const int vs = jv % kNV;
+            bool good = true;
+            if (lane == 0) {
+                if (jv >= kNV) good = mbar_wait(&sm.v_empty[vs], (uint32_t)(((jv / kNV) & 1) ^ 1), a.err);
+                if (good) mbar_arrive_expect_tx(&sm.v_full[vs], kKVTile);
+            }
+            good = __shfl_sync(0xffffffffu, (int)good, 0) != 0;
+            if (good && lane < kPagesPerBlock) {
+                uint8_t *sv = sm.vbuf[vs] + lane * 2048;
+                tma_load_4d(sv, &mv0, 0, 0, prev_h, prev_id, &sm.v_full[vs], pol);
+                tma_load_4d(sv + kKSlab, &mv1, 0, 0, prev_h, prev_id, &sm.v_full[vs], pol);
+            }
+            if (good) ++jv;
+            return good;
+        };
         while (ok) {
             int u = 0;
             if (lane == 0) u = atomicAdd(&a.sched[0], 1);
@@ -163,60 +189,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int cnt = min(32, n - i0);
                 for (int j0 = 0; j0 < cnt; j0 += kPagesPerBlock) {
-                    int ids[kPagesPerBlock];
-#pragma unroll
-                    for (int p = 0; p < kPagesPerBlock; ++p) {
-                        ids[p] = __shfl_sync(0xffffffffu, blk, (j0 + p) & 31);
-                        if (j0 + p >= cnt) ids[p] = a.num_blocks;
-                    }
+                    // lanes 0..3 hold the ids of the block's 4 pages
+                    int my_id = __shfl_sync(0xffffffffu, blk, (j0 + (lane & 3)) & 31);
+                    if (j0 + (lane & 3) >= cnt) my_id = a.num_blocks;
+                    const int bi = (i0 + j0) / kPagesPerBlock;  // block index in the unit
+                    const int ks = jk % kNK;
                     if (lane == 0) {
-                        const int bi = (i0 + j0) / kPagesPerBlock;  // block index in the unit
-                        if (issued >= kStages) ok = mbar_wait(&sm.kv_empty[st], ph ^ 1u, a.err);
+                        if (jk >= kNK) ok = mbar_wait(&sm.k_empty[ks], (uint32_t)(((jk / kNK) & 1) ^ 1), a.err);
                         if (ok && bi == 0 && units >= 2) ok = mbar_wait(&sm.q_empty[qb], par_of(units) ^ 1u, a.err);
                         if (ok) {
-                            BlockMeta &m = sm.meta[st];
+                            BlockMeta &m = sm.meta[jk % kNMeta];
                             m.b = b; m.h = h; m.split = split; m.L = L; m.nsplit = nsplit; m.qb = qb;
                             m.pos0 = (page0 + i0 + j0) * kBlockSize;
                             m.ntok = min(kPagesPerBlock, n - (i0 + j0)) * kBlockSize;
                             m.flags = (bi == 0 ? kFlagFirst : 0) | (bi == nblk - 1 ? kFlagLast : 0);
-                            mbar_arrive_expect_tx(&sm.kv_full[st], kStage + (bi == 0 ? qbytes : 0u));
+                            mbar_arrive_expect_tx(&sm.k_full[ks], kKVTile + (bi == 0 ? qbytes : 0u));
                             if (bi == 0) {
-                                tma_load_4d(&sm.q[qb][0], &mq0, 0, h * a.G, 0, b, &sm.kv_full[st], pol);
-                                tma_load_4d(&sm.q[qb][kQSlab], &mq1, 0, h * a.G, 0, b, &sm.kv_full[st], pol);
-                            }
-                            uint8_t *sk = sm.stage[st];
-                            uint8_t *sv = sk + kKVTile;
-#pragma unroll
-                            for (int p = 0; p < kPagesPerBlock; ++p) {
-                                tma_load_4d(sk + p * 2048, &mk0, 0, 0, h, ids[p], &sm.kv_full[st], pol);
-                                tma_load_4d(sk + kKSlab + p * 2048, &mk1, 0, 0, h, ids[p], &sm.kv_full[st], pol);
-                                tma_load_4d(sv + p * 2048, &mv0, 0, 0, h, ids[p], &sm.kv_full[st], pol);
-                                tma_load_4d(sv + kKSlab + p * 2048, &mv1, 0, 0, h, ids[p], &sm.kv_full[st], pol);
+                                tma_load_4d(&sm.q[qb][0], &mq0, 0, h * a.G, 0, b, &sm.k_full[ks], pol);
+                                tma_load_4d(&sm.q[qb][kQSlab], &mq1, 0, h * a.G, 0, b, &sm.k_full[ks], pol);
                             }
                         }
                     }
                     ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
                     if (!ok) break;
-                    ++issued;
-                    if (++st == kStages) {
-                        st = 0;
-                        ph ^= 1u;
+                    if (lane < kPagesPerBlock) {
+                        uint8_t *sk = sm.kbuf[ks] + lane * 2048;
+                        tma_load_4d(sk, &mk0, 0, 0, h, my_id, &sm.k_full[ks], pol);
+                        tma_load_4d(sk + kKSlab, &mk1, 0, 0, h, my_id, &sm.k_full[ks], pol);
                     }
+                    ++jk;
+                    if (have_prev) {
+                        ok = issue_v();
+                        if (!ok) break;
+                    }
+                    have_prev = true;
+                    prev_id = my_id;
+                    prev_h = h;
                 }
             }
             ++units;
         }
+        if (ok && have_prev) ok = issue_v();
         if (lane == 0) {
-            if (ok && issued >= kStages) ok = mbar_wait(&sm.kv_empty[st], ph ^ 1u, a.err);
+            // end-of-work marker on the K ring
+            const int ks = jk % kNK;
+            if (ok && jk >= kNK) ok = mbar_wait(&sm.k_empty[ks], (uint32_t)(((jk / kNK) & 1) ^ 1), a.err);
             if (ok) {
-                sm.meta[st].flags = kFlagEnd;
-                mbar_arrive(&sm.kv_full[st]);
+                sm.meta[jk % kNMeta].flags = kFlagEnd;
+                mbar_arrive(&sm.k_full[ks]);
             }
-            // wait (bounded) for the copies still in flight; the stage reused
+            // wait (bounded) for the copies still in flight; the K stage reused
             // by the end marker had completed before its empty barrier passed
-            const int first = issued >= kStages ? issued - kStages + 1 : 0;
-            for (int i = first; i < issued && ok; ++i)
-                ok = mbar_wait(&sm.kv_full[i % kStages], (uint32_t)((i / kStages) & 1), a.err);
+            for (int i = jk >= kNK ? jk - kNK + 1 : 0; i < jk && ok; ++i)
+                ok = mbar_wait(&sm.k_full[i % kNK], (uint32_t)((i / kNK) & 1), a.err);
+            for (int i = jv >= kNV ? jv - kNV : 0; i < jv && ok; ++i)
+                ok = mbar_wait(&sm.v_full[i % kNV], (uint32_t)((i / kNV) & 1), a.err);
             __threadfence();
             const int done = atomicAdd(&a.sched[1], 1);
             if (done == (int)gridDim.x - 1) {
@@ -230,15 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idS = umma_idesc_bf16(kRows, kNB, false);
             constexpr uint32_t idPV = umma_idesc_bf16(kRows, kD, true);
             const uint32_t qaddr[2] = {smem_u32(&sm.q[0][0]), smem_u32(&sm.q[1][0])};
-            bool ok = true;
-            int j = 0;          // block index (all units)
-            int st = 0;         // ring stage of block j
-            uint32_t ph = 0;    // ring phase of block j
-            int unit = -1;      // unit index of block j
-            // fetch block j's stage; issue S_j (or forward the end marker)
-            auto issue_s = [&](int jj, int stj, uint32_t phj, int &unit_jj, BlockMeta &m) -> bool {
-                if (!mbar_wait(&sm.kv_full[stj], phj, a.err)) return false;
-                m = sm.meta[stj];
+            // S_jj = Q K_jj^T once K_jj has landed (or forward the end marker)
+            auto issue_s = [&](int jj, int &unit_jj, BlockMeta &m) -> bool {
+                const int ks = jj % kNK;
+                if (!mbar_wait(&sm.k_full[ks], (uint32_t)((jj / kNK) & 1), a.err)) return false;
+                m = sm.meta[jj % kNMeta];
                 if (jj >= 2 && !mbar_wait(&sm.s_empty[jj & 1], par_of(jj) ^ 1u, a.err)) return false;
                 if (m.flags & kFlagEnd) {
                     mbar_arrive(&sm.s_full[jj & 1]);
@@ -247,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (m.flags & kFlagFirst) ++unit_jj;
                 tc_fence_after();
                 const uint32_t qa = qaddr[m.qb];
-                const uint32_t ka = smem_u32(sm.stage[stj]);
+                const uint32_t ka = smem_u32(sm.kbuf[ks]);
                 const uint32_t dS = tmem + kTmemS + (uint32_t)(jj & 1) * kNB;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
@@ -255,30 +278,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bd = umma_desc_sw128(ka + (kk >> 2) * kKSlab + (kk & 3) * 32, 16, 1024);
                     umma_bf16(dS, ad, bd, idS, kk > 0 ? 1u : 0u);
                 }
+                umma_commit(&sm.k_empty[ks]);
                 umma_commit(&sm.s_full[jj & 1]);
                 if (m.flags & kFlagLast) umma_commit(&sm.q_empty[m.qb]);
                 return true;
             };
             BlockMeta cur, nxt;
-            int unit_next = unit;
-            ok = issue_s(0, st, ph, unit_next, cur);
-            unit = unit_next;
+            int j = 0, unit = -1;
+            bool ok = issue_s(0, unit, cur);
             while (ok && !(cur.flags & kFlagEnd)) {
-                // look ahead: S of block j+1 while the softmax works on block j
-                const int st1 = st + 1 == kStages ? 0 : st + 1;
-                const uint32_t ph1 = st + 1 == kStages ? ph ^ 1u : ph;
                 int unit1 = unit;
-                ok = issue_s(j + 1, st1, ph1, unit1, nxt);
-                if (!ok) break;
-                // O += P_j V_j once the softmax has written P_j
+                // S of block j+1 early when its K is already there; PV_j never
+                // waits for the next block's data
+                bool next_done = false;
+                if (mbar_test(&sm.k_full[(j + 1) % kNK], (uint32_t)(((j + 1) / kNK) & 1))) {
+                    ok = issue_s(j + 1, unit1, nxt);
+                    next_done = true;
+                    if (!ok) break;
+                }
+                // O += P_j V_j once the softmax has written P_j and V_j has landed
                 if (!mbar_wait(&sm.p_full[j & 1], par_of(j), a.err)) break;
                 const int ob = unit & 1;
                 if ((cur.flags & kFlagFirst) && unit >= 2 &&
                     !mbar_wait(&sm.o_empty[ob], par_of(unit) ^ 1u, a.err))
                     break;
+                const int vs = j % kNV;
+                if (!mbar_wait(&sm.v_full[vs], (uint32_t)((j / kNV) & 1), a.err)) break;
                 tc_fence_after();
                 const uint32_t pa = smem_u32(&sm.p[j & 1][0]);
-                const uint32_t va = smem_u32(sm.stage[st]) + kKVTile;
+                const uint32_t va = smem_u32(sm.vbuf[vs]);
                 const uint32_t dO = tmem + kTmemO + (uint32_t)ob * kD;
 #pragma unroll
                 for (int kt = 0; kt < kNB / 16; ++kt) {
@@ -286,12 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bd = umma_desc_sw128(va + kt * 2048, kKSlab, 1024);
                     umma_bf16(dO, ad, bd, idPV, ((cur.flags & kFlagFirst) && kt == 0) ? 0u : 1u);
                 }
-                umma_commit(&sm.kv_empty[st]);
+                umma_commit(&sm.v_empty[vs]);
                 umma_commit(&sm.p_empty[j & 1]);
                 if (cur.flags & kFlagLast) umma_commit(&sm.o_full[ob]);
+                if (!next_done) {
+                    ok = issue_s(j + 1, unit1, nxt);
+                    if (!ok) break;
+                }
                 ++j;
-                st = st1;
-                ph = ph1;
                 unit = unit1;
                 cur = nxt;
             }
@@ -310,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int j = 0, unit = -1;
         while (true) {
             if (!mbar_wait(&sm.s_full[j & 1], par_of(j), a.err)) break;
-            const BlockMeta md = sm.meta[j % kStages];
+            const BlockMeta md = sm.meta[j % kNMeta];
             if (md.flags & kFlagEnd) break;
             if (md.flags & kFlagFirst) {
                 ++unit;
@@ -336,8 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&sm.s_empty[j & 1]);
 
             const int L = md.L, T = L + a.n_q;
-            float mx = -CUDART_INF_F;
             const bool need_mask = md.pos0 + kNB > L || md.ntok < kNB;
+            float pm[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) pm[x] = -CUDART_INF_F;
 #pragma unroll
             for (int t = 0; t < kNB; ++t) {
                 float v = s[t] * a.scale_log2;
@@ -348,8 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!vis) v = -CUDART_INF_F;
                 }
                 s[t] = v;
-                mx = fmaxf(mx, v);
+                pm[t & 7] = fmaxf(pm[t & 7], v);
             }
+            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
             float alpha = 1.f;
             bool rescale = false;
             if (mx > m_ref + kRescaleLog2 || (m_ref == -CUDART_INF_F && mx != -CUDART_INF_F)) {
@@ -362,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // P_j goes to the buffer PV_{j-2} read
             if (j >= 2) mbar_wait(&sm.p_empty[j & 1], par_of(j) ^ 1u, a.err);
             uint8_t *prow = &sm.p[j & 1][0] + r * 128;
-            float lsum = 0.f;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c8 = 0; c8 < kNB / 8; ++c8) {
                 uint32_t w[4];
@@ -370,17 +404,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 4; ++e) {
                     const float p0 = live ? exp2f(s[c8 * 8 + 2 * e] - msafe) : 0.f;
                     const float p1 = live ? exp2f(s[c8 * 8 + 2 * e + 1] - msafe) : 0.f;
-                    lsum += p0 + p1;
+                    ls[e] += p0 + p1;
                     w[e] = pack_bf16x2(p0, p1);
                 }
                 *reinterpret_cast<uint4 *>(prow + ((c8 ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            l_run += lsum;
-            // V rows past the sequence's last token may hold anything
+            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            // V rows past the sequence's last token may hold anything: zero
+            // them once V_j has landed (PV_j is not issued before p_full)
             if (md.pos0 + md.ntok > T) {
+                mbar_wait(&sm.v_full[j % kNV], (uint32_t)((j / kNV) & 1), a.err);
                 const int t0 = T - md.pos0;
                 const int nz = (md.ntok - t0) * 2 * 8;
-                uint8_t *sv = sm.stage[j % kStages] + kKVTile;
+                uint8_t *sv = sm.vbuf[j % kNV];
                 for (int z = threadIdx.x - 64; z < nz; z += kSoftmaxThreads) {
                     const int row = t0 + z / 16, rem = z % 16;
                     *reinterpret_cast<uint4 *>(sv + (rem >> 3) * kKSlab + row * 128 + ((rem & 7) << 4)) =

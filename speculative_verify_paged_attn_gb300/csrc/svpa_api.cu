@@ -52,6 +52,8 @@ int sm_count() {
 
 struct AttnPlan {
     int M, split_pages, max_splits;
+    bool use_tc;
+    int grid_slots;      // resident CTAs of the chosen kernel
     size_t off_ml, off_acc, bytes;
 };
 
@@ -72,10 +74,19 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     pl->M = (int)M;
     const int D = p->head_dim;
     const int eb = p->kv_dtype == SVPA_KV_FP8_E4M3 ? 1 : 2;
+    // kernel variant and its resident grid (the persistent CTAs)
+    pl->use_tc = p->variant == 2 || (p->variant == 0 && D == 128 && eb == 2 && M > 16);
+    pl->grid_slots = sm_count();
+    if (!pl->use_tc) {
+        AttnLaunch lp;
+        pl->grid_slots *= attn_plan_launch(D, eb == 1, (int)M, &lp) == cudaSuccess ? lp.ctas_per_sm : 4;
+    }
     int sp = p->split_pages;
     if (sp == 0) {
+        // about 16 units of work per resident CTA (sequences taken at their
+        // maximum length), so that the last units leave a short tail
         const double units = (double)std::max(1, p->batch) * p->num_kv_heads;
-        const double per = units * p->max_blocks_per_seq / (16.0 * sm_count());
+        const double per = units * p->max_blocks_per_seq / (16.0 * pl->grid_slots);
         int pw = 16;
         while (pw * 2 <= per && pw < 1024) pw *= 2;
         // keep the split partials under ~5% of the split's K/V bytes
@@ -234,16 +245,14 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
     for (int j = 0; j < p->n_q; ++j)
         a.anc[j] = ancestor_mask ? ancestor_mask[j] : ((j == 63) ? ~0ull : ((1ull << (j + 1)) - 1ull));
     a.total_units = p->batch * p->num_kv_heads * pl.max_splits;
-    const bool use_tc = p->variant == 2 || (p->variant == 0 && D == 128 && !fp8 && pl.M > 16);
-    if (use_tc) {
-        const int grid = std::max(1, std::min(sm_count(), a.total_units));
+    if (pl.use_tc) {
+        const int grid = std::max(1, std::min(pl.grid_slots, a.total_units));
         return from_cuda(launch_paged_verify_attn_tc(maps, a, grid, static_cast<cudaStream_t>(stream)));
     }
     AttnLaunch lp;
     if (attn_plan_launch(D, fp8, pl.M, &lp) != cudaSuccess) return SVPA_ERR_CUDA;
     a.n_stages = lp.n_stages;
-    const long long slots = (long long)lp.ctas_per_sm * sm_count();
-    const int grid = (int)std::max(1LL, std::min<long long>(slots, a.total_units));
+    const int grid = std::max(1, std::min(lp.ctas_per_sm * sm_count(), a.total_units));
     return from_cuda(launch_paged_verify_attn(maps, a, D, fp8, grid, lp.smem, static_cast<cudaStream_t>(stream)));
 }
 

@@ -69,6 +69,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe: true when phase `parity` of `bar` has completed.
+// (try_wait may suspend the thread for a while; test_wait never does.)
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for phase `parity` of `bar`.  Returns false (and raises
 // SVPA_DEVERR_TIMEOUT) when the limit is reached.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err) {

@@ -35,13 +35,14 @@ def mask_list(inp):
     return None if inp.ancestor_mask is None else [int(x) for x in inp.ancestor_mask.cpu().tolist()]
 
 
-def run_attention(inp: W.AttnInputs, split_pages=0, with_lse=True):
+def run_attention(inp: W.AttnInputs, split_pages=0, with_lse=True, variant=0):
     """Returns (out fp32 numpy [B, n_q, Hq, D], lse numpy or None, device error status)."""
     wl = inp.wl
     d = to_dev(inp)
     B, n_q, Hq, D = d.q.shape
     p = svpa.attn_params(B, n_q, Hq, wl.num_kv_heads, D, d.block_table.shape[1], d.num_blocks,
-                         kv_fp8=wl.kv_fp8, sm_scale=wl.sm_scale, split_pages=split_pages)
+                         kv_fp8=wl.kv_fp8, sm_scale=wl.sm_scale, split_pages=split_pages,
+                         variant=variant)
     ws = torch.zeros(svpa.attn_workspace_size(p), dtype=torch.uint8, device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     out = torch.full((B, n_q, Hq, D), float("nan"), dtype=torch.bfloat16, device=DEV)
@@ -52,8 +53,10 @@ def run_attention(inp: W.AttnInputs, split_pages=0, with_lse=True):
                            error_flag=err, k_scale=d.k_scale, v_scale=d.v_scale,
                            ancestor_mask=mask_list(inp), lse=lse)
     st = svpa.check_error(err)
-    # the workspace tickets are left at zero for the next call
-    assert int(ws[: B * wl.num_kv_heads * 4].view(torch.int32).abs().sum().item()) == 0
+    # the scheduler counters and tickets are left at zero for the next call
+    words = ws[: 256 + B * wl.num_kv_heads * 4].view(torch.int32)
+    assert int(words[:2].abs().sum().item()) == 0
+    assert int(words[64:].abs().sum().item()) == 0
     return out.float().cpu().numpy(), (lse.cpu().numpy() if with_lse else None), st
 
 

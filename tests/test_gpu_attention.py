@@ -125,3 +125,25 @@ def test_full_size_sampled(name):
     assert np.max(np.abs(lse[seqs] - ref_lse)) < 5e-3
     del inp
     torch.cuda.empty_cache()
+
+
+# Both kernels on the shapes where the library picks the tcgen05/TMEM one
+# (many rows per kv head) and on a multi-head shape: 1 = warp-level MMA,
+# 2 = tcgen05 with TMEM accumulators.
+VARIANT_CASES = [
+    ("gqa", small("70b", batch=3, ctx_lo=1, ctx_hi=900), 16),
+    ("gqa_nosplit", small("70b", batch=2, ctx_lo=100, ctx_hi=300), 1024),
+    ("tree", small("tree", batch=3, ctx_lo=1, ctx_hi=500, shared_prefix=32), 8),
+    ("mha", small("7b", batch=3, ctx_lo=1, ctx_hi=300, num_q_heads=8, num_kv_heads=8), 8),
+]
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("name,wl,split", VARIANT_CASES, ids=[c[0] for c in VARIANT_CASES])
+def test_kernel_variants(name, wl, split, variant):
+    inp = W.make_attention(wl, 200 + len(name))
+    got, lse, st = U.run_attention(inp, split_pages=split, variant=variant)
+    assert st == 0
+    ref, ref_lse = U.run_oracle_attention(inp)
+    U.assert_attention_close(got, ref, what=f"{name} variant {variant}")
+    assert np.max(np.abs(lse - ref_lse)) < 2e-3
