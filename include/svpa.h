@@ -271,6 +271,36 @@ svpa_status svpa_block_table_commit(int32_t batch, int32_t n_q,
                                     int32_t head_dim, int32_t kv_dtype,
                                     int32_t *error_flag, void *stream);
 
+/*
+ * svpa_paged_verify_attn without a caller workspace, for callers that may not
+ * allocate device memory: code running inside a host framework that owns all
+ * device allocations and forbids cudaMalloc/cudaFree on its hot path (an
+ * allocation there can synchronise the device and fragments the framework's
+ * pool), or plugin code that is handed only its input and output buffers.
+ * The pages this library follows have no counterpart of this entry point.
+ *
+ * Same arguments and result as svpa_paged_verify_attn minus the workspace.
+ * Its scratch is a fixed 32 MiB array inside the library, present on every
+ * GPU that loads it until the process exits; a shape whose workspace
+ * (svpa_attn_workspace_size) exceeds 32 MiB is rejected with
+ * SVPA_ERR_WORKSPACE before anything is enqueued.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library call.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array and starts by clearing its
+ *    counter words on `stream`; calls that overlap on the GPU (other streams,
+ *    or other threads) race on it and must be serialised by the caller.
+ */
+svpa_status svpa_paged_verify_attn_noalloc(const svpa_attn_params *p, const void *q,
+                                           const void *k_pool, const void *v_pool,
+                                           const float *k_scale, const float *v_scale,
+                                           const int32_t *block_table,
+                                           const int32_t *context_lens,
+                                           const uint64_t *ancestor_mask, void *out,
+                                           float *lse, int32_t *error_flag,
+                                           void *stream);
+
 /* Synchronise `stream`, read the device error word and map it to a status
  * (SVPA_OK when it is zero).  Does not clear the word. */
 svpa_status svpa_check_error(const int32_t *error_flag, void *stream);

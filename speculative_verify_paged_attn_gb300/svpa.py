@@ -27,7 +27,7 @@ STATUS = {0: "SVPA_OK", 1: "SVPA_ERR_INVALID_ARG", 2: "SVPA_ERR_UNSUPPORTED", 3:
           7: "SVPA_ERR_TIMEOUT"}
 EXPORTS = ("svpa_attn_workspace_size", "svpa_paged_verify_attn", "svpa_spec_accept_workspace_size",
            "svpa_spec_accept", "svpa_spec_accept_tree", "svpa_block_table_commit", "svpa_check_error",
-           "svpa_status_string", "svpa_version")
+           "svpa_status_string", "svpa_version", "svpa_paged_verify_attn_noalloc")
 
 
 class SvpaError(RuntimeError):
@@ -64,6 +64,7 @@ def load(path: str = LIB_PATH):
     L.svpa_spec_accept.argtypes = [I, I, I] + [P] * 9 + [U, P, P]
     L.svpa_spec_accept_tree.argtypes = [I, I, I] + [P] * 11 + [U, P, P]
     L.svpa_block_table_commit.argtypes = [I] * 5 + [P] * 7 + [I, P, P, I, I, I, P, P]
+    L.svpa_paged_verify_attn_noalloc.argtypes = [ctypes.POINTER(AttnParams)] + [P] * 12
     L.svpa_check_error.argtypes = [P, P]
     L.svpa_status_string.argtypes = [I]
     L.svpa_status_string.restype = ctypes.c_char_p
@@ -134,6 +135,21 @@ def paged_verify_attn(params: AttnParams, q, k_pool, v_pool, block_table, contex
         _p(error_flag), _stream(stream))
     if check:
         _check(st, "svpa_paged_verify_attn")
+    return st
+
+
+def paged_verify_attn_noalloc(params: AttnParams, q, k_pool, v_pool, block_table, context_lens, out,
+                              *, error_flag, k_scale=None, v_scale=None, ancestor_mask=None,
+                              lse=None, stream=None, check=True) -> int:
+    """svpa_paged_verify_attn_noalloc: no workspace argument; the library's own
+    fixed scratch array is used (for callers that may not allocate)."""
+    m = _mask_array(ancestor_mask)
+    st = load().svpa_paged_verify_attn_noalloc(
+        ctypes.byref(params), _p(q), _p(k_pool), _p(v_pool), _p(k_scale), _p(v_scale),
+        _p(block_table), _p(context_lens), None if m is None else ctypes.cast(m, ctypes.c_void_p),
+        _p(out), _p(lse), _p(error_flag), _stream(stream))
+    if check:
+        _check(st, "svpa_paged_verify_attn_noalloc")
     return st
 
 
