@@ -37,23 +37,24 @@ namespace svpa {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kPagesPerBlock = 4;
-constexpr int kNB = kPagesPerBlock * 16;       // tokens per block
+constexpr int kPagesPerBlock = 8;
+constexpr int kNB = kPagesPerBlock * 16;       // tokens per block (128)
 constexpr int kRows = 128;                      // MMA M
 constexpr int kKSlab = kNB * 128;               // one 128-byte column slab of a K (or V) block
 constexpr int kKVTile = 2 * kKSlab;             // K (or V) block, 128 columns
 constexpr int kQSlab = kRows * 128;
 constexpr int kQBuf = 2 * kQSlab;
-constexpr int kPBuf = kRows * 128;              // 128 rows x 64 bf16
-constexpr int kNK = 4;                          // K ring (freed once S_j is computed)
-constexpr int kNV = 4;                          // V ring (freed once PV_j is computed)
+constexpr int kNK = 3;                          // K ring (freed once S_j is computed)
+constexpr int kNV = 2;                          // V ring (freed once PV_j is computed)
 constexpr int kNMeta = 8;                       // block descriptors in flight
 constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kBarSoftmax = 1;
 constexpr float kRescaleLog2 = 8.f;             // rescale O when a maximum grows by > 2^8
 
-// TMEM columns: O[0] 0..127, O[1] 128..255, S[0] 256..319, S[1] 320..383
+// TMEM columns: O[0] 0..127, O[1] 128..255, S[0] 256..383, S[1] 384..511; the
+// softmax overwrites the first 64 columns of S[x] with P (bf16 pairs), which
+// the PV MMA reads as its A operand straight from TMEM.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0, kTmemS = 256;
 
@@ -66,14 +67,13 @@ struct BlockMeta {
 
 struct Smem {
     uint8_t q[2][kQBuf];                 // 2 x 32 KB, 1024-aligned
-    uint8_t kbuf[kNK][kKVTile];          // 4 x 16 KB
-    uint8_t vbuf[kNV][kKVTile];          // 4 x 16 KB
-    uint8_t p[2][kPBuf];                 // 2 x 16 KB
+    uint8_t kbuf[kNK][kKVTile];          // 3 x 32 KB
+    uint8_t vbuf[kNV][kKVTile];          // 2 x 32 KB
     uint64_t k_full[kNK], k_empty[kNK];
     uint64_t v_full[kNV], v_empty[kNV];
     uint64_t q_empty[2];
-    uint64_t s_full[2], s_empty[2];
-    uint64_t p_full[2], p_empty[2];
+    uint64_t s_full[2];
+    uint64_t p_full, p_empty;
     uint64_t o_full[2], o_empty[2];
     BlockMeta meta[kNMeta];
     uint32_t tmem_base;
@@ -103,12 +103,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.q_empty[i], 1);
             mbar_init(&sm.s_full[i], 1);
-            mbar_init(&sm.s_empty[i], 4);
-            mbar_init(&sm.p_full[i], 4);
-            mbar_init(&sm.p_empty[i], 1);
             mbar_init(&sm.o_full[i], 1);
             mbar_init(&sm.o_empty[i], 4);
         }
+        mbar_init(&sm.p_full, 4);
+        mbar_init(&sm.p_empty, 1);
         fence_mbar_init();
     }
     // query rows past M are never written by the copies: keep them zero
@@ -138,9 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int jk = 0, jv = 0, units = 0;      // K blocks issued, V blocks issued, units started (warp-uniform)
         bool ok = true;
         bool have_prev = false;             // a block whose V still has to be issued
-        int prev_id = 0, prev_h = 0;        // lanes 0..3: page `lane` of that block
+        int prev_id = 0, prev_h = 0;        // lanes 0..7: page `lane` of that block
         const uint32_t qbytes = (uint32_t)(a.M * 128 * 2);
-        // V of block jv, one block behind K so that K can run ahead; lanes 0..3
+        // V of block jv, one block behind K so that K can run ahead; lanes 0..7
         // issue one page each
         auto issue_v = [&]() -> bool {
             const int vs = jv % kNV;
@@ -189,9 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int cnt = min(32, n - i0);
                 for (int j0 = 0; j0 < cnt; j0 += kPagesPerBlock) {
-                    // lanes 0..3 hold the ids of the block's 4 pages
-                    int my_id = __shfl_sync(0xffffffffu, blk, (j0 + (lane & 3)) & 31);
-                    if (j0 + (lane & 3) >= cnt) my_id = a.num_blocks;
+                    // lanes 0..7 hold the ids of the block's 8 pages
+                    int my_id = __shfl_sync(0xffffffffu, blk, (j0 + (lane & 7)) & 31);
+                    if (j0 + (lane & 7) >= cnt) my_id = a.num_blocks;
                     const int bi = (i0 + j0) / kPagesPerBlock;  // block index in the unit
                     const int ks = jk % kNK;
                     if (lane == 0) {
@@ -258,11 +257,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idPV = umma_idesc_bf16(kRows, kD, true);
             const uint32_t qaddr[2] = {smem_u32(&sm.q[0][0]), smem_u32(&sm.q[1][0])};
             // S_jj = Q K_jj^T once K_jj has landed (or forward the end marker)
-            auto issue_s = [&](int jj, int &unit_jj, BlockMeta &m) -> bool {
+            // buf_wait: wait for PV_{jj-2} (whose P shares S_jj's TMEM buffer);
+            // callers pass false when they already know it has completed
+            auto issue_s = [&](int jj, int &unit_jj, BlockMeta &m, bool buf_wait) -> bool {
                 const int ks = jj % kNK;
                 if (!mbar_wait(&sm.k_full[ks], (uint32_t)((jj / kNK) & 1), a.err)) return false;
                 m = sm.meta[jj % kNMeta];
-                if (jj >= 2 && !mbar_wait(&sm.s_empty[jj & 1], par_of(jj) ^ 1u, a.err)) return false;
+                // S buffer jj&1 holds P_{jj-2} until PV_{jj-2} has read it.  Only
+                // waited while PV_{jj-1} cannot have completed yet, so the
+                // barrier is never two phases ahead of the one tested.
+                if (buf_wait && jj >= 2 && !mbar_wait(&sm.p_empty, (uint32_t)((jj - 2) & 1), a.err))
+                    return false;
                 if (m.flags & kFlagEnd) {
                     mbar_arrive(&sm.s_full[jj & 1]);
                     return true;
@@ -285,40 +290,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             BlockMeta cur, nxt;
             int j = 0, unit = -1;
-            bool ok = issue_s(0, unit, cur);
+            bool ok = issue_s(0, unit, cur, true);
             while (ok && !(cur.flags & kFlagEnd)) {
                 int unit1 = unit;
                 // S of block j+1 early when its K is already there; PV_j never
                 // waits for the next block's data
                 bool next_done = false;
                 if (mbar_test(&sm.k_full[(j + 1) % kNK], (uint32_t)(((j + 1) / kNK) & 1))) {
-                    ok = issue_s(j + 1, unit1, nxt);
+                    ok = issue_s(j + 1, unit1, nxt, true);  // PV_j not issued yet
                     next_done = true;
                     if (!ok) break;
                 }
                 // O += P_j V_j once the softmax has written P_j and V_j has landed
-                if (!mbar_wait(&sm.p_full[j & 1], par_of(j), a.err)) break;
+                if (!mbar_wait(&sm.p_full, (uint32_t)(j & 1), a.err)) break;
                 const int ob = unit & 1;
                 if ((cur.flags & kFlagFirst) && unit >= 2 &&
                     !mbar_wait(&sm.o_empty[ob], par_of(unit) ^ 1u, a.err))
                     break;
                 const int vs = j % kNV;
                 if (!mbar_wait(&sm.v_full[vs], (uint32_t)((j / kNV) & 1), a.err)) break;
+                // S_{j+1} will be issued after PV_j: settle its buffer now
+                if (!next_done && j >= 1 && !mbar_wait(&sm.p_empty, (uint32_t)((j - 1) & 1), a.err)) break;
                 tc_fence_after();
-                const uint32_t pa = smem_u32(&sm.p[j & 1][0]);
+                const uint32_t pt = tmem + kTmemS + (uint32_t)(j & 1) * kNB;  // P_j (bf16 pairs)
                 const uint32_t va = smem_u32(sm.vbuf[vs]);
                 const uint32_t dO = tmem + kTmemO + (uint32_t)ob * kD;
 #pragma unroll
                 for (int kt = 0; kt < kNB / 16; ++kt) {
-                    const uint64_t ad = umma_desc_sw128(pa + kt * 32, 16, 1024);
                     const uint64_t bd = umma_desc_sw128(va + kt * 2048, kKSlab, 1024);
-                    umma_bf16(dO, ad, bd, idPV, ((cur.flags & kFlagFirst) && kt == 0) ? 0u : 1u);
+                    umma_bf16_tmem_a(dO, pt + kt * 8, bd, idPV, ((cur.flags & kFlagFirst) && kt == 0) ? 0u : 1u);
                 }
                 umma_commit(&sm.v_empty[vs]);
-                umma_commit(&sm.p_empty[j & 1]);
+                umma_commit(&sm.p_empty);
                 if (cur.flags & kFlagLast) umma_commit(&sm.o_full[ob]);
                 if (!next_done) {
-                    ok = issue_s(j + 1, unit1, nxt);
+                    ok = issue_s(j + 1, unit1, nxt, false);
                     if (!ok) break;
                 }
                 ++j;
@@ -350,64 +356,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             float s[kNB];
             {
-                uint32_t raw[32];
                 const uint32_t sa = tmem + kTmemS + (uint32_t)(j & 1) * kNB + lane_off;
-                tmem_ld32(sa, raw);
-                tmem_ld_wait();
 #pragma unroll
-                for (int t = 0; t < 32; ++t) s[t] = __uint_as_float(raw[t]);
-                tmem_ld32(sa + 32, raw);
-                tmem_ld_wait();
+                for (int c = 0; c < kNB / 32; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(sa + c * 32, raw);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int t = 0; t < 32; ++t) s[32 + t] = __uint_as_float(raw[t]);
+                    for (int t = 0; t < 32; ++t) s[c * 32 + t] = __uint_as_float(raw[t]);
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.s_empty[j & 1]);
 
             const int L = md.L, T = L + a.n_q;
-            const bool need_mask = md.pos0 + kNB > L || md.ntok < kNB;
+            // The hot path below is kept short on purpose (this code runs
+            // once per 64-token block for every query row): max of the raw
+            // scores, the scale folded into the exponent's FMA, and masking
+            // only on the blocks that reach the speculative slots or a
+            // partial block.
+            if (md.pos0 + kNB > L || md.ntok < kNB) {
+                // visibility of the block's tokens, 64 per bit mask word
+                const int h0 = L - md.pos0;  // tokens of the block that are history
+#pragma unroll
+                for (int w = 0; w < kNB / 64; ++w) {
+                    const int hw = min(max(h0 - 64 * w, 0), 64);
+                    unsigned long long vis = hw == 64 ? ~0ull : ((1ull << hw) - 1ull);
+                    const int sh = h0 - 64 * w;  // bit of speculative slot 0 in this word
+                    if (sh >= 0) {
+                        if (sh < 64) vis |= anc << sh;
+                    } else if (-sh < 64) {
+                        vis |= anc >> (-sh);
+                    }
+                    const int nw = min(max(md.ntok - 64 * w, 0), 64);
+                    if (nw < 64) vis &= (1ull << nw) - 1ull;
+#pragma unroll
+                    for (int t = 0; t < 64; ++t)
+                        if (!((vis >> t) & 1ull)) s[64 * w + t] = -CUDART_INF_F;
+                }
+            }
             float pm[8];
 #pragma unroll
-            for (int x = 0; x < 8; ++x) pm[x] = -CUDART_INF_F;
+            for (int x = 0; x < 8; ++x) pm[x] = s[x];
 #pragma unroll
-            for (int t = 0; t < kNB; ++t) {
-                float v = s[t] * a.scale_log2;
-                if (need_mask) {
-                    const int p = md.pos0 + t;
-                    const int si = p - L;
-                    const bool vis = t < md.ntok && (si < 0 || (si < a.n_q && ((anc >> si) & 1ull)));
-                    if (!vis) v = -CUDART_INF_F;
-                }
-                s[t] = v;
-                pm[t & 7] = fmaxf(pm[t & 7], v);
-            }
-            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+            for (int t = 8; t < kNB; ++t) pm[t & 7] = fmaxf(pm[t & 7], s[t]);
+            const float mraw = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                     fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+            const float mx = mraw == -CUDART_INF_F ? -CUDART_INF_F : mraw * a.scale_log2;
             float alpha = 1.f;
             bool rescale = false;
             if (mx > m_ref + kRescaleLog2 || (m_ref == -CUDART_INF_F && mx != -CUDART_INF_F)) {
-                alpha = exp2f(m_ref - mx);  // 0 when m_ref is -inf
+                alpha = ex2_approx(m_ref - mx);  // 0 when m_ref is -inf
                 m_ref = mx;
                 rescale = !(md.flags & kFlagFirst) && l_run > 0.f;
                 l_run *= alpha;
             }
-            const float msafe = m_ref == -CUDART_INF_F ? 0.f : m_ref;
-            // P_j goes to the buffer PV_{j-2} read
-            if (j >= 2) mbar_wait(&sm.p_empty[j & 1], par_of(j) ^ 1u, a.err);
-            uint8_t *prow = &sm.p[j & 1][0] + r * 128;
+            const float neg_m = m_ref == -CUDART_INF_F ? 0.f : -m_ref;
+            const float sc = a.scale_log2;
+            // P_j as bf16 pairs into the first half of S_j's TMEM columns
+            const uint32_t pt = tmem + kTmemS + (uint32_t)(j & 1) * kNB + lane_off;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c8 = 0; c8 < kNB / 8; ++c8) {
-                uint32_t w[4];
+            for (int c = 0; c < kNB / 64; ++c) {
+                uint32_t w[32];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = live ? exp2f(s[c8 * 8 + 2 * e] - msafe) : 0.f;
-                    const float p1 = live ? exp2f(s[c8 * 8 + 2 * e + 1] - msafe) : 0.f;
-                    ls[e] += p0 + p1;
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = live ? ex2_approx(fmaf(s[c * 64 + 2 * e], sc, neg_m)) : 0.f;
+                    const float p1 = live ? ex2_approx(fmaf(s[c * 64 + 2 * e + 1], sc, neg_m)) : 0.f;
+                    ls[e & 3] += p0 + p1;
                     w[e] = pack_bf16x2(p0, p1);
                 }
-                *reinterpret_cast<uint4 *>(prow + ((c8 ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                tmem_st32(pt + c * 32, w);
             }
             l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             // V rows past the sequence's last token may hold anything: zero
@@ -428,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (__any_sync(0xffffffffu, rescale)) {
                 const float f = rescale ? alpha : 1.f;
                 // O (TMEM) holds P_{<j} V; PV_{j-1} must have landed first
-                mbar_wait(&sm.p_empty[(j - 1) & 1], par_of(j - 1), a.err);
+                mbar_wait(&sm.p_empty, (uint32_t)((j - 1) & 1), a.err);
                 tc_fence_after();
                 const uint32_t oa = tmem + kTmemO + (uint32_t)(unit & 1) * kD + lane_off;
 #pragma unroll
@@ -442,10 +459,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st_wait();
             }
+            tmem_st_wait();
+            // P_j is published only once PV_{j-1} has completed (PV_j cannot
+            // have started), which keeps the MMA issuer's p_full and p_empty
+            // waits unambiguous
+            if (j >= 1) mbar_wait(&sm.p_empty, (uint32_t)((j - 1) & 1), a.err);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.p_full[j & 1]);
+            if (lane == 0) mbar_arrive(&sm.p_full);
 
             if (md.flags & kFlagLast) {
                 // ---- unit epilogue: O row from TMEM
@@ -453,46 +475,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(&sm.o_full[ob], par_of(unit), a.err);
                 tc_fence_after();
                 const uint32_t oa = tmem + kTmemO + (uint32_t)ob * kD + lane_off;
-                float o[kD];
-#pragma unroll
+                const int b = md.b, h = md.h;
+                const int u2 = b * a.Hkv + h;
+                const int gi = r - jq * G;
+                const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
+                const size_t pr_own = ((size_t)u2 * a.max_splits + md.split) * a.M + r;
+                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                // O row streamed out of TMEM 32 columns at a time: final
+                // output when the unit is the whole sequence, else a partial
+#pragma unroll 1
                 for (int c = 0; c < kD / 32; ++c) {
                     uint32_t raw[32];
                     tmem_ld32(oa + c * 32, raw);
                     tmem_ld_wait();
+                    if (live) {
+                        if (md.nsplit == 1) {
+                            uint4 *orow = reinterpret_cast<uint4 *>(a.out + od * kD + c * 32);
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) o[c * 32 + t] = __uint_as_float(raw[t]);
+                            for (int c8 = 0; c8 < 4; ++c8) {
+                                uint4 v;
+                                v.x = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 0]) * inv, __uint_as_float(raw[c8 * 8 + 1]) * inv);
+                                v.y = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 2]) * inv, __uint_as_float(raw[c8 * 8 + 3]) * inv);
+                                v.z = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 4]) * inv, __uint_as_float(raw[c8 * 8 + 5]) * inv);
+                                v.w = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 6]) * inv, __uint_as_float(raw[c8 * 8 + 7]) * inv);
+                                orow[c8] = v;
+                            }
+                        } else {
+                            uint4 *prow4 = reinterpret_cast<uint4 *>(a.part_acc + pr_own * kD + c * 32);
+#pragma unroll
+                            for (int c4 = 0; c4 < 8; ++c4)
+                                prow4[c4] = make_uint4(raw[c4 * 4], raw[c4 * 4 + 1], raw[c4 * 4 + 2], raw[c4 * 4 + 3]);
+                        }
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.o_empty[ob]);
-                const int b = md.b, h = md.h;
                 if (md.nsplit == 1) {
-                    if (live) {
-                        const int gi = r - jq * G;
-                        const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
-                        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-                        uint4 *orow = reinterpret_cast<uint4 *>(a.out + od * kD);
-#pragma unroll
-                        for (int c8 = 0; c8 < kD / 8; ++c8) {
-                            uint4 v;
-                            v.x = pack_bf16x2(o[c8 * 8 + 0] * inv, o[c8 * 8 + 1] * inv);
-                            v.y = pack_bf16x2(o[c8 * 8 + 2] * inv, o[c8 * 8 + 3] * inv);
-                            v.z = pack_bf16x2(o[c8 * 8 + 4] * inv, o[c8 * 8 + 5] * inv);
-                            v.w = pack_bf16x2(o[c8 * 8 + 6] * inv, o[c8 * 8 + 7] * inv);
-                            orow[c8] = v;
-                        }
-                        if (a.lse) a.lse[od] = (m_ref + log2f(l_run)) * 0.69314718055994530942f;
-                    }
+                    if (live && a.lse) a.lse[od] = (m_ref + __log2f(l_run)) * 0.69314718055994530942f;
                 } else {
-                    const int u2 = b * a.Hkv + h;
                     if (live) {
-                        const size_t pr = ((size_t)u2 * a.max_splits + md.split) * a.M + r;
-                        float4 *prow4 = reinterpret_cast<float4 *>(a.part_acc + pr * kD);
-#pragma unroll
-                        for (int c4 = 0; c4 < kD / 4; ++c4)
-                            prow4[c4] = make_float4(o[c4 * 4], o[c4 * 4 + 1], o[c4 * 4 + 2], o[c4 * 4 + 3]);
-                        a.part_ml[pr * 2] = m_ref;
-                        a.part_ml[pr * 2 + 1] = l_run;
+                        a.part_ml[pr_own * 2] = m_ref;
+                        a.part_ml[pr_own * 2 + 1] = l_run;
                     }
                     __threadfence();
                     named_barrier_sync(kBarSoftmax, kSoftmaxThreads);
@@ -505,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int last = sm.last;
                     named_barrier_sync(kBarSoftmax, kSoftmaxThreads);
                     if (last && live) {
+                        // merge every split's partial row (log-sum-exp weights)
                         __threadfence();
                         const size_t base = (size_t)u2 * a.max_splits * a.M + r;
                         float mx2 = -CUDART_INF_F;
@@ -512,36 +537,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mx2 = fmaxf(mx2, __ldcg(&a.part_ml[(base + (size_t)s2 * a.M) * 2]));
                         const float ms2 = mx2 == -CUDART_INF_F ? 0.f : mx2;
                         float l2 = 0.f;
-#pragma unroll
-                        for (int d = 0; d < kD; ++d) o[d] = 0.f;
                         for (int s2 = 0; s2 < md.nsplit; ++s2) {
                             const size_t pr = base + (size_t)s2 * a.M;
-                            const float w = exp2f(__ldcg(&a.part_ml[pr * 2]) - ms2);
-                            l2 += w * __ldcg(&a.part_ml[pr * 2 + 1]);
-                            const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + pr * kD);
+                            l2 += ex2_approx(__ldcg(&a.part_ml[pr * 2]) - ms2) * __ldcg(&a.part_ml[pr * 2 + 1]);
+                        }
+                        const float inv2 = l2 > 0.f ? 1.f / l2 : 0.f;
+#pragma unroll 1
+                        for (int c = 0; c < kD / 32; ++c) {
+                            float o[32];
 #pragma unroll
-                            for (int c4 = 0; c4 < kD / 4; ++c4) {
-                                const float4 v = __ldcg(src + c4);
-                                o[c4 * 4] += w * v.x;
-                                o[c4 * 4 + 1] += w * v.y;
-                                o[c4 * 4 + 2] += w * v.z;
-                                o[c4 * 4 + 3] += w * v.w;
+                            for (int d = 0; d < 32; ++d) o[d] = 0.f;
+                            for (int s2 = 0; s2 < md.nsplit; ++s2) {
+                                const size_t pr = base + (size_t)s2 * a.M;
+                                const float w = ex2_approx(__ldcg(&a.part_ml[pr * 2]) - ms2);
+                                const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + pr * kD + c * 32);
+#pragma unroll
+                                for (int c4 = 0; c4 < 8; ++c4) {
+                                    const float4 v = __ldcg(src + c4);
+                                    o[c4 * 4] += w * v.x;
+                                    o[c4 * 4 + 1] += w * v.y;
+                                    o[c4 * 4 + 2] += w * v.z;
+                                    o[c4 * 4 + 3] += w * v.w;
+                                }
+                            }
+                            uint4 *orow = reinterpret_cast<uint4 *>(a.out + od * kD + c * 32);
+#pragma unroll
+                            for (int c8 = 0; c8 < 4; ++c8) {
+                                uint4 v;
+                                v.x = pack_bf16x2(o[c8 * 8 + 0] * inv2, o[c8 * 8 + 1] * inv2);
+                                v.y = pack_bf16x2(o[c8 * 8 + 2] * inv2, o[c8 * 8 + 3] * inv2);
+                                v.z = pack_bf16x2(o[c8 * 8 + 4] * inv2, o[c8 * 8 + 5] * inv2);
+                                v.w = pack_bf16x2(o[c8 * 8 + 6] * inv2, o[c8 * 8 + 7] * inv2);
+                                orow[c8] = v;
                             }
                         }
-                        const int gi = r - jq * G;
-                        const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
-                        const float inv = l2 > 0.f ? 1.f / l2 : 0.f;
-                        uint4 *orow = reinterpret_cast<uint4 *>(a.out + od * kD);
-#pragma unroll
-                        for (int c8 = 0; c8 < kD / 8; ++c8) {
-                            uint4 v;
-                            v.x = pack_bf16x2(o[c8 * 8 + 0] * inv, o[c8 * 8 + 1] * inv);
-                            v.y = pack_bf16x2(o[c8 * 8 + 2] * inv, o[c8 * 8 + 3] * inv);
-                            v.z = pack_bf16x2(o[c8 * 8 + 4] * inv, o[c8 * 8 + 5] * inv);
-                            v.w = pack_bf16x2(o[c8 * 8 + 6] * inv, o[c8 * 8 + 7] * inv);
-                            orow[c8] = v;
-                        }
-                        if (a.lse) a.lse[od] = (mx2 + log2f(l2)) * 0.69314718055994530942f;
+                        if (a.lse) a.lse[od] = (mx2 + __log2f(l2)) * 0.69314718055994530942f;
                     }
                 }
             }
