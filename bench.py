@@ -126,7 +126,7 @@ class ClockSampler:
 class Step:
     """Device buffers and the three library calls of one verification step."""
 
-    def __init__(self, wl: W.Workload, seed: int, dev: torch.device):
+    def __init__(self, wl: W.Workload, seed: int, dev: torch.device, variant: int = 0):
         self.wl, self.dev = wl, dev
         inp = W.make_attention(wl, seed, device=dev, poison=False)
         smp = W.make_sampler(wl, seed, device=dev)
@@ -134,7 +134,8 @@ class Step:
         B, n_q, Hq, D = inp.q.shape
         self.B, self.n_q = B, n_q
         self.params = svpa.attn_params(B, n_q, Hq, wl.num_kv_heads, D, inp.block_table.shape[1],
-                                       inp.num_blocks, kv_fp8=wl.kv_fp8, sm_scale=wl.sm_scale)
+                                       inp.num_blocks, kv_fp8=wl.kv_fp8, sm_scale=wl.sm_scale,
+                                       variant=variant)
         self.ws = torch.zeros(svpa.attn_workspace_size(self.params), dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.out = torch.empty((B, n_q, Hq, D), dtype=torch.bfloat16, device=dev)
@@ -318,6 +319,8 @@ def main():
     ap.add_argument("--config", default="7b", choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="svpa", choices=["svpa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", type=int, default=0, choices=[0, 1, 2],
+                    help="attention kernel: 0 library's choice, 1 warp-level MMA, 2 tcgen05")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiling)")
     args = ap.parse_args()
@@ -337,7 +340,7 @@ def main():
     if args.batch:
         wl = wl.scaled(batch=args.batch)
     seed = W.SEEDS[args.config] + 7 * rank
-    st = Step(wl, seed, dev)
+    st = Step(wl, seed, dev, variant=args.variant)
     stream = torch.cuda.current_stream()
 
     # warm-up

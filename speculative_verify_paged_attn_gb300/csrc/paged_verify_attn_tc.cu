@@ -45,7 +45,7 @@ constexpr int kKVTile = 2 * kKSlab;             // K (or V) block, 128 columns
 constexpr int kQSlab = kRows * 128;
 constexpr int kQBuf = 2 * kQSlab;
 constexpr int kNK = 3;                          // K ring (freed once S_j is computed)
-constexpr int kNV = 2;                          // V ring (freed once PV_j is computed)
+constexpr int kNV = 3;                          // V ring (freed once PV_j is computed)
 constexpr int kNMeta = 8;                       // block descriptors in flight
 constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
@@ -66,12 +66,12 @@ struct BlockMeta {
 };
 
 struct Smem {
-    uint8_t q[2][kQBuf];                 // 2 x 32 KB, 1024-aligned
+    uint8_t q[kQBuf];                    // 32 KB, 1024-aligned (one unit's queries)
     uint8_t kbuf[kNK][kKVTile];          // 3 x 32 KB
-    uint8_t vbuf[kNV][kKVTile];          // 2 x 32 KB
+    uint8_t vbuf[kNV][kKVTile];          // 3 x 32 KB
     uint64_t k_full[kNK], k_empty[kNK];
     uint64_t v_full[kNV], v_empty[kNV];
-    uint64_t q_empty[2];
+    uint64_t q_empty;
     uint64_t s_full[2];
     uint64_t p_full, p_empty;
     uint64_t o_full[2], o_empty[2];
@@ -101,18 +101,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.q_empty[i], 1);
             mbar_init(&sm.s_full[i], 1);
             mbar_init(&sm.o_full[i], 1);
             mbar_init(&sm.o_empty[i], 4);
         }
+        mbar_init(&sm.q_empty, 1);
         mbar_init(&sm.p_full, 4);
         mbar_init(&sm.p_empty, 1);
         fence_mbar_init();
     }
     // query rows past M are never written by the copies: keep them zero
-    for (int x = threadIdx.x; x < 2 * kQBuf / 16; x += blockDim.x)
-        reinterpret_cast<uint4 *>(&sm.q[0][0])[x] = make_uint4(0, 0, 0, 0);
+    for (int x = threadIdx.x; x < kQBuf / 16; x += blockDim.x)
+        reinterpret_cast<uint4 *>(&sm.q[0])[x] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int page0 = split * a.split_pages;
             const int n = min(a.split_pages, npages - page0);
             const int nblk = (n + kPagesPerBlock - 1) / kPagesPerBlock;
-            const int qb = units & 1;
+            const int qb = 0;
             const int32_t *bt = a.block_table + (size_t)b * a.max_blocks + page0;
             for (int i0 = 0; i0 < n && ok; i0 += 32) {
                 int blk = a.num_blocks;  // out of range: zero-filled page
@@ -192,10 +192,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int my_id = __shfl_sync(0xffffffffu, blk, (j0 + (lane & 7)) & 31);
                     if (j0 + (lane & 7) >= cnt) my_id = a.num_blocks;
                     const int bi = (i0 + j0) / kPagesPerBlock;  // block index in the unit
+                    // at a unit boundary the previous unit's last V goes out
+                    // before waiting for the query buffer to free up
+                    if (bi == 0 && have_prev) {
+                        ok = issue_v();
+                        have_prev = false;
+                        if (!ok) break;
+                    }
                     const int ks = jk % kNK;
                     if (lane == 0) {
                         if (jk >= kNK) ok = mbar_wait(&sm.k_empty[ks], (uint32_t)(((jk / kNK) & 1) ^ 1), a.err);
-                        if (ok && bi == 0 && units >= 2) ok = mbar_wait(&sm.q_empty[qb], par_of(units) ^ 1u, a.err);
+                        // the query tile is reloaded once the previous unit's last S is done
+                        if (ok && bi == 0 && units >= 1)
+                            ok = mbar_wait(&sm.q_empty, (uint32_t)((units - 1) & 1), a.err);
                         if (ok) {
                             BlockMeta &m = sm.meta[jk % kNMeta];
                             m.b = b; m.h = h; m.split = split; m.L = L; m.nsplit = nsplit; m.qb = qb;
@@ -204,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             m.flags = (bi == 0 ? kFlagFirst : 0) | (bi == nblk - 1 ? kFlagLast : 0);
                             mbar_arrive_expect_tx(&sm.k_full[ks], kKVTile + (bi == 0 ? qbytes : 0u));
                             if (bi == 0) {
-                                tma_load_4d(&sm.q[qb][0], &mq0, 0, h * a.G, 0, b, &sm.k_full[ks], pol);
-                                tma_load_4d(&sm.q[qb][kQSlab], &mq1, 0, h * a.G, 0, b, &sm.k_full[ks], pol);
+                                tma_load_4d(&sm.q[0], &mq0, 0, h * a.G, 0, b, &sm.k_full[ks], pol);
+                                tma_load_4d(&sm.q[kQSlab], &mq1, 0, h * a.G, 0, b, &sm.k_full[ks], pol);
                             }
                         }
                     }
@@ -255,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idS = umma_idesc_bf16(kRows, kNB, false);
             constexpr uint32_t idPV = umma_idesc_bf16(kRows, kD, true);
-            const uint32_t qaddr[2] = {smem_u32(&sm.q[0][0]), smem_u32(&sm.q[1][0])};
+            const uint32_t qaddr = smem_u32(&sm.q[0]);
             // S_jj = Q K_jj^T once K_jj has landed (or forward the end marker)
             // buf_wait: wait for PV_{jj-2} (whose P shares S_jj's TMEM buffer);
             // callers pass false when they already know it has completed
@@ -274,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (m.flags & kFlagFirst) ++unit_jj;
                 tc_fence_after();
-                const uint32_t qa = qaddr[m.qb];
+                const uint32_t qa = qaddr;
                 const uint32_t ka = smem_u32(sm.kbuf[ks]);
                 const uint32_t dS = tmem + kTmemS + (uint32_t)(jj & 1) * kNB;
 #pragma unroll
@@ -285,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 umma_commit(&sm.k_empty[ks]);
                 umma_commit(&sm.s_full[jj & 1]);
-                if (m.flags & kFlagLast) umma_commit(&sm.q_empty[m.qb]);
+                if (m.flags & kFlagLast) umma_commit(&sm.q_empty);
                 return true;
             };
             BlockMeta cur, nxt;

@@ -9,12 +9,12 @@
 // draft is accepted.  The draw is the first token whose running residual
 // mass exceeds u * (total mass).
 //
-// GB300 layout: one launch; the vocabulary of each row is cut into chunks of
-// kChunk tokens, one CTA per (chunk, row).  Every CTA recomputes the row's
-// acceptance (gamma gathered loads and a warp ballot), sums its chunk of the
-// residual, and the last CTA of the row to finish (atomic ticket, no spin)
-// locates the chunk holding u*S and scans it.  Sums are fp32 within a
-// thread's 16 contiguous tokens and fp64 across threads and chunks.
+// GB300 layout: one 1024-thread CTA per row.  Warp 0 runs the gamma
+// acceptance tests (gathered loads and a warp ballot); then every thread sums
+// its contiguous segment of the residual row in fp32 (vector loads, token
+// order), a block-wide fp64 exclusive scan gives each segment's offset and
+// the total S, and the thread whose segment holds u*S walks it again to
+// find the token.  One pass over the row, no inter-CTA protocol.
 //
 // This file is compiled with -fmad=false; the acceptance product also uses
 // __fmul_rn, which is never contracted.
@@ -27,9 +27,7 @@ namespace svpa {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kPerThread = 16;
-constexpr int kChunk = kThreads * kPerThread;  // 4096 tokens per CTA
+constexpr int kRowThreads = 1024;
 constexpr double kNearBand = 1e-6;
 
 // Block-wide exclusive scan of one double per thread; returns this thread's
@@ -71,77 +69,52 @@ __device__ __forceinline__ float weight(const float *p, const float *q, int t) {
     return d > 0.f ? d : 0.f;
 }
 
-// Thread-segment sum over [lo, hi) of a row: thread i owns tokens
-// lo + i*16 .. lo + i*16 + 15 (fp32, in order).
-__device__ __forceinline__ float segment_sum(const float *p, const float *q, int lo, int hi) {
-    const int s0 = lo + threadIdx.x * kPerThread;
+// fp32 sum of the weights of tokens [s0, s1) in token order; 16-byte vector
+// loads when the segment allows them.
+__device__ float segment_sum(const float *p, const float *q, int s0, int s1) {
     float acc = 0.f;
-#pragma unroll
-    for (int e = 0; e < kPerThread; ++e) {
-        const int t = s0 + e;
-        if (t < hi) acc += weight(p, q, t);
+    const bool vec = ((s1 - s0) & 3) == 0 && ((reinterpret_cast<uintptr_t>(p + s0) & 15) == 0) &&
+                     (!q || (reinterpret_cast<uintptr_t>(q + s0) & 15) == 0);
+    if (vec) {
+        const float4 *p4 = reinterpret_cast<const float4 *>(p + s0);
+        const float4 *q4 = q ? reinterpret_cast<const float4 *>(q + s0) : nullptr;
+        const int n4 = (s1 - s0) >> 2;
+#pragma unroll 8
+        for (int i = 0; i < n4; ++i) {
+            float4 w = __ldg(p4 + i);
+            if (q4) {
+                const float4 v = __ldg(q4 + i);
+                w.x = fmaxf(w.x - v.x, 0.f);
+                w.y = fmaxf(w.y - v.y, 0.f);
+                w.z = fmaxf(w.z - v.z, 0.f);
+                w.w = fmaxf(w.w - v.w, 0.f);
+            }
+            acc += w.x;
+            acc += w.y;
+            acc += w.z;
+            acc += w.w;
+        }
+        return acc;
     }
+    for (int t = s0; t < s1; ++t) acc += weight(p, q, t);
     return acc;
 }
 
-// Find, inside [lo, hi), the first token whose cumulative mass
-// base + (prefix within [lo, hi)) exceeds target.  Returns -1 when none does.
-// Writes the cumulative value before / at the token to cb / ca.
-__device__ int block_locate(const float *p, const float *q, int lo, int hi, double base,
-                            double target, double *s_warp, int *s_tok, double *s_c) {
-    const float seg = segment_sum(p, q, lo, hi);
-    double tot;
-    const double ex = base + block_exclusive_scan((double)seg, &tot, s_warp);
-    if (threadIdx.x == 0) *s_tok = -1;
-    __syncthreads();
-    if (ex <= target && target < ex + (double)seg) {
-        const int s0 = lo + threadIdx.x * kPerThread;
-        float run = 0.f;
-        for (int e = 0; e < kPerThread; ++e) {
-            const int t = s0 + e;
-            if (t >= hi) break;
-            const float w = weight(p, q, t);
-            const float prev = run;
-            run += w;
-            if (ex + (double)run > target) {
-                *s_tok = t;
-                s_c[0] = ex + (double)prev;
-                s_c[1] = ex + (double)run;
-                break;
-            }
-        }
-    }
-    __syncthreads();
-    return *s_tok;
-}
-
-// Last token with positive weight in [lo, hi), or -1.
-__device__ int block_last_positive(const float *p, const float *q, int lo, int hi, int *s_tok) {
-    if (threadIdx.x == 0) *s_tok = -1;
-    __syncthreads();
-    int best = -1;
-    for (int t = lo + threadIdx.x; t < hi; t += blockDim.x)
-        if (weight(p, q, t) > 0.f) best = t;
-    if (best >= 0) atomicMax(s_tok, best);
-    __syncthreads();
-    return *s_tok;
-}
-
-__global__ void __launch_bounds__(kThreads) spec_accept_kernel(const __grid_constant__ AcceptArgs a) {
+__global__ void __launch_bounds__(kRowThreads) spec_accept_kernel(const __grid_constant__ AcceptArgs a) {
     __shared__ double s_warp[72];
     __shared__ double s_c[2];
-    __shared__ int s_k, s_tok, s_last;
-    const int b = blockIdx.x, chunk = blockIdx.y;
+    __shared__ int s_k, s_tok;
+    const int b = blockIdx.x;
     const int gamma = a.gamma, V = a.V;
 
-    // ---- acceptance tests (every CTA of the row computes the same k)
+    // ---- acceptance tests
     if (threadIdx.x < 32) {
         const int i = threadIdx.x;
         bool rejected = false;
         if (i < gamma) {
             int x = a.tokens[(size_t)b * gamma + i];
             if (x < 0 || x >= V) {
-                if (chunk == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
                 x = 0;
             }
             const float qx = __ldg(a.q + ((size_t)b * gamma + i) * V + x);
@@ -150,92 +123,62 @@ __global__ void __launch_bounds__(kThreads) spec_accept_kernel(const __grid_cons
             rejected = !(__fmul_rn(u, qx) <= px);
         }
         const unsigned rej = __ballot_sync(0xffffffffu, rejected);
-        if (i == 0) s_k = rej ? __ffs(rej) - 1 : gamma;
+        if (i == 0) {
+            s_k = rej ? __ffs(rej) - 1 : gamma;
+            s_tok = -1;
+        }
     }
     __syncthreads();
     const int k = s_k;
     const float *prow = a.p + ((size_t)b * (gamma + 1) + k) * V;
     const float *qrow = k < gamma ? a.q + ((size_t)b * gamma + k) * V : nullptr;
 
-    // ---- this chunk's residual mass
-    const int lo = chunk * kChunk, hi = min(V, lo + kChunk);
-    {
-        const float seg = segment_sum(prow, qrow, lo, hi);
-        double tot;
-        block_exclusive_scan((double)seg, &tot, s_warp);
-        if (threadIdx.x == 0) a.chunk_sum[(size_t)b * a.n_chunks + chunk] = tot;
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int t = atomicAdd(&a.tickets[b], 1);
-        s_last = (t == a.n_chunks - 1);
-        if (s_last) a.tickets[b] = 0;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-
-    // ---- last CTA of the row: total mass, boundary chunk, scan inside it
-    const double *cs = a.chunk_sum + (size_t)b * a.n_chunks;
-    double S = 0.0;
-    for (int c2 = 0; c2 < a.n_chunks; ++c2) S += __ldcg(cs + c2);
-    const float u = __ldg(a.u_s + b);
-    int tok = -1;
-    bool near = false;
+    // ---- residual mass of this thread's segment and the row total
+    const int per = ((V + blockDim.x - 1) / blockDim.x + 3) & ~3;
+    const int s0 = min(V, (int)threadIdx.x * per), s1 = min(V, s0 + per);
+    float part = segment_sum(prow, qrow, s0, s1);
+    double S;
+    double ex = block_exclusive_scan((double)part, &S, s_warp);
     if (!(S > 0.0) && qrow) {
-        // empty residual: draw from the target row instead (sequential chunks)
+        // empty residual: draw from the target row instead
         qrow = nullptr;
-        S = 0.0;
-        for (int c2 = 0; c2 < a.n_chunks; ++c2) {
-            const int l2 = c2 * kChunk, h2 = min(V, l2 + kChunk);
-            double tot;
-            block_exclusive_scan((double)segment_sum(prow, nullptr, l2, h2), &tot, s_warp);
-            S += tot;
-        }
-        const double target = (double)u * S;
-        double base = 0.0;
-        for (int c2 = 0; c2 < a.n_chunks && tok < 0; ++c2) {
-            const int l2 = c2 * kChunk, h2 = min(V, l2 + kChunk);
-            double tot;
-            block_exclusive_scan((double)segment_sum(prow, nullptr, l2, h2), &tot, s_warp);
-            if (base + tot > target) tok = block_locate(prow, nullptr, l2, h2, base, target, s_warp, &s_tok, s_c);
-            base += tot;
-        }
-    } else if (S > 0.0) {
-        const double target = (double)u * S;
-        double base = 0.0;
-        int cstar = -1;
-        for (int c2 = 0; c2 < a.n_chunks; ++c2) {
-            const double cv = __ldcg(cs + c2);
-            if (base + cv > target) {
-                cstar = c2;
+        part = segment_sum(prow, nullptr, s0, s1);
+        ex = block_exclusive_scan((double)part, &S, s_warp);
+    }
+    const float u = __ldg(a.u_s + b);
+    const double target = (double)u * S;
+    if (S > 0.0 && ex <= target && target < ex + (double)part) {
+        float run = 0.f;
+        for (int t = s0; t < s1; ++t) {
+            const float w = weight(prow, qrow, t);
+            const float prev = run;
+            run += w;
+            if (ex + (double)run > target) {
+                s_tok = t;
+                s_c[0] = ex + (double)prev;
+                s_c[1] = ex + (double)run;
                 break;
             }
-            base += cv;
-        }
-        if (cstar >= 0) {
-            const int l2 = cstar * kChunk, h2 = min(V, l2 + kChunk);
-            tok = block_locate(prow, qrow, l2, h2, base, target, s_warp, &s_tok, s_c);
-            if (tok >= 0) {
-                near = fabs(s_c[0] / S - (double)u) < kNearBand || fabs(s_c[1] / S - (double)u) < kNearBand;
-            } else {
-                tok = block_last_positive(prow, qrow, l2, h2, &s_tok);
-                near = true;
-            }
         }
     }
-    if (tok < 0) {
+    __syncthreads();
+    int tok = s_tok;
+    bool near = false;
+    if (tok >= 0) {
+        near = fabs(s_c[0] / S - (double)u) < kNearBand || fabs(s_c[1] / S - (double)u) < kNearBand;
+    } else {
         // u*S at or past the total (rounding): the last token with mass
-        for (int c2 = a.n_chunks - 1; c2 >= 0 && tok < 0; --c2) {
-            const int l2 = c2 * kChunk, h2 = min(V, l2 + kChunk);
-            tok = block_last_positive(prow, qrow, l2, h2, &s_tok);
-        }
+        int best = -1;
+        for (int t = threadIdx.x; t < V; t += blockDim.x)
+            if (weight(prow, qrow, t) > 0.f) best = t;
+        if (best >= 0) atomicMax(&s_tok, best);
+        __syncthreads();
+        tok = s_tok;
         near = true;
-    }
-    if (tok < 0) {
-        raise_error(a.err, SVPA_DEVERR_BAD_VALUE);  // a row with no mass at all
-        tok = 0;
+        if (tok < 0) {
+            if (threadIdx.x == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);  // a row with no mass
+            tok = 0;
+        }
     }
     if (threadIdx.x <= gamma) {
         const int i = threadIdx.x;
@@ -403,15 +346,15 @@ __global__ void __launch_bounds__(kTreeThreads) spec_accept_tree_kernel(const __
 }  // namespace
 
 cudaError_t launch_spec_accept(const AcceptArgs &a, cudaStream_t stream) {
-    AcceptArgs x = a;
-    x.chunk = kChunk;
-    x.n_chunks = (a.V + kChunk - 1) / kChunk;
-    dim3 grid(a.B, x.n_chunks);
-    spec_accept_kernel<<<grid, kThreads, 0, stream>>>(x);
+    spec_accept_kernel<<<a.B, kRowThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
-int spec_accept_chunks(int vocab) { return (vocab + kChunk - 1) / kChunk; }
+// The row sampler keeps no state between CTAs: its workspace is a stub.
+int spec_accept_chunks(int vocab) {
+    (void)vocab;
+    return 1;
+}
 
 cudaError_t launch_spec_accept_tree(const TreeArgs &a, cudaStream_t stream) {
     const size_t smem = (size_t)a.V * sizeof(float);

@@ -83,10 +83,11 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     }
     int sp = p->split_pages;
     if (sp == 0) {
-        // about 16 units of work per resident CTA (sequences taken at their
-        // maximum length), so that the last units leave a short tail
+        // about 16 units of work per SM (sequences taken at their maximum
+        // length): enough for the dynamic scheduler to balance the load
+        // without multiplying split partials
         const double units = (double)std::max(1, p->batch) * p->num_kv_heads;
-        const double per = units * p->max_blocks_per_seq / (16.0 * pl->grid_slots);
+        const double per = units * p->max_blocks_per_seq / (16.0 * sm_count());
         int pw = 16;
         while (pw * 2 <= per && pw < 1024) pw *= 2;
         // keep the split partials under ~5% of the split's K/V bytes
