@@ -141,9 +141,9 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q,
                                    size_t workspace_bytes, int32_t *error_flag,
                                    void *stream);
 
-/* Bytes of workspace the samplers need for `batch` rows of `vocab` tokens
- * (per-chunk residual sums and per-row tickets).  Zero-fill once before the
- * first use; completed calls leave the tickets at zero. */
+/* Bytes of workspace the samplers take for `batch` rows of `vocab` tokens.
+ * Reserved: the samplers keep no state in it (the size is 256 bytes); pass a
+ * 16-byte aligned device buffer of at least that size. */
 svpa_status svpa_spec_accept_workspace_size(int32_t batch, int32_t vocab,
                                             size_t *bytes);
 
@@ -216,7 +216,8 @@ svpa_status svpa_spec_accept(int32_t batch, int32_t gamma, int32_t vocab,
  *               the accepted tokens, the correction/bonus token, -1...
  *  near_boundary uint8 [B] or NULL: a later-child test or the final draw fell
  *               within 1e-6 (normalised units) of its threshold.
- *  n_nodes 1..64.
+ *  n_nodes 1..64; V <= 262144 (the residual row is held in the shared memory
+ *  of one thread-block cluster), else SVPA_ERR_UNSUPPORTED.
  */
 svpa_status svpa_spec_accept_tree(int32_t batch, int32_t n_nodes, int32_t vocab,
                                   const int32_t *parent, const float *p_probs,

@@ -9,12 +9,19 @@
 // draft is accepted.  The draw is the first token whose running residual
 // mass exceeds u * (total mass).
 //
-// GB300 layout: one 1024-thread CTA per row.  Warp 0 runs the gamma
-// acceptance tests (gathered loads and a warp ballot); then every thread sums
-// its contiguous segment of the residual row in fp32 (vector loads, token
-// order), a block-wide fp64 exclusive scan gives each segment's offset and
-// the total S, and the thread whose segment holds u*S walks it again to
-// find the token.  One pass over the row, no inter-CTA protocol.
+// GB300 layout.  A row is one sequence: a few gathered loads for the
+// acceptance tests, then one pass over a V-token residual row.  One CTA per
+// row leaves most SMs idle and caps a row at what one SM can pull from
+// memory, so the row is split across a thread-block cluster of up to 8 CTAs
+// (one contiguous slice each).  Each CTA runs the acceptance tests itself
+// (the same loads, hence the same k), sums its slice with coalesced 16-byte
+// loads (fp32 per 4-token lane group, fp32 per warp, fp64 across warps), and
+// the CTA totals are exchanged through distributed shared memory.  The CTA
+// whose slice holds u*S narrows the target down warp -> 128-token step ->
+// lane -> token, re-reading only the 128 tokens of one step.  The GB300 fp64
+// pipe retires two lanes per clock per SM, so fp64 is kept to a handful of
+// scalar operations per CTA.  Vocabularies beyond 262144 tokens take a
+// one-CTA-per-row kernel.
 //
 // This file is compiled with -fmad=false; the acceptance product also uses
 // __fmul_rn, which is never contracted.
@@ -194,175 +201,604 @@ __global__ void __launch_bounds__(kRowThreads) spec_accept_kernel(const __grid_c
     }
 }
 
-// ---------------------------------------------------------------- tree
-constexpr int kTreeThreads = 1024;
+// ---------------------------------------------------------------- cluster rows
+// A row is split into n_ctas <= 8 contiguous slices of kClWarps * NI * 128
+// tokens, one per CTA of a cluster.  Warp w of CTA c owns NI steps of 128
+// tokens; in step i lane l owns tokens [base + 128 i + 4 l, +4).
+constexpr int kClWarps = 8;
+constexpr int kClThreads = kClWarps * 32;
+constexpr int kClMaxCtas = 8;
+constexpr int kStep = 128;
+constexpr int kClMaxSteps = 32;
+constexpr int kLoadBatch = 8;
+constexpr int kClMaxVocab = kClMaxCtas * kClWarps * kClMaxSteps * kStep;  // 262144
 
-// Block sum (fp64) of fp32 per-thread partials.
-__device__ double block_sum(double v, double *s_warp) {
-    double tot;
-    block_exclusive_scan(v, &tot, s_warp);
-    return tot;
+enum : int { kDrawFound = 0, kDrawPastEnd = 1, kDrawNoMass = 2 };
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
-// Inverse-CDF draw from the residual R held in shared memory (fp32, V
-// entries): thread i owns a contiguous segment.
-__device__ int smem_draw(const float *R, int V, double u, double *s_warp, int *s_tok, double *s_c,
-                         bool *near) {
-    const int seg = (V + blockDim.x - 1) / blockDim.x;
-    const int s0 = threadIdx.x * seg, s1 = min(V, s0 + seg);
-    float part = 0.f;
-    for (int t = s0; t < s1; ++t) part += R[t];
-    double S;
-    const double ex = block_exclusive_scan((double)part, &S, s_warp);
-    if (threadIdx.x == 0) *s_tok = -1;
-    __syncthreads();
-    if (!(S > 0.0)) return -2;
-    const double target = u * S;
-    if (ex <= target && target < ex + (double)part) {
-        float run = 0.f;
-        for (int t = s0; t < s1; ++t) {
-            const float prev = run;
-            run += R[t];
-            if (ex + (double)run > target) {
-                *s_tok = t;
-                s_c[0] = (ex + (double)prev) / S;
-                s_c[1] = (ex + (double)run) / S;
-                break;
+__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+    return remote;
+}
+
+// The word at the same shared-memory offset as `p` in the CTA of cluster rank `rank`.
+__device__ __forceinline__ double ld_peer_f64(const double *p, uint32_t rank) {
+    double v;
+    asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(peer_addr(p, rank)) : "memory");
+    return v;
+}
+__device__ __forceinline__ float ld_peer_f32(const float *p, uint32_t rank) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(peer_addr(p, rank)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float lane_sum(float4 w) { return ((w.x + w.y) + w.z) + w.w; }
+
+__device__ __forceinline__ float warp_incl_scan(float s) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += y;
+    }
+    return s;
+}
+
+__device__ __forceinline__ float relu(float d) { return d > 0.f ? d : 0.f; }
+
+// Weight sources.  operator()(t0) gives the weights of tokens t0..t0+3 (t0 a
+// multiple of 4; 0 past V); at(t) the weight of one token.
+// max(0, P - Q) in fp32, or P when q == nullptr, read from global memory.
+struct SrcGlobal {
+    const float *p, *q;
+    int V;
+    bool vec;  // rows 16-byte aligned and V % 4 == 0
+    __device__ float4 operator()(int t0) const {
+        float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (vec) {
+            if (t0 < V) {
+                w = __ldg(reinterpret_cast<const float4 *>(p + t0));
+                if (q) {
+                    const float4 v = __ldg(reinterpret_cast<const float4 *>(q + t0));
+                    w = make_float4(relu(w.x - v.x), relu(w.y - v.y), relu(w.z - v.z), relu(w.w - v.w));
+                }
             }
+        } else {
+            if (t0 < V) w.x = at(t0);
+            if (t0 + 1 < V) w.y = at(t0 + 1);
+            if (t0 + 2 < V) w.z = at(t0 + 2);
+            if (t0 + 3 < V) w.w = at(t0 + 3);
+        }
+        return w;
+    }
+    __device__ float at(int t) const { return weight(p, q, t); }
+};
+
+// A residual slice held in shared memory (tokens [lo, lo + slice)).
+struct SrcSmem {
+    const float *R;
+    int lo;
+    __device__ float4 operator()(int t0) const { return *reinterpret_cast<const float4 *>(R + (t0 - lo)); }
+    __device__ float at(int t) const { return R[t - lo]; }
+};
+
+// Tree rejection update R <- max(0, prev - zf * Q) in fp32 (product rounded,
+// never fused), prev = P on a node's first rejection, else R; stores the new
+// R slice and returns it.
+struct SrcUpdate {
+    float *R;
+    const float *p;  // nullptr: prev = R
+    const float *q;
+    int lo, V;
+    float zf;
+    bool vec;
+    __device__ float4 operator()(int t0) const {
+        float4 prev, qv;
+        if (vec) {
+            prev = make_float4(0.f, 0.f, 0.f, 0.f);
+            qv = prev;
+            if (t0 < V) {
+                prev = p ? __ldg(reinterpret_cast<const float4 *>(p + t0))
+                         : *reinterpret_cast<const float4 *>(R + (t0 - lo));
+                qv = __ldg(reinterpret_cast<const float4 *>(q + t0));
+            }
+        } else {
+            float pv[4], qq[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                pv[j] = 0.f;
+                qq[j] = 0.f;
+                if (t0 + j < V) {
+                    pv[j] = p ? __ldg(p + t0 + j) : R[t0 + j - lo];
+                    qq[j] = __ldg(q + t0 + j);
+                }
+            }
+            prev = make_float4(pv[0], pv[1], pv[2], pv[3]);
+            qv = make_float4(qq[0], qq[1], qq[2], qq[3]);
+        }
+        const float4 r = make_float4(relu(prev.x - __fmul_rn(zf, qv.x)), relu(prev.y - __fmul_rn(zf, qv.y)),
+                                     relu(prev.z - __fmul_rn(zf, qv.z)), relu(prev.w - __fmul_rn(zf, qv.w)));
+        *reinterpret_cast<float4 *>(R + (t0 - lo)) = r;
+        return r;
+    }
+};
+
+// Per-CTA state of the cluster-wide sums and draw of one row.
+template <int NI>
+struct ClusterRow {
+    float g[kClWarps][NI];    // per-step sums (fp32)
+    float wsum[kClWarps];     // per-warp sums (fp32, steps in order)
+    double wincl[kClWarps];   // inclusive fp64 prefix of the warp sums
+    double total[2];          // this CTA's slice total, by exchange parity (read by peers)
+    float probe[2];           // R at a probed token, by exchange parity (read by peers)
+    double peer[kClMaxCtas];  // every CTA's slice total, rank order
+    double S, r;
+    float probe_val;
+    int cta, mode, warp, tok, near, slot;
+};
+
+struct ClusterGeom {
+    int rank, n_ctas, cta_lo, cta_hi, wbase;
+};
+
+// Sums the row's weights over the cluster; returns the row total S (the same
+// double in every CTA).  When probe >= 0 the CTA owning token `probe` also
+// publishes R[probe] from `R` (after the sums), readable as st.probe_val.
+// Every thread of every CTA of the cluster calls this, with the same parity.
+template <int NI, class Src>
+__device__ double cluster_sum(ClusterRow<NI> &st, const Src &src, const ClusterGeom &g, int parity,
+                              int probe = -1, const float *R = nullptr) {
+    constexpr int nb = NI < kLoadBatch ? NI : kLoadBatch;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float G = 0.f;
+#pragma unroll
+    for (int i0 = 0; i0 < NI; i0 += nb) {
+        float4 wv[nb];
+#pragma unroll
+        for (int j = 0; j < nb; ++j) wv[j] = src(g.wbase + (i0 + j) * kStep + 4 * lane);
+#pragma unroll
+        for (int j = 0; j < nb; ++j) {
+            const float s = __shfl_sync(0xffffffffu, warp_incl_scan(lane_sum(wv[j])), 31);
+            if (lane == 0) st.g[warp][i0 + j] = s;
+            G += s;
+        }
+    }
+    if (lane == 0) st.wsum[warp] = G;
+    __syncthreads();
+    const int owner = probe >= 0 ? probe / (kClWarps * NI * kStep) : -1;
+    if (threadIdx.x == 0) {
+        double acc = 0.0;
+        for (int w = 0; w < kClWarps; ++w) {
+            acc += (double)st.wsum[w];
+            st.wincl[w] = acc;
+        }
+        st.total[parity] = acc;
+        if (owner == g.rank) st.probe[parity] = R[probe - g.cta_lo];
+    }
+    cluster_sync_all();
+    if (threadIdx.x < 32) {
+        if (lane < g.n_ctas) st.peer[lane] = ld_peer_f64(&st.total[parity], (uint32_t)lane);
+        if (lane == 0 && owner >= 0) st.probe_val = ld_peer_f32(&st.probe[parity], (uint32_t)owner);
+        __syncwarp();
+        if (lane == 0) {
+            double S = 0.0;
+            for (int c = 0; c < g.n_ctas; ++c) S += st.peer[c];
+            st.S = S;
         }
     }
     __syncthreads();
-    int tok = *s_tok;
-    if (tok >= 0) {
-        *near = fabs(s_c[0] - u) < kNearBand || fabs(s_c[1] - u) < kNearBand;
-    } else {
-        __syncthreads();
-        int best = -1;
-        for (int t = threadIdx.x; t < V; t += blockDim.x)
-            if (R[t] > 0.f) best = t;
-        if (best >= 0) atomicMax(s_tok, best);
-        __syncthreads();
-        tok = *s_tok;
-        *near = true;
-    }
-    __syncthreads();
-    return tok;
+    return st.S;
 }
 
-__global__ void __launch_bounds__(kTreeThreads) spec_accept_tree_kernel(const __grid_constant__ TreeArgs a) {
-    extern __shared__ float R[];  // V fp32 residual weights
-    __shared__ double s_warp[72];
-    __shared__ double s_c[2];
-    __shared__ int s_tok;
-    const int b = blockIdx.x;
-    const int V = a.V;
-    const int32_t *tok = a.tokens + (size_t)b * a.n_nodes;
-    int node = 0, depth = 0;
+// Last token in [lo, hi) with positive weight, or -1 (the whole CTA calls it).
+template <class Src>
+__device__ int cta_last_positive(const Src &src, int lo, int hi, int *s_slot) {
+    if (threadIdx.x == 0) *s_slot = -1;
+    __syncthreads();
+    int best = -1;
+    for (int t = lo + (int)threadIdx.x; t < hi; t += blockDim.x)
+        if (src.at(t) > 0.f) best = t;
+    if (best >= 0) atomicMax(s_slot, best);
+    __syncthreads();
+    return *s_slot;
+}
+
+// Inverse-CDF draw after cluster_sum over the same weights: the first token
+// whose running mass exceeds u*S.  Returns true in the one CTA that made the
+// draw (tok, near set there); tok = -1 there when the row has no mass (then
+// it is CTA 0).  Every thread of every CTA calls this.
+template <int NI, class Src>
+__device__ bool cluster_draw(ClusterRow<NI> &st, const Src &src, const ClusterGeom &g, float u, int *tok_out,
+                             bool *near_out) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // which CTA holds u*S: the first whose running total exceeds it
+    if (threadIdx.x == 0) {
+        const double S = st.S, target = (double)u * S;
+        int mode = kDrawNoMass, cta = 0;
+        double before = 0.0;
+        if (S > 0.0) {
+            mode = kDrawPastEnd;
+            cta = -1;
+            double e = 0.0;
+            for (int c = 0; c < g.n_ctas; ++c) {
+                const double en = e + st.peer[c];
+                if (en > target) {
+                    cta = c;
+                    before = e;
+                    mode = kDrawFound;
+                    break;
+                }
+                e = en;
+            }
+            if (mode == kDrawPastEnd)  // u*S at or past S (rounding): the last token with mass
+                for (int c = g.n_ctas - 1; c >= 0 && cta < 0; --c)
+                    if (st.peer[c] > 0.0) cta = c;
+        }
+        st.mode = mode;
+        st.cta = cta;
+        st.r = target - before;
+    }
+    __syncthreads();
+    const int mode = st.mode;
+    if (g.rank != st.cta) return false;
+    if (mode == kDrawNoMass) {
+        *tok_out = -1;
+        *near_out = true;
+        return true;
+    }
+    int tok;
+    bool near = true;
+    if (mode == kDrawFound) {
+        // warp, then 128-token step, then lane, then token
+        if (threadIdx.x == 0) {
+            const double r1 = st.r;
+            double before = 0.0;
+            int ws = -1;
+            for (int w = 0; w < kClWarps; ++w) {
+                if (st.wincl[w] > r1) {
+                    ws = w;
+                    break;
+                }
+                before = st.wincl[w];
+            }
+            st.warp = ws;
+            st.r = r1 - before;
+            st.tok = -2;
+            st.near = 1;
+        }
+        __syncthreads();
+        const int ws = st.warp;
+        const int wlo = g.cta_lo + (ws < 0 ? 0 : ws) * NI * kStep;
+        if (warp == ws) {
+            const double r2 = st.r;
+            float G = 0.f;
+            int step = -1;
+            for (int i = 0; i < NI; ++i) {
+                const float Gn = G + st.g[ws][i];
+                if ((double)Gn > r2) {
+                    step = i;
+                    break;
+                }
+                G = Gn;
+            }
+            if (step >= 0) {
+                const int t0 = wlo + step * kStep + 4 * lane;
+                const float4 wv = src(t0);
+                const float incl = warp_incl_scan(lane_sum(wv));
+                float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+                if (lane == 0) excl = 0.f;
+                const unsigned hit = __ballot_sync(0xffffffffu, (double)(G + incl) > r2);
+                const int l = hit ? __ffs(hit) - 1 : 31;
+                if (lane == l) {
+                    const float wj[4] = {wv.x, wv.y, wv.z, wv.w};
+                    const double band = kNearBand * st.S;
+                    float c = G + excl;
+                    int found = -1, lastpos = -1;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (wj[j] > 0.f) lastpos = j;
+                        const float cn = c + wj[j];
+                        if (found < 0 && (double)cn > r2) {
+                            found = j;
+                            st.near = (fabs((double)c - r2) < band || fabs((double)cn - r2) < band) ? 1 : 0;
+                        }
+                        c = cn;
+                    }
+                    // found < 0: a rounding gap between levels (u*S within
+                    // a few fp32 ulps of this group's end): its last token
+                    st.tok = found >= 0 ? t0 + found : (lastpos >= 0 ? t0 + lastpos : -2);
+                }
+            }
+        }
+        __syncthreads();
+        tok = st.tok;
+        near = st.near != 0;
+        if (tok == -2) {
+            // rounding gap at the CTA or warp level: the last token with mass
+            // in that range
+            const int lo = ws < 0 ? g.cta_lo : wlo;
+            const int hi = ws < 0 ? g.cta_hi : min(g.cta_hi, wlo + NI * kStep);
+            tok = cta_last_positive(src, lo, hi, &st.slot);
+            near = true;
+        }
+    } else {  // kDrawPastEnd
+        tok = cta_last_positive(src, g.cta_lo, g.cta_hi, &st.slot);
+    }
+    *tok_out = tok;
+    *near_out = near;
+    return true;
+}
+
+template <int NI>
+__device__ __forceinline__ ClusterGeom cluster_geom(int V, int n_ctas) {
+    ClusterGeom g;
+    g.rank = (int)(blockIdx.x % (unsigned)n_ctas);
+    g.n_ctas = n_ctas;
+    g.cta_lo = g.rank * (kClWarps * NI * kStep);
+    g.cta_hi = min(V, g.cta_lo + kClWarps * NI * kStep);
+    g.wbase = g.cta_lo + (int)(threadIdx.x >> 5) * NI * kStep;
+    return g;
+}
+
+// ---------------------------------------------------------------- linear, cluster per row
+template <int NI>
+__global__ void __launch_bounds__(kClThreads, 2)
+    spec_accept_cluster_kernel(const __grid_constant__ AcceptArgs a, int n_ctas) {
+    __shared__ ClusterRow<NI> st;
+    __shared__ int s_k;
+    __shared__ float s_u;
+    const ClusterGeom g = cluster_geom<NI>(a.V, n_ctas);
+    const int b = (int)(blockIdx.x / (unsigned)n_ctas);
+    const int gamma = a.gamma, V = a.V;
+    const int lane = threadIdx.x & 31;
+
+    // acceptance tests: every CTA of the cluster makes the same loads and
+    // reaches the same k
+    if (threadIdx.x < 32) {
+        bool rejected = false;
+        if (lane < gamma) {
+            int x = a.tokens[(size_t)b * gamma + lane];
+            if (x < 0 || x >= V) {
+                if (g.rank == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                x = 0;
+            }
+            const float qx = __ldg(a.q + ((size_t)b * gamma + lane) * V + x);
+            const float px = __ldg(a.p + ((size_t)b * (gamma + 1) + lane) * V + x);
+            const float u = __ldg(a.u_acc + (size_t)b * gamma + lane);
+            rejected = !(__fmul_rn(u, qx) <= px);
+        }
+        const unsigned rej = __ballot_sync(0xffffffffu, rejected);
+        if (lane == 0) {
+            s_k = rej ? __ffs(rej) - 1 : gamma;
+            s_u = __ldg(a.u_s + b);
+        }
+    }
+    __syncthreads();
+    const int k = s_k;
+    const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.p) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
+    SrcGlobal src{a.p + ((size_t)b * (gamma + 1) + k) * V, k < gamma ? a.q + ((size_t)b * gamma + k) * V : nullptr,
+                  V, vec};
+    double S = cluster_sum(st, src, g, 0);
+    if (!(S > 0.0) && src.q) {
+        // empty residual: draw from the target row instead (S is the same in
+        // every CTA, so the whole cluster takes this branch)
+        src.q = nullptr;
+        S = cluster_sum(st, src, g, 1);
+    }
+    int tok;
+    bool near;
+    if (cluster_draw(st, src, g, s_u, &tok, &near) && threadIdx.x == 0) {
+        if (tok < 0) {  // a row with no mass
+            raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+            tok = 0;
+        }
+        a.out_tokens[(size_t)b * (gamma + 1) + k] = tok;
+        if (a.near) a.near[b] = near ? 1 : 0;
+    }
+    if (g.rank == 0) {
+        const int i = threadIdx.x;
+        if (i <= gamma && i != k)
+            a.out_tokens[(size_t)b * (gamma + 1) + i] = i < k ? a.tokens[(size_t)b * gamma + i] : -1;
+        if (i == 0) a.accepted_len[b] = k;
+    }
+    // no CTA leaves while a peer may still read its shared memory
+    cluster_sync_all();
+}
+
+// ---------------------------------------------------------------- tree, cluster per row
+// Multi-draft recursion along the tree ("Tree Attention Mechanism" and the
+// rejection-recovery step of the same page): at a node with children
+// c_1..c_m (node order) and draft distribution Q, child c_1 is accepted iff
+// u * Q(x) <= P(x) (fp32, as in the linear sampler); after a rejection the
+// residual becomes R <- max(0, R - Z * Q) with Z = sum(R) (R = P before the
+// first rejection, Z = 1), and child c_j (j > 1) is accepted iff
+// u * Q(x) * Z <= R(x).  An accepted child becomes the node; when every
+// child is rejected the token is drawn from R (from P when R is empty), and a
+// leaf draws its bonus token from its own P.  The residual slice lives in
+// each CTA's shared memory; R(x) for the next sibling is published by the
+// CTA that owns x along with the slice sums.
+template <int NI>
+__global__ void __launch_bounds__(kClThreads, 2)
+    spec_accept_tree_cluster_kernel(const __grid_constant__ TreeArgs a, int n_ctas) {
+    extern __shared__ float4 dyn_smem[];
+    float *R = reinterpret_cast<float *>(dyn_smem);  // this CTA's residual slice
+    __shared__ ClusterRow<NI> st;
+    const ClusterGeom g = cluster_geom<NI>(a.V, n_ctas);
+    const int b = (int)(blockIdx.x / (unsigned)n_ctas);
+    const int V = a.V, n_nodes = a.n_nodes;
+    const int32_t *ntok = a.tokens + (size_t)b * n_nodes;
+    const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.p) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
+    const bool lead = g.rank == 0 && threadIdx.x == 0;
+    auto token_of = [&](int node) {
+        int x = ntok[node];
+        if (x < 0 || x >= V) {
+            if (lead) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+            x = 0;
+        }
+        return x;
+    };
+    const float u_s = __ldg(a.u_s + b);
+    int node = 0, depth = 0, parity = 0;
     bool near = false;
-    int final_tok = -1;
+    int tok = -1;
+    bool drew;
     while (true) {
-        const float *Pn = a.p + ((size_t)b * a.n_nodes + node) * V;
+        const float *Pn = a.p + ((size_t)b * n_nodes + node) * V;
         const int qr = a.qrow[node];
-        if (qr < 0) {
-            for (int t = threadIdx.x; t < V; t += blockDim.x) R[t] = __ldg(Pn + t);
-            __syncthreads();
+        if (qr < 0) {  // leaf: bonus token from its own P
+            const SrcGlobal src{Pn, nullptr, V, vec};
+            cluster_sum(st, src, g, parity);
+            parity ^= 1;
             bool nb = false;
-            final_tok = smem_draw(R, V, (double)__ldg(a.u_s + b), s_warp, &s_tok, s_c, &nb);
+            drew = cluster_draw(st, src, g, u_s, &tok, &nb);
             near |= nb;
             break;
         }
         const float *Qn = a.q + ((size_t)b * a.n_internal + qr) * V;
         double Z = 1.0;
+        float rx = 0.f;  // R(x) of the child under test, after a rejection
         int accepted = -1, tested = 0;
-        for (int cnode = node + 1; cnode < a.n_nodes; ++cnode) {
-            if (a.parent[cnode] != node) continue;
-            int x = tok[cnode];
-            if (x < 0 || x >= V) {
-                if (threadIdx.x == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
-                x = 0;
-            }
-            const float u = __ldg(a.u_acc + (size_t)b * a.n_nodes + cnode);
+        for (int c = node + 1; c < n_nodes; ++c) {
+            if (a.parent[c] != node) continue;
+            const int x = token_of(c);
+            const float u = __ldg(a.u_acc + (size_t)b * n_nodes + c);
             bool ok;
             if (tested == 0) {
                 ok = __fmul_rn(u, __ldg(Qn + x)) <= __ldg(Pn + x);
             } else {
                 const double lhs = (double)u * (double)__ldg(Qn + x) * Z;
-                const double rx = (double)R[x];
-                ok = lhs <= rx;
-                if (Z > 0.0 && fabs(lhs - rx) / Z < kNearBand) near = true;
+                ok = lhs <= (double)rx;
+                if (Z > 0.0 && fabs(lhs - (double)rx) / Z < kNearBand) near = true;
             }
             if (ok) {
-                accepted = cnode;
+                accepted = c;
                 break;
             }
-            // reject: R <- max(0, R - Z * Q), Z <- sum(R)
-            const float zf = (float)Z;
-            float part = 0.f;
-            for (int t = threadIdx.x; t < V; t += blockDim.x) {
-                const float prev = tested == 0 ? __ldg(Pn + t) : R[t];
-                const float v = prev - zf * __ldg(Qn + t);
-                const float r = v > 0.f ? v : 0.f;
-                R[t] = r;
-                part += r;
-            }
+            int xn = -1;  // the next sibling's token: R is probed there
+            for (int c2 = c + 1; c2 < n_nodes; ++c2)
+                if (a.parent[c2] == node) {
+                    xn = token_of(c2);
+                    break;
+                }
+            const SrcUpdate upd{R, tested == 0 ? Pn : nullptr, Qn, g.cta_lo, V, (float)Z, vec};
+            Z = cluster_sum(st, upd, g, parity, xn, R);
+            parity ^= 1;
+            rx = st.probe_val;
             ++tested;
-            Z = block_sum((double)part, s_warp);
         }
         if (accepted >= 0) {
             ++depth;
-            if (threadIdx.x == 0) {
+            if (lead) {
                 a.path_nodes[(size_t)b * a.width + depth] = accepted;
-                a.out_tokens[(size_t)b * a.width + depth - 1] = tok[accepted];
+                a.out_tokens[(size_t)b * a.width + depth - 1] = ntok[accepted];
             }
             node = accepted;
             continue;
         }
         bool nb = false;
-        final_tok = smem_draw(R, V, (double)__ldg(a.u_s + b), s_warp, &s_tok, s_c, &nb);
-        if (final_tok == -2) {  // empty residual: draw from the node's target row
-            for (int t = threadIdx.x; t < V; t += blockDim.x) R[t] = __ldg(Pn + t);
-            __syncthreads();
-            final_tok = smem_draw(R, V, (double)__ldg(a.u_s + b), s_warp, &s_tok, s_c, &nb);
+        if (Z > 0.0) {
+            drew = cluster_draw(st, SrcSmem{R, g.cta_lo}, g, u_s, &tok, &nb);
+        } else {  // empty residual: draw from the node's target row
+            const SrcGlobal src{Pn, nullptr, V, vec};
+            cluster_sum(st, src, g, parity);
+            parity ^= 1;
+            drew = cluster_draw(st, src, g, u_s, &tok, &nb);
         }
         near |= nb;
         break;
     }
-    if (final_tok < 0) {
-        if (threadIdx.x == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
-        final_tok = 0;
+    if (drew && threadIdx.x == 0) {
+        if (tok < 0) {  // a row with no mass
+            raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+            tok = 0;
+        }
+        a.out_tokens[(size_t)b * a.width + depth] = tok;
+        if (a.near) a.near[b] = near ? 1 : 0;
     }
-    if (threadIdx.x == 0) {
+    if (lead) {
         int32_t *path = a.path_nodes + (size_t)b * a.width;
         int32_t *out = a.out_tokens + (size_t)b * a.width;
         path[0] = 0;
-        for (int d = depth + 1; d < a.width; ++d) path[d] = -1;
-        out[depth] = final_tok;
-        for (int d = depth + 1; d < a.width; ++d) out[d] = -1;
+        for (int d = depth + 1; d < a.width; ++d) {
+            path[d] = -1;
+            out[d] = -1;
+        }
         a.accepted_len[b] = depth;
-        if (a.near) a.near[b] = near ? 1 : 0;
     }
+    cluster_sync_all();
+}
+
+// Steps per warp for a V-token row (a power of two), or 0 when V is beyond
+// the cluster kernels.
+int cluster_steps(int V) {
+    constexpr int per_step_row = kClWarps * kStep * kClMaxCtas;
+    const int need = (V + per_step_row - 1) / per_step_row;
+    int ni = 1;
+    while (ni < need) ni <<= 1;
+    return ni <= kClMaxSteps ? ni : 0;
+}
+
+template <class Args>
+cudaError_t launch_cluster(void (*const *kernels)(Args, int), const Args &a, int V, int B, size_t dyn_smem_per_step,
+                           cudaStream_t stream) {
+    const int ni = cluster_steps(V);
+    const int chunk = kClWarps * ni * kStep;
+    const int n = (V + chunk - 1) / chunk;
+    int idx = 0;
+    while ((1 << idx) < ni) ++idx;
+    void (*kern)(Args, int) = kernels[idx];
+    const size_t smem = dyn_smem_per_step * (size_t)ni;
+    if (smem > 0) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((long long)B * n));
+    cfg.blockDim = dim3(kClThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)n;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, n);
 }
 
 }  // namespace
 
 cudaError_t launch_spec_accept(const AcceptArgs &a, cudaStream_t stream) {
-    spec_accept_kernel<<<a.B, kRowThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    if (a.B <= 0) return cudaSuccess;
+    if (cluster_steps(a.V) == 0 || (long long)a.B * kClMaxCtas > 0x7fffffffLL) {
+        spec_accept_kernel<<<a.B, kRowThreads, 0, stream>>>(a);
+        return cudaGetLastError();
+    }
+    static void (*const kernels[])(AcceptArgs, int) = {
+        spec_accept_cluster_kernel<1>, spec_accept_cluster_kernel<2>,  spec_accept_cluster_kernel<4>,
+        spec_accept_cluster_kernel<8>, spec_accept_cluster_kernel<16>, spec_accept_cluster_kernel<32>};
+    return launch_cluster(kernels, a, a.V, a.B, 0, stream);
 }
 
-// The row sampler keeps no state between CTAs: its workspace is a stub.
-int spec_accept_chunks(int vocab) {
-    (void)vocab;
-    return 1;
-}
+int spec_accept_tree_max_vocab() { return kClMaxVocab; }
 
 cudaError_t launch_spec_accept_tree(const TreeArgs &a, cudaStream_t stream) {
-    const size_t smem = (size_t)a.V * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(spec_accept_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    spec_accept_tree_kernel<<<a.B, kTreeThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    if (a.B <= 0) return cudaSuccess;
+    if (cluster_steps(a.V) == 0) return cudaErrorInvalidValue;
+    static void (*const kernels[])(TreeArgs, int) = {
+        spec_accept_tree_cluster_kernel<1>, spec_accept_tree_cluster_kernel<2>,
+        spec_accept_tree_cluster_kernel<4>, spec_accept_tree_cluster_kernel<8>,
+        spec_accept_tree_cluster_kernel<16>, spec_accept_tree_cluster_kernel<32>};
+    return launch_cluster(kernels, a, a.V, a.B, (size_t)kClWarps * kStep * sizeof(float), stream);
 }
 
 }  // namespace svpa

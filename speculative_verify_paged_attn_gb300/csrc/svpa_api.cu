@@ -14,7 +14,7 @@
 #include "svpa_internal.h"
 
 namespace svpa {
-int spec_accept_chunks(int vocab);
+int spec_accept_tree_max_vocab();
 }  // namespace svpa
 
 using namespace svpa;
@@ -259,9 +259,8 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
 
 svpa_status svpa_spec_accept_workspace_size(int32_t batch, int32_t vocab, size_t *bytes) {
     if (!bytes || batch < 0 || vocab < 1) return SVPA_ERR_INVALID_ARG;
-    const size_t nc = (size_t)spec_accept_chunks(vocab);
-    *bytes = align_up((size_t)batch * sizeof(int32_t)) + align_up((size_t)batch * nc * sizeof(double));
-    *bytes = std::max<size_t>(*bytes, kAlign);
+    // reserved: the samplers keep no state between CTAs
+    *bytes = kAlign;
     return SVPA_OK;
 }
 
@@ -271,7 +270,6 @@ svpa_status svpa_spec_accept(int32_t batch, int32_t gamma, int32_t vocab, const 
                              uint8_t *near_boundary, void *workspace, size_t workspace_bytes,
                              int32_t *error_flag, void *stream) {
     if (batch < 0 || gamma < 1 || gamma > 32 || vocab < 1) return SVPA_ERR_INVALID_ARG;
-    if (spec_accept_chunks(vocab) > 65535) return SVPA_ERR_UNSUPPORTED;
     if (batch == 0) return SVPA_OK;
     if (!p_probs || !q_probs || !draft_tokens || !u_accept || !u_sample || !accepted_len || !out_tokens ||
         !error_flag)
@@ -289,9 +287,6 @@ svpa_status svpa_spec_accept(int32_t batch, int32_t gamma, int32_t vocab, const 
     a.accepted_len = accepted_len;
     a.out_tokens = out_tokens;
     a.near = near_boundary;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    a.tickets = reinterpret_cast<int32_t *>(ws);
-    a.chunk_sum = reinterpret_cast<double *>(ws + align_up((size_t)batch * sizeof(int32_t)));
     a.err = error_flag;
     a.B = batch;
     a.gamma = gamma;
@@ -307,7 +302,7 @@ svpa_status svpa_spec_accept_tree(int32_t batch, int32_t n_nodes, int32_t vocab,
     (void)workspace;
     (void)workspace_bytes;
     if (batch < 0 || n_nodes < 1 || n_nodes > kMaxNq || vocab < 1 || !parent) return SVPA_ERR_INVALID_ARG;
-    if (vocab > 55000) return SVPA_ERR_UNSUPPORTED;  // residual row held in shared memory
+    if (vocab > spec_accept_tree_max_vocab()) return SVPA_ERR_UNSUPPORTED;  // residual slices in shared memory
     if (parent[0] != -1) return SVPA_ERR_INVALID_ARG;
     for (int i = 1; i < n_nodes; ++i)
         if (parent[i] < 0 || parent[i] >= i) return SVPA_ERR_INVALID_ARG;

@@ -66,10 +66,8 @@ struct AcceptArgs {
     int32_t *accepted_len;
     int32_t *out_tokens;
     uint8_t *near;
-    double *chunk_sum;    // [B, n_chunks]
-    int32_t *tickets;     // [B]
     int32_t *err;
-    int32_t B, gamma, V, chunk, n_chunks;
+    int32_t B, gamma, V;
 };
 cudaError_t launch_spec_accept(const AcceptArgs &a, cudaStream_t stream);
 

@@ -116,11 +116,7 @@ def test_linear_uniform_edges():
     check_linear(s)
 
 
-@pytest.mark.parametrize("batch", [4, 128])
-def test_tree_parity(batch):
-    wl = W.WORKLOADS["tree"].scaled(batch=batch)
-    s = W.make_sampler(wl, W.SEEDS["tree"], device="cpu")
-    parent = wl.parent
+def run_tree(parent, s):
     B, n, V = s.p.shape
     W_ = oracle.tree_max_depth(np.array(parent, np.int32)) + 1
     k = torch.full((B,), -7, dtype=torch.int32, device=DEV)
@@ -131,13 +127,52 @@ def test_tree_parity(batch):
     svpa.spec_accept_tree(parent, s.p.to(DEV), s.q.to(DEV), s.tokens.to(DEV), s.u_accept.to(DEV),
                           s.u_sample.to(DEV), k, path, toks, error_flag=err, near_boundary=near)
     assert svpa.check_error(err) == 0
+    return k.cpu().numpy(), path.cpu().numpy(), toks.cpu().numpy()
+
+
+def check_tree(parent, s, max_near=0.25):
+    k, path, toks = run_tree(parent, s)
     rk, rpath, rtoks, rnear = oracle.spec_accept_tree(np.array(parent, np.int32), s.p, s.q, s.tokens,
                                                       s.u_accept, s.u_sample)
     ok = ~rnear
-    assert rnear.mean() <= 0.25  # flagged draws are reported; a flood would mean a bug
-    assert np.array_equal(k.cpu().numpy()[ok], rk[ok])
-    assert np.array_equal(path.cpu().numpy()[ok], rpath[ok])
-    assert np.array_equal(toks.cpu().numpy()[ok], rtoks[ok])
+    assert rnear.mean() <= max_near  # flagged draws are reported; a flood would mean a bug
+    assert np.array_equal(k[ok], rk[ok])
+    assert np.array_equal(path[ok], rpath[ok])
+    assert np.array_equal(toks[ok], rtoks[ok])
+    return k
+
+
+@pytest.mark.parametrize("batch", [4, 128])
+def test_tree_parity(batch):
+    wl = W.WORKLOADS["tree"].scaled(batch=batch)
+    s = W.make_sampler(wl, W.SEEDS["tree"], device="cpu")
+    check_tree(wl.parent, s)
+
+
+@pytest.mark.parametrize("vocab", [4099, 128256])
+def test_tree_vocab_edges(vocab):
+    # 4099: rows not a multiple of 4 tokens (scalar loads); 128256: a
+    # residual row larger than one CTA's shared memory would hold
+    wl = W.WORKLOADS["tree"].scaled(batch=6)
+    s = W.make_sampler(wl, 61, device="cpu", vocab=vocab)
+    check_tree(wl.parent, s)
+
+
+def test_tree_empty_residual_draws_from_target():
+    # chain 0-1-2-3; at the root P = Q/2 (unnormalised) so the residual after
+    # the rejection is empty and the token comes from P_root itself
+    wl = W.WORKLOADS["7b"].scaled(batch=16, vocab=3000, gamma=3)
+    s = W.make_sampler(wl, 62, device="cpu")
+    parent = [-1, 0, 1, 2]
+    B = 16
+    tok = torch.cat([torch.zeros(B, 1, dtype=torch.int32), s.tokens], 1)
+    ua = torch.cat([torch.zeros(B, 1), s.u_accept], 1)
+    ua[:, 1] = 0.99
+    p = s.p.clone()
+    p[:, 0] = 0.5 * s.q[:, 0]
+    t = W.SamplerInputs(p=p, q=s.q, tokens=tok, u_accept=ua, u_sample=s.u_sample)
+    k = check_tree(parent, t)
+    assert np.all(k == 0)
 
 
 def test_tree_chain_matches_linear_kernel():
@@ -157,6 +192,49 @@ def test_tree_chain_matches_linear_kernel():
     assert svpa.check_error(err) == 0
     assert np.array_equal(kt.cpu().numpy(), k)
     assert np.array_equal(outt.cpu().numpy(), toks)
+
+
+def test_linear_empty_residual_draws_from_target():
+    # P_0 = Q_0/2 (unnormalised): draft 0 is rejected for u > 1/2 and the
+    # residual max(0, P_0 - Q_0) is empty, so the token is drawn from P_0
+    wl = W.WORKLOADS["7b"].scaled(batch=16, vocab=5000)
+    s = W.make_sampler(wl, 63, device="cpu")
+    s.p[:, 0] = 0.5 * s.q[:, 0]
+    s.u_accept[:, 0] = 0.9
+    k = check_linear(s)
+    assert np.all(k == 0)
+
+
+def test_linear_unaligned_rows():
+    # rows that start 4 bytes past a 16-byte boundary take the scalar loads
+    wl = W.WORKLOADS["7b"].scaled(batch=12, vocab=6000)
+    s = W.make_sampler(wl, 64, device="cpu")
+    B, g1, V = s.p.shape
+    d = {}
+    for name in ("p", "q"):
+        x = getattr(s, name)
+        buf = torch.empty(x.numel() + 1, dtype=x.dtype, device=DEV)
+        dv = buf[1:].view(x.shape)
+        dv.copy_(x)
+        d[name] = dv
+    assert d["p"].data_ptr() % 16 != 0
+    k = torch.empty(B, dtype=torch.int32, device=DEV)
+    toks = torch.empty((B, g1), dtype=torch.int32, device=DEV)
+    ws = torch.zeros(svpa.spec_accept_workspace_size(B, V), dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    svpa.spec_accept(d["p"], d["q"], s.tokens.to(DEV), s.u_accept.to(DEV), s.u_sample.to(DEV), k, toks,
+                     workspace=ws, error_flag=err)
+    assert svpa.check_error(err) == 0
+    rk, rt, rnear, _ = oracle.spec_accept(s.p, s.q, s.tokens, s.u_accept, s.u_sample)
+    assert np.array_equal(k.cpu().numpy(), rk)
+    assert np.array_equal(toks.cpu().numpy()[~rnear], rt[~rnear])
+
+
+def test_linear_vocab_beyond_cluster_rows():
+    # V > 262144 takes the one-CTA-per-row kernel
+    wl = W.WORKLOADS["7b"].scaled(batch=3, vocab=300_000, gamma=2)
+    s = W.make_sampler(wl, 65, device="cpu")
+    check_linear(s)
 
 
 def test_gpu_output_distribution_equals_target():
