@@ -10,21 +10,26 @@
 //
 // Work unit = (sequence, kv head, KV split); persistent CTAs, one per SM.
 // Warp roles:
-//   warp 0     producer: takes units from an atomic counter, streams blocks of
-//              4 pages (64 tokens) of K and V -- and each unit's query tile --
-//              with tiled TMA copies (128-byte swizzle) into a 3-stage ring;
-//              missing pages of a unit's last block are fetched at an
-//              out-of-range block coordinate, which the copy fills with zeros;
+//   warp 0     producer: takes units from an atomic counter and streams blocks
+//              of 8 pages (128 tokens) of K -- with each unit's query tile on
+//              its first block -- and, one block behind, of V, with tiled TMA
+//              copies (128-byte swizzle) into 3-deep K and V rings; lanes 0..7
+//              issue one page each; missing pages of a unit's last block are
+//              fetched at an out-of-range block coordinate (zero fill);
 //   warp 1     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T
-//              (M 128, N 64, K 128) into one of two TMEM S buffers, looking one
-//              block ahead, and O += P_j V_j (M 128, N 128, K 64) into one of
-//              two TMEM O buffers (one per unit in flight);
-//   warps 2-5  softmax + epilogue, one thread per query row (TMEM lane): S row
-//              from TMEM, mask, online softmax with a lazy reference maximum
-//              (O in TMEM is rescaled only when a row maximum grows by more
-//              than 2^8), P row as bf16 into shared memory for the PV MMA;
-//              at a unit's end, O row from TMEM to the output (or a split
-//              partial, merged by the last split's CTA with a log-sum-exp).
+//              (M 128, N 128, K 128) into one of two TMEM S buffers, issued
+//              ahead of PV_{j-1} when K_j has already landed, and
+//              O += P_j V_j (M 128, N 128, K 128) with P_j read from TMEM,
+//              into one of two TMEM O buffers (one per unit in flight);
+//   warps 2-5  softmax, one thread per query row (TMEM lane): S row from
+//              TMEM, mask (only on blocks that reach the speculative slots),
+//              online softmax with a lazy reference maximum (O is rescaled in
+//              TMEM only when a row maximum grows by more than 2^8), P row as
+//              bf16 pairs written over the S columns it came from;
+//   warps 6-9  epilogue, one thread per query row: a finished unit's O from
+//              TMEM to the output (or a split partial, merged by the last
+//              split's CTA with log-sum-exp weights, one warp per row) while
+//              the softmax warps run the next unit.
 // All waits are bounded; nothing spins forever.
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -47,9 +52,9 @@ constexpr int kQBuf = 2 * kQSlab;
 constexpr int kNK = 3;                          // K ring (freed once S_j is computed)
 constexpr int kNV = 3;                          // V ring (freed once PV_j is computed)
 constexpr int kNMeta = 8;                       // block descriptors in flight
-constexpr int kThreads = 192;
-constexpr int kSoftmaxThreads = 128;
-constexpr int kBarSoftmax = 1;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 128;
+constexpr int kBarEpi = 1;                      // named barrier of the epilogue warps
 constexpr float kRescaleLog2 = 8.f;             // rescale O when a maximum grows by > 2^8
 
 // TMEM columns: O[0] 0..127, O[1] 128..255, S[0] 256..383, S[1] 384..511; the
@@ -75,10 +80,17 @@ struct Smem {
     uint64_t s_full[2];
     uint64_t p_full, p_empty;
     uint64_t o_full[2], o_empty[2];
+    uint64_t stat_full, stat_empty;      // softmax -> epilogue hand-off of a finished unit
     BlockMeta meta[kNMeta];
+    int32_t vid[kNMeta][kPagesPerBlock];  // page ids of a block, for its V copies
+    float2 stat[kRows];                  // (reference maximum, running sum) per row
+    int32_t ep_b, ep_h, ep_split, ep_nsplit, ep_end;
     uint32_t tmem_base;
     int32_t last;
 };
+
+// fits the 227 KB a CTA may opt into, with room to align the base to 1 KB
+static_assert(sizeof(Smem) + 1024 <= 232448, "pva_tc_kernel shared memory");
 
 __device__ __forceinline__ uint32_t par_of(int idx) { return (uint32_t)((idx >> 1) & 1); }
 
@@ -108,6 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sm.q_empty, 1);
         mbar_init(&sm.p_full, 4);
         mbar_init(&sm.p_empty, 1);
+        mbar_init(&sm.stat_full, 4);
+        mbar_init(&sm.stat_empty, 4);
         fence_mbar_init();
     }
     // query rows past M are never written by the copies: keep them zero
@@ -136,26 +150,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int jk = 0, jv = 0, units = 0;      // K blocks issued, V blocks issued, units started (warp-uniform)
         bool ok = true;
-        bool have_prev = false;             // a block whose V still has to be issued
-        int prev_id = 0, prev_h = 0;        // lanes 0..7: page `lane` of that block
         const uint32_t qbytes = (uint32_t)(a.M * 128 * 2);
-        // V of block jv, one block behind K so that K can run ahead; lanes 0..7
-        // issue one page each
-        auto issue_v = [&]() -> bool {
+        // V of the oldest block whose K is out, if its ring slot is free (a
+        // non-blocking test): K runs ahead as far as its own ring allows and
+        // V follows as PV frees slots, neither waiting for the other
+        auto try_issue_v = [&]() -> bool {
+            if (jv >= jk) return false;
             const int vs = jv % kNV;
-            bool good = true;
-            if (lane == 0) {
-                if (jv >= kNV) good = mbar_wait(&sm.v_empty[vs], (uint32_t)(((jv / kNV) & 1) ^ 1), a.err);
-                if (good) mbar_arrive_expect_tx(&sm.v_full[vs], kKVTile);
-            }
-            good = __shfl_sync(0xffffffffu, (int)good, 0) != 0;
-            if (good && lane < kPagesPerBlock) {
+            int ready = 1;
+            if (lane == 0 && jv >= kNV) ready = mbar_test(&sm.v_empty[vs], (uint32_t)(((jv / kNV) & 1) ^ 1));
+            if (!__shfl_sync(0xffffffffu, ready, 0)) return false;
+            if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[vs], kKVTile);
+            if (lane < kPagesPerBlock) {
+                const int id = sm.vid[jv % kNMeta][lane], hh = sm.meta[jv % kNMeta].h;
                 uint8_t *sv = sm.vbuf[vs] + lane * 2048;
-                tma_load_4d(sv, &mv0, 0, 0, prev_h, prev_id, &sm.v_full[vs], pol);
-                tma_load_4d(sv + kKSlab, &mv1, 0, 0, prev_h, prev_id, &sm.v_full[vs], pol);
+                tma_load_4d(sv, &mv0, 0, 0, hh, id, &sm.v_full[vs], pol);
+                tma_load_4d(sv + kKSlab, &mv1, 0, 0, hh, id, &sm.v_full[vs], pol);
             }
-            if (good) ++jv;
-            return good;
+            __syncwarp();
+            ++jv;
+            return true;
+        };
+        // bounded wait for phase `parity` of `bar`, issuing V copies meanwhile
+        auto wait_issuing_v = [&](uint64_t *bar, uint32_t parity) -> bool {
+            unsigned long long t0 = 0;
+            while (true) {
+                int done = 0;
+                if (lane == 0) done = mbar_test(bar, parity);
+                if (__shfl_sync(0xffffffffu, done, 0)) return true;
+                if (try_issue_v()) {
+                    t0 = 0;
+                    continue;
+                }
+                const unsigned long long now = global_ns();
+                if (t0 == 0) {
+                    t0 = now;
+                } else if (now - t0 > kWaitLimitNs) {
+                    if (lane == 0) raise_error(a.err, SVPA_DEVERR_TIMEOUT);
+                    return false;
+                }
+            }
         };
         while (ok) {
             int u = 0;
@@ -175,69 +209,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int page0 = split * a.split_pages;
             const int n = min(a.split_pages, npages - page0);
             const int nblk = (n + kPagesPerBlock - 1) / kPagesPerBlock;
-            const int qb = 0;
             const int32_t *bt = a.block_table + (size_t)b * a.max_blocks + page0;
+            int blk_next = a.num_blocks;
             for (int i0 = 0; i0 < n && ok; i0 += 32) {
                 int blk = a.num_blocks;  // out of range: zero-filled page
-                if (i0 + lane < n) {
-                    blk = __ldg(bt + i0 + lane);
-                    if (blk < 0 || blk >= a.num_blocks) {
-                        raise_error(a.err, SVPA_DEVERR_BAD_BLOCK);
-                        blk = 0;
-                    }
+                if (i0 == 0) {
+                    if (lane < n) blk = __ldg(bt + lane);
+                } else {
+                    blk = blk_next;
                 }
+                if (i0 + lane < n && (blk < 0 || blk >= a.num_blocks)) {
+                    raise_error(a.err, SVPA_DEVERR_BAD_BLOCK);
+                    blk = 0;
+                }
+                blk_next = a.num_blocks;
+                if (i0 + 32 + lane < n) blk_next = __ldg(bt + i0 + 32 + lane);
                 const int cnt = min(32, n - i0);
                 for (int j0 = 0; j0 < cnt; j0 += kPagesPerBlock) {
                     // lanes 0..7 hold the ids of the block's 8 pages
                     int my_id = __shfl_sync(0xffffffffu, blk, (j0 + (lane & 7)) & 31);
                     if (j0 + (lane & 7) >= cnt) my_id = a.num_blocks;
                     const int bi = (i0 + j0) / kPagesPerBlock;  // block index in the unit
-                    // at a unit boundary the previous unit's last V goes out
-                    // before waiting for the query buffer to free up
-                    if (bi == 0 && have_prev) {
-                        ok = issue_v();
-                        have_prev = false;
-                        if (!ok) break;
-                    }
                     const int ks = jk % kNK;
+                    if (jk >= kNK) ok = wait_issuing_v(&sm.k_empty[ks], (uint32_t)(((jk / kNK) & 1) ^ 1));
+                    // the query tile is reloaded once the previous unit's last S is done
+                    if (ok && bi == 0 && units >= 1) ok = wait_issuing_v(&sm.q_empty, (uint32_t)((units - 1) & 1));
+                    if (!ok) break;
                     if (lane == 0) {
-                        if (jk >= kNK) ok = mbar_wait(&sm.k_empty[ks], (uint32_t)(((jk / kNK) & 1) ^ 1), a.err);
-                        // the query tile is reloaded once the previous unit's last S is done
-                        if (ok && bi == 0 && units >= 1)
-                            ok = mbar_wait(&sm.q_empty, (uint32_t)((units - 1) & 1), a.err);
-                        if (ok) {
-                            BlockMeta &m = sm.meta[jk % kNMeta];
-                            m.b = b; m.h = h; m.split = split; m.L = L; m.nsplit = nsplit; m.qb = qb;
-                            m.pos0 = (page0 + i0 + j0) * kBlockSize;
-                            m.ntok = min(kPagesPerBlock, n - (i0 + j0)) * kBlockSize;
-                            m.flags = (bi == 0 ? kFlagFirst : 0) | (bi == nblk - 1 ? kFlagLast : 0);
-                            mbar_arrive_expect_tx(&sm.k_full[ks], kKVTile + (bi == 0 ? qbytes : 0u));
-                            if (bi == 0) {
-                                tma_load_4d(&sm.q[0], &mq0, 0, h * a.G, 0, b, &sm.k_full[ks], pol);
-                                tma_load_4d(&sm.q[kQSlab], &mq1, 0, h * a.G, 0, b, &sm.k_full[ks], pol);
-                            }
+                        BlockMeta &m = sm.meta[jk % kNMeta];
+                        m.b = b; m.h = h; m.split = split; m.L = L; m.nsplit = nsplit; m.qb = 0;
+                        m.pos0 = (page0 + i0 + j0) * kBlockSize;
+                        m.ntok = min(kPagesPerBlock, n - (i0 + j0)) * kBlockSize;
+                        m.flags = (bi == 0 ? kFlagFirst : 0) | (bi == nblk - 1 ? kFlagLast : 0);
+                        mbar_arrive_expect_tx(&sm.k_full[ks], kKVTile + (bi == 0 ? qbytes : 0u));
+                        if (bi == 0) {
+                            tma_load_4d(&sm.q[0], &mq0, 0, h * a.G, 0, b, &sm.k_full[ks], pol);
+                            tma_load_4d(&sm.q[kQSlab], &mq1, 0, h * a.G, 0, b, &sm.k_full[ks], pol);
                         }
                     }
-                    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
-                    if (!ok) break;
                     if (lane < kPagesPerBlock) {
+                        sm.vid[jk % kNMeta][lane] = my_id;
                         uint8_t *sk = sm.kbuf[ks] + lane * 2048;
                         tma_load_4d(sk, &mk0, 0, 0, h, my_id, &sm.k_full[ks], pol);
                         tma_load_4d(sk + kKSlab, &mk1, 0, 0, h, my_id, &sm.k_full[ks], pol);
                     }
+                    __syncwarp();
                     ++jk;
-                    if (have_prev) {
-                        ok = issue_v();
-                        if (!ok) break;
-                    }
-                    have_prev = true;
-                    prev_id = my_id;
-                    prev_h = h;
+                    try_issue_v();
                 }
             }
             ++units;
         }
-        if (ok && have_prev) ok = issue_v();
+        // the V copies still owed
+        while (ok && jv < jk) {
+            if (jv >= kNV) {
+                int good = 1;
+                if (lane == 0) good = mbar_wait(&sm.v_empty[jv % kNV], (uint32_t)(((jv / kNV) & 1) ^ 1), a.err);
+                ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+            }
+            if (ok) try_issue_v();
+        }
         if (lane == 0) {
             // end-of-work marker on the K ring
             const int ks = jk % kNK;
@@ -342,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else {
-        // ================================================= softmax + epilogue
+    } else if (warp < 6) {
+        // ================================================= softmax
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;          // query row == TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -356,7 +387,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (true) {
             if (!mbar_wait(&sm.s_full[j & 1], par_of(j), a.err)) break;
             const BlockMeta md = sm.meta[j % kNMeta];
-            if (md.flags & kFlagEnd) break;
+            if (md.flags & kFlagEnd) {
+                // tell the epilogue warps there is no further unit
+                if (unit >= 0) mbar_wait(&sm.stat_empty, (uint32_t)(unit & 1), a.err);
+                if (threadIdx.x == 64) sm.ep_end = 1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.stat_full);
+                break;
+            }
             if (md.flags & kFlagFirst) {
                 ++unit;
                 m_ref = -CUDART_INF_F;
@@ -443,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int t0 = T - md.pos0;
                 const int nz = (md.ntok - t0) * 2 * 8;
                 uint8_t *sv = sm.vbuf[j % kNV];
-                for (int z = threadIdx.x - 64; z < nz; z += kSoftmaxThreads) {
+                for (int z = threadIdx.x - 64; z < nz; z += 128) {
                     const int row = t0 + z / 16, rem = z % 16;
                     *reinterpret_cast<uint4 *>(sv + (rem >> 3) * kKSlab + row * 128 + ((rem & 7) << 4)) =
                         make_uint4(0, 0, 0, 0);
@@ -479,112 +517,163 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&sm.p_full);
 
             if (md.flags & kFlagLast) {
-                // ---- unit epilogue: O row from TMEM
-                const int ob = unit & 1;
-                mbar_wait(&sm.o_full[ob], par_of(unit), a.err);
-                tc_fence_after();
-                const uint32_t oa = tmem + kTmemO + (uint32_t)ob * kD + lane_off;
-                const int b = md.b, h = md.h;
-                const int u2 = b * a.Hkv + h;
-                const int gi = r - jq * G;
-                const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
-                const size_t pr_own = ((size_t)u2 * a.max_splits + md.split) * a.M + r;
-                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-                // O row streamed out of TMEM 32 columns at a time: final
-                // output when the unit is the whole sequence, else a partial
-#pragma unroll 1
-                for (int c = 0; c < kD / 32; ++c) {
-                    uint32_t raw[32];
-                    tmem_ld32(oa + c * 32, raw);
-                    tmem_ld_wait();
-                    if (live) {
-                        if (md.nsplit == 1) {
-                            uint4 *orow = reinterpret_cast<uint4 *>(a.out + od * kD + c * 32);
-#pragma unroll
-                            for (int c8 = 0; c8 < 4; ++c8) {
-                                uint4 v;
-                                v.x = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 0]) * inv, __uint_as_float(raw[c8 * 8 + 1]) * inv);
-                                v.y = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 2]) * inv, __uint_as_float(raw[c8 * 8 + 3]) * inv);
-                                v.z = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 4]) * inv, __uint_as_float(raw[c8 * 8 + 5]) * inv);
-                                v.w = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 6]) * inv, __uint_as_float(raw[c8 * 8 + 7]) * inv);
-                                orow[c8] = v;
-                            }
-                        } else {
-                            uint4 *prow4 = reinterpret_cast<uint4 *>(a.part_acc + pr_own * kD + c * 32);
-#pragma unroll
-                            for (int c4 = 0; c4 < 8; ++c4)
-                                prow4[c4] = make_uint4(raw[c4 * 4], raw[c4 * 4 + 1], raw[c4 * 4 + 2], raw[c4 * 4 + 3]);
-                        }
-                    }
+                // hand the unit's row statistics to the epilogue warps (one
+                // slot: the previous unit's must have been taken)
+                if (unit >= 1) mbar_wait(&sm.stat_empty, (uint32_t)((unit - 1) & 1), a.err);
+                sm.stat[r] = make_float2(m_ref, l_run);
+                if (threadIdx.x == 64) {
+                    sm.ep_b = md.b;
+                    sm.ep_h = md.h;
+                    sm.ep_split = md.split;
+                    sm.ep_nsplit = md.nsplit;
+                    sm.ep_end = 0;
                 }
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.o_empty[ob]);
-                if (md.nsplit == 1) {
-                    if (live && a.lse) a.lse[od] = (m_ref + __log2f(l_run)) * 0.69314718055994530942f;
-                } else {
-                    if (live) {
-                        a.part_ml[pr_own * 2] = m_ref;
-                        a.part_ml[pr_own * 2 + 1] = l_run;
-                    }
-                    __threadfence();
-                    named_barrier_sync(kBarSoftmax, kSoftmaxThreads);
-                    if (threadIdx.x == 64) {
-                        const int t = atomicAdd(&a.tickets[u2], 1);
-                        sm.last = (t == md.nsplit - 1);
-                        if (sm.last) a.tickets[u2] = 0;
-                    }
-                    named_barrier_sync(kBarSoftmax, kSoftmaxThreads);
-                    const int last = sm.last;
-                    named_barrier_sync(kBarSoftmax, kSoftmaxThreads);
-                    if (last && live) {
-                        // merge every split's partial row (log-sum-exp weights)
-                        __threadfence();
-                        const size_t base = (size_t)u2 * a.max_splits * a.M + r;
-                        float mx2 = -CUDART_INF_F;
-                        for (int s2 = 0; s2 < md.nsplit; ++s2)
-                            mx2 = fmaxf(mx2, __ldcg(&a.part_ml[(base + (size_t)s2 * a.M) * 2]));
-                        const float ms2 = mx2 == -CUDART_INF_F ? 0.f : mx2;
-                        float l2 = 0.f;
-                        for (int s2 = 0; s2 < md.nsplit; ++s2) {
-                            const size_t pr = base + (size_t)s2 * a.M;
-                            l2 += ex2_approx(__ldcg(&a.part_ml[pr * 2]) - ms2) * __ldcg(&a.part_ml[pr * 2 + 1]);
-                        }
-                        const float inv2 = l2 > 0.f ? 1.f / l2 : 0.f;
+                if (lane == 0) mbar_arrive(&sm.stat_full);
+            }
+            ++j;
+        }
+    } else {
+        // ================================================= epilogue
+        // One thread per query row (TMEM lane) streams a finished unit's O
+        // out of TMEM while the softmax warps already work on the next unit
+        // (O is double-buffered in TMEM).
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int G = a.G;
+        const bool live = r < a.M;
+        const int jq = live ? r / G : 0;
+        const int gi = r - jq * G;
+        const int ew = warp - 6;  // 0..3
+        for (int unit = 0;; ++unit) {
+            if (!mbar_wait(&sm.stat_full, (uint32_t)(unit & 1), a.err)) break;
+            if (sm.ep_end) break;
+            const int b = sm.ep_b, h = sm.ep_h, split = sm.ep_split, nsplit = sm.ep_nsplit;
+            const float2 st = sm.stat[r];
+            const float m_ref = st.x, l_run = st.y;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.stat_empty);
+            const int ob = unit & 1;
+            if (!mbar_wait(&sm.o_full[ob], par_of(unit), a.err)) break;
+            tc_fence_after();
+            const uint32_t oa = tmem + kTmemO + (uint32_t)ob * kD + lane_off;
+            const int u2 = b * a.Hkv + h;
+            const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
+            const size_t pr_own = ((size_t)u2 * a.max_splits + split) * a.M + r;
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            // O row streamed out of TMEM 32 columns at a time: final output
+            // when the unit is the whole sequence, else a split partial
 #pragma unroll 1
-                        for (int c = 0; c < kD / 32; ++c) {
-                            float o[32];
+            for (int c = 0; c < kD / 32; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(oa + c * 32, raw);
+                tmem_ld_wait();
+                if (live) {
+                    if (nsplit == 1) {
+                        uint4 *orow = reinterpret_cast<uint4 *>(a.out + od * kD + c * 32);
 #pragma unroll
-                            for (int d = 0; d < 32; ++d) o[d] = 0.f;
-                            for (int s2 = 0; s2 < md.nsplit; ++s2) {
-                                const size_t pr = base + (size_t)s2 * a.M;
-                                const float w = ex2_approx(__ldcg(&a.part_ml[pr * 2]) - ms2);
-                                const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + pr * kD + c * 32);
-#pragma unroll
-                                for (int c4 = 0; c4 < 8; ++c4) {
-                                    const float4 v = __ldcg(src + c4);
-                                    o[c4 * 4] += w * v.x;
-                                    o[c4 * 4 + 1] += w * v.y;
-                                    o[c4 * 4 + 2] += w * v.z;
-                                    o[c4 * 4 + 3] += w * v.w;
-                                }
-                            }
-                            uint4 *orow = reinterpret_cast<uint4 *>(a.out + od * kD + c * 32);
-#pragma unroll
-                            for (int c8 = 0; c8 < 4; ++c8) {
-                                uint4 v;
-                                v.x = pack_bf16x2(o[c8 * 8 + 0] * inv2, o[c8 * 8 + 1] * inv2);
-                                v.y = pack_bf16x2(o[c8 * 8 + 2] * inv2, o[c8 * 8 + 3] * inv2);
-                                v.z = pack_bf16x2(o[c8 * 8 + 4] * inv2, o[c8 * 8 + 5] * inv2);
-                                v.w = pack_bf16x2(o[c8 * 8 + 6] * inv2, o[c8 * 8 + 7] * inv2);
-                                orow[c8] = v;
-                            }
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 0]) * inv, __uint_as_float(raw[c8 * 8 + 1]) * inv);
+                            v.y = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 2]) * inv, __uint_as_float(raw[c8 * 8 + 3]) * inv);
+                            v.z = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 4]) * inv, __uint_as_float(raw[c8 * 8 + 5]) * inv);
+                            v.w = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 6]) * inv, __uint_as_float(raw[c8 * 8 + 7]) * inv);
+                            orow[c8] = v;
                         }
-                        if (a.lse) a.lse[od] = (mx2 + __log2f(l2)) * 0.69314718055994530942f;
+                    } else {
+                        uint4 *prow4 = reinterpret_cast<uint4 *>(a.part_acc + pr_own * kD + c * 32);
+#pragma unroll
+                        for (int c4 = 0; c4 < 8; ++c4)
+                            prow4[c4] = make_uint4(raw[c4 * 4], raw[c4 * 4 + 1], raw[c4 * 4 + 2], raw[c4 * 4 + 3]);
                     }
                 }
             }
-            ++j;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.o_empty[ob]);
+            if (nsplit == 1) {
+                if (live && a.lse) a.lse[od] = (m_ref + __log2f(l_run)) * 0.69314718055994530942f;
+                continue;
+            }
+            if (live) {
+                a.part_ml[pr_own * 2] = m_ref;
+                a.part_ml[pr_own * 2 + 1] = l_run;
+            }
+            __threadfence();
+            named_barrier_sync(kBarEpi, kEpiThreads);
+            if (ew == 0 && lane == 0) {
+                const int t = atomicAdd(&a.tickets[u2], 1);
+                sm.last = (t == nsplit - 1);
+                if (sm.last) a.tickets[u2] = 0;
+            }
+            named_barrier_sync(kBarEpi, kEpiThreads);
+            const int last = sm.last;
+            named_barrier_sync(kBarEpi, kEpiThreads);
+            if (!last) continue;
+            // the last split's CTA merges every split's partial rows with
+            // log-sum-exp weights (an online merge: running maximum, rescaled
+            // sum): one warp per row, 4 columns per lane, four rows and two
+            // splits per pass so that their loads are in flight together
+            __threadfence();
+            const size_t base = (size_t)u2 * a.max_splits * a.M;
+            for (int r0 = ew; r0 < a.M; r0 += 16) {
+                float mrow[4], lrow[4];
+                float4 o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    mrow[i] = -CUDART_INF_F;
+                    lrow[i] = 0.f;
+                    o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                for (int s0 = 0; s0 < nsplit; s0 += 2) {
+                    float2 ml[4][2];
+                    float4 v[4][2];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const int rr = r0 + 4 * i;
+                            if (rr < a.M && s0 + k < nsplit) {
+                                const size_t pr = base + (size_t)(s0 + k) * a.M + rr;
+                                ml[i][k] = __ldcg(reinterpret_cast<const float2 *>(a.part_ml + pr * 2));
+                                v[i][k] = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + pr * kD) + lane);
+                            } else {
+                                ml[i][k] = make_float2(-CUDART_INF_F, 0.f);
+                                v[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                        }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const float mk = ml[i][k].x;
+                            if (mk == -CUDART_INF_F) continue;  // an empty split (or none)
+                            const float mn = fmaxf(mrow[i], mk);
+                            const float f_old = ex2_approx(mrow[i] - mn);  // 0 when mrow is -inf
+                            const float f_new = ex2_approx(mk - mn);
+                            lrow[i] = lrow[i] * f_old + ml[i][k].y * f_new;
+                            o[i].x = o[i].x * f_old + v[i][k].x * f_new;
+                            o[i].y = o[i].y * f_old + v[i][k].y * f_new;
+                            o[i].z = o[i].z * f_old + v[i][k].z * f_new;
+                            o[i].w = o[i].w * f_old + v[i][k].w * f_new;
+                            mrow[i] = mn;
+                        }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = r0 + 4 * i;
+                    if (rr >= a.M) break;
+                    const float inv2 = lrow[i] > 0.f ? 1.f / lrow[i] : 0.f;
+                    const int jq2 = rr / G, gi2 = rr - jq2 * G;
+                    const size_t od2 = (((size_t)b * a.n_q + jq2) * a.Hq + (size_t)h * G + gi2);
+                    uint2 v2;
+                    v2.x = pack_bf16x2(o[i].x * inv2, o[i].y * inv2);
+                    v2.y = pack_bf16x2(o[i].z * inv2, o[i].w * inv2);
+                    reinterpret_cast<uint2 *>(a.out + od2 * kD)[lane] = v2;
+                    if (lane == 0 && a.lse) a.lse[od2] = (mrow[i] + __log2f(lrow[i])) * 0.69314718055994530942f;
+                }
+            }
         }
     }
     // every TMEM user is done (the MMA issuer's last operations were waited

@@ -210,7 +210,8 @@ constexpr int kClThreads = kClWarps * 32;
 constexpr int kClMaxCtas = 8;
 constexpr int kStep = 128;
 constexpr int kClMaxSteps = 32;
-constexpr int kLoadBatch = 8;
+constexpr int kLoadBatch = 4;
+constexpr int kClCtasPerSm = 4;  // resident CTAs per SM the kernels are built for
 constexpr int kClMaxVocab = kClMaxCtas * kClWarps * kClMaxSteps * kStep;  // 262144
 
 enum : int { kDrawFound = 0, kDrawPastEnd = 1, kDrawNoMass = 2 };
@@ -218,6 +219,16 @@ enum : int { kDrawFound = 0, kDrawPastEnd = 1, kDrawNoMass = 2 };
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// This CTA's slice of a row, fetched into L2 by the bulk-copy engine: one
+// request for the whole slice, so the loads that follow find their lines in
+// flight instead of each warp's misses queueing in L1.  Rows that are not
+// 16-byte aligned (or V % 4 != 0) are left to the plain loads.
+__device__ __forceinline__ void prefetch_slice(const float *row, int lo, int hi, bool vec) {
+    if (!row || !vec || hi <= lo) return;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row + lo), "r"((uint32_t)(hi - lo) * 4u)
+                 : "memory");
 }
 
 __device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
@@ -548,7 +559,7 @@ __device__ __forceinline__ ClusterGeom cluster_geom(int V, int n_ctas) {
 
 // ---------------------------------------------------------------- linear, cluster per row
 template <int NI>
-__global__ void __launch_bounds__(kClThreads, 2)
+__global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     spec_accept_cluster_kernel(const __grid_constant__ AcceptArgs a, int n_ctas) {
     __shared__ ClusterRow<NI> st;
     __shared__ int s_k;
@@ -585,6 +596,10 @@ __global__ void __launch_bounds__(kClThreads, 2)
                      (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
     SrcGlobal src{a.p + ((size_t)b * (gamma + 1) + k) * V, k < gamma ? a.q + ((size_t)b * gamma + k) * V : nullptr,
                   V, vec};
+    if (threadIdx.x == 0) {
+        prefetch_slice(src.p, g.cta_lo, g.cta_hi, vec);
+        prefetch_slice(src.q, g.cta_lo, g.cta_hi, vec);
+    }
     double S = cluster_sum(st, src, g, 0);
     if (!(S > 0.0) && src.q) {
         // empty residual: draw from the target row instead (S is the same in
@@ -625,7 +640,7 @@ __global__ void __launch_bounds__(kClThreads, 2)
 // each CTA's shared memory; R(x) for the next sibling is published by the
 // CTA that owns x along with the slice sums.
 template <int NI>
-__global__ void __launch_bounds__(kClThreads, 2)
+__global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     spec_accept_tree_cluster_kernel(const __grid_constant__ TreeArgs a, int n_ctas) {
     extern __shared__ float4 dyn_smem[];
     float *R = reinterpret_cast<float *>(dyn_smem);  // this CTA's residual slice
@@ -637,15 +652,22 @@ __global__ void __launch_bounds__(kClThreads, 2)
     const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.p) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
     const bool lead = g.rank == 0 && threadIdx.x == 0;
-    auto token_of = [&](int node) {
-        int x = ntok[node];
+    // the row's node tokens and uniforms, and per child of the node being
+    // visited Q(x_c) and P(x_c) (each node is some node's child at most once,
+    // so no entry is rewritten)
+    __shared__ int s_x[kMaxNq];
+    __shared__ float s_ua[kMaxNq], s_qx[kMaxNq], s_px[kMaxNq];
+    if (threadIdx.x < (unsigned)n_nodes) {
+        int x = ntok[threadIdx.x];
         if (x < 0 || x >= V) {
-            if (lead) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+            if (g.rank == 0 && threadIdx.x > 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
             x = 0;
         }
-        return x;
-    };
+        s_x[threadIdx.x] = x;
+        s_ua[threadIdx.x] = __ldg(a.u_acc + (size_t)b * n_nodes + threadIdx.x);
+    }
     const float u_s = __ldg(a.u_s + b);
+    __syncthreads();
     int node = 0, depth = 0, parity = 0;
     bool near = false;
     int tok = -1;
@@ -653,6 +675,10 @@ __global__ void __launch_bounds__(kClThreads, 2)
     while (true) {
         const float *Pn = a.p + ((size_t)b * n_nodes + node) * V;
         const int qr = a.qrow[node];
+        if (threadIdx.x == 0) {  // this node's rows, while the acceptance tests run
+            prefetch_slice(Pn, g.cta_lo, g.cta_hi, vec);
+            if (qr >= 0) prefetch_slice(a.q + ((size_t)b * a.n_internal + qr) * V, g.cta_lo, g.cta_hi, vec);
+        }
         if (qr < 0) {  // leaf: bonus token from its own P
             const SrcGlobal src{Pn, nullptr, V, vec};
             cluster_sum(st, src, g, parity);
@@ -663,18 +689,25 @@ __global__ void __launch_bounds__(kClThreads, 2)
             break;
         }
         const float *Qn = a.q + ((size_t)b * a.n_internal + qr) * V;
+        {
+            const int c = node + 1 + (int)threadIdx.x;
+            if (c < n_nodes && a.parent[c] == node) {
+                s_qx[c] = __ldg(Qn + s_x[c]);
+                s_px[c] = __ldg(Pn + s_x[c]);
+            }
+            __syncthreads();
+        }
         double Z = 1.0;
         float rx = 0.f;  // R(x) of the child under test, after a rejection
         int accepted = -1, tested = 0;
         for (int c = node + 1; c < n_nodes; ++c) {
             if (a.parent[c] != node) continue;
-            const int x = token_of(c);
-            const float u = __ldg(a.u_acc + (size_t)b * n_nodes + c);
+            const float u = s_ua[c];
             bool ok;
             if (tested == 0) {
-                ok = __fmul_rn(u, __ldg(Qn + x)) <= __ldg(Pn + x);
+                ok = __fmul_rn(u, s_qx[c]) <= s_px[c];
             } else {
-                const double lhs = (double)u * (double)__ldg(Qn + x) * Z;
+                const double lhs = (double)u * (double)s_qx[c] * Z;
                 ok = lhs <= (double)rx;
                 if (Z > 0.0 && fabs(lhs - (double)rx) / Z < kNearBand) near = true;
             }
@@ -685,7 +718,7 @@ __global__ void __launch_bounds__(kClThreads, 2)
             int xn = -1;  // the next sibling's token: R is probed there
             for (int c2 = c + 1; c2 < n_nodes; ++c2)
                 if (a.parent[c2] == node) {
-                    xn = token_of(c2);
+                    xn = s_x[c2];
                     break;
                 }
             const SrcUpdate upd{R, tested == 0 ? Pn : nullptr, Qn, g.cta_lo, V, (float)Z, vec};
@@ -698,7 +731,7 @@ __global__ void __launch_bounds__(kClThreads, 2)
             ++depth;
             if (lead) {
                 a.path_nodes[(size_t)b * a.width + depth] = accepted;
-                a.out_tokens[(size_t)b * a.width + depth - 1] = ntok[accepted];
+                a.out_tokens[(size_t)b * a.width + depth - 1] = s_x[accepted];
             }
             node = accepted;
             continue;
@@ -736,20 +769,39 @@ __global__ void __launch_bounds__(kClThreads, 2)
     cluster_sync_all();
 }
 
-// Steps per warp for a V-token row (a power of two), or 0 when V is beyond
-// the cluster kernels.
-int cluster_steps(int V) {
+int sm_count_cached() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+            n = v;
+        else
+            return 152;
+    }
+    return n;
+}
+
+// Steps per warp (a power of two) for B rows of V tokens, or 0 when V is
+// beyond the cluster kernels: the fewest steps that cover a row with 8 CTAs,
+// then more steps (fewer CTAs per row) while the grid would not be resident
+// in one wave.  Depends on (B, V) only, so both samplers split a row alike.
+int cluster_steps(int B, int V) {
     constexpr int per_step_row = kClWarps * kStep * kClMaxCtas;
     const int need = (V + per_step_row - 1) / per_step_row;
     int ni = 1;
     while (ni < need) ni <<= 1;
-    return ni <= kClMaxSteps ? ni : 0;
+    if (ni > kClMaxSteps) return 0;
+    const long long slots = (long long)sm_count_cached() * kClCtasPerSm;
+    auto ctas = [&](int n) { return (V + kClWarps * n * kStep - 1) / (kClWarps * n * kStep); };
+    while (ni < kClMaxSteps && ctas(ni) > 1 && (long long)B * ctas(ni) > slots) ni <<= 1;
+    return ni;
 }
 
 template <class Args>
 cudaError_t launch_cluster(void (*const *kernels)(Args, int), const Args &a, int V, int B, size_t dyn_smem_per_step,
                            cudaStream_t stream) {
-    const int ni = cluster_steps(V);
+    const int ni = cluster_steps(B, V);
     const int chunk = kClWarps * ni * kStep;
     const int n = (V + chunk - 1) / chunk;
     int idx = 0;
@@ -779,7 +831,7 @@ cudaError_t launch_cluster(void (*const *kernels)(Args, int), const Args &a, int
 
 cudaError_t launch_spec_accept(const AcceptArgs &a, cudaStream_t stream) {
     if (a.B <= 0) return cudaSuccess;
-    if (cluster_steps(a.V) == 0 || (long long)a.B * kClMaxCtas > 0x7fffffffLL) {
+    if (cluster_steps(a.B, a.V) == 0 || (long long)a.B * kClMaxCtas > 0x7fffffffLL) {
         spec_accept_kernel<<<a.B, kRowThreads, 0, stream>>>(a);
         return cudaGetLastError();
     }
@@ -793,7 +845,7 @@ int spec_accept_tree_max_vocab() { return kClMaxVocab; }
 
 cudaError_t launch_spec_accept_tree(const TreeArgs &a, cudaStream_t stream) {
     if (a.B <= 0) return cudaSuccess;
-    if (cluster_steps(a.V) == 0) return cudaErrorInvalidValue;
+    if (cluster_steps(a.B, a.V) == 0) return cudaErrorInvalidValue;
     static void (*const kernels[])(TreeArgs, int) = {
         spec_accept_tree_cluster_kernel<1>, spec_accept_tree_cluster_kernel<2>,
         spec_accept_tree_cluster_kernel<4>, spec_accept_tree_cluster_kernel<8>,
