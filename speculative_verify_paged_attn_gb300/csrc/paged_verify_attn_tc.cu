@@ -96,7 +96,7 @@ __device__ __forceinline__ uint32_t par_of(int idx) { return (uint32_t)((idx >> 
 
 __global__ void __launch_bounds__(kThreads, 1)
     pva_tc_kernel(const __grid_constant__ CUtensorMap mk0, const __grid_constant__ CUtensorMap mk1,
-                  const __grid_constant__ CUtensorMap mv0, const __grid_constant__ CUtensorMap mv1,
+                  const __grid_constant__ CUtensorMap mvp,
                   const __grid_constant__ CUtensorMap mq0, const __grid_constant__ CUtensorMap mq1,
                   const __grid_constant__ AttnArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -143,8 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tensormap(&mk0);
             prefetch_tensormap(&mk1);
-            prefetch_tensormap(&mv0);
-            prefetch_tensormap(&mv1);
+            prefetch_tensormap(&mvp);
             prefetch_tensormap(&mq0);
             prefetch_tensormap(&mq1);
         }
@@ -163,9 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[vs], kKVTile);
             if (lane < kPagesPerBlock) {
                 const int id = sm.vid[jv % kNMeta][lane], hh = sm.meta[jv % kNMeta].h;
-                uint8_t *sv = sm.vbuf[vs] + lane * 2048;
-                tma_load_4d(sv, &mv0, 0, 0, hh, id, &sm.v_full[vs], pol);
-                tma_load_4d(sv + kKSlab, &mv1, 0, 0, hh, id, &sm.v_full[vs], pol);
+                tma_load_5d(sm.vbuf[vs] + lane * 4096, &mvp, 0, 0, 0, hh, id, &sm.v_full[vs], pol);
             }
             __syncwarp();
             ++jv;
@@ -353,11 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!next_done && j >= 1 && !mbar_wait(&sm.p_empty, (uint32_t)((j - 1) & 1), a.err)) break;
                 tc_fence_after();
                 const uint32_t pt = tmem + kTmemS + (uint32_t)(j & 1) * kNB;  // P_j (bf16 pairs)
+                // V_j: page kt at kt * 4 KB as [slab][16 rows][128 B]; one MMA per page
                 const uint32_t va = smem_u32(sm.vbuf[vs]);
                 const uint32_t dO = tmem + kTmemO + (uint32_t)ob * kD;
 #pragma unroll
                 for (int kt = 0; kt < kNB / 16; ++kt) {
-                    const uint64_t bd = umma_desc_sw128(va + kt * 2048, kKSlab, 1024);
+                    const uint64_t bd = umma_desc_sw128(va + kt * 4096, 2048, 1024);
                     umma_bf16_tmem_a(dO, pt + kt * 8, bd, idPV, ((cur.flags & kFlagFirst) && kt == 0) ? 0u : 1u);
                 }
                 umma_commit(&sm.v_empty[vs]);
@@ -483,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *sv = sm.vbuf[j % kNV];
                 for (int z = threadIdx.x - 64; z < nz; z += 128) {
                     const int row = t0 + z / 16, rem = z % 16;
-                    *reinterpret_cast<uint4 *>(sv + (rem >> 3) * kKSlab + row * 128 + ((rem & 7) << 4)) =
-                        make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(sv + (row >> 4) * 4096 + (rem >> 3) * 2048 + (row & 15) * 128 +
+                                               ((rem & 7) << 4)) = make_uint4(0, 0, 0, 0);
                 }
             }
             // TMEM loads and stores are warp-collective: the whole warp takes
@@ -692,7 +690,7 @@ cudaError_t launch_paged_verify_attn_tc(const AttnMaps &m, const AttnArgs &a, in
     const size_t smem = attn_tc_smem_bytes();
     cudaError_t e = cudaFuncSetAttribute(pva_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    pva_tc_kernel<<<grid, kThreads, smem, st>>>(m.k[0], m.k[1], m.v[0], m.v[1], m.q[0], m.q[1], a);
+    pva_tc_kernel<<<grid, kThreads, smem, st>>>(m.k[0], m.k[1], m.vpage, m.q[0], m.q[1], a);
     return cudaGetLastError();
 }
 

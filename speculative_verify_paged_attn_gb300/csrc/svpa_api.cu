@@ -200,6 +200,19 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
             return SVPA_ERR_CUDA;
     }
 
+    if (pl.use_tc) {
+        // one (page, kv head) V tile per copy: dims (64 columns, 16 rows, 2
+        // column slabs, kv heads, blocks), landing as [slab][row][128 B]
+        const cuuint64_t vd[5] = {64, 16, 2, (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->num_blocks};
+        const cuuint64_t vs[4] = {(cuuint64_t)D * 2, 128, (cuuint64_t)16 * D * 2,
+                                  (cuuint64_t)p->num_kv_heads * 16 * D * 2};
+        const cuuint32_t vbox[5] = {64, 16, 2, 1, 1};
+        const cuuint32_t es5[5] = {1, 1, 1, 1, 1};
+        if (enc(&maps.vpage, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(v_pool), vd, vs, vbox, es5,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return SVPA_ERR_CUDA;
+    }
     {
         // queries [B, n_q, Hq, D] bf16: box = (64 columns, G heads, n_q queries, 1)
         const int G = p->num_q_heads / p->num_kv_heads;

@@ -39,6 +39,7 @@ struct AttnMaps {
     CUtensorMap k[2];     // 128-byte column slabs of the K pages
     CUtensorMap v[2];
     CUtensorMap q[2];     // 128-byte column slabs of the queries of one (sequence, kv head)
+    CUtensorMap vpage;    // a whole bf16 (page, kv head) tile, both slabs in one box
 };
 
 struct AttnLaunch {
