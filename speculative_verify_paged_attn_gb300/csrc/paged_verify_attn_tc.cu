@@ -45,8 +45,7 @@ constexpr int kD = 128;
 constexpr int kPagesPerBlock = 8;
 constexpr int kNB = kPagesPerBlock * 16;       // tokens per block (128)
 constexpr int kRows = 128;                      // MMA M
-constexpr int kKSlab = kNB * 128;               // one 128-byte column slab of a K (or V) block
-constexpr int kKVTile = 2 * kKSlab;             // K (or V) block, 128 columns
+constexpr int kKVTile = kNB * 256;              // K (or V) block: 8 pages of 4 KB
 constexpr int kQSlab = kRows * 128;
 constexpr int kQBuf = 2 * kQSlab;
 constexpr int kNK = 3;                          // K ring (freed once S_j is computed)
@@ -95,8 +94,7 @@ static_assert(sizeof(Smem) + 1024 <= 232448, "pva_tc_kernel shared memory");
 __device__ __forceinline__ uint32_t par_of(int idx) { return (uint32_t)((idx >> 1) & 1); }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    pva_tc_kernel(const __grid_constant__ CUtensorMap mk0, const __grid_constant__ CUtensorMap mk1,
-                  const __grid_constant__ CUtensorMap mvp,
+    pva_tc_kernel(const __grid_constant__ CUtensorMap mkp, const __grid_constant__ CUtensorMap mvp,
                   const __grid_constant__ CUtensorMap mq0, const __grid_constant__ CUtensorMap mq1,
                   const __grid_constant__ AttnArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -141,8 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================================================= producer
         const uint64_t pol = policy_evict_first();
         if (lane == 0) {
-            prefetch_tensormap(&mk0);
-            prefetch_tensormap(&mk1);
+            prefetch_tensormap(&mkp);
             prefetch_tensormap(&mvp);
             prefetch_tensormap(&mq0);
             prefetch_tensormap(&mq1);
@@ -162,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[vs], kKVTile);
             if (lane < kPagesPerBlock) {
                 const int id = sm.vid[jv % kNMeta][lane], hh = sm.meta[jv % kNMeta].h;
-                tma_load_5d(sm.vbuf[vs] + lane * 4096, &mvp, 0, 0, 0, hh, id, &sm.v_full[vs], pol);
+                tma_load_5d(sm.vbuf[vs] + lane * 4096, &mvp, 0, 0, 0, 0, id * a.Hkv + hh, &sm.v_full[vs], pol);
             }
             __syncwarp();
             ++jv;
@@ -246,9 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (lane < kPagesPerBlock) {
                         sm.vid[jk % kNMeta][lane] = my_id;
-                        uint8_t *sk = sm.kbuf[ks] + lane * 2048;
-                        tma_load_4d(sk, &mk0, 0, 0, h, my_id, &sm.k_full[ks], pol);
-                        tma_load_4d(sk + kKSlab, &mk1, 0, 0, h, my_id, &sm.k_full[ks], pol);
+                        tma_load_5d(sm.kbuf[ks] + lane * 4096, &mkp, 0, 0, 0, 0, my_id * a.Hkv + h, &sm.k_full[ks],
+                                    pol);
                     }
                     __syncwarp();
                     ++jk;
@@ -317,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint64_t ad = umma_desc_sw128(qa + (kk >> 2) * kQSlab + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = umma_desc_sw128(ka + (kk >> 2) * kKSlab + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = umma_desc_sw128(ka + (kk >> 2) * 1024 + (kk & 3) * 32, 16, 2048);
                     umma_bf16(dS, ad, bd, idS, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&sm.k_empty[ks]);
@@ -350,12 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!next_done && j >= 1 && !mbar_wait(&sm.p_empty, (uint32_t)((j - 1) & 1), a.err)) break;
                 tc_fence_after();
                 const uint32_t pt = tmem + kTmemS + (uint32_t)(j & 1) * kNB;  // P_j (bf16 pairs)
-                // V_j: page kt at kt * 4 KB as [slab][16 rows][128 B]; one MMA per page
+                // V_j: page kt at kt * 4 KB as [row half][slab][8 rows][128 B]; one
+                // MMA per page
                 const uint32_t va = smem_u32(sm.vbuf[vs]);
                 const uint32_t dO = tmem + kTmemO + (uint32_t)ob * kD;
 #pragma unroll
                 for (int kt = 0; kt < kNB / 16; ++kt) {
-                    const uint64_t bd = umma_desc_sw128(va + kt * 4096, 2048, 1024);
+                    const uint64_t bd = umma_desc_sw128(va + kt * 4096, 1024, 2048);
                     umma_bf16_tmem_a(dO, pt + kt * 8, bd, idPV, ((cur.flags & kFlagFirst) && kt == 0) ? 0u : 1u);
                 }
                 umma_commit(&sm.v_empty[vs]);
@@ -481,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *sv = sm.vbuf[j % kNV];
                 for (int z = threadIdx.x - 64; z < nz; z += 128) {
                     const int row = t0 + z / 16, rem = z % 16;
-                    *reinterpret_cast<uint4 *>(sv + (row >> 4) * 4096 + (rem >> 3) * 2048 + (row & 15) * 128 +
+                    *reinterpret_cast<uint4 *>(sv + (row >> 3) * 2048 + (rem >> 3) * 1024 + (row & 7) * 128 +
                                                ((rem & 7) << 4)) = make_uint4(0, 0, 0, 0);
                 }
             }
@@ -690,7 +687,7 @@ cudaError_t launch_paged_verify_attn_tc(const AttnMaps &m, const AttnArgs &a, in
     const size_t smem = attn_tc_smem_bytes();
     cudaError_t e = cudaFuncSetAttribute(pva_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    pva_tc_kernel<<<grid, kThreads, smem, st>>>(m.k[0], m.k[1], m.vpage, m.q[0], m.q[1], a);
+    pva_tc_kernel<<<grid, kThreads, smem, st>>>(m.kpage, m.vpage, m.q[0], m.q[1], a);
     return cudaGetLastError();
 }
 

@@ -201,14 +201,19 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
     }
 
     if (pl.use_tc) {
-        // one (page, kv head) V tile per copy: dims (64 columns, 16 rows, 2
-        // column slabs, kv heads, blocks), landing as [slab][row][128 B]
-        const cuuint64_t vd[5] = {64, 16, 2, (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->num_blocks};
-        const cuuint64_t vs[4] = {(cuuint64_t)D * 2, 128, (cuuint64_t)16 * D * 2,
-                                  (cuuint64_t)p->num_kv_heads * 16 * D * 2};
-        const cuuint32_t vbox[5] = {64, 16, 2, 1, 1};
+        // one (page, kv head) tile per copy: dims (64 columns, 8 rows, 2 column
+        // slabs, 2 row halves, kv head x block), landing as
+        // [row half][slab][8 rows][128 B] -- 1 KB swizzle atoms with a uniform
+        // 2 KB stride between 8-row groups across the pages of a block
+        const cuuint64_t pd[5] = {64, 8, 2, 2, (cuuint64_t)p->num_kv_heads * p->num_blocks};
+        const cuuint64_t ps[4] = {(cuuint64_t)D * 2, 128, (cuuint64_t)8 * D * 2, (cuuint64_t)16 * D * 2};
+        const cuuint32_t pbox[5] = {64, 8, 2, 2, 1};
         const cuuint32_t es5[5] = {1, 1, 1, 1, 1};
-        if (enc(&maps.vpage, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(v_pool), vd, vs, vbox, es5,
+        if (enc(&maps.kpage, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(k_pool), pd, ps, pbox, es5,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return SVPA_ERR_CUDA;
+        if (enc(&maps.vpage, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(v_pool), pd, ps, pbox, es5,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return SVPA_ERR_CUDA;

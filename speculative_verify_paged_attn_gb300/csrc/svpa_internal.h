@@ -39,7 +39,8 @@ struct AttnMaps {
     CUtensorMap k[2];     // 128-byte column slabs of the K pages
     CUtensorMap v[2];
     CUtensorMap q[2];     // 128-byte column slabs of the queries of one (sequence, kv head)
-    CUtensorMap vpage;    // a whole bf16 (page, kv head) tile, both slabs in one box
+    CUtensorMap kpage;    // a whole bf16 (page, kv head) tile in one box (tcgen05 kernel)
+    CUtensorMap vpage;
 };
 
 struct AttnLaunch {
