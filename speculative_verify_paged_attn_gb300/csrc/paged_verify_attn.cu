@@ -173,10 +173,6 @@ __global__ void __launch_bounds__((MT + 1) * 32, Occ<MT>::MINB)
             prefetch_tensormap(&mk0);
             prefetch_tensormap(&mv0);
             prefetch_tensormap(&mq0);
-            if constexpr (G_::SLABS > 1) {
-                prefetch_tensormap(&mk1);
-                prefetch_tensormap(&mv1);
-            }
             if constexpr (G_::QSLABS > 1) prefetch_tensormap(&mq1);
         }
         int slot = 0, issued = 0, units = 0;
@@ -239,11 +235,13 @@ __global__ void __launch_bounds__((MT + 1) * 32, Occ<MT>::MINB)
                                 if constexpr (G_::QSLABS > 1)
                                     tma_load_4d(qd + QSLAB, &mq1, 0, h * a.G, 0, b, &full[slot], pol);
                             }
-                            tma_load_4d(st, &mk0, 0, 0, h, bj, &full[slot], pol);
-                            tma_load_4d(st + G_::TILE, &mv0, 0, 0, h, bj, &full[slot], pol);
                             if constexpr (G_::SLABS > 1) {
-                                tma_load_4d(st + 2048, &mk1, 0, 0, h, bj, &full[slot], pol);
-                                tma_load_4d(st + G_::TILE + 2048, &mv1, 0, 0, h, bj, &full[slot], pol);
+                                // both slabs of the page in one copy (5-D box)
+                                tma_load_5d(st, &mk0, 0, 0, 0, h, bj, &full[slot], pol);
+                                tma_load_5d(st + G_::TILE, &mv0, 0, 0, 0, h, bj, &full[slot], pol);
+                            } else {
+                                tma_load_4d(st, &mk0, 0, 0, h, bj, &full[slot], pol);
+                                tma_load_4d(st + G_::TILE, &mv0, 0, 0, h, bj, &full[slot], pol);
                             }
                         }
                     }
@@ -598,7 +596,10 @@ cudaError_t plan_mt(AttnLaunch *out) {
 template <int D, bool FP8, int MT>
 cudaError_t launch_mt(const AttnMaps &m, const AttnArgs &a, int grid, size_t smem, cudaStream_t st) {
     constexpr int THREADS = (MT + 1) * 32;
-    pva_kernel<D, FP8, MT><<<grid, THREADS, smem, st>>>(m.k[0], m.k[1], m.v[0], m.v[1], m.q[0], m.q[1], a);
+    // D 128 bf16 pages travel as one 5-D box per page (the slab maps are unused)
+    const bool whole = D * (FP8 ? 1 : 2) > 128;
+    pva_kernel<D, FP8, MT><<<grid, THREADS, smem, st>>>(whole ? m.kslabs : m.k[0], m.k[1], whole ? m.vslabs : m.v[0],
+                                                         m.v[1], m.q[0], m.q[1], a);
     return cudaGetLastError();
 }
 

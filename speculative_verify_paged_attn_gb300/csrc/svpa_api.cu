@@ -218,6 +218,23 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return SVPA_ERR_CUDA;
     }
+    if (!pl.use_tc && !fp8 && D == 128) {
+        // warp-MMA kernel: one (page, kv head) tile per copy, landing as
+        // [slab][16 rows][128 B] (dims 64 columns, 16 rows, 2 slabs, kv heads, blocks)
+        const cuuint64_t sd[5] = {64, 16, 2, (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->num_blocks};
+        const cuuint64_t ss[4] = {(cuuint64_t)D * 2, 128, (cuuint64_t)16 * D * 2,
+                                  (cuuint64_t)p->num_kv_heads * 16 * D * 2};
+        const cuuint32_t sbox[5] = {64, 16, 2, 1, 1};
+        const cuuint32_t es5[5] = {1, 1, 1, 1, 1};
+        if (enc(&maps.kslabs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(k_pool), sd, ss, sbox, es5,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return SVPA_ERR_CUDA;
+        if (enc(&maps.vslabs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(v_pool), sd, ss, sbox, es5,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return SVPA_ERR_CUDA;
+    }
     {
         // queries [B, n_q, Hq, D] bf16: box = (64 columns, G heads, n_q queries, 1)
         const int G = p->num_q_heads / p->num_kv_heads;

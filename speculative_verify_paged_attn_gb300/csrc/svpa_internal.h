@@ -41,6 +41,8 @@ struct AttnMaps {
     CUtensorMap q[2];     // 128-byte column slabs of the queries of one (sequence, kv head)
     CUtensorMap kpage;    // a whole bf16 (page, kv head) tile in one box (tcgen05 kernel)
     CUtensorMap vpage;
+    CUtensorMap kslabs;   // a whole bf16 D-128 (page, kv head) tile in one box, as [slab][16 rows]
+    CUtensorMap vslabs;
 };
 
 struct AttnLaunch {
