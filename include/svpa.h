@@ -85,8 +85,8 @@ typedef struct svpa_attn_params {
     float sm_scale;             /* softmax scale, normally 1/sqrt(D)          */
     int32_t split_pages;        /* pages per KV split; 0 = chosen by library  */
     int32_t variant;            /* 0 = chosen by library; 1 = warp-level MMA
-                                   kernel; 2 = tcgen05/TMEM kernel (bf16,
-                                   head_dim 128)                               */
+                                   kernel; 2 = tcgen05/TMEM kernel (head_dim
+                                   128; FP8 pages with Hq / Hkv * n_q <= 64)   */
 } svpa_attn_params;
 
 /* Bytes of workspace svpa_paged_verify_attn needs for `p` (split-KV partial
@@ -129,7 +129,12 @@ svpa_status svpa_attn_workspace_size(const svpa_attn_params *p, size_t *bytes);
  *  out          bf16 [B, n_q, Hq, D] (written)
  *  lse          fp32 [B, n_q, Hq] natural-log sum of exp(scores), or NULL
  *  workspace    device scratch of at least svpa_attn_workspace_size() bytes
- * Accumulation is fp32; the contraction runs on the tensor cores.
+ * Accumulation is fp32; the contraction runs on the tensor cores.  On the
+ * tcgen05 kernel FP8 pages are dequantised to f16 (the page's scale folded
+ * in) and the queries and P are f16: there a K or V scale above 146 (448 *
+ * scale would pass the f16 maximum) or a negative/NaN scale raises
+ * SVPA_DEVERR_BAD_VALUE, and |q| must stay below 65504; the warp-level
+ * kernel (variant 1) applies the scales in fp32 and has neither limit.
  */
 svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q,
                                    const void *k_pool, const void *v_pool,

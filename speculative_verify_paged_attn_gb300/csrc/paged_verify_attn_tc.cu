@@ -34,6 +34,9 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <algorithm>
+#include <type_traits>
+
 #include "svpa_device.cuh"
 #include "svpa_internal.h"
 
@@ -48,12 +51,34 @@ constexpr int kRows = 128;                      // MMA M
 constexpr int kKVTile = kNB * 256;              // K (or V) block: 8 pages of 4 KB
 constexpr int kQSlab = kRows * 128;
 constexpr int kQBuf = 2 * kQSlab;
-constexpr int kNK = 3;                          // K ring (freed once S_j is computed)
-constexpr int kNV = 3;                          // V ring (freed once PV_j is computed)
 constexpr int kNMeta = 8;                       // block descriptors in flight
-constexpr int kThreads = 320;
-constexpr int kEpiThreads = 128;
 constexpr int kBarEpi = 1;                      // named barrier of the epilogue warps
+constexpr int kPage8 = 16 * 128;                // one FP8 (page, kv head) tile
+constexpr int kTile8 = kPagesPerBlock * kPage8;  // FP8 K (or V) block: 16 KB
+constexpr float kMaxScale8 = 146.f;             // 448 * scale stays below the f16 maximum
+
+// Two layouts of the same kernel.
+//  bf16 pages: warps 0 producer, 1 MMA, 2-5 softmax, 6-9 epilogue; 3-deep K
+//    and V rings of bf16 blocks that the MMA reads directly.
+//  FP8 pages (at most 64 query rows, so two TMEM lane quadrants): warps 0
+//    producer, 1 MMA, 4-5 softmax, 8-9 epilogue, 2/3/10 K converters, 6/7/11
+//    V converters; the producer streams E4M3 pages into 4-deep staging rings,
+//    the converters turn each block into f16 (the page's scale folded in) in
+//    a single K and a single V tile, and the MMAs run kind::f16 with f16
+//    queries (converted in place) and f16 P.
+template <bool FP8>
+struct TcCfg {
+    static constexpr int kThreads = FP8 ? 384 : 320;
+    static constexpr int kNK = FP8 ? 1 : 3;     // tiles the MMA reads (K freed once S_j is done)
+    static constexpr int kNV = FP8 ? 1 : 3;     // (V freed once PV_j is done)
+    static constexpr int kNK8 = FP8 ? 4 : 1;    // FP8 staging rings
+    static constexpr int kNV8 = FP8 ? 4 : 1;
+    static constexpr int kSoftmaxWarp0 = FP8 ? 4 : 2;
+    static constexpr int kSoftmaxWarps = FP8 ? 2 : 4;
+    static constexpr int kEpiWarp0 = FP8 ? 8 : 6;
+    static constexpr int kEpiWarps = FP8 ? 2 : 4;
+    static constexpr int kConvWarps = 3;        // per operand (FP8 only)
+};
 constexpr float kRescaleLog2 = 8.f;             // rescale O when a maximum grows by > 2^8
 
 // TMEM columns: O[0] 0..127, O[1] 128..255, S[0] 256..383, S[1] 384..511; the
@@ -69,12 +94,25 @@ struct BlockMeta {
     int32_t pad[3];
 };
 
+template <bool FP8>
+struct Stage8 {  // FP8 staging rings
+    uint8_t k8[TcCfg<FP8>::kNK8][kTile8];
+    uint8_t v8[TcCfg<FP8>::kNV8][kTile8];
+    uint64_t k8_full[TcCfg<FP8>::kNK8], k8_empty[TcCfg<FP8>::kNK8];
+    uint64_t v8_full[TcCfg<FP8>::kNV8], v8_empty[TcCfg<FP8>::kNV8];
+    uint64_t q_full;
+};
+struct NoStage8 {};
+
+template <bool FP8>
 struct Smem {
+    using C = TcCfg<FP8>;
     uint8_t q[kQBuf];                    // 32 KB, 1024-aligned (one unit's queries)
-    uint8_t kbuf[kNK][kKVTile];          // 3 x 32 KB
-    uint8_t vbuf[kNV][kKVTile];          // 3 x 32 KB
-    uint64_t k_full[kNK], k_empty[kNK];
-    uint64_t v_full[kNV], v_empty[kNV];
+    uint8_t kbuf[C::kNK][kKVTile];       // 32 KB each
+    uint8_t vbuf[C::kNV][kKVTile];
+    typename std::conditional<FP8, Stage8<FP8>, NoStage8>::type st8;
+    uint64_t k_full[C::kNK], k_empty[C::kNK];
+    uint64_t v_full[C::kNV], v_empty[C::kNV];
     uint64_t q_empty;
     uint64_t s_full[2];
     uint64_t p_full, p_empty;
@@ -89,37 +127,71 @@ struct Smem {
 };
 
 // fits the 227 KB a CTA may opt into, with room to align the base to 1 KB
-static_assert(sizeof(Smem) + 1024 <= 232448, "pva_tc_kernel shared memory");
+static_assert(sizeof(Smem<false>) + 1024 <= 232448, "pva_tc_kernel shared memory");
+static_assert(sizeof(Smem<true>) + 1024 <= 232448, "pva_tc_kernel shared memory");
+
+// f16 MMA instruction descriptor (FP8 pages): as umma_idesc_bf16 with both
+// operand formats F16.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, bool b_mn_major) {
+    return umma_idesc_bf16(M, N, b_mn_major) & ~((1u << 7) | (1u << 10));
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// bf16 pair -> f16 pair (round to nearest)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
 
 __device__ __forceinline__ uint32_t par_of(int idx) { return (uint32_t)((idx >> 1) & 1); }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool FP8>
+__global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
     pva_tc_kernel(const __grid_constant__ CUtensorMap mkp, const __grid_constant__ CUtensorMap mvp,
                   const __grid_constant__ CUtensorMap mq0, const __grid_constant__ CUtensorMap mq1,
                   const __grid_constant__ AttnArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using C = TcCfg<FP8>;
+    constexpr int kNK = C::kNK, kNV = C::kNV;
+    Smem<FP8> &sm = *reinterpret_cast<Smem<FP8> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
+        // FP8: the K and V tiles are published by the converter warps
+        const uint32_t tile_arrivals = FP8 ? C::kConvWarps : 1;
         for (int i = 0; i < kNK; ++i) {
-            mbar_init(&sm.k_full[i], 1);
+            mbar_init(&sm.k_full[i], tile_arrivals);
             mbar_init(&sm.k_empty[i], 1);
         }
         for (int i = 0; i < kNV; ++i) {
-            mbar_init(&sm.v_full[i], 1);
+            mbar_init(&sm.v_full[i], tile_arrivals);
             mbar_init(&sm.v_empty[i], 1);
+        }
+        if constexpr (FP8) {
+            for (int i = 0; i < C::kNK8; ++i) {
+                mbar_init(&sm.st8.k8_full[i], 1);
+                mbar_init(&sm.st8.k8_empty[i], C::kConvWarps);
+            }
+            for (int i = 0; i < C::kNV8; ++i) {
+                mbar_init(&sm.st8.v8_full[i], 1);
+                mbar_init(&sm.st8.v8_empty[i], C::kConvWarps);
+            }
+            mbar_init(&sm.st8.q_full, 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.s_full[i], 1);
             mbar_init(&sm.o_full[i], 1);
-            mbar_init(&sm.o_empty[i], 4);
+            mbar_init(&sm.o_empty[i], C::kEpiWarps);
         }
         mbar_init(&sm.q_empty, 1);
-        mbar_init(&sm.p_full, 4);
+        mbar_init(&sm.p_full, C::kSoftmaxWarps);
         mbar_init(&sm.p_empty, 1);
-        mbar_init(&sm.stat_full, 4);
-        mbar_init(&sm.stat_empty, 4);
+        mbar_init(&sm.stat_full, C::kSoftmaxWarps);
+        mbar_init(&sm.stat_empty, C::kEpiWarps);
         fence_mbar_init();
     }
     // query rows past M are never written by the copies: keep them zero
@@ -147,20 +219,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         int jk = 0, jv = 0, units = 0;      // K blocks issued, V blocks issued, units started (warp-uniform)
         bool ok = true;
         const uint32_t qbytes = (uint32_t)(a.M * 128 * 2);
+        // the rings the copies land in: the MMA's tiles (bf16) or the FP8
+        // staging rings in front of the converters
+        constexpr int PNK = FP8 ? C::kNK8 : kNK, PNV = FP8 ? C::kNV8 : kNV;
+        constexpr uint32_t kBlockBytes = FP8 ? kTile8 : kKVTile;
+        uint64_t *pk_full, *pk_empty, *pv_full, *pv_empty;
+        if constexpr (FP8) {
+            pk_full = sm.st8.k8_full;
+            pk_empty = sm.st8.k8_empty;
+            pv_full = sm.st8.v8_full;
+            pv_empty = sm.st8.v8_empty;
+        } else {
+            pk_full = sm.k_full;
+            pk_empty = sm.k_empty;
+            pv_full = sm.v_full;
+            pv_empty = sm.v_empty;
+        }
+        // one copy per page: a 5-D box of a bf16 tile, or a 2 KB FP8 tile
+        auto copy_page = [&](const CUtensorMap *map, uint8_t *ring_slot, int id, int hh, uint64_t *bar) {
+            if constexpr (FP8)
+                tma_load_4d(ring_slot + lane * kPage8, map, 0, 0, hh, id, bar, pol);
+            else
+                tma_load_5d(ring_slot + lane * 4096, map, 0, 0, 0, 0, id * a.Hkv + hh, bar, pol);
+        };
+        auto k_slot = [&](int s_) -> uint8_t * {
+            if constexpr (FP8) return sm.st8.k8[s_]; else return sm.kbuf[s_];
+        };
+        auto v_slot = [&](int s_) -> uint8_t * {
+            if constexpr (FP8) return sm.st8.v8[s_]; else return sm.vbuf[s_];
+        };
         // V of the oldest block whose K is out, if its ring slot is free (a
         // non-blocking test): K runs ahead as far as its own ring allows and
         // V follows as PV frees slots, neither waiting for the other
         auto try_issue_v = [&]() -> bool {
             if (jv >= jk) return false;
-            const int vs = jv % kNV;
+            const int vs = jv % PNV;
             int ready = 1;
-            if (lane == 0 && jv >= kNV) ready = mbar_test(&sm.v_empty[vs], (uint32_t)(((jv / kNV) & 1) ^ 1));
+            if (lane == 0 && jv >= PNV) ready = mbar_test(&pv_empty[vs], (uint32_t)(((jv / PNV) & 1) ^ 1));
             if (!__shfl_sync(0xffffffffu, ready, 0)) return false;
-            if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[vs], kKVTile);
-            if (lane < kPagesPerBlock) {
-                const int id = sm.vid[jv % kNMeta][lane], hh = sm.meta[jv % kNMeta].h;
-                tma_load_5d(sm.vbuf[vs] + lane * 4096, &mvp, 0, 0, 0, 0, id * a.Hkv + hh, &sm.v_full[vs], pol);
-            }
+            if (lane == 0) mbar_arrive_expect_tx(&pv_full[vs], kBlockBytes);
+            if (lane < kPagesPerBlock)
+                copy_page(&mvp, v_slot(vs), sm.vid[jv % kNMeta][lane], sm.meta[jv % kNMeta].h, &pv_full[vs]);
             __syncwarp();
             ++jv;
             return true;
@@ -224,8 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int my_id = __shfl_sync(0xffffffffu, blk, (j0 + (lane & 7)) & 31);
                     if (j0 + (lane & 7) >= cnt) my_id = a.num_blocks;
                     const int bi = (i0 + j0) / kPagesPerBlock;  // block index in the unit
-                    const int ks = jk % kNK;
-                    if (jk >= kNK) ok = wait_issuing_v(&sm.k_empty[ks], (uint32_t)(((jk / kNK) & 1) ^ 1));
+                    const int ks = jk % PNK;
+                    if (jk >= PNK) ok = wait_issuing_v(&pk_empty[ks], (uint32_t)(((jk / PNK) & 1) ^ 1));
                     // the query tile is reloaded once the previous unit's last S is done
                     if (ok && bi == 0 && units >= 1) ok = wait_issuing_v(&sm.q_empty, (uint32_t)((units - 1) & 1));
                     if (!ok) break;
@@ -235,16 +334,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         m.pos0 = (page0 + i0 + j0) * kBlockSize;
                         m.ntok = min(kPagesPerBlock, n - (i0 + j0)) * kBlockSize;
                         m.flags = (bi == 0 ? kFlagFirst : 0) | (bi == nblk - 1 ? kFlagLast : 0);
-                        mbar_arrive_expect_tx(&sm.k_full[ks], kKVTile + (bi == 0 ? qbytes : 0u));
+                        // bf16: the query tile rides on the unit's first K block;
+                        // FP8: it has a barrier of its own (the converters
+                        // turn it into f16 before the first K tile)
+                        uint64_t *qbar = &pk_full[ks];
+                        if constexpr (FP8) qbar = &sm.st8.q_full;
+                        if (FP8 && bi == 0) mbar_arrive_expect_tx(qbar, qbytes);
+                        mbar_arrive_expect_tx(&pk_full[ks], kBlockBytes + (!FP8 && bi == 0 ? qbytes : 0u));
                         if (bi == 0) {
-                            tma_load_4d(&sm.q[0], &mq0, 0, h * a.G, 0, b, &sm.k_full[ks], pol);
-                            tma_load_4d(&sm.q[kQSlab], &mq1, 0, h * a.G, 0, b, &sm.k_full[ks], pol);
+                            tma_load_4d(&sm.q[0], &mq0, 0, h * a.G, 0, b, qbar, pol);
+                            tma_load_4d(&sm.q[kQSlab], &mq1, 0, h * a.G, 0, b, qbar, pol);
                         }
                     }
                     if (lane < kPagesPerBlock) {
                         sm.vid[jk % kNMeta][lane] = my_id;
-                        tma_load_5d(sm.kbuf[ks] + lane * 4096, &mkp, 0, 0, 0, 0, my_id * a.Hkv + h, &sm.k_full[ks],
-                                    pol);
+                        copy_page(&mkp, k_slot(ks), my_id, h, &pk_full[ks]);
                     }
                     __syncwarp();
                     ++jk;
@@ -255,27 +359,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // the V copies still owed
         while (ok && jv < jk) {
-            if (jv >= kNV) {
+            if (jv >= PNV) {
                 int good = 1;
-                if (lane == 0) good = mbar_wait(&sm.v_empty[jv % kNV], (uint32_t)(((jv / kNV) & 1) ^ 1), a.err);
+                if (lane == 0) good = mbar_wait(&pv_empty[jv % PNV], (uint32_t)(((jv / PNV) & 1) ^ 1), a.err);
                 ok = __shfl_sync(0xffffffffu, good, 0) != 0;
             }
             if (ok) try_issue_v();
         }
         if (lane == 0) {
-            // end-of-work marker on the K ring
-            const int ks = jk % kNK;
-            if (ok && jk >= kNK) ok = mbar_wait(&sm.k_empty[ks], (uint32_t)(((jk / kNK) & 1) ^ 1), a.err);
+            // end-of-work marker on the K ring (and, FP8, on the V staging
+            // ring for the V converters)
+            const int ks = jk % PNK;
+            if (ok && jk >= PNK) ok = mbar_wait(&pk_empty[ks], (uint32_t)(((jk / PNK) & 1) ^ 1), a.err);
             if (ok) {
                 sm.meta[jk % kNMeta].flags = kFlagEnd;
-                mbar_arrive(&sm.k_full[ks]);
+                mbar_arrive(&pk_full[ks]);
             }
-            // wait (bounded) for the copies still in flight; the K stage reused
-            // by the end marker had completed before its empty barrier passed
-            for (int i = jk >= kNK ? jk - kNK + 1 : 0; i < jk && ok; ++i)
-                ok = mbar_wait(&sm.k_full[i % kNK], (uint32_t)((i / kNK) & 1), a.err);
-            for (int i = jv >= kNV ? jv - kNV : 0; i < jv && ok; ++i)
-                ok = mbar_wait(&sm.v_full[i % kNV], (uint32_t)((i / kNV) & 1), a.err);
+            const int vs = jv % PNV;
+            if constexpr (FP8) {
+                if (ok && jv >= PNV) ok = mbar_wait(&pv_empty[vs], (uint32_t)(((jv / PNV) & 1) ^ 1), a.err);
+                if (ok) mbar_arrive(&pv_full[vs]);
+            }
+            // wait (bounded) for the copies still in flight; a stage reused
+            // by an end marker had completed before its empty barrier passed
+            for (int i = jk >= PNK ? jk - PNK + 1 : 0; i < jk && ok; ++i)
+                ok = mbar_wait(&pk_full[i % PNK], (uint32_t)((i / PNK) & 1), a.err);
+            for (int i = jv >= PNV ? jv - PNV + (FP8 ? 1 : 0) : 0; i < jv && ok; ++i)
+                ok = mbar_wait(&pv_full[i % PNV], (uint32_t)((i / PNV) & 1), a.err);
+            if constexpr (FP8)
+                if (ok && units >= 1) ok = mbar_wait(&sm.st8.q_full, (uint32_t)((units - 1) & 1), a.err);
             __threadfence();
             const int done = atomicAdd(&a.sched[1], 1);
             if (done == (int)gridDim.x - 1) {
@@ -286,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ================================================= MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idS = umma_idesc_bf16(kRows, kNB, false);
-            constexpr uint32_t idPV = umma_idesc_bf16(kRows, kD, true);
+            constexpr uint32_t idS = FP8 ? umma_idesc_f16(kRows, kNB, false) : umma_idesc_bf16(kRows, kNB, false);
+            constexpr uint32_t idPV = FP8 ? umma_idesc_f16(kRows, kD, true) : umma_idesc_bf16(kRows, kD, true);
             const uint32_t qaddr = smem_u32(&sm.q[0]);
             // S_jj = Q K_jj^T once K_jj has landed (or forward the end marker)
             // buf_wait: wait for PV_{jj-2} (whose P shares S_jj's TMEM buffer);
@@ -368,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp >= C::kSoftmaxWarp0 && warp < C::kSoftmaxWarp0 + C::kSoftmaxWarps) {
         // ================================================= softmax
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;          // query row == TMEM lane
@@ -385,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (md.flags & kFlagEnd) {
                 // tell the epilogue warps there is no further unit
                 if (unit >= 0) mbar_wait(&sm.stat_empty, (uint32_t)(unit & 1), a.err);
-                if (threadIdx.x == 64) sm.ep_end = 1;
+                if (threadIdx.x == C::kSoftmaxWarp0 * 32) sm.ep_end = 1;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.stat_full);
                 break;
@@ -464,19 +576,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float p0 = live ? ex2_approx(fmaf(s[c * 64 + 2 * e], sc, neg_m)) : 0.f;
                     const float p1 = live ? ex2_approx(fmaf(s[c * 64 + 2 * e + 1], sc, neg_m)) : 0.f;
                     ls[e & 3] += p0 + p1;
-                    w[e] = pack_bf16x2(p0, p1);
+                    w[e] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
                 }
                 tmem_st32(pt + c * 32, w);
             }
             l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             // V rows past the sequence's last token may hold anything: zero
             // them once V_j has landed (PV_j is not issued before p_full)
-            if (md.pos0 + md.ntok > T) {
+            if (!FP8 && md.pos0 + md.ntok > T) {  // (FP8: the V converters zero them)
                 mbar_wait(&sm.v_full[j % kNV], (uint32_t)((j / kNV) & 1), a.err);
                 const int t0 = T - md.pos0;
                 const int nz = (md.ntok - t0) * 2 * 8;
                 uint8_t *sv = sm.vbuf[j % kNV];
-                for (int z = threadIdx.x - 64; z < nz; z += 128) {
+                for (int z = threadIdx.x - C::kSoftmaxWarp0 * 32; z < nz; z += C::kSoftmaxWarps * 32) {
                     const int row = t0 + z / 16, rem = z % 16;
                     *reinterpret_cast<uint4 *>(sv + (row >> 3) * 2048 + (rem >> 3) * 1024 + (row & 7) * 128 +
                                                ((rem & 7) << 4)) = make_uint4(0, 0, 0, 0);
@@ -516,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // slot: the previous unit's must have been taken)
                 if (unit >= 1) mbar_wait(&sm.stat_empty, (uint32_t)((unit - 1) & 1), a.err);
                 sm.stat[r] = make_float2(m_ref, l_run);
-                if (threadIdx.x == 64) {
+                if (threadIdx.x == C::kSoftmaxWarp0 * 32) {
                     sm.ep_b = md.b;
                     sm.ep_h = md.h;
                     sm.ep_split = md.split;
@@ -528,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++j;
         }
-    } else {
+    } else if (warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + C::kEpiWarps) {
         // ================================================= epilogue
         // One thread per query row (TMEM lane) streams a finished unit's O
         // out of TMEM while the softmax warps already work on the next unit
@@ -540,7 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool live = r < a.M;
         const int jq = live ? r / G : 0;
         const int gi = r - jq * G;
-        const int ew = warp - 6;  // 0..3
+        const int ew = warp - C::kEpiWarp0;
+        constexpr int NE = C::kEpiWarps;
         for (int unit = 0;; ++unit) {
             if (!mbar_wait(&sm.stat_full, (uint32_t)(unit & 1), a.err)) break;
             if (sm.ep_end) break;
@@ -596,15 +709,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 a.part_ml[pr_own * 2 + 1] = l_run;
             }
             __threadfence();
-            named_barrier_sync(kBarEpi, kEpiThreads);
+            named_barrier_sync(kBarEpi, NE * 32);
             if (ew == 0 && lane == 0) {
                 const int t = atomicAdd(&a.tickets[u2], 1);
                 sm.last = (t == nsplit - 1);
                 if (sm.last) a.tickets[u2] = 0;
             }
-            named_barrier_sync(kBarEpi, kEpiThreads);
+            named_barrier_sync(kBarEpi, NE * 32);
             const int last = sm.last;
-            named_barrier_sync(kBarEpi, kEpiThreads);
+            named_barrier_sync(kBarEpi, NE * 32);
             if (!last) continue;
             // the last split's CTA merges every split's partial rows with
             // log-sum-exp weights (an online merge: running maximum, rescaled
@@ -612,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // splits per pass so that their loads are in flight together
             __threadfence();
             const size_t base = (size_t)u2 * a.max_splits * a.M;
-            for (int r0 = ew; r0 < a.M; r0 += 16) {
+            for (int r0 = ew; r0 < a.M; r0 += 4 * NE) {
                 float mrow[4], lrow[4];
                 float4 o[4];
 #pragma unroll
@@ -628,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 4; ++i)
 #pragma unroll
                         for (int k = 0; k < 2; ++k) {
-                            const int rr = r0 + 4 * i;
+                            const int rr = r0 + NE * i;
                             if (rr < a.M && s0 + k < nsplit) {
                                 const size_t pr = base + (size_t)(s0 + k) * a.M + rr;
                                 ml[i][k] = __ldcg(reinterpret_cast<const float2 *>(a.part_ml + pr * 2));
@@ -657,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int rr = r0 + 4 * i;
+                    const int rr = r0 + NE * i;
                     if (rr >= a.M) break;
                     const float inv2 = lrow[i] > 0.f ? 1.f / lrow[i] : 0.f;
                     const int jq2 = rr / G, gi2 = rr - jq2 * G;
@@ -667,6 +780,104 @@ __global__ void __launch_bounds__(kThreads, 1)
                     v2.y = pack_bf16x2(o[i].z * inv2, o[i].w * inv2);
                     reinterpret_cast<uint2 *>(a.out + od2 * kD)[lane] = v2;
                     if (lane == 0 && a.lse) a.lse[od2] = (mrow[i] + __log2f(lrow[i])) * 0.69314718055994530942f;
+                }
+            }
+        }
+    }
+    if constexpr (FP8) {
+        const bool kconv = warp == 2 || warp == 3 || warp == 10;
+        const bool vconv = warp == 6 || warp == 7 || warp == 11;
+        if (kconv || vconv) {
+            // ================================================= FP8 converters
+            // Block j's E4M3 pages -> one f16 tile in the MMA's layout (page p
+            // at p * 4 KB as [row half][slab][8 rows][128 B], 128-byte
+            // swizzle), each value times its page's scale; the V converters
+            // also zero the rows past the sequence's last token.  The K
+            // converters first turn each unit's bf16 query tile into f16.
+            const int ci = kconv ? (warp == 10 ? 2 : warp - 2) : (warp == 11 ? 2 : warp - 6);
+            const int ct = ci * 32 + lane;  // 0..95
+            constexpr int NCT = C::kConvWarps * 32;
+            const int ring = kconv ? C::kNK8 : C::kNV8;
+            uint64_t *full8 = kconv ? sm.st8.k8_full : sm.st8.v8_full;
+            uint64_t *empty8 = kconv ? sm.st8.k8_empty : sm.st8.v8_empty;
+            uint64_t *tile_full = kconv ? &sm.k_full[0] : &sm.v_full[0];
+            uint64_t *tile_empty = kconv ? &sm.k_empty[0] : &sm.v_empty[0];
+            uint8_t *tile = kconv ? sm.kbuf[0] : sm.vbuf[0];
+            const float *scales = kconv ? a.k_scale : a.v_scale;
+            int units_seen = 0;
+            for (int j = 0;; ++j) {
+                const int s8 = j % ring;
+                if (!mbar_wait(&full8[s8], (uint32_t)((j / ring) & 1), a.err)) break;
+                const BlockMeta md = sm.meta[j % kNMeta];
+                if (md.flags & kFlagEnd) {
+                    // forward the end marker to the MMA issuer, once it has
+                    // taken the last K tile: k_full is a single barrier, and
+                    // an arrival before S_{j-1} completes would land two
+                    // phases ahead of the issuer's wait
+                    if (kconv) {
+                        if (j >= 1 && !mbar_wait(tile_empty, (uint32_t)((j - 1) & 1), a.err)) break;
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tile_full);
+                    }
+                    break;
+                }
+                const uint8_t *src = kconv ? sm.st8.k8[s8] : sm.st8.v8[s8];
+                // this block's page scales (lanes 0..7), as f16 pairs
+                float sc = 0.f;
+                if (lane < kPagesPerBlock) {
+                    const int id = sm.vid[j % kNMeta][lane];
+                    if (id >= 0 && id < a.num_blocks) sc = __ldg(scales + (size_t)id * a.Hkv + md.h);
+                    if (!(sc >= 0.f && sc <= kMaxScale8)) {
+                        raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                        sc = 0.f;
+                    }
+                }
+                if (kconv && (md.flags & kFlagFirst)) {
+                    // the unit's queries, bf16 -> f16 in place (rows < M)
+                    if (!mbar_wait(&sm.st8.q_full, (uint32_t)(units_seen & 1), a.err)) break;
+                    ++units_seen;
+                    for (int i = ct; i < a.M * 16; i += NCT) {
+                        const int row = i >> 4, c = i & 15;
+                        uint4 *qp = reinterpret_cast<uint4 *>(&sm.q[(c >> 3) * kQSlab + row * 128 + ((c & 7) << 4)]);
+                        uint4 v = *qp;
+                        v.x = bf16x2_to_f16x2(v.x);
+                        v.y = bf16x2_to_f16x2(v.y);
+                        v.z = bf16x2_to_f16x2(v.z);
+                        v.w = bf16x2_to_f16x2(v.w);
+                        *qp = v;
+                    }
+                }
+                // the tile is free once S_{j-1} (K) or PV_{j-1} (V) is done
+                if (j >= 1 && !mbar_wait(tile_empty, (uint32_t)((j - 1) & 1), a.err)) break;
+                const int t_end = kconv ? kNB : md.L + a.n_q - md.pos0;  // V rows from t_end on are zeroed
+                for (int i0 = 0; i0 < kNB * 8; i0 += NCT) {  // same trip count in every lane
+                    const int i = i0 + ct;
+                    const int row = i >> 3, g = i & 7;  // 16 columns: 16g .. 16g+15
+                    const float scf = __shfl_sync(0xffffffffu, sc, (row >> 4) & 7);
+                    if (i >= kNB * 8) continue;
+                    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+                    if (row < t_end) {
+                        const uint4 e = *reinterpret_cast<const uint4 *>(src + row * 128 + ((g ^ (row & 7)) << 4));
+                        const uint32_t s2 = pack_f16x2(scf, scf);
+                        lo.x = hmul2(e4m3x2_to_f16x2(e.x & 0xffffu), s2);
+                        lo.y = hmul2(e4m3x2_to_f16x2(e.x >> 16), s2);
+                        lo.z = hmul2(e4m3x2_to_f16x2(e.y & 0xffffu), s2);
+                        lo.w = hmul2(e4m3x2_to_f16x2(e.y >> 16), s2);
+                        hi.x = hmul2(e4m3x2_to_f16x2(e.z & 0xffffu), s2);
+                        hi.y = hmul2(e4m3x2_to_f16x2(e.z >> 16), s2);
+                        hi.z = hmul2(e4m3x2_to_f16x2(e.w & 0xffffu), s2);
+                        hi.w = hmul2(e4m3x2_to_f16x2(e.w >> 16), s2);
+                    }
+                    const int r8 = row & 7, c0 = (g & 3) * 2;
+                    uint8_t *dst = tile + (row >> 3) * 2048 + (g >> 2) * 1024 + r8 * 128;
+                    *reinterpret_cast<uint4 *>(dst + ((c0 ^ r8) << 4)) = lo;
+                    *reinterpret_cast<uint4 *>(dst + (((c0 + 1) ^ r8) << 4)) = hi;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(tile_full);
+                    mbar_arrive(&empty8[s8]);
                 }
             }
         }
@@ -681,14 +892,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t attn_tc_smem_bytes() { return sizeof(Smem) + 1024; }
+size_t attn_tc_smem_bytes() { return std::max(sizeof(Smem<false>), sizeof(Smem<true>)) + 1024; }
 
-cudaError_t launch_paged_verify_attn_tc(const AttnMaps &m, const AttnArgs &a, int grid, cudaStream_t st) {
-    const size_t smem = attn_tc_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(pva_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+namespace {
+template <bool FP8>
+cudaError_t launch_tc(const CUtensorMap &mk, const CUtensorMap &mv, const AttnMaps &m, const AttnArgs &a, int grid,
+                      cudaStream_t st) {
+    const size_t smem = sizeof(Smem<FP8>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(pva_tc_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    pva_tc_kernel<<<grid, kThreads, smem, st>>>(m.kpage, m.vpage, m.q[0], m.q[1], a);
+    pva_tc_kernel<FP8><<<grid, TcCfg<FP8>::kThreads, smem, st>>>(mk, mv, m.q[0], m.q[1], a);
     return cudaGetLastError();
+}
+}  // namespace
+
+// FP8 pages: the E4M3 page maps (one 2 KB box per page); bf16: the 5-D page maps
+cudaError_t launch_paged_verify_attn_tc(const AttnMaps &m, const AttnArgs &a, int grid, bool fp8, cudaStream_t st) {
+    return fp8 ? launch_tc<true>(m.k[0], m.v[0], m, a, grid, st) : launch_tc<false>(m.kpage, m.vpage, m, a, grid, st);
 }
 
 }  // namespace svpa

@@ -65,7 +65,7 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
         return SVPA_ERR_INVALID_ARG;
     if (p->kv_dtype != SVPA_KV_BF16 && p->kv_dtype != SVPA_KV_FP8_E4M3) return SVPA_ERR_INVALID_ARG;
     if (p->variant < 0 || p->variant > 2) return SVPA_ERR_INVALID_ARG;
-    if (p->variant == 2 && (p->head_dim != 128 || p->kv_dtype != SVPA_KV_BF16)) return SVPA_ERR_UNSUPPORTED;
+    if (p->variant == 2 && p->head_dim != 128) return SVPA_ERR_UNSUPPORTED;
     if (p->head_dim != 64 && p->head_dim != 128) return SVPA_ERR_UNSUPPORTED;
     if (p->kv_dtype == SVPA_KV_FP8_E4M3 && p->head_dim != 128) return SVPA_ERR_UNSUPPORTED;
     const int G = p->num_q_heads / p->num_kv_heads;
@@ -74,8 +74,10 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     pl->M = (int)M;
     const int D = p->head_dim;
     const int eb = p->kv_dtype == SVPA_KV_FP8_E4M3 ? 1 : 2;
-    // kernel variant and its resident grid (the persistent CTAs)
-    pl->use_tc = p->variant == 2 || (p->variant == 0 && D == 128 && eb == 2 && M > 16);
+    // kernel variant and its resident grid (the persistent CTAs); the
+    // tcgen05 kernel takes FP8 pages for up to 64 query rows per kv head
+    if (p->variant == 2 && eb == 1 && M > 64) return SVPA_ERR_UNSUPPORTED;
+    pl->use_tc = p->variant == 2 || (p->variant == 0 && D == 128 && M > 16 && (eb == 2 || M <= 64));
     pl->grid_slots = sm_count();
     if (!pl->use_tc) {
         AttnLaunch lp;
@@ -90,10 +92,13 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
         const double per = units * p->max_blocks_per_seq / (16.0 * sm_count());
         int pw = 16;
         while (pw * 2 <= per && pw < 1024) pw *= 2;
-        // keep the split partials under ~5% of the split's K/V bytes
+        // keep a split's partial rows (written, then read back by the merge)
+        // near 1% of its K/V bytes: with many rows per kv head the partials
+        // and their merge cost more than the balance finer splits buy (draft
+        // tree, 116 rows: 128-page splits 607 us, unsplit 476 us on GB300)
         const double page_bytes = 2.0 * kBlockSize * D * eb;
         const double partial_bytes = (double)M * (D + 2) * 4;
-        int min_pages = (int)std::ceil(20.0 * partial_bytes / page_bytes);
+        int min_pages = (int)std::ceil(100.0 * partial_bytes / page_bytes);
         min_pages = (min_pages + 15) / 16 * 16;
         sp = std::max(pw, min_pages);
     }
@@ -200,7 +205,7 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
             return SVPA_ERR_CUDA;
     }
 
-    if (pl.use_tc) {
+    if (pl.use_tc && !fp8) {
         // one (page, kv head) tile per copy: dims (64 columns, 8 rows, 2 column
         // slabs, 2 row halves, kv head x block), landing as
         // [row half][slab][8 rows][128 B] -- 1 KB swizzle atoms with a uniform
@@ -283,7 +288,7 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
     a.total_units = p->batch * p->num_kv_heads * pl.max_splits;
     if (pl.use_tc) {
         const int grid = std::max(1, std::min(pl.grid_slots, a.total_units));
-        return from_cuda(launch_paged_verify_attn_tc(maps, a, grid, static_cast<cudaStream_t>(stream)));
+        return from_cuda(launch_paged_verify_attn_tc(maps, a, grid, fp8, static_cast<cudaStream_t>(stream)));
     }
     AttnLaunch lp;
     if (attn_plan_launch(D, fp8, pl.M, &lp) != cudaSuccess) return SVPA_ERR_CUDA;

@@ -57,7 +57,7 @@ cudaError_t launch_paged_verify_attn(const AttnMaps &maps, const AttnArgs &a, in
 // Stage count, resident CTAs per SM and dynamic shared memory for a shape.
 cudaError_t attn_plan_launch(int head_dim, bool fp8, int M, AttnLaunch *out);
 // tcgen05 / TMEM variant (bf16 pages, head_dim 128, one CTA per SM).
-cudaError_t launch_paged_verify_attn_tc(const AttnMaps &maps, const AttnArgs &a, int grid,
+cudaError_t launch_paged_verify_attn_tc(const AttnMaps &maps, const AttnArgs &a, int grid, bool fp8,
                                         cudaStream_t stream);
 
 // Rejection sampler.

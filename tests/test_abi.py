@@ -48,6 +48,11 @@ def test_workspace_size_and_validation(lib):
         kw.update(bad)
         with pytest.raises(svpa.SvpaError):
             svpa.attn_workspace_size(svpa.attn_params(**kw))
+    # FP8 pages on the tcgen05 kernel take at most 64 rows per kv head
+    with pytest.raises(svpa.SvpaError) as e:
+        svpa.attn_workspace_size(svpa.attn_params(2, 9, 64, 8, 128, 8, 16, kv_fp8=True, variant=2))
+    assert e.value.status == 2
+    assert svpa.attn_workspace_size(svpa.attn_params(2, 8, 64, 8, 128, 8, 16, kv_fp8=True, variant=2)) > 0
     # GQA rows per CTA beyond 128 are not supported
     with pytest.raises(svpa.SvpaError) as e:
         svpa.attn_workspace_size(svpa.attn_params(1, 17, 64, 8, 128, 8, 16, split_pages=4))

@@ -135,6 +135,9 @@ VARIANT_CASES = [
     ("gqa_nosplit", small("70b", batch=2, ctx_lo=100, ctx_hi=300), 1024),
     ("tree", small("tree", batch=3, ctx_lo=1, ctx_hi=500, shared_prefix=32), 8),
     ("mha", small("7b", batch=3, ctx_lo=1, ctx_hi=300, num_q_heads=8, num_kv_heads=8), 8),
+    ("fp8", small("fp8", batch=3, ctx_lo=1, ctx_hi=900), 16),
+    ("fp8_nosplit", small("fp8", batch=2, ctx_lo=100, ctx_hi=300), 1024),
+    ("fp8_g4", small("fp8", batch=3, ctx_lo=40, ctx_hi=700, num_q_heads=32, num_kv_heads=8), 8),
 ]
 
 
@@ -145,5 +148,5 @@ def test_kernel_variants(name, wl, split, variant):
     got, lse, st = U.run_attention(inp, split_pages=split, variant=variant)
     assert st == 0
     ref, ref_lse = U.run_oracle_attention(inp)
-    U.assert_attention_close(got, ref, what=f"{name} variant {variant}")
+    U.assert_attention_close(got, ref, fp8=wl.kv_fp8, what=f"{name} variant {variant}")
     assert np.max(np.abs(lse - ref_lse)) < 2e-3
