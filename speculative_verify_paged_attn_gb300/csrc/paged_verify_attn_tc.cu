@@ -49,8 +49,6 @@ constexpr int kPagesPerBlock = 8;
 constexpr int kNB = kPagesPerBlock * 16;       // tokens per block (128)
 constexpr int kRows = 128;                      // MMA M
 constexpr int kKVTile = kNB * 256;              // K (or V) block: 8 pages of 4 KB
-constexpr int kQSlab = kRows * 128;
-constexpr int kQBuf = 2 * kQSlab;
 constexpr int kNMeta = 8;                       // block descriptors in flight
 constexpr int kBarEpi = 1;                      // named barrier of the epilogue warps
 constexpr int kPage8 = 16 * 128;                // one FP8 (page, kv head) tile
@@ -62,17 +60,24 @@ constexpr float kMaxScale8 = 146.f;             // 448 * scale stays below the f
 //    and V rings of bf16 blocks that the MMA reads directly.
 //  FP8 pages (at most 64 query rows, so two TMEM lane quadrants): warps 0
 //    producer, 1 MMA, 4-5 softmax, 8-9 epilogue, 2/3/10 K converters, 6/7/11
-//    V converters; the producer streams E4M3 pages into 4-deep staging rings,
-//    the converters turn each block into f16 (the page's scale folded in) in
-//    a single K and a single V tile, and the MMAs run kind::f16 with f16
-//    queries (converted in place) and f16 P.
+//    V converters; the producer streams E4M3 pages (and, by cp.async, their
+//    scales) into 2-deep staging rings, the converters turn each block into
+//    f16 (the page's scale folded in) in 2-deep K and V tile rings, and the
+//    MMAs run kind::f16 with f16 queries (converted in place) and f16 P.  The
+//    query buffer holds 64 rows; the MMA still reads 128, rows 64..127 being
+//    whatever follows and feeding only TMEM lanes no thread reads.
 template <bool FP8>
 struct TcCfg {
     static constexpr int kThreads = FP8 ? 384 : 320;
-    static constexpr int kNK = FP8 ? 1 : 3;     // tiles the MMA reads (K freed once S_j is done)
-    static constexpr int kNV = FP8 ? 1 : 3;     // (V freed once PV_j is done)
-    static constexpr int kNK8 = FP8 ? 4 : 1;    // FP8 staging rings
-    static constexpr int kNV8 = FP8 ? 4 : 1;
+    static constexpr int kNK = FP8 ? 2 : 3;     // tiles the MMA reads (K freed once S_j is done)
+    static constexpr int kNV = FP8 ? 2 : 3;     // (V freed once PV_j is done)
+    static constexpr int kNK8 = FP8 ? 2 : 1;    // FP8 staging rings
+    static constexpr int kNV8 = FP8 ? 2 : 1;
+    static constexpr int kQSlab = (FP8 ? 64 : 128) * 128;  // one 64-column slab of the query buffer
+    static constexpr int kQBuf = 2 * kQSlab;
+    // arrivals that complete a staging slot: the producer's expect_tx and
+    // one cp.async scale copy per page
+    static constexpr uint32_t kStageArrivals = 1 + kPagesPerBlock;
     static constexpr int kSoftmaxWarp0 = FP8 ? 4 : 2;
     static constexpr int kSoftmaxWarps = FP8 ? 2 : 4;
     static constexpr int kEpiWarp0 = FP8 ? 8 : 6;
@@ -98,6 +103,8 @@ template <bool FP8>
 struct Stage8 {  // FP8 staging rings
     uint8_t k8[TcCfg<FP8>::kNK8][kTile8];
     uint8_t v8[TcCfg<FP8>::kNV8][kTile8];
+    float ksc[TcCfg<FP8>::kNK8][kPagesPerBlock];  // the staged pages' scales
+    float vsc[TcCfg<FP8>::kNV8][kPagesPerBlock];
     uint64_t k8_full[TcCfg<FP8>::kNK8], k8_empty[TcCfg<FP8>::kNK8];
     uint64_t v8_full[TcCfg<FP8>::kNV8], v8_empty[TcCfg<FP8>::kNV8];
     uint64_t q_full;
@@ -107,7 +114,7 @@ struct NoStage8 {};
 template <bool FP8>
 struct Smem {
     using C = TcCfg<FP8>;
-    uint8_t q[kQBuf];                    // 32 KB, 1024-aligned (one unit's queries)
+    uint8_t q[C::kQBuf];                 // 1024-aligned (one unit's queries)
     uint8_t kbuf[C::kNK][kKVTile];       // 32 KB each
     uint8_t vbuf[C::kNV][kKVTile];
     typename std::conditional<FP8, Stage8<FP8>, NoStage8>::type st8;
@@ -156,7 +163,7 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                   const __grid_constant__ AttnArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     using C = TcCfg<FP8>;
-    constexpr int kNK = C::kNK, kNV = C::kNV;
+    constexpr int kNK = C::kNK, kNV = C::kNV, kQSlab = C::kQSlab, kQBuf = C::kQBuf;
     Smem<FP8> &sm = *reinterpret_cast<Smem<FP8> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -173,11 +180,11 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
         }
         if constexpr (FP8) {
             for (int i = 0; i < C::kNK8; ++i) {
-                mbar_init(&sm.st8.k8_full[i], 1);
+                mbar_init(&sm.st8.k8_full[i], C::kStageArrivals);
                 mbar_init(&sm.st8.k8_empty[i], C::kConvWarps);
             }
             for (int i = 0; i < C::kNV8; ++i) {
-                mbar_init(&sm.st8.v8_full[i], 1);
+                mbar_init(&sm.st8.v8_full[i], C::kStageArrivals);
                 mbar_init(&sm.st8.v8_empty[i], C::kConvWarps);
             }
             mbar_init(&sm.st8.q_full, 1);
@@ -242,6 +249,15 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             else
                 tma_load_5d(ring_slot + lane * 4096, map, 0, 0, 0, 0, id * a.Hkv + hh, bar, pol);
         };
+        // FP8: the page's scale by cp.async, counted on the same staging
+        // barrier (a missing page takes the block's first page's scale: its
+        // bytes are zero)
+        auto copy_scale = [&](const float *scales, int id, int hh, float *dst, uint64_t *bar) {
+            const int id0 = __shfl_sync(0x000000ffu, id, 0);
+            const int sid = (id >= 0 && id < a.num_blocks) ? id : id0;
+            cp_async_4(dst, scales + (size_t)sid * a.Hkv + hh);
+            cp_async_mbar_arrive_noinc(bar);
+        };
         auto k_slot = [&](int s_) -> uint8_t * {
             if constexpr (FP8) return sm.st8.k8[s_]; else return sm.kbuf[s_];
         };
@@ -258,8 +274,11 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             if (lane == 0 && jv >= PNV) ready = mbar_test(&pv_empty[vs], (uint32_t)(((jv / PNV) & 1) ^ 1));
             if (!__shfl_sync(0xffffffffu, ready, 0)) return false;
             if (lane == 0) mbar_arrive_expect_tx(&pv_full[vs], kBlockBytes);
-            if (lane < kPagesPerBlock)
-                copy_page(&mvp, v_slot(vs), sm.vid[jv % kNMeta][lane], sm.meta[jv % kNMeta].h, &pv_full[vs]);
+            if (lane < kPagesPerBlock) {
+                const int id = sm.vid[jv % kNMeta][lane], hh = sm.meta[jv % kNMeta].h;
+                copy_page(&mvp, v_slot(vs), id, hh, &pv_full[vs]);
+                if constexpr (FP8) copy_scale(a.v_scale, id, hh, &sm.st8.vsc[vs][lane], &pv_full[vs]);
+            }
             __syncwarp();
             ++jv;
             return true;
@@ -349,6 +368,7 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                     if (lane < kPagesPerBlock) {
                         sm.vid[jk % kNMeta][lane] = my_id;
                         copy_page(&mkp, k_slot(ks), my_id, h, &pk_full[ks]);
+                        if constexpr (FP8) copy_scale(a.k_scale, my_id, h, &sm.st8.ksc[ks][lane], &pk_full[ks]);
                     }
                     __syncwarp();
                     ++jk;
@@ -373,12 +393,12 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             if (ok && jk >= PNK) ok = mbar_wait(&pk_empty[ks], (uint32_t)(((jk / PNK) & 1) ^ 1), a.err);
             if (ok) {
                 sm.meta[jk % kNMeta].flags = kFlagEnd;
-                mbar_arrive(&pk_full[ks]);
+                mbar_arrive_cnt(&pk_full[ks], FP8 ? C::kStageArrivals : 1u);
             }
             const int vs = jv % PNV;
             if constexpr (FP8) {
                 if (ok && jv >= PNV) ok = mbar_wait(&pv_empty[vs], (uint32_t)(((jv / PNV) & 1) ^ 1), a.err);
-                if (ok) mbar_arrive(&pv_full[vs]);
+                if (ok) mbar_arrive_cnt(&pv_full[vs], C::kStageArrivals);
             }
             // wait (bounded) for the copies still in flight; a stage reused
             // by an end marker had completed before its empty barrier passed
@@ -798,40 +818,29 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             const int ct = ci * 32 + lane;  // 0..95
             constexpr int NCT = C::kConvWarps * 32;
             const int ring = kconv ? C::kNK8 : C::kNV8;
+            const int tiles = kconv ? kNK : kNV;
             uint64_t *full8 = kconv ? sm.st8.k8_full : sm.st8.v8_full;
             uint64_t *empty8 = kconv ? sm.st8.k8_empty : sm.st8.v8_empty;
-            uint64_t *tile_full = kconv ? &sm.k_full[0] : &sm.v_full[0];
-            uint64_t *tile_empty = kconv ? &sm.k_empty[0] : &sm.v_empty[0];
-            uint8_t *tile = kconv ? sm.kbuf[0] : sm.vbuf[0];
-            const float *scales = kconv ? a.k_scale : a.v_scale;
             int units_seen = 0;
             for (int j = 0;; ++j) {
-                const int s8 = j % ring;
+                const int s8 = j % ring, tb = j % tiles;
                 if (!mbar_wait(&full8[s8], (uint32_t)((j / ring) & 1), a.err)) break;
                 const BlockMeta md = sm.meta[j % kNMeta];
+                uint64_t *tile_full = kconv ? &sm.k_full[tb] : &sm.v_full[tb];
+                uint64_t *tile_empty = kconv ? &sm.k_empty[tb] : &sm.v_empty[tb];
+                // the tile is free once S (K) or PV (V) of block j - tiles is done
+                if (j >= tiles && !mbar_wait(tile_empty, (uint32_t)(((j / tiles) & 1) ^ 1), a.err)) break;
                 if (md.flags & kFlagEnd) {
-                    // forward the end marker to the MMA issuer, once it has
-                    // taken the last K tile: k_full is a single barrier, and
-                    // an arrival before S_{j-1} completes would land two
-                    // phases ahead of the issuer's wait
-                    if (kconv) {
-                        if (j >= 1 && !mbar_wait(tile_empty, (uint32_t)((j - 1) & 1), a.err)) break;
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(tile_full);
-                    }
+                    // forward the end marker to the MMA issuer
+                    __syncwarp();
+                    if (kconv && lane == 0) mbar_arrive(tile_full);
                     break;
                 }
                 const uint8_t *src = kconv ? sm.st8.k8[s8] : sm.st8.v8[s8];
-                // this block's page scales (lanes 0..7), as f16 pairs
-                float sc = 0.f;
-                if (lane < kPagesPerBlock) {
-                    const int id = sm.vid[j % kNMeta][lane];
-                    if (id >= 0 && id < a.num_blocks) sc = __ldg(scales + (size_t)id * a.Hkv + md.h);
-                    if (!(sc >= 0.f && sc <= kMaxScale8)) {
-                        raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
-                        sc = 0.f;
-                    }
-                }
+                const float *scl = kconv ? sm.st8.ksc[s8] : sm.st8.vsc[s8];
+                uint8_t *tile = kconv ? sm.kbuf[tb] : sm.vbuf[tb];
+                if (lane < kPagesPerBlock && !(scl[lane] >= 0.f && scl[lane] <= kMaxScale8))
+                    raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
                 if (kconv && (md.flags & kFlagFirst)) {
                     // the unit's queries, bf16 -> f16 in place (rows < M)
                     if (!mbar_wait(&sm.st8.q_full, (uint32_t)(units_seen & 1), a.err)) break;
@@ -847,31 +856,39 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                         *qp = v;
                     }
                 }
-                // the tile is free once S_{j-1} (K) or PV_{j-1} (V) is done
-                if (j >= 1 && !mbar_wait(tile_empty, (uint32_t)((j - 1) & 1), a.err)) break;
                 const int t_end = kconv ? kNB : md.L + a.n_q - md.pos0;  // V rows from t_end on are zeroed
-                for (int i0 = 0; i0 < kNB * 8; i0 += NCT) {  // same trip count in every lane
-                    const int i = i0 + ct;
-                    const int row = i >> 3, g = i & 7;  // 16 columns: 16g .. 16g+15
-                    const float scf = __shfl_sync(0xffffffffu, sc, (row >> 4) & 7);
-                    if (i >= kNB * 8) continue;
-                    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-                    if (row < t_end) {
-                        const uint4 e = *reinterpret_cast<const uint4 *>(src + row * 128 + ((g ^ (row & 7)) << 4));
-                        const uint32_t s2 = pack_f16x2(scf, scf);
-                        lo.x = hmul2(e4m3x2_to_f16x2(e.x & 0xffffu), s2);
-                        lo.y = hmul2(e4m3x2_to_f16x2(e.x >> 16), s2);
-                        lo.z = hmul2(e4m3x2_to_f16x2(e.y & 0xffffu), s2);
-                        lo.w = hmul2(e4m3x2_to_f16x2(e.y >> 16), s2);
-                        hi.x = hmul2(e4m3x2_to_f16x2(e.z & 0xffffu), s2);
-                        hi.y = hmul2(e4m3x2_to_f16x2(e.z >> 16), s2);
-                        hi.z = hmul2(e4m3x2_to_f16x2(e.w & 0xffffu), s2);
-                        hi.w = hmul2(e4m3x2_to_f16x2(e.w >> 16), s2);
+                // item i: row i / 8, 16 columns 16 (i % 8) ..; four items in flight per thread
+                constexpr int kItems = kNB * 8, kPer = (kItems + NCT - 1) / NCT;
+#pragma unroll 1
+                for (int t0 = 0; t0 < kPer; t0 += 4) {
+                    uint4 e[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = ct + NCT * (t0 + u), row = i >> 3, g = i & 7;
+                        e[u] = make_uint4(0, 0, 0, 0);
+                        if (t0 + u < kPer && i < kItems && row < t_end)
+                            e[u] = *reinterpret_cast<const uint4 *>(src + row * 128 + ((g ^ (row & 7)) << 4));
                     }
-                    const int r8 = row & 7, c0 = (g & 3) * 2;
-                    uint8_t *dst = tile + (row >> 3) * 2048 + (g >> 2) * 1024 + r8 * 128;
-                    *reinterpret_cast<uint4 *>(dst + ((c0 ^ r8) << 4)) = lo;
-                    *reinterpret_cast<uint4 *>(dst + (((c0 + 1) ^ r8) << 4)) = hi;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = ct + NCT * (t0 + u), row = i >> 3, g = i & 7;
+                        if (t0 + u >= kPer || i >= kItems) continue;
+                        const float scf = scl[row >> 4];
+                        const uint32_t s2 = pack_f16x2(scf, scf);
+                        uint4 lo, hi;
+                        lo.x = hmul2(e4m3x2_to_f16x2(e[u].x & 0xffffu), s2);
+                        lo.y = hmul2(e4m3x2_to_f16x2(e[u].x >> 16), s2);
+                        lo.z = hmul2(e4m3x2_to_f16x2(e[u].y & 0xffffu), s2);
+                        lo.w = hmul2(e4m3x2_to_f16x2(e[u].y >> 16), s2);
+                        hi.x = hmul2(e4m3x2_to_f16x2(e[u].z & 0xffffu), s2);
+                        hi.y = hmul2(e4m3x2_to_f16x2(e[u].z >> 16), s2);
+                        hi.z = hmul2(e4m3x2_to_f16x2(e[u].w & 0xffffu), s2);
+                        hi.w = hmul2(e4m3x2_to_f16x2(e[u].w >> 16), s2);
+                        const int r8 = row & 7, c0 = (g & 3) * 2;
+                        uint8_t *dst = tile + (row >> 3) * 2048 + (g >> 2) * 1024 + r8 * 128;
+                        *reinterpret_cast<uint4 *>(dst + ((c0 ^ r8) << 4)) = lo;
+                        *reinterpret_cast<uint4 *>(dst + (((c0 + 1) ^ r8) << 4)) = hi;
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
