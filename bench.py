@@ -456,7 +456,8 @@ def main():
                          "traffic": recorded_traffic(args.config),
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s",
-                         "kernel": "pva_kernel (paged_verify_attn)",
+                         "kernel": ("pva_tc_kernel (tcgen05/TMEM)" if svpa.attn_kernel(st.params) == 2
+                                    else "pva_kernel (warp-level MMA)"),
                          "algorithmic_bytes_per_launch": st.attn_bytes},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4)},

@@ -89,6 +89,11 @@ typedef struct svpa_attn_params {
                                    128; FP8 pages with Hq / Hkv * n_q <= 64)   */
 } svpa_attn_params;
 
+/* The attention kernel svpa_paged_verify_attn runs for `p`: 1 = warp-level
+ * MMA kernel, 2 = tcgen05/TMEM kernel (p->variant, or the library's choice
+ * when p->variant is 0).  Same validation as svpa_attn_workspace_size. */
+svpa_status svpa_attn_kernel(const svpa_attn_params *p, int32_t *kernel);
+
 /* Bytes of workspace svpa_paged_verify_attn needs for `p` (split-KV partial
  * results and per-(sequence, kv head) tickets).  The workspace must be
  * zero-filled once before its first use; every completed call leaves its

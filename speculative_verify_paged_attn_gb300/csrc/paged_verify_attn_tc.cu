@@ -103,8 +103,8 @@ template <bool FP8>
 struct Stage8 {  // FP8 staging rings
     uint8_t k8[TcCfg<FP8>::kNK8][kTile8];
     uint8_t v8[TcCfg<FP8>::kNV8][kTile8];
-    float ksc[TcCfg<FP8>::kNK8][kPagesPerBlock];  // the staged pages' scales
-    float vsc[TcCfg<FP8>::kNV8][kPagesPerBlock];
+    float ksc[kNMeta][kPagesPerBlock];  // page scales of the blocks in flight
+    float vsc[kNMeta][kPagesPerBlock];
     uint64_t k8_full[TcCfg<FP8>::kNK8], k8_empty[TcCfg<FP8>::kNK8];
     uint64_t v8_full[TcCfg<FP8>::kNV8], v8_empty[TcCfg<FP8>::kNV8];
     uint64_t q_full;
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             if (lane < kPagesPerBlock) {
                 const int id = sm.vid[jv % kNMeta][lane], hh = sm.meta[jv % kNMeta].h;
                 copy_page(&mvp, v_slot(vs), id, hh, &pv_full[vs]);
-                if constexpr (FP8) copy_scale(a.v_scale, id, hh, &sm.st8.vsc[vs][lane], &pv_full[vs]);
+                if constexpr (FP8) copy_scale(a.v_scale, id, hh, &sm.st8.vsc[jv % kNMeta][lane], &pv_full[vs]);
             }
             __syncwarp();
             ++jv;
@@ -294,6 +294,9 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                     t0 = 0;
                     continue;
                 }
+                // nothing to do yet: back off so the spin does not take issue
+                // slots from the softmax warp sharing this scheduler
+                __nanosleep(64);
                 const unsigned long long now = global_ns();
                 if (t0 == 0) {
                     t0 = now;
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                     if (lane < kPagesPerBlock) {
                         sm.vid[jk % kNMeta][lane] = my_id;
                         copy_page(&mkp, k_slot(ks), my_id, h, &pk_full[ks]);
-                        if constexpr (FP8) copy_scale(a.k_scale, my_id, h, &sm.st8.ksc[ks][lane], &pk_full[ks]);
+                        if constexpr (FP8) copy_scale(a.k_scale, my_id, h, &sm.st8.ksc[jk % kNMeta][lane], &pk_full[ks]);
                     }
                     __syncwarp();
                     ++jk;
@@ -567,11 +570,24 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                         if (!((vis >> t) & 1ull)) s[64 * w + t] = -CUDART_INF_F;
                 }
             }
-            float pm[8];
+            // per-page maxima of the raw scores (FP8: a page's K scale
+            // multiplies its scores; scales are >= 0, so the maximum of the
+            // scaled scores is the largest scaled page maximum)
+            float pm[kPagesPerBlock];
 #pragma unroll
-            for (int x = 0; x < 8; ++x) pm[x] = s[x];
+            for (int x = 0; x < kPagesPerBlock; ++x) pm[x] = s[16 * x];
 #pragma unroll
-            for (int t = 8; t < kNB; ++t) pm[t & 7] = fmaxf(pm[t & 7], s[t]);
+            for (int t = 0; t < kNB; ++t)
+                if (t & 15) pm[t >> 4] = fmaxf(pm[t >> 4], s[t]);
+            float ksc[kPagesPerBlock], vsc[kPagesPerBlock];
+            if constexpr (FP8) {
+#pragma unroll
+                for (int x = 0; x < kPagesPerBlock; ++x) {
+                    ksc[x] = sm.st8.ksc[j % kNMeta][x];
+                    vsc[x] = sm.st8.vsc[j % kNMeta][x];
+                    if (pm[x] != -CUDART_INF_F) pm[x] *= ksc[x];
+                }
+            }
             const float mraw = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                                      fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
             const float mx = mraw == -CUDART_INF_F ? -CUDART_INF_F : mraw * a.scale_log2;
@@ -585,6 +601,11 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             }
             const float neg_m = m_ref == -CUDART_INF_F ? 0.f : -m_ref;
             const float sc = a.scale_log2;
+            if constexpr (FP8) {
+                // V_j's page scales multiply P (PV reads raw E4M3 values as f16)
+                // once the V converters are done with block j
+                mbar_wait(&sm.v_full[j % kNV], (uint32_t)((j / kNV) & 1), a.err);
+            }
             // P_j as bf16 pairs into the first half of S_j's TMEM columns
             const uint32_t pt = tmem + kTmemS + (uint32_t)(j & 1) * kNB + lane_off;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
@@ -593,10 +614,14 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                 uint32_t w[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p0 = live ? ex2_approx(fmaf(s[c * 64 + 2 * e], sc, neg_m)) : 0.f;
-                    const float p1 = live ? ex2_approx(fmaf(s[c * 64 + 2 * e + 1], sc, neg_m)) : 0.f;
+                    const int pg = (c * 64 + 2 * e) >> 4;  // page of both columns
+                    // FP8: a page whose K scale is 0 has scores 0; keep the
+                    // multiplier positive so that masked (-inf) columns stay -inf
+                    const float scp = FP8 ? fmaxf(sc * ksc[pg], 1e-30f) : sc;
+                    const float p0 = live ? ex2_approx(fmaf(s[c * 64 + 2 * e], scp, neg_m)) : 0.f;
+                    const float p1 = live ? ex2_approx(fmaf(s[c * 64 + 2 * e + 1], scp, neg_m)) : 0.f;
                     ls[e & 3] += p0 + p1;
-                    w[e] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+                    w[e] = FP8 ? pack_f16x2(p0 * vsc[pg], p1 * vsc[pg]) : pack_bf16x2(p0, p1);
                 }
                 tmem_st32(pt + c * 32, w);
             }
@@ -837,7 +862,7 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                     break;
                 }
                 const uint8_t *src = kconv ? sm.st8.k8[s8] : sm.st8.v8[s8];
-                const float *scl = kconv ? sm.st8.ksc[s8] : sm.st8.vsc[s8];
+                const float *scl = kconv ? sm.st8.ksc[j % kNMeta] : sm.st8.vsc[j % kNMeta];
                 uint8_t *tile = kconv ? sm.kbuf[tb] : sm.vbuf[tb];
                 if (lane < kPagesPerBlock && !(scl[lane] >= 0.f && scl[lane] <= kMaxScale8))
                     raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
@@ -873,17 +898,15 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                     for (int u = 0; u < 4; ++u) {
                         const int i = ct + NCT * (t0 + u), row = i >> 3, g = i & 7;
                         if (t0 + u >= kPer || i >= kItems) continue;
-                        const float scf = scl[row >> 4];
-                        const uint32_t s2 = pack_f16x2(scf, scf);
                         uint4 lo, hi;
-                        lo.x = hmul2(e4m3x2_to_f16x2(e[u].x & 0xffffu), s2);
-                        lo.y = hmul2(e4m3x2_to_f16x2(e[u].x >> 16), s2);
-                        lo.z = hmul2(e4m3x2_to_f16x2(e[u].y & 0xffffu), s2);
-                        lo.w = hmul2(e4m3x2_to_f16x2(e[u].y >> 16), s2);
-                        hi.x = hmul2(e4m3x2_to_f16x2(e[u].z & 0xffffu), s2);
-                        hi.y = hmul2(e4m3x2_to_f16x2(e[u].z >> 16), s2);
-                        hi.z = hmul2(e4m3x2_to_f16x2(e[u].w & 0xffffu), s2);
-                        hi.w = hmul2(e4m3x2_to_f16x2(e[u].w >> 16), s2);
+                        lo.x = e4m3x2_to_f16x2(e[u].x & 0xffffu);
+                        lo.y = e4m3x2_to_f16x2(e[u].x >> 16);
+                        lo.z = e4m3x2_to_f16x2(e[u].y & 0xffffu);
+                        lo.w = e4m3x2_to_f16x2(e[u].y >> 16);
+                        hi.x = e4m3x2_to_f16x2(e[u].z & 0xffffu);
+                        hi.y = e4m3x2_to_f16x2(e[u].z >> 16);
+                        hi.z = e4m3x2_to_f16x2(e[u].w & 0xffffu);
+                        hi.w = e4m3x2_to_f16x2(e[u].w >> 16);
                         const int r8 = row & 7, c0 = (g & 3) * 2;
                         uint8_t *dst = tile + (row >> 3) * 2048 + (g >> 2) * 1024 + r8 * 128;
                         *reinterpret_cast<uint4 *>(dst + ((c0 ^ r8) << 4)) = lo;

@@ -144,6 +144,15 @@ const char *svpa_status_string(svpa_status s) {
 
 int32_t svpa_version(void) { return 100; }
 
+svpa_status svpa_attn_kernel(const svpa_attn_params *p, int32_t *kernel) {
+    if (!kernel) return SVPA_ERR_INVALID_ARG;
+    AttnPlan pl;
+    const svpa_status s = plan_attn(p, &pl);
+    if (s != SVPA_OK) return s;
+    *kernel = pl.use_tc ? 2 : 1;
+    return SVPA_OK;
+}
+
 svpa_status svpa_attn_workspace_size(const svpa_attn_params *p, size_t *bytes) {
     if (!bytes) return SVPA_ERR_INVALID_ARG;
     AttnPlan pl;

@@ -25,7 +25,7 @@ SVPA_KV_FP8_E4M3 = 1
 STATUS = {0: "SVPA_OK", 1: "SVPA_ERR_INVALID_ARG", 2: "SVPA_ERR_UNSUPPORTED", 3: "SVPA_ERR_CUDA",
           4: "SVPA_ERR_OUT_OF_BLOCKS", 5: "SVPA_ERR_BAD_BLOCK", 6: "SVPA_ERR_WORKSPACE",
           7: "SVPA_ERR_TIMEOUT"}
-EXPORTS = ("svpa_attn_workspace_size", "svpa_paged_verify_attn", "svpa_spec_accept_workspace_size",
+EXPORTS = ("svpa_attn_workspace_size", "svpa_attn_kernel", "svpa_paged_verify_attn", "svpa_spec_accept_workspace_size",
            "svpa_spec_accept", "svpa_spec_accept_tree", "svpa_block_table_commit", "svpa_check_error",
            "svpa_status_string", "svpa_version", "svpa_paged_verify_attn_noalloc")
 
@@ -59,6 +59,7 @@ def load(path: str = LIB_PATH):
     L = ctypes.CDLL(path)
     P, I, U, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
     L.svpa_attn_workspace_size.argtypes = [ctypes.POINTER(AttnParams), ctypes.POINTER(U)]
+    L.svpa_attn_kernel.argtypes = [ctypes.POINTER(AttnParams), ctypes.POINTER(I)]
     L.svpa_paged_verify_attn.argtypes = [ctypes.POINTER(AttnParams)] + [P] * 11 + [U, P, P]
     L.svpa_spec_accept_workspace_size.argtypes = [I, I, ctypes.POINTER(U)]
     L.svpa_spec_accept.argtypes = [I, I, I] + [P] * 9 + [U, P, P]
@@ -107,6 +108,13 @@ def attn_workspace_size(params: AttnParams) -> int:
     _check(load().svpa_attn_workspace_size(ctypes.byref(params), ctypes.byref(n)),
            "svpa_attn_workspace_size")
     return n.value
+
+
+def attn_kernel(params: AttnParams) -> int:
+    """The attention kernel the library runs for `params`: 1 warp-level MMA, 2 tcgen05."""
+    k = ctypes.c_int32(0)
+    _check(load().svpa_attn_kernel(ctypes.byref(params), ctypes.byref(k)), "svpa_attn_kernel")
+    return k.value
 
 
 def spec_accept_workspace_size(batch: int, vocab: int) -> int:

@@ -48,6 +48,12 @@ def test_workspace_size_and_validation(lib):
         kw.update(bad)
         with pytest.raises(svpa.SvpaError):
             svpa.attn_workspace_size(svpa.attn_params(**kw))
+    # which kernel runs: warp-level MMA for few rows per kv head, tcgen05 for many
+    assert svpa.attn_kernel(svpa.attn_params(32, 5, 32, 32, 128, 256, 4096)) == 1
+    assert svpa.attn_kernel(svpa.attn_params(64, 6, 64, 8, 128, 2049, 100000)) == 2
+    assert svpa.attn_kernel(svpa.attn_params(64, 6, 64, 8, 128, 2049, 100000, variant=1)) == 1
+    assert svpa.attn_kernel(svpa.attn_params(16, 6, 64, 8, 128, 2049, 100000, kv_fp8=True)) == 2
+    assert svpa.attn_kernel(svpa.attn_params(16, 29, 32, 8, 128, 600, 100000, kv_fp8=True)) == 1
     # FP8 pages on the tcgen05 kernel take at most 64 rows per kv head
     with pytest.raises(svpa.SvpaError) as e:
         svpa.attn_workspace_size(svpa.attn_params(2, 9, 64, 8, 128, 8, 16, kv_fp8=True, variant=2))
