@@ -85,11 +85,11 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     }
     int sp = p->split_pages;
     if (sp == 0) {
-        // about 16 units of work per SM (sequences taken at their maximum
-        // length): enough for the dynamic scheduler to balance the load
-        // without multiplying split partials
+        // about 16 units of work per resident CTA slot (sequences taken at
+        // their maximum length): enough for the dynamic scheduler to balance
+        // the load without multiplying split partials
         const double units = (double)std::max(1, p->batch) * p->num_kv_heads;
-        const double per = units * p->max_blocks_per_seq / (16.0 * sm_count());
+        const double per = units * p->max_blocks_per_seq / (16.0 * pl->grid_slots);
         int pw = 16;
         while (pw * 2 <= per && pw < 1024) pw *= 2;
         // keep a split's partial rows (written, then read back by the merge)
