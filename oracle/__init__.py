@@ -20,6 +20,12 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*.py``):
   expected_accepted, speedup
                        pinned (the worked example: alpha >= 0.85, r ~ 0.08
                        gives eta >= 2.8)
+  kv_append            pinned (gathered history ++ new rows, copy-on-write leaves
+                       the other holders' pages untouched, conservation of
+                       blocks; FP8: the scale rule on a worked page, decoded
+                       values within half a code of the data)
+  e4m3_encode          pinned (equals torch.float8_e4m3fn rounding on every
+                       in-range value tested; saturation at 448)
 """
 from __future__ import annotations
 
@@ -72,6 +78,10 @@ def _load():
             lib.oracle_bf16_to_double.restype = D
             lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_to_double.restype = D
+            lib.oracle_kv_append.argtypes = [I] * 8 + [P] * 11
+            lib.oracle_kv_append.restype = I
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = I
             _lib = lib
@@ -236,6 +246,47 @@ def block_table_commit(block_table, context_lens, accepted_len, refcount, free_s
         raise OracleError(f"oracle_block_table_commit failed with status {rc}")
     return dict(block_table=bt, context_lens=cl, refcount=rcnt, free_stack=fs,
                 free_top=int(ft[0]), k_pool=kp, v_pool=vp)
+
+
+def kv_append(new_k, new_v, block_table, context_lens, refcount, free_stack, free_top, k_pool,
+              v_pool, k_scale=None, v_scale=None, *, block_size=16):
+    """Append the new rows on copies of the inputs; returns the updated copies.
+
+    new_k, new_v: bf16 [B, n_new, Hkv, D]; pools bf16 or float8_e4m3fn (or raw
+    uint16 / uint8 arrays) [num_blocks, Hkv, 16, D]; scales fp32 for FP8.
+    Returns dict(block_table, refcount, free_stack, free_top, k_pool, v_pool,
+    k_scale, v_scale) -- pools as raw uint16 (bf16 bits) or uint8 (E4M3 bytes).
+    """
+    lib = _load()
+    nk = _c(new_k, np.uint16)
+    nv = _c(new_v, np.uint16)
+    B, n_new, Hkv, D = nk.shape
+    bt = _c(block_table, np.int32).copy()
+    cl = _c(context_lens, np.int32)
+    rcnt = _c(refcount, np.int32).copy()
+    fs = _c(free_stack, np.int32).copy()
+    ft = np.array([int(free_top)], np.int32)
+    isz = k_pool.element_size() if hasattr(k_pool, "element_size") else np.asarray(k_pool).itemsize
+    raw = np.uint8 if isz == 1 else np.uint16
+    kp = _c(k_pool, raw).copy()
+    vp = _c(v_pool, raw).copy()
+    fp8 = isz == 1
+    ks = _c(k_scale, np.float32).copy() if fp8 else None
+    vs = _c(v_scale, np.float32).copy() if fp8 else None
+    rc = lib.oracle_kv_append(B, n_new, Hkv, D, block_size, bt.shape[1], rcnt.shape[0], int(fp8),
+                              _ptr(nk), _ptr(nv), _ptr(bt), _ptr(cl), _ptr(rcnt), _ptr(fs), _ptr(ft),
+                              _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs))
+    if rc != 0:
+        raise OracleError(f"oracle_kv_append failed with status {rc}")
+    return dict(block_table=bt, refcount=rcnt, free_stack=fs, free_top=int(ft[0]), k_pool=kp,
+                v_pool=vp, k_scale=ks, v_scale=vs)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """OCP E4M3 codes (uint8) of fp32 values: nearest, ties to even, saturating at 448."""
+    lib = _load()
+    a = np.asarray(x, np.float32).ravel()
+    return np.array([lib.oracle_e4m3_encode(float(v)) for v in a], np.uint8).reshape(np.shape(x))
 
 
 def expected_accepted(alpha) -> float:

@@ -518,6 +518,170 @@ int oracle_block_table_commit(int B, int n_q, int BS, int max_blocks,
 }
 
 /* ------------------------------------------------------------------ */
+/* paged K/V append (allocation, copy-on-write, FP8 quantise-on-write) */
+/* ------------------------------------------------------------------ */
+
+/* OCP E4M3 ("fn") code of a finite fp32 value: round to nearest, ties to
+ * even, saturating at +-448 (the largest finite code, S.1111.110); written
+ * from the format's definition: 4 exponent bits (bias 7), 3 mantissa bits,
+ * subnormals at exponent field 0 with quantum 2^-9. */
+uint8_t oracle_e4m3_encode(float xf) {
+    double x = (double)xf;
+    uint8_t sign = 0;
+    if (signbit(x)) { sign = 0x80; x = -x; } /* E4M3 has a signed zero: -0 is 0x80 */
+    if (!(x == x)) return 0x7F; /* NaN stays NaN (never produced here) */
+    if (x >= 448.0) return sign | 0x7E;
+    int e = -6; /* exponent of the quantum's binade; subnormals share e = -6 */
+    if (x >= ldexp(1.0, -6)) e = (int)floor(log2(x));
+    /* guard log2 rounding at exact powers of two */
+    while (e > -6 && x < ldexp(1.0, e)) --e;
+    while (x >= ldexp(1.0, e + 1)) ++e;
+    double q = ldexp(1.0, e - 3); /* spacing of codes in this binade */
+    double n = x / q;            /* exact: q is a power of two */
+    double fl = floor(n), fr = n - fl;
+    double r = fl;
+    if (fr > 0.5 || (fr == 0.5 && fmod(fl, 2.0) != 0.0)) r = fl + 1.0;
+    if (e == -6 && r < 8.0) return sign | (uint8_t)r; /* subnormal (or zero) */
+    if (r >= 16.0) { r = 8.0; ++e; }
+    int ef = e + 7;
+    if (ef > 15 || (ef == 15 && r > 14.0)) return sign | 0x7E; /* saturate */
+    return sign | (uint8_t)(ef << 3) | (uint8_t)((int)r - 8);
+}
+
+static float bf16_bits_to_float(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/*
+ * Append n_new token rows to every sequence's paged K/V ("Speculative
+ * Decoding & KV-Cache PagedAttention in Enterprise LLM Serving",
+ * PagedKVCacheManager.EnsureCapacityAndAppendToken: a page past the table's
+ * end is taken from the free pool with count 1; a page whose count is above 1
+ * is cloned before it is written, the shared block losing one reference;
+ * "The Sub-Millisecond Speculative Decoding Meltdown", "Custom FP8 Quantized
+ * Memory Block Layout": e4m3 pages with per-block K and V scales).
+ *
+ * Sequence b's rows go to positions L_b .. L_b + n_new - 1 (L_b =
+ * context_lens[b], which is not changed: the commit step sets the new
+ * length).  Sequences are handled in index order; pages in increasing order.
+ * A page holding history (index * BS < L_b) must already be mapped.
+ * Free pops take free_stack[--free_top].
+ *
+ * FP8 pools (quantise-on-write): for every (written page, kv head) the scale
+ * becomes amax / 448 (1 when amax = 0), amax being the largest magnitude of
+ * the page's history values (stored code times the old scale, an fp32
+ * product) and of the new rows (bf16 values); history codes are re-encoded
+ * from their decoded value only when the scale changes; every code is
+ * e4m3(value / scale) with one fp32 division; slots past the last row are 0.
+ *
+ * new_k, new_v: bf16 bits [B, n_new, Hkv, D]; pools [num_blocks, Hkv, BS, D]
+ * of bf16 bits (fp8 = 0) or E4M3 bytes (fp8 = 1); scales [num_blocks, Hkv].
+ */
+int oracle_kv_append(int B, int n_new, int Hkv, int D, int BS, int max_blocks, int num_blocks,
+                     int fp8, const uint16_t *new_k, const uint16_t *new_v, int32_t *block_table,
+                     const int32_t *context_lens, int32_t *refcount, int32_t *free_stack,
+                     int32_t *free_top, void *k_pool, void *v_pool, float *k_scale,
+                     float *v_scale) {
+    if (B < 0 || n_new < 1 || Hkv < 1 || D < 1 || BS < 1 || max_blocks < 1 || num_blocks < 1)
+        return ORC_ERR_ARG;
+    if (fp8 && (!k_scale || !v_scale)) return ORC_ERR_ARG;
+    const size_t eb = fp8 ? 1 : 2;
+    const size_t page_bytes = (size_t)Hkv * BS * D * eb; /* one block, all heads */
+    for (int b = 0; b < B; ++b) {
+        const long L = context_lens[b], end = L + n_new;
+        if (L < 0 || (end + BS - 1) / BS > max_blocks) return ORC_ERR_ARG;
+        /* map, allocate or clone every page the rows touch */
+        for (long i = L / BS; i <= (end - 1) / BS; ++i) {
+            int32_t *ent = &block_table[(long)b * max_blocks + i];
+            if (*ent < 0) {
+                if (i * BS < L) return ORC_ERR_ARG; /* history without a page */
+                if (*free_top <= 0) return ORC_ERR_OUT_OF_BLOCKS;
+                int32_t blk = free_stack[--(*free_top)];
+                if (blk < 0 || blk >= num_blocks) return ORC_ERR_BAD_BLOCK;
+                refcount[blk] = 1;
+                *ent = blk;
+                continue;
+            }
+            if (*ent >= num_blocks) return ORC_ERR_BAD_BLOCK;
+            if (refcount[*ent] > 1) { /* shared: copy-on-write */
+                if (*free_top <= 0) return ORC_ERR_OUT_OF_BLOCKS;
+                int32_t blk = free_stack[--(*free_top)];
+                if (blk < 0 || blk >= num_blocks) return ORC_ERR_BAD_BLOCK;
+                memcpy((char *)k_pool + (size_t)blk * page_bytes,
+                       (char *)k_pool + (size_t)*ent * page_bytes, page_bytes);
+                memcpy((char *)v_pool + (size_t)blk * page_bytes,
+                       (char *)v_pool + (size_t)*ent * page_bytes, page_bytes);
+                if (fp8)
+                    for (int h = 0; h < Hkv; ++h) {
+                        k_scale[(long)blk * Hkv + h] = k_scale[(long)*ent * Hkv + h];
+                        v_scale[(long)blk * Hkv + h] = v_scale[(long)*ent * Hkv + h];
+                    }
+                refcount[*ent] -= 1;
+                refcount[blk] = 1;
+                *ent = blk;
+            }
+        }
+        /* write the rows */
+        for (long i = L / BS; i <= (end - 1) / BS; ++i) {
+            const int32_t blk = block_table[(long)b * max_blocks + i];
+            const long ps = i * BS;
+            const long hist = L > ps ? (L - ps < BS ? L - ps : BS) : 0; /* history slots in the page */
+            const long vend = end - ps < BS ? end - ps : BS;            /* slots in use after the write */
+            for (int kv = 0; kv < 2; ++kv) {
+                const uint16_t *src = kv ? new_v : new_k;
+                char *pool = (char *)(kv ? v_pool : k_pool);
+                float *scale = kv ? v_scale : k_scale;
+                for (int h = 0; h < Hkv; ++h) {
+                    const size_t tile = ((size_t)blk * Hkv + h) * BS * D; /* element offset of (blk, h) */
+                    if (!fp8) {
+                        uint16_t *t16 = (uint16_t *)pool + tile;
+                        for (long s = hist; s < vend; ++s)
+                            memcpy(t16 + s * D, src + (((size_t)b * n_new + (ps + s - L)) * Hkv + h) * D,
+                                   (size_t)D * 2);
+                        continue;
+                    }
+                    uint8_t *t8 = (uint8_t *)pool + tile;
+                    const float old_scale = scale[(long)blk * Hkv + h];
+                    float amax = 0.f;
+                    for (long s = 0; s < hist; ++s)
+                        for (int d = 0; d < D; ++d) {
+                            volatile float v = (float)oracle_e4m3_to_double(t8[s * D + d]) * old_scale;
+                            float a = v < 0 ? -v : v;
+                            if (a > amax) amax = a;
+                        }
+                    for (long s = hist; s < vend; ++s)
+                        for (int d = 0; d < D; ++d) {
+                            float v = bf16_bits_to_float(src[(((size_t)b * n_new + (ps + s - L)) * Hkv + h) * D + d]);
+                            float a = v < 0 ? -v : v;
+                            if (a > amax) amax = a;
+                        }
+                    volatile float new_scale = amax > 0.f ? amax / 448.0f : 1.0f;
+                    if (hist > 0 && new_scale != old_scale)
+                        for (long s = 0; s < hist; ++s)
+                            for (int d = 0; d < D; ++d) {
+                                volatile float v = (float)oracle_e4m3_to_double(t8[s * D + d]) * old_scale;
+                                volatile float q = v / new_scale;
+                                t8[s * D + d] = oracle_e4m3_encode(q);
+                            }
+                    for (long s = hist; s < vend; ++s)
+                        for (int d = 0; d < D; ++d) {
+                            float v = bf16_bits_to_float(src[(((size_t)b * n_new + (ps + s - L)) * Hkv + h) * D + d]);
+                            volatile float q = v / new_scale;
+                            t8[s * D + d] = oracle_e4m3_encode(q);
+                        }
+                    for (long s = vend; s < BS; ++s) memset(t8 + s * D, 0, (size_t)D);
+                    scale[(long)blk * Hkv + h] = new_scale;
+                }
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
 /* speed-up model                                                      */
 /* ------------------------------------------------------------------ */
 
