@@ -208,6 +208,65 @@ class Step:
                                 num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim, kv_fp8=wl.kv_fp8)
 
 
+class Append:
+    """The K/V append of the same workload (n_q rows per sequence) on its own
+    cache state, restored before every call so that each call does the same
+    work: tables, counts and free stack, and for FP8 the partly filled pages
+    (and scales) whose history a call may requantise."""
+
+    def __init__(self, wl: W.Workload, seed: int, dev: torch.device):
+        inp = W.make_append(wl, seed + 17, device=dev)
+        self.inp, self.fp8 = inp, wl.kv_fp8
+        self.kp = inp.k_pool.view(torch.uint8) if self.fp8 else inp.k_pool
+        self.vp = inp.v_pool.view(torch.uint8) if self.fp8 else inp.v_pool
+        self.bt0, self.rc0, self.fs0 = inp.block_table.clone(), inp.refcount.clone(), inp.free_stack.clone()
+        self.ft0 = torch.tensor([inp.free_top], dtype=torch.int32, device=dev)
+        self.ft = self.ft0.clone()
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        L = inp.context_lens.long()
+        first = inp.block_table.gather(1, (L // 16)[:, None]).squeeze(1)
+        self.partial = first[(L % 16 != 0) & (first >= 0)].long()
+        if self.fp8:
+            self.saved = [t[self.partial].clone() for t in (self.kp, self.vp, inp.k_scale, inp.v_scale)]
+        self.bytes = inp.write_bytes()
+
+    def reset(self):
+        inp = self.inp
+        inp.block_table.copy_(self.bt0)
+        inp.refcount.copy_(self.rc0)
+        inp.free_stack.copy_(self.fs0)
+        self.ft.copy_(self.ft0)
+        if self.fp8:
+            for t, v in zip((self.kp, self.vp, inp.k_scale, inp.v_scale), self.saved):
+                t[self.partial] = v
+
+    def run(self):
+        inp = self.inp
+        svpa.kv_append(inp.new_k, inp.new_v, inp.block_table, inp.context_lens, inp.refcount,
+                       inp.free_stack, self.ft, self.kp, self.vp, error_flag=self.err,
+                       k_scale=inp.k_scale, v_scale=inp.v_scale)
+
+
+def time_append(ap: Append, steps: int, warmup: int, stream) -> float:
+    """Average device time (ms) of one svpa_kv_append, L2 flushed before each."""
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=ap.ft.device)
+    for _ in range(warmup):
+        ap.reset()
+        ap.run()
+    ms = []
+    for _ in range(steps):
+        ap.reset()
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ap.run()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    assert svpa.check_error(ap.err) == 0, "device error in the append"
+    return sum(ms) / len(ms)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -429,6 +488,12 @@ def main():
     e2e = max_over_ranks(e2e_local, world, dev)
     e2e_value = total_bytes / (e2e * 1e-3) / 1e9
 
+    # the K/V append that precedes a verification step, timed on its own
+    ap = Append(wl, seed, dev)
+    app_ms = time_append(ap, K, args.warmup, stream)
+    app_bytes = ap.bytes
+    del ap
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, cores, sample, _ = cpu_baseline(wl, seed)
@@ -450,6 +515,8 @@ def main():
             "spec_accept_us": round(sum(samp_ms) / K * 1e3, 2),
             "spec_accept_rows_per_s": round(rows_per_s, 1),
             "commit_us": round(sum(comm_ms) / K * 1e3, 2),
+            "kv_append_us": round(app_ms * 1e3, 2),
+            "kv_append_gbs": round(app_bytes / (app_ms * 1e-3) / 1e9, 2),
             "kv_bytes_per_step": st.kv_bytes,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),

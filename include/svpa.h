@@ -2,8 +2,11 @@
  * svpa.h -- C ABI of libsvpa.so: the target-model verification step of
  * speculative decoding over a paged KV cache, on one NVIDIA GB300 (sm_103a).
  *
- * Three operations, called in this order once per verification step:
+ * The operations of one verification step, in call order:
  *
+ *   svpa_kv_append           write the n_q new K/V rows of every sequence into
+ *                            its pages (block allocation, copy-on-write of a
+ *                            shared page, FP8 requantisation).
  *   svpa_paged_verify_attn   the n_q verification queries of every sequence
  *                            (the last committed token plus the gamma drafts,
  *                            or the nodes of a draft tree) attend over the
@@ -281,6 +284,75 @@ svpa_status svpa_block_table_commit(int32_t batch, int32_t n_q,
                                     void *v_pool, int32_t num_kv_heads,
                                     int32_t head_dim, int32_t kv_dtype,
                                     int32_t *error_flag, void *stream);
+
+/*
+ * Append n_new K/V rows to every sequence's pages (the write that precedes
+ * verification: the draft tokens' keys and values must be in the cache before
+ * the verify attention reads them).
+ *
+ * Sources: "Speculative Decoding & KV-Cache PagedAttention in Enterprise LLM
+ * Serving", PagedKVCacheManager.EnsureCapacityAndAppendToken (a page past the
+ * table's end comes from the free pool with reference count 1; a page whose
+ * count is above 1 is cloned before the write and the shared block loses one
+ * reference) and its shared-prefix section; "The Sub-Millisecond Speculative
+ * Decoding Meltdown", "Custom FP8 Quantized Memory Block Layout" (E4M3 pages
+ * with per-block K and V scales).
+ *
+ * With L = context_lens[b] (read only; svpa_block_table_commit sets the new
+ * length), row t of sequence b goes to position L + t, t = 0..n_new-1, for
+ * every kv head.  For each logical page i from L/16 to (L+n_new-1)/16:
+ *  - block_table[b][i] == -1: a block is popped (free_stack[--*free_top]),
+ *    its count set to 1 and stored in the table.  A page that holds history
+ *    (i*16 < L) without a block raises SVPA_DEVERR_BAD_VALUE.
+ *  - a mapped block whose count is above 1: when other sequences of the same
+ *    call also write into it, exactly one of them (which one is unspecified)
+ *    keeps it and writes in place; every other holder pops a fresh block,
+ *    copies the whole page (and, for FP8, its two scales) into it, stores it
+ *    in its table and the shared block loses one reference.  A block shared
+ *    with a sequence outside the call is always cloned.
+ *  - otherwise the rows are written in place.
+ * Blocks popped, and which holder keeps a shared page, may differ from a
+ * sequential pass in sequence order; each sequence's gathered content,
+ * the counts of the blocks it maps and the number of blocks popped do not.
+ *
+ * FP8 pools (kv_dtype = SVPA_KV_FP8_E4M3) are requantised on write, per
+ * (page, kv head) and separately for K and V:
+ *   amax  = max |x| over the page's history values (stored code x current
+ *           scale, one fp32 product) and the new bf16 values;
+ *   scale = amax / 448 (one fp32 division; 1 when amax is 0);
+ *   history codes are re-encoded from their values only when the scale
+ *   changes; new codes = e4m3(x / scale), round to nearest even, saturating
+ *   at +-448; slots past the last row of the page are set to 0.
+ * bf16 pools receive the row bits unchanged; their slots past the last row
+ * are left as they were.
+ *
+ *  new_k, new_v  bf16 [B, n_new, Hkv, D], 16-byte aligned
+ *  block_table   int32 [B, max_blocks_per_seq] (in/out)
+ *  context_lens  int32 [B]
+ *  refcount      int32 [num_blocks] (in/out)
+ *  free_stack    int32 [num_blocks] (in/out), free_top int32 [1] (in/out)
+ *  k_pool, v_pool [num_blocks, Hkv, 16, D] bf16 or E4M3 bytes (in/out),
+ *                16-byte aligned
+ *  k_scale, v_scale fp32 [num_blocks, Hkv] (in/out; FP8 only, else NULL)
+ *  error_flag    int32 [1], zero before the call
+ * Limits: 1 <= n_new <= 4096, 8 <= head_dim <= 1024 and a multiple of 8,
+ * block_size 16; else SVPA_ERR_INVALID_ARG before anything is enqueued.
+ * Device errors: an empty free stack sets SVPA_DEVERR_FREE_OVERFLOW
+ * (svpa_check_error: SVPA_ERR_OUT_OF_BLOCKS); a block id outside the pool
+ * SVPA_DEVERR_BAD_BLOCK; a bad length or a mapped block with count 0
+ * SVPA_DEVERR_BAD_VALUE.  When any bit is set no row is written; the blocks
+ * already popped stay mapped with count 1, so tables, counts and the free
+ * stack remain consistent.  Two kernels on `stream`.
+ */
+svpa_status svpa_kv_append(int32_t batch, int32_t n_new, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size,
+                           int32_t max_blocks_per_seq, int32_t num_blocks,
+                           int32_t kv_dtype, const void *new_k,
+                           const void *new_v, int32_t *block_table,
+                           const int32_t *context_lens, int32_t *refcount,
+                           int32_t *free_stack, int32_t *free_top,
+                           void *k_pool, void *v_pool, float *k_scale,
+                           float *v_scale, int32_t *error_flag, void *stream);
 
 /*
  * svpa_paged_verify_attn without a caller workspace, for callers that may not

@@ -25,6 +25,7 @@ SOURCES = {
     "paged_verify_attn_tc.cu": [],
     "spec_accept.cu": ["-fmad=false"],
     "block_table_commit.cu": [],
+    "kv_append.cu": ["-fmad=false"],
     "svpa_noalloc.cu": [],
 }
 

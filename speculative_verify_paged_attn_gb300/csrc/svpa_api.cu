@@ -429,6 +429,48 @@ svpa_status svpa_block_table_commit(int32_t batch, int32_t n_q, int32_t block_si
     return from_cuda(launch_block_table_commit(a, static_cast<cudaStream_t>(stream)));
 }
 
+svpa_status svpa_kv_append(int32_t batch, int32_t n_new, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t max_blocks_per_seq, int32_t num_blocks, int32_t kv_dtype,
+                           const void *new_k, const void *new_v, int32_t *block_table,
+                           const int32_t *context_lens, int32_t *refcount, int32_t *free_stack,
+                           int32_t *free_top, void *k_pool, void *v_pool, float *k_scale, float *v_scale,
+                           int32_t *error_flag, void *stream) {
+    if (batch < 0 || n_new < 1 || n_new > kMaxAppendRows || num_kv_heads < 1 || head_dim < 8 ||
+        head_dim > 1024 || head_dim % 8 != 0 || block_size != kBlockSize || max_blocks_per_seq < 1 ||
+        num_blocks < 1 || (kv_dtype != SVPA_KV_BF16 && kv_dtype != SVPA_KV_FP8_E4M3))
+        return SVPA_ERR_INVALID_ARG;
+    if (batch == 0) return SVPA_OK;
+    const bool fp8 = kv_dtype == SVPA_KV_FP8_E4M3;
+    if (!new_k || !new_v || !block_table || !context_lens || !refcount || !free_stack || !free_top || !k_pool ||
+        !v_pool || !error_flag || (fp8 && (!k_scale || !v_scale)))
+        return SVPA_ERR_INVALID_ARG;
+    if (!aligned16(new_k) || !aligned16(new_v) || !aligned16(k_pool) || !aligned16(v_pool))
+        return SVPA_ERR_INVALID_ARG;
+    AppendArgs a;
+    memset(&a, 0, sizeof a);
+    a.new_k = static_cast<const uint16_t *>(new_k);
+    a.new_v = static_cast<const uint16_t *>(new_v);
+    a.block_table = block_table;
+    a.context_lens = context_lens;
+    a.refcount = refcount;
+    a.free_stack = free_stack;
+    a.free_top = free_top;
+    a.k_pool = static_cast<uint8_t *>(k_pool);
+    a.v_pool = static_cast<uint8_t *>(v_pool);
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.err = error_flag;
+    a.page_bytes = (size_t)num_kv_heads * kBlockSize * head_dim * (fp8 ? 1 : 2);
+    a.B = batch;
+    a.n_new = n_new;
+    a.Hkv = num_kv_heads;
+    a.D = head_dim;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.fp8 = fp8;
+    return from_cuda(launch_kv_append(a, static_cast<cudaStream_t>(stream)));
+}
+
 svpa_status svpa_check_error(const int32_t *error_flag, void *stream) {
     if (!error_flag) return SVPA_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -107,4 +107,25 @@ struct CommitArgs {
 };
 cudaError_t launch_block_table_commit(const CommitArgs &a, cudaStream_t stream);
 
+// Paged K/V append (allocation, copy-on-write, FP8 quantise-on-write).
+constexpr int kMaxAppendRows = 4096;                           // n_new limit
+constexpr int kMaxAppendPages = kMaxAppendRows / kBlockSize + 1;  // pages one sequence touches
+struct AppendArgs {
+    const uint16_t *new_k;  // bf16 bits [B, n_new, Hkv, D]
+    const uint16_t *new_v;
+    int32_t *block_table;
+    const int32_t *context_lens;
+    int32_t *refcount;
+    int32_t *free_stack;
+    int32_t *free_top;
+    uint8_t *k_pool;
+    uint8_t *v_pool;
+    float *k_scale;
+    float *v_scale;
+    int32_t *err;
+    size_t page_bytes;      // one block, all kv heads
+    int32_t B, n_new, Hkv, D, max_blocks, num_blocks, fp8;
+};
+cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream);
+
 }  // namespace svpa

@@ -27,7 +27,7 @@ STATUS = {0: "SVPA_OK", 1: "SVPA_ERR_INVALID_ARG", 2: "SVPA_ERR_UNSUPPORTED", 3:
           7: "SVPA_ERR_TIMEOUT"}
 EXPORTS = ("svpa_attn_workspace_size", "svpa_attn_kernel", "svpa_paged_verify_attn", "svpa_spec_accept_workspace_size",
            "svpa_spec_accept", "svpa_spec_accept_tree", "svpa_block_table_commit", "svpa_check_error",
-           "svpa_status_string", "svpa_version", "svpa_paged_verify_attn_noalloc")
+           "svpa_status_string", "svpa_version", "svpa_paged_verify_attn_noalloc", "svpa_kv_append")
 
 
 class SvpaError(RuntimeError):
@@ -66,6 +66,7 @@ def load(path: str = LIB_PATH):
     L.svpa_spec_accept_tree.argtypes = [I, I, I] + [P] * 11 + [U, P, P]
     L.svpa_block_table_commit.argtypes = [I] * 5 + [P] * 7 + [I, P, P, I, I, I, P, P]
     L.svpa_paged_verify_attn_noalloc.argtypes = [ctypes.POINTER(AttnParams)] + [P] * 12
+    L.svpa_kv_append.argtypes = [I] * 8 + [P] * 13
     L.svpa_check_error.argtypes = [P, P]
     L.svpa_status_string.argtypes = [I]
     L.svpa_status_string.restype = ctypes.c_char_p
@@ -203,6 +204,23 @@ def block_table_commit(n_q, block_table, context_lens, accepted_len, refcount, f
         head_dim, SVPA_KV_FP8_E4M3 if kv_fp8 else SVPA_KV_BF16, _p(error_flag), _stream(stream))
     if check:
         _check(st, "svpa_block_table_commit")
+    return st
+
+
+def kv_append(new_k, new_v, block_table, context_lens, refcount, free_stack, free_top, k_pool, v_pool,
+              *, error_flag, k_scale=None, v_scale=None, stream=None, check=True) -> int:
+    """svpa_kv_append: write new_k/new_v [B, n_new, Hkv, D] (bf16) at positions
+    context_lens[b] .. + n_new - 1, allocating and cloning pages as needed; the
+    pools are bf16 or float8_e4m3fn/uint8 [num_blocks, Hkv, 16, D]."""
+    B, n_new, Hkv, D = new_k.shape
+    fp8 = k_pool.element_size() == 1
+    st = load().svpa_kv_append(
+        B, n_new, Hkv, D, 16, block_table.shape[1], k_pool.shape[0],
+        SVPA_KV_FP8_E4M3 if fp8 else SVPA_KV_BF16, _p(new_k), _p(new_v), _p(block_table),
+        _p(context_lens), _p(refcount), _p(free_stack), _p(free_top), _p(k_pool), _p(v_pool),
+        _p(k_scale), _p(v_scale), _p(error_flag), _stream(stream))
+    if check:
+        _check(st, "svpa_kv_append")
     return st
 
 

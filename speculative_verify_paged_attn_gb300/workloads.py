@@ -319,3 +319,134 @@ def make_sampler(wl: Workload, seed: int, device="cpu", batch: Optional[int] = N
     ua = torch.rand((B, gm), generator=g, device=dev)
     us = torch.rand((B,), generator=g, device=dev)
     return SamplerInputs(p=p.contiguous(), q=q.contiguous(), tokens=x, u_accept=ua, u_sample=us)
+
+
+@dataclass
+class AppendInputs:
+    """The paged cache before an append and the rows to append (torch tensors)."""
+    wl: Workload
+    new_k: torch.Tensor             # bf16 [B, n_new, Hkv, D]
+    new_v: torch.Tensor
+    k_pool: torch.Tensor            # bf16 or float8_e4m3fn [num_blocks, Hkv, 16, D]
+    v_pool: torch.Tensor
+    k_scale: Optional[torch.Tensor]  # fp32 [num_blocks, Hkv] (FP8 only)
+    v_scale: Optional[torch.Tensor]
+    block_table: torch.Tensor       # int32 [B, max_blocks]; pages cover [0, L_b) only
+    context_lens: torch.Tensor      # int32 [B]
+    refcount: torch.Tensor          # int32 [num_blocks]
+    free_stack: torch.Tensor        # int32 [num_blocks]
+    free_top: int
+
+    @property
+    def n_new(self) -> int:
+        return self.new_k.shape[1]
+
+    def write_bytes(self) -> int:
+        """Bytes the append must move at least: the new rows read once and
+        written once (bf16), or, for FP8, each touched (page, head) tile read
+        and written once plus the new rows read once."""
+        wl = self.wl
+        B, n, Hkv, D = self.new_k.shape
+        rows = B * n * Hkv * D * 2 * 2          # K and V, bf16
+        if not wl.kv_fp8:
+            return 2 * rows
+        L = self.context_lens.to(torch.int64).cpu()
+        first, last = L // BLOCK_SIZE, (L + n - 1) // BLOCK_SIZE
+        tiles = int((last - first + 1).sum().item()) * Hkv * 2
+        return rows + tiles * BLOCK_SIZE * D * 2 + tiles * 8
+
+
+def make_append(wl: Workload, seed: int, device="cpu", batch: Optional[int] = None,
+                n_new: Optional[int] = None, shared_prefix: Optional[int] = None,
+                contexts=None) -> AppendInputs:
+    """Draw the cache state before an append of n_new rows (default n_q).
+
+    The whole pages of the first shared_prefix tokens (default: the
+    workload's) are mapped by every sequence, one reference each.  When the
+    prefix ends inside a page, the sequences whose history ends on that page
+    share it (so their append lands on a shared page and copy-on-write runs);
+    the others hold a private copy of it.  Pages cover [0, L_b) only and every
+    other block is on the free stack (shuffled); the pool holds enough blocks
+    for every sequence to own all its pages after the append, plus 10%.
+    New rows are N(0, 1) times a per-row factor from {0.5, 1, 3}, so that FP8
+    page scales grow on some writes and not on others.  Pool slots that hold
+    no token are NaN (bf16) or the code of +448 (FP8): a kernel that took a
+    page maximum over them would change the page's scale.
+    """
+    B = batch if batch is not None else wl.batch
+    n_new = wl.n_q if n_new is None else n_new
+    prefix = wl.shared_prefix if shared_prefix is None else shared_prefix
+    g_cpu = _gen(seed, "cpu")
+    BS = BLOCK_SIZE
+    if contexts is not None:
+        priv = torch.as_tensor(contexts, dtype=torch.int64)
+        B = priv.shape[0]
+    elif wl.fixed_contexts is not None:
+        priv = torch.tensor(wl.fixed_contexts, dtype=torch.int64)[:B]
+    else:
+        priv = torch.randint(wl.ctx_lo, wl.ctx_hi + 1, (B,), generator=g_cpu, dtype=torch.int64)
+    L = priv + prefix
+    pages = (L + BS - 1) // BS
+    after = (L + n_new + BS - 1) // BS
+    max_blocks = int(after.max().item())
+    full = prefix // BS                              # whole pages of the prefix
+    # the prefix's partly filled page is shared by the sequences whose history
+    # ends on it; a longer history holds its own copy of that page (the state
+    # an earlier copy-on-write leaves)
+    on_partial = (prefix % BS != 0) & (L <= (full + 1) * BS)
+    num_blocks = int(math.ceil(int(after.sum().item()) * 1.10)) + 1
+    perm = torch.randperm(num_blocks, generator=g_cpu).to(torch.int32)
+    bt = torch.full((B, max_blocks), -1, dtype=torch.int32)
+    bt[:, :full] = perm[:full]
+    cursor = full
+    if bool(on_partial.any()):
+        bt[on_partial, full] = perm[cursor]
+        cursor += 1
+    for b in range(B):
+        start = full + int(on_partial[b].item())
+        own = int(pages[b].item()) - start
+        bt[b, start:start + own] = perm[cursor:cursor + own]
+        cursor += own
+    refcount = torch.zeros(num_blocks, dtype=torch.int32)
+    used = bt[bt >= 0].to(torch.int64)
+    refcount.index_add_(0, used, torch.ones_like(used, dtype=torch.int32))
+    free = perm[cursor:].clone()
+    free_stack = torch.full((num_blocks,), -1, dtype=torch.int32)
+    free_stack[:free.shape[0]] = free
+
+    Hkv, D = wl.num_kv_heads, wl.head_dim
+    dev = torch.device(device)
+    g_dev = _gen(seed + 7919, dev)
+    valid = torch.zeros((num_blocks, BS), dtype=torch.bool)
+    for b in range(B):
+        t = int(L[b].item())
+        for i in range(int(pages[b].item())):
+            valid[int(bt[b, i].item()), :min(BS, t - i * BS)] = True
+    mask = valid.to(dev)[:, None, :, None]
+    kf = torch.randn((num_blocks, Hkv, BS, D), generator=g_dev, device=dev, dtype=torch.float32)
+    vf = torch.randn((num_blocks, Hkv, BS, D), generator=g_dev, device=dev, dtype=torch.float32)
+    k_scale = v_scale = None
+    if wl.kv_fp8:
+        def quantise(x):
+            x = torch.where(mask, x, torch.zeros((), device=dev))
+            amax = x.abs().amax(dim=(2, 3))
+            scale = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax))
+            y = (x / scale[:, :, None, None]).clamp(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)
+            yb = torch.where(mask, y.view(torch.uint8), torch.tensor(0x7E, dtype=torch.uint8, device=dev))
+            return yb.view(torch.float8_e4m3fn).contiguous(), scale.to(torch.float32).contiguous()
+
+        k_pool, k_scale = quantise(kf)
+        v_pool, v_scale = quantise(vf)
+    else:
+        nan = torch.tensor(float("nan"), device=dev)
+        k_pool = torch.where(mask, kf, nan).to(torch.bfloat16).contiguous()
+        v_pool = torch.where(mask, vf, nan).to(torch.bfloat16).contiguous()
+    del kf, vf
+    factor = torch.tensor([0.5, 1.0, 3.0], device=dev)[
+        torch.randint(0, 3, (B, n_new, 1, 1), generator=g_dev, device=dev)]
+    new_k = (torch.randn((B, n_new, Hkv, D), generator=g_dev, device=dev) * factor).to(torch.bfloat16)
+    new_v = (torch.randn((B, n_new, Hkv, D), generator=g_dev, device=dev) * factor).to(torch.bfloat16)
+    return AppendInputs(wl=wl, new_k=new_k, new_v=new_v, k_pool=k_pool, v_pool=v_pool,
+                        k_scale=k_scale, v_scale=v_scale, block_table=bt.to(dev),
+                        context_lens=L.to(torch.int32).to(dev), refcount=refcount.to(dev),
+                        free_stack=free_stack.to(dev), free_top=int(free.shape[0]))

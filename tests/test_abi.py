@@ -76,6 +76,21 @@ def test_null_pointers_rejected_before_launch(lib):
     assert st == 1
     st = lib.svpa_block_table_commit(2, 5, 16, 8, 16, *([None] * 7), 0, None, None, 4, 64, 0, None, None)
     assert st == 1
+    # K/V append: sizes checked first, then pointers, then alignment
+    nz = ctypes.c_void_p(16)  # never dereferenced: validation returns before any launch
+    base = [2, 5, 4, 64, 16, 8, 16, 0]
+    assert lib.svpa_kv_append(*base, *([None] * 13)) == 1
+    for bad in [dict(n=0), dict(n=4097), dict(d=60), dict(bs=32), dict(dt=2), dict(h=0)]:
+        a = list(base)
+        a[1], a[3], a[4], a[7], a[2] = (bad.get("n", 5), bad.get("d", 64), bad.get("bs", 16),
+                                        bad.get("dt", 0), bad.get("h", 4))
+        assert lib.svpa_kv_append(*a, *([nz] * 13)) == 1, bad
+    # FP8 pools need both scale arrays
+    assert lib.svpa_kv_append(2, 5, 4, 64, 16, 8, 16, 1, *([nz] * 9), None, None, nz, None) == 1
+    # a pool that is not 16-byte aligned
+    odd = ctypes.c_void_p(24)
+    assert lib.svpa_kv_append(*base, nz, nz, nz, nz, nz, nz, nz, odd, nz, None, None, nz, None) == 1
+    assert lib.svpa_kv_append(0, 5, 4, 64, 16, 8, 16, 0, *([None] * 13)) == 0
     # empty batch is a no-op
     p0 = svpa.attn_params(0, 5, 4, 4, 64, 8, 16, split_pages=4)
     assert lib.svpa_paged_verify_attn(ctypes.byref(p0), *([None] * 11), 0, None, None) == 0
