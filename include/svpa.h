@@ -335,14 +335,16 @@ svpa_status svpa_block_table_commit(int32_t batch, int32_t n_q,
  *                16-byte aligned
  *  k_scale, v_scale fp32 [num_blocks, Hkv] (in/out; FP8 only, else NULL)
  *  error_flag    int32 [1], zero before the call
- * Limits: 1 <= n_new <= 4096, 8 <= head_dim <= 1024 and a multiple of 8,
- * block_size 16; else SVPA_ERR_INVALID_ARG before anything is enqueued.
+ * Limits: 1 <= n_new <= 4096, 1 <= num_kv_heads <= 4096, block_size 16;
+ * head_dim a multiple of 8 up to 1024 (bf16) or of 16 up to 256 (FP8); else
+ * SVPA_ERR_INVALID_ARG before anything is enqueued.
  * Device errors: an empty free stack sets SVPA_DEVERR_FREE_OVERFLOW
  * (svpa_check_error: SVPA_ERR_OUT_OF_BLOCKS); a block id outside the pool
  * SVPA_DEVERR_BAD_BLOCK; a bad length or a mapped block with count 0
  * SVPA_DEVERR_BAD_VALUE.  When any bit is set no row is written; the blocks
  * already popped stay mapped with count 1, so tables, counts and the free
- * stack remain consistent.  Two kernels on `stream`.
+ * stack remain consistent.  Two kernels on `stream` (the second a
+ * programmatic dependent launch of the first).
  */
 svpa_status svpa_kv_append(int32_t batch, int32_t n_new, int32_t num_kv_heads,
                            int32_t head_dim, int32_t block_size,

@@ -16,12 +16,16 @@
 //      the touched pages and copies the cloned pages (with their scales).
 //      Nothing is written into a shared page here, so a clone never reads a
 //      page that its last holder is already rewriting.
-//   2. append_write_kernel, one CTA per (sequence, touched page): copies the
-//      bf16 rows, or requantises the FP8 page (one warp per (kv head, K|V)
-//      tile).  It does nothing when the error word is set, so a failed
-//      allocation never writes rows into a page that is still shared.
-// Both kernels are a few microseconds of HBM traffic: the page copies and row
-// writes are 16-byte vector accesses, the FP8 tiles 4-byte groups per lane.
+//   2. append_write_kernel, one CTA per (sequence, touched page, group of
+//      (K|V, kv head) units): copies the bf16 rows, or requantises the FP8
+//      tiles (one warp per tile).  It does nothing when the error word is
+//      set, so a failed allocation never writes rows into a page that is
+//      still shared.  It is a programmatic dependent launch: its CTAs are
+//      scheduled while the first kernel runs and wait for its completion.
+// The work is a few MB of HBM traffic, so both kernels are latency-bound:
+// every access is a 16-byte vector, and each thread issues all its loads
+// (4 per thread per round; an FP8 lane holds its whole share of the tile in
+// registers) before its stores, so one call costs a few memory round trips.
 #include "svpa_device.cuh"
 #include "svpa_internal.h"
 
@@ -29,8 +33,12 @@ namespace svpa {
 
 namespace {
 
-constexpr int kAllocThreads = 128;
+constexpr int kAllocThreads = 256;
 constexpr int kWriteThreads = 256;
+constexpr int kUnitsBf16 = 4;      // (K|V, kv head) row sets per CTA, bf16 pages
+constexpr int kMaxChunksFp8 = 8;   // 16-byte chunks per lane: a 16 x 256-byte FP8 tile
+
+constexpr int kLoadsCopy = 4;  // 16-byte loads per thread in flight in a page copy
 
 // Take one block from the top of the free stack, or -1 (error bit raised).
 // Only pops run during an append, so a failed pop means the stack was empty.
@@ -52,6 +60,8 @@ __device__ int pop_block(const AppendArgs &a) {
 __global__ void __launch_bounds__(kAllocThreads) append_alloc_kernel(const __grid_constant__ AppendArgs a) {
     __shared__ int s_src[kMaxAppendPages], s_dst[kMaxAppendPages];
     __shared__ int s_ncow;
+    // the write kernel may be scheduled now; it waits for this grid's completion
+    asm volatile("griddepcontrol.launch_dependents;");
     const int b = blockIdx.x;
     const int L = a.context_lens[b];
     const long long end = (long long)L + a.n_new;
@@ -108,10 +118,24 @@ __global__ void __launch_bounds__(kAllocThreads) append_alloc_kernel(const __gri
         const uint4 *sv = reinterpret_cast<const uint4 *>(a.v_pool) + so;
         uint4 *dk = reinterpret_cast<uint4 *>(a.k_pool) + dof;
         uint4 *dv = reinterpret_cast<uint4 *>(a.v_pool) + dof;
-        for (size_t w = threadIdx.x; w < words; w += kAllocThreads) {
-            const uint4 x = sk[w], y = sv[w];
-            dk[w] = x;
-            dv[w] = y;
+        for (size_t w0 = threadIdx.x; w0 < words; w0 += (size_t)kLoadsCopy * kAllocThreads) {
+            uint4 x[kLoadsCopy], y[kLoadsCopy];
+#pragma unroll
+            for (int k = 0; k < kLoadsCopy; ++k) {
+                const size_t w = w0 + (size_t)k * kAllocThreads;
+                if (w < words) {
+                    x[k] = sk[w];
+                    y[k] = sv[w];
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kLoadsCopy; ++k) {
+                const size_t w = w0 + (size_t)k * kAllocThreads;
+                if (w < words) {
+                    dk[w] = x[k];
+                    dv[w] = y[k];
+                }
+            }
         }
         if (a.fp8)
             for (int h = threadIdx.x; h < a.Hkv; h += kAllocThreads) {
@@ -146,16 +170,14 @@ __device__ __forceinline__ uint32_t encode4(const float (&v)[4]) {
     return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-__device__ __forceinline__ void load_new4(const uint16_t *row, int d, float (&v)[4]) {
-    const uint2 x = *reinterpret_cast<const uint2 *>(row + d);
-    v[0] = bf16_bits_to_f32(x.x & 0xffffu);
-    v[1] = bf16_bits_to_f32(x.x >> 16);
-    v[2] = bf16_bits_to_f32(x.y & 0xffffu);
-    v[3] = bf16_bits_to_f32(x.y >> 16);
-}
+// Chunk k (16 bytes) of a work list of n chunks, kLoads per thread in flight:
+// every load of a round is issued before its stores.
+constexpr int kLoads = 4;
 
 template <bool FP8>
 __global__ void __launch_bounds__(kWriteThreads) append_write_kernel(const __grid_constant__ AppendArgs a) {
+    // the allocation kernel's tables, counts and copies are complete and visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (*reinterpret_cast<volatile int32_t *>(a.err) != 0) return;
     const int b = blockIdx.x;
     const int L = a.context_lens[b];
@@ -175,71 +197,132 @@ __global__ void __launch_bounds__(kWriteThreads) append_write_kernel(const __gri
     };
 
     if constexpr (!FP8) {
+        // this CTA: units u0 .. u0+kUnitsBf16-1 of the 2*Hkv (K|V, kv head) row sets
+        const int u0 = (int)blockIdx.z * kUnitsBf16;
+        const int units = min(kUnitsBf16, 2 * Hkv - u0);
         const int cpr = D / 8;  // 16-byte chunks per row
         const int nrows = vend - hist;
-        const int per_kv = nrows * Hkv * cpr;
-        for (int w = threadIdx.x; w < 2 * per_kv; w += kWriteThreads) {
-            const int kv = w >= per_kv;
-            int r = w - kv * per_kv;
-            const int s = hist + r / (Hkv * cpr);
-            r %= Hkv * cpr;
-            const int h = r / cpr, c = r - h * cpr;
-            const uint16_t *src = kv ? a.new_v : a.new_k;
-            uint8_t *pool = kv ? a.v_pool : a.k_pool;
-            const uint4 x = reinterpret_cast<const uint4 *>(src_row(src, s, h))[c];
-            reinterpret_cast<uint4 *>(pool + (((size_t)blk * Hkv + h) * kBlockSize + s) * D * 2)[c] = x;
+        const int per_unit = nrows * cpr;
+        const int total = units * per_unit;
+        for (int w0 = threadIdx.x; w0 < total; w0 += kLoads * kWriteThreads) {
+            uint4 x[kLoads];
+            uint4 *dst[kLoads];
+#pragma unroll
+            for (int k = 0; k < kLoads; ++k) {
+                const int w = w0 + k * kWriteThreads;
+                dst[k] = nullptr;
+                if (w < total) {
+                    const int uu = w / per_unit;
+                    const int r = w - uu * per_unit;
+                    const int s = hist + r / cpr, c = r - (r / cpr) * cpr;
+                    const int u = u0 + uu;
+                    const int kv = u >= Hkv, h = u - kv * Hkv;
+                    x[k] = reinterpret_cast<const uint4 *>(src_row(kv ? a.new_v : a.new_k, s, h))[c];
+                    dst[k] = reinterpret_cast<uint4 *>((kv ? a.v_pool : a.k_pool) +
+                                                       (((size_t)blk * Hkv + h) * kBlockSize + s) * D * 2) + c;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kLoads; ++k)
+                if (dst[k]) *dst[k] = x[k];
         }
     } else {
+        // one warp per (K|V, kv head) tile of 16 rows x D bytes, in 16-byte chunks
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        const int gpr = D / 4;  // 4-byte groups per row
-        const int hist_g = hist * gpr, vend_g = vend * gpr, tile_g = kBlockSize * gpr;
-        for (int u = warp; u < 2 * Hkv; u += kWriteThreads / 32) {
-            const int kv = u >= Hkv, h = u - kv * Hkv;
-            const uint16_t *src = kv ? a.new_v : a.new_k;
-            uint32_t *tile = reinterpret_cast<uint32_t *>((kv ? a.v_pool : a.k_pool) +
-                                                          ((size_t)blk * Hkv + h) * kBlockSize * D);
-            float *scale = (kv ? a.v_scale : a.k_scale) + (size_t)blk * Hkv + h;
-            const float old_scale = *scale;
-            // amax over the history (code x old scale, one fp32 product) and the new rows
-            float amax = 0.f;
-            for (int g = lane; g < vend_g; g += 32) {
-                float v[4];
-                if (g < hist_g) {
-                    decode4(tile[g], v);
+        const int u = (int)blockIdx.z * (kWriteThreads / 32) + warp;
+        if (u >= 2 * Hkv) return;
+        const int kv = u >= Hkv, h = u - kv * Hkv;
+        const uint16_t *src = kv ? a.new_v : a.new_k;
+        uint4 *tile = reinterpret_cast<uint4 *>((kv ? a.v_pool : a.k_pool) +
+                                                ((size_t)blk * Hkv + h) * kBlockSize * D);
+        float *scale = (kv ? a.v_scale : a.k_scale) + (size_t)blk * Hkv + h;
+        const float old_scale = *scale;
+        const int cpr = D / 16;  // chunks per row
+        const int nch = kBlockSize * cpr;
+        // load every chunk this lane owns: history codes, or 16 new bf16 values
+        uint4 ra[kMaxChunksFp8], rb[kMaxChunksFp8];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) v[k] = __fmul_rn(v[k], old_scale);
+        for (int k = 0; k < kMaxChunksFp8; ++k) {
+            const int c = lane + 32 * k;
+            const int s = c / cpr;
+            if (c < nch && s < vend) {
+                if (s < hist) {
+                    ra[k] = tile[c];
                 } else {
-                    const int s = g / gpr;
-                    load_new4(src_row(src, s, h), (g - s * gpr) * 4, v);
+                    const uint4 *row = reinterpret_cast<const uint4 *>(src_row(src, s, h));
+                    const int c2 = 2 * (c - s * cpr);
+                    ra[k] = row[c2];
+                    rb[k] = row[c2 + 1];
                 }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fabsf(v[k]));
             }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float ns = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-            const bool rescale = hist > 0 && ns != old_scale;
-            for (int g = lane; g < tile_g; g += 32) {
-                float v[4];
-                if (g < hist_g) {
-                    if (!rescale) continue;
-                    decode4(tile[g], v);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) v[k] = __fdiv_rn(__fmul_rn(v[k], old_scale), ns);
-                } else if (g < vend_g) {
-                    const int s = g / gpr;
-                    load_new4(src_row(src, s, h), (g - s * gpr) * 4, v);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) v[k] = __fdiv_rn(v[k], ns);
-                } else {
-                    tile[g] = 0u;  // slots past the last row
-                    continue;
-                }
-                tile[g] = encode4(v);
-            }
-            __syncwarp();
-            if (lane == 0) *scale = ns;
         }
+        // amax over the history (code x old scale, one fp32 product) and the new rows
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxChunksFp8; ++k) {
+            const int c = lane + 32 * k;
+            const int s = c / cpr;
+            if (!(c < nch && s < vend)) continue;
+            const uint32_t w[4] = {ra[k].x, ra[k].y, ra[k].z, ra[k].w};
+            if (s < hist) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float v[4];
+                    decode4(w[j], v);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(__fmul_rn(v[e], old_scale)));
+                }
+            } else {
+                const uint32_t w2[4] = {rb[k].x, rb[k].y, rb[k].z, rb[k].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[j] & 0xffffu)));
+                    amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[j] >> 16)));
+                    amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w2[j] & 0xffffu)));
+                    amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w2[j] >> 16)));
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float ns = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+        const bool rescale = hist > 0 && ns != old_scale;
+#pragma unroll
+        for (int k = 0; k < kMaxChunksFp8; ++k) {
+            const int c = lane + 32 * k;
+            if (c >= nch) continue;
+            const int s = c / cpr;
+            uint4 out = make_uint4(0u, 0u, 0u, 0u);  // slots past the last row
+            if (s < hist) {
+                if (!rescale) continue;
+                const uint32_t w[4] = {ra[k].x, ra[k].y, ra[k].z, ra[k].w};
+                uint32_t o4[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float v[4];
+                    decode4(w[j], v);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[e] = __fdiv_rn(__fmul_rn(v[e], old_scale), ns);
+                    o4[j] = encode4(v);
+                }
+                out = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            } else if (s < vend) {
+                const uint32_t w[8] = {ra[k].x, ra[k].y, ra[k].z, ra[k].w, rb[k].x, rb[k].y, rb[k].z, rb[k].w};
+                uint32_t o4[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float v[4] = {__fdiv_rn(bf16_bits_to_f32(w[2 * j] & 0xffffu), ns),
+                                  __fdiv_rn(bf16_bits_to_f32(w[2 * j] >> 16), ns),
+                                  __fdiv_rn(bf16_bits_to_f32(w[2 * j + 1] & 0xffffu), ns),
+                                  __fdiv_rn(bf16_bits_to_f32(w[2 * j + 1] >> 16), ns)};
+                    o4[j] = encode4(v);
+                }
+                out = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            }
+            tile[c] = out;
+        }
+        __syncwarp();
+        if (lane == 0) *scale = ns;
     }
 }
 
@@ -249,12 +332,21 @@ cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream) {
     append_alloc_kernel<<<a.B, kAllocThreads, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const dim3 grid(a.B, (a.n_new + kBlockSize - 1) / kBlockSize + 1);
-    if (a.fp8)
-        append_write_kernel<true><<<grid, kWriteThreads, 0, stream>>>(a);
-    else
-        append_write_kernel<false><<<grid, kWriteThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    // (sequence, touched page, group of units); launched as a programmatic
+    // dependent of the allocation kernel so that its launch overlaps it
+    const int units_per_cta = a.fp8 ? kWriteThreads / 32 : kUnitsBf16;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.B, (unsigned)((a.n_new + kBlockSize - 1) / kBlockSize + 1),
+                       (unsigned)((2 * a.Hkv + units_per_cta - 1) / units_per_cta));
+    cfg.blockDim = dim3(kWriteThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.fp8) return cudaLaunchKernelEx(&cfg, append_write_kernel<true>, a);
+    return cudaLaunchKernelEx(&cfg, append_write_kernel<false>, a);
 }
 
 }  // namespace svpa

@@ -435,12 +435,13 @@ svpa_status svpa_kv_append(int32_t batch, int32_t n_new, int32_t num_kv_heads, i
                            const int32_t *context_lens, int32_t *refcount, int32_t *free_stack,
                            int32_t *free_top, void *k_pool, void *v_pool, float *k_scale, float *v_scale,
                            int32_t *error_flag, void *stream) {
-    if (batch < 0 || n_new < 1 || n_new > kMaxAppendRows || num_kv_heads < 1 || head_dim < 8 ||
-        head_dim > 1024 || head_dim % 8 != 0 || block_size != kBlockSize || max_blocks_per_seq < 1 ||
+    if (batch < 0 || n_new < 1 || n_new > kMaxAppendRows || num_kv_heads < 1 || num_kv_heads > 4096 ||
+        head_dim < 8 || head_dim % 8 != 0 || block_size != kBlockSize || max_blocks_per_seq < 1 ||
         num_blocks < 1 || (kv_dtype != SVPA_KV_BF16 && kv_dtype != SVPA_KV_FP8_E4M3))
         return SVPA_ERR_INVALID_ARG;
-    if (batch == 0) return SVPA_OK;
     const bool fp8 = kv_dtype == SVPA_KV_FP8_E4M3;
+    if (fp8 ? (head_dim % 16 != 0 || head_dim > 256) : head_dim > 1024) return SVPA_ERR_INVALID_ARG;
+    if (batch == 0) return SVPA_OK;
     if (!new_k || !new_v || !block_table || !context_lens || !refcount || !free_stack || !free_top || !k_pool ||
         !v_pool || !error_flag || (fp8 && (!k_scale || !v_scale)))
         return SVPA_ERR_INVALID_ARG;

@@ -85,6 +85,9 @@ def test_null_pointers_rejected_before_launch(lib):
         a[1], a[3], a[4], a[7], a[2] = (bad.get("n", 5), bad.get("d", 64), bad.get("bs", 16),
                                         bad.get("dt", 0), bad.get("h", 4))
         assert lib.svpa_kv_append(*a, *([nz] * 13)) == 1, bad
+    # FP8 tiles: head_dim a multiple of 16, at most 256
+    for d in (72, 272):
+        assert lib.svpa_kv_append(2, 5, 4, d, 16, 8, 16, 1, *([nz] * 13)) == 1, d
     # FP8 pools need both scale arrays
     assert lib.svpa_kv_append(2, 5, 4, 64, 16, 8, 16, 1, *([nz] * 9), None, None, nz, None) == 1
     # a pool that is not 16-byte aligned

@@ -117,6 +117,11 @@ SMALL = {
     "fp8_rescale_cow": (W.WORKLOADS["fp8"], (0, 4, 9, 12, 300, 1000), 35, 6),
     "bf16_tree_cow": (W.WORKLOADS["tree"], (0, 3, 5, 700), 803, 29),
     "fp8_single_row": (W.WORKLOADS["fp8"], (5, 16, 95), 0, 1),
+    # widest FP8 tile (16 x 256 bytes) and a copy-on-write at D = 256
+    "fp8_d256_cow": (W.WORKLOADS["fp8"].scaled(num_q_heads=4, num_kv_heads=2, head_dim=256),
+                     (1, 3, 16, 40), 21, 20),
+    # odd head count (a partial group of units) and 9 chunks per bf16 row
+    "bf16_hkv3_d72": (W.WORKLOADS["7b"].scaled(num_q_heads=3, num_kv_heads=3, head_dim=72), (5, 33, 0), 0, 9),
 }
 
 
