@@ -176,9 +176,9 @@ constexpr int kLoads = 4;
 
 template <bool FP8>
 __global__ void __launch_bounds__(kWriteThreads) append_write_kernel(const __grid_constant__ AppendArgs a) {
-    // the allocation kernel's tables, counts and copies are complete and visible
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (*reinterpret_cast<volatile int32_t *>(a.err) != 0) return;
+    // Before the wait only inputs that the allocation kernel never writes are
+    // read (lengths, new rows); the table, counts, pages, scales and error
+    // word are read after it.
     const int b = blockIdx.x;
     const int L = a.context_lens[b];
     const long long end = (long long)L + a.n_new;
@@ -186,14 +186,19 @@ __global__ void __launch_bounds__(kWriteThreads) append_write_kernel(const __gri
     const int i = L / kBlockSize + (int)blockIdx.y;
     const long long ps = (long long)i * kBlockSize;
     if (ps >= end) return;
-    const int blk = a.block_table[(size_t)b * a.max_blocks + i];
-    if (blk < 0 || blk >= a.num_blocks) return;
     const int hist = L > ps ? (L - ps < kBlockSize ? (int)(L - ps) : kBlockSize) : 0;  // history slots
     const int vend = end - ps < kBlockSize ? (int)(end - ps) : kBlockSize;  // slots in use after
     const int D = a.D, Hkv = a.Hkv;
     // source row of page slot s, kv head h: new rows [B, n_new, Hkv, D]
     auto src_row = [&](const uint16_t *src, int s, int h) {
         return src + (((size_t)b * a.n_new + (size_t)(ps + s - L)) * Hkv + h) * D;
+    };
+    // wait for the allocation kernel; then its block id for this page
+    auto wait_block = [&]() -> int {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (*reinterpret_cast<volatile int32_t *>(a.err) != 0) return -1;
+        const int blk = a.block_table[(size_t)b * a.max_blocks + i];
+        return blk >= 0 && blk < a.num_blocks ? blk : -1;
     };
 
     if constexpr (!FP8) {
@@ -204,27 +209,44 @@ __global__ void __launch_bounds__(kWriteThreads) append_write_kernel(const __gri
         const int nrows = vend - hist;
         const int per_unit = nrows * cpr;
         const int total = units * per_unit;
-        for (int w0 = threadIdx.x; w0 < total; w0 += kLoads * kWriteThreads) {
-            uint4 x[kLoads];
-            uint4 *dst[kLoads];
+        // chunk w: unit, page slot and 16-byte column
+        auto where = [&](int w, int &u, int &s, int &c) {
+            const int uu = w / per_unit;
+            const int r = w - uu * per_unit;
+            s = hist + r / cpr;
+            c = r - (r / cpr) * cpr;
+            u = u0 + uu;
+        };
+        auto load_round = [&](int w0, uint4 (&x)[kLoads]) {
 #pragma unroll
             for (int k = 0; k < kLoads; ++k) {
                 const int w = w0 + k * kWriteThreads;
-                dst[k] = nullptr;
                 if (w < total) {
-                    const int uu = w / per_unit;
-                    const int r = w - uu * per_unit;
-                    const int s = hist + r / cpr, c = r - (r / cpr) * cpr;
-                    const int u = u0 + uu;
-                    const int kv = u >= Hkv, h = u - kv * Hkv;
-                    x[k] = reinterpret_cast<const uint4 *>(src_row(kv ? a.new_v : a.new_k, s, h))[c];
-                    dst[k] = reinterpret_cast<uint4 *>((kv ? a.v_pool : a.k_pool) +
-                                                       (((size_t)blk * Hkv + h) * kBlockSize + s) * D * 2) + c;
+                    int u, s, c;
+                    where(w, u, s, c);
+                    const int kv = u >= Hkv;
+                    x[k] = reinterpret_cast<const uint4 *>(src_row(kv ? a.new_v : a.new_k, s, u - kv * Hkv))[c];
                 }
             }
+        };
+        if ((int)threadIdx.x >= total) return;
+        uint4 x[kLoads];
+        load_round(threadIdx.x, x);  // the first round overlaps the allocation kernel
+        const int blk = wait_block();
+        if (blk < 0) return;
+        for (int w0 = threadIdx.x; w0 < total; w0 += kLoads * kWriteThreads) {
+            if (w0 != (int)threadIdx.x) load_round(w0, x);
 #pragma unroll
-            for (int k = 0; k < kLoads; ++k)
-                if (dst[k]) *dst[k] = x[k];
+            for (int k = 0; k < kLoads; ++k) {
+                const int w = w0 + k * kWriteThreads;
+                if (w < total) {
+                    int u, s, c;
+                    where(w, u, s, c);
+                    const int kv = u >= Hkv, h = u - kv * Hkv;
+                    reinterpret_cast<uint4 *>((kv ? a.v_pool : a.k_pool) +
+                                              (((size_t)blk * Hkv + h) * kBlockSize + s) * D * 2)[c] = x[k];
+                }
+            }
         }
     } else {
         // one warp per (K|V, kv head) tile of 16 rows x D bytes, in 16-byte chunks
@@ -233,28 +255,32 @@ __global__ void __launch_bounds__(kWriteThreads) append_write_kernel(const __gri
         if (u >= 2 * Hkv) return;
         const int kv = u >= Hkv, h = u - kv * Hkv;
         const uint16_t *src = kv ? a.new_v : a.new_k;
-        uint4 *tile = reinterpret_cast<uint4 *>((kv ? a.v_pool : a.k_pool) +
-                                                ((size_t)blk * Hkv + h) * kBlockSize * D);
-        float *scale = (kv ? a.v_scale : a.k_scale) + (size_t)blk * Hkv + h;
-        const float old_scale = *scale;
         const int cpr = D / 16;  // chunks per row
         const int nch = kBlockSize * cpr;
-        // load every chunk this lane owns: history codes, or 16 new bf16 values
+        // every chunk this lane owns: 16 new bf16 values (loaded before the
+        // wait), or 16 history codes (after it)
         uint4 ra[kMaxChunksFp8], rb[kMaxChunksFp8];
 #pragma unroll
         for (int k = 0; k < kMaxChunksFp8; ++k) {
             const int c = lane + 32 * k;
             const int s = c / cpr;
-            if (c < nch && s < vend) {
-                if (s < hist) {
-                    ra[k] = tile[c];
-                } else {
-                    const uint4 *row = reinterpret_cast<const uint4 *>(src_row(src, s, h));
-                    const int c2 = 2 * (c - s * cpr);
-                    ra[k] = row[c2];
-                    rb[k] = row[c2 + 1];
-                }
+            if (c < nch && s >= hist && s < vend) {
+                const uint4 *row = reinterpret_cast<const uint4 *>(src_row(src, s, h));
+                const int c2 = 2 * (c - s * cpr);
+                ra[k] = row[c2];
+                rb[k] = row[c2 + 1];
             }
+        }
+        const int blk = wait_block();
+        if (blk < 0) return;
+        uint4 *tile = reinterpret_cast<uint4 *>((kv ? a.v_pool : a.k_pool) +
+                                                ((size_t)blk * Hkv + h) * kBlockSize * D);
+        float *scale = (kv ? a.v_scale : a.k_scale) + (size_t)blk * Hkv + h;
+        const float old_scale = *scale;
+#pragma unroll
+        for (int k = 0; k < kMaxChunksFp8; ++k) {
+            const int c = lane + 32 * k;
+            if (c < nch && c / cpr < hist) ra[k] = tile[c];
         }
         // amax over the history (code x old scale, one fp32 product) and the new rows
         float amax = 0.f;

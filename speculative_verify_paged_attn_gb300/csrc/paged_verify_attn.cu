@@ -565,7 +565,7 @@ __global__ void __launch_bounds__((MT + 1) * 32, Occ<MT>::MINB)
 }
 
 template <int D, bool FP8, int MT>
-cudaError_t plan_mt(AttnLaunch *out) {
+cudaError_t plan_mt_uncached(AttnLaunch *out) {
     using G_ = Geo<D, FP8>;
     constexpr int THREADS = (MT + 1) * 32;
     auto kern = pva_kernel<D, FP8, MT>;
@@ -592,6 +592,14 @@ cudaError_t plan_mt(AttnLaunch *out) {
     if (e != cudaSuccess) return e;
     out->ctas_per_sm = nb < 1 ? 1 : nb;
     return cudaSuccess;
+}
+
+// Stage count, shared memory and residency of one instantiation, computed
+// once per device (the attribute set on the first call stays set).
+template <int D, bool FP8, int MT>
+cudaError_t plan_mt(AttnLaunch *out) {
+    static DeviceMemo<AttnLaunch> memo;
+    return memo.get(out, plan_mt_uncached<D, FP8, MT>);
 }
 
 template <int D, bool FP8, int MT>

@@ -939,7 +939,12 @@ template <bool FP8>
 cudaError_t launch_tc(const CUtensorMap &mk, const CUtensorMap &mv, const AttnMaps &m, const AttnArgs &a, int grid,
                       cudaStream_t st) {
     const size_t smem = sizeof(Smem<FP8>) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(pva_tc_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static DeviceMemo<int> attr_set;  // the shared-memory opt-in, once per device
+    int done = 0;
+    cudaError_t e = attr_set.get(&done, [&](int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(pva_tc_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
     if (e != cudaSuccess) return e;
     pva_tc_kernel<FP8><<<grid, TcCfg<FP8>::kThreads, smem, st>>>(mk, mv, m.q[0], m.q[1], a);
     return cudaGetLastError();

@@ -770,16 +770,15 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
 }
 
 int sm_count_cached() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0, v = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-            n = v;
-        else
-            return 152;
-    }
-    return n;
+    static DeviceMemo<int> memo;
+    int n = 0;
+    const cudaError_t e = memo.get(&n, [](int *v) {
+        int dev = 0;
+        cudaError_t r = cudaGetDevice(&dev);
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+        return r == cudaSuccess && *v <= 0 ? cudaErrorInvalidValue : r;
+    });
+    return e == cudaSuccess ? n : 152;
 }
 
 // Steps per warp (a power of two) for B rows of V tokens, or 0 when V is
@@ -809,7 +808,15 @@ cudaError_t launch_cluster(void (*const *kernels)(Args, int), const Args &a, int
     void (*kern)(Args, int) = kernels[idx];
     const size_t smem = dyn_smem_per_step * (size_t)ni;
     if (smem > 0) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        // the shared-memory opt-in of each step count, once per device
+        static DeviceMemo<size_t> opted[8];
+        size_t have = 0;
+        auto opt_in = [&](size_t *v) {
+            *v = smem;
+            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        };
+        cudaError_t e = opted[idx & 7].get(&have, opt_in);
+        if (e == cudaSuccess && have < smem) e = opt_in(&have);
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};

@@ -44,10 +44,15 @@ EncodeTiledFn encode_fn() {
 }
 
 int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
-    return n;
+    static DeviceMemo<int> memo;
+    int n = 0;
+    const cudaError_t e = memo.get(&n, [](int *v) {
+        int dev = 0;
+        cudaError_t r = cudaGetDevice(&dev);
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+        return r == cudaSuccess && *v <= 0 ? cudaErrorInvalidValue : r;
+    });
+    return e == cudaSuccess ? n : 148;
 }
 
 struct AttnPlan {

@@ -6,10 +6,38 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <mutex>
 
 #include "../../include/svpa.h"
 
 namespace svpa {
+
+// Host-side launch facts (function attributes, occupancy, SM count) are
+// computed once per device and remembered: a serving loop calls with the same
+// shapes every step, and each runtime query costs microseconds of host time.
+constexpr int kMaxDevices = 64;
+template <typename T>
+struct DeviceMemo {
+    std::mutex mu;
+    T value[kMaxDevices];
+    bool have[kMaxDevices] = {};
+    // f(T*) -> cudaError_t computes the value on a miss; errors are not remembered
+    template <typename F>
+    cudaError_t get(T *out, F f) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDevices) return f(out);
+        std::lock_guard<std::mutex> g(mu);
+        if (!have[dev]) {
+            e = f(&value[dev]);
+            if (e != cudaSuccess) return e;
+            have[dev] = true;
+        }
+        *out = value[dev];
+        return cudaSuccess;
+    }
+};
 
 constexpr int kBlockSize = 16;   // tokens per page
 constexpr int kMaxNq = 64;       // queries per sequence (one 64-bit mask row each)
