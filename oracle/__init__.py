@@ -80,6 +80,10 @@ def _load():
             lib.oracle_e4m3_to_double.restype = D
             lib.oracle_kv_append.argtypes = [I] * 8 + [P] * 11
             lib.oracle_kv_append.restype = I
+            lib.oracle_gamma_update.argtypes = [I, I] + [P] * 6 + [ctypes.c_float, ctypes.c_float]
+            lib.oracle_gamma_update.restype = I
+            lib.oracle_gamma_from_alpha.argtypes = [ctypes.c_float]
+            lib.oracle_gamma_from_alpha.restype = I
             lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
             lib.oracle_e4m3_encode.restype = ctypes.c_uint8
             lib.oracle_max_threads.argtypes = []
@@ -296,3 +300,29 @@ def expected_accepted(alpha) -> float:
 
 def speedup(expected_k: float, gamma: int, r: float) -> float:
     return _load().oracle_speedup(float(expected_k), int(gamma), float(r))
+
+
+def gamma_from_alpha(alpha: float) -> int:
+    """Draft length for an acceptance-rate estimate (fp32 comparison)."""
+    return int(_load().oracle_gamma_from_alpha(float(alpha)))
+
+
+def gamma_update(gamma, accepted_len, seq_state=None, batch_state=(0.0, 0.0), *, decay=0.9, r=0.0):
+    """One step of the acceptance moving averages on copies of the state.
+
+    Returns dict(seq_state [B, 2] fp32 or None, seq_gamma [B] int32 or None,
+    batch_state [2] fp32, batch_gamma int, telemetry [4] fp32: batch alpha,
+    mean accepted this step, E[K], speed-up at ratio r)."""
+    lib = _load()
+    k = _c(accepted_len, np.int32)
+    B = k.shape[0]
+    ss = None if seq_state is None else _c(seq_state, np.float32).reshape(B, 2).copy()
+    sg = None if seq_state is None else np.zeros(B, np.int32)
+    bs = np.asarray(batch_state, np.float32).copy()
+    bg = np.zeros(1, np.int32)
+    tel = np.zeros(4, np.float32)
+    rc = lib.oracle_gamma_update(B, int(gamma), _ptr(k), _ptr(ss), _ptr(sg), _ptr(bs), _ptr(bg), _ptr(tel),
+                                 float(decay), float(r))
+    if rc != 0:
+        raise OracleError(f"oracle_gamma_update failed with status {rc}")
+    return dict(seq_state=ss, seq_gamma=sg, batch_state=bs, batch_gamma=int(bg[0]), telemetry=tel)

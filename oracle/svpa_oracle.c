@@ -699,3 +699,87 @@ double oracle_expected_accepted(const double *alpha, int gamma) {
 double oracle_speedup(double expected_accepted, int gamma, double r) {
     return (expected_accepted + 1.0) / ((double)gamma * r + 1.0);
 }
+
+/* ------------------------------------------------------------------ */
+/*
+ * Acceptance telemetry and the adaptive draft length.
+ *
+ * "Speculative Decoding & KV-Cache PagedAttention in Enterprise LLM
+ * Serving": the lookahead follows a moving average of the acceptance rate
+ * (above 0.85 -> 5 drafts, above 0.70 -> 4, above 0.50 -> 3, else 2);
+ * "The Sub-Millisecond Speculative Decoding Meltdown", production failure
+ * scenarios: when the exponential moving average of acceptance collapses
+ * below 0.25, fall back to one token; "LOW-LATENCY INFERENCE: SPECULATIVE
+ * DECODING & PAGING", acceptance math: E[K] = sum_{i=1..gamma} alpha^i for a
+ * per-token rate alpha, speed-up (E[K] + 1) / (gamma * r + 1).
+ *
+ * One step with g drafts per sequence: a sequence that accepted k drafts ran
+ * k + (k < g) acceptance tests (the k that passed and, if any, the one that
+ * failed), so accepted / tests estimates the per-token rate.  Moving averages
+ * in fp32, each product and sum rounded on its own (no fused multiply-add):
+ *   A = decay * A + k,  N = decay * N + tests,  alpha = A / N.
+ * Per sequence: state[b] = (A, N), gamma_next[b] from its alpha.  The batch
+ * keeps its own (A, N) over the step's integer totals (sum k, sum tests), so
+ * its gamma does not depend on the order of a sum.  Draft length from alpha:
+ * > 0.85 -> 5, > 0.70 -> 4, > 0.50 -> 3, >= 0.25 -> 2, else 1.
+ * telemetry: [0] batch alpha, [1] mean accepted per sequence this step,
+ * [2] E[K] at (batch alpha, batch gamma), [3] speed-up at ratio r — fp32,
+ * E[K] as the running product and sum in increasing i.
+ */
+int oracle_gamma_from_alpha(float alpha) {
+    if (alpha > 0.85f) return 5;
+    if (alpha > 0.70f) return 4;
+    if (alpha > 0.50f) return 3;
+    if (alpha >= 0.25f) return 2;
+    return 1;
+}
+
+int oracle_gamma_update(int B, int gamma, const int32_t *accepted_len, float *seq_state,
+                        int32_t *seq_gamma_next, float *batch_state, int32_t *batch_gamma_next,
+                        float *telemetry, float decay, float r) {
+    if (B < 1 || gamma < 1 || !accepted_len || !batch_state || !batch_gamma_next || !telemetry)
+        return ORC_ERR_ARG;
+    long long sum_k = 0, sum_t = 0;
+    for (int b = 0; b < B; ++b) {
+        const int k = accepted_len[b];
+        if (k < 0 || k > gamma) return ORC_ERR_ARG;
+        const int tests = k + (k < gamma ? 1 : 0);
+        sum_k += k;
+        sum_t += tests;
+        if (seq_state) {
+            volatile float a = decay * seq_state[2 * b];
+            volatile float n = decay * seq_state[2 * b + 1];
+            a = a + (float)k;
+            n = n + (float)tests;
+            seq_state[2 * b] = a;
+            seq_state[2 * b + 1] = n;
+            if (seq_gamma_next) {
+                volatile float alpha = a / n;
+                seq_gamma_next[b] = oracle_gamma_from_alpha(alpha);
+            }
+        }
+    }
+    volatile float a = decay * batch_state[0];
+    volatile float n = decay * batch_state[1];
+    a = a + (float)sum_k;
+    n = n + (float)sum_t;
+    batch_state[0] = a;
+    batch_state[1] = n;
+    volatile float alpha = a / n;
+    const int g = oracle_gamma_from_alpha(alpha);
+    *batch_gamma_next = g;
+    volatile float ek = 0.f, prod = 1.f;
+    for (int i = 0; i < g; ++i) {
+        prod = prod * alpha;
+        ek = ek + prod;
+    }
+    volatile float den = (float)g * r;
+    den = den + 1.f;
+    volatile float eta = ek + 1.f;
+    eta = eta / den;
+    telemetry[0] = alpha;
+    telemetry[1] = (float)sum_k / (float)B;
+    telemetry[2] = ek;
+    telemetry[3] = eta;
+    return ORC_OK;
+}
