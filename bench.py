@@ -284,6 +284,36 @@ def gpu_lead():
     torch.cuda._sleep(LEAD_CYCLES)
 
 
+def time_gamma(st: "Step", steps: int, warmup: int, stream) -> float:
+    """Average device time (ms) of one svpa_gamma_update on the step's
+    accepted lengths (per-sequence and batch moving averages)."""
+    dev, B = st.k.device, st.B
+    ss = torch.zeros((B, 2), dtype=torch.float32, device=dev)
+    sg = torch.zeros(B, dtype=torch.int32, device=dev)
+    bs = torch.zeros(2, dtype=torch.float32, device=dev)
+    bg = torch.zeros(1, dtype=torch.int32, device=dev)
+    tel = torch.zeros(4, dtype=torch.float32, device=dev)
+    g = st.path.shape[1] - 1 if st.tree else st.wl.gamma
+
+    def run():
+        svpa.gamma_update(g, st.k, bs, bg, tel, error_flag=st.err, seq_state=ss, seq_gamma=sg,
+                          draft_cost_ratio=0.08)
+
+    for _ in range(warmup):
+        run()
+    ms = []
+    for _ in range(steps):
+        gpu_lead()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    assert svpa.check_error(st.err) == 0, "device error in the draft-length update"
+    return sum(ms) / len(ms)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -513,6 +543,8 @@ def main():
     app_ms = time_append(ap, K, args.warmup, stream)
     app_bytes = ap.bytes
     del ap
+    # the draft-length controller on this step's accepted lengths
+    gam_ms = time_gamma(st, K, args.warmup, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -538,6 +570,7 @@ def main():
             "commit_us": round(sum(comm_ms) / K * 1e3, 2),
             "kv_append_us": round(app_ms * 1e3, 2),
             "kv_append_gbs": round(app_bytes / (app_ms * 1e-3) / 1e9, 2),
+            "gamma_update_us": round(gam_ms * 1e3, 2),
             "kv_bytes_per_step": st.kv_bytes,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),

@@ -18,6 +18,8 @@
  *   svpa_block_table_commit  commit the accepted tokens and roll back the
  *                            rest: new lengths, dropped pages returned to the
  *                            free stack when their reference count reaches 0.
+ *   svpa_gamma_update        acceptance moving averages and the draft length
+ *                            of the next step (with E[K] / speed-up telemetry).
  *
  * Conventions shared by every entry point
  *  - Every pointer argument is a DEVICE pointer unless its comment says HOST.
@@ -355,6 +357,48 @@ svpa_status svpa_kv_append(int32_t batch, int32_t n_new, int32_t num_kv_heads,
                            int32_t *free_stack, int32_t *free_top,
                            void *k_pool, void *v_pool, float *k_scale,
                            float *v_scale, int32_t *error_flag, void *stream);
+
+/*
+ * Acceptance telemetry and the adaptive draft length, from the accepted
+ * lengths a sampler call left in device memory (no host round trip).
+ *
+ * Sources: "Speculative Decoding & KV-Cache PagedAttention in Enterprise LLM
+ * Serving" (the lookahead follows a moving-average acceptance rate: above
+ * 0.85 -> 5 drafts, above 0.70 -> 4, above 0.50 -> 3, otherwise 2); "The
+ * Sub-Millisecond Speculative Decoding Meltdown", production failure
+ * scenarios (when the moving average collapses below 0.25, fall back to one
+ * token) and its telemetry checklist; "LOW-LATENCY INFERENCE: SPECULATIVE
+ * DECODING & PAGING", acceptance math (E[K], speed-up).
+ *
+ * A sequence that accepted k of gamma drafts ran k + (k < gamma) acceptance
+ * tests.  Per sequence (when seq_state is given), in fp32 with every product
+ * and sum rounded separately:
+ *   A = decay * A + k;  N = decay * N + tests;  alpha = A / N
+ *   seq_gamma_next[b] = 5 if alpha > 0.85, 4 if > 0.70, 3 if > 0.50,
+ *                       2 if >= 0.25, else 1
+ * The batch keeps its own (A, N) in batch_state, updated with the step's
+ * integer totals (sum of k, sum of tests), and batch_gamma_next[0] is the
+ * same table at its alpha (one draft length for the next call, whose kernels
+ * take one n_q).  telemetry[4] (fp32): the batch alpha, the mean accepted
+ * count of this step, E[K] = sum_{i=1..g} alpha^i and the speed-up
+ * (E[K] + 1) / (g * draft_cost_ratio + 1) at the batch's g.
+ *
+ *  accepted_len     int32 [B] (from svpa_spec_accept / _tree)
+ *  seq_state        fp32 [B][2] (A, N), in/out, zero for a new sequence; or NULL
+ *  seq_gamma_next   int32 [B] or NULL (requires seq_state)
+ *  batch_state      fp32 [2], in/out; batch_gamma_next int32 [1]; telemetry fp32 [4]
+ *  decay            in [0, 1] (weight of the past; 0.9 in the Python binding)
+ *  draft_cost_ratio r >= 0 (draft step time / target step time)
+ * Limits: batch >= 1, 1 <= gamma <= 63; else SVPA_ERR_INVALID_ARG.  An
+ * accepted length outside [0, gamma] sets SVPA_DEVERR_BAD_VALUE (the batch
+ * state is then left unchanged).  One kernel (one CTA) on `stream`.
+ */
+svpa_status svpa_gamma_update(int32_t batch, int32_t gamma,
+                              const int32_t *accepted_len, float *seq_state,
+                              int32_t *seq_gamma_next, float *batch_state,
+                              int32_t *batch_gamma_next, float *telemetry,
+                              float decay, float draft_cost_ratio,
+                              int32_t *error_flag, void *stream);
 
 /*
  * svpa_paged_verify_attn without a caller workspace, for callers that may not

@@ -26,6 +26,7 @@ SOURCES = {
     "spec_accept.cu": ["-fmad=false"],
     "block_table_commit.cu": [],
     "kv_append.cu": ["-fmad=false"],
+    "gamma_control.cu": ["-fmad=false"],
     "svpa_noalloc.cu": [],
 }
 

@@ -477,6 +477,29 @@ svpa_status svpa_kv_append(int32_t batch, int32_t n_new, int32_t num_kv_heads, i
     return from_cuda(launch_kv_append(a, static_cast<cudaStream_t>(stream)));
 }
 
+svpa_status svpa_gamma_update(int32_t batch, int32_t gamma, const int32_t *accepted_len, float *seq_state,
+                              int32_t *seq_gamma_next, float *batch_state, int32_t *batch_gamma_next,
+                              float *telemetry, float decay, float draft_cost_ratio, int32_t *error_flag,
+                              void *stream) {
+    if (batch < 1 || gamma < 1 || gamma > kMaxNq - 1 || !(decay >= 0.f && decay <= 1.f) ||
+        !(draft_cost_ratio >= 0.f) || !accepted_len || !batch_state || !batch_gamma_next || !telemetry ||
+        !error_flag || (seq_gamma_next && !seq_state))
+        return SVPA_ERR_INVALID_ARG;
+    GammaArgs a;
+    a.accepted_len = accepted_len;
+    a.seq_state = seq_state;
+    a.seq_gamma_next = seq_gamma_next;
+    a.batch_state = batch_state;
+    a.batch_gamma_next = batch_gamma_next;
+    a.telemetry = telemetry;
+    a.err = error_flag;
+    a.B = batch;
+    a.gamma = gamma;
+    a.decay = decay;
+    a.r = draft_cost_ratio;
+    return from_cuda(launch_gamma_update(a, static_cast<cudaStream_t>(stream)));
+}
+
 svpa_status svpa_check_error(const int32_t *error_flag, void *stream) {
     if (!error_flag) return SVPA_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

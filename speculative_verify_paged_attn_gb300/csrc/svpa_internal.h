@@ -156,4 +156,18 @@ struct AppendArgs {
 };
 cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream);
 
+// Acceptance telemetry and the adaptive draft length.
+struct GammaArgs {
+    const int32_t *accepted_len;
+    float *seq_state;         // [B][2] (A, N) or null
+    int32_t *seq_gamma_next;  // [B] or null
+    float *batch_state;       // [2]
+    int32_t *batch_gamma_next;
+    float *telemetry;         // [4]
+    int32_t *err;
+    int32_t B, gamma;
+    float decay, r;
+};
+cudaError_t launch_gamma_update(const GammaArgs &a, cudaStream_t stream);
+
 }  // namespace svpa

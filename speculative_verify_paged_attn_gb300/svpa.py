@@ -27,7 +27,8 @@ STATUS = {0: "SVPA_OK", 1: "SVPA_ERR_INVALID_ARG", 2: "SVPA_ERR_UNSUPPORTED", 3:
           7: "SVPA_ERR_TIMEOUT"}
 EXPORTS = ("svpa_attn_workspace_size", "svpa_attn_kernel", "svpa_paged_verify_attn", "svpa_spec_accept_workspace_size",
            "svpa_spec_accept", "svpa_spec_accept_tree", "svpa_block_table_commit", "svpa_check_error",
-           "svpa_status_string", "svpa_version", "svpa_paged_verify_attn_noalloc", "svpa_kv_append")
+           "svpa_status_string", "svpa_version", "svpa_paged_verify_attn_noalloc", "svpa_kv_append",
+           "svpa_gamma_update")
 
 
 class SvpaError(RuntimeError):
@@ -67,6 +68,7 @@ def load(path: str = LIB_PATH):
     L.svpa_block_table_commit.argtypes = [I] * 5 + [P] * 7 + [I, P, P, I, I, I, P, P]
     L.svpa_paged_verify_attn_noalloc.argtypes = [ctypes.POINTER(AttnParams)] + [P] * 12
     L.svpa_kv_append.argtypes = [I] * 8 + [P] * 13
+    L.svpa_gamma_update.argtypes = [I, I] + [P] * 6 + [ctypes.c_float, ctypes.c_float, P, P]
     L.svpa_check_error.argtypes = [P, P]
     L.svpa_status_string.argtypes = [I]
     L.svpa_status_string.restype = ctypes.c_char_p
@@ -221,6 +223,19 @@ def kv_append(new_k, new_v, block_table, context_lens, refcount, free_stack, fre
         _p(k_scale), _p(v_scale), _p(error_flag), _stream(stream))
     if check:
         _check(st, "svpa_kv_append")
+    return st
+
+
+def gamma_update(gamma, accepted_len, batch_state, batch_gamma, telemetry, *, error_flag, seq_state=None,
+                 seq_gamma=None, decay=0.9, draft_cost_ratio=0.0, stream=None, check=True) -> int:
+    """svpa_gamma_update: acceptance moving averages (per sequence when
+    seq_state [B, 2] is given, and for the batch in batch_state [2]) and the
+    draft length of the next step (seq_gamma [B], batch_gamma [1])."""
+    st = load().svpa_gamma_update(
+        accepted_len.shape[0], gamma, _p(accepted_len), _p(seq_state), _p(seq_gamma), _p(batch_state),
+        _p(batch_gamma), _p(telemetry), float(decay), float(draft_cost_ratio), _p(error_flag), _stream(stream))
+    if check:
+        _check(st, "svpa_gamma_update")
     return st
 
 

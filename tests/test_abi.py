@@ -94,6 +94,14 @@ def test_null_pointers_rejected_before_launch(lib):
     odd = ctypes.c_void_p(24)
     assert lib.svpa_kv_append(*base, nz, nz, nz, nz, nz, nz, nz, odd, nz, None, None, nz, None) == 1
     assert lib.svpa_kv_append(0, 5, 4, 64, 16, 8, 16, 0, *([None] * 13)) == 0
+    # adaptive draft length: sizes, decay and ratio checked before any launch
+    F = ctypes.c_float
+    for args in [(0, 4, F(0.9), F(0.0)), (2, 0, F(0.9), F(0.0)), (2, 64, F(0.9), F(0.0)),
+                 (2, 4, F(1.5), F(0.0)), (2, 4, F(0.9), F(-1.0)), (2, 4, F(float("nan")), F(0.0))]:
+        b, g, d, r = args
+        assert lib.svpa_gamma_update(b, g, nz, None, None, nz, nz, nz, d, r, nz, None) == 1, args
+    assert lib.svpa_gamma_update(2, 4, nz, None, nz, nz, nz, nz, F(0.9), F(0.0), nz, None) == 1
+    assert lib.svpa_gamma_update(2, 4, None, None, None, nz, nz, nz, F(0.9), F(0.0), nz, None) == 1
     # empty batch is a no-op
     p0 = svpa.attn_params(0, 5, 4, 4, 64, 8, 16, split_pages=4)
     assert lib.svpa_paged_verify_attn(ctypes.byref(p0), *([None] * 11), 0, None, None) == 0
