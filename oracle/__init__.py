@@ -136,12 +136,14 @@ def e4m3_to_double(byte: int) -> float:
 
 def paged_verify_attn(q_bits, k_pool, v_pool, block_table, context_lens, *,
                       num_kv_heads, sm_scale, kv_fp8=False, k_scale=None,
-                      v_scale=None, ancestor_mask=None, nthreads=0):
+                      v_scale=None, ancestor_mask=None, nthreads=0, scale_tile=0):
     """fp64 masked attention of each sequence's n_q queries over its paged history.
 
     q_bits: uint16 bf16 bits [B, n_q, Hq, D]; k_pool/v_pool: uint16 bf16 bits or
     uint8 E4M3 bytes [num_blocks, Hkv, BS, D]; block_table int32 [B, max_blocks];
     context_lens int32 [B]; ancestor_mask uint64 [n_q] or None (causal).
+    FP8 scales: [num_blocks, Hkv] (scale_tile 0) or one per 64-element tile of
+    a row, [num_blocks, Hkv, BS, D / 64] (scale_tile 64).
     Returns (out fp64 [B, n_q, Hq, D], lse fp64 [B, n_q, Hq]).
     """
     lib = _load()
@@ -159,7 +161,7 @@ def paged_verify_attn(q_bits, k_pool, v_pool, block_table, context_lens, *,
     out = np.zeros((B, n_q, Hq, D), np.float64)
     lse = np.zeros((B, n_q, Hq), np.float64)
     rc = lib.oracle_paged_verify_attn(B, n_q, Hq, Hkv, D, BS, bt.shape[1], num_blocks,
-                                      int(bool(kv_fp8)), float(sm_scale), _ptr(q),
+                                      (2 if scale_tile == 64 else 1) if kv_fp8 else 0, float(sm_scale), _ptr(q),
                                       _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt),
                                       _ptr(cl), _ptr(am), _ptr(out), _ptr(lse), int(nthreads))
     if rc != 0:
@@ -253,7 +255,7 @@ def block_table_commit(block_table, context_lens, accepted_len, refcount, free_s
 
 
 def kv_append(new_k, new_v, block_table, context_lens, refcount, free_stack, free_top, k_pool,
-              v_pool, k_scale=None, v_scale=None, *, block_size=16):
+              v_pool, k_scale=None, v_scale=None, *, block_size=16, scale_tile=0):
     """Append the new rows on copies of the inputs; returns the updated copies.
 
     new_k, new_v: bf16 [B, n_new, Hkv, D]; pools bf16 or float8_e4m3fn (or raw
@@ -277,7 +279,8 @@ def kv_append(new_k, new_v, block_table, context_lens, refcount, free_stack, fre
     fp8 = isz == 1
     ks = _c(k_scale, np.float32).copy() if fp8 else None
     vs = _c(v_scale, np.float32).copy() if fp8 else None
-    rc = lib.oracle_kv_append(B, n_new, Hkv, D, block_size, bt.shape[1], rcnt.shape[0], int(fp8),
+    mode = (2 if scale_tile == 64 else 1) if fp8 else 0
+    rc = lib.oracle_kv_append(B, n_new, Hkv, D, block_size, bt.shape[1], rcnt.shape[0], mode,
                               _ptr(nk), _ptr(nv), _ptr(bt), _ptr(cl), _ptr(rcnt), _ptr(fs), _ptr(ft),
                               _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs))
     if rc != 0:

@@ -116,7 +116,11 @@ int oracle_max_threads(void) {
  * The kv head of query head h is h / (Hq / Hkv).
  * Inputs: q bf16 bits [B, n_q, Hq, D]; k_pool, v_pool [num_blocks, Hkv, BS, D]
  * of bf16 bits (kv_fp8 == 0) or E4M3 bytes (kv_fp8 != 0); k_scale, v_scale
- * fp32 [num_blocks, Hkv] (FP8 only); block_table int32 [B, max_blocks];
+ * fp32 (FP8 only): kv_fp8 == 1, one per (block, kv head), [num_blocks, Hkv];
+ * kv_fp8 == 2, one per 64 consecutive elements of a token's row ("The
+ * Sub-Millisecond Speculative Decoding Meltdown", implementation checklist:
+ * block scales per 64-element tile), [num_blocks, Hkv, BS, D / 64];
+ * block_table int32 [B, max_blocks];
  * context_lens int32 [B]; ancestor_mask uint64 [n_q] or NULL.
  * Outputs: out fp64 [B, n_q, Hq, D]; lse fp64 [B, n_q, Hq] (may be NULL).
  */
@@ -133,6 +137,7 @@ int oracle_paged_verify_attn(int B, int n_q, int Hq, int Hkv, int D, int BS,
         D < 1 || BS < 1 || max_blocks < 1 || num_blocks < 1)
         return ORC_ERR_ARG;
     if (kv_fp8 && (!k_scale || !v_scale)) return ORC_ERR_ARG;
+    if (kv_fp8 < 0 || kv_fp8 > 2 || (kv_fp8 == 2 && D % 64 != 0)) return ORC_ERR_ARG;
     for (int b = 0; b < B; ++b) {
         long T = (long)context_lens[b] + n_q;
         if (context_lens[b] < 0 || (T + BS - 1) / BS > max_blocks) return ORC_ERR_ARG;
@@ -161,10 +166,11 @@ int oracle_paged_verify_attn(int B, int n_q, int Hq, int Hkv, int D, int BS,
                 if (kv_fp8) {
                     const uint8_t *kp = (const uint8_t *)k_pool;
                     const uint8_t *vp = (const uint8_t *)v_pool;
-                    K[p * D + d] = oracle_e4m3_to_double(kp[base + d]) *
-                                   (double)k_scale[(long)blk * Hkv + g];
-                    V[p * D + d] = oracle_e4m3_to_double(vp[base + d]) *
-                                   (double)v_scale[(long)blk * Hkv + g];
+                    /* scale of this element: its (block, kv head), or its 64-element tile */
+                    const long si = kv_fp8 == 1 ? (long)blk * Hkv + g
+                                                : (((long)blk * Hkv + g) * BS + slot) * (D / 64) + d / 64;
+                    K[p * D + d] = oracle_e4m3_to_double(kp[base + d]) * (double)k_scale[si];
+                    V[p * D + d] = oracle_e4m3_to_double(vp[base + d]) * (double)v_scale[si];
                 } else {
                     const uint16_t *kp = (const uint16_t *)k_pool;
                     const uint16_t *vp = (const uint16_t *)v_pool;
@@ -577,8 +583,15 @@ static float bf16_bits_to_float(uint16_t h) {
  * from their decoded value only when the scale changes; every code is
  * e4m3(value / scale) with one fp32 division; slots past the last row are 0.
  *
+ * FP8 pools with one scale per 64-element tile (fp8 = 2; "The Sub-Millisecond
+ * Speculative Decoding Meltdown", implementation checklist: block scales per
+ * 64-element tile): each 64-value tile of a new row gets scale = amax / 448
+ * of its own values (1 when amax = 0) and codes e4m3(value / scale); history
+ * rows keep their codes and scales; codes past the last row are 0.
+ *
  * new_k, new_v: bf16 bits [B, n_new, Hkv, D]; pools [num_blocks, Hkv, BS, D]
- * of bf16 bits (fp8 = 0) or E4M3 bytes (fp8 = 1); scales [num_blocks, Hkv].
+ * of bf16 bits (fp8 = 0) or E4M3 bytes (fp8 = 1, 2); scales [num_blocks, Hkv]
+ * (fp8 = 1) or [num_blocks, Hkv, BS, D / 64] (fp8 = 2).
  */
 int oracle_kv_append(int B, int n_new, int Hkv, int D, int BS, int max_blocks, int num_blocks,
                      int fp8, const uint16_t *new_k, const uint16_t *new_v, int32_t *block_table,
@@ -588,8 +601,10 @@ int oracle_kv_append(int B, int n_new, int Hkv, int D, int BS, int max_blocks, i
     if (B < 0 || n_new < 1 || Hkv < 1 || D < 1 || BS < 1 || max_blocks < 1 || num_blocks < 1)
         return ORC_ERR_ARG;
     if (fp8 && (!k_scale || !v_scale)) return ORC_ERR_ARG;
+    if (fp8 < 0 || fp8 > 2 || (fp8 == 2 && D % 64 != 0)) return ORC_ERR_ARG;
     const size_t eb = fp8 ? 1 : 2;
     const size_t page_bytes = (size_t)Hkv * BS * D * eb; /* one block, all heads */
+    const long scales_per_block = fp8 == 2 ? (long)Hkv * BS * (D / 64) : Hkv;
     for (int b = 0; b < B; ++b) {
         const long L = context_lens[b], end = L + n_new;
         if (L < 0 || (end + BS - 1) / BS > max_blocks) return ORC_ERR_ARG;
@@ -615,9 +630,9 @@ int oracle_kv_append(int B, int n_new, int Hkv, int D, int BS, int max_blocks, i
                 memcpy((char *)v_pool + (size_t)blk * page_bytes,
                        (char *)v_pool + (size_t)*ent * page_bytes, page_bytes);
                 if (fp8)
-                    for (int h = 0; h < Hkv; ++h) {
-                        k_scale[(long)blk * Hkv + h] = k_scale[(long)*ent * Hkv + h];
-                        v_scale[(long)blk * Hkv + h] = v_scale[(long)*ent * Hkv + h];
+                    for (long x = 0; x < scales_per_block; ++x) {
+                        k_scale[(long)blk * scales_per_block + x] = k_scale[(long)*ent * scales_per_block + x];
+                        v_scale[(long)blk * scales_per_block + x] = v_scale[(long)*ent * scales_per_block + x];
                     }
                 refcount[*ent] -= 1;
                 refcount[blk] = 1;
@@ -644,6 +659,26 @@ int oracle_kv_append(int B, int n_new, int Hkv, int D, int BS, int max_blocks, i
                         continue;
                     }
                     uint8_t *t8 = (uint8_t *)pool + tile;
+                    if (fp8 == 2) {
+                        for (long s = hist; s < vend; ++s)
+                            for (int t0 = 0; t0 < D; t0 += 64) {
+                                const uint16_t *row = src + (((size_t)b * n_new + (ps + s - L)) * Hkv + h) * D;
+                                float amax = 0.f;
+                                for (int d = t0; d < t0 + 64; ++d) {
+                                    float v = bf16_bits_to_float(row[d]);
+                                    float a = v < 0 ? -v : v;
+                                    if (a > amax) amax = a;
+                                }
+                                volatile float sc = amax > 0.f ? amax / 448.0f : 1.0f;
+                                for (int d = t0; d < t0 + 64; ++d) {
+                                    volatile float q = bf16_bits_to_float(row[d]) / sc;
+                                    t8[s * D + d] = oracle_e4m3_encode(q);
+                                }
+                                scale[(((long)blk * Hkv + h) * BS + s) * (D / 64) + t0 / 64] = sc;
+                            }
+                        for (long s = vend; s < BS; ++s) memset(t8 + s * D, 0, (size_t)D);
+                        continue;
+                    }
                     const float old_scale = scale[(long)blk * Hkv + h];
                     float amax = 0.f;
                     for (long s = 0; s < hist; ++s)

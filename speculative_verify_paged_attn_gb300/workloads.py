@@ -74,6 +74,7 @@ class Workload:
     sigma_target: float             # target logits ~ N(0, sigma_target)
     sigma_draft: float              # draft logits = target logits + N(0, sigma_draft)
     kv_fp8: bool = False
+    scale_tile: int = 0             # FP8 scales: 0 = one per (page, kv head); 64 = one per 64-element tile
     tree_branching: Optional[tuple] = None
     shared_prefix: int = 0          # tokens of a refcounted prefix shared by all sequences
     fixed_pool_blocks: Optional[int] = None
@@ -159,7 +160,8 @@ class AttnInputs:
         b = tokens * wl.num_kv_heads * wl.head_dim * 2 * eb
         if wl.kv_fp8:
             pages = int(((T + BLOCK_SIZE - 1) // BLOCK_SIZE).sum().item())
-            b += pages * wl.num_kv_heads * 2 * 4
+            per_page = BLOCK_SIZE * (wl.head_dim // 64) if wl.scale_tile == 64 else 1
+            b += pages * wl.num_kv_heads * per_page * 2 * 4
         return b
 
 
@@ -232,11 +234,19 @@ def make_attention(wl: Workload, seed: int, device="cpu", poison: bool = True,
         vf = torch.where(mask, vf, torch.zeros((), device=dev))
 
         def quantise(x):
+            if wl.scale_tile == 64:
+                # one scale per 64 consecutive elements of a token's row
+                xt = x.unflatten(3, (Hd // 64, 64))
+                amax = xt.abs().amax(dim=4)
+                scale = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax))
+                y = (xt / scale[..., None]).clamp(-FP8_MAX, FP8_MAX).flatten(3)
+                return y.to(torch.float8_e4m3fn), scale.to(torch.float32).contiguous()
             amax = x.abs().amax(dim=(2, 3))
             scale = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax))
             y = (x / scale[:, :, None, None]).clamp(-FP8_MAX, FP8_MAX)
             return y.to(torch.float8_e4m3fn), scale.to(torch.float32).contiguous()
 
+        Hd = D
         k_pool, k_scale = quantise(kf)
         v_pool, v_scale = quantise(vf)
         del kf, vf
@@ -344,12 +354,15 @@ class AppendInputs:
     def write_bytes(self) -> int:
         """Bytes the append must move at least: the new rows read once and
         written once (bf16), or, for FP8, each touched (page, head) tile read
-        and written once plus the new rows read once."""
+        and written once plus the new rows read once (with 64-element tile
+        scales: the new rows read, their codes and scales written)."""
         wl = self.wl
         B, n, Hkv, D = self.new_k.shape
         rows = B * n * Hkv * D * 2 * 2          # K and V, bf16
         if not wl.kv_fp8:
             return 2 * rows
+        if wl.scale_tile == 64:                  # codes and tile scales of the new rows only
+            return rows + rows // 2 + B * n * Hkv * (D // 64) * 4 * 2
         L = self.context_lens.to(torch.int64).cpu()
         first, last = L // BLOCK_SIZE, (L + n - 1) // BLOCK_SIZE
         tiles = int((last - first + 1).sum().item()) * Hkv * 2
@@ -429,6 +442,13 @@ def make_append(wl: Workload, seed: int, device="cpu", batch: Optional[int] = No
     if wl.kv_fp8:
         def quantise(x):
             x = torch.where(mask, x, torch.zeros((), device=dev))
+            if wl.scale_tile == 64:
+                xt = x.unflatten(3, (D // 64, 64))
+                amax = xt.abs().amax(dim=4)
+                scale = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax))
+                y = (xt / scale[..., None]).clamp(-FP8_MAX, FP8_MAX).flatten(3).to(torch.float8_e4m3fn)
+                yb = torch.where(mask, y.view(torch.uint8), torch.tensor(0x7E, dtype=torch.uint8, device=dev))
+                return yb.view(torch.float8_e4m3fn).contiguous(), scale.to(torch.float32).contiguous()
             amax = x.abs().amax(dim=(2, 3))
             scale = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax))
             y = (x / scale[:, :, None, None]).clamp(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)

@@ -152,3 +152,61 @@ def test_fp8_quantise_on_write_worked_page():
                           r2["free_stack"], r2["free_top"], r2["k_pool"], r2["v_pool"], r2["k_scale"], r2["v_scale"])
     assert r3["k_scale"][blk, 0] == s2
     assert np.array_equal(r3["k_pool"][blk, 0, :3], r2["k_pool"][blk, 0, :3])
+
+
+def test_fp8_tile_scales_quantise_each_new_row_tile():
+    # one scale per 64 consecutive elements of a row: a new row's tiles get
+    # amax/448 of their own values; history rows keep codes and scales
+    Hkv, D, nb = 2, 128, 6
+    g = torch.Generator().manual_seed(11)
+    kp = torch.randint(0, 120, (nb, Hkv, BS, D), generator=g).to(torch.uint8)
+    vp = torch.randint(0, 120, (nb, Hkv, BS, D), generator=g).to(torch.uint8)
+    ks = torch.rand(nb, Hkv, BS, D // 64, generator=g) + 0.01
+    vs = torch.rand(nb, Hkv, BS, D // 64, generator=g) + 0.01
+    bt = np.array([[2, -1], [4, 5]], np.int32)  # sequence 1 shares nothing; pages hold 5 and 17 tokens
+    rc = np.zeros(nb, np.int32)
+    rc[[2, 4, 5]] = 1
+    fs = np.array([0, 1, 3, -1, -1, -1], np.int32)
+    L = np.array([5, 17], np.int32)
+    rows = (torch.randn(2, 3, Hkv, D, generator=g) * torch.tensor([0.1, 1.0, 20.0])[None, :, None, None])
+    rows[0, 1, 0, 64:] = 0.0  # an all-zero tile: scale 1
+    rows = rows.to(torch.bfloat16)
+    r = oracle.kv_append(rows, rows, bt, L, rc, fs, 3, kp, vp, ks, vs, scale_tile=64)
+    ksr = r["k_scale"].reshape(nb, Hkv, BS, D // 64)
+    for b, blk, s0 in [(0, 2, 5), (1, 5, 1)]:
+        for t in range(3):
+            for h in range(Hkv):
+                for tile in range(2):
+                    x = rows[b, t, h, 64 * tile:64 * tile + 64].float()
+                    amax = x.abs().max()
+                    sc = np.float32(amax) / np.float32(448.0) if amax > 0 else np.float32(1.0)
+                    assert ksr[blk, h, s0 + t, tile] == sc
+                    want = (x / torch.tensor(sc)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                    assert np.array_equal(r["k_pool"][blk, h, s0 + t, 64 * tile:64 * tile + 64], want)
+    assert ksr[2, 0, 6, 1] == np.float32(1.0)
+    # history rows and their scales are untouched; codes past the last row are 0
+    assert np.array_equal(r["k_pool"][2, :, :5], kp[2, :, :5].numpy())
+    assert np.array_equal(ksr[2, :, :5], ks[2, :, :5].numpy())
+    assert not r["k_pool"][2, :, 8:].any()
+
+
+def test_fp8_tile_scales_copy_on_write_carries_tile_scales():
+    kp, vp, bt, rc, fs, ft, L = make_state(3, L=(10, 10, 37), shared=(0, 1))
+    kp8 = torch.randint(0, 120, tuple(kp.shape)).to(torch.uint8)
+    vp8 = torch.randint(0, 120, tuple(vp.shape)).to(torch.uint8)
+    # D = 8 is not a multiple of 64: the tile mode needs D % 64 == 0
+    nk = torch.randn(3, 2, 2, 8).to(torch.bfloat16)
+    ks = torch.rand(24, 2, BS, 1)
+    with pytest.raises(oracle.OracleError):
+        oracle.kv_append(nk, nk, bt, L, rc, fs, ft, kp8, vp8, ks, ks, scale_tile=64)
+    g = torch.Generator().manual_seed(4)
+    kp8 = torch.randint(0, 120, (24, 2, BS, 64), generator=g).to(torch.uint8)
+    ks = torch.rand(24, 2, BS, 1, generator=g)
+    nk = torch.randn(3, 2, 2, 64, generator=g).to(torch.bfloat16)
+    r = oracle.kv_append(nk, nk, bt, L, rc, fs, ft, kp8, kp8.clone(), ks, ks.clone(), scale_tile=64)
+    shared = int(bt[0, 0])
+    t0, t1 = r["block_table"][0, 0], r["block_table"][1, 0]
+    ksr = r["k_scale"].reshape(24, 2, BS, 1)
+    for t in (t0, t1):  # both views keep the shared history's codes and tile scales
+        assert np.array_equal(r["k_pool"][t, :, :10], kp8[shared, :, :10].numpy())
+        assert np.array_equal(ksr[t, :, :10], ks[shared, :, :10].numpy())

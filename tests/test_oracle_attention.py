@@ -220,3 +220,55 @@ def test_rejects_bad_block(oracle_mod):
     inp.block_table[0, 0] = inp.num_blocks
     with pytest.raises(oracle_mod.OracleError):
         run_oracle(oracle_mod, inp)
+
+
+def tile_scaled_reference(inp: W.AttnInputs):
+    """SDPA in fp64 on pages decoded with one scale per 64-element tile of a
+    row: the scale array [blocks, Hkv, 16, D/64] is broadcast to full rows."""
+    ks = inp.k_scale.double().repeat_interleave(64, dim=3)  # [blocks, Hkv, 16, D]
+    vs = inp.v_scale.double().repeat_interleave(64, dim=3)
+    k = inp.k_pool.to(torch.float64) * ks
+    v = inp.v_pool.to(torch.float64) * vs
+    # the same gather as the per-page reference, on already decoded pages
+    dec = W.AttnInputs(wl=inp.wl.scaled(kv_fp8=False, scale_tile=0), q=inp.q, k_pool=k, v_pool=v,
+                       k_scale=None, v_scale=None, block_table=inp.block_table,
+                       context_lens=inp.context_lens, ancestor_mask=inp.ancestor_mask,
+                       refcount=inp.refcount, free_stack=inp.free_stack, free_top=inp.free_top)
+    return gathered_reference(dec)
+
+
+def run_oracle_tiles(oracle_mod, inp: W.AttnInputs):
+    wl = inp.wl
+    return oracle_mod.paged_verify_attn(
+        inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.context_lens,
+        num_kv_heads=wl.num_kv_heads, sm_scale=wl.sm_scale, kv_fp8=True, k_scale=inp.k_scale,
+        v_scale=inp.v_scale, scale_tile=64,
+        ancestor_mask=None if inp.ancestor_mask is None else inp.ancestor_mask.numpy().view(np.uint64))
+
+
+@pytest.mark.parametrize("name", ["fp8", "tree"])
+def test_fp8_tile_scales_match_sdpa(oracle_mod, name):
+    # one scale per 64 consecutive elements of a token's row: a swapped slot,
+    # head or tile index in the oracle's decode would change the values
+    base = W.WORKLOADS[name]
+    wl = base.scaled(batch=3, ctx_lo=20, ctx_hi=90, fixed_contexts=None, kv_fp8=True, scale_tile=64,
+                     shared_prefix=min(base.shared_prefix, 32))
+    inp = W.make_attention(wl, 9)
+    assert tuple(inp.k_scale.shape[2:]) == (16, wl.head_dim // 64)
+    # the tile scales really differ within every page a sequence maps
+    used = inp.block_table[inp.block_table >= 0].long().unique()
+    assert inp.k_scale[used].std(dim=(2, 3)).min() > 0
+    out, _ = run_oracle_tiles(oracle_mod, inp)
+    ref = tile_scaled_reference(inp)
+    assert np.max(np.abs(out - ref)) < 1e-11
+
+
+def test_fp8_tile_scales_equal_to_page_scale_reduce_to_per_page(oracle_mod):
+    wl = W.WORKLOADS["fp8"].scaled(batch=2, ctx_lo=40, ctx_hi=70, fixed_contexts=None)
+    inp = W.make_attention(wl, 5)
+    out_page, _ = run_oracle(oracle_mod, inp)
+    tiles = W.AttnInputs(**{**inp.__dict__,
+                            "k_scale": inp.k_scale[:, :, None, None].expand(-1, -1, 16, 2).contiguous(),
+                            "v_scale": inp.v_scale[:, :, None, None].expand(-1, -1, 16, 2).contiguous()})
+    out_tile, _ = run_oracle_tiles(oracle_mod, tiles)
+    assert np.array_equal(out_page, out_tile)
