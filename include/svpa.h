@@ -92,6 +92,15 @@ typedef struct svpa_attn_params {
     int32_t variant;            /* 0 = chosen by library; 1 = warp-level MMA
                                    kernel; 2 = tcgen05/TMEM kernel (head_dim
                                    128; FP8 pages with Hq / Hkv * n_q <= 64)   */
+    int32_t scale_tile;         /* FP8 scale granularity: 0 = one scale per
+                                   (page, kv head); 64 = one scale per 64
+                                   consecutive elements of a token's row
+                                   ("The Sub-Millisecond Speculative Decoding
+                                   Meltdown", implementation checklist:
+                                   block scales per 64-element tile), on the
+                                   tcgen05 kernel only (head_dim 128,
+                                   Hq / Hkv * n_q <= 64), else
+                                   SVPA_ERR_UNSUPPORTED                        */
 } svpa_attn_params;
 
 /* The attention kernel svpa_paged_verify_attn runs for `p`: 1 = warp-level
@@ -130,7 +139,10 @@ svpa_status svpa_attn_workspace_size(const svpa_attn_params *p, size_t *bytes);
  *               encoding); 16-byte aligned
  *  k_scale,
  *  v_scale      fp32 [num_blocks, Hkv] (FP8 only; NULL for bf16): the real
- *               value of a stored byte x is e4m3(x) * scale[block][kv head]
+ *               value of a stored byte x is e4m3(x) * scale[block][kv head];
+ *               with scale_tile 64: fp32 [num_blocks, Hkv, 16, D / 64],
+ *               16-byte aligned, the byte at (block, head, slot, d) scaled by
+ *               scale[block][head][slot][d / 64]
  *  block_table  int32 [B, max_blocks_per_seq]; entries past a sequence's last
  *               page are ignored
  *  context_lens int32 [B], committed history L_b >= 0 with
@@ -325,6 +337,12 @@ svpa_status svpa_block_table_commit(int32_t batch, int32_t n_q,
  *   history codes are re-encoded from their values only when the scale
  *   changes; new codes = e4m3(x / scale), round to nearest even, saturating
  *   at +-448; slots past the last row of the page are set to 0.
+ * FP8 pools with scale_tile 64 (one scale per 64 consecutive elements of a
+ * row; scales [num_blocks, Hkv, 16, head_dim / 64]): each 64-value tile of a
+ * new row gets scale = amax / 448 of its own values (1 when amax is 0) and
+ * codes e4m3(value / scale); history rows keep their codes and scales; codes
+ * past the last row are 0.  ("The Sub-Millisecond Speculative Decoding
+ * Meltdown", implementation checklist: block scales per 64-element tile.)
  * bf16 pools receive the row bits unchanged; their slots past the last row
  * are left as they were.
  *
@@ -335,7 +353,9 @@ svpa_status svpa_block_table_commit(int32_t batch, int32_t n_q,
  *  free_stack    int32 [num_blocks] (in/out), free_top int32 [1] (in/out)
  *  k_pool, v_pool [num_blocks, Hkv, 16, D] bf16 or E4M3 bytes (in/out),
  *                16-byte aligned
- *  k_scale, v_scale fp32 [num_blocks, Hkv] (in/out; FP8 only, else NULL)
+ *  k_scale, v_scale fp32 [num_blocks, Hkv], or [num_blocks, Hkv, 16,
+ *                head_dim / 64] with scale_tile 64 (in/out; FP8 only, else NULL)
+ *  scale_tile    0, or 64 (FP8 with head_dim a multiple of 64)
  *  error_flag    int32 [1], zero before the call
  * Limits: 1 <= n_new <= 4096, 1 <= num_kv_heads <= 4096, block_size 16;
  * head_dim a multiple of 8 up to 1024 (bf16) or of 16 up to 256 (FP8); else
@@ -351,7 +371,8 @@ svpa_status svpa_block_table_commit(int32_t batch, int32_t n_q,
 svpa_status svpa_kv_append(int32_t batch, int32_t n_new, int32_t num_kv_heads,
                            int32_t head_dim, int32_t block_size,
                            int32_t max_blocks_per_seq, int32_t num_blocks,
-                           int32_t kv_dtype, const void *new_k,
+                           int32_t kv_dtype, int32_t scale_tile,
+                           const void *new_k,
                            const void *new_v, int32_t *block_table,
                            const int32_t *context_lens, int32_t *refcount,
                            int32_t *free_stack, int32_t *free_top,

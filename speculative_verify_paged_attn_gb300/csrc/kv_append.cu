@@ -137,11 +137,13 @@ __global__ void __launch_bounds__(kAllocThreads) append_alloc_kernel(const __gri
                 }
             }
         }
-        if (a.fp8)
-            for (int h = threadIdx.x; h < a.Hkv; h += kAllocThreads) {
-                a.k_scale[(size_t)s_dst[c] * a.Hkv + h] = a.k_scale[(size_t)s_src[c] * a.Hkv + h];
-                a.v_scale[(size_t)s_dst[c] * a.Hkv + h] = a.v_scale[(size_t)s_src[c] * a.Hkv + h];
+        if (a.fp8) {
+            const size_t n = (size_t)a.scales_per_block;
+            for (size_t x = threadIdx.x; x < n; x += kAllocThreads) {
+                a.k_scale[(size_t)s_dst[c] * n + x] = a.k_scale[(size_t)s_src[c] * n + x];
+                a.v_scale[(size_t)s_dst[c] * n + x] = a.v_scale[(size_t)s_src[c] * n + x];
             }
+        }
     }
 }
 
@@ -275,6 +277,48 @@ __global__ void __launch_bounds__(kWriteThreads) append_write_kernel(const __gri
         if (blk < 0) return;
         uint4 *tile = reinterpret_cast<uint4 *>((kv ? a.v_pool : a.k_pool) +
                                                 ((size_t)blk * Hkv + h) * kBlockSize * D);
+        if (a.scale_tile) {
+            // one scale per 64-element tile of a new row (4 chunks, 4
+            // consecutive lanes): amax / 448 of its own values; history rows
+            // keep codes and scales; codes past the last row are 0
+            float *tsc = (kv ? a.v_scale : a.k_scale) + ((size_t)blk * Hkv + h) * kBlockSize * (D / 64);
+#pragma unroll
+            for (int k = 0; k < kMaxChunksFp8; ++k) {
+                const int c = lane + 32 * k;
+                if (c >= nch) continue;  // uniform across the warp (nch is a multiple of 32)
+                const int s = c / cpr;
+                const bool fresh = s >= hist && s < vend;
+                const uint32_t w[8] = {ra[k].x, ra[k].y, ra[k].z, ra[k].w, rb[k].x, rb[k].y, rb[k].z, rb[k].w};
+                float amax = 0.f;
+                if (fresh) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[j] & 0xffffu)));
+                        amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[j] >> 16)));
+                    }
+                }
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                if (s < hist) continue;
+                if (!fresh) {
+                    tile[c] = make_uint4(0u, 0u, 0u, 0u);
+                    continue;
+                }
+                const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+                uint32_t o4[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float v[4] = {__fdiv_rn(bf16_bits_to_f32(w[2 * j] & 0xffffu), sc),
+                                  __fdiv_rn(bf16_bits_to_f32(w[2 * j] >> 16), sc),
+                                  __fdiv_rn(bf16_bits_to_f32(w[2 * j + 1] & 0xffffu), sc),
+                                  __fdiv_rn(bf16_bits_to_f32(w[2 * j + 1] >> 16), sc)};
+                    o4[j] = encode4(v);
+                }
+                tile[c] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                if ((c & 3) == 0) tsc[s * (D / 64) + (c - s * cpr) / 4] = sc;
+            }
+            return;
+        }
         float *scale = (kv ? a.v_scale : a.k_scale) + (size_t)blk * Hkv + h;
         const float old_scale = *scale;
 #pragma unroll

@@ -54,6 +54,7 @@ constexpr int kBarEpi = 1;                      // named barrier of the epilogue
 constexpr int kPage8 = 16 * 128;                // one FP8 (page, kv head) tile
 constexpr int kTile8 = kPagesPerBlock * kPage8;  // FP8 K (or V) block: 16 KB
 constexpr float kMaxScale8 = 146.f;             // 448 * scale stays below the f16 maximum
+constexpr int kTileScales = 16 * (128 / 64);    // tile scales of one (page, kv head): 16 rows x 2
 
 // Two layouts of the same kernel.
 //  bf16 pages: warps 0 producer, 1 MMA, 2-5 softmax, 6-9 epilogue; 3-deep K
@@ -103,6 +104,9 @@ template <bool FP8>
 struct Stage8 {  // FP8 staging rings
     uint8_t k8[TcCfg<FP8>::kNK8][kTile8];
     uint8_t v8[TcCfg<FP8>::kNV8][kTile8];
+    // one scale per 64-element tile of each row of a staged block (tile-scale mode)
+    float sc64k[TcCfg<FP8>::kNK8][kPagesPerBlock][kTileScales];
+    float sc64v[TcCfg<FP8>::kNV8][kPagesPerBlock][kTileScales];
     float ksc[kNMeta][kPagesPerBlock];  // page scales of the blocks in flight
     float vsc[kNMeta][kPagesPerBlock];
     uint64_t k8_full[TcCfg<FP8>::kNK8], k8_empty[TcCfg<FP8>::kNK8];
@@ -251,13 +255,18 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
         };
         // FP8: the page's scale by cp.async, counted on the same staging
         // barrier (a missing page takes the block's first page's scale: its
-        // bytes are zero)
-        auto copy_scale = [&](const float *scales, int id, int hh, float *dst, uint64_t *bar) {
+        // bytes are zero); with tile scales also the page's 32 tile scales
+        // (128 bytes) by a bulk copy counted in the barrier's bytes, and the
+        // 4-byte copy takes the page's first tile scale
+        auto copy_scale = [&](const float *scales, int id, int hh, float *dst, float *dst64, uint64_t *bar) {
             const int id0 = __shfl_sync(0x000000ffu, id, 0);
             const int sid = (id >= 0 && id < a.num_blocks) ? id : id0;
-            cp_async_4(dst, scales + (size_t)sid * a.Hkv + hh);
+            const size_t page = (size_t)sid * a.Hkv + hh;
+            cp_async_4(dst, scales + (a.scale_tile ? page * kTileScales : page));
             cp_async_mbar_arrive_noinc(bar);
+            if (a.scale_tile) bulk_copy_g2s(dst64, scales + page * kTileScales, kTileScales * 4, bar);
         };
+        const uint32_t tile_bytes = FP8 && a.scale_tile ? kPagesPerBlock * kTileScales * 4 : 0u;
         auto k_slot = [&](int s_) -> uint8_t * {
             if constexpr (FP8) return sm.st8.k8[s_]; else return sm.kbuf[s_];
         };
@@ -273,11 +282,13 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             int ready = 1;
             if (lane == 0 && jv >= PNV) ready = mbar_test(&pv_empty[vs], (uint32_t)(((jv / PNV) & 1) ^ 1));
             if (!__shfl_sync(0xffffffffu, ready, 0)) return false;
-            if (lane == 0) mbar_arrive_expect_tx(&pv_full[vs], kBlockBytes);
+            if (lane == 0) mbar_arrive_expect_tx(&pv_full[vs], kBlockBytes + tile_bytes);
             if (lane < kPagesPerBlock) {
                 const int id = sm.vid[jv % kNMeta][lane], hh = sm.meta[jv % kNMeta].h;
                 copy_page(&mvp, v_slot(vs), id, hh, &pv_full[vs]);
-                if constexpr (FP8) copy_scale(a.v_scale, id, hh, &sm.st8.vsc[jv % kNMeta][lane], &pv_full[vs]);
+                if constexpr (FP8)
+                    copy_scale(a.v_scale, id, hh, &sm.st8.vsc[jv % kNMeta][lane], sm.st8.sc64v[vs][lane],
+                               &pv_full[vs]);
             }
             __syncwarp();
             ++jv;
@@ -362,7 +373,7 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                         uint64_t *qbar = &pk_full[ks];
                         if constexpr (FP8) qbar = &sm.st8.q_full;
                         if (FP8 && bi == 0) mbar_arrive_expect_tx(qbar, qbytes);
-                        mbar_arrive_expect_tx(&pk_full[ks], kBlockBytes + (!FP8 && bi == 0 ? qbytes : 0u));
+                        mbar_arrive_expect_tx(&pk_full[ks], kBlockBytes + tile_bytes + (!FP8 && bi == 0 ? qbytes : 0u));
                         if (bi == 0) {
                             tma_load_4d(&sm.q[0], &mq0, 0, h * a.G, 0, b, qbar, pol);
                             tma_load_4d(&sm.q[kQSlab], &mq1, 0, h * a.G, 0, b, qbar, pol);
@@ -371,7 +382,9 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                     if (lane < kPagesPerBlock) {
                         sm.vid[jk % kNMeta][lane] = my_id;
                         copy_page(&mkp, k_slot(ks), my_id, h, &pk_full[ks]);
-                        if constexpr (FP8) copy_scale(a.k_scale, my_id, h, &sm.st8.ksc[jk % kNMeta][lane], &pk_full[ks]);
+                        if constexpr (FP8)
+                            copy_scale(a.k_scale, my_id, h, &sm.st8.ksc[jk % kNMeta][lane], sm.st8.sc64k[ks][lane],
+                                       &pk_full[ks]);
                     }
                     __syncwarp();
                     ++jk;
@@ -581,10 +594,12 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                 if (t & 15) pm[t >> 4] = fmaxf(pm[t >> 4], s[t]);
             float ksc[kPagesPerBlock], vsc[kPagesPerBlock];
             if constexpr (FP8) {
+                // tile scales are already in the converted tiles
+                const bool tiles = a.scale_tile != 0;
 #pragma unroll
                 for (int x = 0; x < kPagesPerBlock; ++x) {
-                    ksc[x] = sm.st8.ksc[j % kNMeta][x];
-                    vsc[x] = sm.st8.vsc[j % kNMeta][x];
+                    ksc[x] = tiles ? 1.f : sm.st8.ksc[j % kNMeta][x];
+                    vsc[x] = tiles ? 1.f : sm.st8.vsc[j % kNMeta][x];
                     if (pm[x] != -CUDART_INF_F) pm[x] *= ksc[x];
                 }
             }
@@ -862,6 +877,8 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                     break;
                 }
                 const uint8_t *src = kconv ? sm.st8.k8[s8] : sm.st8.v8[s8];
+                const float(*sc64)[kTileScales] = kconv ? sm.st8.sc64k[s8] : sm.st8.sc64v[s8];
+                const bool tiles = a.scale_tile != 0;
                 const float *scl = kconv ? sm.st8.ksc[j % kNMeta] : sm.st8.vsc[j % kNMeta];
                 uint8_t *tile = kconv ? sm.kbuf[tb] : sm.vbuf[tb];
                 if (lane < kPagesPerBlock && !(scl[lane] >= 0.f && scl[lane] <= kMaxScale8))
@@ -881,7 +898,8 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                         *qp = v;
                     }
                 }
-                const int t_end = kconv ? kNB : md.L + a.n_q - md.pos0;  // V rows from t_end on are zeroed
+                const int t_valid = md.L + a.n_q - md.pos0;  // rows of the block that hold tokens
+                const int t_end = kconv ? kNB : t_valid;     // V rows from t_end on are zeroed
                 // item i: row i / 8, 16 columns 16 (i % 8) ..; four items in flight per thread
                 constexpr int kItems = kNB * 8, kPer = (kItems + NCT - 1) / NCT;
 #pragma unroll 1
@@ -907,6 +925,22 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                         hi.y = e4m3x2_to_f16x2(e[u].z >> 16);
                         hi.z = e4m3x2_to_f16x2(e[u].w & 0xffffu);
                         hi.w = e4m3x2_to_f16x2(e[u].w >> 16);
+                        if (tiles && row < t_valid) {
+                            // this group's 64-element tile: (page, slot, half) of the block;
+                            // rows past the last token keep unscaled bytes (their scales
+                            // need not be set: K columns there are masked, V rows zeroed)
+                            const float tsc = sc64[row >> 4][(row & 15) * 2 + (g >> 2)];
+                            if (!(tsc >= 0.f && tsc <= kMaxScale8)) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                            const uint32_t t2 = pack_f16x2(tsc, tsc);
+                            lo.x = mul_f16x2(lo.x, t2);
+                            lo.y = mul_f16x2(lo.y, t2);
+                            lo.z = mul_f16x2(lo.z, t2);
+                            lo.w = mul_f16x2(lo.w, t2);
+                            hi.x = mul_f16x2(hi.x, t2);
+                            hi.y = mul_f16x2(hi.y, t2);
+                            hi.z = mul_f16x2(hi.z, t2);
+                            hi.w = mul_f16x2(hi.w, t2);
+                        }
                         const int r8 = row & 7, c0 = (g & 3) * 2;
                         uint8_t *dst = tile + (row >> 3) * 2048 + (g >> 2) * 1024 + r8 * 128;
                         *reinterpret_cast<uint4 *>(dst + ((c0 ^ r8) << 4)) = lo;

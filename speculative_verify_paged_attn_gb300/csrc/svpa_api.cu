@@ -73,6 +73,9 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     if (p->variant == 2 && p->head_dim != 128) return SVPA_ERR_UNSUPPORTED;
     if (p->head_dim != 64 && p->head_dim != 128) return SVPA_ERR_UNSUPPORTED;
     if (p->kv_dtype == SVPA_KV_FP8_E4M3 && p->head_dim != 128) return SVPA_ERR_UNSUPPORTED;
+    if (p->scale_tile != 0 && p->scale_tile != 64) return SVPA_ERR_INVALID_ARG;
+    // tile scales are applied by the tcgen05 kernel's converter warps only
+    if (p->scale_tile == 64 && (p->kv_dtype != SVPA_KV_FP8_E4M3 || p->variant == 1)) return SVPA_ERR_UNSUPPORTED;
     const int G = p->num_q_heads / p->num_kv_heads;
     const long long M = (long long)G * p->n_q;
     if (M > kMaxRows) return SVPA_ERR_UNSUPPORTED;
@@ -81,8 +84,9 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     const int eb = p->kv_dtype == SVPA_KV_FP8_E4M3 ? 1 : 2;
     // kernel variant and its resident grid (the persistent CTAs); the
     // tcgen05 kernel takes FP8 pages for up to 64 query rows per kv head
-    if (p->variant == 2 && eb == 1 && M > 64) return SVPA_ERR_UNSUPPORTED;
-    pl->use_tc = p->variant == 2 || (p->variant == 0 && D == 128 && M > 16 && (eb == 2 || M <= 64));
+    if ((p->variant == 2 || p->scale_tile == 64) && eb == 1 && M > 64) return SVPA_ERR_UNSUPPORTED;
+    pl->use_tc = p->variant == 2 || p->scale_tile == 64 ||
+                 (p->variant == 0 && D == 128 && M > 16 && (eb == 2 || M <= 64));
     pl->grid_slots = sm_count();
     if (!pl->use_tc) {
         AttnLaunch lp;
@@ -181,6 +185,7 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
     if (!q || !k_pool || !v_pool || !block_table || !context_lens || !out || !error_flag)
         return SVPA_ERR_INVALID_ARG;
     if (fp8 && (!k_scale || !v_scale)) return SVPA_ERR_INVALID_ARG;
+    if (p->scale_tile == 64 && (!aligned16(k_scale) || !aligned16(v_scale))) return SVPA_ERR_INVALID_ARG;
     if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(q) || !aligned16(out)) return SVPA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < pl.bytes || !aligned16(workspace)) return SVPA_ERR_WORKSPACE;
     if (ancestor_mask) {
@@ -297,6 +302,7 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
     a.split_pages = pl.split_pages;
     a.max_splits = pl.max_splits;
     a.scale_log2 = p->sm_scale * 1.4426950408889634f;
+    a.scale_tile = p->scale_tile;
     for (int j = 0; j < p->n_q; ++j)
         a.anc[j] = ancestor_mask ? ancestor_mask[j] : ((j == 63) ? ~0ull : ((1ull << (j + 1)) - 1ull));
     a.total_units = p->batch * p->num_kv_heads * pl.max_splits;
@@ -436,7 +442,7 @@ svpa_status svpa_block_table_commit(int32_t batch, int32_t n_q, int32_t block_si
 
 svpa_status svpa_kv_append(int32_t batch, int32_t n_new, int32_t num_kv_heads, int32_t head_dim,
                            int32_t block_size, int32_t max_blocks_per_seq, int32_t num_blocks, int32_t kv_dtype,
-                           const void *new_k, const void *new_v, int32_t *block_table,
+                           int32_t scale_tile, const void *new_k, const void *new_v, int32_t *block_table,
                            const int32_t *context_lens, int32_t *refcount, int32_t *free_stack,
                            int32_t *free_top, void *k_pool, void *v_pool, float *k_scale, float *v_scale,
                            int32_t *error_flag, void *stream) {
@@ -446,6 +452,7 @@ svpa_status svpa_kv_append(int32_t batch, int32_t n_new, int32_t num_kv_heads, i
         return SVPA_ERR_INVALID_ARG;
     const bool fp8 = kv_dtype == SVPA_KV_FP8_E4M3;
     if (fp8 ? (head_dim % 16 != 0 || head_dim > 256) : head_dim > 1024) return SVPA_ERR_INVALID_ARG;
+    if (scale_tile != 0 && (scale_tile != 64 || !fp8 || head_dim % 64 != 0)) return SVPA_ERR_INVALID_ARG;
     if (batch == 0) return SVPA_OK;
     if (!new_k || !new_v || !block_table || !context_lens || !refcount || !free_stack || !free_top || !k_pool ||
         !v_pool || !error_flag || (fp8 && (!k_scale || !v_scale)))
@@ -467,6 +474,8 @@ svpa_status svpa_kv_append(int32_t batch, int32_t n_new, int32_t num_kv_heads, i
     a.v_scale = v_scale;
     a.err = error_flag;
     a.page_bytes = (size_t)num_kv_heads * kBlockSize * head_dim * (fp8 ? 1 : 2);
+    a.scales_per_block = scale_tile ? num_kv_heads * kBlockSize * (head_dim / 64) : num_kv_heads;
+    a.scale_tile = scale_tile;
     a.B = batch;
     a.n_new = n_new;
     a.Hkv = num_kv_heads;

@@ -59,6 +59,7 @@ struct AttnArgs {
     int32_t *err;
     int32_t B, n_q, Hq, Hkv, G, M;
     int32_t max_blocks, num_blocks, split_pages, max_splits, n_stages, total_units;
+    int32_t scale_tile;   // FP8 scales: 0 per (page, kv head), 64 per 64-element tile
     float scale_log2;     // sm_scale * log2(e)
     unsigned long long anc[kMaxNq];  // visibility of speculative slots per query
 };
@@ -152,7 +153,8 @@ struct AppendArgs {
     float *v_scale;
     int32_t *err;
     size_t page_bytes;      // one block, all kv heads
-    int32_t B, n_new, Hkv, D, max_blocks, num_blocks, fp8;
+    int32_t scales_per_block;  // FP8: Hkv (per page) or Hkv * 16 * D / 64 (per 64-element tile)
+    int32_t B, n_new, Hkv, D, max_blocks, num_blocks, fp8, scale_tile;
 };
 cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream);
 

@@ -43,7 +43,7 @@ class AttnParams(ctypes.Structure):
                 ("block_size", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
                 ("sm_scale", ctypes.c_float), ("split_pages", ctypes.c_int32),
-                ("variant", ctypes.c_int32)]
+                ("variant", ctypes.c_int32), ("scale_tile", ctypes.c_int32)]
 
 
 _lib = None
@@ -67,7 +67,7 @@ def load(path: str = LIB_PATH):
     L.svpa_spec_accept_tree.argtypes = [I, I, I] + [P] * 11 + [U, P, P]
     L.svpa_block_table_commit.argtypes = [I] * 5 + [P] * 7 + [I, P, P, I, I, I, P, P]
     L.svpa_paged_verify_attn_noalloc.argtypes = [ctypes.POINTER(AttnParams)] + [P] * 12
-    L.svpa_kv_append.argtypes = [I] * 8 + [P] * 13
+    L.svpa_kv_append.argtypes = [I] * 9 + [P] * 13
     L.svpa_gamma_update.argtypes = [I, I] + [P] * 6 + [ctypes.c_float, ctypes.c_float, P, P]
     L.svpa_check_error.argtypes = [P, P]
     L.svpa_status_string.argtypes = [I]
@@ -99,11 +99,12 @@ VARIANT_AUTO, VARIANT_MMA, VARIANT_TCGEN05 = 0, 1, 2
 
 
 def attn_params(batch, n_q, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_blocks,
-                kv_fp8=False, sm_scale=None, split_pages=0, block_size=16, variant=0) -> AttnParams:
+                kv_fp8=False, sm_scale=None, split_pages=0, block_size=16, variant=0,
+                scale_tile=0) -> AttnParams:
     return AttnParams(batch, n_q, num_q_heads, num_kv_heads, head_dim, block_size,
                       max_blocks_per_seq, num_blocks, SVPA_KV_FP8_E4M3 if kv_fp8 else SVPA_KV_BF16,
                       1.0 / math.sqrt(head_dim) if sm_scale is None else sm_scale, split_pages,
-                      variant)
+                      variant, scale_tile)
 
 
 def attn_workspace_size(params: AttnParams) -> int:
@@ -210,7 +211,7 @@ def block_table_commit(n_q, block_table, context_lens, accepted_len, refcount, f
 
 
 def kv_append(new_k, new_v, block_table, context_lens, refcount, free_stack, free_top, k_pool, v_pool,
-              *, error_flag, k_scale=None, v_scale=None, stream=None, check=True) -> int:
+              *, error_flag, k_scale=None, v_scale=None, scale_tile=0, stream=None, check=True) -> int:
     """svpa_kv_append: write new_k/new_v [B, n_new, Hkv, D] (bf16) at positions
     context_lens[b] .. + n_new - 1, allocating and cloning pages as needed; the
     pools are bf16 or float8_e4m3fn/uint8 [num_blocks, Hkv, 16, D]."""
@@ -218,7 +219,7 @@ def kv_append(new_k, new_v, block_table, context_lens, refcount, free_stack, fre
     fp8 = k_pool.element_size() == 1
     st = load().svpa_kv_append(
         B, n_new, Hkv, D, 16, block_table.shape[1], k_pool.shape[0],
-        SVPA_KV_FP8_E4M3 if fp8 else SVPA_KV_BF16, _p(new_k), _p(new_v), _p(block_table),
+        SVPA_KV_FP8_E4M3 if fp8 else SVPA_KV_BF16, scale_tile, _p(new_k), _p(new_v), _p(block_table),
         _p(context_lens), _p(refcount), _p(free_stack), _p(free_top), _p(k_pool), _p(v_pool),
         _p(k_scale), _p(v_scale), _p(error_flag), _stream(stream))
     if check:

@@ -112,12 +112,16 @@ WORKLOADS = {
     "fp8": Workload("fp8", batch=16, gamma=5, num_q_heads=64, num_kv_heads=8, head_dim=128,
                     ctx_lo=32768, ctx_hi=32768, vocab=128256, sigma_target=3.0, sigma_draft=0.5,
                     kv_fp8=True),
+    # the FP8 workload with one scale per 64-element tile of a row
+    "fp8_t64": Workload("fp8_t64", batch=16, gamma=5, num_q_heads=64, num_kv_heads=8, head_dim=128,
+                        ctx_lo=32768, ctx_hi=32768, vocab=128256, sigma_target=3.0, sigma_draft=0.5,
+                        kv_fp8=True, scale_tile=64),
     "tree": Workload("tree", batch=128, gamma=3, num_q_heads=32, num_kv_heads=8, head_dim=128,
                      ctx_lo=1024, ctx_hi=8192, vocab=32000, sigma_target=3.0, sigma_draft=0.7,
                      tree_branching=(4, 2, 2), shared_prefix=800),
 }
 
-SEEDS = {"tiny": 1000, "7b": 1001, "70b": 1002, "fp8": 1003, "tree": 1004}
+SEEDS = {"tiny": 1000, "7b": 1001, "70b": 1002, "fp8": 1003, "tree": 1004, "fp8_t64": 1005}
 
 
 def _gen(seed: int, device) -> torch.Generator:

@@ -42,7 +42,7 @@ def run_attention(inp: W.AttnInputs, split_pages=0, with_lse=True, variant=0):
     B, n_q, Hq, D = d.q.shape
     p = svpa.attn_params(B, n_q, Hq, wl.num_kv_heads, D, d.block_table.shape[1], d.num_blocks,
                          kv_fp8=wl.kv_fp8, sm_scale=wl.sm_scale, split_pages=split_pages,
-                         variant=variant)
+                         variant=variant, scale_tile=wl.scale_tile)
     ws = torch.zeros(svpa.attn_workspace_size(p), dtype=torch.uint8, device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     out = torch.full((B, n_q, Hq, D), float("nan"), dtype=torch.bfloat16, device=DEV)
@@ -67,7 +67,7 @@ def run_oracle_attention(inp: W.AttnInputs):
     return oracle.paged_verify_attn(c.q, c.k_pool, c.v_pool, c.block_table, c.context_lens,
                                     num_kv_heads=wl.num_kv_heads, sm_scale=wl.sm_scale,
                                     kv_fp8=wl.kv_fp8, k_scale=c.k_scale, v_scale=c.v_scale,
-                                    ancestor_mask=am)
+                                    ancestor_mask=am, scale_tile=wl.scale_tile)
 
 
 def rel_l2(a, b):

@@ -59,6 +59,16 @@ def test_workspace_size_and_validation(lib):
         svpa.attn_workspace_size(svpa.attn_params(2, 9, 64, 8, 128, 8, 16, kv_fp8=True, variant=2))
     assert e.value.status == 2
     assert svpa.attn_workspace_size(svpa.attn_params(2, 8, 64, 8, 128, 8, 16, kv_fp8=True, variant=2)) > 0
+    # 64-element FP8 tile scales run on the tcgen05 kernel only
+    tile = dict(kv_fp8=True, scale_tile=64)
+    assert svpa.attn_kernel(svpa.attn_params(16, 6, 64, 8, 128, 2049, 100000, **tile)) == 2
+    for bad, code in [(dict(variant=1), 2), (dict(n_q=9), 2), (dict(kv_fp8=False), 2), (dict(scale_tile=32), 1)]:
+        kw = dict(kv_fp8=True, scale_tile=64)
+        kw.update(bad)
+        n_q = kw.pop("n_q", 6)
+        with pytest.raises(svpa.SvpaError) as e:
+            svpa.attn_workspace_size(svpa.attn_params(2, n_q, 64, 8, 128, 8, 16, **kw))
+        assert e.value.status == code, bad
     # GQA rows per CTA beyond 128 are not supported
     with pytest.raises(svpa.SvpaError) as e:
         svpa.attn_workspace_size(svpa.attn_params(1, 17, 64, 8, 128, 8, 16, split_pages=4))
@@ -78,22 +88,25 @@ def test_null_pointers_rejected_before_launch(lib):
     assert st == 1
     # K/V append: sizes checked first, then pointers, then alignment
     nz = ctypes.c_void_p(16)  # never dereferenced: validation returns before any launch
-    base = [2, 5, 4, 64, 16, 8, 16, 0]
+    base = [2, 5, 4, 64, 16, 8, 16, 0, 0]
     assert lib.svpa_kv_append(*base, *([None] * 13)) == 1
-    for bad in [dict(n=0), dict(n=4097), dict(d=60), dict(bs=32), dict(dt=2), dict(h=0)]:
+    for bad in [dict(n=0), dict(n=4097), dict(d=60), dict(bs=32), dict(dt=2), dict(h=0), dict(tile=32)]:
         a = list(base)
-        a[1], a[3], a[4], a[7], a[2] = (bad.get("n", 5), bad.get("d", 64), bad.get("bs", 16),
-                                        bad.get("dt", 0), bad.get("h", 4))
+        a[1], a[3], a[4], a[7], a[2], a[8] = (bad.get("n", 5), bad.get("d", 64), bad.get("bs", 16),
+                                              bad.get("dt", 0), bad.get("h", 4), bad.get("tile", 0))
         assert lib.svpa_kv_append(*a, *([nz] * 13)) == 1, bad
     # FP8 tiles: head_dim a multiple of 16, at most 256
     for d in (72, 272):
-        assert lib.svpa_kv_append(2, 5, 4, d, 16, 8, 16, 1, *([nz] * 13)) == 1, d
+        assert lib.svpa_kv_append(2, 5, 4, d, 16, 8, 16, 1, 0, *([nz] * 13)) == 1, d
+    # 64-element tile scales: FP8 pools with head_dim a multiple of 64 only
+    assert lib.svpa_kv_append(2, 5, 4, 64, 16, 8, 16, 0, 64, *([nz] * 13)) == 1
+    assert lib.svpa_kv_append(2, 5, 4, 80, 16, 8, 16, 1, 64, *([nz] * 13)) == 1
     # FP8 pools need both scale arrays
-    assert lib.svpa_kv_append(2, 5, 4, 64, 16, 8, 16, 1, *([nz] * 9), None, None, nz, None) == 1
+    assert lib.svpa_kv_append(2, 5, 4, 64, 16, 8, 16, 1, 0, *([nz] * 9), None, None, nz, None) == 1
     # a pool that is not 16-byte aligned
     odd = ctypes.c_void_p(24)
     assert lib.svpa_kv_append(*base, nz, nz, nz, nz, nz, nz, nz, odd, nz, None, None, nz, None) == 1
-    assert lib.svpa_kv_append(0, 5, 4, 64, 16, 8, 16, 0, *([None] * 13)) == 0
+    assert lib.svpa_kv_append(0, 5, 4, 64, 16, 8, 16, 0, 0, *([None] * 13)) == 0
     # adaptive draft length: sizes, decay and ratio checked before any launch
     F = ctypes.c_float
     for args in [(0, 4, F(0.9), F(0.0)), (2, 0, F(0.9), F(0.0)), (2, 64, F(0.9), F(0.0)),

@@ -46,7 +46,7 @@ def run_gpu(inp, free_top=None, block_table=None, pools_on_device=False):
     vs = inp.v_scale.to(DEV).clone() if fp8 else None
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     svpa.kv_append(inp.new_k.to(DEV), inp.new_v.to(DEV), bt, cl, rc, fs, ft, kp, vp, error_flag=err,
-                   k_scale=ks, v_scale=vs)
+                   k_scale=ks, v_scale=vs, scale_tile=inp.wl.scale_tile)
     st = svpa.check_error(err)
     return st, dict(block_table=bt.cpu().numpy(), refcount=rc.cpu().numpy(), free_stack=fs.cpu().numpy(),
                     free_top=int(ft.item()),
@@ -60,7 +60,7 @@ def run_oracle(inp):
     return oracle.kv_append(c(inp.new_k), c(inp.new_v), inp.block_table.cpu().numpy(),
                             inp.context_lens.cpu().numpy(), inp.refcount.cpu().numpy(),
                             inp.free_stack.cpu().numpy(), inp.free_top, c(inp.k_pool), c(inp.v_pool),
-                            c(inp.k_scale), c(inp.v_scale))
+                            c(inp.k_scale), c(inp.v_scale), scale_tile=inp.wl.scale_tile)
 
 
 def canon(bt):
@@ -104,8 +104,13 @@ def compare(g, r, inp):
             for name in ("k_pool", "v_pool"):
                 assert np.array_equal(g[name][x, :, :upto], r[name][y, :, :upto]), (b, i, name)
             if fp8:
+                # tile scales of slots past the last row are never written
+                n_used = int(min(BS, end[b] - i * BS))
                 for name in ("k_scale", "v_scale"):
-                    assert np.array_equal(g[name][x], r[name][y]), (b, i, name)
+                    gs, rs = g[name][x], r[name][y]
+                    if inp.wl.scale_tile:
+                        gs, rs = gs[:, :n_used], rs[:, :n_used]
+                    assert np.array_equal(gs, rs), (b, i, name)
 
 
 SMALL = {
@@ -117,6 +122,11 @@ SMALL = {
     "fp8_rescale_cow": (W.WORKLOADS["fp8"], (0, 4, 9, 12, 300, 1000), 35, 6),
     "bf16_tree_cow": (W.WORKLOADS["tree"], (0, 3, 5, 700), 803, 29),
     "fp8_single_row": (W.WORKLOADS["fp8"], (5, 16, 95), 0, 1),
+    # one scale per 64-element tile of a row
+    "fp8_t64_cow": (W.WORKLOADS["fp8_t64"], (0, 4, 9, 12, 300, 1000), 35, 6),
+    "fp8_t64_edges": (W.WORKLOADS["fp8_t64"].scaled(num_q_heads=4, num_kv_heads=2, head_dim=256),
+                      (0, 1, 15, 16, 17, 31), 0, 29),
+    "fp8_t64_d64": (W.WORKLOADS["tiny"].scaled(kv_fp8=True, scale_tile=64), (2, 50, 3, 12), 19, 7),
     # widest FP8 tile (16 x 256 bytes) and a copy-on-write at D = 256
     "fp8_d256_cow": (W.WORKLOADS["fp8"].scaled(num_q_heads=4, num_kv_heads=2, head_dim=256),
                      (1, 3, 16, 40), 21, 20),
@@ -204,7 +214,8 @@ def sequence_oracle(inp, b, old_k, old_v, old_ks, old_vs):
     shape = (nb,) + tuple(inp.k_pool.shape[1:])
     dt = np.uint8 if fp8 else np.uint16
     kp, vp = np.zeros(shape, dt), np.zeros(shape, dt)
-    ks, vs = np.ones((nb, shape[1]), np.float32), np.ones((nb, shape[1]), np.float32)
+    sshape = (nb,) + tuple(inp.k_scale.shape[1:]) if fp8 else (nb, shape[1])
+    ks, vs = np.ones(sshape, np.float32), np.ones(sshape, np.float32)
     bt = np.full((1, i1 + 1), -1, np.int32)
     rc = np.zeros(nb, np.int32)
     for j in range(n):
@@ -218,11 +229,11 @@ def sequence_oracle(inp, b, old_k, old_v, old_ks, old_vs):
     fs = np.concatenate([fs, np.full(nb - fs.size, -1, np.int32)])
     r = oracle.kv_append(inp.new_k[b:b + 1].cpu(), inp.new_v[b:b + 1].cpu(), bt,
                          np.array([L], np.int32), rc, fs, nb - n, kp, vp,
-                         ks if fp8 else None, vs if fp8 else None)
+                         ks if fp8 else None, vs if fp8 else None, scale_tile=inp.wl.scale_tile)
     return r, i0, i1
 
 
-@pytest.mark.parametrize("name", ["7b", "70b", "fp8", "tree"])
+@pytest.mark.parametrize("name", ["7b", "70b", "fp8", "tree", "fp8_t64"])
 def test_append_full_size_workloads(name):
     """The bench's append state (full batch, n_new = n_q, contexts as drawn);
     every sequence's touched pages against the oracle on that sequence."""
@@ -261,8 +272,12 @@ def test_append_full_size_workloads(name):
             for nm in ("k_pool", "v_pool"):
                 assert np.array_equal(raw(g[nm][x])[:, :upto], r[nm][y, :, :upto]), (b, i, nm)
             if fp8:
+                n_used = int(min(BS, end - i * BS))
                 for nm in ("k_scale", "v_scale"):
-                    assert np.array_equal(g[nm][x], r[nm][y]), (b, i, nm)
+                    gs, rs = g[nm][x], r[nm][y]
+                    if inp.wl.scale_tile:  # tile scales past the last row are never written
+                        gs, rs = gs[:, :n_used], rs[:, :n_used]
+                    assert np.array_equal(gs, rs), (b, i, nm)
         # pages before the append are untouched
         for i in range(0, int(i0)):
             assert g["block_table"][b, i] == bt0[b, i]

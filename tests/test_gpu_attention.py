@@ -29,6 +29,10 @@ CASES = [
     ("7b_small_auto", small("7b", batch=5, ctx_lo=1, ctx_hi=700), 0),
     ("70b_small", small("70b", batch=3, ctx_lo=200, ctx_hi=1500), 32),
     ("fp8_small", small("fp8", batch=2, ctx_lo=300, ctx_hi=1200), 16),
+    # one FP8 scale per 64-element tile of a row (tcgen05 kernel)
+    ("fp8_t64_small", small("fp8_t64", batch=3, ctx_lo=1, ctx_hi=900), 16),
+    ("fp8_t64_nosplit", small("fp8_t64", batch=2, ctx_lo=100, ctx_hi=300), 1024),
+    ("fp8_t64_g4", small("fp8_t64", batch=3, ctx_lo=40, ctx_hi=700, num_q_heads=32, num_kv_heads=8), 8),
     ("tree_small", small("tree", batch=4, ctx_lo=1, ctx_hi=400, shared_prefix=32), 16),
     ("tree_prefix800", small("tree", batch=3, ctx_lo=1024, ctx_hi=1300), 32),
     ("d64_gqa", small("tiny", num_q_heads=8, num_kv_heads=2, fixed_contexts=None, ctx_lo=0, ctx_hi=300,
@@ -106,7 +110,7 @@ def test_bad_block_reported_not_faulted():
     assert st == 5  # SVPA_ERR_BAD_BLOCK
 
 
-FULL = ["7b", "70b", "fp8", "tree"]
+FULL = ["7b", "70b", "fp8", "tree", "fp8_t64"]
 
 
 @pytest.mark.parametrize("name", FULL)
