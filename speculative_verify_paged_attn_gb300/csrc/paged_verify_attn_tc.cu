@@ -35,6 +35,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <type_traits>
 
 #include "svpa_device.cuh"
@@ -100,13 +101,18 @@ struct BlockMeta {
     int32_t pad[3];
 };
 
+// one scale per 64-element tile of each row of a staged FP8 block (the
+// tile-scale instantiation only), one slot per staging slot
+struct alignas(16) TileScaleRing {
+    float k[TcCfg<true>::kNK8][kPagesPerBlock][kTileScales];
+    float v[TcCfg<true>::kNV8][kPagesPerBlock][kTileScales];
+};
+struct NoTileScales {};
+
 template <bool FP8>
 struct Stage8 {  // FP8 staging rings
     uint8_t k8[TcCfg<FP8>::kNK8][kTile8];
     uint8_t v8[TcCfg<FP8>::kNV8][kTile8];
-    // one scale per 64-element tile of each row of a staged block (tile-scale mode)
-    float sc64k[TcCfg<FP8>::kNK8][kPagesPerBlock][kTileScales];
-    float sc64v[TcCfg<FP8>::kNV8][kPagesPerBlock][kTileScales];
     float ksc[kNMeta][kPagesPerBlock];  // page scales of the blocks in flight
     float vsc[kNMeta][kPagesPerBlock];
     uint64_t k8_full[TcCfg<FP8>::kNK8], k8_empty[TcCfg<FP8>::kNK8];
@@ -115,7 +121,7 @@ struct Stage8 {  // FP8 staging rings
 };
 struct NoStage8 {};
 
-template <bool FP8>
+template <bool FP8, bool TILES>
 struct Smem {
     using C = TcCfg<FP8>;
     uint8_t q[C::kQBuf];                 // 1024-aligned (one unit's queries)
@@ -135,11 +141,16 @@ struct Smem {
     int32_t ep_b, ep_h, ep_split, ep_nsplit, ep_end;
     uint32_t tmem_base;
     int32_t last;
+    // last, so that the other members keep their offsets without tile scales
+    typename std::conditional<TILES, TileScaleRing, NoTileScales>::type t64;
 };
 
 // fits the 227 KB a CTA may opt into, with room to align the base to 1 KB
-static_assert(sizeof(Smem<false>) + 1024 <= 232448, "pva_tc_kernel shared memory");
-static_assert(sizeof(Smem<true>) + 1024 <= 232448, "pva_tc_kernel shared memory");
+static_assert(sizeof(Smem<false, false>) + 1024 <= 232448, "pva_tc_kernel shared memory");
+static_assert(sizeof(Smem<true, false>) + 1024 <= 232448, "pva_tc_kernel shared memory");
+static_assert(sizeof(Smem<true, true>) + 1024 <= 232448, "pva_tc_kernel shared memory");
+using SmemFp8Tiles = Smem<true, true>;
+static_assert(offsetof(SmemFp8Tiles, t64) % 16 == 0, "bulk copies land on 16-byte boundaries");
 
 // f16 MMA instruction descriptor (FP8 pages): as umma_idesc_bf16 with both
 // operand formats F16.
@@ -160,7 +171,9 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
 
 __device__ __forceinline__ uint32_t par_of(int idx) { return (uint32_t)((idx >> 1) & 1); }
 
-template <bool FP8>
+// TILES (FP8 only): one scale per 64-element tile of a row, applied by the
+// converters, instead of one per (page, kv head) applied in the softmax
+template <bool FP8, bool TILES>
 __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
     pva_tc_kernel(const __grid_constant__ CUtensorMap mkp, const __grid_constant__ CUtensorMap mvp,
                   const __grid_constant__ CUtensorMap mq0, const __grid_constant__ CUtensorMap mq1,
@@ -168,7 +181,8 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     using C = TcCfg<FP8>;
     constexpr int kNK = C::kNK, kNV = C::kNV, kQSlab = C::kQSlab, kQBuf = C::kQBuf;
-    Smem<FP8> &sm = *reinterpret_cast<Smem<FP8> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Smem<FP8, TILES> &sm =
+        *reinterpret_cast<Smem<FP8, TILES> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -255,18 +269,21 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
         };
         // FP8: the page's scale by cp.async, counted on the same staging
         // barrier (a missing page takes the block's first page's scale: its
-        // bytes are zero); with tile scales also the page's 32 tile scales
-        // (128 bytes) by a bulk copy counted in the barrier's bytes, and the
-        // 4-byte copy takes the page's first tile scale
-        auto copy_scale = [&](const float *scales, int id, int hh, float *dst, float *dst64, uint64_t *bar) {
+        // bytes are zero)
+        auto copy_scale = [&](const float *scales, int id, int hh, float *dst, uint64_t *bar) {
             const int id0 = __shfl_sync(0x000000ffu, id, 0);
             const int sid = (id >= 0 && id < a.num_blocks) ? id : id0;
-            const size_t page = (size_t)sid * a.Hkv + hh;
-            cp_async_4(dst, scales + (a.scale_tile ? page * kTileScales : page));
+            cp_async_4(dst, scales + (size_t)sid * a.Hkv + hh);
             cp_async_mbar_arrive_noinc(bar);
-            if (a.scale_tile) bulk_copy_g2s(dst64, scales + page * kTileScales, kTileScales * 4, bar);
         };
-        const uint32_t tile_bytes = FP8 && a.scale_tile ? kPagesPerBlock * kTileScales * 4 : 0u;
+        // tile scales: the page's 32 tile scales (128 bytes) by a bulk copy,
+        // counted in the staging barrier's bytes, into staging slot `slot`
+        auto copy_tile_scales = [&](const float *scales, int id, int hh, float *dst, uint64_t *bar) {
+            const int id0 = __shfl_sync(0x000000ffu, id, 0);
+            const int sid = (id >= 0 && id < a.num_blocks) ? id : id0;
+            bulk_copy_g2s(dst, scales + ((size_t)sid * a.Hkv + hh) * kTileScales, kTileScales * 4, bar);
+        };
+        constexpr uint32_t tile_bytes = TILES ? kPagesPerBlock * kTileScales * 4 : 0u;
         auto k_slot = [&](int s_) -> uint8_t * {
             if constexpr (FP8) return sm.st8.k8[s_]; else return sm.kbuf[s_];
         };
@@ -286,9 +303,8 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             if (lane < kPagesPerBlock) {
                 const int id = sm.vid[jv % kNMeta][lane], hh = sm.meta[jv % kNMeta].h;
                 copy_page(&mvp, v_slot(vs), id, hh, &pv_full[vs]);
-                if constexpr (FP8)
-                    copy_scale(a.v_scale, id, hh, &sm.st8.vsc[jv % kNMeta][lane], sm.st8.sc64v[vs][lane],
-                               &pv_full[vs]);
+                if constexpr (FP8) copy_scale(a.v_scale, id, hh, &sm.st8.vsc[jv % kNMeta][lane], &pv_full[vs]);
+                if constexpr (TILES) copy_tile_scales(a.v_scale, id, hh, sm.t64.v[vs][lane], &pv_full[vs]);
             }
             __syncwarp();
             ++jv;
@@ -382,9 +398,9 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                     if (lane < kPagesPerBlock) {
                         sm.vid[jk % kNMeta][lane] = my_id;
                         copy_page(&mkp, k_slot(ks), my_id, h, &pk_full[ks]);
-                        if constexpr (FP8)
-                            copy_scale(a.k_scale, my_id, h, &sm.st8.ksc[jk % kNMeta][lane], sm.st8.sc64k[ks][lane],
-                                       &pk_full[ks]);
+                        if constexpr (FP8) copy_scale(a.k_scale, my_id, h, &sm.st8.ksc[jk % kNMeta][lane], &pk_full[ks]);
+                        if constexpr (TILES)
+                            copy_tile_scales(a.k_scale, my_id, h, sm.t64.k[ks][lane], &pk_full[ks]);
                     }
                     __syncwarp();
                     ++jk;
@@ -594,12 +610,11 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                 if (t & 15) pm[t >> 4] = fmaxf(pm[t >> 4], s[t]);
             float ksc[kPagesPerBlock], vsc[kPagesPerBlock];
             if constexpr (FP8) {
-                // tile scales are already in the converted tiles
-                const bool tiles = a.scale_tile != 0;
 #pragma unroll
                 for (int x = 0; x < kPagesPerBlock; ++x) {
-                    ksc[x] = tiles ? 1.f : sm.st8.ksc[j % kNMeta][x];
-                    vsc[x] = tiles ? 1.f : sm.st8.vsc[j % kNMeta][x];
+                    // (tile scales are already in the converted tiles)
+                    ksc[x] = TILES ? 1.f : sm.st8.ksc[j % kNMeta][x];
+                    vsc[x] = TILES ? 1.f : sm.st8.vsc[j % kNMeta][x];
                     if (pm[x] != -CUDART_INF_F) pm[x] *= ksc[x];
                 }
             }
@@ -877,8 +892,6 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                     break;
                 }
                 const uint8_t *src = kconv ? sm.st8.k8[s8] : sm.st8.v8[s8];
-                const float(*sc64)[kTileScales] = kconv ? sm.st8.sc64k[s8] : sm.st8.sc64v[s8];
-                const bool tiles = a.scale_tile != 0;
                 const float *scl = kconv ? sm.st8.ksc[j % kNMeta] : sm.st8.vsc[j % kNMeta];
                 uint8_t *tile = kconv ? sm.kbuf[tb] : sm.vbuf[tb];
                 if (lane < kPagesPerBlock && !(scl[lane] >= 0.f && scl[lane] <= kMaxScale8))
@@ -898,8 +911,7 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                         *qp = v;
                     }
                 }
-                const int t_valid = md.L + a.n_q - md.pos0;  // rows of the block that hold tokens
-                const int t_end = kconv ? kNB : t_valid;     // V rows from t_end on are zeroed
+                const int t_end = kconv ? kNB : md.L + a.n_q - md.pos0;  // V rows from t_end on are zeroed
                 // item i: row i / 8, 16 columns 16 (i % 8) ..; four items in flight per thread
                 constexpr int kItems = kNB * 8, kPer = (kItems + NCT - 1) / NCT;
 #pragma unroll 1
@@ -925,11 +937,12 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                         hi.y = e4m3x2_to_f16x2(e[u].z >> 16);
                         hi.z = e4m3x2_to_f16x2(e[u].w & 0xffffu);
                         hi.w = e4m3x2_to_f16x2(e[u].w >> 16);
-                        if (tiles && row < t_valid) {
+                        if constexpr (TILES) {
+                          if (row < md.L + a.n_q - md.pos0) {
                             // this group's 64-element tile: (page, slot, half) of the block;
                             // rows past the last token keep unscaled bytes (their scales
                             // need not be set: K columns there are masked, V rows zeroed)
-                            const float tsc = sc64[row >> 4][(row & 15) * 2 + (g >> 2)];
+                            const float tsc = (kconv ? sm.t64.k[s8] : sm.t64.v[s8])[row >> 4][(row & 15) * 2 + (g >> 2)];
                             if (!(tsc >= 0.f && tsc <= kMaxScale8)) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
                             const uint32_t t2 = pack_f16x2(tsc, tsc);
                             lo.x = mul_f16x2(lo.x, t2);
@@ -940,6 +953,7 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                             hi.y = mul_f16x2(hi.y, t2);
                             hi.z = mul_f16x2(hi.z, t2);
                             hi.w = mul_f16x2(hi.w, t2);
+                          }
                         }
                         const int r8 = row & 7, c0 = (g & 3) * 2;
                         uint8_t *dst = tile + (row >> 3) * 2048 + (g >> 2) * 1024 + r8 * 128;
@@ -966,28 +980,32 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
 
 }  // namespace
 
-size_t attn_tc_smem_bytes() { return std::max(sizeof(Smem<false>), sizeof(Smem<true>)) + 1024; }
+size_t attn_tc_smem_bytes() {
+    return std::max(sizeof(Smem<false, false>), std::max(sizeof(Smem<true, false>), sizeof(Smem<true, true>))) + 1024;
+}
 
 namespace {
-template <bool FP8>
+template <bool FP8, bool TILES>
 cudaError_t launch_tc(const CUtensorMap &mk, const CUtensorMap &mv, const AttnMaps &m, const AttnArgs &a, int grid,
                       cudaStream_t st) {
-    const size_t smem = sizeof(Smem<FP8>) + 1024;
+    const size_t smem = sizeof(Smem<FP8, TILES>) + 1024;
     static DeviceMemo<int> attr_set;  // the shared-memory opt-in, once per device
     int done = 0;
     cudaError_t e = attr_set.get(&done, [&](int *v) {
         *v = 1;
-        return cudaFuncSetAttribute(pva_tc_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        return cudaFuncSetAttribute(pva_tc_kernel<FP8, TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     });
     if (e != cudaSuccess) return e;
-    pva_tc_kernel<FP8><<<grid, TcCfg<FP8>::kThreads, smem, st>>>(mk, mv, m.q[0], m.q[1], a);
+    pva_tc_kernel<FP8, TILES><<<grid, TcCfg<FP8>::kThreads, smem, st>>>(mk, mv, m.q[0], m.q[1], a);
     return cudaGetLastError();
 }
 }  // namespace
 
 // FP8 pages: the E4M3 page maps (one 2 KB box per page); bf16: the 5-D page maps
 cudaError_t launch_paged_verify_attn_tc(const AttnMaps &m, const AttnArgs &a, int grid, bool fp8, cudaStream_t st) {
-    return fp8 ? launch_tc<true>(m.k[0], m.v[0], m, a, grid, st) : launch_tc<false>(m.kpage, m.vpage, m, a, grid, st);
+    if (!fp8) return launch_tc<false, false>(m.kpage, m.vpage, m, a, grid, st);
+    return a.scale_tile ? launch_tc<true, true>(m.k[0], m.v[0], m, a, grid, st)
+                        : launch_tc<true, false>(m.k[0], m.v[0], m, a, grid, st);
 }
 
 }  // namespace svpa
