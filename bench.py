@@ -37,6 +37,7 @@ from speculative_verify_paged_attn_gb300 import svpa  # noqa: E402
 from speculative_verify_paged_attn_gb300 import workloads as W  # noqa: E402
 
 METRIC = "paged verify-attn KV GB/s (% of GB300 HBM peak); spec_accept rows/s"
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 L2_BYTES = 129 * 1024 * 1024
 # the sources that decide an attention kernel's DRAM traffic: its own file,
 # the shared device helpers and the launch planning
@@ -314,6 +315,36 @@ def time_gamma(st: "Step", steps: int, warmup: int, stream) -> float:
     return sum(ms) / len(ms)
 
 
+def percentiles(xs):
+    """(p10, p50, p90) of a list of timings."""
+    a = sorted(xs)
+    pick = lambda q: a[min(len(a) - 1, max(0, int(round(q * (len(a) - 1)))))]
+    return [round(pick(0.1), 5), round(pick(0.5), 5), round(pick(0.9), 5)]
+
+
+def graph_launch_us(fn, launches: int = 100) -> float:
+    """Device time per call of `fn` replayed from one CUDA graph of `launches`
+    calls (no L2 flush between them: the launch-bound view of small calls)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # settle per-device launch facts outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(launches):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b) * 1e3 / launches
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -422,8 +453,8 @@ def config_dict(wl: W.Workload):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="7b", choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="svpa", choices=["svpa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -545,6 +576,22 @@ def main():
     del ap
     # the draft-length controller on this step's accepted lengths
     gam_ms = time_gamma(st, K, args.warmup, stream)
+    # per-launch times from CUDA graphs of 100 launches (launch-bound view)
+    st.reset()
+    graph_attn_us = graph_launch_us(st.attention)
+    graph_samp_us = graph_launch_us(st.sample)
+    torch.cuda.synchronize()
+    assert svpa.check_error(st.err) == 0, "device error in the graph replays"
+    # sampler bytes from each row's outcome: the P row it scanned, and the Q
+    # row too when a draft was rejected, plus the gathered test values
+    kk = st.k.cpu()
+    V = st.smp.p.shape[2]
+    if st.tree:
+        samp_bytes = st.B * V * 4 * 2  # a rejection scans the residual (P and Q rows); bonus: P row
+    else:
+        rej = (kk < wl.gamma).to(torch.int64)
+        samp_bytes = int((V * 4 * (1 + rej)).sum().item()) + st.B * 2 * wl.gamma * 4
+    flops = 4 * wl.head_dim * st.n_q * wl.num_q_heads * int((st.cl0.long() + st.n_q).sum().item())
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -572,6 +619,16 @@ def main():
             "kv_append_gbs": round(app_bytes / (app_ms * 1e-3) / 1e9, 2),
             "gamma_update_us": round(gam_ms * 1e3, 2),
             "kv_bytes_per_step": st.kv_bytes,
+            "kv_bytes_logical_per_step": int((st.cl0.long() + st.n_q).sum().item()) * wl.num_kv_heads
+                                         * wl.head_dim * 2 * (1 if wl.kv_fp8 else 2),
+            "attn_frac_of_nominal": round(st.kv_bytes / (attn_avg * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+            "attn_tflops": round(flops / (attn_avg * 1e-3) / 1e12, 2),
+            "spec_accept_gbs": round(samp_bytes / (sum(samp_ms) / K * 1e-3) / 1e9, 2),
+            "percentiles_p10_p50_p90": {"attn_us": [round(x * 1e3, 2) for x in percentiles(attn_ms)],
+                                        "spec_accept_us": [round(x * 1e3, 2) for x in percentiles(samp_ms)],
+                                        "step_ms": percentiles(step_ms)},
+            "graph_us_per_launch": {"attn": round(graph_attn_us, 2), "spec_accept": round(graph_samp_us, 2),
+                                    "launches": 100, "l2": "not flushed between launches"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": recorded_traffic(args.config, kname),
