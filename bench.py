@@ -141,7 +141,7 @@ class Step:
         self.B, self.n_q = B, n_q
         self.params = svpa.attn_params(B, n_q, Hq, wl.num_kv_heads, D, inp.block_table.shape[1],
                                        inp.num_blocks, kv_fp8=wl.kv_fp8, sm_scale=wl.sm_scale,
-                                       variant=variant)
+                                       variant=variant, scale_tile=wl.scale_tile)
         self.ws = torch.zeros(svpa.attn_workspace_size(self.params), dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.out = torch.empty((B, n_q, Hq, D), dtype=torch.bfloat16, device=dev)
@@ -222,7 +222,7 @@ class Append:
 
     def __init__(self, wl: W.Workload, seed: int, dev: torch.device):
         inp = W.make_append(wl, seed + 17, device=dev)
-        self.inp, self.fp8 = inp, wl.kv_fp8
+        self.inp, self.fp8, self.tile = inp, wl.kv_fp8, wl.scale_tile
         self.kp = inp.k_pool.view(torch.uint8) if self.fp8 else inp.k_pool
         self.vp = inp.v_pool.view(torch.uint8) if self.fp8 else inp.v_pool
         self.bt0, self.rc0, self.fs0 = inp.block_table.clone(), inp.refcount.clone(), inp.free_stack.clone()
@@ -250,7 +250,7 @@ class Append:
         inp = self.inp
         svpa.kv_append(inp.new_k, inp.new_v, inp.block_table, inp.context_lens, inp.refcount,
                        inp.free_stack, self.ft, self.kp, self.vp, error_flag=self.err,
-                       k_scale=inp.k_scale, v_scale=inp.v_scale)
+                       k_scale=inp.k_scale, v_scale=inp.v_scale, scale_tile=self.tile)
 
 
 def time_append(ap: Append, steps: int, warmup: int, stream) -> float:
@@ -395,6 +395,7 @@ def cpu_baseline(wl: W.Workload, seed: int, budget_s: float = 12.0):
         oracle.paged_verify_attn(inp.q[sel], inp.k_pool, inp.v_pool, inp.block_table[sel],
                                  inp.context_lens[sel], num_kv_heads=wl.num_kv_heads,
                                  sm_scale=wl.sm_scale, kv_fp8=wl.kv_fp8, k_scale=inp.k_scale,
+                                 scale_tile=wl.scale_tile,
                                  v_scale=inp.v_scale, ancestor_mask=am)
         if wl.tree_branching:
             oracle.spec_accept_tree(np.array(wl.parent, np.int32), smp.p[sel], smp.q[sel],
