@@ -106,8 +106,6 @@ struct BlockMeta {
 struct alignas(16) TileScaleRing {
     float k[TcCfg<true>::kNK8][kPagesPerBlock][kTileScales];
     float v[TcCfg<true>::kNV8][kPagesPerBlock][kTileScales];
-    // a staged block's scales are ready as f16 pairs (every converter thread of the operand arrives)
-    uint64_t k_ready[TcCfg<true>::kNK8], v_ready[TcCfg<true>::kNV8];
 };
 struct NoTileScales {};
 
@@ -208,10 +206,6 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                 mbar_init(&sm.st8.v8_empty[i], C::kConvWarps);
             }
             mbar_init(&sm.st8.q_full, 1);
-        }
-        if constexpr (TILES) {
-            for (int i = 0; i < C::kNK8; ++i) mbar_init(&sm.t64.k_ready[i], C::kConvWarps * 32);
-            for (int i = 0; i < C::kNV8; ++i) mbar_init(&sm.t64.v_ready[i], C::kConvWarps * 32);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.s_full[i], 1);
@@ -918,23 +912,6 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                     }
                 }
                 const int t_end = kconv ? kNB : md.L + a.n_q - md.pos0;  // V rows from t_end on are zeroed
-                if constexpr (TILES) {
-                    // the block's 256 tile scales, checked and turned into f16 pairs in
-                    // place (scale i belongs to row i / 2 of the block; rows past the
-                    // last token are neither checked nor used)
-                    float *ts = kconv ? &sm.t64.k[s8][0][0] : &sm.t64.v[s8][0][0];
-                    const int t_valid = md.L + a.n_q - md.pos0;
-                    for (int i = ct; i < kPagesPerBlock * kTileScales; i += NCT) {
-                        const float v = ts[i];
-                        if ((i >> 1) < t_valid && !(v >= 0.f && v <= kMaxScale8))
-                            raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
-                        reinterpret_cast<uint32_t *>(ts)[i] = pack_f16x2(v, v);
-                    }
-                    // every converter thread of this operand has written its share
-                    uint64_t *ready = kconv ? &sm.t64.k_ready[s8] : &sm.t64.v_ready[s8];
-                    mbar_arrive(ready);
-                    if (!mbar_wait(ready, (uint32_t)((j / ring) & 1), a.err)) break;
-                }
                 // item i: row i / 8, 16 columns 16 (i % 8) ..; four items in flight per thread
                 constexpr int kItems = kNB * 8, kPer = (kItems + NCT - 1) / NCT;
 #pragma unroll 1
@@ -962,11 +939,12 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                         hi.w = e4m3x2_to_f16x2(e[u].w >> 16);
                         if constexpr (TILES) {
                           if (row < md.L + a.n_q - md.pos0) {
-                            // this group's 64-element tile, (page, slot, half) of the block,
-                            // as the f16 pair prepared above; rows past the last token keep
-                            // unscaled bytes (K columns there are masked, V rows zeroed)
-                            const uint32_t t2 = reinterpret_cast<const uint32_t *>(
-                                kconv ? &sm.t64.k[s8][0][0] : &sm.t64.v[s8][0][0])[row * 2 + (g >> 2)];
+                            // this group's 64-element tile: (page, slot, half) of the block;
+                            // rows past the last token keep unscaled bytes (their scales
+                            // need not be set: K columns there are masked, V rows zeroed)
+                            const float tsc = (kconv ? sm.t64.k[s8] : sm.t64.v[s8])[row >> 4][(row & 15) * 2 + (g >> 2)];
+                            if (!(tsc >= 0.f && tsc <= kMaxScale8)) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                            const uint32_t t2 = pack_f16x2(tsc, tsc);
                             lo.x = mul_f16x2(lo.x, t2);
                             lo.y = mul_f16x2(lo.y, t2);
                             lo.z = mul_f16x2(lo.z, t2);
