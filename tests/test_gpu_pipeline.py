@@ -89,7 +89,15 @@ def test_verification_step_matches_oracle(name):
     smp = W.make_sampler(wl, 77, batch=B)
     got = gpu_step(inp, q, smp, wl)
     ref = oracle_step(inp, q, smp, wl)
-    U.assert_attention_close(got["out"], ref["out"], fp8=wl.kv_fp8, what=f"{name} attention after append")
+    # the appended rows are up to 3x N(0,1), so outputs reach ~8 where bf16's own
+    # rounding is 2^-8 relative: the bound scales with the value (bf16 output
+    # rounding plus the kernel's error), and rel-L2 as in the attention tests
+    if wl.kv_fp8:
+        U.assert_attention_close(got["out"], ref["out"], fp8=True, what=f"{name} attention after append")
+    else:
+        assert np.isfinite(got["out"]).all()
+        assert np.all(np.abs(got["out"] - ref["out"]) <= 2e-2 + 2.0 ** -8 * np.abs(ref["out"]))
+        assert U.rel_l2(got["out"], ref["out"]) <= U.BF16_REL_L2
     assert np.array_equal(got["k"], ref["k"])
     ok = ~(got["near"] | ref["near"])
     assert np.array_equal(got["toks"][ok], ref["toks"][ok])
