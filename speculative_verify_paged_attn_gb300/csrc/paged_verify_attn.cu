@@ -185,7 +185,8 @@ __global__ void __launch_bounds__((MT + 1) * 32, Occ<MT>::MINB)
             u = __shfl_sync(0xffffffffu, u, 0);
             if (u >= a.total_units) break;
             const int bh = u / a.max_splits, split = u - bh * a.max_splits;
-            const int b = bh / a.Hkv, h = bh - b * a.Hkv;
+            const int rb = bh / a.Hkv, h = bh - rb * a.Hkv;
+            const int b = a.order ? __ldg(a.order + rb) : rb;  // longest sequences first
             const int L = __ldg(a.context_lens + b);
             const int npages = (L + a.n_q + kBlockSize - 1) / kBlockSize;
             if (L < 0 || npages > a.max_blocks) {
@@ -642,6 +643,32 @@ cudaError_t launch_d(const AttnMaps &m, const AttnArgs &a, int grid, size_t smem
 }
 
 }  // namespace
+
+namespace {
+
+// Rank of each sequence by decreasing length (ties by index): one CTA, each
+// thread counts the sequences that go before its own (B <= kMaxOrderedSeqs).
+__global__ void __launch_bounds__(1024) seq_order_kernel(const int32_t *context_lens, int B, int32_t *order) {
+    __shared__ int32_t s_len[kMaxOrderedSeqs];
+    for (int i = threadIdx.x; i < B; i += blockDim.x) s_len[i] = context_lens[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < B; i += blockDim.x) {
+        const int li = s_len[i];
+        int rank = 0;
+        for (int j = 0; j < B; ++j) {
+            const int lj = s_len[j];
+            rank += (lj > li) || (lj == li && j < i);
+        }
+        order[rank] = i;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_seq_order(const int32_t *context_lens, int B, int32_t *order, cudaStream_t stream) {
+    seq_order_kernel<<<1, 1024, 0, stream>>>(context_lens, B, order);
+    return cudaGetLastError();
+}
 
 cudaError_t attn_plan_launch(int head_dim, bool fp8, int M, AttnLaunch *out) {
     if (head_dim == 128) return fp8 ? plan_d<128, true>(M, out) : plan_d<128, false>(M, out);

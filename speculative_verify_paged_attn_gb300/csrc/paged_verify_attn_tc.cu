@@ -339,7 +339,8 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             u = __shfl_sync(0xffffffffu, u, 0);
             if (u >= a.total_units) break;
             const int bh = u / a.max_splits, split = u - bh * a.max_splits;
-            const int b = bh / a.Hkv, h = bh - b * a.Hkv;
+            const int rb = bh / a.Hkv, h = bh - rb * a.Hkv;
+            const int b = a.order ? __ldg(a.order + rb) : rb;  // longest sequences first
             const int L = __ldg(a.context_lens + b);
             const int npages = (L + a.n_q + kBlockSize - 1) / kBlockSize;
             if (L < 0 || npages > a.max_blocks) {

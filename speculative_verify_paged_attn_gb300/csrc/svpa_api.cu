@@ -59,7 +59,8 @@ struct AttnPlan {
     int M, split_pages, max_splits;
     bool use_tc;
     int grid_slots;      // resident CTAs of the chosen kernel
-    size_t off_ml, off_acc, bytes;
+    bool ordered;        // units handed out longest sequence first
+    size_t off_order, off_ml, off_acc, bytes;
 };
 
 svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
@@ -117,6 +118,13 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     const size_t units = (size_t)p->batch * p->num_kv_heads;
     // [scheduler counters][tickets][split (max, sum)][split accumulators]
     size_t off = kAlign + align_up(units * sizeof(int32_t));
+    // unsplit units vary most in length: hand out the longest first (a
+    // greedy longest-first order; the draft-tree workload's 1024 unsplit
+    // units on 152 SMs: about 12% above the ideal finish in index order,
+    // about 2% longest first, by a list-scheduling estimate)
+    pl->ordered = pl->max_splits == 1 && p->batch > 1 && p->batch <= kMaxOrderedSeqs;
+    pl->off_order = off;
+    if (pl->ordered) off += align_up((size_t)p->batch * sizeof(int32_t));
     pl->off_ml = off;
     if (pl->max_splits > 1) {
         off += align_up(units * pl->max_splits * M * 2 * sizeof(float));
@@ -288,6 +296,7 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     a.sched = reinterpret_cast<int32_t *>(ws);
     a.tickets = reinterpret_cast<int32_t *>(ws + kAlign);
+    a.order = pl.ordered ? reinterpret_cast<const int32_t *>(ws + pl.off_order) : nullptr;
     a.part_ml = reinterpret_cast<float *>(ws + pl.off_ml);
     a.part_acc = reinterpret_cast<float *>(ws + pl.off_acc);
     a.err = error_flag;
@@ -306,6 +315,11 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
     for (int j = 0; j < p->n_q; ++j)
         a.anc[j] = ancestor_mask ? ancestor_mask[j] : ((j == 63) ? ~0ull : ((1ull << (j + 1)) - 1ull));
     a.total_units = p->batch * p->num_kv_heads * pl.max_splits;
+    if (pl.ordered) {
+        cudaError_t e = launch_seq_order(context_lens, p->batch, reinterpret_cast<int32_t *>(ws + pl.off_order),
+                                         static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return from_cuda(e);
+    }
     if (pl.use_tc) {
         const int grid = std::max(1, std::min(pl.grid_slots, a.total_units));
         return from_cuda(launch_paged_verify_attn_tc(maps, a, grid, fp8, static_cast<cudaStream_t>(stream)));

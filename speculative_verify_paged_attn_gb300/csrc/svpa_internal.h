@@ -55,6 +55,7 @@ struct AttnArgs {
     float *part_acc;      // [B*Hkv, max_splits, M, D]
     float *part_ml;       // [B*Hkv, max_splits, M, 2]  (running max in log2 units, sum)
     int32_t *tickets;     // [B*Hkv]
+    const int32_t *order; // [B] sequences, longest first, in the order units are handed out; or null
     int32_t *sched;       // [2]: next work unit, CTAs finished (both back to 0 after a call)
     int32_t *err;
     int32_t B, n_q, Hq, Hkv, G, M;
@@ -85,6 +86,10 @@ cudaError_t launch_paged_verify_attn(const AttnMaps &maps, const AttnArgs &a, in
                                      bool fp8, int grid, size_t smem, cudaStream_t stream);
 // Stage count, resident CTAs per SM and dynamic shared memory for a shape.
 cudaError_t attn_plan_launch(int head_dim, bool fp8, int M, AttnLaunch *out);
+// Sequence ids sorted by decreasing context length (ties by index) into
+// order[0..B): the persistent kernels hand out long units first.
+constexpr int kMaxOrderedSeqs = 4096;
+cudaError_t launch_seq_order(const int32_t *context_lens, int B, int32_t *order, cudaStream_t stream);
 // tcgen05 / TMEM variant (bf16 pages, head_dim 128, one CTA per SM).
 cudaError_t launch_paged_verify_attn_tc(const AttnMaps &maps, const AttnArgs &a, int grid, bool fp8,
                                         cudaStream_t stream);
