@@ -576,7 +576,8 @@ cudaError_t plan_mt_uncached(AttnLaunch *out) {
     // registers are allocated per warp in units of 256
     const int per_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
     int ctas = 65536 / (per_warp * (THREADS / 32));
-    // up to 6 CTAs per SM (measured on the 7B shape: 4 -> 226 us, 5 -> 223, 6 -> 218)
+    // up to 6 CTAs per SM (measured on the 7B shape: 4 -> 226 us, 5 -> 223, 6 -> 218; 7 and 8,
+    // at 128 registers and fewer stages each, 223 and 221)
     ctas = ctas < 1 ? 1 : (ctas > 6 ? 6 : ctas);
     const int qbuf = 2 * MT * 16 * 128 * G_::QSLABS;
     const int fixed = 1024 + qbuf + 16 + 64;
