@@ -122,7 +122,10 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     // greedy longest-first order; the draft-tree workload's 1024 unsplit
     // units on 152 SMs: about 12% above the ideal finish in index order,
     // about 2% longest first, by a list-scheduling estimate)
-    pl->ordered = pl->max_splits == 1 && p->batch > 1 && p->batch <= kMaxOrderedSeqs;
+    // (only when there are more units than resident CTAs: otherwise every
+    // unit starts at once and the extra launch buys nothing)
+    pl->ordered = pl->max_splits == 1 && p->batch > 1 && p->batch <= kMaxOrderedSeqs &&
+                  units > (size_t)pl->grid_slots;
     pl->off_order = off;
     if (pl->ordered) off += align_up((size_t)p->batch * sizeof(int32_t));
     pl->off_ml = off;
