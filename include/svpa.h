@@ -50,7 +50,8 @@ typedef enum svpa_status {
     SVPA_ERR_INVALID_ARG = 1,   /* null pointer, bad size or shape            */
     SVPA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim)  */
     SVPA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed          */
-    SVPA_ERR_OUT_OF_BLOCKS = 4, /* the free stack overflowed (device)        */
+    SVPA_ERR_OUT_OF_BLOCKS = 4, /* the free stack overflowed or ran empty
+                                   (device)                                   */
     SVPA_ERR_BAD_BLOCK = 5,     /* a block id outside [0, num_blocks) (device)*/
     SVPA_ERR_WORKSPACE = 6,     /* workspace missing or too small             */
     SVPA_ERR_TIMEOUT = 7        /* a device-side wait gave up (device)        */
@@ -59,7 +60,7 @@ typedef enum svpa_status {
 /* bits of the device error word */
 #define SVPA_DEVERR_BAD_BLOCK 1
 #define SVPA_DEVERR_TIMEOUT 2
-#define SVPA_DEVERR_FREE_OVERFLOW 4
+#define SVPA_DEVERR_FREE_OVERFLOW 4 /* free stack overflowed (commit) or empty (append) */
 #define SVPA_DEVERR_BAD_VALUE 8 /* an out-of-range length, count or token id */
 
 /* K/V page element types */
@@ -109,7 +110,8 @@ typedef struct svpa_attn_params {
 svpa_status svpa_attn_kernel(const svpa_attn_params *p, int32_t *kernel);
 
 /* Bytes of workspace svpa_paged_verify_attn needs for `p` (split-KV partial
- * results and per-(sequence, kv head) tickets).  The workspace must be
+ * results, per-(sequence, kv head) tickets and, for unsplit work, the order
+ * in which sequences are handed out: longest first).  The workspace must be
  * zero-filled once before its first use; every completed call leaves its
  * ticket words at zero again. */
 svpa_status svpa_attn_workspace_size(const svpa_attn_params *p, size_t *bytes);
