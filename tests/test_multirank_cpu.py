@@ -25,6 +25,16 @@ def free_port():
     return p
 
 
+def gathered_rows(r, b, n):
+    """K and V bytes (and the FP8 scale of each row's page) of positions 0..n-1
+    of sequence b in an append result, through its block table."""
+    bt = r["block_table"][b]
+    k = np.stack([r["k_pool"][bt[p // 16], :, p % 16] for p in range(n)])
+    v = np.stack([r["v_pool"][bt[p // 16], :, p % 16] for p in range(n)])
+    ks = np.stack([r["k_scale"][bt[p // 16]] for p in range(n)])
+    return k, v, ks
+
+
 def _worker(rank, world, port, outdir):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
@@ -45,8 +55,23 @@ def _worker(rank, world, port, outdir):
                                       sm_scale=wl.sm_scale, nthreads=1)
     k, toks, _, _ = oracle.spec_accept(smp.p[mine], smp.q[mine], smp.tokens[mine],
                                        smp.u_accept[mine], smp.u_sample[mine], nthreads=1)
+    # K/V append on this rank's own copy of the cache (replicas: each GPU
+    # owns its pool), for its sequences only; the gathered rows of each
+    # sequence must not depend on which rank appended it
+    ap = W.make_append(W.WORKLOADS["tiny"].scaled(kv_fp8=True), 56, contexts=(2, 5, 40, 9, 70, 3),
+                       shared_prefix=19, n_new=5)
+    ra = oracle.kv_append(ap.new_k[mine], ap.new_v[mine], ap.block_table.numpy()[mine],
+                          ap.context_lens.numpy()[mine], ap.refcount.numpy(), ap.free_stack.numpy(),
+                          ap.free_top, ap.k_pool, ap.v_pool, ap.k_scale, ap.v_scale)
+    rows = [gathered_rows(ra, b_local, int(ap.context_lens[b]) + 5) for b_local, b in enumerate(mine)]
+    # per-sequence acceptance averages and draft lengths on the shard
+    gk = np.array([[0, 3, 4, 1, 2, 4], [1, 4, 4, 0, 2, 3]], np.int32)
+    st = np.zeros((len(mine), 2), np.float32)
+    for step in range(2):
+        rg = oracle.gamma_update(4, gk[step][mine], seq_state=st, decay=0.8)
+        st = rg["seq_state"]
     parts = [None] * world
-    dist.all_gather_object(parts, (mine, out, k, toks))
+    dist.all_gather_object(parts, (mine, out, k, toks, rows, st, rg["seq_gamma"]))
     cpu = torch.device("cpu")
     mx = bench.max_over_ranks(float(rank + 1), world, cpu)
     sm = bench.sum_over_ranks(float(rank + 1), world, cpu)
@@ -56,10 +81,20 @@ def _worker(rank, world, port, outdir):
         full_out = np.zeros((B,) + out.shape[1:])
         full_k = np.zeros(B, np.int32)
         full_t = np.zeros((B, toks.shape[1]), np.int32)
-        for idx, o, kk, tt in parts:
+        app, gst, gg = [None] * 6, np.zeros((6, 2), np.float32), np.zeros(6, np.int32)
+        for idx, o, kk, tt, rr, ss, gq in parts:
             full_out[idx] = o
             full_k[idx] = kk
             full_t[idx] = tt
+            for j, b in enumerate(idx):
+                app[b] = rr[j]
+            gst[idx], gg[idx] = ss, gq
+        flat = np.empty(len(app), dtype=object)
+        for b, r in enumerate(app):
+            flat[b] = np.concatenate([a.ravel().view(np.uint8) for a in r])
+        np.save(os.path.join(outdir, "append.npy"), flat, allow_pickle=True)
+        np.save(os.path.join(outdir, "gstate.npy"), gst)
+        np.save(os.path.join(outdir, "ggamma.npy"), gg)
         np.save(os.path.join(outdir, "out.npy"), full_out)
         np.save(os.path.join(outdir, "k.npy"), full_k)
         np.save(os.path.join(outdir, "t.npy"), full_t)
@@ -84,3 +119,20 @@ def test_sharded_by_sequence_equals_single_process(tmp_path, oracle_mod):
     assert np.array_equal(np.load(tmp_path / "t.npy"), toks)
     mx, sm = np.load(tmp_path / "reduce.npy")
     assert mx == 2.0 and sm == 3.0
+    # the append and the per-sequence draft-length state, single process
+    ap = W.make_append(W.WORKLOADS["tiny"].scaled(kv_fp8=True), 56, contexts=(2, 5, 40, 9, 70, 3),
+                       shared_prefix=19, n_new=5)
+    ra = oracle_mod.kv_append(ap.new_k, ap.new_v, ap.block_table.numpy(), ap.context_lens.numpy(),
+                              ap.refcount.numpy(), ap.free_stack.numpy(), ap.free_top, ap.k_pool, ap.v_pool,
+                              ap.k_scale, ap.v_scale)
+    got = np.load(tmp_path / "append.npy", allow_pickle=True)
+    for b in range(6):
+        want = np.concatenate([a.ravel().view(np.uint8) for a in gathered_rows(ra, b, int(ap.context_lens[b]) + 5)])
+        assert np.array_equal(got[b], want), b
+    gk = np.array([[0, 3, 4, 1, 2, 4], [1, 4, 4, 0, 2, 3]], np.int32)
+    st = np.zeros((6, 2), np.float32)
+    for step in range(2):
+        rg = oracle_mod.gamma_update(4, gk[step], seq_state=st, decay=0.8)
+        st = rg["seq_state"]
+    assert np.array_equal(np.load(tmp_path / "gstate.npy"), st)
+    assert np.array_equal(np.load(tmp_path / "ggamma.npy"), rg["seq_gamma"])
