@@ -643,7 +643,8 @@ def main():
                          "algorithmic_bytes_per_launch": st.attn_bytes},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4)},
-            "gpu_launches": 3 * K,
+            # per step: the attention (1, or 2 with the unit ranking), sampler, commit
+            "gpu_launches": (svpa.attn_launches(st.params) + 2) * K,
             "clocks": clk,
             "cpu_baseline": cpu,
         }

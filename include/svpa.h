@@ -109,6 +109,11 @@ typedef struct svpa_attn_params {
  * when p->variant is 0).  Same validation as svpa_attn_workspace_size. */
 svpa_status svpa_attn_kernel(const svpa_attn_params *p, int32_t *kernel);
 
+/* Kernel launches one svpa_paged_verify_attn call makes for `p`: 1, or 2
+ * when the unsplit work units are first ranked longest sequence first.  Same
+ * validation as svpa_attn_workspace_size. */
+svpa_status svpa_attn_launches(const svpa_attn_params *p, int32_t *launches);
+
 /* Bytes of workspace svpa_paged_verify_attn needs for `p` (split-KV partial
  * results, per-(sequence, kv head) tickets and, for unsplit work, the order
  * in which sequences are handed out: longest first).  The workspace must be

@@ -173,6 +173,15 @@ svpa_status svpa_attn_kernel(const svpa_attn_params *p, int32_t *kernel) {
     return SVPA_OK;
 }
 
+svpa_status svpa_attn_launches(const svpa_attn_params *p, int32_t *launches) {
+    if (!launches) return SVPA_ERR_INVALID_ARG;
+    AttnPlan pl;
+    const svpa_status s = plan_attn(p, &pl);
+    if (s != SVPA_OK) return s;
+    *launches = p->batch == 0 ? 0 : (pl.ordered ? 2 : 1);
+    return SVPA_OK;
+}
+
 svpa_status svpa_attn_workspace_size(const svpa_attn_params *p, size_t *bytes) {
     if (!bytes) return SVPA_ERR_INVALID_ARG;
     AttnPlan pl;

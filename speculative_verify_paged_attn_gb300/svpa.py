@@ -28,7 +28,7 @@ STATUS = {0: "SVPA_OK", 1: "SVPA_ERR_INVALID_ARG", 2: "SVPA_ERR_UNSUPPORTED", 3:
 EXPORTS = ("svpa_attn_workspace_size", "svpa_attn_kernel", "svpa_paged_verify_attn", "svpa_spec_accept_workspace_size",
            "svpa_spec_accept", "svpa_spec_accept_tree", "svpa_block_table_commit", "svpa_check_error",
            "svpa_status_string", "svpa_version", "svpa_paged_verify_attn_noalloc", "svpa_kv_append",
-           "svpa_gamma_update")
+           "svpa_gamma_update", "svpa_attn_launches")
 
 
 class SvpaError(RuntimeError):
@@ -61,6 +61,7 @@ def load(path: str = LIB_PATH):
     P, I, U, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
     L.svpa_attn_workspace_size.argtypes = [ctypes.POINTER(AttnParams), ctypes.POINTER(U)]
     L.svpa_attn_kernel.argtypes = [ctypes.POINTER(AttnParams), ctypes.POINTER(I)]
+    L.svpa_attn_launches.argtypes = [ctypes.POINTER(AttnParams), ctypes.POINTER(I)]
     L.svpa_paged_verify_attn.argtypes = [ctypes.POINTER(AttnParams)] + [P] * 11 + [U, P, P]
     L.svpa_spec_accept_workspace_size.argtypes = [I, I, ctypes.POINTER(U)]
     L.svpa_spec_accept.argtypes = [I, I, I] + [P] * 9 + [U, P, P]
@@ -119,6 +120,13 @@ def attn_kernel(params: AttnParams) -> int:
     k = ctypes.c_int32(0)
     _check(load().svpa_attn_kernel(ctypes.byref(params), ctypes.byref(k)), "svpa_attn_kernel")
     return k.value
+
+
+def attn_launches(params: AttnParams) -> int:
+    """Kernel launches of one svpa_paged_verify_attn call for `params` (1, or 2 with the unit ranking)."""
+    n = ctypes.c_int32(0)
+    _check(load().svpa_attn_launches(ctypes.byref(params), ctypes.byref(n)), "svpa_attn_launches")
+    return n.value
 
 
 def spec_accept_workspace_size(batch: int, vocab: int) -> int:

@@ -48,6 +48,10 @@ def test_workspace_size_and_validation(lib):
         kw.update(bad)
         with pytest.raises(svpa.SvpaError):
             svpa.attn_workspace_size(svpa.attn_params(**kw))
+    # unsplit units with more units than resident CTAs are ranked first (2 launches)
+    assert svpa.attn_launches(svpa.attn_params(128, 29, 32, 8, 128, 600, 100000)) in (1, 2)
+    assert svpa.attn_launches(svpa.attn_params(2, 5, 4, 4, 64, 8, 16)) == 1
+    assert svpa.attn_launches(svpa.attn_params(0, 5, 4, 4, 64, 8, 16)) == 0
     # which kernel runs: warp-level MMA for few rows per kv head, tcgen05 for many
     assert svpa.attn_kernel(svpa.attn_params(32, 5, 32, 32, 128, 256, 4096)) == 1
     assert svpa.attn_kernel(svpa.attn_params(64, 6, 64, 8, 128, 2049, 100000)) == 2
