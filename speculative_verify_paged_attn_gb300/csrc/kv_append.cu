@@ -9,7 +9,10 @@
 //   page whose count is above 1 is cloned first (the shared block loses one
 //   reference, the last holder keeps writing in place); FP8 pages carry one
 //   fp32 scale per (page, kv head) for K and one for V, rescaled to
-//   amax / 448 over the page's history and new rows on every write.
+//   amax / 448 over the page's history and new rows on every write, or one
+//   scale per 64-element tile of a row (the implementation checklist's
+//   per-64-element block scales), where each new row's tiles are quantised
+//   on their own and the history is left as it is.
 //
 // Two launches on the caller's stream:
 //   1. append_alloc_kernel, one CTA per sequence: maps, allocates and clones
