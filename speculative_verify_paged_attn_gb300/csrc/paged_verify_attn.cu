@@ -14,7 +14,8 @@
 //  * work unit = (sequence, kv head, KV split): all G*n_q query rows of a kv
 //    head share each K/V page, so every page is read from HBM exactly once;
 //  * persistent CTAs, several per SM; a producer warp takes units from an
-//    atomic counter and streams their (K, V) page tiles -- and, at each
+//    atomic counter (unsplit units longest sequence first, ranked by
+//    seq_order_kernel below) and streams their (K, V) page tiles -- and, at each
 //    unit's first page, the unit's query tile -- into a ring of shared-memory
 //    stages with tiled bulk tensor copies (TMA, 128-byte swizzle, one
 //    mbarrier pair per stage), gathering pages by block id.  The ring runs

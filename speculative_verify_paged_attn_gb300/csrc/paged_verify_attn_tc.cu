@@ -8,7 +8,9 @@
 // "Triton CUDA Fused Speculative Tree-Verification Kernel": per-page block
 // lookup, K/V cache [blocks, heads, 16, dim], running max / sum).
 //
-// Work unit = (sequence, kv head, KV split); persistent CTAs, one per SM.
+// Work unit = (sequence, kv head, KV split); persistent CTAs, one per SM
+// (unsplit units are handed out longest sequence first, in the order a small
+// ranking kernel leaves in the workspace).
 // Warp roles:
 //   warp 0     producer: takes units from an atomic counter and streams blocks
 //              of 8 pages (128 tokens) of K -- with each unit's query tile on
@@ -64,8 +66,11 @@ constexpr int kTileScales = 16 * (128 / 64);    // tile scales of one (page, kv 
 //    producer, 1 MMA, 4-5 softmax, 8-9 epilogue, 2/3/10 K converters, 6/7/11
 //    V converters; the producer streams E4M3 pages (and, by cp.async, their
 //    scales) into 2-deep staging rings, the converters turn each block into
-//    f16 (the page's scale folded in) in 2-deep K and V tile rings, and the
-//    MMAs run kind::f16 with f16 queries (converted in place) and f16 P.  The
+//    f16 (exactly; the K page scale then enters the softmax's exponent and the
+//    V page scale multiplies P) in 2-deep K and V tile rings, and the MMAs
+//    run kind::f16 with f16 queries (converted in place) and f16 P.  With one
+//    scale per 64-element tile of a row (the TILES instantiation) the
+//    converters multiply each row-half by its own scale instead.  The
 //    query buffer holds 64 rows; the MMA still reads 128, rows 64..127 being
 //    whatever follows and feeding only TMEM lanes no thread reads.
 template <bool FP8>
