@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -49,10 +50,19 @@ SHARED_SOURCES = ["speculative_verify_paged_attn_gb300/csrc/svpa_device.cuh",
                   "speculative_verify_paged_attn_gb300/csrc/svpa_api.cu"]
 
 
+def code_only(text: str) -> str:
+    """C/C++ source without comments and blank lines (string literals in these
+    files hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_hash(kernel: str) -> str:
+    """Hash of the code (comments excluded) that decides a kernel's traffic."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel] + SHARED_SOURCES:
-        h.update(open(os.path.join(ROOT, f), "rb").read())
+        h.update(code_only(open(os.path.join(ROOT, f)).read()).encode())
     return h.hexdigest()[:16]
 
 
