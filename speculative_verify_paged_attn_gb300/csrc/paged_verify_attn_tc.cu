@@ -645,21 +645,50 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             // P_j as bf16 pairs into the first half of S_j's TMEM columns
             const uint32_t pt = tmem + kTmemS + (uint32_t)(j & 1) * kNB + lane_off;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (FP8) {
+                // FP8 pages: P is f16, so each pair of exponents is evaluated by
+                // one ex2.f16x2 on the fp32 arguments rounded to f16 (an argument
+                // is at most 8 under the lazy maximum, where f16 keeps P within
+                // ~0.14%); the row sum adds those f16 values, in f16 within a
+                // page (16 values) and in fp32 across pages; P times the V page
+                // scale is formed in f16.  A page whose K scale is 0 has scores
+                // 0: its multiplier stays positive so masked columns stay -inf.
 #pragma unroll
-            for (int c = 0; c < kNB / 64; ++c) {
-                uint32_t w[32];
+                for (int c = 0; c < kNB / 64; ++c) {
+                    uint32_t w[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int pg = (c * 64 + 2 * e) >> 4;  // page of both columns
-                    // FP8: a page whose K scale is 0 has scores 0; keep the
-                    // multiplier positive so that masked (-inf) columns stay -inf
-                    const float scp = FP8 ? fmaxf(sc * ksc[pg], 1e-30f) : sc;
-                    const float p0 = live ? ex2_approx(fmaf(s[c * 64 + 2 * e], scp, neg_m)) : 0.f;
-                    const float p1 = live ? ex2_approx(fmaf(s[c * 64 + 2 * e + 1], scp, neg_m)) : 0.f;
-                    ls[e & 3] += p0 + p1;
-                    w[e] = FP8 ? pack_f16x2(p0 * vsc[pg], p1 * vsc[pg]) : pack_bf16x2(p0, p1);
+                    for (int q = 0; q < 4; ++q) {
+                        const int pg = c * 4 + q;  // the page of these 16 columns
+                        const float scp = fmaxf(sc * ksc[pg], 1e-30f);
+                        const uint32_t v2 = pack_f16x2(vsc[pg], vsc[pg]);
+                        uint32_t acc = 0u;  // f16 pair (+0, +0)
+#pragma unroll
+                        for (int e8 = 0; e8 < 8; ++e8) {
+                            const int e = q * 8 + e8;
+                            const float x0 = live ? fmaf(s[c * 64 + 2 * e], scp, neg_m) : -CUDART_INF_F;
+                            const float x1 = live ? fmaf(s[c * 64 + 2 * e + 1], scp, neg_m) : -CUDART_INF_F;
+                            const uint32_t p2 = ex2_f16x2(pack_f16x2(x0, x1));
+                            acc = add_f16x2(acc, p2);
+                            w[e] = mul_f16x2(p2, v2);
+                        }
+                        const float2 f = f16x2_to_float2(acc);
+                        ls[q] += f.x + f.y;
+                    }
+                    tmem_st32(pt + c * 32, w);
                 }
-                tmem_st32(pt + c * 32, w);
+            } else {
+#pragma unroll
+                for (int c = 0; c < kNB / 64; ++c) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float p0 = live ? ex2_approx(fmaf(s[c * 64 + 2 * e], sc, neg_m)) : 0.f;
+                        const float p1 = live ? ex2_approx(fmaf(s[c * 64 + 2 * e + 1], sc, neg_m)) : 0.f;
+                        ls[e & 3] += p0 + p1;
+                        w[e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(pt + c * 32, w);
+                }
             }
             l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             // V rows past the sequence's last token may hold anything: zero

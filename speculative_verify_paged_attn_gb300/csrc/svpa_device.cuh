@@ -202,6 +202,24 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// 2^x of both halves of an f16 pair (one MUFU instruction for two values).
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+    uint32_t y;
+    asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t add_f16x2(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
+}
+
+// Both halves of an f16 pair as fp32 (exact).
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t v) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&v));
+}
+
 __device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
     uint32_t y;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
