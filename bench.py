@@ -263,6 +263,75 @@ class Append:
                        k_scale=inp.k_scale, v_scale=inp.v_scale, scale_tile=self.tile)
 
 
+class WholeStep(Append):
+    """A whole verification step in call order on the append's cache state:
+    K/V append, attention over the appended cache, sampler (the main step's
+    inputs), commit/rollback and the draft-length update.  The cache state
+    (tables, lengths, counts, free stack, FP8 partial pages) is restored
+    before every step."""
+
+    def __init__(self, wl: W.Workload, seed: int, dev: torch.device, step: "Step"):
+        super().__init__(wl, seed, dev)
+        inp, self.wl, self.st = self.inp, wl, step
+        B = inp.new_k.shape[0]
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed + 29)
+        self.q = torch.randn((B, wl.n_q, wl.num_q_heads, wl.head_dim), generator=g, device=dev).to(torch.bfloat16)
+        self.cl0 = inp.context_lens.clone()
+        self.params = svpa.attn_params(B, wl.n_q, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                       inp.block_table.shape[1], self.kp.shape[0], kv_fp8=wl.kv_fp8,
+                                       sm_scale=wl.sm_scale, scale_tile=wl.scale_tile)
+        self.ws = torch.zeros(svpa.attn_workspace_size(self.params), dtype=torch.uint8, device=dev)
+        self.out = torch.empty((B, wl.n_q, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
+        self.gs = torch.zeros((B, 2), dtype=torch.float32, device=dev)
+        self.gq = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.gb = torch.zeros(2, dtype=torch.float32, device=dev)
+        self.gg = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.tel = torch.zeros(4, dtype=torch.float32, device=dev)
+        self.gamma = step.path.shape[1] - 1 if step.tree else wl.gamma
+        T = self.cl0.long() + wl.n_q
+        self.kv_bytes = int(T.sum().item()) * wl.num_kv_heads * wl.head_dim * 2 * (1 if wl.kv_fp8 else 2)
+
+    def reset(self):
+        super().reset()
+        self.inp.context_lens.copy_(self.cl0)
+
+    def run_step(self):
+        inp, st, wl = self.inp, self.st, self.wl
+        self.run()
+        svpa.paged_verify_attn(self.params, self.q, self.kp, self.vp, inp.block_table, inp.context_lens, self.out,
+                               workspace=self.ws, error_flag=self.err, k_scale=inp.k_scale, v_scale=inp.v_scale,
+                               ancestor_mask=st.mask)
+        st.sample()
+        svpa.block_table_commit(wl.n_q, inp.block_table, inp.context_lens, st.k, inp.refcount, inp.free_stack,
+                                self.ft, error_flag=self.err, path_nodes=st.path if st.tree else None,
+                                k_pool=self.kp if st.tree else None, v_pool=self.vp if st.tree else None,
+                                num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim, kv_fp8=wl.kv_fp8)
+        svpa.gamma_update(self.gamma, st.k, self.gb, self.gg, self.tel, error_flag=self.err, seq_state=self.gs,
+                          seq_gamma=self.gq, draft_cost_ratio=0.08)
+
+
+def time_whole_step(ws: WholeStep, steps: int, warmup: int, stream) -> float:
+    """Average device time (ms) of a whole step, L2 flushed before each."""
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=ws.ft.device)
+    for _ in range(warmup):
+        ws.reset()
+        ws.run_step()
+    ms = []
+    for _ in range(steps):
+        ws.reset()
+        flush.fill_(1)
+        gpu_lead()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ws.run_step()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    assert svpa.check_error(ws.err) == 0 and svpa.check_error(ws.st.err) == 0, "device error in the whole step"
+    return sum(ms) / len(ms)
+
+
 def time_append(ap: Append, steps: int, warmup: int, stream) -> float:
     """Average device time (ms) of one svpa_kv_append, L2 flushed before each."""
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=ap.ft.device)
@@ -583,10 +652,13 @@ def main():
     e2e = max_over_ranks(e2e_local, world, dev)
     e2e_value = total_bytes / (e2e * 1e-3) / 1e9
 
-    # the K/V append that precedes a verification step, timed on its own
-    ap = Append(wl, seed, dev)
+    # the K/V append that precedes a verification step, timed on its own, and
+    # the whole step in call order on the same cache state
+    ap = WholeStep(wl, seed, dev, st)
     app_ms = time_append(ap, K, args.warmup, stream)
     app_bytes = ap.bytes
+    whole_ms = time_whole_step(ap, K, args.warmup, stream)
+    whole_bytes = ap.kv_bytes
     del ap
     # the draft-length controller on this step's accepted lengths
     gam_ms = time_gamma(st, K, args.warmup, stream)
@@ -632,6 +704,10 @@ def main():
             "kv_append_us": round(app_ms * 1e3, 2),
             "kv_append_gbs": round(app_bytes / (app_ms * 1e-3) / 1e9, 2),
             "gamma_update_us": round(gam_ms * 1e3, 2),
+            "whole_step": {"us": round(whole_ms * 1e3, 2), "kv_bytes": whole_bytes,
+                           "kv_gbs": round(whole_bytes / (whole_ms * 1e-3) / 1e9, 2),
+                           "calls": "kv_append, paged_verify_attn, spec_accept, block_table_commit, gamma_update",
+                           "state": "the append's cache (its own context lengths), restored before each step"},
             "kv_bytes_per_step": st.kv_bytes,
             "kv_bytes_logical_per_step": int((st.cl0.long() + st.n_q).sum().item()) * wl.num_kv_heads
                                          * wl.head_dim * 2 * (1 if wl.kv_fp8 else 2),
