@@ -452,7 +452,7 @@ def sum_over_ranks(x: float, world: int, dev) -> float:
     return float(t.item())
 
 
-def cpu_baseline(wl: W.Workload, seed: int, budget_s: float = 12.0):
+def cpu_baseline(wl: W.Workload, seed: int, budget_s: float = 12.0, nthreads: int = 0):
     """The oracle, as it stands, on the host cores: attention over chunks of
     the workload's sequences (wrapping around the batch) until the time budget
     is used, plus the sampler and commit of those sequences.  Returns (GB/s,
@@ -461,13 +461,13 @@ def cpu_baseline(wl: W.Workload, seed: int, budget_s: float = 12.0):
     oracle.build()
     inp = W.make_attention(wl, seed, device="cpu", poison=False)
     smp = W.make_sampler(wl, seed, device="cpu")
-    cores = oracle.max_threads()
+    cores = oracle.max_threads() if nthreads == 0 else nthreads
     am = None if inp.ancestor_mask is None else inp.ancestor_mask.numpy().view(np.uint64)
     done_bytes, t_total, nseq = 0, 0.0, 0
     B = inp.q.shape[0]
     n_q = wl.n_q
     eb = 1 if wl.kv_fp8 else 2
-    chunk = max(1, min(B, cores))
+    chunk = max(1, min(B, cores))  # one sequence per thread and pass
     start, passes = 0, 0
     while t_total < budget_s:
         sel = list(range(start, min(B, start + chunk)))
@@ -476,14 +476,14 @@ def cpu_baseline(wl: W.Workload, seed: int, budget_s: float = 12.0):
                                  inp.context_lens[sel], num_kv_heads=wl.num_kv_heads,
                                  sm_scale=wl.sm_scale, kv_fp8=wl.kv_fp8, k_scale=inp.k_scale,
                                  scale_tile=wl.scale_tile,
-                                 v_scale=inp.v_scale, ancestor_mask=am)
+                                 v_scale=inp.v_scale, ancestor_mask=am, nthreads=nthreads)
         if wl.tree_branching:
             oracle.spec_accept_tree(np.array(wl.parent, np.int32), smp.p[sel], smp.q[sel],
-                                    smp.tokens[sel], smp.u_accept[sel], smp.u_sample[sel])
+                                    smp.tokens[sel], smp.u_accept[sel], smp.u_sample[sel], nthreads=nthreads)
             k = np.zeros(len(sel), np.int32)
         else:
             k, *_ = oracle.spec_accept(smp.p[sel], smp.q[sel], smp.tokens[sel], smp.u_accept[sel],
-                                       smp.u_sample[sel])
+                                       smp.u_sample[sel], nthreads=nthreads)
         oracle.block_table_commit(inp.block_table[sel], inp.context_lens[sel], k, inp.refcount,
                                   inp.free_stack, inp.free_top, n_q=n_q)
         t_total += time.perf_counter() - t0
@@ -682,8 +682,9 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, cores, sample, _ = cpu_baseline(wl, seed)
+        gbs1, _, sample1, _ = cpu_baseline(wl, seed, budget_s=4.0, nthreads=1)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": sample}
+               "sample": sample, "single_thread": {"value": round(gbs1, 4), "sample": sample1}}
 
     kname = "pva_tc_kernel" if svpa.attn_kernel(st.params) == 2 else "pva_kernel"
     if rank == 0:
