@@ -26,6 +26,13 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*.py``):
                        values within half a code of the data)
   e4m3_encode          pinned (equals torch.float8_e4m3fn rounding on every
                        in-range value tested; saturation at 448)
+  FP8 tile scales      pinned (attention: SDPA on pages decoded in the test
+  (scale_tile=64)      with the scales broadcast to full rows; equal tile
+                       scales reproduce the per-page result; append: every new
+                       tile's scale and codes on a worked example)
+  gamma_update,        pinned (estimator limit under simulated per-token
+  gamma_from_alpha     acceptance, threshold edges, the moving average's closed
+                       form, E[K] / speed-up closed forms and the worked example)
 """
 from __future__ import annotations
 
