@@ -11,7 +11,8 @@ section 2.1-2.2).
 
 Pins that do not restate the oracle:
   * Monte-Carlo: the emitted token at every reached position is distributed as
-    P at that position (the exactness theorem), chi-square on 2e5 rows;
+    P at that position (the exactness theorem), chi-square on 10^6 rows at
+    V = 8 and 25,000 rows at V = 1000;
   * the mean accepted length equals the page's E[K] formula for fixed drafts,
     and sum_i prod_j (1 - TV(P_j, Q_j)) for drafts drawn from Q;
   * special cases: P == Q always accepts; a draft one-hot on a token the
@@ -59,7 +60,7 @@ def chi2_ok(tokens, probs, min_p=1e-4):
 
 def test_output_distribution_equals_target(oracle_mod):
     rng = np.random.default_rng(2024)
-    gamma, V, B = 3, 8, 200_000
+    gamma, V, B = 3, 8, 1_000_000
     P = fixed_rows(rng, gamma + 1, V)
     Q = fixed_rows(rng, gamma, V)
     x = draw_from(rng, Q, B)
@@ -75,6 +76,23 @@ def test_output_distribution_equals_target(oracle_mod):
     assert np.all(out[idx > k[:, None]] == -1)
     assert np.all(out[:, :gamma][idx[:, :gamma] < k[:, None]] == x[idx[:, :gamma] < k[:, None]])
     assert np.all(out[idx == k[:, None]] >= 0)
+
+
+def test_output_distribution_equals_target_large_vocabulary(oracle_mod):
+    # V = 1000 (the tiny workload's vocabulary): every reached position is
+    # distributed as P there, bins with fewer than 5 expected draws aside
+    rng = np.random.default_rng(77)
+    gamma, V, B = 3, 1000, 25_000
+    P = fixed_rows(rng, gamma + 1, V, spread=1.0)
+    Q = fixed_rows(rng, gamma, V, spread=1.0)
+    x = draw_from(rng, Q, B)
+    ua = rng.random((B, gamma), dtype=np.float32)
+    us = rng.random(B, dtype=np.float32)
+    k, out, near, _ = oracle_mod.spec_accept(broadcast_rows(P, B), broadcast_rows(Q, B), x, ua, us)
+    for i in range(gamma + 1):
+        reached = k >= i
+        assert reached.sum() > 2000
+        assert chi2_ok(out[reached, i], P[i]), f"position {i} is not distributed as P_{i}"
 
 
 def test_resampling_from_target_instead_of_residual_would_fail(oracle_mod):
