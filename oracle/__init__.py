@@ -13,6 +13,9 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*.py``):
                        table)
   spec_accept          pinned (Monte-Carlo output distribution = P, mean
                        accepted length = E[K] formula, special cases)
+  spec_accept_logits   pinned (worked two-token example, softmax shift and
+                       temperature identities, agreement with spec_accept on
+                       the same rows, Monte-Carlo output distribution = P)
   spec_accept_tree     pinned (reduces to spec_accept on a chain; Monte-Carlo
                        distribution of the first emitted token = P[root])
   block_table_commit   pinned (hand-worked example, conservation invariants,
@@ -71,6 +74,10 @@ def _load():
             lib.oracle_paged_verify_attn.restype = I
             lib.oracle_spec_accept.argtypes = [I, I, I] + [P] * 9 + [I]
             lib.oracle_spec_accept.restype = I
+            lib.oracle_spec_accept_logits.argtypes = [I, I, I, D, D, D] + [P] * 10 + [I]
+            lib.oracle_spec_accept_logits.restype = I
+            lib.oracle_logits_draw_window.argtypes = [I, I, I, D, D, D] + [P] * 6 + [I]
+            lib.oracle_logits_draw_window.restype = I
             lib.oracle_spec_accept_tree.argtypes = [I, I, I] + [P] * 10 + [I]
             lib.oracle_spec_accept_tree.restype = I
             lib.oracle_block_table_commit.argtypes = [I] * 5 + [P] * 7 + [I, P, P, I, I, I]
@@ -196,6 +203,66 @@ def spec_accept(p_probs, q_probs, draft_tokens, u_accept, u_sample, nthreads=0):
     if rc != 0:
         raise OracleError(f"oracle_spec_accept failed with status {rc}")
     return k, out, near.astype(bool), dist
+
+
+# Near-boundary band of the logits front-end: relative for the acceptance
+# test, absolute (probability units) for the residual mass and the draw.  An
+# fp32 formation of P and Q errs by ~1.2e-7 * |log2 P| relative per entry
+# (exponent rounding, <= 1.6e-5 down to 2^-126) plus <= ~1e-5 in the
+# normaliser (partial sums of <= 128 fp32 terms); 5e-5 covers both.
+LOGIT_BAND = 5e-5
+
+
+def spec_accept_logits(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature=1.0,
+                       draft_temperature=None, band=LOGIT_BAND, nthreads=0, tests=False):
+    """Linear rejection sampler on P = softmax(Lp / T), Q = softmax(Lq / T_draft)
+    formed in fp64.  Returns (accepted_len, out_tokens, near_boundary), and with
+    tests=True also every acceptance test's decision and near flag [B, gamma]."""
+    lib = _load()
+    Lp = _c(target_logits, np.float32)
+    Lq = _c(draft_logits, np.float32)
+    x = _c(draft_tokens, np.int32)
+    ua = _c(u_accept, np.float32)
+    us = _c(u_sample, np.float32)
+    B, g1, V = Lp.shape
+    gamma = g1 - 1
+    assert Lq.shape == (B, gamma, V) and x.shape == (B, gamma)
+    assert ua.shape == (B, gamma) and us.shape == (B,)
+    td = temperature if draft_temperature is None else draft_temperature
+    k = np.zeros(B, np.int32)
+    out = np.zeros((B, gamma + 1), np.int32)
+    near = np.zeros(B, np.uint8)
+    acc = np.zeros((B, gamma), np.uint8)
+    accn = np.zeros((B, gamma), np.uint8)
+    rc = lib.oracle_spec_accept_logits(B, gamma, V, float(temperature), float(td), float(band), _ptr(Lp),
+                                       _ptr(Lq), _ptr(x), _ptr(ua), _ptr(us), _ptr(k), _ptr(out), _ptr(near),
+                                       _ptr(acc), _ptr(accn), int(nthreads))
+    if rc != 0:
+        raise OracleError(f"oracle_spec_accept_logits failed with status {rc}")
+    if tests:
+        return k, out, near.astype(bool), acc.astype(bool), accn.astype(bool)
+    return k, out, near.astype(bool)
+
+
+def logits_draw_window(target_logits, draft_logits, accepted_len, u_sample, temperature=1.0,
+                       draft_temperature=None, band=LOGIT_BAND, nthreads=0):
+    """For each row and its given accepted count k, the range [lo, hi] of
+    tokens an fp32 formation of P and Q may draw (the running-sum intervals
+    within `band` of u * Z).  Returns (lo, hi)."""
+    lib = _load()
+    Lp = _c(target_logits, np.float32)
+    Lq = _c(draft_logits, np.float32)
+    k = _c(accepted_len, np.int32)
+    us = _c(u_sample, np.float32)
+    B, g1, V = Lp.shape
+    td = temperature if draft_temperature is None else draft_temperature
+    lo = np.zeros(B, np.int32)
+    hi = np.zeros(B, np.int32)
+    rc = lib.oracle_logits_draw_window(B, g1 - 1, V, float(temperature), float(td), float(band), _ptr(Lp),
+                                       _ptr(Lq), _ptr(k), _ptr(us), _ptr(lo), _ptr(hi), int(nthreads))
+    if rc != 0:
+        raise OracleError(f"oracle_logits_draw_window failed with status {rc}")
+    return lo, hi
 
 
 def tree_max_depth(parent) -> int:

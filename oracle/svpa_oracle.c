@@ -36,7 +36,9 @@
  *  cumulative mass exceeds u*S (strict); accept iff fp32(u*Q) <= P; a draw
  *  within 1e-6 of a CDF boundary is flagged; new committed length after the
  *  step = L + k + 1; tree acceptance by recursive residual rejection over a
- *  node's children in index order.
+ *  node's children in index order; the logits front-end takes one
+ *  temperature for the target rows and one for the draft rows, and flags
+ *  decisions within 5e-5 of their thresholds (the fp32 formation of P, Q).
  */
 #include <math.h>
 #include <stdint.h>
@@ -324,6 +326,228 @@ int oracle_spec_accept(int B, int gamma, int V, const float *P, const float *Q,
         if (dist) dist[b] = dd;
     }
     return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* sampler front-end: probabilities formed from logits                 */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Max and normaliser of one row of logits at temperature T:
+ * m = max_t l_t, S = sum_t exp((l_t - m) / T), so that
+ * softmax(l / T)_t = exp((l_t - m) / T) / S.  -inf entries are masked tokens
+ * (probability 0).  Returns -1 for a NaN or +inf entry or a row without a
+ * finite entry.
+ */
+static int logit_row_stats(const float *l, int V, double T, double *m_out, double *S_out) {
+    double m = -INFINITY;
+    for (int t = 0; t < V; ++t) {
+        if (isnan(l[t]) || (isinf(l[t]) && l[t] > 0.0f)) return -1;
+        if ((double)l[t] > m) m = (double)l[t];
+    }
+    if (!isfinite(m)) return -1;
+    double S = 0.0;
+    for (int t = 0; t < V; ++t) S += exp(((double)l[t] - m) / T);
+    *m_out = m;
+    *S_out = S;
+    return 0;
+}
+
+static double logit_prob(float l, double m, double S, double T) {
+    return exp(((double)l - m) / T) / S;
+}
+
+/*
+ * Inverse-CDF draw over unnormalised weights r (mass Z = sum r), the first
+ * token whose running sum exceeds u*Z, with the near flag in absolute units:
+ * set when u*Z lies within `band` of a running sum (0 before the first token
+ * counts as one), or when u*Z reached Z by rounding.  Returns -1 when Z == 0.
+ */
+static int32_t draw_abs_band(const double *r, int V, double u, double band, uint8_t *near) {
+    double Z = 0.0;
+    for (int t = 0; t < V; ++t) Z += r[t];
+    if (!(Z > 0.0)) return -1;
+    const double target = u * Z;
+    double C = 0.0, best = fabs(target);
+    int32_t tok = -1;
+    for (int t = 0; t < V; ++t) {
+        C += r[t];
+        if (fabs(C - target) < best) best = fabs(C - target);
+        if (tok < 0 && C > target) tok = t;
+    }
+    if (tok < 0) {
+        for (int t = V - 1; t >= 0; --t)
+            if (r[t] > 0.0) { tok = t; break; }
+        *near = 1;
+    }
+    if (best < band) *near = 1;
+    return tok;
+}
+
+/*
+ * Linear speculative sampler fed by logits.  The target pass yields logits,
+ * the acceptance ratio takes softmax(logits)[x] for each draft token, and the
+ * draft probability is the draft model's own ("Speculative Decoding and
+ * KV-Cache Compression", section 2.3; "LOW-LATENCY INFERENCE: SPECULATIVE
+ * DECODING & PAGING", architecture: target logits P checked against draft
+ * logits Q).  The sampling temperatures are separate knobs for the target
+ * and the draft (the first page's alert table lowers the draft temperature
+ * alone), so P_i = softmax(Lp_i / T_target) and Q_i = softmax(Lq_i / T_draft),
+ * Q being the distribution the drafts were drawn from.
+ *
+ * Lp fp32 [B, gamma+1, V] target logits; Lq fp32 [B, gamma, V] draft logits;
+ * x, u_acc, u_s, accepted_len, out_tokens as in oracle_spec_accept.  Every
+ * probability is fp64 (exp of the fp64 difference), and so are the tests:
+ * accept x_i iff u_i * Q_i(x_i) <= P_i(x_i); the residual max(0, P_k - Q_k)
+ * (P_k when it has no mass) or, with every draft accepted, P_gamma; the token
+ * is the first whose running mass exceeds u * (total mass).
+ *
+ * near[b] is set when a decision sits within `band` of its threshold, where
+ * an fp32 formation of P and Q may take it the other way: an acceptance test
+ * that ran with |u Q - P| <= band * max(P, u Q) or max(P, u Q) < 2^-100; a
+ * residual with mass below band; a draw with u*Z within band of a running sum
+ * (absolute, in probability units).
+ *
+ * test_accept / test_near (uint8 [B, gamma], may be NULL) receive every
+ * test's decision and near flag, the tests after the first rejection
+ * included, so that a sampler whose near-threshold decisions went the other
+ * way can be checked test by test.
+ *
+ * Returns ORC_ERR_ARG for bad sizes or temperatures, a draft token out of
+ * range, or a row that logit_row_stats rejects.
+ */
+int oracle_spec_accept_logits(int B, int gamma, int V, double T_target, double T_draft, double band,
+                              const float *Lp, const float *Lq, const int32_t *x, const float *u_acc,
+                              const float *u_s, int32_t *accepted_len, int32_t *out_tokens,
+                              uint8_t *near, uint8_t *test_accept, uint8_t *test_near, int nthreads) {
+    if (B < 0 || gamma < 1 || V < 1 || !(T_target > 0.0) || !(T_draft > 0.0) || !(band >= 0.0))
+        return ORC_ERR_ARG;
+    for (long i = 0; i < (long)B * gamma; ++i)
+        if (x[i] < 0 || x[i] >= V) return ORC_ERR_ARG;
+    const double tiny = ldexp(1.0, -100);
+    int bad = 0;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int b = 0; b < B; ++b) {
+        const float *Pb = Lp + (long)b * (gamma + 1) * V;
+        const float *Qb = Lq + (long)b * gamma * V;
+        double *mp = (double *)malloc(sizeof(double) * (size_t)(4 * gamma + 2));
+        double *Sp = mp + (gamma + 1), *mq = Sp + (gamma + 1), *Sq = mq + gamma;
+        double *r = (double *)malloc(sizeof(double) * (size_t)V);
+        uint8_t nb = 0;
+        int ok = 1;
+        for (int i = 0; i <= gamma && ok; ++i)
+            ok = logit_row_stats(Pb + (long)i * V, V, T_target, &mp[i], &Sp[i]) == 0;
+        for (int i = 0; i < gamma && ok; ++i)
+            ok = logit_row_stats(Qb + (long)i * V, V, T_draft, &mq[i], &Sq[i]) == 0;
+        if (!ok) {
+            bad = 1;
+            free(mp);
+            free(r);
+            continue;
+        }
+        int k = gamma;
+        for (int i = 0; i < gamma; ++i) {
+            const int32_t xi = x[(long)b * gamma + i];
+            const double P = logit_prob(Pb[(long)i * V + xi], mp[i], Sp[i], T_target);
+            const double Q = logit_prob(Qb[(long)i * V + xi], mq[i], Sq[i], T_draft);
+            const double uq = (double)u_acc[(long)b * gamma + i] * Q;
+            const double hi = P > uq ? P : uq;
+            const int close = fabs(uq - P) <= band * hi || hi < tiny;
+            const int accept = uq <= P;
+            if (test_accept) test_accept[(long)b * gamma + i] = (uint8_t)accept;
+            if (test_near) test_near[(long)b * gamma + i] = (uint8_t)close;
+            if (k == gamma) {  /* a test that ran */
+                if (close) nb = 1;
+                if (!accept) k = i;
+            }
+        }
+        int32_t tok;
+        if (k < gamma) {
+            double Z = 0.0;
+            for (int t = 0; t < V; ++t) {
+                const double d = logit_prob(Pb[(long)k * V + t], mp[k], Sp[k], T_target) -
+                                 logit_prob(Qb[(long)k * V + t], mq[k], Sq[k], T_draft);
+                r[t] = d > 0.0 ? d : 0.0;
+                Z += r[t];
+            }
+            if (Z < band) nb = 1;
+            if (!(Z > 0.0))  /* empty residual: draw from the target row */
+                for (int t = 0; t < V; ++t) r[t] = logit_prob(Pb[(long)k * V + t], mp[k], Sp[k], T_target);
+        } else {
+            for (int t = 0; t < V; ++t) r[t] = logit_prob(Pb[(long)gamma * V + t], mp[gamma], Sp[gamma], T_target);
+        }
+        tok = draw_abs_band(r, V, (double)u_s[b], band, &nb);
+        free(mp);
+        free(r);
+        accepted_len[b] = k;
+        int32_t *o = out_tokens + (long)b * (gamma + 1);
+        for (int i = 0; i <= gamma; ++i)
+            o[i] = i < k ? x[(long)b * gamma + i] : (i == k ? tok : -1);
+        if (near) near[b] = nb;
+    }
+    return bad ? ORC_ERR_ARG : ORC_OK;
+}
+
+/*
+ * The tokens an fp32 formation of P and Q may draw for a given accepted count:
+ * with k[b] < gamma the residual max(0, P_k - Q_k) of mass Z, else P_gamma
+ * (Z = 1), and target u*Z; every token whose running-sum interval
+ * [C_{t-1}, C_t], widened by `band` on both sides, contains the target.  The
+ * sums are monotone, so the tokens form the range [tok_lo, tok_hi].  When the
+ * residual's mass is below band (it may be empty, so the draw may come from
+ * P_k) the range is the whole vocabulary.
+ */
+int oracle_logits_draw_window(int B, int gamma, int V, double T_target, double T_draft, double band,
+                              const float *Lp, const float *Lq, const int32_t *k_in, const float *u_s,
+                              int32_t *tok_lo, int32_t *tok_hi, int nthreads) {
+    if (B < 0 || gamma < 1 || V < 1 || !(T_target > 0.0) || !(T_draft > 0.0) || !(band >= 0.0))
+        return ORC_ERR_ARG;
+    for (int b = 0; b < B; ++b)
+        if (k_in[b] < 0 || k_in[b] > gamma) return ORC_ERR_ARG;
+    int bad = 0;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int b = 0; b < B; ++b) {
+        const int k = k_in[b];
+        const float *lp = Lp + ((long)b * (gamma + 1) + k) * V;
+        const float *lq = k < gamma ? Lq + ((long)b * gamma + k) * V : NULL;
+        double m_p, S_p, m_q = 0.0, S_q = 1.0;
+        if (logit_row_stats(lp, V, T_target, &m_p, &S_p) != 0 ||
+            (lq && logit_row_stats(lq, V, T_draft, &m_q, &S_q) != 0)) {
+            bad = 1;
+            continue;
+        }
+        double *r = (double *)malloc(sizeof(double) * (size_t)V);
+        double Z = 0.0;
+        for (int t = 0; t < V; ++t) {
+            double w = logit_prob(lp[t], m_p, S_p, T_target);
+            if (lq) {
+                w -= logit_prob(lq[t], m_q, S_q, T_draft);
+                if (w < 0.0) w = 0.0;
+            }
+            r[t] = w;
+            Z += w;
+        }
+        int32_t lo = 0, hi = V - 1;
+        if (!(lq && Z < band)) {
+            const double target = (double)u_s[b] * Z;
+            double C = 0.0;
+            lo = -1;
+            hi = -1;
+            for (int t = 0; t < V; ++t) {
+                C += r[t];
+                if (lo < 0 && C >= target - band) lo = t;
+                if (hi < 0 && C > target + band) hi = t;
+            }
+            if (lo < 0) lo = V - 1;
+            if (hi < 0) hi = V - 1;
+        }
+        free(r);
+        tok_lo[b] = lo;
+        tok_hi[b] = hi;
+    }
+    return bad ? ORC_ERR_ARG : ORC_OK;
 }
 
 /* Tree helpers: a node is internal when some node names it as parent; its
