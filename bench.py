@@ -353,6 +353,42 @@ def time_append(ap: Append, steps: int, warmup: int, stream) -> float:
     return sum(ms) / len(ms)
 
 
+def time_logits(wl: W.Workload, seed: int, steps: int, warmup: int, stream):
+    """The sampler's logits front-end (svpa_spec_accept_logits) on the
+    workload's sampler shape: B sequences, gamma + 1 target and gamma draft
+    logit rows of V fp32 each, read once; L2 flushed before each launch.
+    Returns (average ms, per-launch ms list, algorithmic bytes per launch)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    li = W.make_logits(wl, seed + 5, device=dev)
+    B, g1, V = li.lp.shape
+    k = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = torch.empty((B, g1), dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.zeros(svpa.spec_accept_workspace_size(B, V), dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def run():
+        svpa.spec_accept_logits(li.lp, li.lq, li.tokens, li.u_accept, li.u_sample, k, toks, workspace=ws,
+                                error_flag=err, temperature=li.temperature)
+
+    for _ in range(warmup):
+        run()
+    ms = []
+    for _ in range(steps):
+        flush.fill_(1)
+        gpu_lead()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    assert svpa.check_error(err) == 0, "device error in the logits front-end"
+    g = g1 - 1
+    nbytes = (2 * g + 1) * B * V * 4 + B * g * 8 + B * 4 + B * (g1 + 1) * 4
+    return sum(ms) / len(ms), ms, nbytes
+
+
 LEAD_CYCLES = 200_000  # about 0.1 ms of GPU spin at GB300 clocks
 
 
@@ -662,6 +698,15 @@ def main():
     del ap
     # the draft-length controller on this step's accepted lengths
     gam_ms = time_gamma(st, K, args.warmup, stream)
+    # the sampler fed by logits (linear workloads)
+    logit = None
+    if not st.tree:
+        lg_ms, lg_list, lg_bytes = time_logits(wl, seed, K, args.warmup, stream)
+        lg_gbs = lg_bytes / (lg_ms * 1e-3) / 1e9
+        logit = {"us": round(lg_ms * 1e3, 2), "gbs": round(lg_gbs, 2), "frac_of_peak": round(lg_gbs / peak, 4),
+                 "bytes_per_launch": lg_bytes, "p10_p50_p90_us": [round(x * 1e3, 2) for x in percentiles(lg_list)],
+                 "shape": f"B={st.B}, gamma={wl.gamma}, V={wl.vocab}, fp32 logits",
+                 "bytes": "every target and draft logit read once, plus tokens, uniforms and outputs"}
     # per-launch times from CUDA graphs of 100 launches (launch-bound view)
     st.reset()
     graph_attn_us = graph_launch_us(st.attention)
@@ -705,6 +750,7 @@ def main():
             "kv_append_us": round(app_ms * 1e3, 2),
             "kv_append_gbs": round(app_bytes / (app_ms * 1e-3) / 1e9, 2),
             "gamma_update_us": round(gam_ms * 1e3, 2),
+            "spec_accept_logits": logit,
             "whole_step": {"us": round(whole_ms * 1e3, 2), "kv_bytes": whole_bytes,
                            "kv_gbs": round(whole_bytes / (whole_ms * 1e-3) / 1e9, 2),
                            "calls": "kv_append, paged_verify_attn, spec_accept, block_table_commit, gamma_update",

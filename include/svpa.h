@@ -15,6 +15,8 @@
  *   svpa_spec_accept         draft/target rejection sampling over the gamma
  *   svpa_spec_accept_tree    drafts (or along a draft tree): accepted count,
  *                            accepted tokens and the correction/bonus token.
+ *   svpa_spec_accept_logits  the same from logits (the softmax rows formed
+ *                            in the kernel, at sampling temperatures).
  *   svpa_block_table_commit  commit the accepted tokens and roll back the
  *                            rest: new lengths, dropped pages returned to the
  *                            free stack when their reference count reaches 0.
@@ -221,6 +223,47 @@ svpa_status svpa_spec_accept(int32_t batch, int32_t gamma, int32_t vocab,
                              uint8_t *near_boundary, void *workspace,
                              size_t workspace_bytes, int32_t *error_flag,
                              void *stream);
+
+/*
+ * The linear sampler fed by logits: P_i = softmax(target_logits_i / T) and
+ * Q_i = softmax(draft_logits_i / T_draft) are formed inside the kernel and
+ * never written out.  Q must be the distribution the drafts were drawn from.
+ * Then the rule of svpa_spec_accept, with the acceptance test in fp64 on the
+ * fp32 exponentials (accept iff u * Q(x) <= P(x)) and the residual
+ * max(0, P_k - Q_k) formed in fp32.
+ *
+ * Sources: "Speculative Decoding and KV-Cache Compression", section 2.3 (the
+ * acceptance ratio takes softmax(logits)[x] of the target pass); "LOW-LATENCY
+ * INFERENCE: SPECULATIVE DECODING & PAGING", architecture (target logits
+ * checked against draft logits); the same first page's alert table treats
+ * the draft's temperature as its own knob.
+ *
+ *  temperature, draft_temperature  > 0 and finite (log2(e)/T must fit fp32)
+ *  target_logits fp32 [B, gamma+1, V]; draft_logits fp32 [B, gamma, V]:
+ *               finite or -inf (a masked token); every row needs a finite
+ *               entry, else SVPA_DEVERR_BAD_VALUE is raised
+ *  draft_tokens, u_accept, u_sample, accepted_len, out_tokens: as in
+ *               svpa_spec_accept
+ *  near_boundary uint8 [B] or NULL: 1 when a decision lay within 5e-5 of its
+ *               threshold, where forming P and Q in fp32 (relative error up
+ *               to ~2.5e-5) may decide it the other way: an acceptance test
+ *               with |u Q - P| <= 5e-5 max(P, u Q), a residual of mass below
+ *               5e-5, or u * (mass) within 5e-5 of a running sum.  With
+ *               large vocabularies the running sums are closer together than
+ *               that, so most draws are flagged.
+ *  workspace    as for svpa_spec_accept (reserved)
+ *  gamma 1..32; 1 <= V <= 262144, else SVPA_ERR_UNSUPPORTED.
+ */
+svpa_status svpa_spec_accept_logits(int32_t batch, int32_t gamma, int32_t vocab,
+                                    float temperature, float draft_temperature,
+                                    const float *target_logits,
+                                    const float *draft_logits,
+                                    const int32_t *draft_tokens,
+                                    const float *u_accept, const float *u_sample,
+                                    int32_t *accepted_len, int32_t *out_tokens,
+                                    uint8_t *near_boundary, void *workspace,
+                                    size_t workspace_bytes, int32_t *error_flag,
+                                    void *stream);
 
 /*
  * Draft-tree rejection sampler (recursive residual rejection over the

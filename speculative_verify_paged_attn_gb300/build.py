@@ -28,6 +28,7 @@ SOURCES = {
     "kv_append.cu": ["-fmad=false"],
     "gamma_control.cu": ["-fmad=false"],
     "svpa_noalloc.cu": [],
+    "svpa_logits_api.cu": [],
 }
 
 

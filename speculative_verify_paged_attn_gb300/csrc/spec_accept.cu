@@ -423,10 +423,11 @@ __device__ int cta_last_positive(const Src &src, int lo, int hi, int *s_slot) {
 // Inverse-CDF draw after cluster_sum over the same weights: the first token
 // whose running mass exceeds u*S.  Returns true in the one CTA that made the
 // draw (tok, near set there); tok = -1 there when the row has no mass (then
-// it is CTA 0).  Every thread of every CTA calls this.
+// it is CTA 0).  near: u*S within 1e-6 * S of a running sum, or within
+// band_abs when that is given.  Every thread of every CTA calls this.
 template <int NI, class Src>
 __device__ bool cluster_draw(ClusterRow<NI> &st, const Src &src, const ClusterGeom &g, float u, int *tok_out,
-                             bool *near_out) {
+                             bool *near_out, double band_abs = -1.0) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // which CTA holds u*S: the first whose running total exceeds it
     if (threadIdx.x == 0) {
@@ -508,7 +509,7 @@ __device__ bool cluster_draw(ClusterRow<NI> &st, const Src &src, const ClusterGe
                 const int l = hit ? __ffs(hit) - 1 : 31;
                 if (lane == l) {
                     const float wj[4] = {wv.x, wv.y, wv.z, wv.w};
-                    const double band = kNearBand * st.S;
+                    const double band = band_abs >= 0.0 ? band_abs : kNearBand * st.S;
                     float c = G + excl;
                     int found = -1, lastpos = -1;
 #pragma unroll
@@ -769,6 +770,251 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     cluster_sync_all();
 }
 
+// ---------------------------------------------------------------- logits front-end
+// The sampler fed by logits: P_i = softmax(Lp_i / T), Q_i = softmax(Lq_i /
+// T_draft) are never written out.  "Speculative Decoding and KV-Cache
+// Compression", section 2.3 (the acceptance ratio takes softmax(logits)[x]);
+// "LOW-LATENCY INFERENCE: SPECULATIVE DECODING & PAGING", architecture
+// (target logits checked against draft logits).
+//
+// One cluster per sequence, each CTA on one slice of every row, as in the
+// linear sampler.  Pass 1 reads the slice of all 2 gamma + 1 rows once (the
+// whole slice of each row is requested into L2 up front), keeping per thread
+// a running max m and sum s of 2^((l - m) c), c = log2(e) / T; warps merge
+// (m, s) pairs in fp32, the CTA in fp64, and the CTAs exchange theirs through
+// distributed shared memory, each merging all of them in rank order so that
+// every CTA holds the same row maxima and normalisers.  The acceptance tests
+// then use P(x) = 2^((l_x - m) c) / S in fp64, and the residual row k is read
+// again (from L2) with its weights formed in fp32.
+//
+// fp32 formation errs by ~1.2e-7 * |log2 P| relative per probability (the
+// exponent's rounding; <= 1.3e-5 down to 2^-100) plus <= ~1e-5 in the
+// normaliser (partial sums of <= 128 terms), so decisions within 5e-5 of
+// their thresholds are reported as near: a test with |u Q - P| <= 5e-5 *
+// max(P, u Q) (or both below 2^-100), a residual with mass below 5e-5, a
+// draw within 5e-5 (absolute) of a running sum.
+constexpr int kMaxLogitRows = 2 * 32 + 1;
+constexpr double kLogitBand = 5e-5;
+constexpr double kLogitTiny = 7.888609052210118e-31;  // 2^-100
+
+// Four logits of a row from token t0 (a multiple of 4); -inf past V.
+__device__ __forceinline__ float4 load_logits4(const float *row, int t0, int V, bool vec) {
+    float4 w = make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F);
+    if (vec) {
+        if (t0 < V) w = __ldg(reinterpret_cast<const float4 *>(row + t0));
+    } else {
+        if (t0 < V) w.x = __ldg(row + t0);
+        if (t0 + 1 < V) w.y = __ldg(row + t0 + 1);
+        if (t0 + 2 < V) w.z = __ldg(row + t0 + 2);
+        if (t0 + 3 < V) w.w = __ldg(row + t0 + 3);
+    }
+    return w;
+}
+
+// Running (max m, sum s of 2^((l - m) c)) over four more logits.  -inf
+// entries add nothing; while m is -inf there is nothing to add.
+__device__ __forceinline__ void online_add4(float &m, float &s, float4 w, float c) {
+    const float lm = fmaxf(fmaxf(w.x, w.y), fmaxf(w.z, w.w));
+    if (lm > m) {
+        s = s * ex2_approx((m - lm) * c);
+        m = lm;
+    }
+    if (m > -CUDART_INF_F) {
+        s += ex2_approx((w.x - m) * c);
+        s += ex2_approx((w.y - m) * c);
+        s += ex2_approx((w.z - m) * c);
+        s += ex2_approx((w.w - m) * c);
+    }
+}
+
+// (m, s) <- the merge of (m, s) and (m2, s2).
+__device__ __forceinline__ void online_merge(float &m, float &s, float m2, float s2, float c) {
+    if (m2 > m) {
+        s = s * ex2_approx((m - m2) * c) + s2;
+        m = m2;
+    } else if (m2 > -CUDART_INF_F) {
+        s = s + s2 * ex2_approx((m2 - m) * c);
+    }
+}
+
+// Residual weights from logits: max(0, P - Q) in fp32 with P = 2^((l - mp)
+// cp) * ip (ip = 1/S rounded to fp32), likewise Q; P alone when q == nullptr.
+struct SrcLogits {
+    const float *p, *q;
+    int V;
+    bool vec;
+    float mp, cp, ip, mq, cq, iq;
+    __device__ float prob_p(float l) const { return ex2_approx((l - mp) * cp) * ip; }
+    __device__ float prob_q(float l) const { return ex2_approx((l - mq) * cq) * iq; }
+    __device__ float4 operator()(int t0) const {
+        if (t0 >= V) return make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 lp = load_logits4(p, t0, V, vec);
+        float4 w = make_float4(prob_p(lp.x), prob_p(lp.y), prob_p(lp.z), prob_p(lp.w));
+        if (q) {
+            const float4 lq = load_logits4(q, t0, V, vec);
+            w = make_float4(relu(w.x - prob_q(lq.x)), relu(w.y - prob_q(lq.y)), relu(w.z - prob_q(lq.z)),
+                            relu(w.w - prob_q(lq.w)));
+        }
+        return w;
+    }
+    __device__ float at(int t) const {
+        const float pv = prob_p(__ldg(p + t));
+        return q ? relu(pv - prob_q(__ldg(q + t))) : pv;
+    }
+};
+
+template <int NI>
+__global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
+    spec_accept_logits_cluster_kernel(const __grid_constant__ LogitsArgs a, int n_ctas) {
+    __shared__ ClusterRow<NI> st;
+    __shared__ float s_wm[kMaxLogitRows][kClWarps], s_ws[kMaxLogitRows][kClWarps];
+    __shared__ float s_cm[kMaxLogitRows], s_m[kMaxLogitRows];  // slice max (read by peers), row max
+    __shared__ double s_cs[kMaxLogitRows], s_S[kMaxLogitRows]; // slice sum at s_cm (read by peers), row sum
+    __shared__ int s_k, s_near;
+    __shared__ float s_u;
+    const ClusterGeom g = cluster_geom<NI>(a.V, n_ctas);
+    const int b = (int)(blockIdx.x / (unsigned)n_ctas);
+    const int gamma = a.gamma, V = a.V, rows = 2 * gamma + 1;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.lp) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.lq) & 15) == 0;
+    // rows 0..gamma: target logits; gamma+1..2 gamma: draft logits
+    auto row_ptr = [&](int r) -> const float * {
+        return r <= gamma ? a.lp + ((size_t)b * (gamma + 1) + r) * V
+                          : a.lq + ((size_t)b * gamma + (r - gamma - 1)) * V;
+    };
+    auto row_c = [&](int r) { return r <= gamma ? a.c_target : a.c_draft; };
+    if (threadIdx.x < (unsigned)rows) prefetch_slice(row_ptr(threadIdx.x), g.cta_lo, g.cta_hi, vec);
+
+    // ---- pass 1: per-row max and normaliser of this slice
+    constexpr int nb = NI < kLoadBatch ? NI : kLoadBatch;
+    for (int r = 0; r < rows; ++r) {
+        const float *row = row_ptr(r);
+        const float c = row_c(r);
+        float m = -CUDART_INF_F, s = 0.f;
+#pragma unroll
+        for (int i0 = 0; i0 < NI; i0 += nb) {
+            float4 w[nb];
+#pragma unroll
+            for (int j = 0; j < nb; ++j) w[j] = load_logits4(row, g.wbase + (i0 + j) * kStep + 4 * lane, V, vec);
+#pragma unroll
+            for (int j = 0; j < nb; ++j) online_add4(m, s, w[j], c);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+            online_merge(m, s, m2, s2, c);
+        }
+        if (lane == 0) {
+            s_wm[r][warp] = m;
+            s_ws[r][warp] = s;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < (unsigned)rows) {
+        const int r = threadIdx.x;
+        const float c = row_c(r);
+        float m = -CUDART_INF_F;
+        for (int w = 0; w < kClWarps; ++w) m = fmaxf(m, s_wm[r][w]);
+        double S = 0.0;
+        for (int w = 0; w < kClWarps; ++w)
+            if (s_wm[r][w] > -CUDART_INF_F) S += (double)s_ws[r][w] * (double)ex2_approx((s_wm[r][w] - m) * c);
+        s_cm[r] = m;
+        s_cs[r] = S;
+    }
+    cluster_sync_all();
+    if (threadIdx.x < (unsigned)rows) {
+        const int r = threadIdx.x;
+        const float c = row_c(r);
+        float m = -CUDART_INF_F;
+        for (int cc = 0; cc < n_ctas; ++cc) m = fmaxf(m, ld_peer_f32(&s_cm[r], (uint32_t)cc));
+        double S = 0.0;
+        for (int cc = 0; cc < n_ctas; ++cc) {
+            const float mc = ld_peer_f32(&s_cm[r], (uint32_t)cc);
+            if (mc > -CUDART_INF_F) S += ld_peer_f64(&s_cs[r], (uint32_t)cc) * (double)ex2_approx((mc - m) * c);
+        }
+        s_m[r] = m;
+        s_S[r] = S;
+        // a row with no finite logit, or with NaN / +inf
+        if (!(S > 0.0) || !(S < CUDART_INF) || !(m > -CUDART_INF_F) || !(m < CUDART_INF_F))
+            if (g.rank == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+    }
+    __syncthreads();
+
+    // ---- acceptance tests (fp64 on the fp32 exponentials); every CTA makes
+    // the same loads on the same merged statistics and reaches the same k
+    if (threadIdx.x < 32) {
+        bool rejected = false, close = false;
+        if (lane < gamma) {
+            int x = a.tokens[(size_t)b * gamma + lane];
+            if (x < 0 || x >= V) {
+                if (g.rank == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                x = 0;
+            }
+            const int rq = gamma + 1 + lane;
+            const float ep = ex2_approx((__ldg(row_ptr(lane) + x) - s_m[lane]) * a.c_target);
+            const float eq = ex2_approx((__ldg(row_ptr(rq) + x) - s_m[rq]) * a.c_draft);
+            const double P = (double)ep / s_S[lane];
+            const double uq = (double)__ldg(a.u_acc + (size_t)b * gamma + lane) * ((double)eq / s_S[rq]);
+            const double hi = fmax(P, uq);
+            rejected = !(uq <= P);
+            close = fabs(uq - P) <= kLogitBand * hi || hi < kLogitTiny;
+        }
+        const unsigned rej = __ballot_sync(0xffffffffu, rejected);
+        const unsigned cl = __ballot_sync(0xffffffffu, close);
+        if (lane == 0) {
+            const int k = rej ? __ffs(rej) - 1 : gamma;
+            const unsigned ran = k >= 31 ? 0xffffffffu : (2u << k) - 1u;  // tests 0..k
+            s_k = k;
+            s_near = (cl & ran) ? 1 : 0;
+            s_u = __ldg(a.u_s + b);
+        }
+    }
+    __syncthreads();
+
+    // ---- the draw from the residual of row k (or the bonus row)
+    const int k = s_k;
+    SrcLogits src;
+    src.p = row_ptr(k);
+    src.q = k < gamma ? row_ptr(gamma + 1 + k) : nullptr;
+    src.V = V;
+    src.vec = vec;
+    src.mp = s_m[k];
+    src.cp = a.c_target;
+    src.ip = (float)(1.0 / s_S[k]);
+    src.mq = k < gamma ? s_m[gamma + 1 + k] : 0.f;
+    src.cq = a.c_draft;
+    src.iq = k < gamma ? (float)(1.0 / s_S[gamma + 1 + k]) : 0.f;
+    bool near = s_near != 0;
+    double S = cluster_sum(st, src, g, 0);
+    if (src.q) {
+        if (S < kLogitBand) near = true;
+        if (!(S > 0.0)) {  // empty residual: draw from the target row (S is the same in every CTA)
+            src.q = nullptr;
+            S = cluster_sum(st, src, g, 1);
+        }
+    }
+    int tok;
+    bool nd;
+    if (cluster_draw(st, src, g, s_u, &tok, &nd, kLogitBand) && threadIdx.x == 0) {
+        if (tok < 0) {  // a row with no mass
+            raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+            tok = 0;
+        }
+        a.out_tokens[(size_t)b * (gamma + 1) + k] = tok;
+        if (a.near) a.near[b] = (near || nd) ? 1 : 0;
+    }
+    if (g.rank == 0) {
+        const int i = threadIdx.x;
+        if (i <= gamma && i != k)
+            a.out_tokens[(size_t)b * (gamma + 1) + i] = i < k ? a.tokens[(size_t)b * gamma + i] : -1;
+        if (i == 0) a.accepted_len[b] = k;
+    }
+    // no CTA leaves while a peer may still read its shared memory
+    cluster_sync_all();
+}
+
 int sm_count_cached() {
     static DeviceMemo<int> memo;
     int n = 0;
@@ -849,6 +1095,18 @@ cudaError_t launch_spec_accept(const AcceptArgs &a, cudaStream_t stream) {
 }
 
 int spec_accept_tree_max_vocab() { return kClMaxVocab; }
+
+cudaError_t launch_spec_accept_logits(const LogitsArgs &a, cudaStream_t stream) {
+    if (a.B <= 0) return cudaSuccess;
+    if (a.gamma < 1 || 2 * a.gamma + 1 > kMaxLogitRows || cluster_steps(a.B, a.V) == 0 ||
+        (long long)a.B * kClMaxCtas > 0x7fffffffLL)
+        return cudaErrorInvalidValue;
+    static void (*const kernels[])(LogitsArgs, int) = {
+        spec_accept_logits_cluster_kernel<1>, spec_accept_logits_cluster_kernel<2>,
+        spec_accept_logits_cluster_kernel<4>, spec_accept_logits_cluster_kernel<8>,
+        spec_accept_logits_cluster_kernel<16>, spec_accept_logits_cluster_kernel<32>};
+    return launch_cluster(kernels, a, a.V, a.B, 0, stream);
+}
 
 cudaError_t launch_spec_accept_tree(const TreeArgs &a, cudaStream_t stream) {
     if (a.B <= 0) return cudaSuccess;

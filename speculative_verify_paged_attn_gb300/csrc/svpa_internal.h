@@ -109,6 +109,23 @@ struct AcceptArgs {
 };
 cudaError_t launch_spec_accept(const AcceptArgs &a, cudaStream_t stream);
 
+// Rejection sampler fed by logits (P and Q formed in the kernel).
+struct LogitsArgs {
+    const float *lp;  // target logits [B, gamma+1, V]
+    const float *lq;  // draft logits [B, gamma, V]
+    const int32_t *tokens;
+    const float *u_acc;
+    const float *u_s;
+    int32_t *accepted_len;
+    int32_t *out_tokens;
+    uint8_t *near;
+    int32_t *err;
+    int32_t B, gamma, V;
+    float c_target, c_draft;  // log2(e) / temperature, > 0
+};
+cudaError_t launch_spec_accept_logits(const LogitsArgs &a, cudaStream_t stream);
+int spec_accept_tree_max_vocab();
+
 struct TreeArgs {
     const float *p;
     const float *q;

@@ -1,0 +1,62 @@
+// svpa_logits_api.cu -- the C ABI of the sampler's logits front-end: host-side
+// validation and the launch.  No function here allocates device memory.
+#include <cuda_runtime.h>
+#include <float.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <cmath>
+
+#include "../../include/svpa.h"
+#include "svpa_internal.h"
+
+using namespace svpa;
+
+extern "C" {
+
+svpa_status svpa_spec_accept_logits(int32_t batch, int32_t gamma, int32_t vocab, float temperature,
+                                    float draft_temperature, const float *target_logits,
+                                    const float *draft_logits, const int32_t *draft_tokens,
+                                    const float *u_accept, const float *u_sample, int32_t *accepted_len,
+                                    int32_t *out_tokens, uint8_t *near_boundary, void *workspace,
+                                    size_t workspace_bytes, int32_t *error_flag, void *stream) {
+    if (batch < 0 || gamma < 1 || gamma > 32 || vocab < 1) return SVPA_ERR_INVALID_ARG;
+    if (!std::isfinite(temperature) || !(temperature > 0.f) || !std::isfinite(draft_temperature) ||
+        !(draft_temperature > 0.f))
+        return SVPA_ERR_INVALID_ARG;
+    // log2(e) / T, rounded once to fp32; a temperature so small that it
+    // overflows fp32 is refused
+    const double ct = 1.4426950408889634 / (double)temperature;
+    const double cd = 1.4426950408889634 / (double)draft_temperature;
+    if (!(ct <= (double)FLT_MAX) || !(cd <= (double)FLT_MAX)) return SVPA_ERR_INVALID_ARG;
+    if (vocab > spec_accept_tree_max_vocab()) return SVPA_ERR_UNSUPPORTED;  // one cluster per row
+    if (batch > 0x7fffffff / 8) return SVPA_ERR_UNSUPPORTED;
+    if (batch == 0) return SVPA_OK;
+    if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_sample || !accepted_len ||
+        !out_tokens || !error_flag)
+        return SVPA_ERR_INVALID_ARG;
+    size_t need = 0;
+    svpa_spec_accept_workspace_size(batch, vocab, &need);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15) != 0)
+        return SVPA_ERR_WORKSPACE;
+    LogitsArgs a;
+    memset(&a, 0, sizeof a);
+    a.lp = target_logits;
+    a.lq = draft_logits;
+    a.tokens = draft_tokens;
+    a.u_acc = u_accept;
+    a.u_s = u_sample;
+    a.accepted_len = accepted_len;
+    a.out_tokens = out_tokens;
+    a.near = near_boundary;
+    a.err = error_flag;
+    a.B = batch;
+    a.gamma = gamma;
+    a.V = vocab;
+    a.c_target = (float)ct;
+    a.c_draft = (float)cd;
+    const cudaError_t e = launch_spec_accept_logits(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVPA_OK : SVPA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -28,7 +28,7 @@ STATUS = {0: "SVPA_OK", 1: "SVPA_ERR_INVALID_ARG", 2: "SVPA_ERR_UNSUPPORTED", 3:
 EXPORTS = ("svpa_attn_workspace_size", "svpa_attn_kernel", "svpa_paged_verify_attn", "svpa_spec_accept_workspace_size",
            "svpa_spec_accept", "svpa_spec_accept_tree", "svpa_block_table_commit", "svpa_check_error",
            "svpa_status_string", "svpa_version", "svpa_paged_verify_attn_noalloc", "svpa_kv_append",
-           "svpa_gamma_update", "svpa_attn_launches")
+           "svpa_gamma_update", "svpa_attn_launches", "svpa_spec_accept_logits")
 
 
 class SvpaError(RuntimeError):
@@ -66,6 +66,7 @@ def load(path: str = LIB_PATH):
     L.svpa_spec_accept_workspace_size.argtypes = [I, I, ctypes.POINTER(U)]
     L.svpa_spec_accept.argtypes = [I, I, I] + [P] * 9 + [U, P, P]
     L.svpa_spec_accept_tree.argtypes = [I, I, I] + [P] * 11 + [U, P, P]
+    L.svpa_spec_accept_logits.argtypes = [I, I, I, ctypes.c_float, ctypes.c_float] + [P] * 9 + [U, P, P]
     L.svpa_block_table_commit.argtypes = [I] * 5 + [P] * 7 + [I, P, P, I, I, I, P, P]
     L.svpa_paged_verify_attn_noalloc.argtypes = [ctypes.POINTER(AttnParams)] + [P] * 12
     L.svpa_kv_append.argtypes = [I] * 9 + [P] * 13
@@ -183,6 +184,22 @@ def spec_accept(p_probs, q_probs, draft_tokens, u_accept, u_sample, accepted_len
                                  _stream(stream))
     if check:
         _check(st, "svpa_spec_accept")
+    return st
+
+
+def spec_accept_logits(target_logits, draft_logits, draft_tokens, u_accept, u_sample, accepted_len, out_tokens,
+                       *, workspace, error_flag, temperature=1.0, draft_temperature=None, near_boundary=None,
+                       stream=None, check=True) -> int:
+    """The linear sampler on P = softmax(target_logits / T), Q = softmax(draft_logits / T_draft)."""
+    B, g1, V = target_logits.shape
+    td = temperature if draft_temperature is None else draft_temperature
+    st = load().svpa_spec_accept_logits(B, g1 - 1, V, float(temperature), float(td), _p(target_logits),
+                                        _p(draft_logits), _p(draft_tokens), _p(u_accept), _p(u_sample),
+                                        _p(accepted_len), _p(out_tokens), _p(near_boundary), _p(workspace),
+                                        workspace.numel() * workspace.element_size(), _p(error_flag),
+                                        _stream(stream))
+    if check:
+        _check(st, "svpa_spec_accept_logits")
     return st
 
 

@@ -336,6 +336,40 @@ def make_sampler(wl: Workload, seed: int, device="cpu", batch: Optional[int] = N
 
 
 @dataclass
+class LogitInputs:
+    lp: torch.Tensor         # fp32 [B, gamma+1, V] target logits
+    lq: torch.Tensor         # fp32 [B, gamma, V]   draft logits
+    tokens: torch.Tensor     # int32 [B, gamma] drawn from softmax(lq / draft_temperature)
+    u_accept: torch.Tensor   # fp32 [B, gamma]
+    u_sample: torch.Tensor   # fp32 [B]
+    temperature: float
+    draft_temperature: float
+
+
+def make_logits(wl: Workload, seed: int, device="cpu", batch: Optional[int] = None, vocab: Optional[int] = None,
+                gamma: Optional[int] = None, temperature: float = 1.0,
+                draft_temperature: Optional[float] = None) -> LogitInputs:
+    """Logits for the sampler's front-end: target N(0, s_t), draft = target +
+    N(0, s_d) (the recipe of make_sampler, before the softmax); draft tokens
+    drawn from softmax(draft / draft_temperature); uniforms U[0, 1)."""
+    B = batch if batch is not None else wl.batch
+    V = vocab if vocab is not None else wl.vocab
+    gm = gamma if gamma is not None else wl.gamma
+    td = temperature if draft_temperature is None else draft_temperature
+    dev = torch.device(device)
+    g = _gen(seed + 130363, dev)
+    lp = torch.randn((B, gm + 1, V), generator=g, device=dev) * wl.sigma_target
+    lq = lp[:, :gm, :] + torch.randn((B, gm, V), generator=g, device=dev) * wl.sigma_draft
+    q = torch.softmax(lq.reshape(B * gm, V).double() / td, dim=-1)
+    x = torch.multinomial(q, 1, generator=g).reshape(B, gm).to(torch.int32)
+    del q
+    ua = torch.rand((B, gm), generator=g, device=dev)
+    us = torch.rand((B,), generator=g, device=dev)
+    return LogitInputs(lp=lp.contiguous(), lq=lq.contiguous(), tokens=x, u_accept=ua, u_sample=us,
+                       temperature=float(temperature), draft_temperature=float(td))
+
+
+@dataclass
 class AppendInputs:
     """The paged cache before an append and the rows to append (torch tensors)."""
     wl: Workload

@@ -119,6 +119,17 @@ def test_null_pointers_rejected_before_launch(lib):
         assert lib.svpa_gamma_update(b, g, nz, None, None, nz, nz, nz, d, r, nz, None) == 1, args
     assert lib.svpa_gamma_update(2, 4, nz, None, nz, nz, nz, nz, F(0.9), F(0.0), nz, None) == 1
     assert lib.svpa_gamma_update(2, 4, None, None, None, nz, nz, nz, F(0.9), F(0.0), nz, None) == 1
+    # logits front-end: sizes, temperatures, vocabulary, pointers, workspace
+    for args in [(2, 0, 1000, F(1.0), F(1.0)), (2, 33, 1000, F(1.0), F(1.0)), (2, 4, 0, F(1.0), F(1.0)),
+                 (2, 4, 1000, F(0.0), F(1.0)), (2, 4, 1000, F(1.0), F(-0.5)),
+                 (2, 4, 1000, F(float("inf")), F(1.0)), (2, 4, 1000, F(1.0), F(float("nan"))),
+                 (2, 4, 1000, F(1e-39), F(1.0))]:
+        assert lib.svpa_spec_accept_logits(*args, *([nz] * 9), 256, nz, None) == 1, args
+    assert lib.svpa_spec_accept_logits(2, 4, 262145, F(1.0), F(1.0), *([nz] * 9), 256, nz, None) == 2
+    assert lib.svpa_spec_accept_logits(2, 4, 1000, F(1.0), F(1.0), *([None] * 9), 0, None, None) == 1
+    assert lib.svpa_spec_accept_logits(2, 4, 1000, F(1.0), F(1.0), *([nz] * 8), None, 0, nz, None) == 6
+    assert lib.svpa_spec_accept_logits(2, 4, 1000, F(1.0), F(1.0), *([nz] * 8), odd, 256, nz, None) == 6
+    assert lib.svpa_spec_accept_logits(0, 4, 1000, F(0.7), F(1.0), *([None] * 9), 0, None, None) == 0
     # empty batch is a no-op
     p0 = svpa.attn_params(0, 5, 4, 4, 64, 8, 16, split_pages=4)
     assert lib.svpa_paged_verify_attn(ctypes.byref(p0), *([None] * 11), 0, None, None) == 0
