@@ -27,6 +27,8 @@
 // __fmul_rn, which is never contracted.
 #include <math_constants.h>
 
+#include <algorithm>
+
 #include "svpa_device.cuh"
 #include "svpa_internal.h"
 
@@ -778,9 +780,9 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
 // (target logits checked against draft logits).
 //
 // One cluster per sequence, each CTA on one slice of every row, as in the
-// linear sampler.  Pass 1 reads the slice of all 2 gamma + 1 rows once (the
-// whole slice of each row is requested into L2 up front), keeping per thread
-// a running max m and sum s of 2^((l - m) c), c = log2(e) / T; warps merge
+// linear sampler.  Pass 1 reads the slice of all 2 gamma + 1 rows once,
+// streamed through a ring of shared-memory stages by bulk copies, keeping per
+// thread a running max m and sum s of 2^((l - m) c), c = log2(e) / T; warps merge
 // (m, s) pairs in fp32, the CTA in fp64, and the CTAs exchange theirs through
 // distributed shared memory, each merging all of them in rank order so that
 // every CTA holds the same row maxima and normalisers.  The acceptance tests
@@ -794,6 +796,7 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
 // max(P, u Q) (or both below 2^-100), a residual with mass below 5e-5, a
 // draw within 5e-5 (absolute) of a running sum.
 constexpr int kMaxLogitRows = 2 * 32 + 1;
+constexpr int kLgMaxStages = 12;  // bulk-copy ring stages (<= 16 KB each); the launch picks 3..12
 constexpr double kLogitBand = 5e-5;
 constexpr double kLogitTiny = 7.888609052210118e-31;  // 2^-100
 
@@ -824,6 +827,27 @@ __device__ __forceinline__ void online_add4(float &m, float &s, float4 w, float 
         s += ex2_approx((w.y - m) * c);
         s += ex2_approx((w.z - m) * c);
         s += ex2_approx((w.w - m) * c);
+    }
+}
+
+// Running (m, s) over sixteen more logits (four float4): the max of all
+// sixteen first, then their exponentials (independent of one another) summed
+// as a tree, so one thread keeps many exponentials in flight.
+__device__ __forceinline__ void online_add16(float &m, float &s, const float4 (&w)[4], float c) {
+    float lm = -CUDART_INF_F;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) lm = fmaxf(lm, fmaxf(fmaxf(w[i].x, w[i].y), fmaxf(w[i].z, w[i].w)));
+    if (lm > m) {
+        s = s * ex2_approx((m - lm) * c);
+        m = lm;
+    }
+    if (m > -CUDART_INF_F) {
+        float e[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            e[i] = (ex2_approx((w[i].x - m) * c) + ex2_approx((w[i].y - m) * c)) +
+                   (ex2_approx((w[i].z - m) * c) + ex2_approx((w[i].w - m) * c));
+        s += (e[0] + e[1]) + (e[2] + e[3]);
     }
 }
 
@@ -870,8 +894,11 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     __shared__ float s_wm[kMaxLogitRows][kClWarps], s_ws[kMaxLogitRows][kClWarps];
     __shared__ float s_cm[kMaxLogitRows], s_m[kMaxLogitRows];  // slice max (read by peers), row max
     __shared__ double s_cs[kMaxLogitRows], s_S[kMaxLogitRows]; // slice sum at s_cm (read by peers), row sum
-    __shared__ int s_k, s_near;
+    __shared__ float s_inv[kMaxLogitRows];                     // 1 / row sum, rounded to fp32
+    __shared__ int s_k, s_near, s_bad;
     __shared__ float s_u;
+    __shared__ __align__(8) uint64_t s_full[kLgMaxStages];
+    extern __shared__ float4 lg_ring[];  // a.stages stages of min(NI, 4) * 1024 tokens
     const ClusterGeom g = cluster_geom<NI>(a.V, n_ctas);
     const int b = (int)(blockIdx.x / (unsigned)n_ctas);
     const int gamma = a.gamma, V = a.V, rows = 2 * gamma + 1;
@@ -884,22 +911,8 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
                           : a.lq + ((size_t)b * gamma + (r - gamma - 1)) * V;
     };
     auto row_c = [&](int r) { return r <= gamma ? a.c_target : a.c_draft; };
-    if (threadIdx.x < (unsigned)rows) prefetch_slice(row_ptr(threadIdx.x), g.cta_lo, g.cta_hi, vec);
-
     // ---- pass 1: per-row max and normaliser of this slice
-    constexpr int nb = NI < kLoadBatch ? NI : kLoadBatch;
-    for (int r = 0; r < rows; ++r) {
-        const float *row = row_ptr(r);
-        const float c = row_c(r);
-        float m = -CUDART_INF_F, s = 0.f;
-#pragma unroll
-        for (int i0 = 0; i0 < NI; i0 += nb) {
-            float4 w[nb];
-#pragma unroll
-            for (int j = 0; j < nb; ++j) w[j] = load_logits4(row, g.wbase + (i0 + j) * kStep + 4 * lane, V, vec);
-#pragma unroll
-            for (int j = 0; j < nb; ++j) online_add4(m, s, w[j], c);
-        }
+    auto warp_publish = [&](int r, float m, float s, float c) {
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
             const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -909,6 +922,98 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
         if (lane == 0) {
             s_wm[r][warp] = m;
             s_ws[r][warp] = s;
+        }
+    };
+    if (vec) {
+        // The slice of every row streams through a ring of a.stages shared-
+        // memory stages filled by bulk copies (up to 16 KB each, issued by
+        // thread 0 ahead of the consumers): the copies in flight take no
+        // registers, so the whole ring's bytes are outstanding at once.
+        constexpr int CH = (NI < 4 ? NI : 4) * 1024;  // tokens per copy
+        float *ring = reinterpret_cast<float *>(lg_ring);
+        const int n_tok = g.cta_hi - g.cta_lo;
+        const int nch = (n_tok + CH - 1) / CH;
+        const int J = rows * nch;
+        const int S = a.stages;
+        if (threadIdx.x == 0) {
+            for (int st = 0; st < S; ++st) mbar_init(&s_full[st], 1);
+            fence_mbar_init();
+            s_bad = 0;
+        }
+        __syncthreads();
+        auto issue = [&](int j) {
+            const int r = j / nch;
+            const int t0 = g.cta_lo + (j - r * nch) * CH;
+            const uint32_t bytes = (uint32_t)min(CH, g.cta_hi - t0) * 4u;
+            const int st = j % S;
+            mbar_arrive_expect_tx(&s_full[st], bytes);
+            bulk_copy_g2s(ring + st * CH, row_ptr(r) + t0, bytes, &s_full[st]);
+        };
+        int issued = 0;  // thread 0: chunks issued so far
+        if (threadIdx.x == 0)
+            for (; issued < S && issued < J; ++issued) issue(issued);
+        int j = 0;
+        for (int r = 0; r < rows; ++r) {
+            const float c = row_c(r);
+            float m = -CUDART_INF_F, s = 0.f;
+            for (int cc = 0; cc < nch; ++cc, ++j) {
+                const int st = j % S;
+                const int n4 = min(CH, g.cta_hi - (g.cta_lo + cc * CH)) >> 2;
+                if (s_bad == 0) {
+                    if (mbar_wait(&s_full[st], (uint32_t)((j / S) & 1), a.err)) {
+                        const float4 *q4 = reinterpret_cast<const float4 *>(ring + st * CH);
+                        if constexpr (CH / 1024 == 4) {
+                            float4 w[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int f = (int)threadIdx.x + i * kClThreads;
+                                w[i] = f < n4 ? q4[f]
+                                              : make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F,
+                                                            -CUDART_INF_F);
+                            }
+                            online_add16(m, s, w, c);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < CH / 1024; ++i) {
+                                const int f = (int)threadIdx.x + i * kClThreads;
+                                if (f < n4) online_add4(m, s, q4[f], c);
+                            }
+                        }
+                    } else {
+                        s_bad = 1;
+                    }
+                }
+                __syncthreads();  // the stage is consumed: it may be refilled
+                if (threadIdx.x == 0 && s_bad == 0 && issued < J) issue(issued++);
+            }
+            warp_publish(r, m, s, c);
+        }
+        // after a wait that ran out of time, the copies still in flight (the
+        // latest of each stage) are waited for, bounded, before the CTA moves on
+        if (threadIdx.x == 0 && s_bad != 0)
+            for (int jj = issued - 1; jj >= 0 && jj >= issued - S; --jj)
+                mbar_wait(&s_full[jj % S], (uint32_t)((jj / S) & 1), a.err);
+    } else {
+        // rows that are not 16-byte aligned, or V % 4 != 0: per-thread loads
+        constexpr int nb = NI < kLoadBatch ? NI : kLoadBatch;
+        for (int r = 0; r < rows; ++r) {
+            const float *row = row_ptr(r);
+            const float c = row_c(r);
+            float m = -CUDART_INF_F, s = 0.f;
+#pragma unroll
+            for (int i0 = 0; i0 < NI; i0 += nb) {
+                float4 w[nb];
+#pragma unroll
+                for (int jn = 0; jn < nb; ++jn)
+                    w[jn] = load_logits4(row, g.wbase + (i0 + jn) * kStep + 4 * lane, V, false);
+                if constexpr (nb == 4) {
+                    online_add16(m, s, w, c);
+                } else {
+#pragma unroll
+                    for (int jn = 0; jn < nb; ++jn) online_add4(m, s, w[jn], c);
+                }
+            }
+            warp_publish(r, m, s, c);
         }
     }
     __syncthreads();
@@ -936,6 +1041,7 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
         }
         s_m[r] = m;
         s_S[r] = S;
+        s_inv[r] = (float)(1.0 / S);
         // a row with no finite logit, or with NaN / +inf
         if (!(S > 0.0) || !(S < CUDART_INF) || !(m > -CUDART_INF_F) || !(m < CUDART_INF_F))
             if (g.rank == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
@@ -955,11 +1061,13 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
             const int rq = gamma + 1 + lane;
             const float ep = ex2_approx((__ldg(row_ptr(lane) + x) - s_m[lane]) * a.c_target);
             const float eq = ex2_approx((__ldg(row_ptr(rq) + x) - s_m[rq]) * a.c_draft);
-            const double P = (double)ep / s_S[lane];
-            const double uq = (double)__ldg(a.u_acc + (size_t)b * gamma + lane) * ((double)eq / s_S[rq]);
+            // u Q <= P with both sides multiplied by Sp Sq > 0 (no fp64 division)
+            const double sp = s_S[lane], sq = s_S[rq];
+            const double P = (double)ep * sq;
+            const double uq = (double)__ldg(a.u_acc + (size_t)b * gamma + lane) * (double)eq * sp;
             const double hi = fmax(P, uq);
             rejected = !(uq <= P);
-            close = fabs(uq - P) <= kLogitBand * hi || hi < kLogitTiny;
+            close = fabs(uq - P) <= kLogitBand * hi || hi < kLogitTiny * (sp * sq);
         }
         const unsigned rej = __ballot_sync(0xffffffffu, rejected);
         const unsigned cl = __ballot_sync(0xffffffffu, close);
@@ -982,10 +1090,10 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     src.vec = vec;
     src.mp = s_m[k];
     src.cp = a.c_target;
-    src.ip = (float)(1.0 / s_S[k]);
+    src.ip = s_inv[k];
     src.mq = k < gamma ? s_m[gamma + 1 + k] : 0.f;
     src.cq = a.c_draft;
-    src.iq = k < gamma ? (float)(1.0 / s_S[gamma + 1 + k]) : 0.f;
+    src.iq = k < gamma ? s_inv[gamma + 1 + k] : 0.f;
     bool near = s_near != 0;
     double S = cluster_sum(st, src, g, 0);
     if (src.q) {
@@ -1045,14 +1153,15 @@ int cluster_steps(int B, int V) {
 
 template <class Args>
 cudaError_t launch_cluster(void (*const *kernels)(Args, int), const Args &a, int V, int B, size_t dyn_smem_per_step,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, size_t dyn_smem_total = 0) {
     const int ni = cluster_steps(B, V);
     const int chunk = kClWarps * ni * kStep;
     const int n = (V + chunk - 1) / chunk;
     int idx = 0;
     while ((1 << idx) < ni) ++idx;
     void (*kern)(Args, int) = kernels[idx];
-    const size_t smem = dyn_smem_per_step * (size_t)ni;
+    // dynamic shared memory: per step count, or a total the caller fixed
+    const size_t smem = dyn_smem_total ? dyn_smem_total : dyn_smem_per_step * (size_t)ni;
     if (smem > 0) {
         // the shared-memory opt-in of each step count, once per device
         static DeviceMemo<size_t> opted[8];
@@ -1105,7 +1214,21 @@ cudaError_t launch_spec_accept_logits(const LogitsArgs &a, cudaStream_t stream) 
         spec_accept_logits_cluster_kernel<1>, spec_accept_logits_cluster_kernel<2>,
         spec_accept_logits_cluster_kernel<4>, spec_accept_logits_cluster_kernel<8>,
         spec_accept_logits_cluster_kernel<16>, spec_accept_logits_cluster_kernel<32>};
-    return launch_cluster(kernels, a, a.V, a.B, 0, stream);
+    // The ring: stages of min(NI, 4) * 1024 tokens, as many as the CTAs that
+    // must share an SM leave shared memory for (228 KB per SM; 1 KB reserved
+    // and under 8 KB of static shared memory per CTA), 3 to 12.
+    const int ni = cluster_steps(a.B, a.V);
+    const long long grid = (long long)a.B * ((a.V + 1024 * ni - 1) / (1024 * ni));
+    const int sms = sm_count_cached();
+    const long long per_sm = std::max(1LL, std::min(4LL, (grid + sms - 1) / sms));
+    const size_t stage = (size_t)1024 * sizeof(float) * (ni < 4 ? ni : 4);
+    const size_t budget = (size_t)(233472 / per_sm) - 1024 - 8192;
+    const int rows = 2 * a.gamma + 1, chunks = rows * (ni < 4 ? 1 : ni / 4);
+    int stages = (int)std::min<size_t>(budget / stage, (size_t)kLgMaxStages);
+    stages = std::max(3, std::min(stages, std::max(3, chunks)));
+    LogitsArgs b = a;
+    b.stages = stages;
+    return launch_cluster(kernels, b, a.V, a.B, 0, stream, stage * (size_t)stages);
 }
 
 cudaError_t launch_spec_accept_tree(const TreeArgs &a, cudaStream_t stream) {

@@ -122,6 +122,7 @@ struct LogitsArgs {
     int32_t *err;
     int32_t B, gamma, V;
     float c_target, c_draft;  // log2(e) / temperature, > 0
+    int32_t stages;           // bulk-copy ring depth (set by the launch)
 };
 cudaError_t launch_spec_accept_logits(const LogitsArgs &a, cudaStream_t stream);
 int spec_accept_tree_max_vocab();
