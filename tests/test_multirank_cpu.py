@@ -55,6 +55,10 @@ def _worker(rank, world, port, outdir):
                                       sm_scale=wl.sm_scale, nthreads=1)
     k, toks, _, _ = oracle.spec_accept(smp.p[mine], smp.q[mine], smp.tokens[mine],
                                        smp.u_accept[mine], smp.u_sample[mine], nthreads=1)
+    # the sampler fed by logits on the shard's sequences
+    li = W.make_logits(wl.scaled(vocab=700), 57, temperature=0.8)
+    lk, lt, _ = oracle.spec_accept_logits(li.lp[mine], li.lq[mine], li.tokens[mine], li.u_accept[mine],
+                                          li.u_sample[mine], temperature=0.8, nthreads=1)
     # K/V append on this rank's own copy of the cache (replicas: each GPU
     # owns its pool), for its sequences only; the gathered rows of each
     # sequence must not depend on which rank appended it
@@ -71,7 +75,7 @@ def _worker(rank, world, port, outdir):
         rg = oracle.gamma_update(4, gk[step][mine], seq_state=st, decay=0.8)
         st = rg["seq_state"]
     parts = [None] * world
-    dist.all_gather_object(parts, (mine, out, k, toks, rows, st, rg["seq_gamma"]))
+    dist.all_gather_object(parts, (mine, out, k, toks, rows, st, rg["seq_gamma"], lk, lt))
     cpu = torch.device("cpu")
     mx = bench.max_over_ranks(float(rank + 1), world, cpu)
     sm = bench.sum_over_ranks(float(rank + 1), world, cpu)
@@ -82,10 +86,14 @@ def _worker(rank, world, port, outdir):
         full_k = np.zeros(B, np.int32)
         full_t = np.zeros((B, toks.shape[1]), np.int32)
         app, gst, gg = [None] * 6, np.zeros((6, 2), np.float32), np.zeros(6, np.int32)
-        for idx, o, kk, tt, rr, ss, gq in parts:
+        full_lk = np.zeros(B, np.int32)
+        full_lt = np.zeros((B, lt.shape[1]), np.int32)
+        for idx, o, kk, tt, rr, ss, gq, lkk, ltt in parts:
             full_out[idx] = o
             full_k[idx] = kk
             full_t[idx] = tt
+            full_lk[idx] = lkk
+            full_lt[idx] = ltt
             for j, b in enumerate(idx):
                 app[b] = rr[j]
             gst[idx], gg[idx] = ss, gq
@@ -98,6 +106,8 @@ def _worker(rank, world, port, outdir):
         np.save(os.path.join(outdir, "out.npy"), full_out)
         np.save(os.path.join(outdir, "k.npy"), full_k)
         np.save(os.path.join(outdir, "t.npy"), full_t)
+        np.save(os.path.join(outdir, "lk.npy"), full_lk)
+        np.save(os.path.join(outdir, "lt.npy"), full_lt)
     dist.barrier()
     dist.destroy_process_group()
 
@@ -117,6 +127,10 @@ def test_sharded_by_sequence_equals_single_process(tmp_path, oracle_mod):
     assert np.array_equal(np.load(tmp_path / "out.npy"), ref)
     assert np.array_equal(np.load(tmp_path / "k.npy"), k)
     assert np.array_equal(np.load(tmp_path / "t.npy"), toks)
+    li = W.make_logits(wl.scaled(vocab=700), 57, temperature=0.8)
+    lk, lt, _ = oracle_mod.spec_accept_logits(li.lp, li.lq, li.tokens, li.u_accept, li.u_sample, temperature=0.8)
+    assert np.array_equal(np.load(tmp_path / "lk.npy"), lk)
+    assert np.array_equal(np.load(tmp_path / "lt.npy"), lt)
     mx, sm = np.load(tmp_path / "reduce.npy")
     assert mx == 2.0 and sm == 3.0
     # the append and the per-sequence draft-length state, single process
