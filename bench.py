@@ -364,7 +364,7 @@ def time_logits(wl: W.Workload, seed: int, steps: int, warmup: int, stream):
     k = torch.empty(B, dtype=torch.int32, device=dev)
     toks = torch.empty((B, g1), dtype=torch.int32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws = torch.zeros(svpa.spec_accept_workspace_size(B, V), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(svpa.spec_accept_logits_workspace_size(B, g1 - 1, V), dtype=torch.uint8, device=dev)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
 
     def run():

@@ -251,9 +251,17 @@ svpa_status svpa_spec_accept(int32_t batch, int32_t gamma, int32_t vocab,
  *               5e-5, or u * (mass) within 5e-5 of a running sum.  With
  *               large vocabularies the running sums are closer together than
  *               that, so most draws are flagged.
- *  workspace    as for svpa_spec_accept (reserved)
+ *  workspace    16-byte aligned device buffer of at least
+ *               svpa_spec_accept_logits_workspace_size() bytes: the (max,
+ *               sum) pair of every 4096-token slab of every row, written by
+ *               the first kernel and read by the second
  *  gamma 1..32; 1 <= V <= 262144, else SVPA_ERR_UNSUPPORTED.
+ * Two kernels on `stream`: the slab statistics (one CTA per slab of a row),
+ * then the sampler clusters (a programmatic dependent launch of the first).
  */
+svpa_status svpa_spec_accept_logits_workspace_size(int32_t batch, int32_t gamma,
+                                                   int32_t vocab, size_t *bytes);
+
 svpa_status svpa_spec_accept_logits(int32_t batch, int32_t gamma, int32_t vocab,
                                     float temperature, float draft_temperature,
                                     const float *target_logits,

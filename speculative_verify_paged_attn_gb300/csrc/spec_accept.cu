@@ -779,24 +779,27 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
 // "LOW-LATENCY INFERENCE: SPECULATIVE DECODING & PAGING", architecture
 // (target logits checked against draft logits).
 //
-// One cluster per sequence, each CTA on one slice of every row, as in the
-// linear sampler.  Pass 1 reads the slice of all 2 gamma + 1 rows once,
-// streamed through a ring of shared-memory stages by bulk copies, keeping per
-// thread a running max m and sum s of 2^((l - m) c), c = log2(e) / T; warps merge
-// (m, s) pairs in fp32, the CTA in fp64, and the CTAs exchange theirs through
-// distributed shared memory, each merging all of them in rank order so that
-// every CTA holds the same row maxima and normalisers.  The acceptance tests
-// then use P(x) = 2^((l_x - m) c) / S in fp64, and the residual row k is read
-// again (from L2) with its weights formed in fp32.
+// Two kernels.  logit_stats_kernel reads every logit once, one CTA per
+// 4096-token slab of a row (thousands of independent CTAs, so the read runs
+// at memory speed whatever the batch), and writes the slab's max m and sum s
+// of 2^((l - m) c), c = log2(e) / T.  The sampler kernel, launched as its
+// programmatic dependent, is the linear sampler's cluster kernel: each CTA
+// merges every row's slab pairs in a fixed order (a warp butterfly, fp64
+// sums), so all CTAs of a cluster hold the same maxima and normalisers; the
+// acceptance tests use P(x) = 2^((l_x - m) c) / S in fp64 (cross-multiplied,
+// no division), and the residual row k is read again (from L2) with its
+// weights formed in fp32 for the cluster sum and draw.
 //
 // fp32 formation errs by ~1.2e-7 * |log2 P| relative per probability (the
 // exponent's rounding; <= 1.3e-5 down to 2^-100) plus <= ~1e-5 in the
-// normaliser (partial sums of <= 128 terms), so decisions within 5e-5 of
-// their thresholds are reported as near: a test with |u Q - P| <= 5e-5 *
-// max(P, u Q) (or both below 2^-100), a residual with mass below 5e-5, a
-// draw within 5e-5 (absolute) of a running sum.
+// normaliser (partial sums of 16 terms per thread, fp32 merges within a
+// slab, fp64 across slabs), so decisions within 5e-5 of their thresholds are
+// reported as near: a test with |u Q - P| <= 5e-5 * max(P, u Q) (or both below
+// 2^-100), a residual with mass below 5e-5, a draw within 5e-5 (absolute) of a
+// running sum.
 constexpr int kMaxLogitRows = 2 * 32 + 1;
-constexpr int kLgMaxStages = 12;  // bulk-copy ring stages (<= 16 KB each); the launch picks 3..12
+constexpr int kSlab = 4096;                          // tokens per statistics CTA
+constexpr int kMaxSlabs = kClMaxVocab / kSlab;       // 64
 constexpr double kLogitBand = 5e-5;
 constexpr double kLogitTiny = 7.888609052210118e-31;  // 2^-100
 
@@ -814,40 +817,21 @@ __device__ __forceinline__ float4 load_logits4(const float *row, int t0, int V, 
     return w;
 }
 
-// Running (max m, sum s of 2^((l - m) c)) over four more logits.  -inf
-// entries add nothing; while m is -inf there is nothing to add.
-__device__ __forceinline__ void online_add4(float &m, float &s, float4 w, float c) {
-    const float lm = fmaxf(fmaxf(w.x, w.y), fmaxf(w.z, w.w));
-    if (lm > m) {
-        s = s * ex2_approx((m - lm) * c);
-        m = lm;
-    }
-    if (m > -CUDART_INF_F) {
-        s += ex2_approx((w.x - m) * c);
-        s += ex2_approx((w.y - m) * c);
-        s += ex2_approx((w.z - m) * c);
-        s += ex2_approx((w.w - m) * c);
-    }
-}
-
-// Running (m, s) over sixteen more logits (four float4): the max of all
-// sixteen first, then their exponentials (independent of one another) summed
-// as a tree, so one thread keeps many exponentials in flight.
-__device__ __forceinline__ void online_add16(float &m, float &s, const float4 (&w)[4], float c) {
-    float lm = -CUDART_INF_F;
+// (m, s) of sixteen logits (four float4): the max of all sixteen, then their
+// exponentials (independent of one another) summed as a tree.  -inf entries
+// add nothing; an all -inf group gives (-inf, 0).
+__device__ __forceinline__ void group_stats16(const float4 (&w)[4], float c, float &m, float &s) {
+    m = -CUDART_INF_F;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) lm = fmaxf(lm, fmaxf(fmaxf(w[i].x, w[i].y), fmaxf(w[i].z, w[i].w)));
-    if (lm > m) {
-        s = s * ex2_approx((m - lm) * c);
-        m = lm;
-    }
+    for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fmaxf(w[i].x, w[i].y), fmaxf(w[i].z, w[i].w)));
+    s = 0.f;
     if (m > -CUDART_INF_F) {
         float e[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             e[i] = (ex2_approx((w[i].x - m) * c) + ex2_approx((w[i].y - m) * c)) +
                    (ex2_approx((w[i].z - m) * c) + ex2_approx((w[i].w - m) * c));
-        s += (e[0] + e[1]) + (e[2] + e[3]);
+        s = (e[0] + e[1]) + (e[2] + e[3]);
     }
 }
 
@@ -858,6 +842,49 @@ __device__ __forceinline__ void online_merge(float &m, float &s, float m2, float
         m = m2;
     } else if (m2 > -CUDART_INF_F) {
         s = s + s2 * ex2_approx((m2 - m) * c);
+    }
+}
+
+// Row r of sequence b: target rows 0..gamma, draft rows gamma+1..2 gamma.
+__device__ __forceinline__ const float *logit_row(const LogitsArgs &a, int b, int r) {
+    return r <= a.gamma ? a.lp + ((size_t)b * (a.gamma + 1) + r) * a.V
+                        : a.lq + ((size_t)b * a.gamma + (r - a.gamma - 1)) * a.V;
+}
+
+// One CTA per (sequence, row, slab): the slab's (max, sum) into a.stats.
+__global__ void __launch_bounds__(kClThreads) logit_stats_kernel(const __grid_constant__ LogitsArgs a) {
+    // the sampler may be scheduled now; it waits for this grid before reading
+    asm volatile("griddepcontrol.launch_dependents;");
+    __shared__ float s_wm[kClWarps], s_ws[kClWarps];
+    const int rows = 2 * a.gamma + 1;
+    const int slab = (int)(blockIdx.x % (unsigned)a.n_slabs);
+    const int br = (int)(blockIdx.x / (unsigned)a.n_slabs);  // b * rows + r
+    const int b = br / rows, r = br - b * rows;
+    const float *row = logit_row(a, b, r);
+    const float c = r <= a.gamma ? a.c_target : a.c_draft;
+    const bool vec = (a.V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.lp) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.lq) & 15) == 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float4 w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = load_logits4(row, slab * kSlab + 4 * ((int)threadIdx.x + i * kClThreads), a.V, vec);
+    float m, s;
+    group_stats16(w, c, m, s);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        online_merge(m, s, m2, s2, c);
+    }
+    if (lane == 0) {
+        s_wm[warp] = m;
+        s_ws[warp] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float mm = s_wm[0], ss = s_ws[0];
+        for (int i = 1; i < kClWarps; ++i) online_merge(mm, ss, s_wm[i], s_ws[i], c);
+        a.stats[(size_t)br * a.n_slabs + slab] = make_float2(mm, ss);
     }
 }
 
@@ -891,165 +918,51 @@ template <int NI>
 __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     spec_accept_logits_cluster_kernel(const __grid_constant__ LogitsArgs a, int n_ctas) {
     __shared__ ClusterRow<NI> st;
-    __shared__ float s_wm[kMaxLogitRows][kClWarps], s_ws[kMaxLogitRows][kClWarps];
-    __shared__ float s_cm[kMaxLogitRows], s_m[kMaxLogitRows];  // slice max (read by peers), row max
-    __shared__ double s_cs[kMaxLogitRows], s_S[kMaxLogitRows]; // slice sum at s_cm (read by peers), row sum
-    __shared__ float s_inv[kMaxLogitRows];                     // 1 / row sum, rounded to fp32
-    __shared__ int s_k, s_near, s_bad;
+    __shared__ float s_m[kMaxLogitRows], s_inv[kMaxLogitRows];  // row max, 1 / row sum (fp32)
+    __shared__ double s_S[kMaxLogitRows];                       // row sum
+    __shared__ int s_k, s_near;
     __shared__ float s_u;
-    __shared__ __align__(8) uint64_t s_full[kLgMaxStages];
-    extern __shared__ float4 lg_ring[];  // a.stages stages of min(NI, 4) * 1024 tokens
     const ClusterGeom g = cluster_geom<NI>(a.V, n_ctas);
     const int b = (int)(blockIdx.x / (unsigned)n_ctas);
     const int gamma = a.gamma, V = a.V, rows = 2 * gamma + 1;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.lp) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(a.lq) & 15) == 0;
-    // rows 0..gamma: target logits; gamma+1..2 gamma: draft logits
-    auto row_ptr = [&](int r) -> const float * {
-        return r <= gamma ? a.lp + ((size_t)b * (gamma + 1) + r) * V
-                          : a.lq + ((size_t)b * gamma + (r - gamma - 1)) * V;
-    };
-    auto row_c = [&](int r) { return r <= gamma ? a.c_target : a.c_draft; };
-    // ---- pass 1: per-row max and normaliser of this slice
-    auto warp_publish = [&](int r, float m, float s, float c) {
+    // the slab statistics are complete once the statistics grid is
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // ---- row maxima and normalisers: warp w merges rows w, w + 8, ...; lane l
+    // holds slabs l and l + 32; max by butterfly, then the rescaled sums in
+    // fp64 by butterfly (lane 0's order is the same in every CTA)
+    const int nsl = a.n_slabs;
+    for (int r = warp; r < rows; r += kClWarps) {
+        const float c = r <= gamma ? a.c_target : a.c_draft;
+        const float2 *ps = a.stats + ((size_t)b * rows + r) * nsl;
+        const float2 p0 = lane < nsl ? ps[lane] : make_float2(-CUDART_INF_F, 0.f);
+        const float2 p1 = lane + 32 < nsl ? ps[lane + 32] : make_float2(-CUDART_INF_F, 0.f);
+        float m = fmaxf(p0.x, p1.x);
 #pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-            const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-            online_merge(m, s, m2, s2, c);
+        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        double S = 0.0;
+        if (m > -CUDART_INF_F) {
+            if (p0.x > -CUDART_INF_F) S += (double)p0.y * (double)ex2_approx((p0.x - m) * c);
+            if (p1.x > -CUDART_INF_F) S += (double)p1.y * (double)ex2_approx((p1.x - m) * c);
         }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
         if (lane == 0) {
-            s_wm[r][warp] = m;
-            s_ws[r][warp] = s;
+            s_m[r] = m;
+            s_S[r] = S;
+            s_inv[r] = (float)(1.0 / S);
+            // a row with no finite logit, or with NaN / +inf
+            if (!(S > 0.0) || !(S < CUDART_INF) || !(m > -CUDART_INF_F) || !(m < CUDART_INF_F))
+                if (g.rank == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
         }
-    };
-    if (vec) {
-        // The slice of every row streams through a ring of a.stages shared-
-        // memory stages filled by bulk copies (up to 16 KB each, issued by
-        // thread 0 ahead of the consumers): the copies in flight take no
-        // registers, so the whole ring's bytes are outstanding at once.
-        constexpr int CH = (NI < 4 ? NI : 4) * 1024;  // tokens per copy
-        float *ring = reinterpret_cast<float *>(lg_ring);
-        const int n_tok = g.cta_hi - g.cta_lo;
-        const int nch = (n_tok + CH - 1) / CH;
-        const int J = rows * nch;
-        const int S = a.stages;
-        if (threadIdx.x == 0) {
-            for (int st = 0; st < S; ++st) mbar_init(&s_full[st], 1);
-            fence_mbar_init();
-            s_bad = 0;
-        }
-        __syncthreads();
-        auto issue = [&](int j) {
-            const int r = j / nch;
-            const int t0 = g.cta_lo + (j - r * nch) * CH;
-            const uint32_t bytes = (uint32_t)min(CH, g.cta_hi - t0) * 4u;
-            const int st = j % S;
-            mbar_arrive_expect_tx(&s_full[st], bytes);
-            bulk_copy_g2s(ring + st * CH, row_ptr(r) + t0, bytes, &s_full[st]);
-        };
-        int issued = 0;  // thread 0: chunks issued so far
-        if (threadIdx.x == 0)
-            for (; issued < S && issued < J; ++issued) issue(issued);
-        int j = 0;
-        for (int r = 0; r < rows; ++r) {
-            const float c = row_c(r);
-            float m = -CUDART_INF_F, s = 0.f;
-            for (int cc = 0; cc < nch; ++cc, ++j) {
-                const int st = j % S;
-                const int n4 = min(CH, g.cta_hi - (g.cta_lo + cc * CH)) >> 2;
-                if (s_bad == 0) {
-                    if (mbar_wait(&s_full[st], (uint32_t)((j / S) & 1), a.err)) {
-                        const float4 *q4 = reinterpret_cast<const float4 *>(ring + st * CH);
-                        if constexpr (CH / 1024 == 4) {
-                            float4 w[4];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int f = (int)threadIdx.x + i * kClThreads;
-                                w[i] = f < n4 ? q4[f]
-                                              : make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F,
-                                                            -CUDART_INF_F);
-                            }
-                            online_add16(m, s, w, c);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < CH / 1024; ++i) {
-                                const int f = (int)threadIdx.x + i * kClThreads;
-                                if (f < n4) online_add4(m, s, q4[f], c);
-                            }
-                        }
-                    } else {
-                        s_bad = 1;
-                    }
-                }
-                __syncthreads();  // the stage is consumed: it may be refilled
-                if (threadIdx.x == 0 && s_bad == 0 && issued < J) issue(issued++);
-            }
-            warp_publish(r, m, s, c);
-        }
-        // after a wait that ran out of time, the copies still in flight (the
-        // latest of each stage) are waited for, bounded, before the CTA moves on
-        if (threadIdx.x == 0 && s_bad != 0)
-            for (int jj = issued - 1; jj >= 0 && jj >= issued - S; --jj)
-                mbar_wait(&s_full[jj % S], (uint32_t)((jj / S) & 1), a.err);
-    } else {
-        // rows that are not 16-byte aligned, or V % 4 != 0: per-thread loads
-        constexpr int nb = NI < kLoadBatch ? NI : kLoadBatch;
-        for (int r = 0; r < rows; ++r) {
-            const float *row = row_ptr(r);
-            const float c = row_c(r);
-            float m = -CUDART_INF_F, s = 0.f;
-#pragma unroll
-            for (int i0 = 0; i0 < NI; i0 += nb) {
-                float4 w[nb];
-#pragma unroll
-                for (int jn = 0; jn < nb; ++jn)
-                    w[jn] = load_logits4(row, g.wbase + (i0 + jn) * kStep + 4 * lane, V, false);
-                if constexpr (nb == 4) {
-                    online_add16(m, s, w, c);
-                } else {
-#pragma unroll
-                    for (int jn = 0; jn < nb; ++jn) online_add4(m, s, w[jn], c);
-                }
-            }
-            warp_publish(r, m, s, c);
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x < (unsigned)rows) {
-        const int r = threadIdx.x;
-        const float c = row_c(r);
-        float m = -CUDART_INF_F;
-        for (int w = 0; w < kClWarps; ++w) m = fmaxf(m, s_wm[r][w]);
-        double S = 0.0;
-        for (int w = 0; w < kClWarps; ++w)
-            if (s_wm[r][w] > -CUDART_INF_F) S += (double)s_ws[r][w] * (double)ex2_approx((s_wm[r][w] - m) * c);
-        s_cm[r] = m;
-        s_cs[r] = S;
-    }
-    cluster_sync_all();
-    if (threadIdx.x < (unsigned)rows) {
-        const int r = threadIdx.x;
-        const float c = row_c(r);
-        float m = -CUDART_INF_F;
-        for (int cc = 0; cc < n_ctas; ++cc) m = fmaxf(m, ld_peer_f32(&s_cm[r], (uint32_t)cc));
-        double S = 0.0;
-        for (int cc = 0; cc < n_ctas; ++cc) {
-            const float mc = ld_peer_f32(&s_cm[r], (uint32_t)cc);
-            if (mc > -CUDART_INF_F) S += ld_peer_f64(&s_cs[r], (uint32_t)cc) * (double)ex2_approx((mc - m) * c);
-        }
-        s_m[r] = m;
-        s_S[r] = S;
-        s_inv[r] = (float)(1.0 / S);
-        // a row with no finite logit, or with NaN / +inf
-        if (!(S > 0.0) || !(S < CUDART_INF) || !(m > -CUDART_INF_F) || !(m < CUDART_INF_F))
-            if (g.rank == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
     }
     __syncthreads();
 
     // ---- acceptance tests (fp64 on the fp32 exponentials); every CTA makes
-    // the same loads on the same merged statistics and reaches the same k
+    // the same loads on the same statistics and reaches the same k
     if (threadIdx.x < 32) {
         bool rejected = false, close = false;
         if (lane < gamma) {
@@ -1059,8 +972,8 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
                 x = 0;
             }
             const int rq = gamma + 1 + lane;
-            const float ep = ex2_approx((__ldg(row_ptr(lane) + x) - s_m[lane]) * a.c_target);
-            const float eq = ex2_approx((__ldg(row_ptr(rq) + x) - s_m[rq]) * a.c_draft);
+            const float ep = ex2_approx((__ldg(logit_row(a, b, lane) + x) - s_m[lane]) * a.c_target);
+            const float eq = ex2_approx((__ldg(logit_row(a, b, rq) + x) - s_m[rq]) * a.c_draft);
             // u Q <= P with both sides multiplied by Sp Sq > 0 (no fp64 division)
             const double sp = s_S[lane], sq = s_S[rq];
             const double P = (double)ep * sq;
@@ -1084,8 +997,8 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     // ---- the draw from the residual of row k (or the bonus row)
     const int k = s_k;
     SrcLogits src;
-    src.p = row_ptr(k);
-    src.q = k < gamma ? row_ptr(gamma + 1 + k) : nullptr;
+    src.p = logit_row(a, b, k);
+    src.q = k < gamma ? logit_row(a, b, gamma + 1 + k) : nullptr;
     src.V = V;
     src.vec = vec;
     src.mp = s_m[k];
@@ -1153,7 +1066,7 @@ int cluster_steps(int B, int V) {
 
 template <class Args>
 cudaError_t launch_cluster(void (*const *kernels)(Args, int), const Args &a, int V, int B, size_t dyn_smem_per_step,
-                           cudaStream_t stream, size_t dyn_smem_total = 0) {
+                           cudaStream_t stream, size_t dyn_smem_total = 0, bool programmatic = false) {
     const int ni = cluster_steps(B, V);
     const int chunk = kClWarps * ni * kStep;
     const int n = (V + chunk - 1) / chunk;
@@ -1179,13 +1092,17 @@ cudaError_t launch_cluster(void (*const *kernels)(Args, int), const Args &a, int
     cfg.blockDim = dim3(kClThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)n;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // a programmatic dependent of the previous kernel on the stream: it may
+    // start early and waits (griddepcontrol.wait) before reading its results
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = programmatic ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, a, n);
 }
 
@@ -1205,30 +1122,27 @@ cudaError_t launch_spec_accept(const AcceptArgs &a, cudaStream_t stream) {
 
 int spec_accept_tree_max_vocab() { return kClMaxVocab; }
 
+size_t spec_accept_logits_stats_bytes(int B, int gamma, int V) {
+    return (size_t)B * (size_t)(2 * gamma + 1) * (size_t)((V + kSlab - 1) / kSlab) * sizeof(float2);
+}
+
 cudaError_t launch_spec_accept_logits(const LogitsArgs &a, cudaStream_t stream) {
     if (a.B <= 0) return cudaSuccess;
     if (a.gamma < 1 || 2 * a.gamma + 1 > kMaxLogitRows || cluster_steps(a.B, a.V) == 0 ||
-        (long long)a.B * kClMaxCtas > 0x7fffffffLL)
+        (long long)a.B * kClMaxCtas > 0x7fffffffLL || !a.stats)
         return cudaErrorInvalidValue;
+    LogitsArgs b = a;
+    b.n_slabs = (a.V + kSlab - 1) / kSlab;
+    const long long stat_ctas = (long long)a.B * (2 * a.gamma + 1) * b.n_slabs;
+    if (b.n_slabs > kMaxSlabs || stat_ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    logit_stats_kernel<<<(unsigned)stat_ctas, kClThreads, 0, stream>>>(b);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     static void (*const kernels[])(LogitsArgs, int) = {
         spec_accept_logits_cluster_kernel<1>, spec_accept_logits_cluster_kernel<2>,
         spec_accept_logits_cluster_kernel<4>, spec_accept_logits_cluster_kernel<8>,
         spec_accept_logits_cluster_kernel<16>, spec_accept_logits_cluster_kernel<32>};
-    // The ring: stages of min(NI, 4) * 1024 tokens, as many as the CTAs that
-    // must share an SM leave shared memory for (228 KB per SM; 1 KB reserved
-    // and under 8 KB of static shared memory per CTA), 3 to 12.
-    const int ni = cluster_steps(a.B, a.V);
-    const long long grid = (long long)a.B * ((a.V + 1024 * ni - 1) / (1024 * ni));
-    const int sms = sm_count_cached();
-    const long long per_sm = std::max(1LL, std::min(4LL, (grid + sms - 1) / sms));
-    const size_t stage = (size_t)1024 * sizeof(float) * (ni < 4 ? ni : 4);
-    const size_t budget = (size_t)(233472 / per_sm) - 1024 - 8192;
-    const int rows = 2 * a.gamma + 1, chunks = rows * (ni < 4 ? 1 : ni / 4);
-    int stages = (int)std::min<size_t>(budget / stage, (size_t)kLgMaxStages);
-    stages = std::max(3, std::min(stages, std::max(3, chunks)));
-    LogitsArgs b = a;
-    b.stages = stages;
-    return launch_cluster(kernels, b, a.V, a.B, 0, stream, stage * (size_t)stages);
+    return launch_cluster(kernels, b, a.V, a.B, 0, stream, 0, /*programmatic=*/true);
 }
 
 cudaError_t launch_spec_accept_tree(const TreeArgs &a, cudaStream_t stream) {

@@ -14,6 +14,15 @@ using namespace svpa;
 
 extern "C" {
 
+svpa_status svpa_spec_accept_logits_workspace_size(int32_t batch, int32_t gamma, int32_t vocab, size_t *bytes) {
+    if (!bytes || batch < 0 || gamma < 1 || gamma > 32 || vocab < 1) return SVPA_ERR_INVALID_ARG;
+    if (vocab > spec_accept_tree_max_vocab()) return SVPA_ERR_UNSUPPORTED;
+    // the (max, sum) pair of every 4096-token slab of every row
+    const size_t need = spec_accept_logits_stats_bytes(batch, gamma, vocab);
+    *bytes = need < 256 ? 256 : (need + 255) / 256 * 256;
+    return SVPA_OK;
+}
+
 svpa_status svpa_spec_accept_logits(int32_t batch, int32_t gamma, int32_t vocab, float temperature,
                                     float draft_temperature, const float *target_logits,
                                     const float *draft_logits, const int32_t *draft_tokens,
@@ -31,12 +40,13 @@ svpa_status svpa_spec_accept_logits(int32_t batch, int32_t gamma, int32_t vocab,
     if (!(ct <= (double)FLT_MAX) || !(cd <= (double)FLT_MAX)) return SVPA_ERR_INVALID_ARG;
     if (vocab > spec_accept_tree_max_vocab()) return SVPA_ERR_UNSUPPORTED;  // one cluster per row
     if (batch > 0x7fffffff / 8) return SVPA_ERR_UNSUPPORTED;
+    if ((long long)batch * (2 * gamma + 1) * ((vocab + 4095) / 4096) > 0x7fffffffLL) return SVPA_ERR_UNSUPPORTED;
     if (batch == 0) return SVPA_OK;
     if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_sample || !accepted_len ||
         !out_tokens || !error_flag)
         return SVPA_ERR_INVALID_ARG;
     size_t need = 0;
-    svpa_spec_accept_workspace_size(batch, vocab, &need);
+    svpa_spec_accept_logits_workspace_size(batch, gamma, vocab, &need);
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15) != 0)
         return SVPA_ERR_WORKSPACE;
     LogitsArgs a;
@@ -55,6 +65,7 @@ svpa_status svpa_spec_accept_logits(int32_t batch, int32_t gamma, int32_t vocab,
     a.V = vocab;
     a.c_target = (float)ct;
     a.c_draft = (float)cd;
+    a.stats = static_cast<float2 *>(workspace);
     const cudaError_t e = launch_spec_accept_logits(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SVPA_OK : SVPA_ERR_CUDA;
 }

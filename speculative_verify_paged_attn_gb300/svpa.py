@@ -28,7 +28,8 @@ STATUS = {0: "SVPA_OK", 1: "SVPA_ERR_INVALID_ARG", 2: "SVPA_ERR_UNSUPPORTED", 3:
 EXPORTS = ("svpa_attn_workspace_size", "svpa_attn_kernel", "svpa_paged_verify_attn", "svpa_spec_accept_workspace_size",
            "svpa_spec_accept", "svpa_spec_accept_tree", "svpa_block_table_commit", "svpa_check_error",
            "svpa_status_string", "svpa_version", "svpa_paged_verify_attn_noalloc", "svpa_kv_append",
-           "svpa_gamma_update", "svpa_attn_launches", "svpa_spec_accept_logits")
+           "svpa_gamma_update", "svpa_attn_launches", "svpa_spec_accept_logits",
+           "svpa_spec_accept_logits_workspace_size")
 
 
 class SvpaError(RuntimeError):
@@ -67,6 +68,7 @@ def load(path: str = LIB_PATH):
     L.svpa_spec_accept.argtypes = [I, I, I] + [P] * 9 + [U, P, P]
     L.svpa_spec_accept_tree.argtypes = [I, I, I] + [P] * 11 + [U, P, P]
     L.svpa_spec_accept_logits.argtypes = [I, I, I, ctypes.c_float, ctypes.c_float] + [P] * 9 + [U, P, P]
+    L.svpa_spec_accept_logits_workspace_size.argtypes = [I, I, I, ctypes.POINTER(U)]
     L.svpa_block_table_commit.argtypes = [I] * 5 + [P] * 7 + [I, P, P, I, I, I, P, P]
     L.svpa_paged_verify_attn_noalloc.argtypes = [ctypes.POINTER(AttnParams)] + [P] * 12
     L.svpa_kv_append.argtypes = [I] * 9 + [P] * 13
@@ -185,6 +187,13 @@ def spec_accept(p_probs, q_probs, draft_tokens, u_accept, u_sample, accepted_len
     if check:
         _check(st, "svpa_spec_accept")
     return st
+
+
+def spec_accept_logits_workspace_size(batch: int, gamma: int, vocab: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().svpa_spec_accept_logits_workspace_size(batch, gamma, vocab, ctypes.byref(n)),
+           "svpa_spec_accept_logits_workspace_size")
+    return n.value
 
 
 def spec_accept_logits(target_logits, draft_logits, draft_tokens, u_accept, u_sample, accepted_len, out_tokens,

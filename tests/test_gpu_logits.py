@@ -44,7 +44,7 @@ def gpu_run(li, offset=0):
     toks = torch.full((B, g1), -7, dtype=torch.int32, device=DEV)
     nb = torch.full((B,), 7, dtype=torch.uint8, device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    ws = torch.zeros(svpa.spec_accept_workspace_size(B, V), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(svpa.spec_accept_logits_workspace_size(B, g1 - 1, V), dtype=torch.uint8, device=DEV)
     svpa.spec_accept_logits(dev(li.lp), dev(li.lq), li.tokens.to(DEV), li.u_accept.to(DEV), li.u_sample.to(DEV),
                             k, toks, workspace=ws, error_flag=err, temperature=li.temperature,
                             draft_temperature=li.draft_temperature, near_boundary=nb)
@@ -173,7 +173,7 @@ def test_graph_replay_matches_eager():
     k = torch.empty(B, dtype=torch.int32, device=DEV)
     toks = torch.empty((B, g1), dtype=torch.int32, device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    ws = torch.zeros(svpa.spec_accept_workspace_size(B, V), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(svpa.spec_accept_logits_workspace_size(B, g1 - 1, V), dtype=torch.uint8, device=DEV)
     run = lambda: svpa.spec_accept_logits(*ins, k, toks, workspace=ws, error_flag=err, temperature=0.9)
     run()
     torch.cuda.synchronize()
