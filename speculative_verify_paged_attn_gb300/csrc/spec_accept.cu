@@ -23,6 +23,10 @@
 // scalar operations per CTA.  Vocabularies beyond 262144 tokens take a
 // one-CTA-per-row kernel.
 //
+// Also here: the draft-tree sampler on the same cluster split, and the
+// linear sampler fed by logits (softmax rows formed in the kernels: slab
+// statistics, then the cluster sampler on a logits weight source).
+//
 // This file is compiled with -fmad=false; the acceptance product also uses
 // __fmul_rn, which is never contracted.
 #include <math_constants.h>
