@@ -31,8 +31,6 @@
 // __fmul_rn, which is never contracted.
 #include <math_constants.h>
 
-#include <algorithm>
-
 #include "svpa_device.cuh"
 #include "svpa_internal.h"
 
@@ -1070,15 +1068,14 @@ int cluster_steps(int B, int V) {
 
 template <class Args>
 cudaError_t launch_cluster(void (*const *kernels)(Args, int), const Args &a, int V, int B, size_t dyn_smem_per_step,
-                           cudaStream_t stream, size_t dyn_smem_total = 0, bool programmatic = false) {
+                           cudaStream_t stream, bool programmatic = false) {
     const int ni = cluster_steps(B, V);
     const int chunk = kClWarps * ni * kStep;
     const int n = (V + chunk - 1) / chunk;
     int idx = 0;
     while ((1 << idx) < ni) ++idx;
     void (*kern)(Args, int) = kernels[idx];
-    // dynamic shared memory: per step count, or a total the caller fixed
-    const size_t smem = dyn_smem_total ? dyn_smem_total : dyn_smem_per_step * (size_t)ni;
+    const size_t smem = dyn_smem_per_step * (size_t)ni;
     if (smem > 0) {
         // the shared-memory opt-in of each step count, once per device
         static DeviceMemo<size_t> opted[8];
@@ -1146,7 +1143,7 @@ cudaError_t launch_spec_accept_logits(const LogitsArgs &a, cudaStream_t stream) 
         spec_accept_logits_cluster_kernel<1>, spec_accept_logits_cluster_kernel<2>,
         spec_accept_logits_cluster_kernel<4>, spec_accept_logits_cluster_kernel<8>,
         spec_accept_logits_cluster_kernel<16>, spec_accept_logits_cluster_kernel<32>};
-    return launch_cluster(kernels, b, a.V, a.B, 0, stream, 0, /*programmatic=*/true);
+    return launch_cluster(kernels, b, a.V, a.B, 0, stream, /*programmatic=*/true);
 }
 
 cudaError_t launch_spec_accept_tree(const TreeArgs &a, cudaStream_t stream) {
