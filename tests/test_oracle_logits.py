@@ -21,7 +21,9 @@ Pins that do not restate the oracle:
     positions 0 and 1, the mean first acceptance is 1 - TV(P, Q), and masked
     (-inf) target tokens are never emitted;
   * special cases: V = 1; an exact tie u Q = P is accepted and flagged; a draw
-    exactly on a boundary is flagged; invalid rows raise.
+    exactly on a boundary is flagged; invalid rows raise;
+  * the band itself: an emulation of the fp32 formation at V = 128256 errs by
+    well under half of it.
 """
 import numpy as np
 import pytest
@@ -226,3 +228,74 @@ def test_invalid_inputs_raise(oracle_mod, bad):
         T = 0.0
     with pytest.raises(oracle_mod.OracleError):
         run(oracle_mod, lp, lq, x, np.full((2, 1), 0.5), np.full(2, 0.5), temperature=T)
+
+
+def _fp32_formation(l, T, rng):
+    """P formed the way the GPU front-end forms it, emulated in numpy fp32:
+    per 16 logits the max, then 2^((l - m) c) (exp2 perturbed by up to two
+    units in the last place, the hardware approximation's bound) summed as a
+    tree; groups merged in fp32 within a 4096-token slab; slabs merged with
+    the rescaled sums in fp64; P = 2^((l - m) c) * fp32(1 / S)."""
+    f32 = np.float32
+    c = f32(np.log2(np.e) / T)
+
+    def ex2(x):
+        y = np.exp2(x.astype(f32)).astype(f32)
+        return (y * (1 + rng.uniform(-2, 2, y.shape) * 2.0 ** -23)).astype(f32)
+
+    V = l.shape[0]
+    pad = (-V) % 4096
+    lp = np.concatenate([l.astype(f32), np.full(pad, -np.inf, f32)])
+    g = lp.reshape(-1, 16)
+    gm = g.max(1)
+    fin = gm > -np.inf  # an all -inf group adds nothing (the kernel skips it)
+    ge = np.zeros_like(g)
+    ge[fin] = ex2((g[fin] - gm[fin, None]) * c)
+    while ge.shape[1] > 1:  # tree sum of the sixteen terms
+        ge = (ge[:, 0::2] + ge[:, 1::2]).astype(f32)
+    gs = ge[:, 0]
+
+    def scale(mi, mm):  # 2^((mi - mm) c), 0 for an empty part
+        out = np.zeros(mi.shape, f32)
+        ok = mi > -np.inf
+        out[ok] = ex2((mi[ok] - mm[ok]) * c)
+        return out
+
+    # groups -> slab, merged in fp32 pairwise (butterfly and warp order differ
+    # in order only)
+    m, s = gm.reshape(-1, 256), gs.reshape(-1, 256)
+    while m.shape[1] > 1:
+        m1, m2, s1, s2 = m[:, 0::2], m[:, 1::2], s[:, 0::2], s[:, 1::2]
+        mm = np.maximum(m1, m2)
+        s = (s1 * scale(m1, mm) + s2 * scale(m2, mm)).astype(f32)
+        m = mm
+    sm, ss = m[:, 0], s[:, 0]
+    M = sm.max()
+    S = float(np.sum(ss.astype(np.float64) * scale(sm, np.full_like(sm, M)).astype(np.float64)))
+    return (ex2((l.astype(f32) - M) * c) * f32(1.0 / S)).astype(f32)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_band_covers_fp32_formation(T):
+    """The 5e-5 band against an emulation of the fp32 formation at V = 128256:
+    the relative error of P over entries down to 2^-100 (the acceptance
+    test's) and the absolute error of the residual's running sums (the
+    draw's) must stay well inside it."""
+    rng = np.random.default_rng(29)
+    V = 128256
+    worst_rel, worst_cdf = 0.0, 0.0
+    for _ in range(6):
+        lp = (rng.standard_normal(V) * 3).astype(np.float32)
+        lq = (lp + rng.standard_normal(V) * 0.5).astype(np.float32)
+        P32, Q32 = _fp32_formation(lp, T, rng), _fp32_formation(lq, T, rng)
+        P64, Q64 = softmax64(lp, T), softmax64(lq, T)
+        sig = P64 > 2.0 ** -100
+        rel = float(np.max(np.abs(P32[sig] - P64[sig]) / P64[sig]))
+        r32 = np.maximum(P32.astype(np.float64) - Q32, 0)
+        r64 = np.maximum(P64 - Q64, 0)
+        cdf = float(np.max(np.abs(np.cumsum(r32) - np.cumsum(r64))))
+        assert np.isfinite(rel) and np.isfinite(cdf)
+        worst_rel, worst_cdf = max(worst_rel, rel), max(worst_cdf, cdf)
+    # an acceptance test compares P with u Q: both errors add
+    assert 0 < worst_rel and 2 * worst_rel < 5e-5 / 2, worst_rel
+    assert 0 < worst_cdf < 5e-5 / 10, worst_cdf
