@@ -390,6 +390,7 @@ def time_logits(wl: W.Workload, seed: int, steps: int, warmup: int, stream):
 
 
 LEAD_CYCLES = 200_000  # about 0.1 ms of GPU spin at GB300 clocks
+LAUNCH_BOUND_US = 10.0  # roofline time below which a call is flagged launch-bound
 
 
 def gpu_lead():
@@ -723,6 +724,13 @@ def main():
         rej = (kk < wl.gamma).to(torch.int64)
         samp_bytes = int((V * 4 * (1 + rej)).sum().item()) + st.B * 2 * wl.gamma * 4
     flops = 4 * wl.head_dim * st.n_q * wl.num_q_heads * int((st.cl0.long() + st.n_q).sum().item())
+    # a call whose algorithmic bytes would take under 10 us at the measured peak is
+    # launch/latency-bound: its fraction of peak is reported but says little about bandwidth
+    roof_us = lambda nbytes: nbytes / (peak * 1e9) * 1e6
+    launch_bound = {"attn": roof_us(st.attn_bytes) < LAUNCH_BOUND_US,
+                    "spec_accept": roof_us(samp_bytes) < LAUNCH_BOUND_US}
+    if logit is not None:
+        launch_bound["spec_accept_logits"] = roof_us(logit["bytes_per_launch"]) < LAUNCH_BOUND_US
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -764,6 +772,7 @@ def main():
             "percentiles_p10_p50_p90": {"attn_us": [round(x * 1e3, 2) for x in percentiles(attn_ms)],
                                         "spec_accept_us": [round(x * 1e3, 2) for x in percentiles(samp_ms)],
                                         "step_ms": percentiles(step_ms)},
+            "launch_bound": launch_bound,
             "graph_us_per_launch": {"attn": round(graph_attn_us, 2), "spec_accept": round(graph_samp_us, 2),
                                     "launches": 100, "l2": "not flushed between launches"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
