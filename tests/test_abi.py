@@ -158,3 +158,19 @@ def test_library_is_not_the_oracle(lib):
     from speculative_verify_paged_attn_gb300 import svpa
     data = open(svpa.LIB_PATH, "rb").read()
     assert b"oracle_" not in data
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++17")])
+def test_header_compiles_standalone(lang, std, tmp_path):
+    """include/svpa.h is usable from plain C and from C++ with no other header
+    (stdint/stddef only), with no warnings."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("use." + ("c" if lang == "c" else "cpp"))
+    src.write_text('#include "svpa.h"\nint main(void) { return (int)SVPA_OK; }\n')
+    r = subprocess.run([cc, std, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-I",
+                        os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
