@@ -552,7 +552,7 @@ int oracle_logits_draw_window(int B, int gamma, int V, double T_target, double T
 
 /* Tree helpers: a node is internal when some node names it as parent; its
  * draft row in Q is its rank among internal nodes in node order. */
-static int tree_depth_of(const int32_t *parent, int n, int node) {
+static int tree_depth_of(const int32_t *parent, int node) {
     int d = 0;
     while (node > 0) { node = parent[node]; ++d; }
     return d;
@@ -561,7 +561,7 @@ static int tree_depth_of(const int32_t *parent, int n, int node) {
 int oracle_tree_max_depth(const int32_t *parent, int n_nodes) {
     int md = 0;
     for (int i = 0; i < n_nodes; ++i) {
-        int d = tree_depth_of(parent, n_nodes, i);
+        int d = tree_depth_of(parent, i);
         if (d > md) md = d;
     }
     return md;
