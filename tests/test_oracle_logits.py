@@ -14,7 +14,8 @@ Pins that do not restate the oracle:
     in fp32 here) that would overflow exp() without the max subtracted;
   * on the same rows, the probability-input sampler (pinned on its own)
     makes the same decisions wherever neither flags a near-boundary case,
-    and its every draw lies in the draw window;
+    and its every draw lies in the draw window (fixed cases, and 150 random
+    shapes with temperatures and masked tokens);
   * the draw window of a worked example, and its definition (the running
     sums within the band) checked with numpy on larger rows;
   * Monte-Carlo: with drafts drawn from Q, the emitted tokens follow P at
@@ -299,3 +300,36 @@ def test_band_covers_fp32_formation(T):
     # an acceptance test compares P with u Q: both errors add
     assert 0 < worst_rel and 2 * worst_rel < 5e-5 / 2, worst_rel
     assert 0 < worst_cdf < 5e-5 / 10, worst_cdf
+
+
+def test_agrees_with_probability_sampler_on_random_shapes(oracle_mod):
+    """Property form of the agreement pin: random vocabularies (1..60), draft
+    lengths (1..6), temperatures and masked tokens; wherever neither sampler
+    flags a near decision they agree, and every draw of the probability
+    sampler lies in the logits oracle's window."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=150, deadline=None, derandomize=True)
+    @hyp.given(V=st.integers(1, 60), g=st.integers(1, 6), B=st.integers(1, 24),
+               T=st.floats(0.3, 3.0), Td=st.floats(0.3, 3.0), seed=st.integers(0, 2**31 - 1),
+               mask=st.booleans())
+    def check(V, g, B, T, Td, seed, mask):
+        rng = np.random.default_rng(seed)
+        lp = rng.normal(0, 2, (B, g + 1, V)).astype(np.float32)
+        lq = (lp[:, :g] + rng.normal(0, 0.7, (B, g, V))).astype(np.float32)
+        if mask and V > 1:  # mask one target token per row (never the whole row)
+            lp[np.arange(B)[:, None], np.arange(g + 1)[None, :], rng.integers(0, V, (B, g + 1))] = -np.inf
+        P, Q = softmax64(lp, T), softmax64(lq, Td)
+        x = draw_rows(rng, Q.reshape(-1, V)).reshape(B, g)
+        ua, us = rng.random((B, g)).astype(np.float32), rng.random(B).astype(np.float32)
+        k1, t1, n1 = run(oracle_mod, lp, lq, x, ua, us, temperature=T, draft_temperature=Td, band=1e-6)
+        k2, t2, n2, _ = oracle_mod.spec_accept(P.astype(np.float32), Q.astype(np.float32), x, ua, us)
+        ok = ~(n1 | n2)
+        assert np.array_equal(k1[ok], k2[ok])
+        assert np.array_equal(t1[ok], t2[ok])
+        lo, hi = oracle_mod.logits_draw_window(lp, lq, k2, us, temperature=T, draft_temperature=Td, band=1e-6)
+        drawn = t2[np.arange(B), k2]
+        assert np.all((lo <= drawn) & (drawn <= hi))
+
+    check()
