@@ -5,11 +5,14 @@ A step is one pass of the whole hot path over one batch of seeded synthetic
 input already resident in HBM: paged verification attention (the gamma+1
 queries of every sequence over its paged K/V history), the draft/target
 rejection sampler, and the block-table commit/rollback.  Default workload: the
-7B-shaped multi-head configuration (batch 32, contexts uniform in
-[512, 4096], gamma = 4, 32 heads, head_dim 128, bf16 pages; sampler vocabulary
-32000).
+70B-shaped grouped-query configuration, the largest that fits one GPU (batch
+64, contexts uniform in [8192, 32768], gamma = 5, 64 query / 8 kv heads,
+head_dim 128, bf16 pages; sampler vocabulary 128256).  The same run times the
+attention alone on the other workloads (7B-shape MHA, FP8 pages, FP8 pages
+with 64-element tile scales, draft tree with shared prefix): the line's
+`per_config` object.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 7b|70b|fp8|tree|tiny]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 70b|7b|fp8|fp8_t64|tree|tiny]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
 
 Prints one JSON line.  value = algorithmic K/V bytes per step / step time
@@ -431,6 +434,105 @@ def time_gamma(st: "Step", steps: int, warmup: int, stream) -> float:
     return sum(ms) / len(ms)
 
 
+PER_CONFIG = ("7b", "70b", "fp8", "fp8_t64", "tree")
+
+
+def time_attention_only(name: str, steps: int, warmup: int, peak: float):
+    """The attention call of workload `name` alone (its own seeded inputs,
+    one launch per step, L2 flushed before each): µs, KV GB/s, the roofline
+    fraction of its algorithmic bytes (K/V of valid tokens, FP8 scales,
+    queries, outputs, LSE, block ids) and the DRAM traffic recorded for it."""
+    wl = W.WORKLOADS[name]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    inp = W.make_attention(wl, W.SEEDS[name], device=dev, poison=False)
+    B, n_q, Hq, D = inp.q.shape
+    params = svpa.attn_params(B, n_q, Hq, wl.num_kv_heads, D, inp.block_table.shape[1], inp.num_blocks,
+                              kv_fp8=wl.kv_fp8, sm_scale=wl.sm_scale, scale_tile=wl.scale_tile)
+    ws = torch.zeros(svpa.attn_workspace_size(params), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty((B, n_q, Hq, D), dtype=torch.bfloat16, device=dev)
+    kp = inp.k_pool.view(torch.uint8) if wl.kv_fp8 else inp.k_pool
+    vp = inp.v_pool.view(torch.uint8) if wl.kv_fp8 else inp.v_pool
+    mask = None if inp.ancestor_mask is None else [int(x) for x in inp.ancestor_mask.cpu().tolist()]
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def run():
+        svpa.paged_verify_attn(params, inp.q, kp, vp, inp.block_table, inp.context_lens, out, workspace=ws,
+                               error_flag=err, k_scale=inp.k_scale, v_scale=inp.v_scale, ancestor_mask=mask)
+
+    for _ in range(warmup):
+        run()
+    ms = []
+    for _ in range(steps):
+        flush.fill_(1)
+        gpu_lead()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    assert svpa.check_error(err) == 0, f"device error in the {name} attention"
+    avg = sum(ms) / len(ms)
+    kv = inp.kv_bytes()
+    pages = int(((inp.context_lens.long() + n_q + 15) // 16).sum().item())
+    alg = kv + 2 * inp.q.numel() * 2 + B * n_q * Hq * 4 + pages * 4
+    kname = "pva_tc_kernel" if svpa.attn_kernel(params) == 2 else "pva_kernel"
+    return {"attn_us": round(avg * 1e3, 2), "kv_gbs": round(kv / (avg * 1e-3) / 1e9, 2),
+            "frac": round(alg / (avg * 1e-3) / 1e9 / peak, 4), "frac_kv": round(kv / (avg * 1e-3) / 1e9 / peak, 4),
+            "traffic": recorded_traffic(name, kname), "algorithmic_bytes_per_launch": alg, "kernel": kname,
+            "p10_p50_p90_us": [round(x * 1e3, 2) for x in percentiles(ms)],
+            "workload": config_dict(wl)["workload"]}
+
+
+def sampler_metrics(st: "Step", draws: int = 64, seed: int = 9090):
+    """Acceptance statistics of the workload's sampler rows (P, Q and drafts
+    fixed, `draws` fresh sets of uniforms, each one svpa call): the accepted
+    length histogram, the mean accepted length with its standard error, and,
+    for linear drafts, the expected accepted length of the same rows from
+    "LOW-LATENCY INFERENCE: SPECULATIVE DECODING & PAGING" (Verification
+    Acceptance Probabilities and Speedup Math): E[K] = sum_i prod_{j<=i}
+    alpha_j with alpha_j = min(1, P_j(x_j) / Q_j(x_j)), averaged over rows;
+    and how many final draws fell within 1e-6 of a CDF boundary."""
+    s, dev, B = st.smp, st.k.device, st.B
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    near = torch.zeros(B, dtype=torch.uint8, device=dev)
+    ks, nears = [], 0
+    for _ in range(draws):
+        ua = torch.rand(s.u_accept.shape, generator=g, device=dev)
+        us = torch.rand(s.u_sample.shape, generator=g, device=dev)
+        if st.tree:
+            svpa.spec_accept_tree(st.parent, s.p, s.q, s.tokens, ua, us, st.k, st.path, st.toks,
+                                  error_flag=st.err, near_boundary=near)
+        else:
+            svpa.spec_accept(s.p, s.q, s.tokens, ua, us, st.k, st.toks, workspace=st.sws, error_flag=st.err,
+                             near_boundary=near)
+        ks.append(st.k.clone())
+        nears += int(near.sum().item())
+    assert svpa.check_error(st.err) == 0, "device error in the sampler draws"
+    k = torch.stack(ks).double()
+    width = (st.path.shape[1] - 1) if st.tree else st.wl.gamma
+    hist = torch.bincount(k.long().flatten(), minlength=width + 1).tolist()
+    m = {"draws": draws * B, "rows": B, "accepted_len_hist": hist,
+         "mean_k": round(float(k.mean()), 5),
+         "mean_k_stderr": round(float(k.std() / (k.numel() ** 0.5)), 5),
+         "near_boundary": nears, "near_boundary_frac": round(nears / (draws * B), 6)}
+    if not st.tree:
+        x = s.tokens.long()
+        px = s.p[:, :-1, :].gather(2, x[:, :, None]).squeeze(2).double()
+        qx = s.q.gather(2, x[:, :, None]).squeeze(2).double()
+        alpha = torch.where(qx > 0, torch.clamp(px / qx.clamp(min=1e-300), max=1.0), torch.ones_like(px))
+        ek = torch.cumprod(alpha, dim=1).sum(dim=1)
+        m["expected_k_formula"] = round(float(ek.mean()), 5)
+        m["formula"] = "E[K] = sum_i prod_{j<=i} min(1, P_j(x_j)/Q_j(x_j)), mean over the rows"
+    else:
+        m["expected_k_formula"] = None
+        m["formula"] = "the pages' E[K] is for a chain of drafts; not evaluated for the tree sampler"
+    return m
+
+
 def percentiles(xs):
     """(p10, p50, p90) of a list of timings."""
     a = sorted(xs)
@@ -489,50 +591,77 @@ def sum_over_ranks(x: float, world: int, dev) -> float:
     return float(t.item())
 
 
-def cpu_baseline(wl: W.Workload, seed: int, budget_s: float = 12.0, nthreads: int = 0):
-    """The oracle, as it stands, on the host cores: attention over chunks of
-    the workload's sequences (wrapping around the batch) until the time budget
-    is used, plus the sampler and commit of those sequences.  Returns (GB/s,
-    cores, sample, sequences per second)."""
+def subset_to_cpu(inp: W.AttnInputs, smp: W.SamplerInputs, seqs):
+    """The selected sequences on the host: their queries, tables and lengths,
+    a compacted pool holding only their pages (block ids renumbered), and their
+    sampler rows.  (The oracle then needs no copy of a multi-GB pool.)"""
+    seqs = torch.as_tensor(list(seqs), dtype=torch.long, device=inp.q.device)
+    bt = inp.block_table[seqs]
+    used = torch.unique(bt[bt >= 0]).long()
+    remap = torch.full((inp.num_blocks,), -1, dtype=torch.int32, device=bt.device)
+    remap[used] = torch.arange(used.numel(), dtype=torch.int32, device=bt.device)
+    nbt = torch.where(bt >= 0, remap[bt.clamp(min=0).long()], bt)
+    n = int(used.numel())
+    d = dict(inp.__dict__)
+    d.update(q=inp.q[seqs].cpu(), block_table=nbt.cpu(), context_lens=inp.context_lens[seqs].cpu(),
+             k_pool=inp.k_pool[used].cpu(), v_pool=inp.v_pool[used].cpu(),
+             k_scale=None if inp.k_scale is None else inp.k_scale[used].cpu(),
+             v_scale=None if inp.v_scale is None else inp.v_scale[used].cpu(),
+             ancestor_mask=None if inp.ancestor_mask is None else inp.ancestor_mask.cpu(),
+             refcount=inp.refcount[used].cpu(), free_stack=torch.full((n,), -1, dtype=torch.int32),
+             free_top=0)
+    s = W.SamplerInputs(p=smp.p[seqs].cpu(), q=smp.q[seqs].cpu(), tokens=smp.tokens[seqs].cpu(),
+                        u_accept=smp.u_accept[seqs].cpu(), u_sample=smp.u_sample[seqs].cpu())
+    return W.AttnInputs(**d), s
+
+
+def cpu_baseline(wl: W.Workload, inp: W.AttnInputs, smp: W.SamplerInputs, seed: int, budget_s: float = 12.0,
+                 nthreads: int = 0):
+    """The oracle, as it stands, on the host cores: attention, sampler and
+    commit over chunks of the workload's sequences, taken in a seeded random
+    order (one sequence per thread and chunk, wrapping around the batch), until
+    the time budget is used.  Only the oracle calls are timed (not the copies
+    of a chunk's pages to the host).  Returns (GB/s, cores, sample, sequences
+    per second); the rate is K/V bytes of the sequences done over oracle time,
+    i.e. the subset extrapolated to the workload by bytes."""
     import oracle
     oracle.build()
-    inp = W.make_attention(wl, seed, device="cpu", poison=False)
-    smp = W.make_sampler(wl, seed, device="cpu")
     cores = oracle.max_threads() if nthreads == 0 else nthreads
-    am = None if inp.ancestor_mask is None else inp.ancestor_mask.numpy().view(np.uint64)
-    done_bytes, t_total, nseq = 0, 0.0, 0
     B = inp.q.shape[0]
     n_q = wl.n_q
     eb = 1 if wl.kv_fp8 else 2
+    order = torch.randperm(B, generator=torch.Generator().manual_seed(seed + 4242)).tolist()
     chunk = max(1, min(B, cores))  # one sequence per thread and pass
+    done_bytes, t_total, nseq = 0, 0.0, 0
     start, passes = 0, 0
     while t_total < budget_s:
-        sel = list(range(start, min(B, start + chunk)))
+        sel = order[start:min(B, start + chunk)]
+        c, s = subset_to_cpu(inp, smp, sel)
+        am = None if c.ancestor_mask is None else c.ancestor_mask.numpy().view(np.uint64)
         t0 = time.perf_counter()
-        oracle.paged_verify_attn(inp.q[sel], inp.k_pool, inp.v_pool, inp.block_table[sel],
-                                 inp.context_lens[sel], num_kv_heads=wl.num_kv_heads,
-                                 sm_scale=wl.sm_scale, kv_fp8=wl.kv_fp8, k_scale=inp.k_scale,
-                                 scale_tile=wl.scale_tile,
-                                 v_scale=inp.v_scale, ancestor_mask=am, nthreads=nthreads)
+        oracle.paged_verify_attn(c.q, c.k_pool, c.v_pool, c.block_table, c.context_lens,
+                                 num_kv_heads=wl.num_kv_heads, sm_scale=wl.sm_scale, kv_fp8=wl.kv_fp8,
+                                 k_scale=c.k_scale, scale_tile=wl.scale_tile, v_scale=c.v_scale,
+                                 ancestor_mask=am, nthreads=nthreads)
         if wl.tree_branching:
-            oracle.spec_accept_tree(np.array(wl.parent, np.int32), smp.p[sel], smp.q[sel],
-                                    smp.tokens[sel], smp.u_accept[sel], smp.u_sample[sel], nthreads=nthreads)
+            oracle.spec_accept_tree(np.array(wl.parent, np.int32), s.p, s.q, s.tokens, s.u_accept,
+                                    s.u_sample, nthreads=nthreads)
             k = np.zeros(len(sel), np.int32)
         else:
-            k, *_ = oracle.spec_accept(smp.p[sel], smp.q[sel], smp.tokens[sel], smp.u_accept[sel],
-                                       smp.u_sample[sel], nthreads=nthreads)
-        oracle.block_table_commit(inp.block_table[sel], inp.context_lens[sel], k, inp.refcount,
-                                  inp.free_stack, inp.free_top, n_q=n_q)
+            k, *_ = oracle.spec_accept(s.p, s.q, s.tokens, s.u_accept, s.u_sample, nthreads=nthreads)
+        oracle.block_table_commit(c.block_table, c.context_lens, k, c.refcount, c.free_stack, c.free_top,
+                                  n_q=n_q)
         t_total += time.perf_counter() - t0
-        T = inp.context_lens[sel].long() + n_q
+        T = c.context_lens.long() + n_q
         done_bytes += int(T.sum().item()) * wl.num_kv_heads * wl.head_dim * 2 * eb
         nseq += len(sel)
         start += chunk
         if start >= B:
             start, passes = 0, passes + 1
     gbs = done_bytes / t_total / 1e9
-    sample = (f"{nseq} sequence-steps ({passes} full passes over the {B} sequences, then part of one) of the "
-              f"{wl.name} workload (attention + sampler + commit), {t_total:.1f} s of oracle time")
+    sample = (f"{nseq} sequence-steps of the {wl.name} workload ({B} sequences, taken in a seeded random "
+              f"order, {chunk} per chunk; {passes} full passes), attention + sampler + commit, "
+              f"{t_total:.1f} s of oracle time; GB/s = K/V bytes of those sequences / oracle time")
     return gbs, cores, sample, nseq / t_total
 
 
@@ -541,8 +670,14 @@ def run_reference(args):
     if rank != 0:
         return
     wl = W.WORKLOADS[args.config]
+    seed = W.SEEDS[args.config]
+    # inputs drawn with the same generators as the GPU arm (on the GPU when
+    # there is one: a 5 GB pool is slow to draw on the host)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = W.make_attention(wl, seed, device=dev, poison=False)
+    smp = W.make_sampler(wl, seed, device=dev)
     budget = max(4.0, min(60.0, 3.0 * (args.steps + args.warmup)))
-    gbs, cores, sample, seq_per_s = cpu_baseline(wl, W.SEEDS[args.config], budget_s=budget)
+    gbs, cores, sample, seq_per_s = cpu_baseline(wl, inp, smp, seed, budget_s=budget)
     line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -575,7 +710,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="7b", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--config", default="70b", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the attention timings of the other workloads")
     ap.add_argument("--impl", default="svpa", choices=["svpa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--variant", type=int, default=0, choices=[0, 1, 2],
@@ -732,10 +869,20 @@ def main():
     if logit is not None:
         launch_bound["spec_accept_logits"] = roof_us(logit["bytes_per_launch"]) < LAUNCH_BOUND_US
 
+    smetrics = sampler_metrics(st)
+    per_config = None
+    if not args.no_per_config and not args.batch:
+        per_config = {}
+        for name in PER_CONFIG:
+            if name == args.config:
+                continue
+            per_config[name] = time_attention_only(name, K, args.warmup, peak)
+            torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, cores, sample, _ = cpu_baseline(wl, seed)
-        gbs1, _, sample1, _ = cpu_baseline(wl, seed, budget_s=4.0, nthreads=1)
+        gbs, cores, sample, _ = cpu_baseline(wl, st.inp, st.smp, seed)
+        gbs1, _, sample1, _ = cpu_baseline(wl, st.inp, st.smp, seed, budget_s=4.0, nthreads=1)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": sample, "single_thread": {"value": round(gbs1, 4), "sample": sample1}}
 
@@ -773,6 +920,8 @@ def main():
                                         "spec_accept_us": [round(x * 1e3, 2) for x in percentiles(samp_ms)],
                                         "step_ms": percentiles(step_ms)},
             "launch_bound": launch_bound,
+            "sampler_metrics": smetrics,
+            "per_config": per_config,
             "graph_us_per_launch": {"attn": round(graph_attn_us, 2), "spec_accept": round(graph_samp_us, 2),
                                     "launches": 100, "l2": "not flushed between launches"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,

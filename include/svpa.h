@@ -25,7 +25,9 @@
  *
  * Conventions shared by every entry point
  *  - Every pointer argument is a DEVICE pointer unless its comment says HOST.
- *    The caller owns and allocates all memory; the library allocates nothing.
+ *    The caller owns and allocates all memory; no entry point calls an
+ *    allocator (the one fixed array the library holds, the scratch of
+ *    svpa_paged_verify_attn_noalloc, is reserved when its module loads).
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *    void*; NULL = the legacy default stream).  Arguments are validated on the
  *    host before anything is enqueued; a non-OK status means nothing ran.
@@ -327,6 +329,10 @@ svpa_status svpa_spec_accept_tree(int32_t batch, int32_t n_nodes, int32_t vocab,
  *    dropped: block_table[b][i] = -1 and refcount[block] -= 1; a block whose
  *    count reaches 0 is pushed on the free stack (free_stack[(*free_top)++]).
  * The order of pushes within one call is unspecified.
+ * A sequence whose length, k or tree path is invalid (path_nodes[b][d] < d or
+ * >= n_q, k >= path_width, a page of the moved rows without a block) raises a
+ * device error bit and is left untouched: no row moves, no page is dropped
+ * and its length stays L.
  *
  * Sources: "LOW-LATENCY INFERENCE: SPECULATIVE DECODING & PAGING",
  * architecture diagram (commit to the KV-cache block table; discard the KV
@@ -491,11 +497,18 @@ svpa_status svpa_gamma_update(int32_t batch, int32_t gamma,
  * Its scratch is a fixed 32 MiB array inside the library, present on every
  * GPU that loads it until the process exits; a shape whose workspace
  * (svpa_attn_workspace_size) exceeds 32 MiB is rejected with
- * SVPA_ERR_WORKSPACE before anything is enqueued.  Nothing is allocated: no
+ * SVPA_ERR_WORKSPACE before anything is enqueued, as is any call that
+ * svpa_paged_verify_attn would reject.  No call makes an allocation: no
  * cudaMalloc, cudaFree or allocating library call.
  *  - The first call on a device looks up the array's device address (once per
- *    device, with that device current); make that first call before any
- *    stream capture.
+ *    device, with that device current).  Under CUDA's lazy module loading
+ *    (the default) that lookup loads the library's module on the device,
+ *    and loading reserves the 32 MiB array there: the driver's one
+ *    reservation for this entry point, which may block.  Make one call per
+ *    device at initialisation (a batch of 0 does not count: it returns
+ *    before the lookup), outside any stream capture, before the hot path.
+ *  - Only the runtime's primary context of each device is supported (the
+ *    address is cached per device index).
  *  - Every call on a device shares the one array and starts by clearing its
  *    counter words on `stream`; calls that overlap on the GPU (other streams,
  *    or other threads) race on it and must be serialised by the caller.
@@ -512,6 +525,28 @@ svpa_status svpa_paged_verify_attn_noalloc(const svpa_attn_params *p, const void
 /* Synchronise `stream`, read the device error word and map it to a status
  * (SVPA_OK when it is zero).  Does not clear the word. */
 svpa_status svpa_check_error(const int32_t *error_flag, void *stream);
+
+/*
+ * Diagnostic of the device-side wait limit.  Every wait inside the library's
+ * kernels is bounded in wall time: when the limit passes, the kernel sets
+ * SVPA_DEVERR_TIMEOUT in its error word, releases what it holds (tensor
+ * memory, copies in flight) and returns, so the GPU stays usable and
+ * svpa_check_error reports SVPA_ERR_TIMEOUT.  This call exercises that path on
+ * purpose: one CTA allocates tensor memory, waits with the kernels' own
+ * bounded mbarrier wait, under limit_ns, on a barrier that no thread ever
+ * arrives on (no copy is in flight), frees the tensor memory and returns.
+ * The pages this library follows have no counterpart of this entry point;
+ * they name stalls in production ("The Sub-Millisecond Speculative Decoding
+ * Meltdown", production failure scenarios) but no detection mechanism.
+ *  limit_ns    the wait's limit, 1 ns .. 10 s (the kernels use 2 s)
+ *  error_flag  int32 [1], device, zero before the call: SVPA_DEVERR_TIMEOUT
+ *              is OR-ed in when the wait runs out (always, by construction)
+ *  reached     int32 [1], device, zero before the call: 1 is added when the
+ *              wait returned as timed out (2 if it had completed)
+ * SVPA_ERR_INVALID_ARG for a null pointer or a limit outside that range.
+ * One kernel of one CTA on `stream`.
+ */
+svpa_status svpa_wait_selftest(uint64_t limit_ns, int32_t *error_flag, int32_t *reached, void *stream);
 
 /* Static description of a status code. */
 const char *svpa_status_string(svpa_status s);

@@ -12,8 +12,9 @@
 // For a draft tree the accepted path's K/V rows are first moved to the
 // linear slots L+1 .. L+k so that the committed history stays contiguous.
 //
-// One CTA per sequence.  Device-side checks raise error bits and skip the
-// offending page instead of trapping.
+// One CTA per sequence.  Device-side checks raise error bits instead of
+// trapping: a bad length or draft-tree path leaves that sequence untouched; a
+// bad block id among the dropped pages is skipped.
 #include "svpa_device.cuh"
 #include "svpa_internal.h"
 
@@ -24,19 +25,35 @@ namespace {
 __global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ CommitArgs a) {
     const int b = blockIdx.x;
     __shared__ int s_L, s_k, s_ok;
+    int32_t *table = a.block_table + (size_t)b * a.max_blocks;
     if (threadIdx.x == 0) {
         const int L = a.context_lens[b];
         const int k = a.accepted_len[b];
         const int had = (L + a.n_q + kBlockSize - 1) / kBlockSize;
-        s_ok = !(L < 0 || k < 0 || k >= a.n_q || had > a.max_blocks);
-        if (!s_ok) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+        int ok = !(L < 0 || k < 0 || k >= a.n_q || had > a.max_blocks);
+        if (!ok) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+        if (ok && a.path_nodes) {
+            // the whole path is checked before any row moves, so that a bad
+            // path leaves the sequence (rows, table, counts, length) untouched
+            const int32_t *path = a.path_nodes + (size_t)b * a.path_width;
+            ok = k < a.path_width;
+            for (int d = 1; ok && d <= k; ++d) {
+                const int pd = path[d];
+                ok = pd >= d && pd < a.n_q;
+                if (ok) {
+                    const int sb = table[(L + pd) / kBlockSize], db = table[(L + d) / kBlockSize];
+                    ok = sb >= 0 && sb < a.num_blocks && db >= 0 && db < a.num_blocks;
+                }
+            }
+            if (!ok) raise_error(a.err, SVPA_DEVERR_BAD_BLOCK);
+        }
+        s_ok = ok;
         s_L = L;
         s_k = k;
     }
     __syncthreads();
     if (!s_ok) return;
     const int L = s_L, k = s_k;
-    int32_t *table = a.block_table + (size_t)b * a.max_blocks;
 
     if (a.path_nodes) {
         // move slot L + path[d] to slot L + d for d = 1..k, in increasing d
@@ -47,12 +64,6 @@ __global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ Com
         for (int d = 1; d <= k; ++d) {
             const int src = L + path[d], dst = L + d;
             const int sb = table[src / kBlockSize], db = table[dst / kBlockSize];
-            const bool good = path[d] >= d && path[d] < a.n_q && sb >= 0 && sb < a.num_blocks &&
-                              db >= 0 && db < a.num_blocks;
-            if (!good) {
-                if (threadIdx.x == 0) raise_error(a.err, SVPA_DEVERR_BAD_BLOCK);
-                break;
-            }
             const int total = 2 * a.Hkv * words;
             for (int w = threadIdx.x; w < total; w += blockDim.x) {
                 const int which = w / (a.Hkv * words);

@@ -146,6 +146,31 @@ svpa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SVPA_OK : SVPA_
 
 }  // namespace
 
+namespace svpa {
+
+svpa_status check_attn_call(const svpa_attn_params *p, const void *q, const void *k_pool, const void *v_pool,
+                            const float *k_scale, const float *v_scale, const int32_t *block_table,
+                            const int32_t *context_lens, const uint64_t *ancestor_mask, const void *out,
+                            const int32_t *error_flag) {
+    if (p->batch > 65535) return SVPA_ERR_UNSUPPORTED;
+    const bool fp8 = p->kv_dtype == SVPA_KV_FP8_E4M3;
+    if (!q || !k_pool || !v_pool || !block_table || !context_lens || !out || !error_flag)
+        return SVPA_ERR_INVALID_ARG;
+    if (fp8 && (!k_scale || !v_scale)) return SVPA_ERR_INVALID_ARG;
+    if (p->scale_tile == 64 && (!aligned16(k_scale) || !aligned16(v_scale))) return SVPA_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(q) || !aligned16(out)) return SVPA_ERR_INVALID_ARG;
+    if (ancestor_mask) {
+        for (int j = 0; j < p->n_q; ++j) {
+            // a query always sees itself, never a later slot
+            if (!((ancestor_mask[j] >> j) & 1ull)) return SVPA_ERR_INVALID_ARG;
+            if (j + 1 < 64 && (ancestor_mask[j] >> (j + 1)) != 0ull) return SVPA_ERR_INVALID_ARG;
+        }
+    }
+    return SVPA_OK;
+}
+
+}  // namespace svpa
+
 extern "C" {
 
 const char *svpa_status_string(svpa_status s) {
@@ -196,25 +221,16 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
                                    const int32_t *block_table, const int32_t *context_lens,
                                    const uint64_t *ancestor_mask, void *out, float *lse, void *workspace,
                                    size_t workspace_bytes, int32_t *error_flag, void *stream) {
+    svpa::NvtxRange nvtx_range("svpa_paged_verify_attn");
     AttnPlan pl;
     svpa_status s = plan_attn(p, &pl);
     if (s != SVPA_OK) return s;
     if (p->batch == 0) return SVPA_OK;
-    if (p->batch > 65535) return SVPA_ERR_UNSUPPORTED;
+    s = svpa::check_attn_call(p, q, k_pool, v_pool, k_scale, v_scale, block_table, context_lens, ancestor_mask,
+                              out, error_flag);
+    if (s != SVPA_OK) return s;
     const bool fp8 = p->kv_dtype == SVPA_KV_FP8_E4M3;
-    if (!q || !k_pool || !v_pool || !block_table || !context_lens || !out || !error_flag)
-        return SVPA_ERR_INVALID_ARG;
-    if (fp8 && (!k_scale || !v_scale)) return SVPA_ERR_INVALID_ARG;
-    if (p->scale_tile == 64 && (!aligned16(k_scale) || !aligned16(v_scale))) return SVPA_ERR_INVALID_ARG;
-    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(q) || !aligned16(out)) return SVPA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < pl.bytes || !aligned16(workspace)) return SVPA_ERR_WORKSPACE;
-    if (ancestor_mask) {
-        for (int j = 0; j < p->n_q; ++j) {
-            // a query always sees itself, never a later slot
-            if (!((ancestor_mask[j] >> j) & 1ull)) return SVPA_ERR_INVALID_ARG;
-            if (j + 1 < 64 && (ancestor_mask[j] >> (j + 1)) != 0ull) return SVPA_ERR_INVALID_ARG;
-        }
-    }
     EncodeTiledFn enc = encode_fn();
     if (!enc) return SVPA_ERR_CUDA;
 
@@ -355,6 +371,7 @@ svpa_status svpa_spec_accept(int32_t batch, int32_t gamma, int32_t vocab, const 
                              const float *u_sample, int32_t *accepted_len, int32_t *out_tokens,
                              uint8_t *near_boundary, void *workspace, size_t workspace_bytes,
                              int32_t *error_flag, void *stream) {
+    svpa::NvtxRange nvtx_range("svpa_spec_accept");
     if (batch < 0 || gamma < 1 || gamma > 32 || vocab < 1) return SVPA_ERR_INVALID_ARG;
     if (batch == 0) return SVPA_OK;
     if (!p_probs || !q_probs || !draft_tokens || !u_accept || !u_sample || !accepted_len || !out_tokens ||
@@ -385,6 +402,7 @@ svpa_status svpa_spec_accept_tree(int32_t batch, int32_t n_nodes, int32_t vocab,
                                   const float *u_accept, const float *u_sample, int32_t *accepted_len,
                                   int32_t *path_nodes, int32_t *out_tokens, uint8_t *near_boundary,
                                   void *workspace, size_t workspace_bytes, int32_t *error_flag, void *stream) {
+    svpa::NvtxRange nvtx_range("svpa_spec_accept_tree");
     (void)workspace;
     (void)workspace_bytes;
     if (batch < 0 || n_nodes < 1 || n_nodes > kMaxNq || vocab < 1 || !parent) return SVPA_ERR_INVALID_ARG;
@@ -432,6 +450,7 @@ svpa_status svpa_block_table_commit(int32_t batch, int32_t n_q, int32_t block_si
                                     int32_t *free_top, const int32_t *path_nodes, int32_t path_width,
                                     void *k_pool, void *v_pool, int32_t num_kv_heads, int32_t head_dim,
                                     int32_t kv_dtype, int32_t *error_flag, void *stream) {
+    svpa::NvtxRange nvtx_range("svpa_block_table_commit");
     if (batch < 0 || n_q < 1 || n_q > kMaxNq || block_size != kBlockSize || max_blocks_per_seq < 1 ||
         num_blocks < 1)
         return SVPA_ERR_INVALID_ARG;
@@ -472,6 +491,7 @@ svpa_status svpa_kv_append(int32_t batch, int32_t n_new, int32_t num_kv_heads, i
                            const int32_t *context_lens, int32_t *refcount, int32_t *free_stack,
                            int32_t *free_top, void *k_pool, void *v_pool, float *k_scale, float *v_scale,
                            int32_t *error_flag, void *stream) {
+    svpa::NvtxRange nvtx_range("svpa_kv_append");
     if (batch < 0 || n_new < 1 || n_new > kMaxAppendRows || num_kv_heads < 1 || num_kv_heads > 4096 ||
         head_dim < 8 || head_dim % 8 != 0 || block_size != kBlockSize || max_blocks_per_seq < 1 ||
         num_blocks < 1 || (kv_dtype != SVPA_KV_BF16 && kv_dtype != SVPA_KV_FP8_E4M3))
@@ -516,6 +536,7 @@ svpa_status svpa_gamma_update(int32_t batch, int32_t gamma, const int32_t *accep
                               int32_t *seq_gamma_next, float *batch_state, int32_t *batch_gamma_next,
                               float *telemetry, float decay, float draft_cost_ratio, int32_t *error_flag,
                               void *stream) {
+    svpa::NvtxRange nvtx_range("svpa_gamma_update");
     if (batch < 1 || gamma < 1 || gamma > kMaxNq - 1 || !(decay >= 0.f && decay <= 1.f) ||
         !(draft_cost_ratio >= 0.f) || !accepted_len || !batch_state || !batch_gamma_next || !telemetry ||
         !error_flag || (seq_gamma_next && !seq_state))
@@ -536,6 +557,7 @@ svpa_status svpa_gamma_update(int32_t batch, int32_t gamma, const int32_t *accep
 }
 
 svpa_status svpa_check_error(const int32_t *error_flag, void *stream) {
+    svpa::NvtxRange nvtx_range("svpa_check_error");
     if (!error_flag) return SVPA_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(st) != cudaSuccess) return SVPA_ERR_CUDA;

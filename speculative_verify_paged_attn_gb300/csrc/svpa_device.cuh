@@ -99,13 +99,14 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait for phase `parity` of `bar`.  Returns false (and raises
-// SVPA_DEVERR_TIMEOUT) when the limit is reached.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err) {
+// SVPA_DEVERR_TIMEOUT) when `limit_ns` of wall time have passed.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             raise_error(err, SVPA_DEVERR_TIMEOUT);
             return false;
         }

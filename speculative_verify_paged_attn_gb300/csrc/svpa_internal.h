@@ -5,12 +5,23 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 #include <mutex>
 
 #include "../../include/svpa.h"
 
 namespace svpa {
+
+// An NVTX range around one C-ABI call, named after the entry point, so that a
+// profiler's timeline shows which library call enqueued which kernels.  With
+// no tool attached the NVTX calls return at once.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 // Host-side launch facts (function attributes, occupancy, SM count) are
 // computed once per device and remembered: a serving loop calls with the same
@@ -80,6 +91,14 @@ struct AttnLaunch {
     int ctas_per_sm;
     size_t smem;
 };
+
+// The attention call's pointer, alignment, batch and ancestor-mask checks
+// (everything but the shape, which plan checks, and the workspace): both
+// attention entry points run them before enqueueing anything.
+svpa_status check_attn_call(const svpa_attn_params *p, const void *q, const void *k_pool, const void *v_pool,
+                            const float *k_scale, const float *v_scale, const int32_t *block_table,
+                            const int32_t *context_lens, const uint64_t *ancestor_mask, const void *out,
+                            const int32_t *error_flag);
 
 // Launch the attention kernel matching (head_dim, fp8, row tiles).
 cudaError_t launch_paged_verify_attn(const AttnMaps &maps, const AttnArgs &a, int head_dim,

@@ -29,6 +29,7 @@ svpa_status svpa_spec_accept_logits(int32_t batch, int32_t gamma, int32_t vocab,
                                     const float *u_accept, const float *u_sample, int32_t *accepted_len,
                                     int32_t *out_tokens, uint8_t *near_boundary, void *workspace,
                                     size_t workspace_bytes, int32_t *error_flag, void *stream) {
+    svpa::NvtxRange nvtx_range("svpa_spec_accept_logits");
     if (batch < 0 || gamma < 1 || gamma > 32 || vocab < 1) return SVPA_ERR_INVALID_ARG;
     if (!std::isfinite(temperature) || !(temperature > 0.f) || !std::isfinite(draft_temperature) ||
         !(draft_temperature > 0.f))

@@ -17,6 +17,7 @@
 #include <mutex>
 
 #include "../../include/svpa.h"
+#include "svpa_internal.h"
 
 namespace {
 
@@ -31,7 +32,12 @@ std::mutex g_mu;
 void *g_scratch_ptr[kMaxDevices];  // device address of g_svpa_scratch, per device
 
 // Look up (once per device, with that device current) the device address of
-// the scratch array.
+// the scratch array.  With CUDA's lazy module loading (the default), this
+// first lookup is also what loads the library's module on that device, and
+// loading it reserves the 32 MiB array there: the one time this entry point
+// makes the driver reserve memory.  The cached address belongs to the
+// runtime's primary context of each device; contexts made through the driver
+// API are not supported.
 svpa_status scratch_for_current_device(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SVPA_ERR_CUDA;
@@ -55,14 +61,17 @@ svpa_status svpa_paged_verify_attn_noalloc(const svpa_attn_params *p, const void
                                            const int32_t *block_table, const int32_t *context_lens,
                                            const uint64_t *ancestor_mask, void *out, float *lse,
                                            int32_t *error_flag, void *stream) {
+    svpa::NvtxRange nvtx_range("svpa_paged_verify_attn_noalloc");
     size_t need = 0;
     svpa_status s = svpa_attn_workspace_size(p, &need);
     if (s != SVPA_OK) return s;
     if (need > kScratchBytes) return SVPA_ERR_WORKSPACE;  // the shape needs more than the fixed array
     if (p->batch == 0) return SVPA_OK;
-    if (!q || !k_pool || !v_pool || !block_table || !context_lens || !out || !error_flag)
-        return SVPA_ERR_INVALID_ARG;
-    if (p->kv_dtype == SVPA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return SVPA_ERR_INVALID_ARG;
+    // every check of the workspace entry point but the workspace itself, so
+    // that a rejected call has enqueued nothing (not even the clear below)
+    s = svpa::check_attn_call(p, q, k_pool, v_pool, k_scale, v_scale, block_table, context_lens, ancestor_mask,
+                              out, error_flag);
+    if (s != SVPA_OK) return s;
     void *ws = nullptr;
     s = scratch_for_current_device(&ws);
     if (s != SVPA_OK) return s;

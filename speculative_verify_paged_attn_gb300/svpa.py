@@ -29,7 +29,7 @@ EXPORTS = ("svpa_attn_workspace_size", "svpa_attn_kernel", "svpa_paged_verify_at
            "svpa_spec_accept", "svpa_spec_accept_tree", "svpa_block_table_commit", "svpa_check_error",
            "svpa_status_string", "svpa_version", "svpa_paged_verify_attn_noalloc", "svpa_kv_append",
            "svpa_gamma_update", "svpa_attn_launches", "svpa_spec_accept_logits",
-           "svpa_spec_accept_logits_workspace_size")
+           "svpa_spec_accept_logits_workspace_size", "svpa_wait_selftest")
 
 
 class SvpaError(RuntimeError):
@@ -74,6 +74,7 @@ def load(path: str = LIB_PATH):
     L.svpa_kv_append.argtypes = [I] * 9 + [P] * 13
     L.svpa_gamma_update.argtypes = [I, I] + [P] * 6 + [ctypes.c_float, ctypes.c_float, P, P]
     L.svpa_check_error.argtypes = [P, P]
+    L.svpa_wait_selftest.argtypes = [ctypes.c_uint64, P, P, P]
     L.svpa_status_string.argtypes = [I]
     L.svpa_status_string.restype = ctypes.c_char_p
     L.svpa_version.argtypes = []
@@ -192,7 +193,7 @@ def spec_accept(p_probs, q_probs, draft_tokens, u_accept, u_sample, accepted_len
 def spec_accept_logits_workspace_size(batch: int, gamma: int, vocab: int) -> int:
     n = ctypes.c_size_t(0)
     _check(load().svpa_spec_accept_logits_workspace_size(batch, gamma, vocab, ctypes.byref(n)),
-           "svpa_spec_accept_logits_workspace_size")
+           "svpa_spec_accept_logits_workspace_size", "svpa_wait_selftest")
     return n.value
 
 
@@ -278,6 +279,15 @@ def check_error(error_flag, stream=None) -> int:
     """svpa_check_error: synchronise the stream and map the device error word."""
     return load().svpa_check_error(_p(error_flag), _stream(stream))
 
+
+
+def wait_selftest(limit_ns: int, error_flag, reached, stream=None, check=True) -> int:
+    """svpa_wait_selftest: one kernel waits, bounded by limit_ns, on an
+    mbarrier no thread arrives on (the wait-limit path of every kernel)."""
+    st = load().svpa_wait_selftest(int(limit_ns), _p(error_flag), _p(reached), _stream(stream))
+    if check:
+        _check(st, "svpa_wait_selftest")
+    return st
 
 def status_string(status: int) -> str:
     return load().svpa_status_string(status).decode()

@@ -409,7 +409,7 @@ class AppendInputs:
 
 def make_append(wl: Workload, seed: int, device="cpu", batch: Optional[int] = None,
                 n_new: Optional[int] = None, shared_prefix: Optional[int] = None,
-                contexts=None) -> AppendInputs:
+                contexts=None, row_factors=(0.5, 1.0, 3.0)) -> AppendInputs:
     """Draw the cache state before an append of n_new rows (default n_q).
 
     The whole pages of the first shared_prefix tokens (default: the
@@ -419,8 +419,9 @@ def make_append(wl: Workload, seed: int, device="cpu", batch: Optional[int] = No
     the others hold a private copy of it.  Pages cover [0, L_b) only and every
     other block is on the free stack (shuffled); the pool holds enough blocks
     for every sequence to own all its pages after the append, plus 10%.
-    New rows are N(0, 1) times a per-row factor from {0.5, 1, 3}, so that FP8
-    page scales grow on some writes and not on others.  Pool slots that hold
+    New rows are N(0, 1) times a per-row factor drawn from `row_factors`
+    (default {0.5, 1, 3}, so that FP8 page scales grow on some writes and not
+    on others; (1,) gives plain N(0, 1) rows, as in the task's workloads).  Pool slots that hold
     no token are NaN (bf16) or the code of +448 (FP8): a kernel that took a
     page maximum over them would change the page's scale.
     """
@@ -500,8 +501,8 @@ def make_append(wl: Workload, seed: int, device="cpu", batch: Optional[int] = No
         k_pool = torch.where(mask, kf, nan).to(torch.bfloat16).contiguous()
         v_pool = torch.where(mask, vf, nan).to(torch.bfloat16).contiguous()
     del kf, vf
-    factor = torch.tensor([0.5, 1.0, 3.0], device=dev)[
-        torch.randint(0, 3, (B, n_new, 1, 1), generator=g_dev, device=dev)]
+    factor = torch.tensor(list(row_factors), dtype=torch.float32, device=dev)[
+        torch.randint(0, len(row_factors), (B, n_new, 1, 1), generator=g_dev, device=dev)]
     new_k = (torch.randn((B, n_new, Hkv, D), generator=g_dev, device=dev) * factor).to(torch.bfloat16)
     new_v = (torch.randn((B, n_new, Hkv, D), generator=g_dev, device=dev) * factor).to(torch.bfloat16)
     return AppendInputs(wl=wl, new_k=new_k, new_v=new_v, k_pool=k_pool, v_pool=v_pool,

@@ -112,3 +112,33 @@ def test_bad_accepted_len_reported():
     inp = W.make_attention(W.WORKLOADS["tiny"], 303, poison=False)
     st, _ = run_commit(inp, np.array([0, 9], np.int32))
     assert st == 1
+
+
+def test_tree_commit_bad_path_leaves_sequence_untouched():
+    # sequence 3's path names node 1 at depth 2 (a node's index is at least its
+    # depth in BFS order): the call reports it and leaves that sequence's rows,
+    # pages and length as they were; the other sequences commit normally
+    wl = W.WORKLOADS["tree"].scaled(batch=6, ctx_lo=1, ctx_hi=90, shared_prefix=32)
+    inp = W.make_attention(wl, 304, poison=False)
+    paths = np.full((6, 4), -1, np.int32)
+    paths[:, 0] = 0
+    paths[:, 1] = 2
+    paths[:, 2] = [c for c in range(len(wl.parent)) if wl.parent[c] == 2][0]
+    ks = np.full(6, 2, np.int32)
+    paths[3, 2] = 1
+    st, g = run_commit(inp, ks, paths)
+    assert st == 5  # SVPA_ERR_BAD_BLOCK
+    good = [0, 1, 2, 4, 5]
+    r = oracle.block_table_commit(inp.block_table[good], inp.context_lens[good], ks[good], inp.refcount,
+                                  inp.free_stack, inp.free_top, n_q=wl.n_q, path_nodes=paths[good],
+                                  k_pool=inp.k_pool.view(torch.int16).numpy(),
+                                  v_pool=inp.v_pool.view(torch.int16).numpy())
+    assert np.array_equal(g["block_table"][good], r["block_table"])
+    assert np.array_equal(g["context_lens"][good], r["context_lens"])
+    assert np.array_equal(g["block_table"][3], inp.block_table[3].numpy())
+    assert g["context_lens"][3] == int(inp.context_lens[3])
+    own = inp.block_table[3]
+    own = own[own >= 0].long()
+    assert torch.equal(g["k_pool"][own], inp.k_pool[own])
+    assert torch.equal(g["v_pool"][own], inp.v_pool[own])
+    assert np.array_equal(g["refcount"][own.numpy()], inp.refcount[own].numpy())

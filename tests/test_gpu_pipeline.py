@@ -72,32 +72,30 @@ def oracle_step(inp, q, smp, wl):
 
 
 CASES = {
-    # workload, contexts (private part), shared prefix (ends inside a page: copy-on-write)
-    "bf16": (W.WORKLOADS["7b"].scaled(num_q_heads=8, num_kv_heads=8, vocab=4000), (1, 3, 40, 250), 19),
-    "fp8": (W.WORKLOADS["fp8"].scaled(vocab=4000), (2, 6, 100, 700), 35),
-    "fp8_t64": (W.WORKLOADS["fp8_t64"].scaled(vocab=4000), (0, 9, 64, 300), 21),
+    # workload, contexts (private part), shared prefix (ends inside a page:
+    # copy-on-write), factors of the appended rows.  bf16 rows are N(0, 1) as
+    # in the task's workloads, so the plain attention bounds apply; the FP8
+    # cases keep rows of 0.5x, 1x and 3x N(0, 1), so that page and tile scales
+    # grow on some writes (requantised history) and not on others.
+    "bf16": (W.WORKLOADS["7b"].scaled(num_q_heads=8, num_kv_heads=8, vocab=4000), (1, 3, 40, 250), 19, (1.0,)),
+    "fp8": (W.WORKLOADS["fp8"].scaled(vocab=4000), (2, 6, 100, 700), 35, (0.5, 1.0, 3.0)),
+    "fp8_t64": (W.WORKLOADS["fp8_t64"].scaled(vocab=4000), (0, 9, 64, 300), 21, (0.5, 1.0, 3.0)),
 }
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_verification_step_matches_oracle(name):
-    wl, ctx, prefix = CASES[name]
-    inp = W.make_append(wl, 31 + len(name), contexts=ctx, shared_prefix=prefix)
+    wl, ctx, prefix, factors = CASES[name]
+    inp = W.make_append(wl, 31 + len(name), contexts=ctx, shared_prefix=prefix, row_factors=factors)
     B = inp.new_k.shape[0]
     g = torch.Generator().manual_seed(5)
     q = torch.randn((B, wl.n_q, wl.num_q_heads, wl.head_dim), generator=g).to(torch.bfloat16)
     smp = W.make_sampler(wl, 77, batch=B)
     got = gpu_step(inp, q, smp, wl)
     ref = oracle_step(inp, q, smp, wl)
-    # the appended rows are up to 3x N(0,1), so outputs reach ~8 where bf16's own
-    # rounding is 2^-8 relative: the bound scales with the value (bf16 output
-    # rounding plus the kernel's error), and rel-L2 as in the attention tests
-    if wl.kv_fp8:
-        U.assert_attention_close(got["out"], ref["out"], fp8=True, what=f"{name} attention after append")
-    else:
-        assert np.isfinite(got["out"]).all()
-        assert np.all(np.abs(got["out"] - ref["out"]) <= 2e-2 + 2.0 ** -8 * np.abs(ref["out"]))
-        assert U.rel_l2(got["out"], ref["out"]) <= U.BF16_REL_L2
+    # the attention bounds of every other parity test: bf16 max-abs 2e-2 and
+    # rel-L2 5e-3, FP8 rel-L2 3e-2
+    U.assert_attention_close(got["out"], ref["out"], fp8=wl.kv_fp8, what=f"{name} attention after append")
     assert np.array_equal(got["k"], ref["k"])
     ok = ~(got["near"] | ref["near"])
     assert np.array_equal(got["toks"][ok], ref["toks"][ok])
