@@ -193,7 +193,7 @@ def spec_accept(p_probs, q_probs, draft_tokens, u_accept, u_sample, accepted_len
 def spec_accept_logits_workspace_size(batch: int, gamma: int, vocab: int) -> int:
     n = ctypes.c_size_t(0)
     _check(load().svpa_spec_accept_logits_workspace_size(batch, gamma, vocab, ctypes.byref(n)),
-           "svpa_spec_accept_logits_workspace_size", "svpa_wait_selftest")
+           "svpa_spec_accept_logits_workspace_size")
     return n.value
 
 
@@ -278,7 +278,6 @@ def gamma_update(gamma, accepted_len, batch_state, batch_gamma, telemetry, *, er
 def check_error(error_flag, stream=None) -> int:
     """svpa_check_error: synchronise the stream and map the device error word."""
     return load().svpa_check_error(_p(error_flag), _stream(stream))
-
 
 
 def wait_selftest(limit_ns: int, error_flag, reached, stream=None, check=True) -> int:

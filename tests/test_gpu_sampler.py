@@ -154,20 +154,23 @@ def check_tree(parent, s, max_near):
     return k
 
 
-@pytest.mark.parametrize("batch", [4, 128])
-def test_tree_parity(batch):
+# The oracle's flagged fractions on these seeded inputs (deterministic): batch
+# 4 none, batch 128 2 rows (0.016); vocabulary 4099 none, 128256 1 of 6 rows.
+# The bounds sit just above them: a flood of flags would mean a bug.
+@pytest.mark.parametrize("batch,max_near", [(4, 0.01), (128, 0.02)])
+def test_tree_parity(batch, max_near):
     wl = W.WORKLOADS["tree"].scaled(batch=batch)
     s = W.make_sampler(wl, W.SEEDS["tree"], device="cpu")
-    check_tree(wl.parent, s, max_near=0.25)
+    check_tree(wl.parent, s, max_near=max_near)
 
 
-@pytest.mark.parametrize("vocab", [4099, 128256])
-def test_tree_vocab_edges(vocab):
+@pytest.mark.parametrize("vocab,max_near", [(4099, 0.01), (128256, 0.17)])
+def test_tree_vocab_edges(vocab, max_near):
     # 4099: rows not a multiple of 4 tokens (scalar loads); 128256: a
     # residual row larger than one CTA's shared memory would hold
     wl = W.WORKLOADS["tree"].scaled(batch=6)
     s = W.make_sampler(wl, 61, device="cpu", vocab=vocab)
-    check_tree(wl.parent, s, max_near=0.25)
+    check_tree(wl.parent, s, max_near=max_near)
 
 
 def test_tree_empty_residual_draws_from_target():
@@ -183,7 +186,7 @@ def test_tree_empty_residual_draws_from_target():
     p = s.p.clone()
     p[:, 0] = 0.5 * s.q[:, 0]
     t = W.SamplerInputs(p=p, q=s.q, tokens=tok, u_accept=ua, u_sample=s.u_sample)
-    k = check_tree(parent, t, max_near=0.25)
+    k = check_tree(parent, t, max_near=0.01)
     assert np.all(k == 0)
 
 
