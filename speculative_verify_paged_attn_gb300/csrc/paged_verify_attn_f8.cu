@@ -1,0 +1,1079 @@
+// paged_verify_attn_f8.cu -- paged verification attention over FP8-E4M3
+// pages on the 5th-generation tensor cores (tcgen05 + TMEM) for sm_103a, for
+// up to 64 query rows per kv head (grouped-query models: G * n_q <= 64).
+//
+// Same computation as paged_verify_attn.cu ("The Sub-Millisecond Speculative
+// Decoding Meltdown", section "Speculative Decoding Mechanics & The K-Token
+// Penalty": A = softmax(Q K^T * scale + M_tree) V over a paged K/V history;
+// "Custom FP8 Quantized Memory Block Layout": E4M3 pages with per-block
+// scales; "Triton CUDA Fused Speculative Tree-Verification Kernel": per-page
+// block lookup, K/V cache [blocks, heads, 16, dim], K/V scales [blocks,
+// heads], running max / sum; the implementation checklist's scales per
+// 64-element tile in the TILES instantiation).
+//
+// The tokens of a 128-token block (8 pages) sit on the 128 TMEM lanes and the
+// query rows on the columns, so that every softmax thread owns one token and
+// all four SM sub-partitions share the exponentials of a block however few
+// query rows a kv head has:
+//   S^T = K Q^T  tcgen05.mma kind::f8f6f4, A = the staged E4M3 K page bytes as
+//                they arrived (no conversion), B = the unit's queries split
+//                into two E4M3 terms (high part and remainder, at one
+//                power-of-two scale), two MMAs accumulating into one fp32
+//                TMEM tile [128 tokens x N rows];
+//   O^T += V^T P^T  tcgen05.mma kind::f16, A = the block's V converted
+//                exactly to f16 (MN-major), B = P^T in f16 written to shared
+//                memory by the softmax threads (MN-major), D = O^T [128 dims
+//                x N rows] in TMEM.
+// A page's K scale multiplies its scores in fp32; its V scale joins the
+// exponent (P' = 2^(x + log2 s_v - m')), so the f16 P' never exceeds 2^8 and
+// no scale range is refused; the row sums add P' / s_v in fp32.
+//
+// Work unit = (sequence, kv head, KV split); persistent CTAs, one per SM.
+// Warp roles (384 threads):
+//   warp 0     producer: units from an atomic counter; per block, 8 TMA page
+//              copies of K (2 KB each) into a 4-deep ring with the page
+//              scales (cp.async), V the same into a 2-deep ring; the unit's
+//              split queries (a 16 KB record written by qsplit_kernel) by one
+//              bulk copy;
+//   warp 1     MMA issuer (one thread) and TMEM owner;
+//   warps 2-3  V converters: E4M3 -> f16 in the MMA's layout, rows past the
+//              sequence's end and pages with scale 0 zeroed (TILES: each row
+//              half times its tile scale);
+//   warps 4-7  softmax, one thread per token (TMEM lane quadrant = warp % 4):
+//              row scores from TMEM, mask, lazy reference maxima shared in
+//              shared memory (re-computed only when some score passes the
+//              reference by 2^8, decided by one barrier vote), P^T to shared
+//              memory, per-thread partial row sums reduced at a unit's end;
+//   warps 8-11 epilogue, one thread per head dimension: O^T from TMEM to the
+//              output (or a split partial, merged by the last split's CTA).
+// All waits are bounded; nothing spins forever.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include <algorithm>
+#include <cstddef>
+#include <type_traits>
+
+#include "svpa_device.cuh"
+#include "svpa_internal.h"
+
+namespace svpa {
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kPB = 8;                   // pages per block
+constexpr int kNB = kPB * 16;            // tokens per block (128 TMEM lanes)
+constexpr int kPage8 = 16 * 128;         // one E4M3 (page, kv head) tile
+constexpr int kTile8 = kPB * kPage8;     // E4M3 block: 16 KB
+constexpr int kTile16 = kNB * kD * 2;    // f16 V block: 32 KB
+constexpr int kNK8 = 4, kNV8 = 2, kNV16 = 2;
+constexpr int kNMeta = 8;                // block descriptors in flight
+constexpr int kMaxN = 64;                // query rows per kv head (TMEM columns of a tile)
+constexpr int kPtTile = kNB * 128;       // P^T: 128 token rows of 64 f16
+constexpr int kThreads = 384;
+constexpr int kConvWarp0 = 2, kConvWarps = 2;
+constexpr int kSoftWarp0 = 4, kEpiWarp0 = 8, kEpiWarps = 4;
+constexpr uint32_t kStageArrivals = 1 + kPB;  // expect_tx + one cp.async scale per page
+constexpr int kTileScales = 16 * (kD / 64);   // tile scales of one (page, kv head)
+constexpr float kRescaleLog2 = 8.f;           // a new reference maximum when a score passes it by 2^8
+constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagEnd = 4;
+
+struct BlockMeta {
+    int32_t b, h, split, pos0, ntok, L, nsplit, flags;
+    float qsc;  // the unit's query scale
+    int32_t pad[3];
+};
+
+struct alignas(16) TileScales {  // TILES only: per block in flight, [page][slot * 2 + row half]
+    float k[kNMeta][kPB][kTileScales];
+    float v[kNV8][kPB][kTileScales];
+};
+struct NoTileScales {};
+
+template <bool TILES>
+struct SmemF8 {
+    uint8_t k8[kNK8][kTile8];        // 1024-aligned; A operand of S^T as staged
+    uint8_t v8[kNV8][kTile8];
+    uint8_t v16[kNV16][kTile16];     // A operand of O^T
+    uint8_t pt[2][kPtTile];          // B operand of O^T
+    uint8_t qs[2][kMaxN * 128];      // B operand of S^T: high and low query terms
+    float ksc[kNMeta][kPB];
+    float vsc[kNMeta][kPB];
+    float mref[2][kMaxN];            // reference maximum of each row (log2 units, V scale included),
+                                     // the current one and the next
+    float salpha[kMaxN];             // factor of each row when its reference changes
+    float red[4][kMaxN];
+    float2 stat[kMaxN];              // (reference maximum, row sum) of a finished unit
+    BlockMeta meta[kNMeta];
+    int32_t vid[kNMeta][kPB];
+    uint64_t k8_full[kNK8], k8_empty[kNK8];
+    uint64_t v8_full[kNV8], v8_empty[kNV8];
+    uint64_t v16_full[kNV16], v16_empty[kNV16];
+    uint64_t qs_full, qs_empty;
+    uint64_t s_full[2], s_empty[2];
+    uint64_t p_full[2], p_empty[2];
+    uint64_t o_full[2], o_empty[2];
+    uint64_t stat_full, stat_empty;
+    uint64_t soft_sync, epi_sync;    // group barriers of the softmax and of the epilogue warps
+    int32_t vote[2][4];              // the softmax warps' votes, by barrier phase parity
+    int32_t ep_b, ep_h, ep_split, ep_nsplit, ep_end;
+    uint32_t tmem_base;
+    int32_t last;
+    int32_t pad_[3];
+    typename std::conditional<TILES, TileScales, NoTileScales>::type ts;
+};
+
+static_assert(sizeof(SmemF8<false>) + 1024 <= 232448, "pva_f8_kernel shared memory");
+static_assert(sizeof(SmemF8<true>) + 1024 <= 232448, "pva_f8_kernel shared memory");
+static_assert(offsetof(SmemF8<true>, ts) % 16 == 0, "bulk copies land on 16-byte boundaries");
+
+// the split-query record of one (sequence, kv head): high and low E4M3 terms
+// [64 rows][128 B] each in the 128-byte-swizzled K-major layout (one bulk
+// copy of kQCodes bytes), then the scale (read by the producer)
+constexpr int kQCodes = 2 * kMaxN * 128;
+constexpr int kQRecord = kQCodes + 16;
+
+// instruction descriptors: D fp32; A, B E4M3 (kind::f8f6f4) both K-major
+__host__ __device__ constexpr uint32_t idesc_f8(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// D fp32; A, B f16 (kind::f16), both MN-major
+__host__ __device__ constexpr uint32_t idesc_f16_mn(int M, int N) {
+    return (1u << 4) | (1u << 15) | (1u << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// maximum over the warp (every lane gets it)
+__device__ __forceinline__ float warp_max(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// A barrier of a group of warps on an mbarrier whose count is the number of
+// warps: every warp of the group calls it at the same points in the same
+// order, `phase` (a per-thread counter) numbers those points.  The wait is
+// bounded: false (and SVPA_DEVERR_TIMEOUT) when it ran out, after which the
+// caller leaves its loop, so that no warp is left waiting on a peer that gave
+// up (a named barrier would have no limit).
+__device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, int32_t *err) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    const bool ok = mbar_wait(bar, phase & 1u, err);
+    ++phase;
+    return ok;
+}
+
+__device__ __forceinline__ uint32_t par_of(int idx) { return (uint32_t)((idx >> 1) & 1); }
+
+// NPAD: TMEM columns (query rows) a thread keeps in registers, 32, 48 or 64;
+// TILES: one scale per 64-element tile of a row instead of one per (page, kv head)
+template <int NPAD, bool TILES>
+__global__ void __launch_bounds__(kThreads, 1)
+    pva_f8_kernel(const __grid_constant__ CUtensorMap mkp, const __grid_constant__ CUtensorMap mvp,
+                  const uint8_t *__restrict__ qrec, const __grid_constant__ AttnArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    SmemF8<TILES> &sm =
+        *reinterpret_cast<SmemF8<TILES> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = a.npad;  // MMA N: the query rows rounded up to 16 (16 .. NPAD)
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNK8; ++i) {
+            mbar_init(&sm.k8_full[i], kStageArrivals);
+            mbar_init(&sm.k8_empty[i], 1);
+        }
+        for (int i = 0; i < kNV8; ++i) {
+            mbar_init(&sm.v8_full[i], kStageArrivals);
+            mbar_init(&sm.v8_empty[i], kConvWarps);
+        }
+        for (int i = 0; i < kNV16; ++i) {
+            mbar_init(&sm.v16_full[i], kConvWarps);
+            mbar_init(&sm.v16_empty[i], 1);
+        }
+        mbar_init(&sm.qs_full, 1);
+        mbar_init(&sm.qs_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.s_full[i], 1);
+            mbar_init(&sm.s_empty[i], 4);
+            mbar_init(&sm.p_full[i], 4);
+            mbar_init(&sm.p_empty[i], 1);
+            mbar_init(&sm.o_full[i], 1);
+            mbar_init(&sm.o_empty[i], kEpiWarps);
+        }
+        mbar_init(&sm.stat_full, 4);
+        mbar_init(&sm.stat_empty, kEpiWarps);
+        mbar_init(&sm.soft_sync, 4);
+        mbar_init(&sm.epi_sync, kEpiWarps);
+        fence_mbar_init();
+    }
+    // references start at -inf (rows past the query rows stay there)
+    for (int i = threadIdx.x; i < 2 * kMaxN; i += blockDim.x) sm.mref[i / kMaxN][i % kMaxN] = -CUDART_INF_F;
+    // TMEM columns: S^T[x] at 64 x (x = 0, 1), O^T[x] at 128 + 64 x; with
+    // tile scales the scores of d 64..127 go to a second tile at 256 + 64 x
+    constexpr uint32_t kTmemS = 0, kTmemO = 128, kTmemCols = TILES ? 512 : 256;
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == 0) {
+        // ================================================= producer
+        const uint64_t pol = policy_evict_first();
+        if (lane == 0) {
+            prefetch_tensormap(&mkp);
+            prefetch_tensormap(&mvp);
+        }
+        // the split-query records are written by the kernel launched just
+        // before this one (programmatic dependent launch)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        int jk = 0, jv = 0, units = 0;  // K blocks issued, V blocks issued, units started (warp-uniform)
+        bool ok = true;
+        float qsc = 1.f;  // the current unit's query scale (lane 0)
+        constexpr uint32_t tile_bytes = TILES ? kPB * kTileScales * 4 : 0u;
+        auto copy_scale = [&](const float *scales, int id, int hh, float *dst, uint64_t *bar) {
+            // a missing page takes the block's first page's scale (its bytes are zero)
+            const int id0 = __shfl_sync(0x000000ffu, id, 0);
+            const int sid = (id >= 0 && id < a.num_blocks) ? id : id0;
+            cp_async_4(dst, scales + (size_t)sid * a.Hkv + hh);
+            cp_async_mbar_arrive_noinc(bar);
+        };
+        auto copy_tile_scales = [&](const float *scales, int id, int hh, float *dst, uint64_t *bar) {
+            const int id0 = __shfl_sync(0x000000ffu, id, 0);
+            const int sid = (id >= 0 && id < a.num_blocks) ? id : id0;
+            bulk_copy_g2s(dst, scales + ((size_t)sid * a.Hkv + hh) * kTileScales, kTileScales * 4, bar);
+        };
+        // V of the oldest block whose K is out, if its staging slot is free
+        auto try_issue_v = [&]() -> bool {
+            if (jv >= jk) return false;
+            const int vs = jv % kNV8;
+            int ready = 1;
+            if (lane == 0 && jv >= kNV8) ready = mbar_test(&sm.v8_empty[vs], (uint32_t)(((jv / kNV8) & 1) ^ 1));
+            if (!__shfl_sync(0xffffffffu, ready, 0)) return false;
+            if (lane == 0) mbar_arrive_expect_tx(&sm.v8_full[vs], kTile8 + tile_bytes);
+            if (lane < kPB) {
+                const int id = sm.vid[jv % kNMeta][lane], hh = sm.meta[jv % kNMeta].h;
+                tma_load_4d(sm.v8[vs] + lane * kPage8, &mvp, 0, 0, hh, id, &sm.v8_full[vs], pol);
+                copy_scale(a.v_scale, id, hh, &sm.vsc[jv % kNMeta][lane], &sm.v8_full[vs]);
+                if constexpr (TILES) copy_tile_scales(a.v_scale, id, hh, sm.ts.v[vs][lane], &sm.v8_full[vs]);
+            }
+            __syncwarp();
+            ++jv;
+            return true;
+        };
+        auto wait_issuing_v = [&](uint64_t *bar, uint32_t parity) -> bool {
+            unsigned long long t0 = 0;
+            while (true) {
+                int done = 0;
+                if (lane == 0) done = mbar_test(bar, parity);
+                if (__shfl_sync(0xffffffffu, done, 0)) return true;
+                if (try_issue_v()) {
+                    t0 = 0;
+                    continue;
+                }
+                __nanosleep(64);
+                const unsigned long long now = global_ns();
+                if (t0 == 0) {
+                    t0 = now;
+                } else if (now - t0 > kWaitLimitNs) {
+                    if (lane == 0) raise_error(a.err, SVPA_DEVERR_TIMEOUT);
+                    return false;
+                }
+            }
+        };
+        while (ok) {
+            int u = 0;
+            if (lane == 0) u = atomicAdd(&a.sched[0], 1);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (u >= a.total_units) break;
+            const int bh = u / a.max_splits, split = u - bh * a.max_splits;
+            const int rb = bh / a.Hkv, h = bh - rb * a.Hkv;
+            const int b = a.order ? __ldg(a.order + rb) : rb;  // longest sequences first
+            const int L = __ldg(a.context_lens + b);
+            const int npages = (L + a.n_q + kBlockSize - 1) / kBlockSize;
+            if (L < 0 || npages > a.max_blocks) {
+                if (lane == 0 && split == 0 && h == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                continue;
+            }
+            const int nsplit = (npages + a.split_pages - 1) / a.split_pages;
+            if (split >= nsplit) continue;
+            const int page0 = split * a.split_pages;
+            const int n = min(a.split_pages, npages - page0);
+            const int nblk = (n + kPB - 1) / kPB;
+            const int32_t *bt = a.block_table + (size_t)b * a.max_blocks + page0;
+            int blk_next = a.num_blocks;
+            for (int i0 = 0; i0 < n && ok; i0 += 32) {
+                int blk = a.num_blocks;  // out of range: a zero-filled page
+                if (i0 == 0) {
+                    if (lane < n) blk = __ldg(bt + lane);
+                } else {
+                    blk = blk_next;
+                }
+                if (i0 + lane < n && (blk < 0 || blk >= a.num_blocks)) {
+                    raise_error(a.err, SVPA_DEVERR_BAD_BLOCK);
+                    blk = 0;
+                }
+                blk_next = a.num_blocks;
+                if (i0 + 32 + lane < n) blk_next = __ldg(bt + i0 + 32 + lane);
+                const int cnt = min(32, n - i0);
+                for (int j0 = 0; j0 < cnt; j0 += kPB) {
+                    int my_id = __shfl_sync(0xffffffffu, blk, (j0 + (lane & 7)) & 31);
+                    if (j0 + (lane & 7) >= cnt) my_id = a.num_blocks;
+                    const int bi = (i0 + j0) / kPB;  // block index in the unit
+                    const int ks = jk % kNK8;
+                    if (jk >= kNK8) ok = wait_issuing_v(&sm.k8_empty[ks], (uint32_t)(((jk / kNK8) & 1) ^ 1));
+                    // the query record is replaced once the previous unit's last S is done
+                    if (ok && bi == 0 && units >= 1) ok = wait_issuing_v(&sm.qs_empty, (uint32_t)((units - 1) & 1));
+                    if (!ok) break;
+                    if (lane == 0) {
+                        BlockMeta &m = sm.meta[jk % kNMeta];
+                        if (bi == 0) {
+                            const uint8_t *rec = qrec + ((size_t)b * a.Hkv + h) * kQRecord;
+                            qsc = *reinterpret_cast<const float *>(rec + kQCodes);
+                            mbar_arrive_expect_tx(&sm.qs_full, kQCodes);
+                            bulk_copy_g2s(&sm.qs[0][0], rec, kQCodes, &sm.qs_full);
+                        }
+                        m.b = b; m.h = h; m.split = split; m.L = L; m.nsplit = nsplit; m.qsc = qsc;
+                        m.pos0 = (page0 + i0 + j0) * kBlockSize;
+                        m.ntok = min(kPB, n - (i0 + j0)) * kBlockSize;
+                        m.flags = (bi == 0 ? kFlagFirst : 0) | (bi == nblk - 1 ? kFlagLast : 0);
+                        mbar_arrive_expect_tx(&sm.k8_full[ks], kTile8 + tile_bytes);
+                    }
+                    if (lane < kPB) {
+                        sm.vid[jk % kNMeta][lane] = my_id;
+                        tma_load_4d(sm.k8[ks] + lane * kPage8, &mkp, 0, 0, h, my_id, &sm.k8_full[ks], pol);
+                        copy_scale(a.k_scale, my_id, h, &sm.ksc[jk % kNMeta][lane], &sm.k8_full[ks]);
+                        if constexpr (TILES)
+                            copy_tile_scales(a.k_scale, my_id, h, sm.ts.k[jk % kNMeta][lane], &sm.k8_full[ks]);
+                    }
+                    __syncwarp();
+                    ++jk;
+                    try_issue_v();
+                }
+            }
+            ++units;
+        }
+        // the V copies still owed
+        while (ok && jv < jk) {
+            if (jv >= kNV8) {
+                int good = 1;
+                if (lane == 0) good = mbar_wait(&sm.v8_empty[jv % kNV8], (uint32_t)(((jv / kNV8) & 1) ^ 1), a.err);
+                ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+            }
+            if (ok) try_issue_v();
+        }
+        if (lane == 0) {
+            // end-of-work marker on the K ring (for the MMA issuer) and the V
+            // staging ring (for the converters)
+            const int ks = jk % kNK8;
+            bool kmark = false, vmark = false;  // end markers placed
+            if (ok && jk >= kNK8) ok = mbar_wait(&sm.k8_empty[ks], (uint32_t)(((jk / kNK8) & 1) ^ 1), a.err);
+            if (ok) {
+                sm.meta[jk % kNMeta].flags = kFlagEnd;
+                mbar_arrive_cnt(&sm.k8_full[ks], kStageArrivals);
+                kmark = true;
+            }
+            const int vs = jv % kNV8;
+            if (ok && jv >= kNV8) ok = mbar_wait(&sm.v8_empty[vs], (uint32_t)(((jv / kNV8) & 1) ^ 1), a.err);
+            if (ok) {
+                mbar_arrive_cnt(&sm.v8_full[vs], kStageArrivals);
+                vmark = true;
+            }
+            // wait (bounded) for the copies still in flight, also after a
+            // wait above ran out: no copy may land after the CTA has exited.
+            // Only the last ring-depth blocks can be in flight (a block is
+            // issued once the one a ring depth before it was consumed); a slot
+            // that took an end marker had completed its block already.
+            bool drained = true;
+            for (int i = max(0, jk - kNK8 + (kmark ? 1 : 0)); i < jk && drained; ++i)
+                drained = mbar_wait(&sm.k8_full[i % kNK8], (uint32_t)((i / kNK8) & 1), a.err);
+            for (int i = max(0, jv - kNV8 + (vmark ? 1 : 0)); i < jv && drained; ++i)
+                drained = mbar_wait(&sm.v8_full[i % kNV8], (uint32_t)((i / kNV8) & 1), a.err);
+            if (drained && units >= 1) drained = mbar_wait(&sm.qs_full, (uint32_t)((units - 1) & 1), a.err);
+            __threadfence();
+            const int done = atomicAdd(&a.sched[1], 1);
+            if (done == (int)gridDim.x - 1) {
+                a.sched[0] = 0;
+                a.sched[1] = 0;
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================= MMA issuer
+        if (lane == 0) {
+            const uint32_t idS = idesc_f8(kNB, N);
+            const uint32_t idPV = idesc_f16_mn(kNB, N);
+            const uint32_t qa = smem_u32(&sm.qs[0][0]);
+            // S^T_jj = K_jj (Q_hi + Q_lo)^T once K_jj has landed (or forward the end marker)
+            auto issue_s = [&](int jj, int &unit_jj, BlockMeta &m) -> bool {
+                const int ks = jj % kNK8;
+                if (!mbar_wait(&sm.k8_full[ks], (uint32_t)((jj / kNK8) & 1), a.err)) return false;
+                m = sm.meta[jj % kNMeta];
+                if (m.flags & kFlagEnd) {
+                    mbar_arrive(&sm.s_full[jj & 1]);
+                    return true;
+                }
+                if (m.flags & kFlagFirst) {
+                    ++unit_jj;
+                    if (!mbar_wait(&sm.qs_full, (uint32_t)(unit_jj & 1), a.err)) return false;
+                }
+                // the softmax has read S^T_{jj-2} out of this buffer
+                if (jj >= 2 && !mbar_wait(&sm.s_empty[jj & 1], par_of(jj - 2), a.err)) return false;
+                tc_fence_after();
+                const uint32_t ka = smem_u32(sm.k8[ks]);
+                const uint32_t dS = tmem + kTmemS + (uint32_t)(jj & 1) * kMaxN;
+#pragma unroll
+                for (int term = 0; term < 2; ++term)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = umma_desc_sw128(ka + kk * 32, 16, 1024);
+                        const uint64_t bd = umma_desc_sw128(qa + term * (kMaxN * 128) + kk * 32, 16, 1024);
+                        if constexpr (TILES) {
+                            // columns 0..63 and 64..127 of d into separate tiles
+                            umma_f8(dS + (uint32_t)(kk >> 1) * 256, ad, bd, idS, (term | (kk & 1)) ? 1u : 0u);
+                        } else {
+                            umma_f8(dS, ad, bd, idS, (term | kk) ? 1u : 0u);
+                        }
+                    }
+                umma_commit(&sm.k8_empty[ks]);
+                umma_commit(&sm.s_full[jj & 1]);
+                if (m.flags & kFlagLast) umma_commit(&sm.qs_empty);
+                return true;
+            };
+            BlockMeta cur, nxt;
+            int j = 0, unit = -1;
+            bool ok = issue_s(0, unit, cur);
+            while (ok && !(cur.flags & kFlagEnd)) {
+                int unit1 = unit;
+                bool next_done = false;
+                if (mbar_test(&sm.k8_full[(j + 1) % kNK8], (uint32_t)(((j + 1) / kNK8) & 1))) {
+                    ok = issue_s(j + 1, unit1, nxt);
+                    next_done = true;
+                    if (!ok) break;
+                }
+                // O^T += V_j^T P_j^T once the softmax has written P_j and V_j is converted
+                if (!mbar_wait(&sm.p_full[j & 1], par_of(j), a.err)) break;
+                const int ob = unit & 1;
+                if ((cur.flags & kFlagFirst) && unit >= 2 && !mbar_wait(&sm.o_empty[ob], par_of(unit) ^ 1u, a.err))
+                    break;
+                const int vs = j % kNV16;
+                if (!mbar_wait(&sm.v16_full[vs], (uint32_t)((j / kNV16) & 1), a.err)) break;
+                tc_fence_after();
+                const uint32_t va = smem_u32(sm.v16[vs]);
+                const uint32_t pa = smem_u32(sm.pt[j & 1]);
+                const uint32_t dO = tmem + kTmemO + (uint32_t)ob * kMaxN;
+#pragma unroll
+                for (int kt = 0; kt < kPB; ++kt) {
+                    // V^T: page kt as [row half][d slab][8 rows][128 B]; P^T: 8-token row groups of 128 B
+                    const uint64_t ad = umma_desc_sw128(va + kt * 4096, 1024, 2048);
+                    const uint64_t bd = umma_desc_sw128(pa + kt * 2048, 8192, 1024);
+                    umma_bf16(dO, ad, bd, idPV, ((cur.flags & kFlagFirst) && kt == 0) ? 0u : 1u);
+                }
+                umma_commit(&sm.v16_empty[vs]);
+                umma_commit(&sm.p_empty[j & 1]);
+                if (cur.flags & kFlagLast) umma_commit(&sm.o_full[ob]);
+                if (!next_done) {
+                    ok = issue_s(j + 1, unit1, nxt);
+                    if (!ok) break;
+                }
+                ++j;
+                unit = unit1;
+                cur = nxt;
+            }
+        }
+        __syncwarp();
+    } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
+        // ================================================= V converters
+        // Block j's E4M3 V pages -> one f16 tile in the MMA's layout (page p
+        // at p * 4 KB as [row half][d slab][8 rows][128 B], 128-byte swizzle),
+        // exact (the page scale is applied through P); rows past the
+        // sequence's last token and pages whose scale is 0 are zeroed.
+        const int ct = (warp - kConvWarp0) * 32 + lane;
+        constexpr int NCT = kConvWarps * 32;
+        for (int j = 0;; ++j) {
+            const int s8 = j % kNV8, tb = j % kNV16;
+            if (!mbar_wait(&sm.v8_full[s8], (uint32_t)((j / kNV8) & 1), a.err)) break;
+            const BlockMeta md = sm.meta[j % kNMeta];
+            if (md.flags & kFlagEnd) break;
+            if (j >= kNV16 && !mbar_wait(&sm.v16_empty[tb], (uint32_t)(((j / kNV16) & 1) ^ 1), a.err)) break;
+            const uint8_t *src = sm.v8[s8];
+            const float *scl = sm.vsc[j % kNMeta];
+            uint8_t *tile = sm.v16[tb];
+            if (lane < kPB && !(scl[lane] >= 0.f && scl[lane] <= 3.0e38f)) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+            const int t_end = md.L + a.n_q - md.pos0;  // rows from t_end on are zeroed
+            constexpr int kItems = kNB * 8, kPer = kItems / NCT;
+#pragma unroll 1
+            for (int t0 = 0; t0 < kPer; t0 += 4) {
+                uint4 e[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = ct + NCT * (t0 + u), row = i >> 3, g = i & 7;
+                    e[u] = make_uint4(0, 0, 0, 0);
+                    if (row < t_end && (TILES || scl[row >> 4] > 0.f))
+                        e[u] = *reinterpret_cast<const uint4 *>(src + row * 128 + ((g ^ (row & 7)) << 4));
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = ct + NCT * (t0 + u), row = i >> 3, g = i & 7;
+                    uint4 lo, hi;
+                    lo.x = e4m3x2_to_f16x2(e[u].x & 0xffffu);
+                    lo.y = e4m3x2_to_f16x2(e[u].x >> 16);
+                    lo.z = e4m3x2_to_f16x2(e[u].y & 0xffffu);
+                    lo.w = e4m3x2_to_f16x2(e[u].y >> 16);
+                    hi.x = e4m3x2_to_f16x2(e[u].z & 0xffffu);
+                    hi.y = e4m3x2_to_f16x2(e[u].z >> 16);
+                    hi.z = e4m3x2_to_f16x2(e[u].w & 0xffffu);
+                    hi.w = e4m3x2_to_f16x2(e[u].w >> 16);
+                    if constexpr (TILES) {
+                        if (row < t_end) {
+                            // this group's 64-element tile: (page, slot, half); a tile
+                            // scale multiplies the values in f16 (so at most 146)
+                            const float tsc = sm.ts.v[s8][row >> 4][(row & 15) * 2 + (g >> 2)];
+                            if (!(tsc >= 0.f && tsc <= 146.f)) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                            const uint32_t t2 = pack_f16x2(tsc, tsc);
+                            lo.x = mul_f16x2(lo.x, t2);
+                            lo.y = mul_f16x2(lo.y, t2);
+                            lo.z = mul_f16x2(lo.z, t2);
+                            lo.w = mul_f16x2(lo.w, t2);
+                            hi.x = mul_f16x2(hi.x, t2);
+                            hi.y = mul_f16x2(hi.y, t2);
+                            hi.z = mul_f16x2(hi.z, t2);
+                            hi.w = mul_f16x2(hi.w, t2);
+                        }
+                    }
+                    const int r8 = row & 7, c0 = (g & 3) * 2;
+                    uint8_t *dst = tile + (row >> 3) * 2048 + (g >> 2) * 1024 + r8 * 128;
+                    *reinterpret_cast<uint4 *>(dst + ((c0 ^ r8) << 4)) = lo;
+                    *reinterpret_cast<uint4 *>(dst + (((c0 + 1) ^ r8) << 4)) = hi;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sm.v16_full[tb]);
+                mbar_arrive(&sm.v8_empty[s8]);
+            }
+        }
+    } else if (warp >= kSoftWarp0 && warp < kSoftWarp0 + 4) {
+        // ================================================= softmax
+        const int quarter = warp & 3;
+        const int t = quarter * 32 + lane;                   // token of the block == TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int G = a.G, M = a.M;
+        float lsum[NPAD];                                    // this token slot's share of each row sum
+#pragma unroll
+        for (int r = 0; r < NPAD; ++r) lsum[r] = 0.f;
+        int j = 0, unit = -1, cur = 0;                       // cur: the current reference set
+        uint32_t sp = 0;                                     // soft_sync phases passed
+        while (true) {
+            if (!mbar_wait(&sm.s_full[j & 1], par_of(j), a.err)) break;
+            const BlockMeta md = sm.meta[j % kNMeta];
+            if (md.flags & kFlagEnd) {
+                // tell the epilogue warps there is no further unit
+                if (unit >= 0) mbar_wait(&sm.stat_empty, (uint32_t)(unit & 1), a.err);
+                if (threadIdx.x == kSoftWarp0 * 32) sm.ep_end = 1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.stat_full);
+                break;
+            }
+            const bool first = md.flags & kFlagFirst;
+            if (first) {
+                ++unit;
+#pragma unroll
+                for (int r = 0; r < NPAD; ++r) lsum[r] = 0.f;
+            }
+            tc_fence_after();
+            // this token's raw scores against every query row (TILES: the two
+            // 64-element halves of d, each times its tile scale)
+            float x[NPAD];
+            {
+                float k0 = 1.f, k1 = 1.f;
+                if constexpr (TILES) {
+                    k0 = sm.ts.k[j % kNMeta][t >> 4][(t & 15) * 2];
+                    k1 = sm.ts.k[j % kNMeta][t >> 4][(t & 15) * 2 + 1];
+                }
+                const uint32_t sa = tmem + kTmemS + (uint32_t)(j & 1) * kMaxN + lane_off;
+#pragma unroll
+                for (int c = 0; c < NPAD / 16; ++c) {
+                    if (c * 16 < N) {  // (uniform)
+                        uint32_t raw[16];
+                        tmem_ld16(sa + c * 16, raw);
+                        if constexpr (TILES) {
+                            uint32_t raw1[16];
+                            tmem_ld16(sa + 256 + c * 16, raw1);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                x[c * 16 + e] = __uint_as_float(raw[e]) * k0 + __uint_as_float(raw1[e]) * k1;
+                        } else {
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) x[c * 16 + e] = __uint_as_float(raw[e]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) x[c * 16 + e] = 0.f;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.s_empty[j & 1]);  // S^T_j's buffer is free
+
+            // the block's page scales arrive with its V pages: V_j converted
+            // (this wait also keeps the converters within the descriptor ring)
+            mbar_wait(&sm.v16_full[j % kNV16], (uint32_t)((j / kNV16) & 1), a.err);
+            const int L = md.L, T = L + a.n_q, p = md.pos0 + t;
+            const bool valid = t < md.ntok && p < T;
+            const float kscale = TILES ? 1.f : sm.ksc[j % kNMeta][t >> 4];
+            const float vscale = TILES ? 1.f : sm.vsc[j % kNMeta][t >> 4];
+            const float sc = a.scale_log2 * kscale * md.qsc;
+            const bool vpos = vscale > 0.f;
+            const float lv = vpos ? __log2f(vscale) : 0.f;  // (a zero scale: the converters zero the rows)
+            const float inv_v = vpos ? 1.f / vscale : 1.f;
+            // visibility: history for every row, a speculative slot for the
+            // rows whose query has it among its ancestors (or is it)
+            const bool spec = valid && p >= L;
+#pragma unroll
+            for (int r = 0; r < NPAD; ++r) {
+                bool vis = valid && r < M;
+                if (spec && vis) vis = (a.anc[r / G] >> (p - L)) & 1ull;
+                x[r] = vis ? fmaf(x[r], sc, lv) : -CUDART_INF_F;
+            }
+            // reference maxima: the shared ones, unless a score passes one by
+            // 2^8 (or the unit starts); then the block's row maxima, reduced
+            // over the 128 tokens, replace the references they pass
+            bool pass = false;
+            if (!first) {
+#pragma unroll
+                for (int r = 0; r < NPAD; ++r) {
+                    const float m = sm.mref[cur][r];
+                    pass |= m == -CUDART_INF_F ? x[r] != -CUDART_INF_F : x[r] - m > kRescaleLog2;
+                }
+            }
+            bool slow = first;
+            if (!first) {
+                // one vote of the four warps (the flags by barrier phase parity)
+                const bool wpass = __any_sync(0xffffffffu, pass);
+                if (lane == 0) sm.vote[sp & 1][quarter] = wpass;
+                const uint32_t ph = sp;
+                if (!group_sync(&sm.soft_sync, sp, a.err)) break;
+                slow = sm.vote[ph & 1][0] | sm.vote[ph & 1][1] | sm.vote[ph & 1][2] | sm.vote[ph & 1][3];
+            }
+            if (slow) {  // (uniform)
+#pragma unroll
+                for (int r = 0; r < NPAD; ++r) {
+                    if (r < N) {
+                        const float bm = warp_max(x[r]);
+                        if (lane == 0) sm.red[quarter][r] = bm;
+                    }
+                }
+                if (!group_sync(&sm.soft_sync, sp, a.err)) break;
+                bool rescale = false;
+#pragma unroll
+                for (int r = 0; r < NPAD; ++r) {
+                    if (r < N) {
+                        const float bm = fmaxf(fmaxf(sm.red[0][r], sm.red[1][r]), fmaxf(sm.red[2][r], sm.red[3][r]));
+                        const float mold = first ? -CUDART_INF_F : sm.mref[cur][r];
+                        float mnew = mold, al = 1.f;
+                        if (mold == -CUDART_INF_F ? bm != -CUDART_INF_F : bm > mold + kRescaleLog2) {
+                            mnew = bm;
+                            al = ex2_approx(mold - mnew);  // 0 when the old reference is -inf
+                            rescale = true;
+                        }
+                        lsum[r] *= al;
+                        if (t == r) {
+                            sm.mref[cur ^ 1][r] = mnew;
+                            sm.salpha[r] = al;
+                        }
+                    }
+                }
+                rescale &= !first;  // (O^T starts from zero at a unit's first block)
+                if (!group_sync(&sm.soft_sync, sp, a.err)) break;  // new references written, red free
+                cur ^= 1;
+                if (rescale) {
+                    // O^T holds P_{<j} V of this unit: scale each row's column
+                    // once PV_{j-1} has landed (lane = head dimension t)
+                    mbar_wait(&sm.p_empty[(j - 1) & 1], par_of(j - 1), a.err);
+                    tc_fence_after();
+                    const uint32_t oa = tmem + kTmemO + (uint32_t)(unit & 1) * kMaxN + lane_off;
+#pragma unroll
+                    for (int c = 0; c < NPAD / 16; ++c) {
+                        if (c * 16 < N) {
+                            uint32_t raw[16];
+                            tmem_ld16(oa + c * 16, raw);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                raw[e] = __float_as_uint(__uint_as_float(raw[e]) * sm.salpha[c * 16 + e]);
+                            tmem_st16(oa + c * 16, raw);
+                        }
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                }
+            }
+            // P'^T_j: f16 pairs (r, r + 1) of this token, 2^(x - m), into the
+            // P^T buffer once PV_{j-2} has read it
+            if (j >= 2) mbar_wait(&sm.p_empty[j & 1], par_of(j - 2), a.err);
+            uint8_t *prow = sm.pt[j & 1] + (t >> 3) * 1024 + (t & 7) * 128;
+#pragma unroll
+            for (int c = 0; c < NPAD / 8; ++c) {
+                if (c * 8 < N) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = c * 8 + 2 * e;
+                        const float m0 = sm.mref[cur][r], m1 = sm.mref[cur][r + 1];
+                        const float z0 = x[r] - (m0 == -CUDART_INF_F ? 0.f : m0);
+                        const float z1 = x[r + 1] - (m1 == -CUDART_INF_F ? 0.f : m1);
+                        const uint32_t p2 = ex2_f16x2(pack_f16x2(z0, z1));
+                        const float2 f = f16x2_to_float2(p2);
+                        lsum[r] = fmaf(f.x, inv_v, lsum[r]);
+                        lsum[r + 1] = fmaf(f.y, inv_v, lsum[r + 1]);
+                        w[e] = p2;
+                    }
+                    *reinterpret_cast<uint4 *>(prow + ((c ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.p_full[j & 1]);
+
+            if (md.flags & kFlagLast) {
+                // the unit's row sums: reduce the 128 token slots' shares, in
+                // place (within a warp by halving exchanges over RC = 32 or 64
+                // rows, absent rows counting 0, lane l ending with rows
+                // (RC / 32) l + i; then across the four warps)
+                constexpr int RC = NPAD > 32 ? 64 : 32;
+#pragma unroll
+                for (int hsz = RC / 2, mask = 16; mask >= 1; hsz >>= 1, mask >>= 1) {
+                    const bool upper = lane & mask;
+#pragma unroll
+                    for (int i = 0; i < hsz; ++i) {
+                        const float hi = i + hsz < NPAD ? lsum[i + hsz] : 0.f;
+                        const float send = upper ? lsum[i] : hi;
+                        const float keep = upper ? hi : lsum[i];
+                        lsum[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+                    }
+                }
+                if (unit >= 1) mbar_wait(&sm.stat_empty, (uint32_t)((unit - 1) & 1), a.err);
+#pragma unroll
+                for (int i = 0; i < RC / 32; ++i) sm.red[quarter][(RC / 32) * lane + i] = lsum[i];
+                if (!group_sync(&sm.soft_sync, sp, a.err)) break;
+                if (t < RC)
+                    sm.stat[t] = make_float2(sm.mref[cur][t],
+                                             (sm.red[0][t] + sm.red[1][t]) + (sm.red[2][t] + sm.red[3][t]));
+                if (threadIdx.x == kSoftWarp0 * 32) {
+                    sm.ep_b = md.b;
+                    sm.ep_h = md.h;
+                    sm.ep_split = md.split;
+                    sm.ep_nsplit = md.nsplit;
+                    sm.ep_end = 0;
+                }
+                if (!group_sync(&sm.soft_sync, sp, a.err)) break;  // red free again, stat complete
+                if (lane == 0) mbar_arrive(&sm.stat_full);
+            }
+            ++j;
+        }
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
+        // ================================================= epilogue
+        // One thread per head dimension (TMEM lane of O^T) writes a finished
+        // unit's rows while the softmax warps already work on the next unit.
+        const int quarter = warp & 3;
+        const int d = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int G = a.G, M = a.M;
+        const int ew = warp - kEpiWarp0;
+        constexpr int NE = kEpiWarps;
+        uint32_t ep_sp = 0;  // epi_sync phases passed
+        for (int unit = 0;; ++unit) {
+            if (!mbar_wait(&sm.stat_full, (uint32_t)(unit & 1), a.err)) break;
+            if (sm.ep_end) break;
+            const int b = sm.ep_b, h = sm.ep_h, split = sm.ep_split, nsplit = sm.ep_nsplit;
+            const int ob = unit & 1;
+            if (!mbar_wait(&sm.o_full[ob], par_of(unit), a.err)) break;
+            tc_fence_after();
+            const uint32_t oa = tmem + kTmemO + (uint32_t)ob * kMaxN + lane_off;
+            const int u2 = b * a.Hkv + h;
+            const size_t pr0 = ((size_t)u2 * a.max_splits + split) * M;
+#pragma unroll
+            for (int c = 0; c < NPAD / 16; ++c) {
+                if (c * 16 < N) {
+                    uint32_t raw[16];
+                    tmem_ld16(oa + c * 16, raw);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int r = c * 16 + e;
+                        if (r < M) {
+                            const float2 st = sm.stat[r];
+                            if (nsplit == 1) {
+                                const int jq = r / G, gi = r - jq * G;
+                                const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
+                                const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
+                                a.out[od * kD + d] = __float2bfloat16_rn(__uint_as_float(raw[e]) * inv);
+                            } else {
+                                a.part_acc[(pr0 + r) * kD + d] = __uint_as_float(raw[e]);
+                            }
+                        }
+                    }
+                }
+            }
+            if (d < M) {
+                const float2 st = sm.stat[d];
+                if (nsplit == 1) {
+                    const int jq = d / G, gi = d - jq * G;
+                    const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
+                    if (a.lse) a.lse[od] = (st.x + __log2f(st.y)) * 0.69314718055994530942f;
+                } else {
+                    a.part_ml[(pr0 + d) * 2] = st.x;
+                    a.part_ml[(pr0 + d) * 2 + 1] = st.y;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sm.o_empty[ob]);
+                mbar_arrive(&sm.stat_empty);
+            }
+            if (nsplit == 1) continue;
+            __threadfence();
+            if (!group_sync(&sm.epi_sync, ep_sp, a.err)) break;
+            if (ew == 0 && lane == 0) {
+                const int tk = atomicAdd(&a.tickets[u2], 1);
+                sm.last = (tk == nsplit - 1);
+                if (sm.last) a.tickets[u2] = 0;
+            }
+            if (!group_sync(&sm.epi_sync, ep_sp, a.err)) break;
+            const int last = sm.last;
+            if (!group_sync(&sm.epi_sync, ep_sp, a.err)) break;
+            if (!last) continue;
+            // the last split's CTA merges every split's partial rows with
+            // log-sum-exp weights (an online merge: running maximum, rescaled
+            // sum): one warp per row, 4 columns per lane, four rows and two
+            // splits per pass so that their loads are in flight together
+            __threadfence();
+            const size_t base = (size_t)u2 * a.max_splits * M;
+            for (int r0 = ew; r0 < M; r0 += 4 * NE) {
+                float mrow[4], lrow[4];
+                float4 o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    mrow[i] = -CUDART_INF_F;
+                    lrow[i] = 0.f;
+                    o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                for (int s0 = 0; s0 < nsplit; s0 += 2) {
+                    float2 ml[4][2];
+                    float4 v[4][2];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const int rr = r0 + NE * i;
+                            if (rr < M && s0 + k < nsplit) {
+                                const size_t pr = base + (size_t)(s0 + k) * M + rr;
+                                ml[i][k] = __ldcg(reinterpret_cast<const float2 *>(a.part_ml + pr * 2));
+                                v[i][k] = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + pr * kD) + lane);
+                            } else {
+                                ml[i][k] = make_float2(-CUDART_INF_F, 0.f);
+                                v[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                        }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const float mk = ml[i][k].x;
+                            if (mk == -CUDART_INF_F) continue;  // an empty split (or none)
+                            const float mn = fmaxf(mrow[i], mk);
+                            const float f_old = ex2_approx(mrow[i] - mn);
+                            const float f_new = ex2_approx(mk - mn);
+                            lrow[i] = lrow[i] * f_old + ml[i][k].y * f_new;
+                            o[i].x = o[i].x * f_old + v[i][k].x * f_new;
+                            o[i].y = o[i].y * f_old + v[i][k].y * f_new;
+                            o[i].z = o[i].z * f_old + v[i][k].z * f_new;
+                            o[i].w = o[i].w * f_old + v[i][k].w * f_new;
+                            mrow[i] = mn;
+                        }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = r0 + NE * i;
+                    if (rr >= M) break;
+                    const float inv2 = lrow[i] > 0.f ? 1.f / lrow[i] : 0.f;
+                    const int jq2 = rr / G, gi2 = rr - jq2 * G;
+                    const size_t od2 = (((size_t)b * a.n_q + jq2) * a.Hq + (size_t)h * G + gi2);
+                    uint2 v2;
+                    v2.x = pack_bf16x2(o[i].x * inv2, o[i].y * inv2);
+                    v2.y = pack_bf16x2(o[i].z * inv2, o[i].w * inv2);
+                    reinterpret_cast<uint2 *>(a.out + od2 * kD)[lane] = v2;
+                    if (lane == 0 && a.lse) a.lse[od2] = (mrow[i] + __log2f(lrow[i])) * 0.69314718055994530942f;
+                }
+            }
+        }
+    }
+    // every TMEM user is done before the owner frees it
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// The queries of every (sequence, kv head) as two E4M3 terms for the score
+// MMA: with c = 2^(e - 8) where amax = m 2^e (m in [1/2, 1)), v = q / c lies
+// in (-256, 256); hi = E4M3(v), lo = E4M3(v - hi), both round-to-nearest-even
+// (hi + lo carries a bf16 query's 8 significant bits).  Rows G * n_q .. 63
+// are zero.  One CTA per (sequence, kv head); the record goes straight into
+// the attention kernel's shared memory by one bulk copy.
+__global__ void __launch_bounds__(128) qsplit_kernel(const __grid_constant__ AttnArgs a, uint8_t *qrec) {
+    // the attention kernel may launch now; it waits for this grid before
+    // reading the records
+    asm volatile("griddepcontrol.launch_dependents;");
+    __shared__ float wmax[4];
+    const int u = blockIdx.x, b = u / a.Hkv, h = u - b * a.Hkv;
+    const int M = a.M, G = a.G;
+    const int tid = threadIdx.x;
+    // item = (row, 16-element chunk): 64 rows x 8 chunks
+    float amax = 0.f;
+    for (int i = tid; i < M * 8; i += 128) {
+        const int r = i >> 3, c = i & 7, jq = r / G, gi = r - jq * G;
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            a.q + (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi) * kD + c * 16);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const uint4 w = __ldg(src + k);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                amax = fmaxf(amax, fabsf(__uint_as_float(ww[e] << 16)));
+                amax = fmaxf(amax, fabsf(__uint_as_float(ww[e] & 0xffff0000u)));
+            }
+        }
+    }
+    amax = warp_max(amax);
+    if ((tid & 31) == 0) wmax[tid >> 5] = amax;
+    __syncthreads();
+    amax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    if (!(amax <= 3.0e38f)) {  // inf or NaN in the queries
+        if (tid == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+        amax = 1.f;
+    }
+    int e2 = 0;
+    if (amax > 0.f) frexpf(amax, &e2);
+    const float c = amax > 0.f ? ldexpf(1.f, e2 - 8) : 1.f;
+    const float inv_c = 1.f / c;  // a power of two: exact
+    uint8_t *rec = qrec + (size_t)u * kQRecord;
+    for (int i = tid; i < kMaxN * 8; i += 128) {
+        const int r = i >> 3, c8 = i & 7;
+        uint4 hi16 = make_uint4(0, 0, 0, 0), lo16 = make_uint4(0, 0, 0, 0);
+        if (r < M) {
+            const int jq = r / G, gi = r - jq * G;
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                a.q + (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi) * kD + c8 * 16);
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const uint4 w = __ldg(src + k);
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    // four values: two bf16 pairs -> one word of E4M3 codes per term
+                    const float v0 = __uint_as_float(ww[e] << 16) * inv_c;
+                    const float v1 = __uint_as_float(ww[e] & 0xffff0000u) * inv_c;
+                    const float v2 = __uint_as_float(ww[e + 1] << 16) * inv_c;
+                    const float v3 = __uint_as_float(ww[e + 1] & 0xffff0000u) * inv_c;
+                    uint16_t h01, h23, l01, l23;
+                    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h01) : "f"(v1), "f"(v0));
+                    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h23) : "f"(v3), "f"(v2));
+                    const float2 d01 = f16x2_to_float2(e4m3x2_to_f16x2(h01));
+                    const float2 d23 = f16x2_to_float2(e4m3x2_to_f16x2(h23));
+                    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(l01) : "f"(v1 - d01.y), "f"(v0 - d01.x));
+                    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(l23) : "f"(v3 - d23.y), "f"(v2 - d23.x));
+                    hw[k * 2 + e / 2] = (uint32_t)h01 | ((uint32_t)h23 << 16);
+                    lw[k * 2 + e / 2] = (uint32_t)l01 | ((uint32_t)l23 << 16);
+                }
+            }
+            hi16 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            lo16 = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        const size_t off = (size_t)(r >> 3) * 1024 + (r & 7) * 128 + ((c8 ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4 *>(rec + off) = hi16;
+        *reinterpret_cast<uint4 *>(rec + kMaxN * 128 + off) = lo16;
+    }
+    if (tid == 0) *reinterpret_cast<float4 *>(rec + 2 * kMaxN * 128) = make_float4(c, 0.f, 0.f, 0.f);
+}
+
+template <int NPAD, bool TILES>
+cudaError_t launch_f8(const AttnMaps &m, const AttnArgs &a, const uint8_t *qrec, int grid, cudaStream_t st) {
+    const size_t smem = sizeof(SmemF8<TILES>) + 1024;
+    static DeviceMemo<int> attr_set;  // the shared-memory opt-in, once per device
+    int done = 0;
+    cudaError_t e = attr_set.get(&done, [&](int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(pva_f8_kernel<NPAD, TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem);
+    });
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pva_f8_kernel<NPAD, TILES>, m.k[0], m.v[0], qrec, a);
+}
+
+}  // namespace
+
+size_t attn_f8_qrec_bytes(int batch, int num_kv_heads) { return (size_t)batch * num_kv_heads * kQRecord; }
+
+// FP8 pages, head_dim 128, G * n_q <= 64: the split-query kernel, then the
+// attention kernel as its programmatic dependent
+cudaError_t launch_paged_verify_attn_f8(const AttnMaps &m, const AttnArgs &a, uint8_t *qrec, int grid,
+                                        cudaStream_t st) {
+    qsplit_kernel<<<a.B * a.Hkv, 128, 0, st>>>(a, qrec);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (a.M <= 32) return a.scale_tile ? launch_f8<32, true>(m, a, qrec, grid, st) : launch_f8<32, false>(m, a, qrec, grid, st);
+    if (a.M <= 48) return a.scale_tile ? launch_f8<48, true>(m, a, qrec, grid, st) : launch_f8<48, false>(m, a, qrec, grid, st);
+    return a.scale_tile ? launch_f8<64, true>(m, a, qrec, grid, st) : launch_f8<64, false>(m, a, qrec, grid, st);
+}
+
+}  // namespace svpa

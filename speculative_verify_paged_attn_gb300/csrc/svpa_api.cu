@@ -58,9 +58,10 @@ int sm_count() {
 struct AttnPlan {
     int M, split_pages, max_splits;
     bool use_tc;
+    bool f8;             // FP8 pages on the tensor cores: the split-query kernel, then pva_f8_kernel
     int grid_slots;      // resident CTAs of the chosen kernel
     bool ordered;        // units handed out longest sequence first
-    size_t off_order, off_ml, off_acc, bytes;
+    size_t off_order, off_ml, off_acc, off_qrec, bytes;
 };
 
 svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
@@ -136,6 +137,11 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     } else {
         pl->off_acc = off;
     }
+    // FP8 pages on the tensor cores: each (sequence, kv head)'s queries as two
+    // E4M3 terms, written by the split-query kernel before the attention
+    pl->f8 = pl->use_tc && eb == 1;
+    pl->off_qrec = off;
+    if (pl->f8) off += align_up(attn_f8_qrec_bytes(p->batch, p->num_kv_heads));
     pl->bytes = std::max<size_t>(off, kAlign);
     return SVPA_OK;
 }
@@ -203,7 +209,7 @@ svpa_status svpa_attn_launches(const svpa_attn_params *p, int32_t *launches) {
     AttnPlan pl;
     const svpa_status s = plan_attn(p, &pl);
     if (s != SVPA_OK) return s;
-    *launches = p->batch == 0 ? 0 : (pl.ordered ? 2 : 1);
+    *launches = p->batch == 0 ? 0 : (pl.ordered ? 2 : 1) + (pl.f8 ? 1 : 0);
     return SVPA_OK;
 }
 
@@ -347,6 +353,11 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
         cudaError_t e = launch_seq_order(context_lens, p->batch, reinterpret_cast<int32_t *>(ws + pl.off_order),
                                          static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return from_cuda(e);
+    }
+    if (pl.f8) {
+        a.npad = (pl.M + 15) / 16 * 16;
+        const int grid = std::max(1, std::min(pl.grid_slots, a.total_units));
+        return from_cuda(launch_paged_verify_attn_f8(maps, a, ws + pl.off_qrec, grid, static_cast<cudaStream_t>(stream)));
     }
     if (pl.use_tc) {
         const int grid = std::max(1, std::min(pl.grid_slots, a.total_units));

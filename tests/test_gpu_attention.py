@@ -142,6 +142,12 @@ VARIANT_CASES = [
     ("fp8", small("fp8", batch=3, ctx_lo=1, ctx_hi=900), 16),
     ("fp8_nosplit", small("fp8", batch=2, ctx_lo=100, ctx_hi=300), 1024),
     ("fp8_g4", small("fp8", batch=3, ctx_lo=40, ctx_hi=700, num_q_heads=32, num_kv_heads=8), 8),
+    # FP8 tensor-core kernel at other row counts: 64 rows (gamma 7, G 8), 12
+    # rows (G 2, MMA N 16), 40 rows (gamma 4: rows 40..47 of the N = 48 tile
+    # are padding)
+    ("fp8_m64", small("fp8", gamma=7, batch=2, ctx_lo=1, ctx_hi=700), 16),
+    ("fp8_m12", small("fp8", num_q_heads=16, num_kv_heads=8, batch=3, ctx_lo=1, ctx_hi=600), 8),
+    ("fp8_m40", small("fp8", gamma=4, batch=3, ctx_lo=30, ctx_hi=500), 0),
 ]
 
 
@@ -154,3 +160,25 @@ def test_kernel_variants(name, wl, split, variant):
     ref, ref_lse = U.run_oracle_attention(inp)
     U.assert_attention_close(got, ref, fp8=wl.kv_fp8, what=f"{name} variant {variant}")
     assert np.max(np.abs(lse - ref_lse)) < 2e-3
+
+
+def test_fp8_page_scales_of_any_size():
+    # K and V page scales spread over eight decades (up to ~1e3, far past the
+    # f16 range of 448 x scale) and a few zero V scales: the kernel applies
+    # the K scale to the scores in fp32 and folds the V scale into the
+    # exponent, so every scale is taken, and the output follows the oracle
+    wl = small("fp8", batch=3, ctx_lo=100, ctx_hi=900)
+    inp = W.make_attention(wl, 17)
+    g = torch.Generator().manual_seed(23)
+    nb = inp.num_blocks
+    fk = 10.0 ** (torch.rand(inp.k_scale.shape, generator=g) * 8 - 3)
+    fv = 10.0 ** (torch.rand(inp.v_scale.shape, generator=g) * 8 - 3)
+    fv[torch.rand(inp.v_scale.shape, generator=g) < 0.05] = 0.0
+    inp.k_scale = (inp.k_scale * fk).contiguous()
+    inp.v_scale = (inp.v_scale * fv).contiguous()
+    assert float(inp.v_scale.max()) > 146 and float(inp.k_scale.max()) > 146
+    for variant in (0, 1):
+        got, lse, st = U.run_attention(inp, split_pages=8, variant=variant)
+        assert st == 0
+        ref, ref_lse = U.run_oracle_attention(inp)
+        U.assert_attention_close(got, ref, fp8=True, what=f"wide scales, variant {variant}")
