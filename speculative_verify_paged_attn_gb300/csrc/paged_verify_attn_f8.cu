@@ -519,33 +519,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         // at p * 4 KB as [row half][d slab][8 rows][128 B], 128-byte swizzle),
         // exact (the page scale is applied through P); rows past the
         // sequence's last token and pages whose scale is 0 are zeroed.
+        // Thread ct converts the 16-byte group g = ct % 8 of rows r0 + 8 k
+        // (r0 = ct / 8, k = 0..15): its source and destination offsets are
+        // fixed plus k times 1 KB (source) and 2 KB (destination).
         const int ct = (warp - kConvWarp0) * 32 + lane;
-        constexpr int NCT = kConvWarps * 32;
+        static_assert(kConvWarps * 32 == 64, "converter thread layout");
+        const int g = ct & 7, r0 = ct >> 3;
+        const int src_off = r0 * 128 + ((g ^ r0) << 4);
+        const int c0 = (g & 3) * 2;
+        const int dst_off = (g >> 2) * 1024 + r0 * 128;
+        const int dlo = ((c0 ^ r0) << 4), dhi = (((c0 + 1) ^ r0) << 4);
         for (int j = 0;; ++j) {
             const int s8 = j % kNV8, tb = j % kNV16;
-            if (!mbar_wait(&sm.v8_full[s8], (uint32_t)((j / kNV8) & 1), a.err)) break;
+            if (!mbar_wait_sleep(&sm.v8_full[s8], (uint32_t)((j / kNV8) & 1), a.err, 32)) break;
             const BlockMeta md = sm.meta[j % kNMeta];
             if (md.flags & kFlagEnd) break;
-            if (j >= kNV16 && !mbar_wait(&sm.v16_empty[tb], (uint32_t)(((j / kNV16) & 1) ^ 1), a.err)) break;
-            const uint8_t *src = sm.v8[s8];
+            if (j >= kNV16 && !mbar_wait_sleep(&sm.v16_empty[tb], (uint32_t)(((j / kNV16) & 1) ^ 1), a.err, 32))
+                break;
+            const uint8_t *src = sm.v8[s8] + src_off;
             const float *scl = sm.vsc[j % kNMeta];
-            uint8_t *tile = sm.v16[tb];
+            uint8_t *dst = sm.v16[tb] + dst_off;
             if (lane < kPB && !(scl[lane] >= 0.f && scl[lane] <= 3.0e38f)) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
             const int t_end = md.L + a.n_q - md.pos0;  // rows from t_end on are zeroed
-            constexpr int kItems = kNB * 8, kPer = kItems / NCT;
-#pragma unroll 1
-            for (int t0 = 0; t0 < kPer; t0 += 4) {
+#pragma unroll
+            for (int k0 = 0; k0 < 16; k0 += 4) {
                 uint4 e[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int i = ct + NCT * (t0 + u), row = i >> 3, g = i & 7;
+                    const int row = r0 + 8 * (k0 + u);
                     e[u] = make_uint4(0, 0, 0, 0);
                     if (row < t_end && (TILES || scl[row >> 4] > 0.f))
-                        e[u] = *reinterpret_cast<const uint4 *>(src + row * 128 + ((g ^ (row & 7)) << 4));
+                        e[u] = *reinterpret_cast<const uint4 *>(src + (k0 + u) * 1024);
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int i = ct + NCT * (t0 + u), row = i >> 3, g = i & 7;
+                    const int k = k0 + u, row = r0 + 8 * k;
                     uint4 lo, hi;
                     lo.x = e4m3x2_to_f16x2(e[u].x & 0xffffu);
                     lo.y = e4m3x2_to_f16x2(e[u].x >> 16);
@@ -572,10 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             hi.w = mul_f16x2(hi.w, t2);
                         }
                     }
-                    const int r8 = row & 7, c0 = (g & 3) * 2;
-                    uint8_t *dst = tile + (row >> 3) * 2048 + (g >> 2) * 1024 + r8 * 128;
-                    *reinterpret_cast<uint4 *>(dst + ((c0 ^ r8) << 4)) = lo;
-                    *reinterpret_cast<uint4 *>(dst + (((c0 + 1) ^ r8) << 4)) = hi;
+                    *reinterpret_cast<uint4 *>(dst + k * 2048 + dlo) = lo;
+                    *reinterpret_cast<uint4 *>(dst + k * 2048 + dhi) = hi;
                 }
             }
             fence_proxy_async_smem();
@@ -661,26 +667,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float sc = a.scale_log2 * kscale * md.qsc;
             const bool vpos = vscale > 0.f;
             const float lv = vpos ? __log2f(vscale) : 0.f;  // (a zero scale: the converters zero the rows)
-            const float inv_v = vpos ? 1.f / vscale : 1.f;
+            const float inv_v = vpos ? __frcp_rn(vscale) : 1.f;
             // visibility: history for every row, a speculative slot for the
-            // rows whose query has it among its ancestors (or is it)
-            const bool spec = valid && p >= L;
+            // rows whose query has it among its ancestors (or is it); rows
+            // from M on are padding, never read, and left unmasked
 #pragma unroll
-            for (int r = 0; r < NPAD; ++r) {
-                bool vis = valid && r < M;
-                if (spec && vis) vis = (a.anc[r / G] >> (p - L)) & 1ull;
-                x[r] = vis ? fmaf(x[r], sc, lv) : -CUDART_INF_F;
+            for (int r = 0; r < NPAD; ++r) x[r] = valid ? fmaf(x[r], sc, lv) : -CUDART_INF_F;
+            const bool spec = valid && p >= L;
+            if (__any_sync(0xffffffffu, spec)) {  // only blocks that reach the speculative slots
+                if (spec) {
+                    const int sl = p - L;
+#pragma unroll
+                    for (int r = 0; r < NPAD; ++r)
+                        if (r < M && !((a.anc[r / G] >> sl) & 1ull)) x[r] = -CUDART_INF_F;
+                }
             }
             // reference maxima: the shared ones, unless a score passes one by
             // 2^8 (or the unit starts); then the block's row maxima, reduced
             // over the 128 tokens, replace the references they pass
+            // (after a unit's first block every reference is finite: each row
+            // sees at least its own slot, padding rows see every valid token)
             bool pass = false;
             if (!first) {
+                const float4 *m4 = reinterpret_cast<const float4 *>(sm.mref[cur]);
+                float mx = -CUDART_INF_F;
 #pragma unroll
-                for (int r = 0; r < NPAD; ++r) {
-                    const float m = sm.mref[cur][r];
-                    pass |= m == -CUDART_INF_F ? x[r] != -CUDART_INF_F : x[r] - m > kRescaleLog2;
+                for (int r4 = 0; r4 < NPAD / 4; ++r4) {
+                    const float4 m = m4[r4];
+                    mx = fmaxf(mx, fmaxf(fmaxf(x[4 * r4] - m.x, x[4 * r4 + 1] - m.y),
+                                         fmaxf(x[4 * r4 + 2] - m.z, x[4 * r4 + 3] - m.w)));
                 }
+                pass = mx > kRescaleLog2;
             }
             bool slow = first;
             if (!first) {
@@ -748,16 +765,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // P^T buffer once PV_{j-2} has read it
             if (j >= 2) mbar_wait(&sm.p_empty[j & 1], par_of(j - 2), a.err);
             uint8_t *prow = sm.pt[j & 1] + (t >> 3) * 1024 + (t & 7) * 128;
+            const float4 *m4 = reinterpret_cast<const float4 *>(sm.mref[cur]);
 #pragma unroll
             for (int c = 0; c < NPAD / 8; ++c) {
                 if (c * 8 < N) {
                     uint32_t w[4];
+                    const float4 ma = m4[2 * c], mb = m4[2 * c + 1];
+                    const float mr[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int r = c * 8 + 2 * e;
-                        const float m0 = sm.mref[cur][r], m1 = sm.mref[cur][r + 1];
-                        const float z0 = x[r] - (m0 == -CUDART_INF_F ? 0.f : m0);
-                        const float z1 = x[r + 1] - (m1 == -CUDART_INF_F ? 0.f : m1);
+                        const float z0 = x[r] - mr[2 * e];
+                        const float z1 = x[r + 1] - mr[2 * e + 1];
                         const uint32_t p2 = ex2_f16x2(pack_f16x2(z0, z1));
                         const float2 f = f16x2_to_float2(p2);
                         lsum[r] = fmaf(f.x, inv_v, lsum[r]);
@@ -819,11 +838,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int NE = kEpiWarps;
         uint32_t ep_sp = 0;  // epi_sync phases passed
         for (int unit = 0;; ++unit) {
-            if (!mbar_wait(&sm.stat_full, (uint32_t)(unit & 1), a.err)) break;
+            // (a whole unit away: sleep between probes)
+            if (!mbar_wait_sleep(&sm.stat_full, (uint32_t)(unit & 1), a.err, 256)) break;
             if (sm.ep_end) break;
             const int b = sm.ep_b, h = sm.ep_h, split = sm.ep_split, nsplit = sm.ep_nsplit;
             const int ob = unit & 1;
-            if (!mbar_wait(&sm.o_full[ob], par_of(unit), a.err)) break;
+            if (!mbar_wait_sleep(&sm.o_full[ob], par_of(unit), a.err, 32)) break;
             tc_fence_after();
             const uint32_t oa = tmem + kTmemO + (uint32_t)ob * kMaxN + lane_off;
             const int u2 = b * a.Hkv + h;

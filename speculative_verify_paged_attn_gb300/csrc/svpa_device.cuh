@@ -113,6 +113,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     }
 }
 
+// Bounded wait for a phase that may take a while (a whole unit of work):
+// between probes the thread sleeps `sleep_ns`, leaving its scheduler's issue
+// slots to the warps doing the work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, int32_t *err, unsigned sleep_ns,
+                                                unsigned long long limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) {
+            raise_error(err, SVPA_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 // 4-D tiled bulk tensor copy global -> shared, completion counted on `bar`.
 // The L2 policy marks the streamed K/V pages evict-first.
