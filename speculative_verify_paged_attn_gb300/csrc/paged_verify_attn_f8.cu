@@ -29,22 +29,23 @@
 // no scale range is refused; the row sums add P' / s_v in fp32.
 //
 // Work unit = (sequence, kv head, KV split); persistent CTAs, one per SM.
-// Warp roles (384 threads):
+// Warp roles (320 threads; a TMEM lane quadrant is warp % 4):
 //   warp 0     producer: units from an atomic counter; per block, 8 TMA page
-//              copies of K (2 KB each) into a 4-deep ring with the page
-//              scales (cp.async), V the same into a 2-deep ring; the unit's
-//              split queries (a 16 KB record written by qsplit_kernel) by one
-//              bulk copy;
+//              copies of K (2 KB each) into a 3-deep ring together with both
+//              page scales of each page (cp.async), V into a 3-deep ring; the
+//              unit's split queries (a 16 KB record written by qsplit_kernel)
+//              by one bulk copy;
 //   warp 1     MMA issuer (one thread) and TMEM owner;
-//   warps 2-3  V converters: E4M3 -> f16 in the MMA's layout, rows past the
-//              sequence's end and pages with scale 0 zeroed (TILES: each row
-//              half times its tile scale);
-//   warps 4-7  softmax, one thread per token (TMEM lane quadrant = warp % 4):
-//              row scores from TMEM, mask, lazy reference maxima shared in
-//              shared memory (re-computed only when some score passes the
-//              reference by 2^8, decided by one barrier vote), P^T to shared
-//              memory, per-thread partial row sums reduced at a unit's end;
-//   warps 8-11 epilogue, one thread per head dimension: O^T from TMEM to the
+//   warps 2-5  softmax, one thread per token: row scores from TMEM, mask,
+//              lazy reference maxima shared in shared memory (re-computed
+//              only when some score passes the reference by 2^8, decided by
+//              one vote of the four warps), P'^T to shared memory, per-thread
+//              partial row sums reduced at a unit's end;
+//   warps 6-9  one thread per token row of V: E4M3 -> f16 by moving the bits
+//              (the value times 2^-8, exact; the epilogue multiplies by 2^8),
+//              pages whose scale is 0 zeroed (TILES: each row half times its
+//              tile scale); and, when a unit's statistics are ready, its
+//              epilogue, one thread per head dimension: O^T from TMEM to the
 //              output (or a split partial, merged by the last split's CTA).
 // All waits are bounded; nothing spins forever.
 #include <cuda_bf16.h>
@@ -67,14 +68,15 @@ constexpr int kNB = kPB * 16;            // tokens per block (128 TMEM lanes)
 constexpr int kPage8 = 16 * 128;         // one E4M3 (page, kv head) tile
 constexpr int kTile8 = kPB * kPage8;     // E4M3 block: 16 KB
 constexpr int kTile16 = kNB * kD * 2;    // f16 V block: 32 KB
-constexpr int kNK8 = 4, kNV8 = 2, kNV16 = 2;
+constexpr int kNK8 = 3, kNV8 = 3, kNV16 = 2;
 constexpr int kNMeta = 8;                // block descriptors in flight
 constexpr int kMaxN = 64;                // query rows per kv head (TMEM columns of a tile)
 constexpr int kPtTile = kNB * 128;       // P^T: 128 token rows of 64 f16
-constexpr int kThreads = 384;
-constexpr int kConvWarp0 = 2, kConvWarps = 2;
-constexpr int kSoftWarp0 = 4, kEpiWarp0 = 8, kEpiWarps = 4;
-constexpr uint32_t kStageArrivals = 1 + kPB;  // expect_tx + one cp.async scale per page
+constexpr int kThreads = 320;
+constexpr int kSoftWarp0 = 2, kCvWarp0 = 6, kEpiWarps = 4;
+// K stage: expect_tx + one arrival per page for its two scale copies (cp.async)
+constexpr uint32_t kStageArrivals = 1 + kPB;
+constexpr float kOutScale = 256.f;           // V is held in f16 as its value times 2^-8
 constexpr int kTileScales = 16 * (kD / 64);   // tile scales of one (page, kv head)
 constexpr float kRescaleLog2 = 8.f;           // a new reference maximum when a score passes it by 2^8
 constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagEnd = 4;
@@ -109,13 +111,14 @@ struct SmemF8 {
     int32_t vid[kNMeta][kPB];
     uint64_t k8_full[kNK8], k8_empty[kNK8];
     uint64_t v8_full[kNV8], v8_empty[kNV8];
-    uint64_t v16_full[kNV16], v16_empty[kNV16];
+    uint64_t v16_full[kNV16];
     uint64_t qs_full, qs_empty;
     uint64_t s_full[2], s_empty[2];
-    uint64_t p_full[2], p_empty[2];
+    uint64_t p_full[2];
+    uint64_t pv_done[2];             // PV_j done: its V16 and P^T buffers (j % 2) are free
     uint64_t o_full[2], o_empty[2];
     uint64_t stat_full, stat_empty;
-    uint64_t soft_sync, epi_sync;    // group barriers of the softmax and of the epilogue warps
+    uint64_t soft_sync, epi_sync;    // group barriers of the softmax and of the converter/epilogue warps
     int32_t vote[2][4];              // the softmax warps' votes, by barrier phase parity
     int32_t ep_b, ep_h, ep_split, ep_nsplit, ep_end;
     uint32_t tmem_base;
@@ -194,6 +197,17 @@ __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, int32
 
 __device__ __forceinline__ uint32_t par_of(int idx) { return (uint32_t)((idx >> 1) & 1); }
 
+// Two E4M3 codes of w (the bytes `sel` picks: 0x4140 bytes 0 and 1, 0x4342
+// bytes 2 and 3) to an f16 pair holding each code's value times 2^-8: the
+// sign goes to bit 15, exponent and mantissa bits to bits 7..13.  An E4M3
+// value 2^(e-7) (1 + m/8) lands as f16 2^(e-15) (1 + m/8), and a subnormal
+// 2^-6 m/8 as the f16 subnormal 2^-14 m/8, so the factor is exactly 2^-8 for
+// every finite code (a NaN code gives a finite value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w, uint32_t sel) {
+    const uint32_t u = __byte_perm(w, 0u, sel);  // code0 | code1 << 16
+    return (u + (u & 0x00800080u)) << 7;         // sign from bit 7 to bit 8, then all up by 7
+}
+
 // NPAD: TMEM columns (query rows) a thread keeps in registers, 32, 48 or 64;
 // TILES: one scale per 64-element tile of a row instead of one per (page, kv head)
 template <int NPAD, bool TILES>
@@ -212,20 +226,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.k8_empty[i], 1);
         }
         for (int i = 0; i < kNV8; ++i) {
-            mbar_init(&sm.v8_full[i], kStageArrivals);
-            mbar_init(&sm.v8_empty[i], kConvWarps);
+            mbar_init(&sm.v8_full[i], 1);
+            mbar_init(&sm.v8_empty[i], 4);
         }
-        for (int i = 0; i < kNV16; ++i) {
-            mbar_init(&sm.v16_full[i], kConvWarps);
-            mbar_init(&sm.v16_empty[i], 1);
-        }
+        for (int i = 0; i < kNV16; ++i) mbar_init(&sm.v16_full[i], 4);
         mbar_init(&sm.qs_full, 1);
         mbar_init(&sm.qs_empty, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.s_full[i], 1);
             mbar_init(&sm.s_empty[i], 4);
             mbar_init(&sm.p_full[i], 4);
-            mbar_init(&sm.p_empty[i], 1);
+            mbar_init(&sm.pv_done[i], 1);
             mbar_init(&sm.o_full[i], 1);
             mbar_init(&sm.o_empty[i], kEpiWarps);
         }
@@ -263,11 +274,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         float qsc = 1.f;  // the current unit's query scale (lane 0)
         constexpr uint32_t tile_bytes = TILES ? kPB * kTileScales * 4 : 0u;
-        auto copy_scale = [&](const float *scales, int id, int hh, float *dst, uint64_t *bar) {
-            // a missing page takes the block's first page's scale (its bytes are zero)
+        // both page scales of a page by cp.async, one arrival on `bar` once
+        // both have landed (a missing page takes the block's first page's
+        // scales: its bytes are zero)
+        auto copy_scales = [&](int id, int hh, float *kdst, float *vdst, uint64_t *bar) {
             const int id0 = __shfl_sync(0x000000ffu, id, 0);
             const int sid = (id >= 0 && id < a.num_blocks) ? id : id0;
-            cp_async_4(dst, scales + (size_t)sid * a.Hkv + hh);
+            cp_async_4(kdst, a.k_scale + (size_t)sid * a.Hkv + hh);
+            cp_async_4(vdst, a.v_scale + (size_t)sid * a.Hkv + hh);
             cp_async_mbar_arrive_noinc(bar);
         };
         auto copy_tile_scales = [&](const float *scales, int id, int hh, float *dst, uint64_t *bar) {
@@ -286,7 +300,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane < kPB) {
                 const int id = sm.vid[jv % kNMeta][lane], hh = sm.meta[jv % kNMeta].h;
                 tma_load_4d(sm.v8[vs] + lane * kPage8, &mvp, 0, 0, hh, id, &sm.v8_full[vs], pol);
-                copy_scale(a.v_scale, id, hh, &sm.vsc[jv % kNMeta][lane], &sm.v8_full[vs]);
                 if constexpr (TILES) copy_tile_scales(a.v_scale, id, hh, sm.ts.v[vs][lane], &sm.v8_full[vs]);
             }
             __syncwarp();
@@ -374,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane < kPB) {
                         sm.vid[jk % kNMeta][lane] = my_id;
                         tma_load_4d(sm.k8[ks] + lane * kPage8, &mkp, 0, 0, h, my_id, &sm.k8_full[ks], pol);
-                        copy_scale(a.k_scale, my_id, h, &sm.ksc[jk % kNMeta][lane], &sm.k8_full[ks]);
+                        copy_scales(my_id, h, &sm.ksc[jk % kNMeta][lane], &sm.vsc[jk % kNMeta][lane], &sm.k8_full[ks]);
                         if constexpr (TILES)
                             copy_tile_scales(a.k_scale, my_id, h, sm.ts.k[jk % kNMeta][lane], &sm.k8_full[ks]);
                     }
@@ -408,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int vs = jv % kNV8;
             if (ok && jv >= kNV8) ok = mbar_wait(&sm.v8_empty[vs], (uint32_t)(((jv / kNV8) & 1) ^ 1), a.err);
             if (ok) {
-                mbar_arrive_cnt(&sm.v8_full[vs], kStageArrivals);
+                mbar_arrive(&sm.v8_full[vs]);
                 vmark = true;
             }
             // wait (bounded) for the copies still in flight, also after a
@@ -488,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if ((cur.flags & kFlagFirst) && unit >= 2 && !mbar_wait(&sm.o_empty[ob], par_of(unit) ^ 1u, a.err))
                     break;
                 const int vs = j % kNV16;
-                if (!mbar_wait(&sm.v16_full[vs], (uint32_t)((j / kNV16) & 1), a.err)) break;
+                if (!mbar_wait(&sm.v16_full[vs], par_of(j), a.err)) break;
                 tc_fence_after();
                 const uint32_t va = smem_u32(sm.v16[vs]);
                 const uint32_t pa = smem_u32(sm.pt[j & 1]);
@@ -500,8 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bd = umma_desc_sw128(pa + kt * 2048, 8192, 1024);
                     umma_bf16(dO, ad, bd, idPV, ((cur.flags & kFlagFirst) && kt == 0) ? 0u : 1u);
                 }
-                umma_commit(&sm.v16_empty[vs]);
-                umma_commit(&sm.p_empty[j & 1]);
+                umma_commit(&sm.pv_done[j & 1]);
                 if (cur.flags & kFlagLast) umma_commit(&sm.o_full[ob]);
                 if (!next_done) {
                     ok = issue_s(j + 1, unit1, nxt);
@@ -513,75 +525,219 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
-        // ================================================= V converters
-        // Block j's E4M3 V pages -> one f16 tile in the MMA's layout (page p
-        // at p * 4 KB as [row half][d slab][8 rows][128 B], 128-byte swizzle),
-        // exact (the page scale is applied through P); rows past the
-        // sequence's last token and pages whose scale is 0 are zeroed.
-        // Thread ct converts the 16-byte group g = ct % 8 of rows r0 + 8 k
-        // (r0 = ct / 8, k = 0..15): its source and destination offsets are
-        // fixed plus k times 1 KB (source) and 2 KB (destination).
-        const int ct = (warp - kConvWarp0) * 32 + lane;
-        static_assert(kConvWarps * 32 == 64, "converter thread layout");
-        const int g = ct & 7, r0 = ct >> 3;
-        const int src_off = r0 * 128 + ((g ^ r0) << 4);
-        const int c0 = (g & 3) * 2;
-        const int dst_off = (g >> 2) * 1024 + r0 * 128;
-        const int dlo = ((c0 ^ r0) << 4), dhi = (((c0 + 1) ^ r0) << 4);
-        for (int j = 0;; ++j) {
-            const int s8 = j % kNV8, tb = j % kNV16;
-            if (!mbar_wait_sleep(&sm.v8_full[s8], (uint32_t)((j / kNV8) & 1), a.err, 32)) break;
-            const BlockMeta md = sm.meta[j % kNMeta];
-            if (md.flags & kFlagEnd) break;
-            if (j >= kNV16 && !mbar_wait_sleep(&sm.v16_empty[tb], (uint32_t)(((j / kNV16) & 1) ^ 1), a.err, 32))
-                break;
-            const uint8_t *src = sm.v8[s8] + src_off;
-            const float *scl = sm.vsc[j % kNMeta];
-            uint8_t *dst = sm.v16[tb] + dst_off;
-            if (lane < kPB && !(scl[lane] >= 0.f && scl[lane] <= 3.0e38f)) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
-            const int t_end = md.L + a.n_q - md.pos0;  // rows from t_end on are zeroed
+    } else if (warp >= kCvWarp0 && warp < kCvWarp0 + 4) {
+        // ================================================= V rows + epilogue
+        const int quarter = warp & 3;
+        const int t = quarter * 32 + lane;  // the V row (token) this thread converts; the head dimension it writes
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int G = a.G, M = a.M;
+        const int ew = warp - kCvWarp0;
+        constexpr int NE = kEpiWarps;
+        uint32_t ep_sp = 0;  // epi_sync phases passed
+        // A finished unit's rows, one thread per head dimension d = t (TMEM
+        // lane of O^T), while the softmax warps already work on later blocks;
+        // called once its statistics are published (stat_full of `unit`).
+        auto epilogue = [&](int unit) -> bool {
+            const int d = t;
+            const int b = sm.ep_b, h = sm.ep_h, split = sm.ep_split, nsplit = sm.ep_nsplit;
+            const int ob = unit & 1;
+            if (!mbar_wait_sleep(&sm.o_full[ob], par_of(unit), a.err, 32)) return false;
+            tc_fence_after();
+            const uint32_t oa = tmem + kTmemO + (uint32_t)ob * kMaxN + lane_off;
+            const int u2 = b * a.Hkv + h;
+            const size_t pr0 = ((size_t)u2 * a.max_splits + split) * M;
 #pragma unroll
-            for (int k0 = 0; k0 < 16; k0 += 4) {
-                uint4 e[4];
+            for (int c = 0; c < NPAD / 16; ++c) {
+                if (c * 16 < N) {
+                    uint32_t raw[16];
+                    tmem_ld16(oa + c * 16, raw);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int row = r0 + 8 * (k0 + u);
-                    e[u] = make_uint4(0, 0, 0, 0);
-                    if (row < t_end && (TILES || scl[row >> 4] > 0.f))
-                        e[u] = *reinterpret_cast<const uint4 *>(src + (k0 + u) * 1024);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int k = k0 + u, row = r0 + 8 * k;
-                    uint4 lo, hi;
-                    lo.x = e4m3x2_to_f16x2(e[u].x & 0xffffu);
-                    lo.y = e4m3x2_to_f16x2(e[u].x >> 16);
-                    lo.z = e4m3x2_to_f16x2(e[u].y & 0xffffu);
-                    lo.w = e4m3x2_to_f16x2(e[u].y >> 16);
-                    hi.x = e4m3x2_to_f16x2(e[u].z & 0xffffu);
-                    hi.y = e4m3x2_to_f16x2(e[u].z >> 16);
-                    hi.z = e4m3x2_to_f16x2(e[u].w & 0xffffu);
-                    hi.w = e4m3x2_to_f16x2(e[u].w >> 16);
-                    if constexpr (TILES) {
-                        if (row < t_end) {
-                            // this group's 64-element tile: (page, slot, half); a tile
-                            // scale multiplies the values in f16 (so at most 146)
-                            const float tsc = sm.ts.v[s8][row >> 4][(row & 15) * 2 + (g >> 2)];
-                            if (!(tsc >= 0.f && tsc <= 146.f)) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
-                            const uint32_t t2 = pack_f16x2(tsc, tsc);
-                            lo.x = mul_f16x2(lo.x, t2);
-                            lo.y = mul_f16x2(lo.y, t2);
-                            lo.z = mul_f16x2(lo.z, t2);
-                            lo.w = mul_f16x2(lo.w, t2);
-                            hi.x = mul_f16x2(hi.x, t2);
-                            hi.y = mul_f16x2(hi.y, t2);
-                            hi.z = mul_f16x2(hi.z, t2);
-                            hi.w = mul_f16x2(hi.w, t2);
+                    for (int e = 0; e < 16; ++e) {
+                        const int r = c * 16 + e;
+                        if (r < M) {
+                            const float2 st = sm.stat[r];
+                            const float o = __uint_as_float(raw[e]) * kOutScale;
+                            if (nsplit == 1) {
+                                const int jq = r / G, gi = r - jq * G;
+                                const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
+                                const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
+                                a.out[od * kD + d] = __float2bfloat16_rn(o * inv);
+                            } else {
+                                a.part_acc[(pr0 + r) * kD + d] = o;
+                            }
                         }
                     }
-                    *reinterpret_cast<uint4 *>(dst + k * 2048 + dlo) = lo;
-                    *reinterpret_cast<uint4 *>(dst + k * 2048 + dhi) = hi;
+                }
+            }
+            if (d < M) {
+                const float2 st = sm.stat[d];
+                if (nsplit == 1) {
+                    const int jq = d / G, gi = d - jq * G;
+                    const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
+                    if (a.lse) a.lse[od] = (st.x + __log2f(st.y)) * 0.69314718055994530942f;
+                } else {
+                    a.part_ml[(pr0 + d) * 2] = st.x;
+                    a.part_ml[(pr0 + d) * 2 + 1] = st.y;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sm.o_empty[ob]);
+                mbar_arrive(&sm.stat_empty);
+            }
+            if (nsplit == 1) return true;
+            __threadfence();
+            if (!group_sync(&sm.epi_sync, ep_sp, a.err)) return false;
+            if (ew == 0 && lane == 0) {
+                const int tk = atomicAdd(&a.tickets[u2], 1);
+                sm.last = (tk == nsplit - 1);
+                if (sm.last) a.tickets[u2] = 0;
+            }
+            if (!group_sync(&sm.epi_sync, ep_sp, a.err)) return false;
+            const int last = sm.last;
+            if (!group_sync(&sm.epi_sync, ep_sp, a.err)) return false;
+            if (!last) return true;
+            // the last split's CTA merges every split's partial rows with
+            // log-sum-exp weights (an online merge: running maximum, rescaled
+            // sum): one warp per row, 4 columns per lane, four rows and two
+            // splits per pass so that their loads are in flight together
+            __threadfence();
+            const size_t base = (size_t)u2 * a.max_splits * M;
+            for (int r0 = ew; r0 < M; r0 += 4 * NE) {
+                float mrow[4], lrow[4];
+                float4 o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    mrow[i] = -CUDART_INF_F;
+                    lrow[i] = 0.f;
+                    o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                for (int s0 = 0; s0 < nsplit; s0 += 2) {
+                    float2 ml[4][2];
+                    float4 v[4][2];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const int rr = r0 + NE * i;
+                            if (rr < M && s0 + k < nsplit) {
+                                const size_t pr = base + (size_t)(s0 + k) * M + rr;
+                                ml[i][k] = __ldcg(reinterpret_cast<const float2 *>(a.part_ml + pr * 2));
+                                v[i][k] = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + pr * kD) + lane);
+                            } else {
+                                ml[i][k] = make_float2(-CUDART_INF_F, 0.f);
+                                v[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                        }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const float mk = ml[i][k].x;
+                            if (mk == -CUDART_INF_F) continue;  // an empty split (or none)
+                            const float mn = fmaxf(mrow[i], mk);
+                            const float f_old = ex2_approx(mrow[i] - mn);
+                            const float f_new = ex2_approx(mk - mn);
+                            lrow[i] = lrow[i] * f_old + ml[i][k].y * f_new;
+                            o[i].x = o[i].x * f_old + v[i][k].x * f_new;
+                            o[i].y = o[i].y * f_old + v[i][k].y * f_new;
+                            o[i].z = o[i].z * f_old + v[i][k].z * f_new;
+                            o[i].w = o[i].w * f_old + v[i][k].w * f_new;
+                            mrow[i] = mn;
+                        }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = r0 + NE * i;
+                    if (rr >= M) break;
+                    const float inv2 = lrow[i] > 0.f ? 1.f / lrow[i] : 0.f;
+                    const int jq2 = rr / G, gi2 = rr - jq2 * G;
+                    const size_t od2 = (((size_t)b * a.n_q + jq2) * a.Hq + (size_t)h * G + gi2);
+                    uint2 v2;
+                    v2.x = pack_bf16x2(o[i].x * inv2, o[i].y * inv2);
+                    v2.y = pack_bf16x2(o[i].z * inv2, o[i].w * inv2);
+                    reinterpret_cast<uint2 *>(a.out + od2 * kD)[lane] = v2;
+                    if (lane == 0 && a.lse) a.lse[od2] = (mrow[i] + __log2f(lrow[i])) * 0.69314718055994530942f;
+                }
+            }
+            return true;
+        };
+
+        // V row t of every block: 128 E4M3 codes (one swizzled 128-byte row
+        // of the staged block) -> 128 f16 values (the code's value times
+        // 2^-8: its bits moved into place, exact for every finite code) in
+        // the MMA's layout: page t / 16 at 4 KB, [row half][d slab][8 rows][128 B]
+        const int r7 = t & 7;
+        const uint32_t src_off = (uint32_t)t * 128;
+        const uint32_t dst_off = (uint32_t)(t >> 3) * 2048 + (uint32_t)r7 * 128;
+        int eu = 0;          // the next unit to write out
+        bool ended = false;  // the softmax has signalled the end of the work
+        bool alive = true;
+        for (int j = 0;; ++j) {
+            const int s8 = j % kNV8, tb = j & 1;
+            if (!mbar_wait_sleep(&sm.v8_full[s8], (uint32_t)((j / kNV8) & 1), a.err, 32)) {
+                alive = false;
+                break;
+            }
+            const BlockMeta md = sm.meta[j % kNMeta];
+            if (md.flags & kFlagEnd) break;
+            // this row's page scale (the K stage copied it to shared memory;
+            // read from global memory here, an L2 hit): a page whose scale is
+            // 0 holds zero values whatever its codes
+            bool zero = false;
+            if constexpr (!TILES) {
+                const int id = sm.vid[j % kNMeta][t >> 4];
+                const float vs = (id >= 0 && id < a.num_blocks) ? __ldg(a.v_scale + (size_t)id * a.Hkv + md.h) : 1.f;
+                if (!(vs >= 0.f && vs <= 3.0e38f)) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                zero = !(vs > 0.f);
+            }
+            // the V16 buffer is free once PV_{j-2} is done
+            if (j >= 2 && !mbar_wait_sleep(&sm.pv_done[tb], par_of(j - 2), a.err, 32)) {
+                alive = false;
+                break;
+            }
+            const uint8_t *src = sm.v8[s8] + src_off;
+            uint8_t *dst = sm.v16[tb] + dst_off;
+#pragma unroll
+            for (int c2 = 0; c2 < 8; c2 += 4) {
+                uint4 e[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    e[u] = zero ? make_uint4(0, 0, 0, 0)
+                                : *reinterpret_cast<const uint4 *>(src + (((c2 + u) ^ r7) << 4));
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c2 + u;  // d 16 c .. 16 c + 15
+                    uint4 lo, hi;
+                    lo.x = e4m3x2_to_f16x2_scaled(e[u].x, 0x4140u);
+                    lo.y = e4m3x2_to_f16x2_scaled(e[u].x, 0x4342u);
+                    lo.z = e4m3x2_to_f16x2_scaled(e[u].y, 0x4140u);
+                    lo.w = e4m3x2_to_f16x2_scaled(e[u].y, 0x4342u);
+                    hi.x = e4m3x2_to_f16x2_scaled(e[u].z, 0x4140u);
+                    hi.y = e4m3x2_to_f16x2_scaled(e[u].z, 0x4342u);
+                    hi.z = e4m3x2_to_f16x2_scaled(e[u].w, 0x4140u);
+                    hi.w = e4m3x2_to_f16x2_scaled(e[u].w, 0x4342u);
+                    if constexpr (TILES) {
+                        // this half's 64-element tile scale, in f16 (the values
+                        // are at most 1.75 here, so scales up to 32768)
+                        const float tsc = sm.ts.v[s8][t >> 4][(t & 15) * 2 + (c >> 2)];
+                        if (!(tsc >= 0.f && tsc <= 32768.f)) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                        const uint32_t t2 = pack_f16x2(tsc, tsc);
+                        lo.x = mul_f16x2(lo.x, t2);
+                        lo.y = mul_f16x2(lo.y, t2);
+                        lo.z = mul_f16x2(lo.z, t2);
+                        lo.w = mul_f16x2(lo.w, t2);
+                        hi.x = mul_f16x2(hi.x, t2);
+                        hi.y = mul_f16x2(hi.y, t2);
+                        hi.z = mul_f16x2(hi.z, t2);
+                        hi.w = mul_f16x2(hi.w, t2);
+                    }
+                    const int c0 = (c & 3) * 2;
+                    uint8_t *drow = dst + (c >> 2) * 1024;
+                    *reinterpret_cast<uint4 *>(drow + ((c0 ^ r7) << 4)) = lo;
+                    *reinterpret_cast<uint4 *>(drow + (((c0 + 1) ^ r7) << 4)) = hi;
                 }
             }
             fence_proxy_async_smem();
@@ -590,6 +746,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&sm.v16_full[tb]);
                 mbar_arrive(&sm.v8_empty[s8]);
             }
+            // a finished unit whose statistics are published: write it out
+            // (its O^T is double-buffered; the MMA reuses it two units later)
+            if (!ended && mbar_test(&sm.stat_full, (uint32_t)(eu & 1))) {
+                if (sm.ep_end) {
+                    ended = true;
+                } else {
+                    if (!epilogue(eu)) {
+                        alive = false;
+                        break;
+                    }
+                    ++eu;
+                }
+            }
+        }
+        // the units still to write out, until the softmax signals the end
+        while (alive && !ended) {
+            if (!mbar_wait_sleep(&sm.stat_full, (uint32_t)(eu & 1), a.err, 128)) break;
+            if (sm.ep_end) break;
+            if (!epilogue(eu)) break;
+            ++eu;
         }
     } else if (warp >= kSoftWarp0 && warp < kSoftWarp0 + 4) {
         // ================================================= softmax
@@ -657,9 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.s_empty[j & 1]);  // S^T_j's buffer is free
 
-            // the block's page scales arrive with its V pages: V_j converted
-            // (this wait also keeps the converters within the descriptor ring)
-            mbar_wait(&sm.v16_full[j % kNV16], (uint32_t)((j / kNV16) & 1), a.err);
+            // (the block's page scales came with its K pages)
             const int L = md.L, T = L + a.n_q, p = md.pos0 + t;
             const bool valid = t < md.ntok && p < T;
             const float kscale = TILES ? 1.f : sm.ksc[j % kNMeta][t >> 4];
@@ -742,7 +916,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (rescale) {
                     // O^T holds P_{<j} V of this unit: scale each row's column
                     // once PV_{j-1} has landed (lane = head dimension t)
-                    mbar_wait(&sm.p_empty[(j - 1) & 1], par_of(j - 1), a.err);
+                    mbar_wait(&sm.pv_done[(j - 1) & 1], par_of(j - 1), a.err);
                     tc_fence_after();
                     const uint32_t oa = tmem + kTmemO + (uint32_t)(unit & 1) * kMaxN + lane_off;
 #pragma unroll
@@ -763,7 +937,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // P'^T_j: f16 pairs (r, r + 1) of this token, 2^(x - m), into the
             // P^T buffer once PV_{j-2} has read it
-            if (j >= 2) mbar_wait(&sm.p_empty[j & 1], par_of(j - 2), a.err);
+            if (j >= 2) mbar_wait(&sm.pv_done[j & 1], par_of(j - 2), a.err);
             uint8_t *prow = sm.pt[j & 1] + (t >> 3) * 1024 + (t & 7) * 128;
             const float4 *m4 = reinterpret_cast<const float4 *>(sm.mref[cur]);
 #pragma unroll
@@ -825,144 +999,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&sm.stat_full);
             }
             ++j;
-        }
-    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
-        // ================================================= epilogue
-        // One thread per head dimension (TMEM lane of O^T) writes a finished
-        // unit's rows while the softmax warps already work on the next unit.
-        const int quarter = warp & 3;
-        const int d = quarter * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const int G = a.G, M = a.M;
-        const int ew = warp - kEpiWarp0;
-        constexpr int NE = kEpiWarps;
-        uint32_t ep_sp = 0;  // epi_sync phases passed
-        for (int unit = 0;; ++unit) {
-            // (a whole unit away: sleep between probes)
-            if (!mbar_wait_sleep(&sm.stat_full, (uint32_t)(unit & 1), a.err, 256)) break;
-            if (sm.ep_end) break;
-            const int b = sm.ep_b, h = sm.ep_h, split = sm.ep_split, nsplit = sm.ep_nsplit;
-            const int ob = unit & 1;
-            if (!mbar_wait_sleep(&sm.o_full[ob], par_of(unit), a.err, 32)) break;
-            tc_fence_after();
-            const uint32_t oa = tmem + kTmemO + (uint32_t)ob * kMaxN + lane_off;
-            const int u2 = b * a.Hkv + h;
-            const size_t pr0 = ((size_t)u2 * a.max_splits + split) * M;
-#pragma unroll
-            for (int c = 0; c < NPAD / 16; ++c) {
-                if (c * 16 < N) {
-                    uint32_t raw[16];
-                    tmem_ld16(oa + c * 16, raw);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int r = c * 16 + e;
-                        if (r < M) {
-                            const float2 st = sm.stat[r];
-                            if (nsplit == 1) {
-                                const int jq = r / G, gi = r - jq * G;
-                                const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
-                                const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
-                                a.out[od * kD + d] = __float2bfloat16_rn(__uint_as_float(raw[e]) * inv);
-                            } else {
-                                a.part_acc[(pr0 + r) * kD + d] = __uint_as_float(raw[e]);
-                            }
-                        }
-                    }
-                }
-            }
-            if (d < M) {
-                const float2 st = sm.stat[d];
-                if (nsplit == 1) {
-                    const int jq = d / G, gi = d - jq * G;
-                    const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
-                    if (a.lse) a.lse[od] = (st.x + __log2f(st.y)) * 0.69314718055994530942f;
-                } else {
-                    a.part_ml[(pr0 + d) * 2] = st.x;
-                    a.part_ml[(pr0 + d) * 2 + 1] = st.y;
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&sm.o_empty[ob]);
-                mbar_arrive(&sm.stat_empty);
-            }
-            if (nsplit == 1) continue;
-            __threadfence();
-            if (!group_sync(&sm.epi_sync, ep_sp, a.err)) break;
-            if (ew == 0 && lane == 0) {
-                const int tk = atomicAdd(&a.tickets[u2], 1);
-                sm.last = (tk == nsplit - 1);
-                if (sm.last) a.tickets[u2] = 0;
-            }
-            if (!group_sync(&sm.epi_sync, ep_sp, a.err)) break;
-            const int last = sm.last;
-            if (!group_sync(&sm.epi_sync, ep_sp, a.err)) break;
-            if (!last) continue;
-            // the last split's CTA merges every split's partial rows with
-            // log-sum-exp weights (an online merge: running maximum, rescaled
-            // sum): one warp per row, 4 columns per lane, four rows and two
-            // splits per pass so that their loads are in flight together
-            __threadfence();
-            const size_t base = (size_t)u2 * a.max_splits * M;
-            for (int r0 = ew; r0 < M; r0 += 4 * NE) {
-                float mrow[4], lrow[4];
-                float4 o[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    mrow[i] = -CUDART_INF_F;
-                    lrow[i] = 0.f;
-                    o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                for (int s0 = 0; s0 < nsplit; s0 += 2) {
-                    float2 ml[4][2];
-                    float4 v[4][2];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-#pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            const int rr = r0 + NE * i;
-                            if (rr < M && s0 + k < nsplit) {
-                                const size_t pr = base + (size_t)(s0 + k) * M + rr;
-                                ml[i][k] = __ldcg(reinterpret_cast<const float2 *>(a.part_ml + pr * 2));
-                                v[i][k] = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + pr * kD) + lane);
-                            } else {
-                                ml[i][k] = make_float2(-CUDART_INF_F, 0.f);
-                                v[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            }
-                        }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-#pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            const float mk = ml[i][k].x;
-                            if (mk == -CUDART_INF_F) continue;  // an empty split (or none)
-                            const float mn = fmaxf(mrow[i], mk);
-                            const float f_old = ex2_approx(mrow[i] - mn);
-                            const float f_new = ex2_approx(mk - mn);
-                            lrow[i] = lrow[i] * f_old + ml[i][k].y * f_new;
-                            o[i].x = o[i].x * f_old + v[i][k].x * f_new;
-                            o[i].y = o[i].y * f_old + v[i][k].y * f_new;
-                            o[i].z = o[i].z * f_old + v[i][k].z * f_new;
-                            o[i].w = o[i].w * f_old + v[i][k].w * f_new;
-                            mrow[i] = mn;
-                        }
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int rr = r0 + NE * i;
-                    if (rr >= M) break;
-                    const float inv2 = lrow[i] > 0.f ? 1.f / lrow[i] : 0.f;
-                    const int jq2 = rr / G, gi2 = rr - jq2 * G;
-                    const size_t od2 = (((size_t)b * a.n_q + jq2) * a.Hq + (size_t)h * G + gi2);
-                    uint2 v2;
-                    v2.x = pack_bf16x2(o[i].x * inv2, o[i].y * inv2);
-                    v2.y = pack_bf16x2(o[i].z * inv2, o[i].w * inv2);
-                    reinterpret_cast<uint2 *>(a.out + od2 * kD)[lane] = v2;
-                    if (lane == 0 && a.lse) a.lse[od2] = (mrow[i] + __log2f(lrow[i])) * 0.69314718055994530942f;
-                }
-            }
         }
     }
     // every TMEM user is done before the owner frees it
