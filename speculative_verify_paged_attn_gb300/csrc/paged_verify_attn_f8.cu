@@ -673,6 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t src_off = (uint32_t)t * 128;
         const uint32_t dst_off = (uint32_t)(t >> 3) * 2048 + (uint32_t)r7 * 128;
         int eu = 0;          // the next unit to write out
+        int ucv = 0;         // units whose last block this warp has converted
         bool ended = false;  // the softmax has signalled the end of the work
         bool alive = true;
         for (int j = 0;; ++j) {
@@ -746,9 +747,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&sm.v16_full[tb]);
                 mbar_arrive(&sm.v8_empty[s8]);
             }
+            if (md.flags & kFlagLast) ++ucv;
             // a finished unit whose statistics are published: write it out
-            // (its O^T is double-buffered; the MMA reuses it two units later)
-            if (!ended && mbar_test(&sm.stat_full, (uint32_t)(eu & 1))) {
+            // (its O^T is double-buffered; the MMA reuses it two units later).
+            // Only once this warp has converted the unit's last block: the
+            // softmax runs ahead of V, and the unit's last PV needs that block.
+            if (!ended && eu < ucv && mbar_test(&sm.stat_full, (uint32_t)(eu & 1))) {
                 if (sm.ep_end) {
                     ended = true;
                 } else {
