@@ -77,6 +77,7 @@ constexpr int kSoftWarp0 = 2, kCvWarp0 = 6, kEpiWarps = 4;
 // K stage: expect_tx + one arrival per page for its two scale copies (cp.async)
 constexpr uint32_t kStageArrivals = 1 + kPB;
 constexpr float kOutScale = 256.f;           // V is held in f16 as its value times 2^-8
+constexpr int kBarVote = 2, kBarSoft = 3;    // named barriers of the four softmax warps
 constexpr int kTileScales = 16 * (kD / 64);   // tile scales of one (page, kv head)
 constexpr float kRescaleLog2 = 8.f;           // a new reference maximum when a score passes it by 2^8
 constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagEnd = 4;
@@ -99,7 +100,7 @@ struct SmemF8 {
     uint8_t v8[kNV8][kTile8];
     uint8_t v16[kNV16][kTile16];     // A operand of O^T
     uint8_t pt[2][kPtTile];          // B operand of O^T
-    uint8_t qs[2][kMaxN * 128];      // B operand of S^T: high and low query terms
+    uint8_t qs[2][kMaxN * 128];      // B operand of S^T: high then low query terms (rows 0..2N-1)
     float ksc[kNMeta][kPB];
     float vsc[kNMeta][kPB];
     float mref[2][kMaxN];            // reference maximum of each row (log2 units, V scale included),
@@ -118,8 +119,9 @@ struct SmemF8 {
     uint64_t pv_done[2];             // PV_j done: its V16 and P^T buffers (j % 2) are free
     uint64_t o_full[2], o_empty[2];
     uint64_t stat_full, stat_empty;
-    uint64_t soft_sync, epi_sync;    // group barriers of the softmax and of the converter/epilogue warps
-    int32_t vote[2][4];              // the softmax warps' votes, by barrier phase parity
+    uint64_t epi_sync;               // group barrier of the converter/epilogue warps
+    float vsc_v[kNV8][kPB];          // the V page scales again, staged with V (for the converters)
+    int32_t soft_dead;               // a softmax wait ran out: the four warps leave together
     int32_t ep_b, ep_h, ep_split, ep_nsplit, ep_end;
     uint32_t tmem_base;
     int32_t last;
@@ -197,6 +199,22 @@ __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, int32
 
 __device__ __forceinline__ uint32_t par_of(int idx) { return (uint32_t)((idx >> 1) & 1); }
 
+// Barrier of the four softmax warps (named barrier kBarVote, 128 threads)
+// that also returns whether any of them passed `pred`.  The four warps reach
+// it at the same points in the same order: their control flow depends only on
+// values they all read alike, and a wait of theirs that runs out is turned
+// into a vote that ends the loop for all four together.
+__device__ __forceinline__ bool soft_any(bool pred) {
+    uint32_t any;
+    asm volatile(
+        "{\n\t.reg .pred q, w;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred w, %2, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, w;\n\t}"
+        : "=r"(any)
+        : "r"((uint32_t)pred), "n"(kBarVote)
+        : "memory");
+    return any != 0;
+}
+
 // Two E4M3 codes of w (the bytes `sel` picks: 0x4140 bytes 0 and 1, 0x4342
 // bytes 2 and 3) to an f16 pair holding each code's value times 2^-8: the
 // sign goes to bit 15, exponent and mantissa bits to bits 7..13.  An E4M3
@@ -226,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.k8_empty[i], 1);
         }
         for (int i = 0; i < kNV8; ++i) {
-            mbar_init(&sm.v8_full[i], 1);
+            mbar_init(&sm.v8_full[i], kStageArrivals);
             mbar_init(&sm.v8_empty[i], 4);
         }
         for (int i = 0; i < kNV16; ++i) mbar_init(&sm.v16_full[i], 4);
@@ -242,15 +260,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&sm.stat_full, 4);
         mbar_init(&sm.stat_empty, kEpiWarps);
-        mbar_init(&sm.soft_sync, 4);
         mbar_init(&sm.epi_sync, kEpiWarps);
+        sm.soft_dead = 0;
         fence_mbar_init();
     }
     // references start at -inf (rows past the query rows stay there)
     for (int i = threadIdx.x; i < 2 * kMaxN; i += blockDim.x) sm.mref[i / kMaxN][i % kMaxN] = -CUDART_INF_F;
-    // TMEM columns: S^T[x] at 64 x (x = 0, 1), O^T[x] at 128 + 64 x; with
-    // tile scales the scores of d 64..127 go to a second tile at 256 + 64 x
-    constexpr uint32_t kTmemS = 0, kTmemO = 128, kTmemCols = TILES ? 512 : 256;
+    // TMEM columns: S^T[x] at 128 x (x = 0, 1): the high and low query terms'
+    // scores (page scales), or the two halves of d (tile scales), 2 x 64;
+    // O^T[x] at 256 + 64 x
+    constexpr uint32_t kTmemS = 0, kTmemO = 256, kTmemCols = 512;
     if (warp == 1) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
@@ -300,6 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane < kPB) {
                 const int id = sm.vid[jv % kNMeta][lane], hh = sm.meta[jv % kNMeta].h;
                 tma_load_4d(sm.v8[vs] + lane * kPage8, &mvp, 0, 0, hh, id, &sm.v8_full[vs], pol);
+                // the page's V scale for the converters, on the same barrier
+                const int id0 = __shfl_sync(0x000000ffu, id, 0);
+                const int sid = (id >= 0 && id < a.num_blocks) ? id : id0;
+                cp_async_4(&sm.vsc_v[vs][lane], a.v_scale + (size_t)sid * a.Hkv + hh);
+                cp_async_mbar_arrive_noinc(&sm.v8_full[vs]);
                 if constexpr (TILES) copy_tile_scales(a.v_scale, id, hh, sm.ts.v[vs][lane], &sm.v8_full[vs]);
             }
             __syncwarp();
@@ -421,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int vs = jv % kNV8;
             if (ok && jv >= kNV8) ok = mbar_wait(&sm.v8_empty[vs], (uint32_t)(((jv / kNV8) & 1) ^ 1), a.err);
             if (ok) {
-                mbar_arrive(&sm.v8_full[vs]);
+                mbar_arrive_cnt(&sm.v8_full[vs], kStageArrivals);
                 vmark = true;
             }
             // wait (bounded) for the copies still in flight, also after a
@@ -445,7 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ================================================= MMA issuer
         if (lane == 0) {
-            const uint32_t idS = idesc_f8(kNB, N);
+            // page scales: one MMA per K step over both query terms (B rows
+            // 0..N-1 high, N..2N-1 low: N = 2 N columns of S^T, added by the
+            // softmax); tile scales: a tile per half of d, the terms in turn
+            const uint32_t idS = idesc_f8(kNB, TILES ? N : 2 * N);
             const uint32_t idPV = idesc_f16_mn(kNB, N);
             const uint32_t qa = smem_u32(&sm.qs[0][0]);
             // S^T_jj = K_jj (Q_hi + Q_lo)^T once K_jj has landed (or forward the end marker)
@@ -465,20 +492,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (jj >= 2 && !mbar_wait(&sm.s_empty[jj & 1], par_of(jj - 2), a.err)) return false;
                 tc_fence_after();
                 const uint32_t ka = smem_u32(sm.k8[ks]);
-                const uint32_t dS = tmem + kTmemS + (uint32_t)(jj & 1) * kMaxN;
+                const uint32_t dS = tmem + kTmemS + (uint32_t)(jj & 1) * 2 * kMaxN;
+                if constexpr (TILES) {
 #pragma unroll
-                for (int term = 0; term < 2; ++term)
+                    for (int term = 0; term < 2; ++term)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = umma_desc_sw128(ka + kk * 32, 16, 1024);
+                            const uint64_t bd = umma_desc_sw128(qa + term * N * 128 + kk * 32, 16, 1024);
+                            // columns 0..63 and 64..127 of d into separate tiles
+                            umma_f8(dS + (uint32_t)(kk >> 1) * kMaxN, ad, bd, idS, (term | (kk & 1)) ? 1u : 0u);
+                        }
+                } else {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = umma_desc_sw128(ka + kk * 32, 16, 1024);
-                        const uint64_t bd = umma_desc_sw128(qa + term * (kMaxN * 128) + kk * 32, 16, 1024);
-                        if constexpr (TILES) {
-                            // columns 0..63 and 64..127 of d into separate tiles
-                            umma_f8(dS + (uint32_t)(kk >> 1) * 256, ad, bd, idS, (term | (kk & 1)) ? 1u : 0u);
-                        } else {
-                            umma_f8(dS, ad, bd, idS, (term | kk) ? 1u : 0u);
-                        }
+                        const uint64_t bd = umma_desc_sw128(qa + kk * 32, 16, 1024);
+                        umma_f8(dS, ad, bd, idS, kk ? 1u : 0u);
                     }
+                }
                 umma_commit(&sm.k8_empty[ks]);
                 umma_commit(&sm.s_full[jj & 1]);
                 if (m.flags & kFlagLast) umma_commit(&sm.qs_empty);
@@ -684,13 +716,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const BlockMeta md = sm.meta[j % kNMeta];
             if (md.flags & kFlagEnd) break;
-            // this row's page scale (the K stage copied it to shared memory;
-            // read from global memory here, an L2 hit): a page whose scale is
-            // 0 holds zero values whatever its codes
+            // this row's page scale (staged with the V pages): a page whose
+            // scale is 0 holds zero values whatever its codes
             bool zero = false;
             if constexpr (!TILES) {
-                const int id = sm.vid[j % kNMeta][t >> 4];
-                const float vs = (id >= 0 && id < a.num_blocks) ? __ldg(a.v_scale + (size_t)id * a.Hkv + md.h) : 1.f;
+                const float vs = sm.vsc_v[s8][t >> 4];
                 if (!(vs >= 0.f && vs <= 3.0e38f)) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
                 zero = !(vs > 0.f);
             }
@@ -701,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint8_t *src = sm.v8[s8] + src_off;
             uint8_t *dst = sm.v16[tb] + dst_off;
-#pragma unroll
+#pragma unroll 1
             for (int c2 = 0; c2 < 8; c2 += 4) {
                 uint4 e[4];
 #pragma unroll
@@ -781,12 +811,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int r = 0; r < NPAD; ++r) lsum[r] = 0.f;
         int j = 0, unit = -1, cur = 0;                       // cur: the current reference set
-        uint32_t sp = 0;                                     // soft_sync phases passed
+        bool dead = false;                                   // a wait of this thread ran out
         while (true) {
-            if (!mbar_wait(&sm.s_full[j & 1], par_of(j), a.err)) break;
+            // S^T_j; a wait that ran out (here or in the previous block)
+            // ends the loop for the four warps together
+            if (!mbar_wait(&sm.s_full[j & 1], par_of(j), a.err)) dead = true;
+            if (soft_any(dead)) break;
             const BlockMeta md = sm.meta[j % kNMeta];
             if (md.flags & kFlagEnd) {
-                // tell the epilogue warps there is no further unit
+                // tell the epilogue there is no further unit
                 if (unit >= 0) mbar_wait(&sm.stat_empty, (uint32_t)(unit & 1), a.err);
                 if (threadIdx.x == kSoftWarp0 * 32) sm.ep_end = 1;
                 __syncwarp();
@@ -800,33 +833,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int r = 0; r < NPAD; ++r) lsum[r] = 0.f;
             }
             tc_fence_after();
-            // this token's raw scores against every query row (TILES: the two
-            // 64-element halves of d, each times its tile scale)
+            // this token's scores against every query row: the high and low
+            // query terms' columns added (page scales), or the two halves of
+            // d each times its tile scale
             float x[NPAD];
             {
                 float k0 = 1.f, k1 = 1.f;
+                uint32_t second = (uint32_t)N;
                 if constexpr (TILES) {
                     k0 = sm.ts.k[j % kNMeta][t >> 4][(t & 15) * 2];
                     k1 = sm.ts.k[j % kNMeta][t >> 4][(t & 15) * 2 + 1];
+                    second = kMaxN;
                 }
-                const uint32_t sa = tmem + kTmemS + (uint32_t)(j & 1) * kMaxN + lane_off;
+                const uint32_t sa = tmem + kTmemS + (uint32_t)(j & 1) * 2 * kMaxN + lane_off;
 #pragma unroll
                 for (int c = 0; c < NPAD / 16; ++c) {
                     if (c * 16 < N) {  // (uniform)
-                        uint32_t raw[16];
-                        tmem_ld16(sa + c * 16, raw);
-                        if constexpr (TILES) {
-                            uint32_t raw1[16];
-                            tmem_ld16(sa + 256 + c * 16, raw1);
-                            tmem_ld_wait();
+                        uint32_t r0[16], r1[16];
+                        tmem_ld16(sa + c * 16, r0);
+                        tmem_ld16(sa + second + c * 16, r1);
+                        tmem_ld_wait();
 #pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                x[c * 16 + e] = __uint_as_float(raw[e]) * k0 + __uint_as_float(raw1[e]) * k1;
-                        } else {
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) x[c * 16 + e] = __uint_as_float(raw[e]);
-                        }
+                        for (int e = 0; e < 16; ++e)
+                            x[c * 16 + e] = TILES ? __uint_as_float(r0[e]) * k0 + __uint_as_float(r1[e]) * k1
+                                                  : __uint_as_float(r0[e]) + __uint_as_float(r1[e]);
                     } else {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) x[c * 16 + e] = 0.f;
@@ -837,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.s_empty[j & 1]);  // S^T_j's buffer is free
 
-            // (the block's page scales came with its K pages)
+            // page scales (both came with the block's K pages)
             const int L = md.L, T = L + a.n_q, p = md.pos0 + t;
             const bool valid = t < md.ntok && p < T;
             const float kscale = TILES ? 1.f : sm.ksc[j % kNMeta][t >> 4];
@@ -861,10 +891,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // reference maxima: the shared ones, unless a score passes one by
-            // 2^8 (or the unit starts); then the block's row maxima, reduced
-            // over the 128 tokens, replace the references they pass
-            // (after a unit's first block every reference is finite: each row
-            // sees at least its own slot, padding rows see every valid token)
+            // 2^8 (or the unit starts): then the block's row maxima, reduced
+            // over the 128 tokens, replace the references they pass.  (After
+            // a unit's first block every reference is finite: each row sees
+            // at least its own slot, padding rows every valid token.)
             bool pass = false;
             if (!first) {
                 const float4 *m4 = reinterpret_cast<const float4 *>(sm.mref[cur]);
@@ -877,16 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 pass = mx > kRescaleLog2;
             }
-            bool slow = first;
-            if (!first) {
-                // one vote of the four warps (the flags by barrier phase parity)
-                const bool wpass = __any_sync(0xffffffffu, pass);
-                if (lane == 0) sm.vote[sp & 1][quarter] = wpass;
-                const uint32_t ph = sp;
-                if (!group_sync(&sm.soft_sync, sp, a.err)) break;
-                slow = sm.vote[ph & 1][0] | sm.vote[ph & 1][1] | sm.vote[ph & 1][2] | sm.vote[ph & 1][3];
-            }
-            if (slow) {  // (uniform)
+            if (first || soft_any(pass)) {  // (uniform)
 #pragma unroll
                 for (int r = 0; r < NPAD; ++r) {
                     if (r < N) {
@@ -894,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (lane == 0) sm.red[quarter][r] = bm;
                     }
                 }
-                if (!group_sync(&sm.soft_sync, sp, a.err)) break;
+                named_barrier_sync(kBarSoft, 128);
                 bool rescale = false;
 #pragma unroll
                 for (int r = 0; r < NPAD; ++r) {
@@ -915,12 +936,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 rescale &= !first;  // (O^T starts from zero at a unit's first block)
-                if (!group_sync(&sm.soft_sync, sp, a.err)) break;  // new references written, red free
+                named_barrier_sync(kBarSoft, 128);  // new references written, red free
                 cur ^= 1;
                 if (rescale) {
                     // O^T holds P_{<j} V of this unit: scale each row's column
                     // once PV_{j-1} has landed (lane = head dimension t)
-                    mbar_wait(&sm.pv_done[(j - 1) & 1], par_of(j - 1), a.err);
+                    if (!mbar_wait(&sm.pv_done[(j - 1) & 1], par_of(j - 1), a.err)) dead = true;
                     tc_fence_after();
                     const uint32_t oa = tmem + kTmemO + (uint32_t)(unit & 1) * kMaxN + lane_off;
 #pragma unroll
@@ -941,7 +962,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // P'^T_j: f16 pairs (r, r + 1) of this token, 2^(x - m), into the
             // P^T buffer once PV_{j-2} has read it
-            if (j >= 2) mbar_wait(&sm.pv_done[j & 1], par_of(j - 2), a.err);
+            if (j >= 2 && !mbar_wait(&sm.pv_done[j & 1], par_of(j - 2), a.err)) dead = true;
             uint8_t *prow = sm.pt[j & 1] + (t >> 3) * 1024 + (t & 7) * 128;
             const float4 *m4 = reinterpret_cast<const float4 *>(sm.mref[cur]);
 #pragma unroll
@@ -953,9 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int r = c * 8 + 2 * e;
-                        const float z0 = x[r] - mr[2 * e];
-                        const float z1 = x[r + 1] - mr[2 * e + 1];
-                        const uint32_t p2 = ex2_f16x2(pack_f16x2(z0, z1));
+                        const uint32_t p2 = ex2_f16x2(pack_f16x2(x[r] - mr[2 * e], x[r + 1] - mr[2 * e + 1]));
                         const float2 f = f16x2_to_float2(p2);
                         lsum[r] = fmaf(f.x, inv_v, lsum[r]);
                         lsum[r + 1] = fmaf(f.y, inv_v, lsum[r + 1]);
@@ -985,10 +1004,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         lsum[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
                     }
                 }
-                if (unit >= 1) mbar_wait(&sm.stat_empty, (uint32_t)((unit - 1) & 1), a.err);
+                if (unit >= 1 && !mbar_wait(&sm.stat_empty, (uint32_t)((unit - 1) & 1), a.err)) dead = true;
 #pragma unroll
                 for (int i = 0; i < RC / 32; ++i) sm.red[quarter][(RC / 32) * lane + i] = lsum[i];
-                if (!group_sync(&sm.soft_sync, sp, a.err)) break;
+                named_barrier_sync(kBarSoft, 128);
                 if (t < RC)
                     sm.stat[t] = make_float2(sm.mref[cur][t],
                                              (sm.red[0][t] + sm.red[1][t]) + (sm.red[2][t] + sm.red[3][t]));
@@ -999,7 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sm.ep_nsplit = md.nsplit;
                     sm.ep_end = 0;
                 }
-                if (!group_sync(&sm.soft_sync, sp, a.err)) break;  // red free again, stat complete
+                named_barrier_sync(kBarSoft, 128);  // red free again, stat complete
                 if (lane == 0) mbar_arrive(&sm.stat_full);
             }
             ++j;
@@ -1015,8 +1034,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The queries of every (sequence, kv head) as two E4M3 terms for the score
 // MMA: with c = 2^(e - 8) where amax = m 2^e (m in [1/2, 1)), v = q / c lies
 // in (-256, 256); hi = E4M3(v), lo = E4M3(v - hi), both round-to-nearest-even
-// (hi + lo carries a bf16 query's 8 significant bits).  Rows G * n_q .. 63
-// are zero.  One CTA per (sequence, kv head); the record goes straight into
+// (hi + lo carries a bf16 query's 8 significant bits).  Record rows 0..N-1
+// hold the high terms and N..2N-1 the low terms (N = G * n_q rounded up to
+// 16; rows of the padding and past 2N are zero), so one MMA of N' = 2N
+// columns scores both.  One CTA per (sequence, kv head); the record goes straight into
 // the attention kernel's shared memory by one bulk copy.
 __global__ void __launch_bounds__(128) qsplit_kernel(const __grid_constant__ AttnArgs a, uint8_t *qrec) {
     // the attention kernel may launch now; it waits for this grid before
@@ -1056,10 +1077,15 @@ __global__ void __launch_bounds__(128) qsplit_kernel(const __grid_constant__ Att
     const float c = amax > 0.f ? ldexpf(1.f, e2 - 8) : 1.f;
     const float inv_c = 1.f / c;  // a power of two: exact
     uint8_t *rec = qrec + (size_t)u * kQRecord;
-    for (int i = tid; i < kMaxN * 8; i += 128) {
-        const int r = i >> 3, c8 = i & 7;
+    // record rows: the high terms of query rows 0..N-1 (N = a.npad, rows M..N-1
+    // zero), then the low terms of the same rows, then zeros up to row 127
+    const int N = a.npad;
+    for (int i = tid; i < 2 * kMaxN * 8; i += 128) {
+        const int pos = i >> 3, c8 = i & 7;
+        const bool low = pos >= N;
+        const int r = low ? pos - N : pos;
         uint4 hi16 = make_uint4(0, 0, 0, 0), lo16 = make_uint4(0, 0, 0, 0);
-        if (r < M) {
+        if (r < M && pos < 2 * N) {
             const int jq = r / G, gi = r - jq * G;
             const uint4 *src = reinterpret_cast<const uint4 *>(
                 a.q + (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi) * kD + c8 * 16);
@@ -1089,11 +1115,10 @@ __global__ void __launch_bounds__(128) qsplit_kernel(const __grid_constant__ Att
             hi16 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             lo16 = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
-        const size_t off = (size_t)(r >> 3) * 1024 + (r & 7) * 128 + ((c8 ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4 *>(rec + off) = hi16;
-        *reinterpret_cast<uint4 *>(rec + kMaxN * 128 + off) = lo16;
+        const size_t off = (size_t)(pos >> 3) * 1024 + (pos & 7) * 128 + ((c8 ^ (pos & 7)) << 4);
+        *reinterpret_cast<uint4 *>(rec + off) = low ? lo16 : hi16;
     }
-    if (tid == 0) *reinterpret_cast<float4 *>(rec + 2 * kMaxN * 128) = make_float4(c, 0.f, 0.f, 0.f);
+    if (tid == 0) *reinterpret_cast<float4 *>(rec + kQCodes) = make_float4(c, 0.f, 0.f, 0.f);
 }
 
 template <int NPAD, bool TILES>
