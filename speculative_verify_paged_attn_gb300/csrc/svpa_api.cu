@@ -56,12 +56,11 @@ int sm_count() {
 }
 
 struct AttnPlan {
-    int M, split_pages, max_splits;
+    int M, split_pages, max_splits, part_slots;
     bool use_tc;
-    bool f8;             // FP8 pages on the tensor cores: the split-query kernel, then pva_f8_kernel
     int grid_slots;      // resident CTAs of the chosen kernel
     bool ordered;        // units handed out longest sequence first
-    size_t off_order, off_ml, off_acc, off_qrec, bytes;
+    size_t off_order, off_ml, off_acc, bytes;
 };
 
 svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
@@ -130,18 +129,16 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     pl->off_order = off;
     if (pl->ordered) off += align_up((size_t)p->batch * sizeof(int32_t));
     pl->off_ml = off;
-    if (pl->max_splits > 1) {
-        off += align_up(units * pl->max_splits * M * 2 * sizeof(float));
+    // FP8 pages with per-page scales on tcgen05: each split leaves two partial
+    // rows per query row (the two token halves of every block), merged like splits
+    pl->part_slots = (pl->use_tc && eb == 1 && p->scale_tile == 0) ? 2 * pl->max_splits : pl->max_splits;
+    if (pl->part_slots > 1) {
+        off += align_up(units * pl->part_slots * M * 2 * sizeof(float));
         pl->off_acc = off;
-        off += align_up(units * pl->max_splits * M * D * sizeof(float));
+        off += align_up(units * pl->part_slots * M * D * sizeof(float));
     } else {
         pl->off_acc = off;
     }
-    // FP8 pages on the tensor cores: each (sequence, kv head)'s queries as two
-    // E4M3 terms, written by the split-query kernel before the attention
-    pl->f8 = pl->use_tc && eb == 1;
-    pl->off_qrec = off;
-    if (pl->f8) off += align_up(attn_f8_qrec_bytes(p->batch, p->num_kv_heads));
     pl->bytes = std::max<size_t>(off, kAlign);
     return SVPA_OK;
 }
@@ -209,7 +206,7 @@ svpa_status svpa_attn_launches(const svpa_attn_params *p, int32_t *launches) {
     AttnPlan pl;
     const svpa_status s = plan_attn(p, &pl);
     if (s != SVPA_OK) return s;
-    *launches = p->batch == 0 ? 0 : (pl.ordered ? 2 : 1) + (pl.f8 ? 1 : 0);
+    *launches = p->batch == 0 ? 0 : (pl.ordered ? 2 : 1);
     return SVPA_OK;
 }
 
@@ -344,6 +341,7 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
     a.num_blocks = p->num_blocks;
     a.split_pages = pl.split_pages;
     a.max_splits = pl.max_splits;
+    a.part_slots = pl.part_slots;
     a.scale_log2 = p->sm_scale * 1.4426950408889634f;
     a.scale_tile = p->scale_tile;
     for (int j = 0; j < p->n_q; ++j)
@@ -353,11 +351,6 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
         cudaError_t e = launch_seq_order(context_lens, p->batch, reinterpret_cast<int32_t *>(ws + pl.off_order),
                                          static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return from_cuda(e);
-    }
-    if (pl.f8) {
-        a.npad = (pl.M + 15) / 16 * 16;
-        const int grid = std::max(1, std::min(pl.grid_slots, a.total_units));
-        return from_cuda(launch_paged_verify_attn_f8(maps, a, ws + pl.off_qrec, grid, static_cast<cudaStream_t>(stream)));
     }
     if (pl.use_tc) {
         const int grid = std::max(1, std::min(pl.grid_slots, a.total_units));

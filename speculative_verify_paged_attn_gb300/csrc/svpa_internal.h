@@ -63,16 +63,17 @@ struct AttnArgs {
     const int32_t *context_lens;
     __nv_bfloat16 *out;
     float *lse;
-    float *part_acc;      // [B*Hkv, max_splits, M, D]
-    float *part_ml;       // [B*Hkv, max_splits, M, 2]  (running max in log2 units, sum)
+    float *part_acc;      // [B*Hkv, part_slots, M, D]
+    float *part_ml;       // [B*Hkv, part_slots, M, 2]  (running max in log2 units, sum)
     int32_t *tickets;     // [B*Hkv]
     const int32_t *order; // [B] sequences, longest first, in the order units are handed out; or null
     int32_t *sched;       // [2]: next work unit, CTAs finished (both back to 0 after a call)
     int32_t *err;
     int32_t B, n_q, Hq, Hkv, G, M;
     int32_t max_blocks, num_blocks, split_pages, max_splits, n_stages, total_units;
+    int32_t part_slots;   // partial rows per (sequence, kv head): max_splits, or 2 max_splits for
+                          // FP8 pages on tcgen05 (each split's two token halves)
     int32_t scale_tile;   // FP8 scales: 0 per (page, kv head), 64 per 64-element tile
-    int32_t npad;         // FP8 tcgen05 kernel: MMA N, the query rows M rounded up to 16
     float scale_log2;     // sm_scale * log2(e)
     unsigned long long anc[kMaxNq];  // visibility of speculative slots per query
 };
@@ -110,13 +111,6 @@ cudaError_t attn_plan_launch(int head_dim, bool fp8, int M, AttnLaunch *out);
 // order[0..B): the persistent kernels hand out long units first.
 constexpr int kMaxOrderedSeqs = 4096;
 cudaError_t launch_seq_order(const int32_t *context_lens, int B, int32_t *order, cudaStream_t stream);
-// FP8 pages on tcgen05 (head_dim 128, G * n_q <= 64, one CTA per SM): the
-// split-query kernel writes one record per (sequence, kv head) into `qrec`
-// (attn_f8_qrec_bytes), then the attention kernel runs as its programmatic
-// dependent.
-size_t attn_f8_qrec_bytes(int batch, int num_kv_heads);
-cudaError_t launch_paged_verify_attn_f8(const AttnMaps &maps, const AttnArgs &a, uint8_t *qrec, int grid,
-                                        cudaStream_t stream);
 // tcgen05 / TMEM variant (bf16 pages, head_dim 128, one CTA per SM).
 cudaError_t launch_paged_verify_attn_tc(const AttnMaps &maps, const AttnArgs &a, int grid, bool fp8,
                                         cudaStream_t stream);
