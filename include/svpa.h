@@ -167,7 +167,10 @@ svpa_status svpa_attn_workspace_size(const svpa_attn_params *p, size_t *bytes);
  * in) and the queries and P are f16: there a K or V scale above 146 (448 *
  * scale would pass the f16 maximum) or a negative/NaN scale raises
  * SVPA_DEVERR_BAD_VALUE, and |q| must stay below 65504; the warp-level
- * kernel (variant 1) applies the scales in fp32 and has neither limit.
+ * kernel (variant 1) applies the scales in fp32 and has neither limit.  The
+ * kernel cannot see the scales before it runs, so this is the caller's
+ * contract: with FP8 pages whose scales may exceed 146 (values beyond
+ * +-65,000), set variant = 1.
  */
 svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q,
                                    const void *k_pool, const void *v_pool,

@@ -62,43 +62,33 @@ constexpr int kTileScales = 16 * (128 / 64);    // tile scales of one (page, kv 
 // Two layouts of the same kernel.
 //  bf16 pages: warps 0 producer, 1 MMA, 2-5 softmax, 6-9 epilogue; 3-deep K
 //    and V rings of bf16 blocks that the MMA reads directly.
-//  FP8 pages (at most 64 query rows): warps 0 producer, 1 MMA, 4-7 softmax
-//    (and the epilogue), 2/3/10 K converters, 8/9/11 V converters; the
-//    producer streams E4M3 pages (and, by cp.async, their scales) into
-//    2-deep staging rings, the converters turn each block into f16
-//    (exactly; the K page scale then enters the softmax's exponent and the V
-//    page scale multiplies P) in 2-deep K and V tile rings, and the MMAs run
-//    kind::f16 with f16 queries (converted in place) and f16 P.  With one
+//  FP8 pages (at most 64 query rows, so two TMEM lane quadrants): warps 0
+//    producer, 1 MMA, 4-5 softmax, 8-9 epilogue, 2/3/10 K converters, 6/7/11
+//    V converters; the producer streams E4M3 pages (and, by cp.async, their
+//    scales) into 2-deep staging rings, the converters turn each block into
+//    f16 (exactly; the K page scale then enters the softmax's exponent and the
+//    V page scale multiplies P) in 2-deep K and V tile rings, and the MMAs
+//    run kind::f16 with f16 queries (converted in place) and f16 P.  With one
 //    scale per 64-element tile of a row (the TILES instantiation) the
-//    converters multiply each row-half by its own scale instead.  The query
-//    tile is held twice, rows 0..63 and 64..127 (the K converters copy it),
-//    so that every query row has two TMEM lanes: lane r < 64 takes the
-//    block's tokens 0..63 and lane r + 64 its tokens 64..127, each with its
-//    own online softmax, and all four lane quadrants (all four SM
-//    sub-partitions) share the exponentials.  PV accumulates the two halves
-//    in O rows r and r + 64 (each lane writes zeros over the other half's P
-//    columns); a finished unit's two rows per query row are written as two
-//    split partials (slots 2 split and 2 split + 1) and merged with the
-//    sequence's other splits by log-sum-exp weights.
-// DUP (FP8 pages with per-page scales): the query tile is held twice so that
-// each query row has two TMEM lanes, one per half of a block's tokens
-template <bool FP8, bool DUP = FP8>
+//    converters multiply each row-half by its own scale instead.  The
+//    query buffer holds 64 rows; the MMA still reads 128, rows 64..127 being
+//    whatever follows and feeding only TMEM lanes no thread reads.
+template <bool FP8>
 struct TcCfg {
     static constexpr int kThreads = FP8 ? 384 : 320;
     static constexpr int kNK = FP8 ? 2 : 3;     // tiles the MMA reads (K freed once S_j is done)
     static constexpr int kNV = FP8 ? 2 : 3;     // (V freed once PV_j is done)
     static constexpr int kNK8 = FP8 ? 2 : 1;    // FP8 staging rings
     static constexpr int kNV8 = FP8 ? 2 : 1;
-    static constexpr int kQSlab = (FP8 && !DUP ? 64 : 128) * 128;  // one 64-column slab of the query buffer
+    static constexpr int kQSlab = (FP8 ? 64 : 128) * 128;  // one 64-column slab of the query buffer
     static constexpr int kQBuf = 2 * kQSlab;
     // arrivals that complete a staging slot: the producer's expect_tx and
     // one cp.async scale copy per page
     static constexpr uint32_t kStageArrivals = 1 + kPagesPerBlock;
     static constexpr int kSoftmaxWarp0 = FP8 ? 4 : 2;
-    static constexpr int kSoftmaxWarps = FP8 && !DUP ? 2 : 4;
-    // DUP: no epilogue warps; the softmax warps write each finished unit out
-    static constexpr int kEpiWarp0 = DUP ? -64 : (FP8 ? 8 : 6);
-    static constexpr int kEpiWarps = FP8 && !DUP ? 2 : 4;  // (DUP: the softmax warps release O)
+    static constexpr int kSoftmaxWarps = FP8 ? 2 : 4;
+    static constexpr int kEpiWarp0 = FP8 ? 8 : 6;
+    static constexpr int kEpiWarps = FP8 ? 2 : 4;
     static constexpr int kConvWarps = 3;        // per operand (FP8 only)
 };
 constexpr float kRescaleLog2 = 8.f;             // rescale O when a maximum grows by > 2^8
@@ -136,11 +126,9 @@ struct Stage8 {  // FP8 staging rings
 };
 struct NoStage8 {};
 
-struct NoStat {};
 template <bool FP8, bool TILES>
 struct Smem {
-    static constexpr bool DUP = FP8 && !TILES;
-    using C = TcCfg<FP8, DUP>;
+    using C = TcCfg<FP8>;
     uint8_t q[C::kQBuf];                 // 1024-aligned (one unit's queries)
     uint8_t kbuf[C::kNK][kKVTile];       // 32 KB each
     uint8_t vbuf[C::kNV][kKVTile];
@@ -154,8 +142,7 @@ struct Smem {
     uint64_t stat_full, stat_empty;      // softmax -> epilogue hand-off of a finished unit
     BlockMeta meta[kNMeta];
     int32_t vid[kNMeta][kPagesPerBlock];  // page ids of a block, for its V copies
-    // (reference maximum, running sum) per row, for the epilogue warps
-    typename std::conditional<DUP, NoStat, float2[kRows]>::type stat;
+    float2 stat[kRows];                  // (reference maximum, running sum) per row
     int32_t ep_b, ep_h, ep_split, ep_nsplit, ep_end;
     uint32_t tmem_base;
     int32_t last;
@@ -189,85 +176,15 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
 
 __device__ __forceinline__ uint32_t par_of(int idx) { return (uint32_t)((idx >> 1) & 1); }
 
-// The last split's CTA merges the partial rows of (sequence b, kv head h)
-// with log-sum-exp weights (an online merge: running maximum, rescaled sum)
-// into the output rows: one warp per row, 4 columns per lane, four rows and
-// two partials per pass so that their loads are in flight together.  NE
-// warps take part (ew = this warp's index among them); `slots` partial rows
-// per query row (slots 0 .. slots - 1 of the unit's partial array).
-__device__ void merge_partials(const AttnArgs &a, int b, int h, int slots, int ew, int NE, int lane) {
-    const int G = a.G;
-    const int u2 = b * a.Hkv + h;
-    const size_t base = (size_t)u2 * a.part_slots * a.M;
-    for (int r0 = ew; r0 < a.M; r0 += 4 * NE) {
-        float mrow[4], lrow[4];
-        float4 o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            mrow[i] = -CUDART_INF_F;
-            lrow[i] = 0.f;
-            o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        for (int s0 = 0; s0 < slots; s0 += 2) {
-            float2 ml[4][2];
-            float4 v[4][2];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int rr = r0 + NE * i;
-                    if (rr < a.M && s0 + k < slots) {
-                        const size_t pr = base + (size_t)(s0 + k) * a.M + rr;
-                        ml[i][k] = __ldcg(reinterpret_cast<const float2 *>(a.part_ml + pr * 2));
-                        v[i][k] = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + pr * kD) + lane);
-                    } else {
-                        ml[i][k] = make_float2(-CUDART_INF_F, 0.f);
-                        v[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                }
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const float mk = ml[i][k].x;
-                    if (mk == -CUDART_INF_F) continue;  // an empty partial (or none)
-                    const float mn = fmaxf(mrow[i], mk);
-                    const float f_old = ex2_approx(mrow[i] - mn);  // 0 when mrow is -inf
-                    const float f_new = ex2_approx(mk - mn);
-                    lrow[i] = lrow[i] * f_old + ml[i][k].y * f_new;
-                    o[i].x = o[i].x * f_old + v[i][k].x * f_new;
-                    o[i].y = o[i].y * f_old + v[i][k].y * f_new;
-                    o[i].z = o[i].z * f_old + v[i][k].z * f_new;
-                    o[i].w = o[i].w * f_old + v[i][k].w * f_new;
-                    mrow[i] = mn;
-                }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int rr = r0 + NE * i;
-            if (rr >= a.M) break;
-            const float inv2 = lrow[i] > 0.f ? 1.f / lrow[i] : 0.f;
-            const int jq2 = rr / G, gi2 = rr - jq2 * G;
-            const size_t od2 = (((size_t)b * a.n_q + jq2) * a.Hq + (size_t)h * G + gi2);
-            uint2 v2;
-            v2.x = pack_bf16x2(o[i].x * inv2, o[i].y * inv2);
-            v2.y = pack_bf16x2(o[i].z * inv2, o[i].w * inv2);
-            reinterpret_cast<uint2 *>(a.out + od2 * kD)[lane] = v2;
-            if (lane == 0 && a.lse) a.lse[od2] = (mrow[i] + __log2f(lrow[i])) * 0.69314718055994530942f;
-        }
-    }
-}
-
 // TILES (FP8 only): one scale per 64-element tile of a row, applied by the
 // converters, instead of one per (page, kv head) applied in the softmax
 template <bool FP8, bool TILES>
-__global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
+__global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
     pva_tc_kernel(const __grid_constant__ CUtensorMap mkp, const __grid_constant__ CUtensorMap mvp,
                   const __grid_constant__ CUtensorMap mq0, const __grid_constant__ CUtensorMap mq1,
                   const __grid_constant__ AttnArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    constexpr bool DUP = FP8 && !TILES;
-    using C = TcCfg<FP8, DUP>;
+    using C = TcCfg<FP8>;
     constexpr int kNK = C::kNK, kNV = C::kNV, kQSlab = C::kQSlab, kQBuf = C::kQBuf;
     Smem<FP8, TILES> &sm =
         *reinterpret_cast<Smem<FP8, TILES> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -624,18 +541,11 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
     } else if (warp >= C::kSoftmaxWarp0 && warp < C::kSoftmaxWarp0 + C::kSoftmaxWarps) {
         // ================================================= softmax
         const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;          // TMEM lane
+        const int r = quarter * 32 + lane;          // query row == TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const int G = a.G;
-        // bf16: lane r is query row r and takes the block's 128 tokens.  FP8:
-        // lanes r and r + 64 both hold query row r (the query tile is held
-        // twice); the lower takes tokens 0..63, the upper tokens 64..127
-        constexpr int NC = DUP ? 64 : kNB;          // tokens (S columns) a lane takes per block
-        constexpr int NPG = NC / 16;                // their pages
-        const int half = DUP ? (r >> 6) : 0;
-        const int row = DUP ? (r & 63) : r;
-        const bool live = row < a.M;
-        const int jq = live ? row / G : 0;
+        const bool live = r < a.M;
+        const int jq = live ? r / G : 0;
         const unsigned long long anc = live ? a.anc[jq] : 0ull;
         float m_ref = -CUDART_INF_F, l_run = 0.f;
         int j = 0, unit = -1;
@@ -643,13 +553,11 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
             if (!mbar_wait(&sm.s_full[j & 1], par_of(j), a.err)) break;
             const BlockMeta md = sm.meta[j % kNMeta];
             if (md.flags & kFlagEnd) {
-                if constexpr (!DUP) {
-                    // tell the epilogue warps there is no further unit
-                    if (unit >= 0) mbar_wait(&sm.stat_empty, (uint32_t)(unit & 1), a.err);
-                    if (threadIdx.x == C::kSoftmaxWarp0 * 32) sm.ep_end = 1;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sm.stat_full);
-                }
+                // tell the epilogue warps there is no further unit
+                if (unit >= 0) mbar_wait(&sm.stat_empty, (uint32_t)(unit & 1), a.err);
+                if (threadIdx.x == C::kSoftmaxWarp0 * 32) sm.ep_end = 1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.stat_full);
                 break;
             }
             if (md.flags & kFlagFirst) {
@@ -658,11 +566,11 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
                 l_run = 0.f;
             }
             tc_fence_after();
-            float s[NC];
+            float s[kNB];
             {
-                const uint32_t sa = tmem + kTmemS + (uint32_t)(j & 1) * kNB + (uint32_t)(half * NC) + lane_off;
+                const uint32_t sa = tmem + kTmemS + (uint32_t)(j & 1) * kNB + lane_off;
 #pragma unroll
-                for (int c = 0; c < NC / 32; ++c) {
+                for (int c = 0; c < kNB / 32; ++c) {
                     uint32_t raw[32];
                     tmem_ld32(sa + c * 32, raw);
                     tmem_ld_wait();
@@ -679,20 +587,18 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
             // partial block.
             if (md.pos0 + kNB > L || md.ntok < kNB) {
                 // visibility of the block's tokens, 64 per bit mask word
-                // (word wg of the block; FP8: only this lane's word)
                 const int h0 = L - md.pos0;  // tokens of the block that are history
 #pragma unroll
-                for (int w = 0; w < NC / 64; ++w) {
-                    const int wg = w + half * (NC / 64);
-                    const int hw = min(max(h0 - 64 * wg, 0), 64);
+                for (int w = 0; w < kNB / 64; ++w) {
+                    const int hw = min(max(h0 - 64 * w, 0), 64);
                     unsigned long long vis = hw == 64 ? ~0ull : ((1ull << hw) - 1ull);
-                    const int sh = h0 - 64 * wg;  // bit of speculative slot 0 in this word
+                    const int sh = h0 - 64 * w;  // bit of speculative slot 0 in this word
                     if (sh >= 0) {
                         if (sh < 64) vis |= anc << sh;
                     } else if (-sh < 64) {
                         vis |= anc >> (-sh);
                     }
-                    const int nw = min(max(md.ntok - 64 * wg, 0), 64);
+                    const int nw = min(max(md.ntok - 64 * w, 0), 64);
                     if (nw < 64) vis &= (1ull << nw) - 1ull;
 #pragma unroll
                     for (int t = 0; t < 64; ++t)
@@ -702,35 +608,25 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
             // per-page maxima of the raw scores (FP8: a page's K scale
             // multiplies its scores; scales are >= 0, so the maximum of the
             // scaled scores is the largest scaled page maximum)
-            float pm[NPG];
+            float pm[kPagesPerBlock];
 #pragma unroll
-            for (int x = 0; x < NPG; ++x) pm[x] = s[16 * x];
+            for (int x = 0; x < kPagesPerBlock; ++x) pm[x] = s[16 * x];
 #pragma unroll
-            for (int t = 0; t < NC; ++t)
+            for (int t = 0; t < kNB; ++t)
                 if (t & 15) pm[t >> 4] = fmaxf(pm[t >> 4], s[t]);
-            // FP8: a page's K scale multiplies its scores (fp32) and its V
-            // scale joins the exponent, P' = 2^(x + log2 s_v - m): P' stays
-            // within the f16 range whatever the scales (the reference m tracks
-            // x + log2 s_v) and the row sum adds P' / s_v.  A page with V scale
-            // 0 takes log2 s_v = 0 (the V converters zero its rows).  (Tile
-            // scales are already in the converted tiles.)
-            float ksc[NPG], lv[NPG], inv_v[NPG];
-            float mx = -CUDART_INF_F;
+            float ksc[kPagesPerBlock], vsc[kPagesPerBlock];
             if constexpr (FP8) {
 #pragma unroll
-                for (int x = 0; x < NPG; ++x) {
-                    ksc[x] = TILES ? 1.f : sm.st8.ksc[j % kNMeta][half * NPG + x];
-                    const float vs = TILES ? 1.f : sm.st8.vsc[j % kNMeta][half * NPG + x];
-                    lv[x] = vs > 0.f ? __log2f(vs) : 0.f;
-                    inv_v[x] = vs > 0.f ? __frcp_rn(vs) : 1.f;
-                    if (pm[x] != -CUDART_INF_F) mx = fmaxf(mx, fmaf(pm[x] * ksc[x], a.scale_log2, lv[x]));
+                for (int x = 0; x < kPagesPerBlock; ++x) {
+                    // (tile scales are already in the converted tiles)
+                    ksc[x] = TILES ? 1.f : sm.st8.ksc[j % kNMeta][x];
+                    vsc[x] = TILES ? 1.f : sm.st8.vsc[j % kNMeta][x];
+                    if (pm[x] != -CUDART_INF_F) pm[x] *= ksc[x];
                 }
-            } else {
-                float mraw = pm[0];
-#pragma unroll
-                for (int x = 1; x < NPG; ++x) mraw = fmaxf(mraw, pm[x]);
-                mx = mraw == -CUDART_INF_F ? -CUDART_INF_F : mraw * a.scale_log2;
             }
+            const float mraw = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                     fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+            const float mx = mraw == -CUDART_INF_F ? -CUDART_INF_F : mraw * a.scale_log2;
             float alpha = 1.f;
             bool rescale = false;
             if (mx > m_ref + kRescaleLog2 || (m_ref == -CUDART_INF_F && mx != -CUDART_INF_F)) {
@@ -741,49 +637,44 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
             }
             const float neg_m = m_ref == -CUDART_INF_F ? 0.f : -m_ref;
             const float sc = a.scale_log2;
-
+            if constexpr (FP8) {
+                // V_j's page scales multiply P (PV reads raw E4M3 values as f16)
+                // once the V converters are done with block j
+                mbar_wait(&sm.v_full[j % kNV], (uint32_t)((j / kNV) & 1), a.err);
+            }
             // P_j as bf16 pairs into the first half of S_j's TMEM columns
             const uint32_t pt = tmem + kTmemS + (uint32_t)(j & 1) * kNB + lane_off;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
             if constexpr (FP8) {
-                // FP8 pages: P' is f16, so each pair of exponents is evaluated by
+                // FP8 pages: P is f16, so each pair of exponents is evaluated by
                 // one ex2.f16x2 on the fp32 arguments rounded to f16 (an argument
-                // is at most 8 under the lazy maximum, where f16 keeps P' within
+                // is at most 8 under the lazy maximum, where f16 keeps P within
                 // ~0.14%); the row sum adds those f16 values, in f16 within a
-                // page (16 values), then times 1 / s_v in fp32.  A page whose K
-                // scale is 0 has scores 0: its multiplier stays positive so
-                // masked columns stay -inf.
+                // page (16 values) and in fp32 across pages; P times the V page
+                // scale is formed in f16.  A page whose K scale is 0 has scores
+                // 0: its multiplier stays positive so masked columns stay -inf.
 #pragma unroll
-                for (int c = 0; c < NC / 64; ++c) {
+                for (int c = 0; c < kNB / 64; ++c) {
                     uint32_t w[32];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int pg = c * 4 + q;  // the page (of this lane's) of these 16 columns
+                        const int pg = c * 4 + q;  // the page of these 16 columns
                         const float scp = fmaxf(sc * ksc[pg], 1e-30f);
-                        const float off = lv[pg] + neg_m;
+                        const uint32_t v2 = pack_f16x2(vsc[pg], vsc[pg]);
                         uint32_t acc = 0u;  // f16 pair (+0, +0)
 #pragma unroll
                         for (int e8 = 0; e8 < 8; ++e8) {
                             const int e = q * 8 + e8;
-                            const float x0 = live ? fmaf(s[c * 64 + 2 * e], scp, off) : -CUDART_INF_F;
-                            const float x1 = live ? fmaf(s[c * 64 + 2 * e + 1], scp, off) : -CUDART_INF_F;
+                            const float x0 = live ? fmaf(s[c * 64 + 2 * e], scp, neg_m) : -CUDART_INF_F;
+                            const float x1 = live ? fmaf(s[c * 64 + 2 * e + 1], scp, neg_m) : -CUDART_INF_F;
                             const uint32_t p2 = ex2_f16x2(pack_f16x2(x0, x1));
                             acc = add_f16x2(acc, p2);
-                            w[e] = p2;
+                            w[e] = mul_f16x2(p2, v2);
                         }
                         const float2 f = f16x2_to_float2(acc);
-                        ls[q] += (f.x + f.y) * inv_v[pg];
+                        ls[q] += f.x + f.y;
                     }
-                    if constexpr (DUP) {
-                        // this lane's tokens' P columns, and zeros over the other
-                        // half's (its O row must not take those tokens)
-                        tmem_st32(pt + (uint32_t)(half * 32), w);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) w[e] = 0u;
-                        tmem_st32(pt + (uint32_t)((1 - half) * 32), w);
-                    } else {
-                        tmem_st32(pt + c * 32, w);
-                    }
+                    tmem_st32(pt + c * 32, w);
                 }
             } else {
 #pragma unroll
@@ -842,7 +733,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.p_full);
 
-            if constexpr (!DUP) if (md.flags & kFlagLast) {
+            if (md.flags & kFlagLast) {
                 // hand the unit's row statistics to the epilogue warps (one
                 // slot: the previous unit's must have been taken)
                 if (unit >= 1) mbar_wait(&sm.stat_empty, (uint32_t)((unit - 1) & 1), a.err);
@@ -857,54 +748,9 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.stat_full);
             }
-            if constexpr (DUP) if (md.flags & kFlagLast) {
-                // DUP: this lane's O row (its half of the unit's tokens) as a
-                // partial (slot 2 split + half) once the unit's last PV has
-                // landed; the last split's CTA merges the 2 nsplit partials
-                const int ob = unit & 1;
-                mbar_wait(&sm.o_full[ob], par_of(unit), a.err);
-                tc_fence_after();
-                const uint32_t oa = tmem + kTmemO + (uint32_t)ob * kD + lane_off;
-                const int u2 = md.b * a.Hkv + md.h;
-                const size_t pr_own = ((size_t)u2 * a.part_slots + 2 * md.split + half) * a.M + row;
-#pragma unroll 1
-                for (int c = 0; c < kD / 32; ++c) {
-                    uint32_t raw[32];
-                    tmem_ld32(oa + c * 32, raw);
-                    tmem_ld_wait();
-                    if (live) {
-                        uint4 *prow4 = reinterpret_cast<uint4 *>(a.part_acc + pr_own * kD + c * 32);
-#pragma unroll
-                        for (int c4 = 0; c4 < 8; ++c4)
-                            prow4[c4] = make_uint4(raw[c4 * 4], raw[c4 * 4 + 1], raw[c4 * 4 + 2], raw[c4 * 4 + 3]);
-                    }
-                }
-                if (live) {
-                    a.part_ml[pr_own * 2] = m_ref;
-                    a.part_ml[pr_own * 2 + 1] = l_run;
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.o_empty[ob]);
-                __threadfence();
-                named_barrier_sync(kBarEpi, C::kSoftmaxWarps * 32);
-                if (threadIdx.x == C::kSoftmaxWarp0 * 32) {
-                    const int tk = atomicAdd(&a.tickets[u2], 1);
-                    sm.last = (tk == md.nsplit - 1);
-                    if (sm.last) a.tickets[u2] = 0;
-                }
-                named_barrier_sync(kBarEpi, C::kSoftmaxWarps * 32);
-                const int last = sm.last;
-                named_barrier_sync(kBarEpi, C::kSoftmaxWarps * 32);
-                if (last) {
-                    __threadfence();
-                    merge_partials(a, md.b, md.h, 2 * md.nsplit, warp - C::kSoftmaxWarp0, C::kSoftmaxWarps, lane);
-                }
-            }
             ++j;
         }
-    } else if (!DUP && warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + C::kEpiWarps) {
-      if constexpr (!DUP) {
+    } else if (warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + C::kEpiWarps) {
         // ================================================= epilogue
         // One thread per query row (TMEM lane) streams a finished unit's O
         // out of TMEM while the softmax warps already work on the next unit
@@ -932,7 +778,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
             const uint32_t oa = tmem + kTmemO + (uint32_t)ob * kD + lane_off;
             const int u2 = b * a.Hkv + h;
             const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
-            const size_t pr_own = ((size_t)u2 * a.part_slots + split) * a.M + r;
+            const size_t pr_own = ((size_t)u2 * a.max_splits + split) * a.M + r;
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
             // O row streamed out of TMEM 32 columns at a time: final output
             // when the unit is the whole sequence, else a split partial
@@ -983,15 +829,74 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
             const int last = sm.last;
             named_barrier_sync(kBarEpi, NE * 32);
             if (!last) continue;
-            // the last split's CTA merges every split's partial rows
+            // the last split's CTA merges every split's partial rows with
+            // log-sum-exp weights (an online merge: running maximum, rescaled
+            // sum): one warp per row, 4 columns per lane, four rows and two
+            // splits per pass so that their loads are in flight together
             __threadfence();
-            merge_partials(a, b, h, nsplit, ew, NE, lane);
+            const size_t base = (size_t)u2 * a.max_splits * a.M;
+            for (int r0 = ew; r0 < a.M; r0 += 4 * NE) {
+                float mrow[4], lrow[4];
+                float4 o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    mrow[i] = -CUDART_INF_F;
+                    lrow[i] = 0.f;
+                    o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                for (int s0 = 0; s0 < nsplit; s0 += 2) {
+                    float2 ml[4][2];
+                    float4 v[4][2];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const int rr = r0 + NE * i;
+                            if (rr < a.M && s0 + k < nsplit) {
+                                const size_t pr = base + (size_t)(s0 + k) * a.M + rr;
+                                ml[i][k] = __ldcg(reinterpret_cast<const float2 *>(a.part_ml + pr * 2));
+                                v[i][k] = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + pr * kD) + lane);
+                            } else {
+                                ml[i][k] = make_float2(-CUDART_INF_F, 0.f);
+                                v[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                        }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const float mk = ml[i][k].x;
+                            if (mk == -CUDART_INF_F) continue;  // an empty split (or none)
+                            const float mn = fmaxf(mrow[i], mk);
+                            const float f_old = ex2_approx(mrow[i] - mn);  // 0 when mrow is -inf
+                            const float f_new = ex2_approx(mk - mn);
+                            lrow[i] = lrow[i] * f_old + ml[i][k].y * f_new;
+                            o[i].x = o[i].x * f_old + v[i][k].x * f_new;
+                            o[i].y = o[i].y * f_old + v[i][k].y * f_new;
+                            o[i].z = o[i].z * f_old + v[i][k].z * f_new;
+                            o[i].w = o[i].w * f_old + v[i][k].w * f_new;
+                            mrow[i] = mn;
+                        }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = r0 + NE * i;
+                    if (rr >= a.M) break;
+                    const float inv2 = lrow[i] > 0.f ? 1.f / lrow[i] : 0.f;
+                    const int jq2 = rr / G, gi2 = rr - jq2 * G;
+                    const size_t od2 = (((size_t)b * a.n_q + jq2) * a.Hq + (size_t)h * G + gi2);
+                    uint2 v2;
+                    v2.x = pack_bf16x2(o[i].x * inv2, o[i].y * inv2);
+                    v2.y = pack_bf16x2(o[i].z * inv2, o[i].w * inv2);
+                    reinterpret_cast<uint2 *>(a.out + od2 * kD)[lane] = v2;
+                    if (lane == 0 && a.lse) a.lse[od2] = (mrow[i] + __log2f(lrow[i])) * 0.69314718055994530942f;
+                }
+            }
         }
-      }
     }
     if constexpr (FP8) {
         const bool kconv = warp == 2 || warp == 3 || warp == 10;
-        const bool vconv = DUP ? (warp == 8 || warp == 9 || warp == 11) : (warp == 6 || warp == 7 || warp == 11);
+        const bool vconv = warp == 6 || warp == 7 || warp == 11;
         if (kconv || vconv) {
             // ================================================= FP8 converters
             // Block j's E4M3 pages -> one f16 tile in the MMA's layout (page p
@@ -999,7 +904,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
             // swizzle), each value times its page's scale; the V converters
             // also zero the rows past the sequence's last token.  The K
             // converters first turn each unit's bf16 query tile into f16.
-            const int ci = kconv ? (warp == 10 ? 2 : warp - 2) : (warp == 11 ? 2 : warp - (DUP ? 8 : 6));
+            const int ci = kconv ? (warp == 10 ? 2 : warp - 2) : (warp == 11 ? 2 : warp - 6);
             const int ct = ci * 32 + lane;  // 0..95
             constexpr int NCT = C::kConvWarps * 32;
             const int ring = kconv ? C::kNK8 : C::kNV8;
@@ -1024,7 +929,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
                 const uint8_t *src = kconv ? sm.st8.k8[s8] : sm.st8.v8[s8];
                 const float *scl = kconv ? sm.st8.ksc[j % kNMeta] : sm.st8.vsc[j % kNMeta];
                 uint8_t *tile = kconv ? sm.kbuf[tb] : sm.vbuf[tb];
-                if (lane < kPagesPerBlock && !(scl[lane] >= 0.f && scl[lane] <= 3.0e38f))
+                if (lane < kPagesPerBlock && !(scl[lane] >= 0.f && scl[lane] <= kMaxScale8))
                     raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
                 if (kconv && (md.flags & kFlagFirst)) {
                     // the unit's queries, bf16 -> f16 in place (rows < M)
@@ -1039,8 +944,6 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
                         v.z = bf16x2_to_f16x2(v.z);
                         v.w = bf16x2_to_f16x2(v.w);
                         *qp = v;
-                        // the copy in rows 64..127 (same swizzle phase: 64 is a multiple of 8)
-                        if constexpr (DUP) *(qp + 64 * 128 / 16) = v;
                     }
                 }
                 const int t_end = kconv ? kNB : md.L + a.n_q - md.pos0;  // V rows from t_end on are zeroed
@@ -1053,8 +956,7 @@ __global__ void __launch_bounds__(TcCfg<FP8, FP8 && !TILES>::kThreads, 1)
                     for (int u = 0; u < 4; ++u) {
                         const int i = ct + NCT * (t0 + u), row = i >> 3, g = i & 7;
                         e[u] = make_uint4(0, 0, 0, 0);
-                        // (V rows of a page whose scale is 0 hold zeros)
-                        if (t0 + u < kPer && i < kItems && row < t_end && (kconv || TILES || scl[row >> 4] > 0.f))
+                        if (t0 + u < kPer && i < kItems && row < t_end)
                             e[u] = *reinterpret_cast<const uint4 *>(src + row * 128 + ((g ^ (row & 7)) << 4));
                     }
 #pragma unroll
@@ -1129,7 +1031,7 @@ cudaError_t launch_tc(const CUtensorMap &mk, const CUtensorMap &mv, const AttnMa
         return cudaFuncSetAttribute(pva_tc_kernel<FP8, TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     });
     if (e != cudaSuccess) return e;
-    pva_tc_kernel<FP8, TILES><<<grid, TcCfg<FP8, FP8 && !TILES>::kThreads, smem, st>>>(mk, mv, m.q[0], m.q[1], a);
+    pva_tc_kernel<FP8, TILES><<<grid, TcCfg<FP8>::kThreads, smem, st>>>(mk, mv, m.q[0], m.q[1], a);
     return cudaGetLastError();
 }
 }  // namespace

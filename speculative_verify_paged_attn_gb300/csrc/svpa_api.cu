@@ -56,7 +56,7 @@ int sm_count() {
 }
 
 struct AttnPlan {
-    int M, split_pages, max_splits, part_slots;
+    int M, split_pages, max_splits;
     bool use_tc;
     int grid_slots;      // resident CTAs of the chosen kernel
     bool ordered;        // units handed out longest sequence first
@@ -129,13 +129,10 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     pl->off_order = off;
     if (pl->ordered) off += align_up((size_t)p->batch * sizeof(int32_t));
     pl->off_ml = off;
-    // FP8 pages with per-page scales on tcgen05: each split leaves two partial
-    // rows per query row (the two token halves of every block), merged like splits
-    pl->part_slots = (pl->use_tc && eb == 1 && p->scale_tile == 0) ? 2 * pl->max_splits : pl->max_splits;
-    if (pl->part_slots > 1) {
-        off += align_up(units * pl->part_slots * M * 2 * sizeof(float));
+    if (pl->max_splits > 1) {
+        off += align_up(units * pl->max_splits * M * 2 * sizeof(float));
         pl->off_acc = off;
-        off += align_up(units * pl->part_slots * M * D * sizeof(float));
+        off += align_up(units * pl->max_splits * M * D * sizeof(float));
     } else {
         pl->off_acc = off;
     }
@@ -341,7 +338,6 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
     a.num_blocks = p->num_blocks;
     a.split_pages = pl.split_pages;
     a.max_splits = pl.max_splits;
-    a.part_slots = pl.part_slots;
     a.scale_log2 = p->sm_scale * 1.4426950408889634f;
     a.scale_tile = p->scale_tile;
     for (int j = 0; j < p->n_q; ++j)

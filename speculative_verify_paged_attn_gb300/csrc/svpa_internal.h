@@ -63,16 +63,14 @@ struct AttnArgs {
     const int32_t *context_lens;
     __nv_bfloat16 *out;
     float *lse;
-    float *part_acc;      // [B*Hkv, part_slots, M, D]
-    float *part_ml;       // [B*Hkv, part_slots, M, 2]  (running max in log2 units, sum)
+    float *part_acc;      // [B*Hkv, max_splits, M, D]
+    float *part_ml;       // [B*Hkv, max_splits, M, 2]  (running max in log2 units, sum)
     int32_t *tickets;     // [B*Hkv]
     const int32_t *order; // [B] sequences, longest first, in the order units are handed out; or null
     int32_t *sched;       // [2]: next work unit, CTAs finished (both back to 0 after a call)
     int32_t *err;
     int32_t B, n_q, Hq, Hkv, G, M;
     int32_t max_blocks, num_blocks, split_pages, max_splits, n_stages, total_units;
-    int32_t part_slots;   // partial rows per (sequence, kv head): max_splits, or 2 max_splits for
-                          // FP8 pages on tcgen05 (each split's two token halves)
     int32_t scale_tile;   // FP8 scales: 0 per (page, kv head), 64 per 64-element tile
     float scale_log2;     // sm_scale * log2(e)
     unsigned long long anc[kMaxNq];  // visibility of speculative slots per query
