@@ -18,6 +18,15 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*.py``):
                        the same rows, Monte-Carlo output distribution = P)
   spec_accept_tree     pinned (reduces to spec_accept on a chain; Monte-Carlo
                        distribution of the first emitted token = P[root])
+  spec_accept_tree_logits
+                       pinned (hand-worked three-token trees; reduces to
+                       spec_accept_logits on a chain and to spec_accept_tree
+                       on the softmax rows off the band; doubled logits at
+                       temperature 2; Monte-Carlo distribution = P at the root
+                       and at an accepted child)
+  tree_logits_outcomes pinned (a zero band leaves exactly the sampler's own
+                       outcome, a band of 1 every outcome, the default band
+                       contains the sampler's outcome)
   block_table_commit   pinned (hand-worked example, conservation invariants,
                        tree compaction moves the path's K/V bytes)
   expected_accepted, speedup
@@ -80,6 +89,10 @@ def _load():
             lib.oracle_logits_draw_window.restype = I
             lib.oracle_spec_accept_tree.argtypes = [I, I, I] + [P] * 10 + [I]
             lib.oracle_spec_accept_tree.restype = I
+            lib.oracle_spec_accept_tree_logits.argtypes = [I, I, I, P, D, D, D] + [P] * 9 + [I]
+            lib.oracle_spec_accept_tree_logits.restype = I
+            lib.oracle_tree_logits_outcomes.argtypes = [I, I, I, P, D, D, D] + [P] * 8 + [I]
+            lib.oracle_tree_logits_outcomes.restype = I
             lib.oracle_block_table_commit.argtypes = [I] * 5 + [P] * 7 + [I, P, P, I, I, I]
             lib.oracle_block_table_commit.restype = I
             lib.oracle_tree_max_depth.argtypes = [P, I]
@@ -267,7 +280,10 @@ def logits_draw_window(target_logits, draft_logits, accepted_len, u_sample, temp
 
 def tree_max_depth(parent) -> int:
     par = _c(parent, np.int32)
-    return _load().oracle_tree_max_depth(_ptr(par), par.shape[0])
+    d = _load().oracle_tree_max_depth(_ptr(par), par.shape[0])
+    if d < 0:
+        raise OracleError("parent array is not a tree in node order")
+    return d
 
 
 def spec_accept_tree(parent, p_probs, q_probs, node_tokens, u_accept, u_sample, nthreads=0):
@@ -291,6 +307,60 @@ def spec_accept_tree(parent, p_probs, q_probs, node_tokens, u_accept, u_sample, 
     if rc != 0:
         raise OracleError(f"oracle_spec_accept_tree failed with status {rc}")
     return k, path, out, near.astype(bool)
+
+
+def spec_accept_tree_logits(parent, target_logits, draft_logits, node_tokens, u_accept, u_sample, temperature=1.0,
+                            draft_temperature=None, band=LOGIT_BAND, nthreads=0):
+    """Tree rejection sampler on P = softmax(Lp / T) at every node and
+    Q = softmax(Lq / T_draft) at every internal node, formed in fp64.
+    Returns (accepted_len, path_nodes, out_tokens, near)."""
+    lib = _load()
+    par = _c(parent, np.int32)
+    Lp = _c(target_logits, np.float32)
+    Lq = _c(draft_logits, np.float32)
+    tok = _c(node_tokens, np.int32)
+    ua = _c(u_accept, np.float32)
+    us = _c(u_sample, np.float32)
+    B, n_nodes, V = Lp.shape
+    assert par.shape == (n_nodes,) and tok.shape == (B, n_nodes) and ua.shape == (B, n_nodes)
+    assert Lq.shape[0] == B and Lq.shape[2] == V and us.shape == (B,)
+    td = temperature if draft_temperature is None else draft_temperature
+    W = tree_max_depth(par) + 1
+    k = np.zeros(B, np.int32)
+    path = np.zeros((B, W), np.int32)
+    out = np.zeros((B, W), np.int32)
+    near = np.zeros(B, np.uint8)
+    rc = lib.oracle_spec_accept_tree_logits(B, n_nodes, V, _ptr(par), float(temperature), float(td), float(band),
+                                            _ptr(Lp), _ptr(Lq), _ptr(tok), _ptr(ua), _ptr(us), _ptr(k),
+                                            _ptr(path), _ptr(out), _ptr(near), int(nthreads))
+    if rc != 0:
+        raise OracleError(f"oracle_spec_accept_tree_logits failed with status {rc}")
+    return k, path, out, near.astype(bool)
+
+
+def tree_logits_outcomes(parent, target_logits, draft_logits, node_tokens, u_accept, u_sample, temperature=1.0,
+                         draft_temperature=None, band=LOGIT_BAND, nthreads=0):
+    """Per sequence and node: whether an fp32 formation of the tree sampler
+    fed by logits may end its walk there, and the range [lo, hi] of tokens its
+    final draw there may give.  Returns (end_ok [B, n_nodes] bool, lo, hi)."""
+    lib = _load()
+    par = _c(parent, np.int32)
+    Lp = _c(target_logits, np.float32)
+    Lq = _c(draft_logits, np.float32)
+    tok = _c(node_tokens, np.int32)
+    ua = _c(u_accept, np.float32)
+    us = _c(u_sample, np.float32)
+    B, n_nodes, V = Lp.shape
+    td = temperature if draft_temperature is None else draft_temperature
+    ok = np.zeros((B, n_nodes), np.uint8)
+    lo = np.zeros((B, n_nodes), np.int32)
+    hi = np.zeros((B, n_nodes), np.int32)
+    rc = lib.oracle_tree_logits_outcomes(B, n_nodes, V, _ptr(par), float(temperature), float(td), float(band),
+                                         _ptr(Lp), _ptr(Lq), _ptr(tok), _ptr(ua), _ptr(us), _ptr(ok), _ptr(lo),
+                                         _ptr(hi), int(nthreads))
+    if rc != 0:
+        raise OracleError(f"oracle_tree_logits_outcomes failed with status {rc}")
+    return ok.astype(bool), lo, hi
 
 
 def block_table_commit(block_table, context_lens, accepted_len, refcount, free_stack,

@@ -558,7 +558,12 @@ static int tree_depth_of(const int32_t *parent, int node) {
     return d;
 }
 
+/* Depth of the deepest node, or -1 when parent[] is not a tree in node order
+ * (parent[0] = -1, 0 <= parent[i] < i). */
 int oracle_tree_max_depth(const int32_t *parent, int n_nodes) {
+    if (n_nodes < 1 || parent[0] != -1) return -1;
+    for (int i = 1; i < n_nodes; ++i)
+        if (parent[i] < 0 || parent[i] >= i) return -1;
     int md = 0;
     for (int i = 0; i < n_nodes; ++i) {
         int d = tree_depth_of(parent, i);
@@ -673,6 +678,262 @@ int oracle_spec_accept_tree(int B, int n_nodes, int V, const int32_t *parent,
     }
     free(qrow);
     return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* draft-tree sampler fed by logits                                    */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Near-boundary scale after j rejected siblings at a node.  An fp32
+ * formation of P and Q errs by at most eps ~ band/2 relative per
+ * probability.  Carried through the recursion, the residual entry R_j(t)
+ * then errs by at most eps (P(t) + a_j Q(t)) and its mass Z_j by eps (1 + a_j),
+ * where a_0 = 0, a_1 = 1 and a_{j+1} = 2 a_j + 2.  A test after j
+ * rejections, u Q(x) Z_j against R_j(x), is then off by at most
+ * eps (P(x) + a_{j+1} Q(x)), which is <= 2^(j+1) band max(P(x), Q(x)).
+ * A draw's running sums are off by at most eps (1 + a_j) <= 2^(j+1) band.
+ */
+static double tree_logit_scale(int j, double band) { return ldexp(band, j + 1); }
+
+/* One node's children tests on fp64 P = P[node], Q = Q[qrow(node)]: for the
+ * children c_1..c_m in index order, the exact decision of c_i given that
+ * c_1..c_{i-1} were rejected (acc[i]) and whether it lies in the band
+ * (close[i]); R ends as the residual after every child is rejected, with
+ * mass *Z_out.  kids[] lists the children. */
+static void tree_logit_node_tests(const double *Pn, const double *Qn, int V, const int32_t *kids, int m,
+                                  const int32_t *tok, const float *ua, double band, double *R,
+                                  uint8_t *acc, uint8_t *close, double *Z_out) {
+    const double tiny = ldexp(1.0, -100);
+    for (int t = 0; t < V; ++t) R[t] = Pn[t];
+    double Z = 1.0;
+    for (int i = 0; i < m; ++i) {
+        const int c = kids[i];
+        const int32_t x = tok[c];
+        const double lhs = (double)ua[c] * Qn[x] * Z;
+        const double hi = Pn[x] > Qn[x] ? Pn[x] : Qn[x];
+        acc[i] = (uint8_t)(lhs <= R[x]);
+        close[i] = (uint8_t)(fabs(lhs - R[x]) <= tree_logit_scale(i, band) * hi || hi < tiny);
+        double Zn = 0.0;
+        for (int t = 0; t < V; ++t) {
+            const double v = R[t] - Z * Qn[t];
+            R[t] = v > 0.0 ? v : 0.0;
+            Zn += R[t];
+        }
+        Z = Zn;
+    }
+    *Z_out = Z;
+}
+
+/* fp64 softmax(l / T) of one row into out; -1 for a row logit_row_stats rejects. */
+static int softmax_row(const float *l, int V, double T, double *out) {
+    double m, S;
+    if (logit_row_stats(l, V, T, &m, &S) != 0) return -1;
+    for (int t = 0; t < V; ++t) out[t] = logit_prob(l[t], m, S, T);
+    return 0;
+}
+
+/* The tree's shape: children of every node in index order, and each internal
+ * node's row in the draft logits.  Returns the number of internal nodes, or
+ * -1 for a parent array that is not a tree in node order. */
+static int tree_shape(const int32_t *parent, int n_nodes, int32_t *kid_start, int32_t *kids, int32_t *qrow) {
+    if (n_nodes < 1 || n_nodes > 64 || parent[0] != -1) return -1;
+    for (int i = 1; i < n_nodes; ++i)
+        if (parent[i] < 0 || parent[i] >= i) return -1;
+    int n = 0, internal = 0;
+    for (int i = 0; i < n_nodes; ++i) {
+        kid_start[i] = n;
+        for (int c = i + 1; c < n_nodes; ++c)
+            if (parent[c] == i) kids[n++] = c;
+        qrow[i] = n > kid_start[i] ? internal++ : -1;
+    }
+    kid_start[n_nodes] = n;
+    return internal;
+}
+
+/*
+ * Draft-tree sampler fed by logits: the tree recursion of
+ * oracle_spec_accept_tree (children tested in index order, the residual
+ * R <- max(0, R - Z Q) after each rejection, a draw from R when every child is
+ * rejected -- from P when R is empty -- and a bonus from P at a leaf) on
+ * P[node] = softmax(Lp[node] / T_target) and Q[node] = softmax(Lq[qrow(node)] /
+ * T_draft), formed in fp64 ("Speculative Decoding and KV-Cache Compression",
+ * section 2.3: the ratio takes softmax(logits)[x]; "The Sub-Millisecond
+ * Speculative Decoding Meltdown", tree attention: the target scores every
+ * node of the draft tree in one pass).  Every test is fp64: child c, after j
+ * rejected siblings, is accepted iff u_acc[c] * Q(x_c) * Z <= R(x_c), where
+ * R = P and Z = 1 for the first child.
+ *
+ * near[b] is set when a decision sits where an fp32 formation of P and Q may
+ * take it the other way (tree_logit_scale): a test that ran with
+ * |u Q Z - R(x)| <= 2^(j+1) band max(P(x), Q(x)), or max(P(x), Q(x)) < 2^-100;
+ * a residual after j >= 1 rejections with mass below 2^(j+1) band; a draw
+ * with u*Z within 2^(j+1) band (absolute) of a running sum, or within band
+ * for a draw from P.
+ *
+ * Lp fp32 [B, n_nodes, V]; Lq fp32 [B, n_internal, V] (internal nodes in node
+ * order); node_tokens, u_acc int32/fp32 [B, n_nodes]; u_s fp32 [B]; outputs
+ * as oracle_spec_accept_tree.  Returns ORC_ERR_ARG for a bad tree, sizes or
+ * temperatures, a node token out of range, or a row logit_row_stats rejects.
+ */
+int oracle_spec_accept_tree_logits(int B, int n_nodes, int V, const int32_t *parent, double T_target,
+                                   double T_draft, double band, const float *Lp, const float *Lq,
+                                   const int32_t *node_tokens, const float *u_acc, const float *u_s,
+                                   int32_t *accepted_len, int32_t *path_nodes, int32_t *out_tokens,
+                                   uint8_t *near, int nthreads) {
+    int32_t kid_start[65], kids[64], qrow[64];
+    const int n_internal = tree_shape(parent, n_nodes, kid_start, kids, qrow);
+    if (n_internal < 0 || B < 0 || V < 1 || !(T_target > 0.0) || !(T_draft > 0.0) || !(band >= 0.0))
+        return ORC_ERR_ARG;
+    for (long i = 0; i < (long)B * n_nodes; ++i)
+        if (i % n_nodes && (node_tokens[i] < 0 || node_tokens[i] >= V)) return ORC_ERR_ARG;
+    const int W = oracle_tree_max_depth(parent, n_nodes) + 1;
+    int bad = 0;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int b = 0; b < B; ++b) {
+        double *P = (double *)malloc(sizeof(double) * (size_t)V * 3);
+        double *Q = P + V, *R = Q + V;
+        const int32_t *tok = node_tokens + (long)b * n_nodes;
+        const float *ua = u_acc + (long)b * n_nodes;
+        int32_t *path = path_nodes + (long)b * W;
+        int32_t *outt = out_tokens + (long)b * W;
+        for (int i = 0; i < W; ++i) path[i] = outt[i] = -1;
+        path[0] = 0;
+        int node = 0, depth = 0, ok = 1;
+        uint8_t nb = 0;
+        int32_t final_tok = -1;
+        for (;;) {
+            ok = softmax_row(Lp + ((long)b * n_nodes + node) * V, V, T_target, P) == 0;
+            if (!ok) break;
+            const int m = kid_start[node + 1] - kid_start[node];
+            if (m == 0) { /* leaf: bonus from its own P, band as for any draw from P */
+                final_tok = draw_abs_band(P, V, (double)u_s[b], band, &nb);
+                break;
+            }
+            ok = softmax_row(Lq + ((long)b * n_internal + qrow[node]) * V, V, T_draft, Q) == 0;
+            if (!ok) break;
+            uint8_t acc[64], cl[64];
+            double Z;
+            tree_logit_node_tests(P, Q, V, kids + kid_start[node], m, tok, ua, band, R, acc, cl, &Z);
+            int taken = -1;
+            for (int i = 0; i < m && taken < 0; ++i) {
+                if (cl[i]) nb = 1; /* a test that ran */
+                if (acc[i]) taken = i;
+            }
+            if (taken >= 0) {
+                node = kids[kid_start[node] + taken];
+                ++depth;
+                path[depth] = node;
+                outt[depth - 1] = tok[node];
+                continue;
+            }
+            /* every child rejected: R and Z are the residual after m rejections
+             * (tree_logit_node_tests recomputed the residual past the accepted
+             * child only when there was none) */
+            const double s = tree_logit_scale(m, band);
+            if (Z < s) nb = 1;
+            if (Z > 0.0) {
+                final_tok = draw_abs_band(R, V, (double)u_s[b], s, &nb);
+            } else { /* empty residual: draw from the node's target row */
+                final_tok = draw_abs_band(P, V, (double)u_s[b], band, &nb);
+            }
+            break;
+        }
+        free(P);
+        if (!ok) {
+            bad = 1;
+            continue;
+        }
+        accepted_len[b] = depth;
+        outt[depth] = final_tok;
+        if (near) near[b] = nb;
+    }
+    return bad ? ORC_ERR_ARG : ORC_OK;
+}
+
+/*
+ * Every outcome an fp32 formation of the tree sampler fed by logits may
+ * produce, per sequence b and node n, from the inputs alone (the decisions
+ * and bands of oracle_spec_accept_tree_logits):
+ *   end_ok[b][n] = 1 when the walk may end at n: each test on the way from the
+ *   root (the siblings before the path's child rejected, the path's child
+ *   accepted) and, at an internal n, every child's rejection is the exact
+ *   decision or lies in its band;
+ *   [tok_lo, tok_hi][b][n] = the tokens the final draw at n may give: the
+ *   tokens whose running-sum interval, widened by the draw's band, holds u*Z
+ *   (from P[n] at a leaf; from the residual after all m children are
+ *   rejected at an internal node, the whole vocabulary when its mass is below
+ *   the band, as it may then be empty).
+ */
+int oracle_tree_logits_outcomes(int B, int n_nodes, int V, const int32_t *parent, double T_target,
+                                double T_draft, double band, const float *Lp, const float *Lq,
+                                const int32_t *node_tokens, const float *u_acc, const float *u_s,
+                                uint8_t *end_ok, int32_t *tok_lo, int32_t *tok_hi, int nthreads) {
+    int32_t kid_start[65], kids[64], qrow[64];
+    const int n_internal = tree_shape(parent, n_nodes, kid_start, kids, qrow);
+    if (n_internal < 0 || B < 0 || V < 1 || !(T_target > 0.0) || !(T_draft > 0.0) || !(band >= 0.0))
+        return ORC_ERR_ARG;
+    for (long i = 0; i < (long)B * n_nodes; ++i)
+        if (i % n_nodes && (node_tokens[i] < 0 || node_tokens[i] >= V)) return ORC_ERR_ARG;
+    int bad = 0;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int b = 0; b < B; ++b) {
+        double *P = (double *)malloc(sizeof(double) * (size_t)V * 3);
+        double *Q = P + V, *R = Q + V;
+        const int32_t *tok = node_tokens + (long)b * n_nodes;
+        const float *ua = u_acc + (long)b * n_nodes;
+        uint8_t reach[64];
+        uint8_t *eo = end_ok + (long)b * n_nodes;
+        int32_t *lo = tok_lo + (long)b * n_nodes, *hi = tok_hi + (long)b * n_nodes;
+        reach[0] = 1;
+        for (int n = 0; n < n_nodes && !bad; ++n) { /* parents come before children */
+            if (softmax_row(Lp + ((long)b * n_nodes + n) * V, V, T_target, P) != 0) {
+                bad = 1;
+                break;
+            }
+            const int m = kid_start[n + 1] - kid_start[n];
+            double Z = 1.0, s = band;
+            const double *W = P;
+            int all_rejected_ok = 1;
+            if (m > 0) {
+                if (softmax_row(Lq + ((long)b * n_internal + qrow[n]) * V, V, T_draft, Q) != 0) {
+                    bad = 1;
+                    break;
+                }
+                uint8_t acc[64], cl[64];
+                tree_logit_node_tests(P, Q, V, kids + kid_start[n], m, tok, ua, band, R, acc, cl, &Z);
+                int before_ok = 1; /* the siblings before child i may all be rejected */
+                for (int i = 0; i < m; ++i) {
+                    const int c = kids[kid_start[n] + i];
+                    reach[c] = (uint8_t)(reach[n] && before_ok && (acc[i] || cl[i]));
+                    before_ok = before_ok && (!acc[i] || cl[i]);
+                }
+                all_rejected_ok = before_ok;
+                s = tree_logit_scale(m, band);
+                W = R;
+            }
+            eo[n] = (uint8_t)(reach[n] && all_rejected_ok);
+            if (m > 0 && Z < s) { /* a residual that may be empty: any token */
+                lo[n] = 0;
+                hi[n] = V - 1;
+                continue;
+            }
+            const double target = (double)u_s[b] * Z;
+            double C = 0.0;
+            int32_t l = -1, h = -1;
+            for (int t = 0; t < V; ++t) {
+                C += W[t];
+                if (l < 0 && C >= target - s) l = t;
+                if (h < 0 && C > target + s) h = t;
+            }
+            lo[n] = l < 0 ? V - 1 : l;
+            hi[n] = h < 0 ? V - 1 : h;
+        }
+        free(P);
+    }
+    return bad ? ORC_ERR_ARG : ORC_OK;
 }
 
 /* ------------------------------------------------------------------ */
