@@ -392,6 +392,64 @@ def time_logits(wl: W.Workload, seed: int, steps: int, warmup: int, stream):
     return sum(ms) / len(ms), ms, nbytes
 
 
+def time_tree_logits(wl: W.Workload, seed: int, steps: int, warmup: int, stream, peak: float):
+    """The draft-tree sampler fed by logits (svpa_spec_accept_tree_logits) on
+    the draft-tree workload's sampler shape: B sequences, a target logit row at
+    every node and a draft row at every internal node, V fp32 each; L2 flushed
+    before each launch.  The walk reads only the rows of the nodes it visits
+    (a target row per node on the accepted path, the draft row of each
+    internal node on it), so the algorithmic bytes count those rows from the
+    launch's own paths; `dense_bytes` counts every row (what a front-end that
+    forms all softmax statistics first would read)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ti = W.make_tree_logits(wl, seed + 6, device=dev)
+    B, n, V = ti.lp.shape
+    par = ti.parent.tolist()
+    depth = [0] * n
+    for i in range(1, n):
+        depth[i] = depth[par[i]] + 1
+    Wd = max(depth) + 1
+    internal = {p for p in par[1:]}
+    k = torch.empty(B, dtype=torch.int32, device=dev)
+    path = torch.empty((B, Wd), dtype=torch.int32, device=dev)
+    toks = torch.empty((B, Wd), dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def run():
+        svpa.spec_accept_tree_logits(par, ti.lp, ti.lq, ti.tokens, ti.u_accept, ti.u_sample, k, path, toks,
+                                     error_flag=err, temperature=ti.temperature)
+
+    for _ in range(warmup):
+        run()
+    ms = []
+    for _ in range(steps):
+        flush.fill_(1)
+        gpu_lead()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    assert svpa.check_error(err) == 0, "device error in the tree logits front-end"
+    rows = 0
+    for b_path, b_k in zip(path.cpu().tolist(), k.cpu().tolist()):
+        nodes = b_path[:b_k + 1]
+        rows += len(nodes) + sum(1 for x in nodes if x in internal)
+    small = B * n * (4 + 4) + B * 4 + B * Wd * 4 * 2 + B * 4
+    nbytes = rows * V * 4 + small
+    dense = (n + len(internal)) * B * V * 4 + small
+    avg = sum(ms) / len(ms)
+    gbs = nbytes / (avg * 1e-3) / 1e9
+    return {"us": round(avg * 1e3, 2), "gbs": round(gbs, 2), "frac_of_peak": round(gbs / peak, 4),
+            "bytes_per_launch": nbytes, "dense_bytes": dense, "rows_read_per_seq": round(rows / B, 3),
+            "p10_p50_p90_us": [round(x * 1e3, 2) for x in percentiles(ms)],
+            "shape": f"B={B}, {n} nodes ({len(internal)} internal), V={V}, fp32 logits",
+            "bytes": "the visited rows' logits (target row per node on the path, draft row per internal node "
+                     "on it), plus tokens, uniforms and outputs"}
+
+
 LEAD_CYCLES = 200_000  # about 0.1 ms of GPU spin at GB300 clocks
 LAUNCH_BOUND_US = 10.0  # roofline time below which a call is flagged launch-bound
 
@@ -836,9 +894,11 @@ def main():
     del ap
     # the draft-length controller on this step's accepted lengths
     gam_ms = time_gamma(st, K, args.warmup, stream)
-    # the sampler fed by logits (linear workloads)
+    # the sampler fed by logits
     logit = None
-    if not st.tree:
+    if st.tree:
+        logit = time_tree_logits(wl, seed, K, args.warmup, stream, peak)
+    else:
         lg_ms, lg_list, lg_bytes = time_logits(wl, seed, K, args.warmup, stream)
         lg_gbs = lg_bytes / (lg_ms * 1e-3) / 1e9
         logit = {"us": round(lg_ms * 1e3, 2), "gbs": round(lg_gbs, 2), "frac_of_peak": round(lg_gbs / peak, 4),
@@ -878,6 +938,10 @@ def main():
                 continue
             per_config[name] = time_attention_only(name, K, args.warmup, peak)
             torch.cuda.empty_cache()
+            if W.WORKLOADS[name].tree_branching:
+                per_config[name]["spec_accept_tree_logits"] = time_tree_logits(
+                    W.WORKLOADS[name], W.SEEDS[name], K, args.warmup, stream, peak)
+                torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

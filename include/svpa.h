@@ -16,7 +16,7 @@
  *   svpa_spec_accept_tree    drafts (or along a draft tree): accepted count,
  *                            accepted tokens and the correction/bonus token.
  *   svpa_spec_accept_logits  the same from logits (the softmax rows formed
- *                            in the kernel, at sampling temperatures).
+ *   svpa_spec_accept_tree_logits  in the kernel, at sampling temperatures).
  *   svpa_block_table_commit  commit the accepted tokens and roll back the
  *                            rest: new lengths, dropped pages returned to the
  *                            free stack when their reference count reaches 0.
@@ -318,6 +318,56 @@ svpa_status svpa_spec_accept_tree(int32_t batch, int32_t n_nodes, int32_t vocab,
                                   int32_t *out_tokens, uint8_t *near_boundary,
                                   void *workspace, size_t workspace_bytes,
                                   int32_t *error_flag, void *stream);
+
+/*
+ * Draft-tree rejection sampler fed by logits: the recursion of
+ * svpa_spec_accept_tree on P[node] = softmax(target_logits[node] /
+ * temperature) and Q[node] = softmax(draft_logits[row of node] /
+ * draft_temperature), formed in the kernel and never written out.  The walk
+ * forms the softmax statistics (max and normaliser) of the rows it visits
+ * only: one target row per node on the accepted path and the draft row of
+ * each internal node on it, read from memory once for the statistics and
+ * again (from L2) for a residual update or draw; the rows of nodes off the
+ * path are never read.  Every test is made in fp64 on fp32 exponentials:
+ * child c, after j rejected siblings, is accepted iff
+ * u_accept[c] * Q(x_c) * Z <= R(x_c), with R = P, Z = 1 for the first child
+ * (there the test is cross-multiplied by both normalisers, as in
+ * svpa_spec_accept_logits); the residual R <- max(0, R - Z Q) is fp32.
+ *
+ * Sources: "Speculative Decoding and KV-Cache Compression", section 2.3 (the
+ * acceptance ratio takes softmax(logits)[x]); "The Sub-Millisecond
+ * Speculative Decoding Meltdown" (the target scores every node of the draft
+ * tree in one pass); the multi-child rule as for svpa_spec_accept_tree.
+ *
+ *  parent       HOST int32 [n_nodes]: parent[0] = -1, 0 <= parent[i] < i
+ *  target_logits fp32 [B, n_nodes, V]; -inf entries are masked tokens; a row
+ *               the walk visits that has no finite entry, a NaN or +inf
+ *               raises SVPA_DEVERR_BAD_VALUE
+ *  draft_logits fp32 [B, n_internal, V]: the draft logits of the children of
+ *               each internal node, in node order
+ *  temperature, draft_temperature  > 0 and finite (log2(e)/T must be finite
+ *               in fp32), else SVPA_ERR_INVALID_ARG
+ *  node_tokens, u_accept, u_sample, accepted_len, path_nodes, out_tokens as
+ *               for svpa_spec_accept_tree
+ *  near_boundary uint8 [B] or NULL: 1 when a decision lay where forming P and
+ *               Q in fp32 may take it the other way; after j rejected
+ *               siblings the band is s_j = 2^(j+1) * 5e-5: a test with
+ *               |u Q Z - R(x)| <= s_j max(P(x), Q(x)), a residual of mass
+ *               below s_j, a draw with u * Z within s_j (within 5e-5 for a
+ *               draw from P) of a running sum.
+ *  n_nodes 1..64; V <= 262144, else SVPA_ERR_UNSUPPORTED.  Needs no
+ *  workspace.  One kernel on `stream` (a thread-block cluster per sequence).
+ */
+svpa_status svpa_spec_accept_tree_logits(int32_t batch, int32_t n_nodes, int32_t vocab,
+                                         const int32_t *parent, float temperature,
+                                         float draft_temperature,
+                                         const float *target_logits,
+                                         const float *draft_logits,
+                                         const int32_t *node_tokens,
+                                         const float *u_accept, const float *u_sample,
+                                         int32_t *accepted_len, int32_t *path_nodes,
+                                         int32_t *out_tokens, uint8_t *near_boundary,
+                                         int32_t *error_flag, void *stream);
 
 /*
  * Commit the accepted tokens of every sequence and roll back the rest.

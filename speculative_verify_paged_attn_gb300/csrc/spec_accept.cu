@@ -23,9 +23,11 @@
 // scalar operations per CTA.  Vocabularies beyond 262144 tokens take a
 // one-CTA-per-row kernel.
 //
-// Also here: the draft-tree sampler on the same cluster split, and the
-// linear sampler fed by logits (softmax rows formed in the kernels: slab
-// statistics, then the cluster sampler on a logits weight source).
+// Also here: the draft-tree sampler on the same cluster split, the linear
+// sampler fed by logits (softmax rows formed in the kernels: slab
+// statistics, then the cluster sampler on a logits weight source), and the
+// draft-tree sampler fed by logits (the statistics of the visited rows only,
+// formed by the cluster at each node of the walk).
 //
 // This file is compiled with -fmad=false; the acceptance product also uses
 // __fmul_rn, which is never contracted.
@@ -1038,6 +1040,310 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     cluster_sync_all();
 }
 
+// ---------------------------------------------------------------- tree, fed by logits
+// The draft-tree recursion of spec_accept_tree_cluster_kernel on P[node] =
+// softmax(Lp[node] / T) and Q[node] = softmax(Lq[qrow(node)] / T_draft)
+// ("Speculative Decoding and KV-Cache Compression", section 2.3; "The
+// Sub-Millisecond Speculative Decoding Meltdown", tree attention).  The walk
+// visits one node per level, so the softmax statistics are formed for the
+// visited rows only, by the cluster at each node: every CTA reduces its slice
+// of the node's target row and draft row to (max, sum of 2^((l - max) c)),
+// the pairs are exchanged through distributed shared memory and merged in
+// rank order (fp64 sums), so every CTA holds the same normalisers.  The first
+// child's test is fp64 on fp32 exponentials cross-multiplied by both
+// normalisers (as in the linear sampler fed by logits); a later child is
+// tested as u Q(x) Z <= R(x) with the fp32 residual R, formed from fp32
+// probabilities 2^((l - max) c) / S and probed at x by the CTA that owns x.
+//
+// Near band after j rejected siblings: s_j = 2^(j+1) * 5e-5.  Each fp32
+// probability errs by at most ~2.5e-5 relative; carried through the
+// recursion R <- max(0, R - Z Q), Z = sum R, a residual entry errs by at most
+// eps (P + a_j Q) and its mass by eps (1 + a_j) with a_1 = 1, a_{j+1} = 2 a_j + 2,
+// so a test after j rejections is off by at most eps (P + a_{j+1} Q) <= s_j
+// max(P, Q), and a draw's running sums by at most s_j.
+
+// Residual update from logits: R <- max(0, prev - zf * Q) in fp32, prev = P
+// (formed from its logits) on a node's first rejection, else R.
+struct SrcUpdateLogits {
+    float *R;
+    const float *p;  // nullptr: prev = R
+    const float *q;
+    int lo, V;
+    float zf;
+    bool vec;
+    float mp, cp, ip, mq, cq, iq;
+    __device__ float4 operator()(int t0) const {
+        float4 prev = make_float4(0.f, 0.f, 0.f, 0.f), qv = prev;
+        if (t0 < V) {
+            if (p) {
+                const float4 l = load_logits4(p, t0, V, vec);
+                prev = make_float4(ex2_approx((l.x - mp) * cp) * ip, ex2_approx((l.y - mp) * cp) * ip,
+                                   ex2_approx((l.z - mp) * cp) * ip, ex2_approx((l.w - mp) * cp) * ip);
+            } else {
+                prev = *reinterpret_cast<const float4 *>(R + (t0 - lo));
+            }
+            const float4 l = load_logits4(q, t0, V, vec);
+            qv = make_float4(ex2_approx((l.x - mq) * cq) * iq, ex2_approx((l.y - mq) * cq) * iq,
+                             ex2_approx((l.z - mq) * cq) * iq, ex2_approx((l.w - mq) * cq) * iq);
+        }
+        const float4 r = make_float4(relu(prev.x - __fmul_rn(zf, qv.x)), relu(prev.y - __fmul_rn(zf, qv.y)),
+                                     relu(prev.z - __fmul_rn(zf, qv.z)), relu(prev.w - __fmul_rn(zf, qv.w)));
+        *reinterpret_cast<float4 *>(R + (t0 - lo)) = r;
+        return r;
+    }
+};
+
+// Softmax statistics of a node's two rows (0: target, 1: draft), as every CTA
+// of the cluster holds them after cluster_row_stats.
+struct TreeRowStats {
+    float2 mine[2][2];  // this CTA's (max, sum) by exchange parity and row (read by peers)
+    float2 w[2][kClWarps];
+    float m[2];
+    double S[2];
+    float inv[2];       // 1 / S rounded to fp32
+    int bad;
+};
+
+// (max, sum) of this CTA's slice of `row` at scale c, merged over warp w's
+// steps (groups of 16 logits), then over the warp's lanes; lane 0 stores the
+// warp's pair in w[warp].
+template <int NI>
+__device__ __forceinline__ void warp_row_stats(const float *row, float c, const ClusterGeom &g, int V, bool vec,
+                                               float2 *w) {
+    const int lane = threadIdx.x & 31;
+    float m = -CUDART_INF_F, s = 0.f;
+#pragma unroll
+    for (int i0 = 0; i0 < NI; i0 += 4) {
+        float4 x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            x[j] = i0 + j < NI ? load_logits4(row, g.wbase + (i0 + j) * kStep + 4 * lane, V, vec)
+                               : make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F);
+        float m2, s2;
+        group_stats16(x, c, m2, s2);
+        online_merge(m, s, m2, s2, c);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        online_merge(m, s, m2, s2, c);
+    }
+    if (lane == 0) w[threadIdx.x >> 5] = make_float2(m, s);
+}
+
+// The softmax statistics of the target row p (scale cp) and, when q is not
+// null, the draft row q (scale cq) over the whole cluster.  Every thread of
+// every CTA calls this with the same parity; on return ts.m, ts.S, ts.inv
+// are the same in every CTA, and ts.bad is set for a row with no finite
+// logit, a NaN or +inf.
+template <int NI>
+__device__ void cluster_row_stats(TreeRowStats &ts, const float *p, const float *q, float cp, float cq,
+                                  const ClusterGeom &g, int V, bool vec, int parity) {
+    const int lane = threadIdx.x & 31;
+    warp_row_stats<NI>(p, cp, g, V, vec, ts.w[0]);
+    if (q) warp_row_stats<NI>(q, cq, g, V, vec, ts.w[1]);
+    __syncthreads();
+    if (threadIdx.x < 2) {
+        const int r = threadIdx.x;
+        const float c = r == 0 ? cp : cq;
+        float m = -CUDART_INF_F, s = 0.f;
+        if (r == 0 || q)
+            for (int w = 0; w < kClWarps; ++w) online_merge(m, s, ts.w[r][w].x, ts.w[r][w].y, c);
+        ts.mine[parity][r] = make_float2(m, s);
+    }
+    cluster_sync_all();
+    if (threadIdx.x < 32) {
+        for (int r = 0; r < (q ? 2 : 1); ++r) {
+            const float c = r == 0 ? cp : cq;
+            float2 v = make_float2(-CUDART_INF_F, 0.f);
+            if (lane < g.n_ctas) {
+                v.x = ld_peer_f32(&ts.mine[parity][r].x, (uint32_t)lane);
+                v.y = ld_peer_f32(&ts.mine[parity][r].y, (uint32_t)lane);
+            }
+            float m = v.x;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            double S = (m > -CUDART_INF_F && v.x > -CUDART_INF_F) ? (double)v.y * (double)ex2_approx((v.x - m) * c)
+                                                                   : 0.0;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+            if (lane == 0) {
+                ts.m[r] = m;
+                ts.S[r] = S;
+                ts.inv[r] = (float)(1.0 / S);
+                if (!(S > 0.0) || !(S < CUDART_INF) || !(m > -CUDART_INF_F) || !(m < CUDART_INF_F)) ts.bad = 1;
+            }
+        }
+    }
+    __syncthreads();
+}
+
+template <int NI>
+__global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
+    spec_accept_tree_logits_cluster_kernel(const __grid_constant__ TreeArgs a, int n_ctas) {
+    extern __shared__ float4 dyn_smem[];
+    float *R = reinterpret_cast<float *>(dyn_smem);  // this CTA's residual slice
+    __shared__ ClusterRow<NI> st;
+    __shared__ TreeRowStats ts;
+    const ClusterGeom g = cluster_geom<NI>(a.V, n_ctas);
+    const int b = (int)(blockIdx.x / (unsigned)n_ctas);
+    const int V = a.V, n_nodes = a.n_nodes;
+    const int32_t *ntok = a.tokens + (size_t)b * n_nodes;
+    const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.p) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
+    const bool lead = g.rank == 0 && threadIdx.x == 0;
+    // node tokens and uniforms; per child of the node being visited the
+    // exponentials 2^((l_x - max) c) of its token in the node's two rows
+    __shared__ int s_x[kMaxNq];
+    __shared__ float s_ua[kMaxNq], s_ep[kMaxNq], s_eq[kMaxNq];
+    if (threadIdx.x < (unsigned)n_nodes) {
+        int x = ntok[threadIdx.x];
+        if (x < 0 || x >= V) {
+            if (g.rank == 0 && threadIdx.x > 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+            x = 0;
+        }
+        s_x[threadIdx.x] = x;
+        s_ua[threadIdx.x] = __ldg(a.u_acc + (size_t)b * n_nodes + threadIdx.x);
+    }
+    if (threadIdx.x == 0) ts.bad = 0;
+    const float u_s = __ldg(a.u_s + b);
+    __syncthreads();
+    int node = 0, depth = 0, parity = 0;
+    bool near = false, drew = false;
+    int tok = -1;
+    while (true) {
+        const float *Pn = a.p + ((size_t)b * n_nodes + node) * V;
+        const int qr = a.qrow[node];
+        const float *Qn = qr >= 0 ? a.q + ((size_t)b * a.n_internal + qr) * V : nullptr;
+        if (threadIdx.x == 0) {
+            prefetch_slice(Pn, g.cta_lo, g.cta_hi, vec);
+            prefetch_slice(Qn, g.cta_lo, g.cta_hi, vec);
+        }
+        cluster_row_stats<NI>(ts, Pn, Qn, a.c_target, a.c_draft, g, V, vec, parity);
+        parity ^= 1;
+        SrcLogits srcp;
+        srcp.p = Pn;
+        srcp.q = nullptr;
+        srcp.V = V;
+        srcp.vec = vec;
+        srcp.mp = ts.m[0];
+        srcp.cp = a.c_target;
+        srcp.ip = ts.inv[0];
+        srcp.mq = 0.f;
+        srcp.cq = a.c_draft;
+        srcp.iq = 0.f;
+        if (qr < 0) {  // leaf: bonus token from its own P
+            cluster_sum(st, srcp, g, parity);
+            parity ^= 1;
+            bool nb = false;
+            drew = cluster_draw(st, srcp, g, u_s, &tok, &nb, kLogitBand);
+            near |= nb;
+            break;
+        }
+        {
+            const int c = node + 1 + (int)threadIdx.x;
+            if (c < n_nodes && a.parent[c] == node) {
+                s_ep[c] = ex2_approx((__ldg(Pn + s_x[c]) - ts.m[0]) * a.c_target);
+                s_eq[c] = ex2_approx((__ldg(Qn + s_x[c]) - ts.m[1]) * a.c_draft);
+            }
+            __syncthreads();
+        }
+        const double Sp = ts.S[0], Sq = ts.S[1];
+        double Z = 1.0;
+        float rx = 0.f;  // R(x) of the child under test, after a rejection
+        int accepted = -1, j = 0;
+        for (int c = node + 1; c < n_nodes; ++c) {
+            if (a.parent[c] != node) continue;
+            const double ep = s_ep[c], eq = s_eq[c], u = s_ua[c];
+            const double band = ldexp(kLogitBand, j + 1);
+            bool ok, close;
+            if (j == 0) {  // u Q <= P with both sides multiplied by Sp Sq > 0
+                const double P = ep * Sq, Qs = eq * Sp, uq = u * Qs;
+                const double hi = fmax(P, Qs);
+                ok = uq <= P;
+                close = fabs(uq - P) <= band * hi || hi < kLogitTiny * (Sp * Sq);
+            } else {
+                const double P = ep / Sp, Qx = eq / Sq;
+                const double lhs = u * Qx * Z;
+                const double hi = fmax(P, Qx);
+                ok = lhs <= (double)rx;
+                close = fabs(lhs - (double)rx) <= band * hi || hi < kLogitTiny;
+            }
+            near |= close;
+            if (ok) {
+                accepted = c;
+                break;
+            }
+            int xn = -1;  // the next sibling's token: R is probed there
+            for (int c2 = c + 1; c2 < n_nodes; ++c2)
+                if (a.parent[c2] == node) {
+                    xn = s_x[c2];
+                    break;
+                }
+            SrcUpdateLogits upd;
+            upd.R = R;
+            upd.p = j == 0 ? Pn : nullptr;
+            upd.q = Qn;
+            upd.lo = g.cta_lo;
+            upd.V = V;
+            upd.zf = (float)Z;
+            upd.vec = vec;
+            upd.mp = ts.m[0];
+            upd.cp = a.c_target;
+            upd.ip = ts.inv[0];
+            upd.mq = ts.m[1];
+            upd.cq = a.c_draft;
+            upd.iq = ts.inv[1];
+            Z = cluster_sum(st, upd, g, parity, xn, R);
+            parity ^= 1;
+            rx = st.probe_val;
+            ++j;
+        }
+        if (accepted >= 0) {
+            ++depth;
+            if (lead) {
+                a.path_nodes[(size_t)b * a.width + depth] = accepted;
+                a.out_tokens[(size_t)b * a.width + depth - 1] = s_x[accepted];
+            }
+            node = accepted;
+            continue;
+        }
+        const double s = ldexp(kLogitBand, j + 1);
+        if (Z < s) near = true;
+        bool nb = false;
+        if (Z > 0.0) {
+            drew = cluster_draw(st, SrcSmem{R, g.cta_lo}, g, u_s, &tok, &nb, s);
+        } else {  // empty residual: draw from the node's target row
+            cluster_sum(st, srcp, g, parity);
+            parity ^= 1;
+            drew = cluster_draw(st, srcp, g, u_s, &tok, &nb, kLogitBand);
+        }
+        near |= nb;
+        break;
+    }
+    if (drew && threadIdx.x == 0) {
+        if (tok < 0) {  // a row with no mass
+            raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+            tok = 0;
+        }
+        a.out_tokens[(size_t)b * a.width + depth] = tok;
+        if (a.near) a.near[b] = near ? 1 : 0;
+    }
+    if (lead) {
+        if (ts.bad) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+        int32_t *path = a.path_nodes + (size_t)b * a.width;
+        int32_t *out = a.out_tokens + (size_t)b * a.width;
+        path[0] = 0;
+        for (int d = depth + 1; d < a.width; ++d) {
+            path[d] = -1;
+            out[d] = -1;
+        }
+        a.accepted_len[b] = depth;
+    }
+    cluster_sync_all();
+}
+
 int sm_count_cached() {
     static DeviceMemo<int> memo;
     int n = 0;
@@ -1153,6 +1459,17 @@ cudaError_t launch_spec_accept_tree(const TreeArgs &a, cudaStream_t stream) {
         spec_accept_tree_cluster_kernel<1>, spec_accept_tree_cluster_kernel<2>,
         spec_accept_tree_cluster_kernel<4>, spec_accept_tree_cluster_kernel<8>,
         spec_accept_tree_cluster_kernel<16>, spec_accept_tree_cluster_kernel<32>};
+    return launch_cluster(kernels, a, a.V, a.B, (size_t)kClWarps * kStep * sizeof(float), stream);
+}
+
+
+cudaError_t launch_spec_accept_tree_logits(const TreeArgs &a, cudaStream_t stream) {
+    if (a.B <= 0) return cudaSuccess;
+    if (cluster_steps(a.B, a.V) == 0) return cudaErrorInvalidValue;
+    static void (*const kernels[])(TreeArgs, int) = {
+        spec_accept_tree_logits_cluster_kernel<1>,  spec_accept_tree_logits_cluster_kernel<2>,
+        spec_accept_tree_logits_cluster_kernel<4>,  spec_accept_tree_logits_cluster_kernel<8>,
+        spec_accept_tree_logits_cluster_kernel<16>, spec_accept_tree_logits_cluster_kernel<32>};
     return launch_cluster(kernels, a, a.V, a.B, (size_t)kClWarps * kStep * sizeof(float), stream);
 }
 

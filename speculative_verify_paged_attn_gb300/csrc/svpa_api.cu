@@ -169,6 +169,26 @@ svpa_status check_attn_call(const svpa_attn_params *p, const void *q, const void
     return SVPA_OK;
 }
 
+bool fill_tree_shape(const int32_t *parent, int n_nodes, TreeArgs &a) {
+    if (!parent || n_nodes < 1 || n_nodes > kMaxNq || parent[0] != -1) return false;
+    for (int i = 1; i < n_nodes; ++i)
+        if (parent[i] < 0 || parent[i] >= i) return false;
+    int depth_max = 0, n_internal = 0;
+    for (int i = 0; i < n_nodes; ++i) {
+        int d = 0;
+        for (int x = i; x > 0; x = parent[x]) ++d;
+        depth_max = std::max(depth_max, d);
+        bool has_child = false;
+        for (int c = i + 1; c < n_nodes; ++c) has_child |= parent[c] == i;
+        a.qrow[i] = has_child ? (int8_t)n_internal++ : (int8_t)-1;
+        a.parent[i] = (int8_t)parent[i];
+    }
+    a.n_nodes = n_nodes;
+    a.n_internal = n_internal;
+    a.width = depth_max + 1;
+    return true;
+}
+
 }  // namespace svpa
 
 extern "C" {
@@ -405,27 +425,14 @@ svpa_status svpa_spec_accept_tree(int32_t batch, int32_t n_nodes, int32_t vocab,
     svpa::NvtxRange nvtx_range("svpa_spec_accept_tree");
     (void)workspace;
     (void)workspace_bytes;
-    if (batch < 0 || n_nodes < 1 || n_nodes > kMaxNq || vocab < 1 || !parent) return SVPA_ERR_INVALID_ARG;
+    TreeArgs a;
+    memset(&a, 0, sizeof a);
+    if (batch < 0 || vocab < 1 || !fill_tree_shape(parent, n_nodes, a)) return SVPA_ERR_INVALID_ARG;
     if (vocab > spec_accept_tree_max_vocab()) return SVPA_ERR_UNSUPPORTED;  // residual slices in shared memory
-    if (parent[0] != -1) return SVPA_ERR_INVALID_ARG;
-    for (int i = 1; i < n_nodes; ++i)
-        if (parent[i] < 0 || parent[i] >= i) return SVPA_ERR_INVALID_ARG;
     if (batch == 0) return SVPA_OK;
     if (!p_probs || !q_probs || !node_tokens || !u_accept || !u_sample || !accepted_len || !path_nodes ||
         !out_tokens || !error_flag)
         return SVPA_ERR_INVALID_ARG;
-    TreeArgs a;
-    memset(&a, 0, sizeof a);
-    int depth_max = 0, n_internal = 0;
-    for (int i = 0; i < n_nodes; ++i) {
-        int d = 0;
-        for (int x = i; x > 0; x = parent[x]) ++d;
-        depth_max = std::max(depth_max, d);
-        bool has_child = false;
-        for (int c = i + 1; c < n_nodes; ++c) has_child |= parent[c] == i;
-        a.qrow[i] = has_child ? (int8_t)n_internal++ : (int8_t)-1;
-        a.parent[i] = (int8_t)parent[i];
-    }
     a.p = p_probs;
     a.q = q_probs;
     a.tokens = node_tokens;
@@ -437,10 +444,7 @@ svpa_status svpa_spec_accept_tree(int32_t batch, int32_t n_nodes, int32_t vocab,
     a.near = near_boundary;
     a.err = error_flag;
     a.B = batch;
-    a.n_nodes = n_nodes;
     a.V = vocab;
-    a.width = depth_max + 1;
-    a.n_internal = n_internal;
     return from_cuda(launch_spec_accept_tree(a, static_cast<cudaStream_t>(stream)));
 }
 

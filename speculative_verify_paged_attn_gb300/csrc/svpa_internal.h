@@ -160,10 +160,15 @@ struct TreeArgs {
     uint8_t *near;
     int32_t *err;
     int32_t B, n_nodes, V, width, n_internal;
+    float c_target, c_draft;  // fed by logits (p, q are logits): log2(e) / temperature
     int8_t parent[kMaxNq];
     int8_t qrow[kMaxNq];
 };
+// parent[] validated (parent[0] = -1, 0 <= parent[i] < i, n_nodes 1..64) into
+// a.parent, a.qrow, a.n_nodes, a.n_internal and a.width; false when invalid.
+bool fill_tree_shape(const int32_t *parent, int n_nodes, TreeArgs &a);
 cudaError_t launch_spec_accept_tree(const TreeArgs &a, cudaStream_t stream);
+cudaError_t launch_spec_accept_tree_logits(const TreeArgs &a, cudaStream_t stream);
 
 struct CommitArgs {
     int32_t *block_table;

@@ -1,5 +1,5 @@
-// svpa_logits_api.cu -- the C ABI of the sampler's logits front-end: host-side
-// validation and the launch.  No function here allocates device memory.
+// svpa_logits_api.cu -- the C ABI of the samplers' logits front-ends (linear
+// and draft tree): host-side validation and the launches.  No function here allocates device memory.
 #include <cuda_runtime.h>
 #include <float.h>
 #include <stdint.h>
@@ -11,6 +11,20 @@
 #include "svpa_internal.h"
 
 using namespace svpa;
+
+namespace {
+
+// log2(e) / T rounded once to fp32, for a finite T > 0 whose scale is finite
+// in fp32 (a temperature so small that it overflows is refused).
+bool scale_of_temperature(float T, float *c) {
+    if (!std::isfinite(T) || !(T > 0.f)) return false;
+    const double v = 1.4426950408889634 / (double)T;
+    if (!(v <= (double)FLT_MAX)) return false;
+    *c = (float)v;
+    return true;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -31,14 +45,9 @@ svpa_status svpa_spec_accept_logits(int32_t batch, int32_t gamma, int32_t vocab,
                                     size_t workspace_bytes, int32_t *error_flag, void *stream) {
     svpa::NvtxRange nvtx_range("svpa_spec_accept_logits");
     if (batch < 0 || gamma < 1 || gamma > 32 || vocab < 1) return SVPA_ERR_INVALID_ARG;
-    if (!std::isfinite(temperature) || !(temperature > 0.f) || !std::isfinite(draft_temperature) ||
-        !(draft_temperature > 0.f))
+    float ct = 0.f, cd = 0.f;
+    if (!scale_of_temperature(temperature, &ct) || !scale_of_temperature(draft_temperature, &cd))
         return SVPA_ERR_INVALID_ARG;
-    // log2(e) / T, rounded once to fp32; a temperature so small that it
-    // overflows fp32 is refused
-    const double ct = 1.4426950408889634 / (double)temperature;
-    const double cd = 1.4426950408889634 / (double)draft_temperature;
-    if (!(ct <= (double)FLT_MAX) || !(cd <= (double)FLT_MAX)) return SVPA_ERR_INVALID_ARG;
     if (vocab > spec_accept_tree_max_vocab()) return SVPA_ERR_UNSUPPORTED;  // one cluster per row
     if (batch > 0x7fffffff / 8) return SVPA_ERR_UNSUPPORTED;
     if ((long long)batch * (2 * gamma + 1) * ((vocab + 4095) / 4096) > 0x7fffffffLL) return SVPA_ERR_UNSUPPORTED;
@@ -64,10 +73,47 @@ svpa_status svpa_spec_accept_logits(int32_t batch, int32_t gamma, int32_t vocab,
     a.B = batch;
     a.gamma = gamma;
     a.V = vocab;
-    a.c_target = (float)ct;
-    a.c_draft = (float)cd;
+    a.c_target = ct;
+    a.c_draft = cd;
     a.stats = static_cast<float2 *>(workspace);
     const cudaError_t e = launch_spec_accept_logits(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVPA_OK : SVPA_ERR_CUDA;
+}
+
+svpa_status svpa_spec_accept_tree_logits(int32_t batch, int32_t n_nodes, int32_t vocab, const int32_t *parent,
+                                         float temperature, float draft_temperature, const float *target_logits,
+                                         const float *draft_logits, const int32_t *node_tokens,
+                                         const float *u_accept, const float *u_sample, int32_t *accepted_len,
+                                         int32_t *path_nodes, int32_t *out_tokens, uint8_t *near_boundary,
+                                         int32_t *error_flag, void *stream) {
+    svpa::NvtxRange nvtx_range("svpa_spec_accept_tree_logits");
+    TreeArgs a;
+    memset(&a, 0, sizeof a);
+    if (batch < 0 || vocab < 1 || !fill_tree_shape(parent, n_nodes, a)) return SVPA_ERR_INVALID_ARG;
+    float ct = 0.f, cd = 0.f;
+    if (!scale_of_temperature(temperature, &ct) || !scale_of_temperature(draft_temperature, &cd))
+        return SVPA_ERR_INVALID_ARG;
+    if (vocab > spec_accept_tree_max_vocab()) return SVPA_ERR_UNSUPPORTED;  // one cluster per row
+    if (batch > 0x7fffffff / 8) return SVPA_ERR_UNSUPPORTED;
+    if (batch == 0) return SVPA_OK;
+    if (!target_logits || !draft_logits || !node_tokens || !u_accept || !u_sample || !accepted_len ||
+        !path_nodes || !out_tokens || !error_flag)
+        return SVPA_ERR_INVALID_ARG;
+    a.p = target_logits;
+    a.q = draft_logits;
+    a.tokens = node_tokens;
+    a.u_acc = u_accept;
+    a.u_s = u_sample;
+    a.accepted_len = accepted_len;
+    a.path_nodes = path_nodes;
+    a.out_tokens = out_tokens;
+    a.near = near_boundary;
+    a.err = error_flag;
+    a.B = batch;
+    a.V = vocab;
+    a.c_target = ct;
+    a.c_draft = cd;
+    const cudaError_t e = launch_spec_accept_tree_logits(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SVPA_OK : SVPA_ERR_CUDA;
 }
 

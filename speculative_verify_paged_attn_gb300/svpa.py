@@ -29,7 +29,7 @@ EXPORTS = ("svpa_attn_workspace_size", "svpa_attn_kernel", "svpa_paged_verify_at
            "svpa_spec_accept", "svpa_spec_accept_tree", "svpa_block_table_commit", "svpa_check_error",
            "svpa_status_string", "svpa_version", "svpa_paged_verify_attn_noalloc", "svpa_kv_append",
            "svpa_gamma_update", "svpa_attn_launches", "svpa_spec_accept_logits",
-           "svpa_spec_accept_logits_workspace_size", "svpa_wait_selftest")
+           "svpa_spec_accept_logits_workspace_size", "svpa_wait_selftest", "svpa_spec_accept_tree_logits")
 
 
 class SvpaError(RuntimeError):
@@ -69,6 +69,7 @@ def load(path: str = LIB_PATH):
     L.svpa_spec_accept_tree.argtypes = [I, I, I] + [P] * 11 + [U, P, P]
     L.svpa_spec_accept_logits.argtypes = [I, I, I, ctypes.c_float, ctypes.c_float] + [P] * 9 + [U, P, P]
     L.svpa_spec_accept_logits_workspace_size.argtypes = [I, I, I, ctypes.POINTER(U)]
+    L.svpa_spec_accept_tree_logits.argtypes = [I, I, I, P, ctypes.c_float, ctypes.c_float] + [P] * 11
     L.svpa_block_table_commit.argtypes = [I] * 5 + [P] * 7 + [I, P, P, I, I, I, P, P]
     L.svpa_paged_verify_attn_noalloc.argtypes = [ctypes.POINTER(AttnParams)] + [P] * 12
     L.svpa_kv_append.argtypes = [I] * 9 + [P] * 13
@@ -228,6 +229,25 @@ def spec_accept_tree(parent: Sequence[int], p_probs, q_probs, node_tokens, u_acc
                                       _p(error_flag), _stream(stream))
     if check:
         _check(st, "svpa_spec_accept_tree")
+    return st
+
+
+def spec_accept_tree_logits(parent: Sequence[int], target_logits, draft_logits, node_tokens, u_accept, u_sample,
+                            accepted_len, path_nodes, out_tokens, *, error_flag, temperature=1.0,
+                            draft_temperature=None, near_boundary=None, stream=None, check=True) -> int:
+    """The draft-tree sampler on P = softmax(target_logits / T) at every node and
+    Q = softmax(draft_logits / T_draft) at every internal node; parent: host
+    sequence (parent[0] = -1)."""
+    par = [int(x) for x in (parent.tolist() if hasattr(parent, "tolist") else parent)]
+    arr = (ctypes.c_int32 * len(par))(*par)
+    B, n, V = target_logits.shape
+    td = temperature if draft_temperature is None else draft_temperature
+    st = load().svpa_spec_accept_tree_logits(B, n, V, ctypes.cast(arr, ctypes.c_void_p), float(temperature),
+                                             float(td), _p(target_logits), _p(draft_logits), _p(node_tokens),
+                                             _p(u_accept), _p(u_sample), _p(accepted_len), _p(path_nodes),
+                                             _p(out_tokens), _p(near_boundary), _p(error_flag), _stream(stream))
+    if check:
+        _check(st, "svpa_spec_accept_tree_logits")
     return st
 
 

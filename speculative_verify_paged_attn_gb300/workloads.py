@@ -370,6 +370,53 @@ def make_logits(wl: Workload, seed: int, device="cpu", batch: Optional[int] = No
 
 
 @dataclass
+class TreeLogitInputs:
+    lp: torch.Tensor         # fp32 [B, n_nodes, V] target logits at every node
+    lq: torch.Tensor         # fp32 [B, n_internal, V] draft logits of each internal node's children
+    tokens: torch.Tensor     # int32 [B, n_nodes] (entry 0 unused), drawn from the parent's draft softmax
+    u_accept: torch.Tensor   # fp32 [B, n_nodes]
+    u_sample: torch.Tensor   # fp32 [B]
+    parent: torch.Tensor     # int32 [n_nodes]
+    temperature: float
+    draft_temperature: float
+
+
+def make_tree_logits(wl: Workload, seed: int, device="cpu", batch: Optional[int] = None,
+                     vocab: Optional[int] = None, branching: Optional[tuple] = None, temperature: float = 1.0,
+                     draft_temperature: Optional[float] = None) -> TreeLogitInputs:
+    """Logits for the draft-tree sampler's front-end (the recipe of
+    make_sampler's tree, before the softmax): target N(0, s_t) at every node,
+    draft = the node's target logits + N(0, s_d) at every internal node; each
+    child's token drawn independently from softmax(parent's draft /
+    draft_temperature); uniforms U[0, 1)."""
+    B = batch if batch is not None else wl.batch
+    V = vocab if vocab is not None else wl.vocab
+    br = branching if branching is not None else wl.tree_branching
+    parent = tree_parents(br)
+    td = temperature if draft_temperature is None else draft_temperature
+    dev = torch.device(device)
+    g = _gen(seed + 151051, dev)
+    n = len(parent)
+    internal = [i for i in range(n) if i in set(parent[1:])]
+    row_of = {node: r for r, node in enumerate(internal)}
+    lp = torch.randn((B, n, V), generator=g, device=dev) * wl.sigma_target
+    lq = lp[:, internal, :] + torch.randn((B, len(internal), V), generator=g, device=dev) * wl.sigma_draft
+    tokens = torch.zeros((B, n), dtype=torch.int32, device=dev)
+    for r, node in enumerate(internal):
+        q = torch.softmax(lq[:, r, :].double() / td, dim=-1)
+        kids = [c for c in range(1, n) if parent[c] == node]
+        draws = torch.multinomial(q, len(kids), replacement=True, generator=g).to(torch.int32)
+        for i, c in enumerate(kids):
+            tokens[:, c] = draws[:, i]
+        del q
+    ua = torch.rand((B, n), generator=g, device=dev)
+    us = torch.rand((B,), generator=g, device=dev)
+    return TreeLogitInputs(lp=lp.contiguous(), lq=lq.contiguous(), tokens=tokens, u_accept=ua, u_sample=us,
+                           parent=torch.tensor(parent, dtype=torch.int32, device=dev),
+                           temperature=float(temperature), draft_temperature=float(td))
+
+
+@dataclass
 class AppendInputs:
     """The paged cache before an append and the rows to append (torch tensors)."""
     wl: Workload
