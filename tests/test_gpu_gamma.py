@@ -75,7 +75,11 @@ def test_gamma_update_reads_the_sampler_output_in_place():
     tel = torch.zeros(4, dtype=torch.float32, device=DEV)
     svpa.gamma_update(wl.gamma, k, bs, bg, tel, error_flag=err, seq_state=ss, seq_gamma=sg, draft_cost_ratio=0.08)
     assert svpa.check_error(err) == 0
-    ref = oracle.gamma_update(wl.gamma, k.cpu().numpy(), seq_state=np.zeros((B, 2), np.float32), r=0.08)
+    # the oracle's own sampler on the same rows gives the accepted lengths
+    # (the kernel's are the same: its acceptance tests are bit-exact)
+    ko, _, _, _ = oracle.spec_accept(s.p.cpu(), s.q.cpu(), s.tokens.cpu(), s.u_accept.cpu(), s.u_sample.cpu())
+    assert np.array_equal(k.cpu().numpy(), ko)
+    ref = oracle.gamma_update(wl.gamma, ko, seq_state=np.zeros((B, 2), np.float32), r=0.08)
     assert np.array_equal(sg.cpu().numpy(), ref["seq_gamma"])
     assert np.array_equal(tel.cpu().numpy(), ref["telemetry"])
 

@@ -8,7 +8,8 @@ checked:
     the band;
   * the tokens before k are the drafts, those after it -1;
   * its drawn token lies in the oracle's draw window at the kernel's own k
-    (the tokens whose running-sum interval, widened by the band, holds u*Z);
+    (the tokens whose running-sum interval, widened by the band, holds u*Z;
+    the oracle computes the window at every k from the inputs alone);
   * where neither side flags a near decision, k and the tokens are the
     oracle's exactly.
 Plus the output distribution (chi-square at V = 8) and the edge cases: V = 1,
@@ -74,7 +75,12 @@ def check_against_oracle(li, offset=0, min_same_k=0.98):
     assert np.array_equal(np.where(pos < kg[:, None], np.pad(x, ((0, 0), (0, 1))), 0)[pos < kg[:, None]],
                           tg[pos < kg[:, None]])
     assert np.all(tg[pos > kg[:, None]] == -1)
-    lo, hi = oracle.logits_draw_window(li.lp, li.lq, kg, li.u_sample, temperature=T, draft_temperature=Td)
+    # the draw windows at every possible accepted count, from the inputs alone;
+    # the row's own count picks one
+    win = [oracle.logits_draw_window(li.lp, li.lq, np.full(B, kk, np.int32), li.u_sample, temperature=T,
+                                     draft_temperature=Td) for kk in range(g + 1)]
+    lo = np.stack([w[0] for w in win], 1)[np.arange(B), kg]
+    hi = np.stack([w[1] for w in win], 1)[np.arange(B), kg]
     drawn = tg[np.arange(B), kg]
     assert np.all((lo <= drawn) & (drawn <= hi)), np.nonzero(~((lo <= drawn) & (drawn <= hi)))
     ok = ~(ng | no)
