@@ -258,7 +258,7 @@ svpa_status svpa_spec_accept(int32_t batch, int32_t gamma, int32_t vocab,
  *               that, so most draws are flagged.
  *  workspace    16-byte aligned device buffer of at least
  *               svpa_spec_accept_logits_workspace_size() bytes: the (max,
- *               sum) pair of every 4096-token slab of every row, written by
+ *               sum) pair of every 8192-token slab of every row, written by
  *               the first kernel and read by the second
  *  gamma 1..32; 1 <= V <= 262144, else SVPA_ERR_UNSUPPORTED.
  * Two kernels on `stream`: the slab statistics (one CTA per slab of a row),

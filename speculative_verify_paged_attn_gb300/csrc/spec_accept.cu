@@ -227,6 +227,16 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
+// The cluster's start-up barrier, split: every CTA arrives on entry and waits
+// before its first store into a peer's shared memory, by which time every
+// CTA of the cluster has started (the wait is normally long satisfied).
+__device__ __forceinline__ void cluster_arrive_on_entry() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_started() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
 // This CTA's slice of a row, fetched into L2 by the bulk-copy engine: one
 // request for the whole slice, so the loads that follow find their lines in
 // flight instead of each warp's misses queueing in L1.  Rows that are not
@@ -243,16 +253,17 @@ __device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
     return remote;
 }
 
-// The word at the same shared-memory offset as `p` in the CTA of cluster rank `rank`.
-__device__ __forceinline__ double ld_peer_f64(const double *p, uint32_t rank) {
-    double v;
-    asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(peer_addr(p, rank)) : "memory");
-    return v;
+// Stores into the word at the same shared-memory offset as `p` in the CTA of
+// cluster rank `rank`.  The exchanges push every CTA's values into every
+// peer before a cluster barrier (release / acquire), so that after the
+// barrier each CTA reads them from its own shared memory, and no CTA touches
+// a peer's shared memory after the cluster's last barrier (a CTA may then
+// exit without waiting for its peers).
+__device__ __forceinline__ void st_peer_f64(double *p, uint32_t rank, double v) {
+    asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(peer_addr(p, rank)), "d"(v) : "memory");
 }
-__device__ __forceinline__ float ld_peer_f32(const float *p, uint32_t rank) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(peer_addr(p, rank)) : "memory");
-    return v;
+__device__ __forceinline__ void st_peer_f32(float *p, uint32_t rank, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(peer_addr(p, rank)), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ float lane_sum(float4 w) { return ((w.x + w.y) + w.z) + w.w; }
@@ -349,16 +360,27 @@ struct SrcUpdate {
 // Per-CTA state of the cluster-wide sums and draw of one row.
 template <int NI>
 struct ClusterRow {
-    float g[kClWarps][NI];    // per-step sums (fp32)
-    float wsum[kClWarps];     // per-warp sums (fp32, steps in order)
-    double wincl[kClWarps];   // inclusive fp64 prefix of the warp sums
-    double total[2];          // this CTA's slice total, by exchange parity (read by peers)
-    float probe[2];           // R at a probed token, by exchange parity (read by peers)
-    double peer[kClMaxCtas];  // every CTA's slice total, rank order
+    float g[kClWarps][NI];        // per-step sums (fp32)
+    float wsum[kClWarps];         // per-warp sums (fp32, steps in order)
+    double wincl[kClWarps];       // inclusive fp64 prefix of the warp sums
+    double total;                 // this CTA's slice total
+    double peer[2][kClMaxCtas];   // every CTA's slice total by exchange parity, pushed by each CTA
+    double pincl[kClMaxCtas];     // inclusive prefix of the last exchange's totals (rank order)
+    float probe[2];               // R at a probed token by exchange parity, pushed by its owner
     double S, r;
     float probe_val;
-    int cta, mode, warp, tok, near, slot;
+    int cta, mode, warp, tok, near, slot, last;
 };
+
+// The weights a thread loaded for its NI steps in cluster_sum, kept in
+// registers for cluster_draw when the row is short enough (KEEP); the draw
+// then scans its step from these instead of loading it again.
+template <int NI, bool KEEP>
+struct Kept {
+    float4 v[KEEP ? NI : 1];
+};
+template <int NI>
+constexpr bool kKeepWeights = NI <= 4;
 
 struct ClusterGeom {
     int rank, n_ctas, cta_lo, cta_hi, wbase;
@@ -368,9 +390,9 @@ struct ClusterGeom {
 // double in every CTA).  When probe >= 0 the CTA owning token `probe` also
 // publishes R[probe] from `R` (after the sums), readable as st.probe_val.
 // Every thread of every CTA of the cluster calls this, with the same parity.
-template <int NI, class Src>
-__device__ double cluster_sum(ClusterRow<NI> &st, const Src &src, const ClusterGeom &g, int parity,
-                              int probe = -1, const float *R = nullptr) {
+template <int NI, class Src, bool KEEP = false>
+__device__ __forceinline__ double cluster_sum(ClusterRow<NI> &st, const Src &src, const ClusterGeom &g,
+                                              int parity, int probe, const float *R, Kept<NI, KEEP> &keep) {
     constexpr int nb = NI < kLoadBatch ? NI : kLoadBatch;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float G = 0.f;
@@ -384,33 +406,59 @@ __device__ double cluster_sum(ClusterRow<NI> &st, const Src &src, const ClusterG
             const float s = __shfl_sync(0xffffffffu, warp_incl_scan(lane_sum(wv[j])), 31);
             if (lane == 0) st.g[warp][i0 + j] = s;
             G += s;
+            if constexpr (KEEP) keep.v[i0 + j] = wv[j];
         }
     }
     if (lane == 0) st.wsum[warp] = G;
     __syncthreads();
     const int owner = probe >= 0 ? probe / (kClWarps * NI * kStep) : -1;
-    if (threadIdx.x == 0) {
-        double acc = 0.0;
-        for (int w = 0; w < kClWarps; ++w) {
-            acc += (double)st.wsum[w];
-            st.wincl[w] = acc;
+    if (threadIdx.x < 32) {
+        // inclusive fp64 prefix of the warp sums (a 3-step scan over lanes
+        // 0..7); the CTA total is its last entry
+        double v = lane < kClWarps ? (double)st.wsum[lane] : 0.0;
+#pragma unroll
+        for (int o = 1; o < kClWarps; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
         }
-        st.total[parity] = acc;
-        if (owner == g.rank) st.probe[parity] = R[probe - g.cta_lo];
+        if (lane < kClWarps) st.wincl[lane] = v;
+        const double total = __shfl_sync(0xffffffffu, v, kClWarps - 1);
+        if (lane == 0) {
+            st.total = total;
+            st.last = parity;
+        }
+        // push this CTA's total (and the probed R value from its owner) into every CTA
+        if (lane < g.n_ctas) {
+            st_peer_f64(&st.peer[parity][g.rank], (uint32_t)lane, total);
+            if (owner == g.rank) st_peer_f32(&st.probe[parity], (uint32_t)lane, R[probe - g.cta_lo]);
+        }
     }
     cluster_sync_all();
     if (threadIdx.x < 32) {
-        if (lane < g.n_ctas) st.peer[lane] = ld_peer_f64(&st.total[parity], (uint32_t)lane);
-        if (lane == 0 && owner >= 0) st.probe_val = ld_peer_f32(&st.probe[parity], (uint32_t)owner);
-        __syncwarp();
+        // the totals in rank order, by the same scan in every CTA: the row
+        // total S is the last entry of the prefix
+        double v = lane < g.n_ctas ? st.peer[parity][lane] : 0.0;
+#pragma unroll
+        for (int o = 1; o < kClMaxCtas; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        if (lane < kClMaxCtas) st.pincl[lane] = v;
+        const double S = __shfl_sync(0xffffffffu, v, kClMaxCtas - 1);
         if (lane == 0) {
-            double S = 0.0;
-            for (int c = 0; c < g.n_ctas; ++c) S += st.peer[c];
             st.S = S;
+            if (owner >= 0) st.probe_val = st.probe[parity];
         }
     }
     __syncthreads();
     return st.S;
+}
+
+template <int NI, class Src>
+__device__ __forceinline__ double cluster_sum(ClusterRow<NI> &st, const Src &src, const ClusterGeom &g,
+                                              int parity, int probe = -1, const float *R = nullptr) {
+    Kept<NI, false> none;
+    return cluster_sum<NI, Src, false>(st, src, g, parity, probe, R, none);
 }
 
 // Last token in [lo, hi) with positive weight, or -1 (the whole CTA calls it).
@@ -431,36 +479,33 @@ __device__ int cta_last_positive(const Src &src, int lo, int hi, int *s_slot) {
 // draw (tok, near set there); tok = -1 there when the row has no mass (then
 // it is CTA 0).  near: u*S within 1e-6 * S of a running sum, or within
 // band_abs when that is given.  Every thread of every CTA calls this.
-template <int NI, class Src>
+template <int NI, class Src, bool KEEP = false>
 __device__ bool cluster_draw(ClusterRow<NI> &st, const Src &src, const ClusterGeom &g, float u, int *tok_out,
-                             bool *near_out, double band_abs = -1.0) {
+                             bool *near_out, double band_abs, const Kept<NI, KEEP> &keep) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // which CTA holds u*S: the first whose running total exceeds it
-    if (threadIdx.x == 0) {
+    // which CTA holds u*S: the first whose running total exceeds it (warp 0,
+    // all ranks compared at once)
+    if (threadIdx.x < 32) {
         const double S = st.S, target = (double)u * S;
         int mode = kDrawNoMass, cta = 0;
         double before = 0.0;
         if (S > 0.0) {
-            mode = kDrawPastEnd;
-            cta = -1;
-            double e = 0.0;
-            for (int c = 0; c < g.n_ctas; ++c) {
-                const double en = e + st.peer[c];
-                if (en > target) {
-                    cta = c;
-                    before = e;
-                    mode = kDrawFound;
-                    break;
-                }
-                e = en;
+            const unsigned hit = __ballot_sync(0xffffffffu, lane < g.n_ctas && st.pincl[lane] > target);
+            if (hit) {
+                cta = __ffs(hit) - 1;
+                before = cta > 0 ? st.pincl[cta - 1] : 0.0;
+                mode = kDrawFound;
+            } else {  // u*S at or past S (rounding): the last CTA with mass
+                const unsigned pos = __ballot_sync(0xffffffffu, lane < g.n_ctas && st.peer[st.last][lane] > 0.0);
+                cta = pos ? 31 - __clz(pos) : -1;
+                mode = kDrawPastEnd;
             }
-            if (mode == kDrawPastEnd)  // u*S at or past S (rounding): the last token with mass
-                for (int c = g.n_ctas - 1; c >= 0 && cta < 0; --c)
-                    if (st.peer[c] > 0.0) cta = c;
         }
-        st.mode = mode;
-        st.cta = cta;
-        st.r = target - before;
+        if (lane == 0) {
+            st.mode = mode;
+            st.cta = cta;
+            st.r = target - before;
+        }
     }
     __syncthreads();
     const int mode = st.mode;
@@ -473,41 +518,49 @@ __device__ bool cluster_draw(ClusterRow<NI> &st, const Src &src, const ClusterGe
     int tok;
     bool near = true;
     if (mode == kDrawFound) {
-        // warp, then 128-token step, then lane, then token
-        if (threadIdx.x == 0) {
+        // warp (all eight compared at once), then 128-token step, then lane,
+        // then token
+        if (threadIdx.x < 32) {
             const double r1 = st.r;
-            double before = 0.0;
-            int ws = -1;
-            for (int w = 0; w < kClWarps; ++w) {
-                if (st.wincl[w] > r1) {
-                    ws = w;
-                    break;
-                }
-                before = st.wincl[w];
+            const unsigned hit = __ballot_sync(0xffffffffu, lane < kClWarps && st.wincl[lane] > r1);
+            const int ws = hit ? __ffs(hit) - 1 : -1;
+            if (lane == 0) {
+                st.warp = ws;
+                st.r = r1 - (ws > 0 ? st.wincl[ws - 1] : 0.0);
+                st.tok = -2;
+                st.near = 1;
             }
-            st.warp = ws;
-            st.r = r1 - before;
-            st.tok = -2;
-            st.near = 1;
         }
         __syncthreads();
         const int ws = st.warp;
         const int wlo = g.cta_lo + (ws < 0 ? 0 : ws) * NI * kStep;
         if (warp == ws) {
+            // the running fp32 sums over the steps in cluster_sum's order, the
+            // comparisons independent of one another
             const double r2 = st.r;
-            float G = 0.f;
+            float G = 0.f, Gs = 0.f;
             int step = -1;
+#pragma unroll
             for (int i = 0; i < NI; ++i) {
                 const float Gn = G + st.g[ws][i];
-                if ((double)Gn > r2) {
+                if (step < 0 && (double)Gn > r2) {
                     step = i;
-                    break;
+                    Gs = G;
                 }
                 G = Gn;
             }
+            G = Gs;
             if (step >= 0) {
                 const int t0 = wlo + step * kStep + 4 * lane;
-                const float4 wv = src(t0);
+                float4 wv;
+                if constexpr (KEEP) {  // this lane loaded these weights in cluster_sum
+                    wv = keep.v[0];
+#pragma unroll
+                    for (int i = 1; i < NI; ++i)
+                        if (i == step) wv = keep.v[i];
+                } else {
+                    wv = src(t0);
+                }
                 const float incl = warp_incl_scan(lane_sum(wv));
                 float excl = __shfl_up_sync(0xffffffffu, incl, 1);
                 if (lane == 0) excl = 0.f;
@@ -553,6 +606,13 @@ __device__ bool cluster_draw(ClusterRow<NI> &st, const Src &src, const ClusterGe
     return true;
 }
 
+template <int NI, class Src>
+__device__ __forceinline__ bool cluster_draw(ClusterRow<NI> &st, const Src &src, const ClusterGeom &g, float u,
+                                             int *tok_out, bool *near_out, double band_abs = -1.0) {
+    const Kept<NI, false> none{};
+    return cluster_draw<NI, Src, false>(st, src, g, u, tok_out, near_out, band_abs, none);
+}
+
 template <int NI>
 __device__ __forceinline__ ClusterGeom cluster_geom(int V, int n_ctas) {
     ClusterGeom g;
@@ -575,6 +635,7 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     const int b = (int)(blockIdx.x / (unsigned)n_ctas);
     const int gamma = a.gamma, V = a.V;
     const int lane = threadIdx.x & 31;
+    cluster_arrive_on_entry();
 
     // acceptance tests: every CTA of the cluster makes the same loads and
     // reaches the same k
@@ -607,16 +668,18 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
         prefetch_slice(src.p, g.cta_lo, g.cta_hi, vec);
         prefetch_slice(src.q, g.cta_lo, g.cta_hi, vec);
     }
-    double S = cluster_sum(st, src, g, 0);
+    cluster_wait_started();
+    Kept<NI, kKeepWeights<NI>> keep;
+    double S = cluster_sum(st, src, g, 0, -1, nullptr, keep);
     if (!(S > 0.0) && src.q) {
         // empty residual: draw from the target row instead (S is the same in
         // every CTA, so the whole cluster takes this branch)
         src.q = nullptr;
-        S = cluster_sum(st, src, g, 1);
+        S = cluster_sum(st, src, g, 1, -1, nullptr, keep);
     }
     int tok;
     bool near;
-    if (cluster_draw(st, src, g, s_u, &tok, &near) && threadIdx.x == 0) {
+    if (cluster_draw(st, src, g, s_u, &tok, &near, -1.0, keep) && threadIdx.x == 0) {
         if (tok < 0) {  // a row with no mass
             raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
             tok = 0;
@@ -630,8 +693,8 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
             a.out_tokens[(size_t)b * (gamma + 1) + i] = i < k ? a.tokens[(size_t)b * gamma + i] : -1;
         if (i == 0) a.accepted_len[b] = k;
     }
-    // no CTA leaves while a peer may still read its shared memory
-    cluster_sync_all();
+    // no peer touches this CTA's shared memory after the last exchange: no
+    // closing cluster barrier
 }
 
 // ---------------------------------------------------------------- tree, cluster per row
@@ -659,6 +722,7 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.p) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
     const bool lead = g.rank == 0 && threadIdx.x == 0;
+    cluster_arrive_on_entry();
     // the row's node tokens and uniforms, and per child of the node being
     // visited Q(x_c) and P(x_c) (each node is some node's child at most once,
     // so no entry is rewritten)
@@ -675,6 +739,7 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     }
     const float u_s = __ldg(a.u_s + b);
     __syncthreads();
+    cluster_wait_started();
     int node = 0, depth = 0, parity = 0;
     bool near = false;
     int tok = -1;
@@ -688,10 +753,11 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
         }
         if (qr < 0) {  // leaf: bonus token from its own P
             const SrcGlobal src{Pn, nullptr, V, vec};
-            cluster_sum(st, src, g, parity);
+            Kept<NI, kKeepWeights<NI>> keep;
+            cluster_sum(st, src, g, parity, -1, nullptr, keep);
             parity ^= 1;
             bool nb = false;
-            drew = cluster_draw(st, src, g, u_s, &tok, &nb);
+            drew = cluster_draw(st, src, g, u_s, &tok, &nb, -1.0, keep);
             near |= nb;
             break;
         }
@@ -748,9 +814,10 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
             drew = cluster_draw(st, SrcSmem{R, g.cta_lo}, g, u_s, &tok, &nb);
         } else {  // empty residual: draw from the node's target row
             const SrcGlobal src{Pn, nullptr, V, vec};
-            cluster_sum(st, src, g, parity);
+            Kept<NI, kKeepWeights<NI>> keep;
+            cluster_sum(st, src, g, parity, -1, nullptr, keep);
             parity ^= 1;
-            drew = cluster_draw(st, src, g, u_s, &tok, &nb);
+            drew = cluster_draw(st, src, g, u_s, &tok, &nb, -1.0, keep);
         }
         near |= nb;
         break;
@@ -773,7 +840,7 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
         }
         a.accepted_len[b] = depth;
     }
-    cluster_sync_all();
+    // no peer touches this CTA's shared memory after the last exchange
 }
 
 // ---------------------------------------------------------------- logits front-end
@@ -784,15 +851,17 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
 // (target logits checked against draft logits).
 //
 // Two kernels.  logit_stats_kernel reads every logit once, one CTA per
-// 4096-token slab of a row (thousands of independent CTAs, so the read runs
+// 8192-token slab of a row (thousands of independent CTAs, so the read runs
 // at memory speed whatever the batch), and writes the slab's max m and sum s
 // of 2^((l - m) c), c = log2(e) / T.  The sampler kernel, launched as its
-// programmatic dependent, is the linear sampler's cluster kernel: each CTA
-// merges every row's slab pairs in a fixed order (a warp butterfly, fp64
-// sums), so all CTAs of a cluster hold the same maxima and normalisers; the
-// acceptance tests use P(x) = 2^((l_x - m) c) / S in fp64 (cross-multiplied,
-// no division), and the residual row k is read again (from L2) with its
-// weights formed in fp32 for the cluster sum and draw.
+// programmatic dependent, is the linear sampler's cluster kernel: it loads
+// the draft tokens, their logits and the uniforms while the statistics grid
+// runs, then each CTA merges every row's slab pairs in a fixed order (a
+// half-warp butterfly per row, fp64 sums), so all CTAs of a cluster hold the
+// same maxima and normalisers; the acceptance tests use P(x) = 2^((l_x - m)
+// c) / S in fp64 (cross-multiplied, no division), and the residual row k is
+// read again (from L2) with its weights formed in fp32 for the cluster sum
+// and draw.
 //
 // fp32 formation errs by ~1.2e-7 * |log2 P| relative per probability (the
 // exponent's rounding; <= 1.3e-5 down to 2^-100) plus <= ~1e-5 in the
@@ -802,8 +871,8 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
 // 2^-100), a residual with mass below 5e-5, a draw within 5e-5 (absolute) of a
 // running sum.
 constexpr int kMaxLogitRows = 2 * 32 + 1;
-constexpr int kSlab = 4096;                          // tokens per statistics CTA
-constexpr int kMaxSlabs = kClMaxVocab / kSlab;       // 64
+constexpr int kSlab = 8192;                          // tokens per statistics CTA
+constexpr int kMaxSlabs = kClMaxVocab / kSlab;       // 32
 constexpr double kLogitBand = 5e-5;
 constexpr double kLogitTiny = 7.888609052210118e-31;  // 2^-100
 
@@ -856,6 +925,8 @@ __device__ __forceinline__ const float *logit_row(const LogitsArgs &a, int b, in
 }
 
 // One CTA per (sequence, row, slab): the slab's (max, sum) into a.stats.
+// Each thread loads its 32 logits (eight float4, all in flight together) and
+// reduces them as two groups of sixteen.
 __global__ void __launch_bounds__(kClThreads) logit_stats_kernel(const __grid_constant__ LogitsArgs a) {
     // the sampler may be scheduled now; it waits for this grid before reading
     asm volatile("griddepcontrol.launch_dependents;");
@@ -869,15 +940,20 @@ __global__ void __launch_bounds__(kClThreads) logit_stats_kernel(const __grid_co
     const bool vec = (a.V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.lp) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(a.lq) & 15) == 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float4 w[4];
+    float4 w[2][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) w[i] = load_logits4(row, slab * kSlab + 4 * ((int)threadIdx.x + i * kClThreads), a.V, vec);
-    float m, s;
-    group_stats16(w, c, m, s);
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[h][i] = load_logits4(row, slab * kSlab + 4 * ((int)threadIdx.x + (4 * h + i) * kClThreads), a.V, vec);
+    float m, s, m2, s2;
+    group_stats16(w[0], c, m, s);
+    group_stats16(w[1], c, m2, s2);
+    online_merge(m, s, m2, s2, c);
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        s2 = __shfl_xor_sync(0xffffffffu, s, o);
         online_merge(m, s, m2, s2, c);
     }
     if (lane == 0) {
@@ -932,29 +1008,50 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.lp) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(a.lq) & 15) == 0;
+    cluster_arrive_on_entry();
+    // the inputs the statistics grid does not write (draft tokens, their two
+    // logits, the uniforms) are loaded while that grid still runs
+    float lpx = 0.f, lqx = 0.f, ua = 0.f;
+    if (threadIdx.x < 32 && lane < gamma) {
+        int x = a.tokens[(size_t)b * gamma + lane];
+        if (x < 0 || x >= V) {
+            if (g.rank == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+            x = 0;
+        }
+        lpx = __ldg(logit_row(a, b, lane) + x);
+        lqx = __ldg(logit_row(a, b, gamma + 1 + lane) + x);
+        ua = __ldg(a.u_acc + (size_t)b * gamma + lane);
+    }
+    if (threadIdx.x == 32) s_u = __ldg(a.u_s + b);
     // the slab statistics are complete once the statistics grid is
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // ---- row maxima and normalisers: warp w merges rows w, w + 8, ...; lane l
-    // holds slabs l and l + 32; max by butterfly, then the rescaled sums in
-    // fp64 by butterfly (lane 0's order is the same in every CTA)
+    // ---- row maxima and normalisers: half-warp h of the CTA merges rows h,
+    // h + 16, ...; lane l of the half holds slabs l and l + 16; max by
+    // butterfly, then the rescaled sums in fp64 by butterfly (the same order
+    // in every CTA)
     const int nsl = a.n_slabs;
-    for (int r = warp; r < rows; r += kClWarps) {
+    const int hl = lane & 15;
+    // the loop is uniform over the warp (both halves run every iteration and
+    // every shuffle; a half past the last row works on an empty row)
+    for (int r0 = 2 * warp; r0 < rows; r0 += 2 * kClWarps) {
+        const int r = r0 + (lane >> 4);
+        const bool row_ok = r < rows;
         const float c = r <= gamma ? a.c_target : a.c_draft;
         const float2 *ps = a.stats + ((size_t)b * rows + r) * nsl;
-        const float2 p0 = lane < nsl ? ps[lane] : make_float2(-CUDART_INF_F, 0.f);
-        const float2 p1 = lane + 32 < nsl ? ps[lane + 32] : make_float2(-CUDART_INF_F, 0.f);
+        const float2 p0 = row_ok && hl < nsl ? ps[hl] : make_float2(-CUDART_INF_F, 0.f);
+        const float2 p1 = row_ok && hl + 16 < nsl ? ps[hl + 16] : make_float2(-CUDART_INF_F, 0.f);
         float m = fmaxf(p0.x, p1.x);
 #pragma unroll
-        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        for (int o = 8; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         double S = 0.0;
         if (m > -CUDART_INF_F) {
             if (p0.x > -CUDART_INF_F) S += (double)p0.y * (double)ex2_approx((p0.x - m) * c);
             if (p1.x > -CUDART_INF_F) S += (double)p1.y * (double)ex2_approx((p1.x - m) * c);
         }
 #pragma unroll
-        for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-        if (lane == 0) {
+        for (int o = 8; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+        if (row_ok && hl == 0) {
             s_m[r] = m;
             s_S[r] = S;
             s_inv[r] = (float)(1.0 / S);
@@ -970,18 +1067,13 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     if (threadIdx.x < 32) {
         bool rejected = false, close = false;
         if (lane < gamma) {
-            int x = a.tokens[(size_t)b * gamma + lane];
-            if (x < 0 || x >= V) {
-                if (g.rank == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
-                x = 0;
-            }
             const int rq = gamma + 1 + lane;
-            const float ep = ex2_approx((__ldg(logit_row(a, b, lane) + x) - s_m[lane]) * a.c_target);
-            const float eq = ex2_approx((__ldg(logit_row(a, b, rq) + x) - s_m[rq]) * a.c_draft);
+            const float ep = ex2_approx((lpx - s_m[lane]) * a.c_target);
+            const float eq = ex2_approx((lqx - s_m[rq]) * a.c_draft);
             // u Q <= P with both sides multiplied by Sp Sq > 0 (no fp64 division)
             const double sp = s_S[lane], sq = s_S[rq];
             const double P = (double)ep * sq;
-            const double uq = (double)__ldg(a.u_acc + (size_t)b * gamma + lane) * (double)eq * sp;
+            const double uq = (double)ua * (double)eq * sp;
             const double hi = fmax(P, uq);
             rejected = !(uq <= P);
             close = fabs(uq - P) <= kLogitBand * hi || hi < kLogitTiny * (sp * sq);
@@ -993,7 +1085,6 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
             const unsigned ran = k >= 31 ? 0xffffffffu : (2u << k) - 1u;  // tests 0..k
             s_k = k;
             s_near = (cl & ran) ? 1 : 0;
-            s_u = __ldg(a.u_s + b);
         }
     }
     __syncthreads();
@@ -1012,17 +1103,19 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     src.cq = a.c_draft;
     src.iq = k < gamma ? s_inv[gamma + 1 + k] : 0.f;
     bool near = s_near != 0;
-    double S = cluster_sum(st, src, g, 0);
+    cluster_wait_started();
+    Kept<NI, kKeepWeights<NI>> keep;
+    double S = cluster_sum(st, src, g, 0, -1, nullptr, keep);
     if (src.q) {
         if (S < kLogitBand) near = true;
         if (!(S > 0.0)) {  // empty residual: draw from the target row (S is the same in every CTA)
             src.q = nullptr;
-            S = cluster_sum(st, src, g, 1);
+            S = cluster_sum(st, src, g, 1, -1, nullptr, keep);
         }
     }
     int tok;
     bool nd;
-    if (cluster_draw(st, src, g, s_u, &tok, &nd, kLogitBand) && threadIdx.x == 0) {
+    if (cluster_draw(st, src, g, s_u, &tok, &nd, kLogitBand, keep) && threadIdx.x == 0) {
         if (tok < 0) {  // a row with no mass
             raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
             tok = 0;
@@ -1036,8 +1129,7 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
             a.out_tokens[(size_t)b * (gamma + 1) + i] = i < k ? a.tokens[(size_t)b * gamma + i] : -1;
         if (i == 0) a.accepted_len[b] = k;
     }
-    // no CTA leaves while a peer may still read its shared memory
-    cluster_sync_all();
+    // no peer touches this CTA's shared memory after the last exchange
 }
 
 // ---------------------------------------------------------------- tree, fed by logits
@@ -1096,7 +1188,7 @@ struct SrcUpdateLogits {
 // Softmax statistics of a node's two rows (0: target, 1: draft), as every CTA
 // of the cluster holds them after cluster_row_stats.
 struct TreeRowStats {
-    float2 mine[2][2];  // this CTA's (max, sum) by exchange parity and row (read by peers)
+    float2 peer[2][2][kClMaxCtas];  // every CTA's (max, sum) by exchange parity and row, pushed by each CTA
     float2 w[2][kClWarps];
     float m[2];
     double S[2];
@@ -1144,23 +1236,28 @@ __device__ void cluster_row_stats(TreeRowStats &ts, const float *p, const float 
     warp_row_stats<NI>(p, cp, g, V, vec, ts.w[0]);
     if (q) warp_row_stats<NI>(q, cq, g, V, vec, ts.w[1]);
     __syncthreads();
-    if (threadIdx.x < 2) {
-        const int r = threadIdx.x;
-        const float c = r == 0 ? cp : cq;
+    if (threadIdx.x < 32) {
+        // lane r < 2 merges the warps' pairs of row r, in warp order
         float m = -CUDART_INF_F, s = 0.f;
-        if (r == 0 || q)
-            for (int w = 0; w < kClWarps; ++w) online_merge(m, s, ts.w[r][w].x, ts.w[r][w].y, c);
-        ts.mine[parity][r] = make_float2(m, s);
+        if (lane < 2 && (lane == 0 || q)) {
+            const float c = lane == 0 ? cp : cq;
+            for (int w = 0; w < kClWarps; ++w) online_merge(m, s, ts.w[lane][w].x, ts.w[lane][w].y, c);
+        }
+        // push both rows' pairs into every CTA (lane t: peer t)
+        const float m0 = __shfl_sync(0xffffffffu, m, 0), s0 = __shfl_sync(0xffffffffu, s, 0);
+        const float m1 = __shfl_sync(0xffffffffu, m, 1), s1 = __shfl_sync(0xffffffffu, s, 1);
+        if (lane < g.n_ctas) {
+            st_peer_f32(&ts.peer[parity][0][g.rank].x, (uint32_t)lane, m0);
+            st_peer_f32(&ts.peer[parity][0][g.rank].y, (uint32_t)lane, s0);
+            st_peer_f32(&ts.peer[parity][1][g.rank].x, (uint32_t)lane, m1);
+            st_peer_f32(&ts.peer[parity][1][g.rank].y, (uint32_t)lane, s1);
+        }
     }
     cluster_sync_all();
     if (threadIdx.x < 32) {
         for (int r = 0; r < (q ? 2 : 1); ++r) {
             const float c = r == 0 ? cp : cq;
-            float2 v = make_float2(-CUDART_INF_F, 0.f);
-            if (lane < g.n_ctas) {
-                v.x = ld_peer_f32(&ts.mine[parity][r].x, (uint32_t)lane);
-                v.y = ld_peer_f32(&ts.mine[parity][r].y, (uint32_t)lane);
-            }
+            const float2 v = lane < g.n_ctas ? ts.peer[parity][r][lane] : make_float2(-CUDART_INF_F, 0.f);
             float m = v.x;
 #pragma unroll
             for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -1193,6 +1290,7 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.p) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
     const bool lead = g.rank == 0 && threadIdx.x == 0;
+    cluster_arrive_on_entry();
     // node tokens and uniforms; per child of the node being visited the
     // exponentials 2^((l_x - max) c) of its token in the node's two rows
     __shared__ int s_x[kMaxNq];
@@ -1209,6 +1307,7 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     if (threadIdx.x == 0) ts.bad = 0;
     const float u_s = __ldg(a.u_s + b);
     __syncthreads();
+    cluster_wait_started();
     int node = 0, depth = 0, parity = 0;
     bool near = false, drew = false;
     int tok = -1;
@@ -1234,10 +1333,11 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
         srcp.cq = a.c_draft;
         srcp.iq = 0.f;
         if (qr < 0) {  // leaf: bonus token from its own P
-            cluster_sum(st, srcp, g, parity);
+            Kept<NI, kKeepWeights<NI>> keep;
+            cluster_sum(st, srcp, g, parity, -1, nullptr, keep);
             parity ^= 1;
             bool nb = false;
-            drew = cluster_draw(st, srcp, g, u_s, &tok, &nb, kLogitBand);
+            drew = cluster_draw(st, srcp, g, u_s, &tok, &nb, kLogitBand, keep);
             near |= nb;
             break;
         }
@@ -1315,9 +1415,10 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
         if (Z > 0.0) {
             drew = cluster_draw(st, SrcSmem{R, g.cta_lo}, g, u_s, &tok, &nb, s);
         } else {  // empty residual: draw from the node's target row
-            cluster_sum(st, srcp, g, parity);
+            Kept<NI, kKeepWeights<NI>> keep;
+            cluster_sum(st, srcp, g, parity, -1, nullptr, keep);
             parity ^= 1;
-            drew = cluster_draw(st, srcp, g, u_s, &tok, &nb, kLogitBand);
+            drew = cluster_draw(st, srcp, g, u_s, &tok, &nb, kLogitBand, keep);
         }
         near |= nb;
         break;
@@ -1341,7 +1442,7 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
         }
         a.accepted_len[b] = depth;
     }
-    cluster_sync_all();
+    // no peer touches this CTA's shared memory after the last exchange
 }
 
 int sm_count_cached() {

@@ -141,7 +141,7 @@ struct LogitsArgs {
     int32_t *err;
     int32_t B, gamma, V;
     float c_target, c_draft;  // log2(e) / temperature, > 0
-    float2 *stats;            // workspace: (max, sum) per 4096-token slab [B, 2 gamma + 1, n_slabs]
+    float2 *stats;            // workspace: (max, sum) per 8192-token slab [B, 2 gamma + 1, n_slabs]
     int32_t n_slabs;          // set by the launch
 };
 size_t spec_accept_logits_stats_bytes(int B, int gamma, int V);

@@ -31,7 +31,7 @@ extern "C" {
 svpa_status svpa_spec_accept_logits_workspace_size(int32_t batch, int32_t gamma, int32_t vocab, size_t *bytes) {
     if (!bytes || batch < 0 || gamma < 1 || gamma > 32 || vocab < 1) return SVPA_ERR_INVALID_ARG;
     if (vocab > spec_accept_tree_max_vocab()) return SVPA_ERR_UNSUPPORTED;
-    // the (max, sum) pair of every 4096-token slab of every row
+    // the (max, sum) pair of every 8192-token slab of every row
     const size_t need = spec_accept_logits_stats_bytes(batch, gamma, vocab);
     *bytes = need < 256 ? 256 : (need + 255) / 256 * 256;
     return SVPA_OK;
@@ -50,7 +50,7 @@ svpa_status svpa_spec_accept_logits(int32_t batch, int32_t gamma, int32_t vocab,
         return SVPA_ERR_INVALID_ARG;
     if (vocab > spec_accept_tree_max_vocab()) return SVPA_ERR_UNSUPPORTED;  // one cluster per row
     if (batch > 0x7fffffff / 8) return SVPA_ERR_UNSUPPORTED;
-    if ((long long)batch * (2 * gamma + 1) * ((vocab + 4095) / 4096) > 0x7fffffffLL) return SVPA_ERR_UNSUPPORTED;
+    if ((long long)batch * (2 * gamma + 1) * ((vocab + 8191) / 8192) > 0x7fffffffLL) return SVPA_ERR_UNSUPPORTED;
     if (batch == 0) return SVPA_OK;
     if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_sample || !accepted_len ||
         !out_tokens || !error_flag)

@@ -130,17 +130,17 @@ def test_null_pointers_rejected_before_launch(lib):
     assert lib.svpa_spec_accept_logits(2, 4, 1000, F(1.0), F(1.0), *([nz] * 8), None, 0, nz, None) == 6
     assert lib.svpa_spec_accept_logits(2, 4, 1000, F(1.0), F(1.0), *([nz] * 8), odd, 256, nz, None) == 6
     assert lib.svpa_spec_accept_logits(0, 4, 1000, F(0.7), F(1.0), *([None] * 9), 0, None, None) == 0
-    # its workspace: one (max, sum) pair per 4096-token slab of each of the 2 gamma + 1 rows
+    # its workspace: one (max, sum) pair per 8192-token slab of each of the 2 gamma + 1 rows
     n = ctypes.c_size_t(0)
     assert lib.svpa_spec_accept_logits_workspace_size(2, 4, 32000, ctypes.byref(n)) == 0
-    assert n.value == 1280  # 2 * 9 * 8 * 8 = 1152 bytes, in 256-byte units
+    assert n.value == 768  # 2 * 9 * 4 * 8 = 576 bytes, in 256-byte units
     assert lib.svpa_spec_accept_logits_workspace_size(64, 5, 128256, ctypes.byref(n)) == 0
-    assert n.value == 64 * 11 * 32 * 8
+    assert n.value == 64 * 11 * 16 * 8
     assert lib.svpa_spec_accept_logits_workspace_size(1, 1, 1, ctypes.byref(n)) == 0 and n.value == 256
     assert lib.svpa_spec_accept_logits_workspace_size(2, 0, 1000, ctypes.byref(n)) == 1
     assert lib.svpa_spec_accept_logits_workspace_size(2, 4, 262145, ctypes.byref(n)) == 2
     ws = ctypes.c_void_p(256)
-    assert lib.svpa_spec_accept_logits(2, 4, 32000, F(1.0), F(1.0), *([nz] * 8), ws, 1024, nz, None) == 6
+    assert lib.svpa_spec_accept_logits(2, 4, 32000, F(1.0), F(1.0), *([nz] * 8), ws, 512, nz, None) == 6
     # empty batch is a no-op
     p0 = svpa.attn_params(0, 5, 4, 4, 64, 8, 16, split_pages=4)
     assert lib.svpa_paged_verify_attn(ctypes.byref(p0), *([None] * 11), 0, None, None) == 0
@@ -151,6 +151,25 @@ def test_tree_topology_validated(lib):
     st = lib.svpa_spec_accept_tree(1, 3, 10, ctypes.cast(par, ctypes.c_void_p), *([None] * 10),
                                    0, None, None)
     assert st == 1
+
+
+def test_tree_logits_arguments_validated(lib):
+    F = ctypes.c_float
+    nz = ctypes.c_void_p(16)
+    good = (ctypes.c_int32 * 3)(-1, 0, 0)
+    bad = (ctypes.c_int32 * 3)(-1, 1, 0)  # a parent after its child
+    g = ctypes.cast(good, ctypes.c_void_p)
+    assert lib.svpa_spec_accept_tree_logits(1, 3, 10, ctypes.cast(bad, ctypes.c_void_p), F(1.0), F(1.0),
+                                            *([nz] * 11)) == 1
+    assert lib.svpa_spec_accept_tree_logits(1, 3, 10, None, F(1.0), F(1.0), *([nz] * 11)) == 1
+    assert lib.svpa_spec_accept_tree_logits(1, 65, 10, g, F(1.0), F(1.0), *([nz] * 11)) == 1
+    for t, td in ((0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf")), (1e-39, 1.0)):
+        assert lib.svpa_spec_accept_tree_logits(1, 3, 10, g, F(t), F(td), *([nz] * 11)) == 1, (t, td)
+    assert lib.svpa_spec_accept_tree_logits(1, 3, 262145, g, F(1.0), F(1.0), *([nz] * 11)) == 2
+    assert lib.svpa_spec_accept_tree_logits(1, 3, 10, g, F(1.0), F(1.0), *([None] * 11)) == 1
+    # the error word is required
+    assert lib.svpa_spec_accept_tree_logits(1, 3, 10, g, F(1.0), F(1.0), *([nz] * 9), None, None) == 1
+    assert lib.svpa_spec_accept_tree_logits(0, 3, 10, g, F(1.0), F(1.0), *([None] * 11)) == 0
 
 
 def test_library_is_not_the_oracle(lib):
