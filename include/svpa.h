@@ -233,8 +233,8 @@ svpa_status svpa_spec_accept(int32_t batch, int32_t gamma, int32_t vocab,
  * The linear sampler fed by logits: P_i = softmax(target_logits_i / T) and
  * Q_i = softmax(draft_logits_i / T_draft) are formed inside the kernel and
  * never written out.  Q must be the distribution the drafts were drawn from.
- * Then the rule of svpa_spec_accept, with the acceptance test in fp64 on the
- * fp32 exponentials (accept iff u * Q(x) <= P(x)) and the residual
+ * Then the rule of svpa_spec_accept, with P(x) and Q(x) formed in fp32 as for
+ * the residual (accept iff fp32(u * Q(x)) <= P(x)) and the residual
  * max(0, P_k - Q_k) formed in fp32.
  *
  * Sources: "Speculative Decoding and KV-Cache Compression", section 2.3 (the
@@ -328,11 +328,11 @@ svpa_status svpa_spec_accept_tree(int32_t batch, int32_t n_nodes, int32_t vocab,
  * only: one target row per node on the accepted path and the draft row of
  * each internal node on it, read from memory once for the statistics and
  * again (from L2) for a residual update or draw; the rows of nodes off the
- * path are never read.  Every test is made in fp64 on fp32 exponentials:
- * child c, after j rejected siblings, is accepted iff
+ * path are never read.  Every test is made in fp32, P and Q formed as for
+ * the residual: child c, after j rejected siblings, is accepted iff
  * u_accept[c] * Q(x_c) * Z <= R(x_c), with R = P, Z = 1 for the first child
- * (there the test is cross-multiplied by both normalisers, as in
- * svpa_spec_accept_logits); the residual R <- max(0, R - Z Q) is fp32.
+ * (the products rounded in that order); the residual R <- max(0, R - Z Q) is
+ * fp32 and its mass Z is summed in fp64.
  *
  * Sources: "Speculative Decoding and KV-Cache Compression", section 2.3 (the
  * acceptance ratio takes softmax(logits)[x]); "The Sub-Millisecond

@@ -782,7 +782,8 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
             } else {
                 const double lhs = (double)u * (double)s_qx[c] * Z;
                 ok = lhs <= (double)rx;
-                if (Z > 0.0 && fabs(lhs - (double)rx) / Z < kNearBand) near = true;
+                // within 1e-6 of the threshold in normalised units (no fp64 division)
+                if (Z > 0.0 && fabs(lhs - (double)rx) < kNearBand * Z) near = true;
             }
             if (ok) {
                 accepted = c;
@@ -857,16 +858,18 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
 // programmatic dependent, is the linear sampler's cluster kernel: it loads
 // the draft tokens, their logits and the uniforms while the statistics grid
 // runs, then each CTA merges every row's slab pairs in a fixed order (a
-// half-warp butterfly per row, fp64 sums), so all CTAs of a cluster hold the
-// same maxima and normalisers; the acceptance tests use P(x) = 2^((l_x - m)
-// c) / S in fp64 (cross-multiplied, no division), and the residual row k is
-// read again (from L2) with its weights formed in fp32 for the cluster sum
-// and draw.
+// half-warp butterfly per row), so all CTAs of a cluster hold the same
+// maxima and normalisers; the acceptance tests use P(x) = 2^((l_x - m) c) /
+// S formed in fp32 exactly as the residual's weights, and the residual row k
+// is read again (from L2) with its weights formed in fp32 for the cluster
+// sum and draw.  The GB300 fp64 pipe has a 64-cycle dependent latency and a
+// ~1400-cycle division, so nothing on this latency chain but the cluster
+// sums is fp64.
 //
 // fp32 formation errs by ~1.2e-7 * |log2 P| relative per probability (the
 // exponent's rounding; <= 1.3e-5 down to 2^-100) plus <= ~1e-5 in the
 // normaliser (partial sums of 16 terms per thread, fp32 merges within a
-// slab, fp64 across slabs), so decisions within 5e-5 of their thresholds are
+// slab and across at most 32 slabs), so decisions within 5e-5 of their thresholds are
 // reported as near: a test with |u Q - P| <= 5e-5 * max(P, u Q) (or both below
 // 2^-100), a residual with mass below 5e-5, a draw within 5e-5 (absolute) of a
 // running sum.
@@ -875,6 +878,8 @@ constexpr int kSlab = 8192;                          // tokens per statistics CT
 constexpr int kMaxSlabs = kClMaxVocab / kSlab;       // 32
 constexpr double kLogitBand = 5e-5;
 constexpr double kLogitTiny = 7.888609052210118e-31;  // 2^-100
+constexpr float kLogitBandF = 5e-5f;
+constexpr float kLogitTinyF = 7.888609052210118e-31f;  // 2^-100, a normal fp32 value
 
 // Four logits of a row from token t0 (a multiple of 4); -inf past V.
 __device__ __forceinline__ float4 load_logits4(const float *row, int t0, int V, bool vec) {
@@ -999,7 +1004,6 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     spec_accept_logits_cluster_kernel(const __grid_constant__ LogitsArgs a, int n_ctas) {
     __shared__ ClusterRow<NI> st;
     __shared__ float s_m[kMaxLogitRows], s_inv[kMaxLogitRows];  // row max, 1 / row sum (fp32)
-    __shared__ double s_S[kMaxLogitRows];                       // row sum
     __shared__ int s_k, s_near;
     __shared__ float s_u;
     const ClusterGeom g = cluster_geom<NI>(a.V, n_ctas);
@@ -1028,8 +1032,8 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
 
     // ---- row maxima and normalisers: half-warp h of the CTA merges rows h,
     // h + 16, ...; lane l of the half holds slabs l and l + 16; max by
-    // butterfly, then the rescaled sums in fp64 by butterfly (the same order
-    // in every CTA)
+    // butterfly, then the rescaled sums by butterfly (fp32, the same order in
+    // every CTA; at most 32 terms, so the sum errs by < 2e-6 relative)
     const int nsl = a.n_slabs;
     const int hl = lane & 15;
     // the loop is uniform over the warp (both halves run every iteration and
@@ -1044,39 +1048,37 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
         float m = fmaxf(p0.x, p1.x);
 #pragma unroll
         for (int o = 8; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        double S = 0.0;
+        float S = 0.f;
         if (m > -CUDART_INF_F) {
-            if (p0.x > -CUDART_INF_F) S += (double)p0.y * (double)ex2_approx((p0.x - m) * c);
-            if (p1.x > -CUDART_INF_F) S += (double)p1.y * (double)ex2_approx((p1.x - m) * c);
+            if (p0.x > -CUDART_INF_F) S += p0.y * ex2_approx((p0.x - m) * c);
+            if (p1.x > -CUDART_INF_F) S += p1.y * ex2_approx((p1.x - m) * c);
         }
 #pragma unroll
         for (int o = 8; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
         if (row_ok && hl == 0) {
             s_m[r] = m;
-            s_S[r] = S;
-            s_inv[r] = (float)(1.0 / S);
+            s_inv[r] = __frcp_rn(S);
             // a row with no finite logit, or with NaN / +inf
-            if (!(S > 0.0) || !(S < CUDART_INF) || !(m > -CUDART_INF_F) || !(m < CUDART_INF_F))
+            if (!(S > 0.f) || !(S < CUDART_INF_F) || !(m > -CUDART_INF_F) || !(m < CUDART_INF_F))
                 if (g.rank == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
         }
     }
     __syncthreads();
 
-    // ---- acceptance tests (fp64 on the fp32 exponentials); every CTA makes
-    // the same loads on the same statistics and reaches the same k
+    // ---- acceptance tests (fp32: P and Q formed as for the residual, the
+    // product u Q rounded once; they err by ~1e-7 relative, far inside the
+    // band); every CTA makes the same loads on the same statistics and
+    // reaches the same k
     if (threadIdx.x < 32) {
         bool rejected = false, close = false;
         if (lane < gamma) {
             const int rq = gamma + 1 + lane;
-            const float ep = ex2_approx((lpx - s_m[lane]) * a.c_target);
-            const float eq = ex2_approx((lqx - s_m[rq]) * a.c_draft);
-            // u Q <= P with both sides multiplied by Sp Sq > 0 (no fp64 division)
-            const double sp = s_S[lane], sq = s_S[rq];
-            const double P = (double)ep * sq;
-            const double uq = (double)ua * (double)eq * sp;
-            const double hi = fmax(P, uq);
+            const float P = ex2_approx((lpx - s_m[lane]) * a.c_target) * s_inv[lane];
+            const float Q = ex2_approx((lqx - s_m[rq]) * a.c_draft) * s_inv[rq];
+            const float uq = __fmul_rn(ua, Q);
+            const float hi = fmaxf(P, uq);
             rejected = !(uq <= P);
-            close = fabs(uq - P) <= kLogitBand * hi || hi < kLogitTiny * (sp * sq);
+            close = fabsf(uq - P) <= kLogitBandF * hi || hi < kLogitTinyF;
         }
         const unsigned rej = __ballot_sync(0xffffffffu, rejected);
         const unsigned cl = __ballot_sync(0xffffffffu, close);
@@ -1141,11 +1143,10 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
 // visited rows only, by the cluster at each node: every CTA reduces its slice
 // of the node's target row and draft row to (max, sum of 2^((l - max) c)),
 // the pairs are exchanged through distributed shared memory and merged in
-// rank order (fp64 sums), so every CTA holds the same normalisers.  The first
-// child's test is fp64 on fp32 exponentials cross-multiplied by both
-// normalisers (as in the linear sampler fed by logits); a later child is
-// tested as u Q(x) Z <= R(x) with the fp32 residual R, formed from fp32
-// probabilities 2^((l - max) c) / S and probed at x by the CTA that owns x.
+// rank order (fp32), so every CTA holds the same normalisers.  The tests are
+// fp32 on probabilities formed as the residual's weights: the first child
+// u Q(x) <= P(x), a later child u Q(x) Z <= R(x) with the fp32 residual R
+// probed at x by the CTA that owns x.
 //
 // Near band after j rejected siblings: s_j = 2^(j+1) * 5e-5.  Each fp32
 // probability errs by at most ~2.5e-5 relative; carried through the
@@ -1191,8 +1192,7 @@ struct TreeRowStats {
     float2 peer[2][2][kClMaxCtas];  // every CTA's (max, sum) by exchange parity and row, pushed by each CTA
     float2 w[2][kClWarps];
     float m[2];
-    double S[2];
-    float inv[2];       // 1 / S rounded to fp32
+    float inv[2];       // 1 / S (fp32)
     int bad;
 };
 
@@ -1226,9 +1226,9 @@ __device__ __forceinline__ void warp_row_stats(const float *row, float c, const 
 
 // The softmax statistics of the target row p (scale cp) and, when q is not
 // null, the draft row q (scale cq) over the whole cluster.  Every thread of
-// every CTA calls this with the same parity; on return ts.m, ts.S, ts.inv
-// are the same in every CTA, and ts.bad is set for a row with no finite
-// logit, a NaN or +inf.
+// every CTA calls this with the same parity; on return ts.m and ts.inv are
+// the same in every CTA (the CTAs' pairs merged by the same fp32 butterfly),
+// and ts.bad is set for a row with no finite logit, a NaN or +inf.
 template <int NI>
 __device__ void cluster_row_stats(TreeRowStats &ts, const float *p, const float *q, float cp, float cq,
                                   const ClusterGeom &g, int V, bool vec, int parity) {
@@ -1255,22 +1255,21 @@ __device__ void cluster_row_stats(TreeRowStats &ts, const float *p, const float 
     }
     cluster_sync_all();
     if (threadIdx.x < 32) {
-        for (int r = 0; r < (q ? 2 : 1); ++r) {
-            const float c = r == 0 ? cp : cq;
-            const float2 v = lane < g.n_ctas ? ts.peer[parity][r][lane] : make_float2(-CUDART_INF_F, 0.f);
-            float m = v.x;
+        // half r of warp 0 merges row r: lane c of the half holds CTA c's pair
+        const int r = lane >> 4, c16 = lane & 15;
+        const bool have = c16 < g.n_ctas && (r == 0 || q);
+        const float c = r == 0 ? cp : cq;
+        const float2 v = have ? ts.peer[parity][r][c16] : make_float2(-CUDART_INF_F, 0.f);
+        float m = v.x;
 #pragma unroll
-            for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            double S = (m > -CUDART_INF_F && v.x > -CUDART_INF_F) ? (double)v.y * (double)ex2_approx((v.x - m) * c)
-                                                                   : 0.0;
+        for (int o = 8; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float S = (m > -CUDART_INF_F && v.x > -CUDART_INF_F) ? v.y * ex2_approx((v.x - m) * c) : 0.f;
 #pragma unroll
-            for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-            if (lane == 0) {
-                ts.m[r] = m;
-                ts.S[r] = S;
-                ts.inv[r] = (float)(1.0 / S);
-                if (!(S > 0.0) || !(S < CUDART_INF) || !(m > -CUDART_INF_F) || !(m < CUDART_INF_F)) ts.bad = 1;
-            }
+        for (int o = 8; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+        if (c16 == 0 && (r == 0 || q)) {
+            ts.m[r] = m;
+            ts.inv[r] = __frcp_rn(S);
+            if (!(S > 0.f) || !(S < CUDART_INF_F) || !(m > -CUDART_INF_F) || !(m < CUDART_INF_F)) ts.bad = 1;
         }
     }
     __syncthreads();
@@ -1291,10 +1290,10 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
                      (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
     const bool lead = g.rank == 0 && threadIdx.x == 0;
     cluster_arrive_on_entry();
-    // node tokens and uniforms; per child of the node being visited the
-    // exponentials 2^((l_x - max) c) of its token in the node's two rows
+    // node tokens and uniforms; per child of the node being visited P and Q
+    // of its token (fp32, formed as for the residual)
     __shared__ int s_x[kMaxNq];
-    __shared__ float s_ua[kMaxNq], s_ep[kMaxNq], s_eq[kMaxNq];
+    __shared__ float s_ua[kMaxNq], s_px[kMaxNq], s_qx[kMaxNq];
     if (threadIdx.x < (unsigned)n_nodes) {
         int x = ntok[threadIdx.x];
         if (x < 0 || x >= V) {
@@ -1344,32 +1343,26 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
         {
             const int c = node + 1 + (int)threadIdx.x;
             if (c < n_nodes && a.parent[c] == node) {
-                s_ep[c] = ex2_approx((__ldg(Pn + s_x[c]) - ts.m[0]) * a.c_target);
-                s_eq[c] = ex2_approx((__ldg(Qn + s_x[c]) - ts.m[1]) * a.c_draft);
+                s_px[c] = ex2_approx((__ldg(Pn + s_x[c]) - ts.m[0]) * a.c_target) * ts.inv[0];
+                s_qx[c] = ex2_approx((__ldg(Qn + s_x[c]) - ts.m[1]) * a.c_draft) * ts.inv[1];
             }
             __syncthreads();
         }
-        const double Sp = ts.S[0], Sq = ts.S[1];
+        // the tests in fp32 (they err by ~1e-7 relative, far inside the band):
+        // the first child u Q <= P, a later one u Q Z <= R(x)
         double Z = 1.0;
+        float zf = 1.f;
         float rx = 0.f;  // R(x) of the child under test, after a rejection
         int accepted = -1, j = 0;
         for (int c = node + 1; c < n_nodes; ++c) {
             if (a.parent[c] != node) continue;
-            const double ep = s_ep[c], eq = s_eq[c], u = s_ua[c];
-            const double band = ldexp(kLogitBand, j + 1);
-            bool ok, close;
-            if (j == 0) {  // u Q <= P with both sides multiplied by Sp Sq > 0
-                const double P = ep * Sq, Qs = eq * Sp, uq = u * Qs;
-                const double hi = fmax(P, Qs);
-                ok = uq <= P;
-                close = fabs(uq - P) <= band * hi || hi < kLogitTiny * (Sp * Sq);
-            } else {
-                const double P = ep / Sp, Qx = eq / Sq;
-                const double lhs = u * Qx * Z;
-                const double hi = fmax(P, Qx);
-                ok = lhs <= (double)rx;
-                close = fabs(lhs - (double)rx) <= band * hi || hi < kLogitTiny;
-            }
+            const float P = s_px[c], Qx = s_qx[c];
+            const float band = kLogitBandF * (float)(2u << min(j, 29));
+            const float lhs = __fmul_rn(__fmul_rn(s_ua[c], Qx), zf);
+            const float Rx = j == 0 ? P : rx;  // the residual at x: P before any rejection
+            const float hi = fmaxf(P, Qx);
+            const bool ok = lhs <= Rx;
+            const bool close = fabsf(lhs - Rx) <= band * hi || hi < kLogitTinyF;
             near |= close;
             if (ok) {
                 accepted = c;
@@ -1396,6 +1389,7 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
             upd.cq = a.c_draft;
             upd.iq = ts.inv[1];
             Z = cluster_sum(st, upd, g, parity, xn, R);
+            zf = (float)Z;
             parity ^= 1;
             rx = st.probe_val;
             ++j;
@@ -1409,7 +1403,7 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
             node = accepted;
             continue;
         }
-        const double s = ldexp(kLogitBand, j + 1);
+        const double s = kLogitBand * (double)(2u << min(j, 29));
         if (Z < s) near = true;
         bool nb = false;
         if (Z > 0.0) {
