@@ -43,6 +43,16 @@ from speculative_verify_paged_attn_gb300 import workloads as W  # noqa: E402
 METRIC = "paged verify-attn KV GB/s (% of GB300 HBM peak); spec_accept rows/s"
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 L2_BYTES = 129 * 1024 * 1024
+
+
+def flush_l2(buf: torch.Tensor) -> None:
+    """Evict L2 before a timed launch: write a buffer twice the size of L2,
+    then read it back.  The read writes back the dirty lines the fill left,
+    so the timed launch starts from an L2 that holds only clean, unrelated
+    lines (as ncu's cache control does) instead of paying for up to 129 MB of
+    the flush's own write-backs inside its timed region."""
+    buf.fill_(1)
+    buf.sum()
 # the sources that decide an attention kernel's DRAM traffic: its own file,
 # the shared device helpers and the launch planning
 KERNEL_SOURCES = {
@@ -200,7 +210,7 @@ class Step:
         self.ft.copy_(self.ft0)
 
     def flush_l2(self):
-        self.flush_buf.fill_(1)
+        flush_l2(self.flush_buf)
 
     def attention(self):
         inp = self.inp
@@ -323,7 +333,7 @@ def time_whole_step(ws: WholeStep, steps: int, warmup: int, stream) -> float:
     ms = []
     for _ in range(steps):
         ws.reset()
-        flush.fill_(1)
+        flush_l2(flush)
         gpu_lead()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -344,7 +354,7 @@ def time_append(ap: Append, steps: int, warmup: int, stream) -> float:
     ms = []
     for _ in range(steps):
         ap.reset()
-        flush.fill_(1)
+        flush_l2(flush)
         gpu_lead()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -378,7 +388,7 @@ def time_logits(wl: W.Workload, seed: int, steps: int, warmup: int, stream):
         run()
     ms = []
     for _ in range(steps):
-        flush.fill_(1)
+        flush_l2(flush)
         gpu_lead()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -424,7 +434,7 @@ def time_tree_logits(wl: W.Workload, seed: int, steps: int, warmup: int, stream,
         run()
     ms = []
     for _ in range(steps):
-        flush.fill_(1)
+        flush_l2(flush)
         gpu_lead()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -523,7 +533,7 @@ def time_attention_only(name: str, steps: int, warmup: int, peak: float):
         run()
     ms = []
     for _ in range(steps):
-        flush.fill_(1)
+        flush_l2(flush)
         gpu_lead()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -756,7 +766,8 @@ def config_dict(wl: W.Workload):
          "batch": wl.batch, "n_q": wl.n_q, "num_q_heads": wl.num_q_heads,
          "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "vocab": wl.vocab,
          "kv_dtype": "fp8_e4m3" if wl.kv_fp8 else "bf16",
-         "l2": "flushed before every step (256 MiB write, outside the step events)",
+         "l2": "flushed before every step, outside the step events: 256 MiB written, then read back so "
+               "that the step starts from a clean L2 (the inputs are also larger than L2)",
          "timing": "CUDA events on the launching stream; a 0.1 ms GPU spin precedes each step's "
                    "first event so the host's enqueue path is not counted (e2e counts it)",
          "parallelism": "replicas (one independent batch per GPU)"}

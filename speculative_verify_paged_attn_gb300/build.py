@@ -29,6 +29,7 @@ SOURCES = {
     "gamma_control.cu": ["-fmad=false"],
     "svpa_noalloc.cu": [],
     "svpa_logits_api.cu": [],
+    "svpa_step_api.cu": [],
     "wait_selftest.cu": [],
 }
 
