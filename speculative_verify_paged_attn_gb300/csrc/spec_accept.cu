@@ -852,9 +852,9 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
 // (target logits checked against draft logits).
 //
 // Two kernels.  logit_stats_kernel reads every logit once, one CTA per
-// 8192-token slab of a row (thousands of independent CTAs, so the read runs
-// at memory speed whatever the batch), and writes the slab's max m and sum s
-// of 2^((l - m) c), c = log2(e) / T.  The sampler kernel, launched as its
+// 8192-token slab of a row (independent CTAs, so the read runs at memory
+// speed whatever the batch), and writes the slab's max m and sum s of
+// 2^((l - m) c), c = log2(e) / T.  The sampler kernel, launched as its
 // programmatic dependent, is the linear sampler's cluster kernel: it loads
 // the draft tokens, their logits and the uniforms while the statistics grid
 // runs, then each CTA merges every row's slab pairs in a fixed order (a
@@ -929,13 +929,18 @@ __device__ __forceinline__ const float *logit_row(const LogitsArgs &a, int b, in
                         : a.lq + ((size_t)b * a.gamma + (r - a.gamma - 1)) * a.V;
 }
 
-// One CTA per (sequence, row, slab): the slab's (max, sum) into a.stats.
-// Each thread loads its 32 logits (eight float4, all in flight together) and
-// reduces them as two groups of sixteen.
-__global__ void __launch_bounds__(kClThreads) logit_stats_kernel(const __grid_constant__ LogitsArgs a) {
+// One CTA of 128 threads per (sequence, row, slab): the slab's (max, sum)
+// into a.stats.  Each thread reduces 64 logits in two batches of eight
+// float4 loads (a batch's loads all in flight together).  At 48 registers
+// ten CTAs fit on an SM, so the 7B sampler shape's 1152 slabs run as one
+// wave.
+constexpr int kStatThreads = 128;
+constexpr int kStatWarps = kStatThreads / 32;
+static_assert(kSlab == kStatThreads * 64, "a statistics CTA covers one slab");
+__global__ void __launch_bounds__(kStatThreads) logit_stats_kernel(const __grid_constant__ LogitsArgs a) {
     // the sampler may be scheduled now; it waits for this grid before reading
     asm volatile("griddepcontrol.launch_dependents;");
-    __shared__ float s_wm[kClWarps], s_ws[kClWarps];
+    __shared__ float s_wm[kStatWarps], s_ws[kStatWarps];
     const int rows = 2 * a.gamma + 1;
     const int slab = (int)(blockIdx.x % (unsigned)a.n_slabs);
     const int br = (int)(blockIdx.x / (unsigned)a.n_slabs);  // b * rows + r
@@ -945,16 +950,22 @@ __global__ void __launch_bounds__(kClThreads) logit_stats_kernel(const __grid_co
     const bool vec = (a.V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.lp) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(a.lq) & 15) == 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float4 w[2][4];
+    float m = -CUDART_INF_F, s = 0.f, m2, s2;
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < 2; ++h) {
+        float4 w[2][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            w[h][i] = load_logits4(row, slab * kSlab + 4 * ((int)threadIdx.x + (4 * h + i) * kClThreads), a.V, vec);
-    float m, s, m2, s2;
-    group_stats16(w[0], c, m, s);
-    group_stats16(w[1], c, m2, s2);
-    online_merge(m, s, m2, s2, c);
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                w[g][i] = load_logits4(row, slab * kSlab + 4 * ((int)threadIdx.x + (8 * h + 4 * g + i) * kStatThreads),
+                                       a.V, vec);
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            group_stats16(w[g], c, m2, s2);
+            online_merge(m, s, m2, s2, c);
+        }
+    }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
         m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -968,7 +979,7 @@ __global__ void __launch_bounds__(kClThreads) logit_stats_kernel(const __grid_co
     __syncthreads();
     if (threadIdx.x == 0) {
         float mm = s_wm[0], ss = s_ws[0];
-        for (int i = 1; i < kClWarps; ++i) online_merge(mm, ss, s_wm[i], s_ws[i], c);
+        for (int i = 1; i < kStatWarps; ++i) online_merge(mm, ss, s_wm[i], s_ws[i], c);
         a.stats[(size_t)br * a.n_slabs + slab] = make_float2(mm, ss);
     }
 }
@@ -1537,7 +1548,7 @@ cudaError_t launch_spec_accept_logits(const LogitsArgs &a, cudaStream_t stream) 
     b.n_slabs = (a.V + kSlab - 1) / kSlab;
     const long long stat_ctas = (long long)a.B * (2 * a.gamma + 1) * b.n_slabs;
     if (b.n_slabs > kMaxSlabs || stat_ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-    logit_stats_kernel<<<(unsigned)stat_ctas, kClThreads, 0, stream>>>(b);
+    logit_stats_kernel<<<(unsigned)stat_ctas, kStatThreads, 0, stream>>>(b);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     static void (*const kernels[])(LogitsArgs, int) = {
