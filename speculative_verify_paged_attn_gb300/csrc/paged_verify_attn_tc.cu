@@ -82,9 +82,12 @@ struct TcCfg {
     static constexpr int kNV8 = FP8 ? 2 : 1;
     static constexpr int kQSlab = (FP8 ? 64 : 128) * 128;  // one 64-column slab of the query buffer
     static constexpr int kQBuf = 2 * kQSlab;
-    // arrivals that complete a staging slot: the producer's expect_tx and
-    // one cp.async scale copy per page
-    static constexpr uint32_t kStageArrivals = 1 + kPagesPerBlock;
+    // arrivals that complete a staging slot: the producer's expect_tx, and on
+    // a K slot one cp.async per page for each of its two page scales (K's and
+    // V's: the softmax takes both with block j's scores, so it never waits
+    // for V's conversion)
+    static constexpr uint32_t kStageArrivalsK = 1 + 2 * kPagesPerBlock;
+    static constexpr uint32_t kStageArrivalsV = 1;
     static constexpr int kSoftmaxWarp0 = FP8 ? 4 : 2;
     static constexpr int kSoftmaxWarps = FP8 ? 2 : 4;
     static constexpr int kEpiWarp0 = FP8 ? 8 : 6;
@@ -203,11 +206,11 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
         }
         if constexpr (FP8) {
             for (int i = 0; i < C::kNK8; ++i) {
-                mbar_init(&sm.st8.k8_full[i], C::kStageArrivals);
+                mbar_init(&sm.st8.k8_full[i], C::kStageArrivalsK);
                 mbar_init(&sm.st8.k8_empty[i], C::kConvWarps);
             }
             for (int i = 0; i < C::kNV8; ++i) {
-                mbar_init(&sm.st8.v8_full[i], C::kStageArrivals);
+                mbar_init(&sm.st8.v8_full[i], C::kStageArrivalsV);
                 mbar_init(&sm.st8.v8_empty[i], C::kConvWarps);
             }
             mbar_init(&sm.st8.q_full, 1);
@@ -308,7 +311,6 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             if (lane < kPagesPerBlock) {
                 const int id = sm.vid[jv % kNMeta][lane], hh = sm.meta[jv % kNMeta].h;
                 copy_page(&mvp, v_slot(vs), id, hh, &pv_full[vs]);
-                if constexpr (FP8) copy_scale(a.v_scale, id, hh, &sm.st8.vsc[jv % kNMeta][lane], &pv_full[vs]);
                 if constexpr (TILES) copy_tile_scales(a.v_scale, id, hh, sm.t64.v[vs][lane], &pv_full[vs]);
             }
             __syncwarp();
@@ -404,7 +406,10 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                     if (lane < kPagesPerBlock) {
                         sm.vid[jk % kNMeta][lane] = my_id;
                         copy_page(&mkp, k_slot(ks), my_id, h, &pk_full[ks]);
-                        if constexpr (FP8) copy_scale(a.k_scale, my_id, h, &sm.st8.ksc[jk % kNMeta][lane], &pk_full[ks]);
+                        if constexpr (FP8) {
+                            copy_scale(a.k_scale, my_id, h, &sm.st8.ksc[jk % kNMeta][lane], &pk_full[ks]);
+                            copy_scale(a.v_scale, my_id, h, &sm.st8.vsc[jk % kNMeta][lane], &pk_full[ks]);
+                        }
                         if constexpr (TILES)
                             copy_tile_scales(a.k_scale, my_id, h, sm.t64.k[ks][lane], &pk_full[ks]);
                     }
@@ -431,12 +436,12 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             if (ok && jk >= PNK) ok = mbar_wait(&pk_empty[ks], (uint32_t)(((jk / PNK) & 1) ^ 1), a.err);
             if (ok) {
                 sm.meta[jk % kNMeta].flags = kFlagEnd;
-                mbar_arrive_cnt(&pk_full[ks], FP8 ? C::kStageArrivals : 1u);
+                mbar_arrive_cnt(&pk_full[ks], FP8 ? C::kStageArrivalsK : 1u);
             }
             const int vs = jv % PNV;
             if constexpr (FP8) {
                 if (ok && jv >= PNV) ok = mbar_wait(&pv_empty[vs], (uint32_t)(((jv / PNV) & 1) ^ 1), a.err);
-                if (ok) mbar_arrive_cnt(&pv_full[vs], C::kStageArrivals);
+                if (ok) mbar_arrive_cnt(&pv_full[vs], C::kStageArrivalsV);
             }
             // wait (bounded) for the copies still in flight; a stage reused
             // by an end marker had completed before its empty barrier passed
@@ -569,13 +574,26 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             float s[kNB];
             {
                 const uint32_t sa = tmem + kTmemS + (uint32_t)(j & 1) * kNB + lane_off;
+                if constexpr (FP8) {
+                    // the block's four 32-column loads issued back to back, one
+                    // wait (the FP8 softmax is the critical path)
+                    uint32_t raw[kNB / 32][32];
 #pragma unroll
-                for (int c = 0; c < kNB / 32; ++c) {
-                    uint32_t raw[32];
-                    tmem_ld32(sa + c * 32, raw);
+                    for (int c = 0; c < kNB / 32; ++c) tmem_ld32(sa + c * 32, raw[c]);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) s[c * 32 + t] = __uint_as_float(raw[t]);
+                    for (int c = 0; c < kNB / 32; ++c)
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) s[c * 32 + t] = __uint_as_float(raw[c][t]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kNB / 32; ++c) {
+                        uint32_t raw[32];
+                        tmem_ld32(sa + c * 32, raw);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) s[c * 32 + t] = __uint_as_float(raw[t]);
+                    }
                 }
             }
 
@@ -637,11 +655,8 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
             }
             const float neg_m = m_ref == -CUDART_INF_F ? 0.f : -m_ref;
             const float sc = a.scale_log2;
-            if constexpr (FP8) {
-                // V_j's page scales multiply P (PV reads raw E4M3 values as f16)
-                // once the V converters are done with block j
-                mbar_wait(&sm.v_full[j % kNV], (uint32_t)((j / kNV) & 1), a.err);
-            }
+            // (FP8: V_j's page scales, which multiply P, came with K_j's
+            // staging, which S_j's completion follows)
             // P_j as bf16 pairs into the first half of S_j's TMEM columns
             const uint32_t pt = tmem + kTmemS + (uint32_t)(j & 1) * kNB + lane_off;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
@@ -927,10 +942,13 @@ __global__ void __launch_bounds__(TcCfg<FP8>::kThreads, 1)
                     break;
                 }
                 const uint8_t *src = kconv ? sm.st8.k8[s8] : sm.st8.v8[s8];
-                const float *scl = kconv ? sm.st8.ksc[j % kNMeta] : sm.st8.vsc[j % kNMeta];
                 uint8_t *tile = kconv ? sm.kbuf[tb] : sm.vbuf[tb];
-                if (lane < kPagesPerBlock && !(scl[lane] >= 0.f && scl[lane] <= kMaxScale8))
-                    raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                // both page scales of the block came with its K staging slot
+                if (kconv && lane < kPagesPerBlock) {
+                    const float ks = sm.st8.ksc[j % kNMeta][lane], vs = sm.st8.vsc[j % kNMeta][lane];
+                    if (!(ks >= 0.f && ks <= kMaxScale8) || !(vs >= 0.f && vs <= kMaxScale8))
+                        raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                }
                 if (kconv && (md.flags & kFlagFirst)) {
                     // the unit's queries, bf16 -> f16 in place (rows < M)
                     if (!mbar_wait(&sm.st8.q_full, (uint32_t)(units_seen & 1), a.err)) break;
