@@ -237,16 +237,6 @@ __device__ __forceinline__ void cluster_wait_started() {
     asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
-// This CTA's slice of a row, fetched into L2 by the bulk-copy engine: one
-// request for the whole slice, so the loads that follow find their lines in
-// flight instead of each warp's misses queueing in L1.  Rows that are not
-// 16-byte aligned (or V % 4 != 0) are left to the plain loads.
-__device__ __forceinline__ void prefetch_slice(const float *row, int lo, int hi, bool vec) {
-    if (!row || !vec || hi <= lo) return;
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row + lo), "r"((uint32_t)(hi - lo) * 4u)
-                 : "memory");
-}
-
 __device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
@@ -664,10 +654,6 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
                      (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
     SrcGlobal src{a.p + ((size_t)b * (gamma + 1) + k) * V, k < gamma ? a.q + ((size_t)b * gamma + k) * V : nullptr,
                   V, vec};
-    if (threadIdx.x == 0) {
-        prefetch_slice(src.p, g.cta_lo, g.cta_hi, vec);
-        prefetch_slice(src.q, g.cta_lo, g.cta_hi, vec);
-    }
     cluster_wait_started();
     Kept<NI, kKeepWeights<NI>> keep;
     double S = cluster_sum(st, src, g, 0, -1, nullptr, keep);
@@ -747,10 +733,6 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
     while (true) {
         const float *Pn = a.p + ((size_t)b * n_nodes + node) * V;
         const int qr = a.qrow[node];
-        if (threadIdx.x == 0) {  // this node's rows, while the acceptance tests run
-            prefetch_slice(Pn, g.cta_lo, g.cta_hi, vec);
-            if (qr >= 0) prefetch_slice(a.q + ((size_t)b * a.n_internal + qr) * V, g.cta_lo, g.cta_hi, vec);
-        }
         if (qr < 0) {  // leaf: bonus token from its own P
             const SrcGlobal src{Pn, nullptr, V, vec};
             Kept<NI, kKeepWeights<NI>> keep;
@@ -1325,10 +1307,6 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
         const float *Pn = a.p + ((size_t)b * n_nodes + node) * V;
         const int qr = a.qrow[node];
         const float *Qn = qr >= 0 ? a.q + ((size_t)b * a.n_internal + qr) * V : nullptr;
-        if (threadIdx.x == 0) {
-            prefetch_slice(Pn, g.cta_lo, g.cta_hi, vec);
-            prefetch_slice(Qn, g.cta_lo, g.cta_hi, vec);
-        }
         cluster_row_stats<NI>(ts, Pn, Qn, a.c_target, a.c_draft, g, V, vec, parity);
         parity ^= 1;
         SrcLogits srcp;
