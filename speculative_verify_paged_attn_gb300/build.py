@@ -23,6 +23,7 @@ SOURCES = {
     "svpa_api.cu": [],
     "paged_verify_attn.cu": [],
     "paged_verify_attn_tc.cu": [],
+    "paged_verify_attn_f8.cu": [],
     "spec_accept.cu": ["-fmad=false"],
     "block_table_commit.cu": [],
     "kv_append.cu": ["-fmad=false"],

@@ -1057,8 +1057,9 @@ cudaError_t launch_tc(const CUtensorMap &mk, const CUtensorMap &mv, const AttnMa
 // FP8 pages: the E4M3 page maps (one 2 KB box per page); bf16: the 5-D page maps
 cudaError_t launch_paged_verify_attn_tc(const AttnMaps &m, const AttnArgs &a, int grid, bool fp8, cudaStream_t st) {
     if (!fp8) return launch_tc<false, false>(m.kpage, m.vpage, m, a, grid, st);
-    return a.scale_tile ? launch_tc<true, true>(m.k[0], m.v[0], m, a, grid, st)
-                        : launch_tc<true, false>(m.k[0], m.v[0], m, a, grid, st);
+    // (FP8 pages with one scale per page take paged_verify_attn_f8.cu's kernel)
+    if (!a.scale_tile) return cudaErrorInvalidValue;
+    return launch_tc<true, true>(m.k[0], m.v[0], m, a, grid, st);
 }
 
 }  // namespace svpa

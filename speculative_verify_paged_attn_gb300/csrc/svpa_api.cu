@@ -58,7 +58,8 @@ struct AttnPlan {
     bool use_tc;
     int grid_slots;      // resident CTAs of the chosen kernel
     bool ordered;        // units handed out longest sequence first
-    size_t off_order, off_ml, off_acc, bytes;
+    bool streamk;        // blocks split evenly over the grid (FP8 tcgen05 kernel)
+    size_t off_order, off_prefix, off_ml, off_acc, bytes;
 };
 
 svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
@@ -124,6 +125,26 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     // unit starts at once and the extra launch buys nothing)
     pl->ordered = pl->max_splits == 1 && p->batch > 1 && p->batch <= kMaxOrderedSeqs &&
                   units > (size_t)pl->grid_slots;
+    // FP8 pages with per-page scales on the tcgen05 kernel: the blocks of all
+    // (sequence, kv head) pairs are split evenly over the grid (no split
+    // size, no ordering): [per-sequence block prefix, int64][pieces' (max,
+    // sum)][pieces' accumulators], two piece slots per CTA
+    pl->streamk = pl->use_tc && eb == 1 && p->scale_tile == 0;
+    if (pl->streamk) {
+        pl->ordered = false;
+        pl->split_pages = 0;
+        pl->max_splits = 1;
+        pl->off_order = off;
+        pl->off_prefix = off;
+        off += align_up(((size_t)p->batch + 1) * sizeof(long long));
+        pl->off_ml = off;
+        off += align_up((size_t)2 * pl->grid_slots * M * 2 * sizeof(float));
+        pl->off_acc = off;
+        off += align_up((size_t)2 * pl->grid_slots * M * D * sizeof(float));
+        pl->bytes = off;
+        return SVPA_OK;
+    }
+    pl->off_prefix = 0;
     pl->off_order = off;
     if (pl->ordered) off += align_up((size_t)p->batch * sizeof(int32_t));
     pl->off_ml = off;
@@ -201,7 +222,7 @@ svpa_status svpa_attn_launches(const svpa_attn_params *p, int32_t *launches) {
     AttnPlan pl;
     const svpa_status s = plan_attn(p, &pl);
     if (s != SVPA_OK) return s;
-    *launches = p->batch == 0 ? 0 : (pl.ordered ? 2 : 1);
+    *launches = p->batch == 0 ? 0 : (pl.ordered || pl.streamk ? 2 : 1);
     return SVPA_OK;
 }
 
@@ -345,6 +366,17 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
         cudaError_t e = launch_seq_order(context_lens, p->batch, reinterpret_cast<int32_t *>(ws + pl.off_order),
                                          static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return from_cuda(e);
+    }
+    if (pl.streamk) {
+        a.sk_prefix = reinterpret_cast<const long long *>(ws + pl.off_prefix);
+        a.sk_ml = reinterpret_cast<float *>(ws + pl.off_ml);
+        a.sk_acc = reinterpret_cast<float *>(ws + pl.off_acc);
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        cudaError_t e = launch_streamk_prefix(context_lens, p->batch, p->n_q, p->num_kv_heads,
+                                              p->max_blocks_per_seq, reinterpret_cast<long long *>(ws + pl.off_prefix),
+                                              error_flag, st);
+        if (e != cudaSuccess) return from_cuda(e);
+        return from_cuda(launch_paged_verify_attn_f8(maps, a, pl.grid_slots, st));
     }
     if (pl.use_tc) {
         const int grid = std::max(1, std::min(pl.grid_slots, a.total_units));

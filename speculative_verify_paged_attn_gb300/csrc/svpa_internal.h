@@ -74,6 +74,12 @@ struct AttnArgs {
     int32_t scale_tile;   // FP8 scales: 0 per (page, kv head), 64 per 64-element tile
     float scale_log2;     // sm_scale * log2(e)
     unsigned long long anc[kMaxNq];  // visibility of speculative slots per query
+    // even split of the blocks over the grid (FP8 tcgen05 kernel): the
+    // per-sequence block prefix [B + 1], and the pieces' partial rows, two
+    // slots per CTA: (max, sum) [2 * grid, M, 2] and accumulators [2 * grid, M, D]
+    const long long *sk_prefix;
+    float *sk_ml;
+    float *sk_acc;
 };
 
 struct AttnMaps {
@@ -112,6 +118,12 @@ cudaError_t launch_seq_order(const int32_t *context_lens, int B, int32_t *order,
 // tcgen05 / TMEM variant (bf16 pages, head_dim 128, one CTA per SM).
 cudaError_t launch_paged_verify_attn_tc(const AttnMaps &maps, const AttnArgs &a, int grid, bool fp8,
                                         cudaStream_t stream);
+// tcgen05 / TMEM variant for FP8 pages with one scale per (page, kv head):
+// E4M3 scores MMA on the staged K pages, G * n_q <= 64, one CTA per SM.
+cudaError_t launch_paged_verify_attn_f8(const AttnMaps &maps, const AttnArgs &a, int grid, cudaStream_t stream);
+// The per-sequence block prefix the FP8 tcgen05 kernel splits its work by.
+cudaError_t launch_streamk_prefix(const int32_t *context_lens, int B, int n_q, int Hkv, int max_blocks,
+                                  long long *prefix, int32_t *err, cudaStream_t stream);
 
 // Rejection sampler.
 struct AcceptArgs {

@@ -165,8 +165,9 @@ def test_kernel_variants(name, wl, split, variant):
 def test_fp8_page_scales_wide_range():
     # K and V page scales spread over eight decades and a few zero V scales:
     # the warp-level kernel applies the scales in fp32 and takes any of them;
-    # the tcgen05 kernel folds them into f16 and takes scales up to 146 (its
-    # documented contract; larger ones are reported, see the next test)
+    # the tcgen05 kernel (one scale per page) takes any K scale and V scales
+    # up to 255 (its documented contract; larger ones are reported, see the
+    # next test)
     wl = small("fp8", batch=3, ctx_lo=100, ctx_hi=900)
     inp = W.make_attention(wl, 17)
     g = torch.Generator().manual_seed(23)
@@ -181,13 +182,44 @@ def test_fp8_page_scales_wide_range():
     assert st == 0
     ref, _ = U.run_oracle_attention(inp)
     U.assert_attention_close(got, ref, fp8=True, what="wide scales, warp-level kernel")
-    # the same spread capped at 146 on the tcgen05 kernel
-    inp.k_scale = (base_k * fk).clamp(max=146.0).contiguous()
-    inp.v_scale = (base_v * fv).clamp(max=146.0).contiguous()
+    # the same spread, V scales capped at 255, on the tcgen05 kernel
+    inp.v_scale = (base_v * fv).clamp(max=255.0).contiguous()
     got, _, st = U.run_attention(inp, split_pages=8, variant=2)
     assert st == 0
     ref, _ = U.run_oracle_attention(inp)
-    U.assert_attention_close(got, ref, fp8=True, what="scales up to 146, tcgen05 kernel")
+    U.assert_attention_close(got, ref, fp8=True, what="K scales to 1e5, V scales to 255, tcgen05 kernel")
+
+
+def test_fp8_query_rows_of_any_magnitude():
+    # the tcgen05 kernel splits each query row into two E4M3 terms at a
+    # power-of-two scale of its own: rows of very different norms (1e-4 ..
+    # 1e4 times N(0, 1)) keep their relative accuracy
+    wl = small("fp8", batch=3, ctx_lo=100, ctx_hi=900)
+    inp = W.make_attention(wl, 19)
+    g = torch.Generator().manual_seed(29)
+    B, n_q, Hq, D = inp.q.shape
+    f = 10.0 ** (torch.rand((B, n_q, Hq, 1), generator=g) * 8 - 4)
+    inp.q = (inp.q.float() * f).to(torch.bfloat16).contiguous()
+    got, lse, st = U.run_attention(inp, variant=2)
+    assert st == 0
+    ref, ref_lse = U.run_oracle_attention(inp)
+    U.assert_attention_close(got, ref, fp8=True, what="query rows over eight decades, tcgen05 kernel")
+    # the log-sum-exp is relative to the scores' scale here
+    assert np.max(np.abs(lse - ref_lse) / np.maximum(1.0, np.abs(ref_lse))) < 2e-3
+
+
+def test_fp8_even_split_mixed_lengths():
+    # the tcgen05 kernel for per-page FP8 scales splits all blocks evenly over
+    # the SMs: sequences of mixed lengths (some shorter than one block, some
+    # cut into several pieces) and a batch whose blocks are fewer than the SMs
+    for seed, kw in ((31, dict(batch=9, ctx_lo=0, ctx_hi=6000)), (37, dict(batch=2, ctx_lo=1, ctx_hi=40)),
+                     (41, dict(batch=5, ctx_lo=20000, ctx_hi=40000))):
+        inp = W.make_attention(small("fp8", **kw), seed)
+        got, lse, st = U.run_attention(inp, variant=2)
+        assert st == 0
+        ref, ref_lse = U.run_oracle_attention(inp)
+        U.assert_attention_close(got, ref, fp8=True, what=f"even split, {kw}")
+        assert np.max(np.abs(lse - ref_lse)) < 2e-3
 
 
 def test_fp8_scale_beyond_f16_range_reported_on_tcgen05():
