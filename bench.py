@@ -58,7 +58,19 @@ def flush_l2(buf: torch.Tensor) -> None:
 KERNEL_SOURCES = {
     "pva_kernel": ["speculative_verify_paged_attn_gb300/csrc/paged_verify_attn.cu"],
     "pva_tc_kernel": ["speculative_verify_paged_attn_gb300/csrc/paged_verify_attn_tc.cu"],
+    "pva_f8_kernel": ["speculative_verify_paged_attn_gb300/csrc/paged_verify_attn_f8.cu"],
 }
+KERNEL_LABELS = {"pva_kernel": "pva_kernel (warp-level MMA)", "pva_tc_kernel": "pva_tc_kernel (tcgen05/TMEM)",
+                 "pva_f8_kernel": "pva_f8_kernel (tcgen05/TMEM, E4M3 scores)"}
+
+
+def attn_kernel_name(params, wl) -> str:
+    """The attention kernel the library runs for these parameters: the warp-level
+    MMA kernel, or on the tcgen05 path the FP8 kernel for pages with one scale
+    per page and the general tcgen05 kernel otherwise."""
+    if svpa.attn_kernel(params) != 2:
+        return "pva_kernel"
+    return "pva_f8_kernel" if wl.kv_fp8 and not wl.scale_tile else "pva_tc_kernel"
 SHARED_SOURCES = ["speculative_verify_paged_attn_gb300/csrc/svpa_device.cuh",
                   "speculative_verify_paged_attn_gb300/csrc/svpa_api.cu"]
 
@@ -546,7 +558,7 @@ def time_attention_only(name: str, steps: int, warmup: int, peak: float):
     kv = inp.kv_bytes()
     pages = int(((inp.context_lens.long() + n_q + 15) // 16).sum().item())
     alg = kv + 2 * inp.q.numel() * 2 + B * n_q * Hq * 4 + pages * 4
-    kname = "pva_tc_kernel" if svpa.attn_kernel(params) == 2 else "pva_kernel"
+    kname = attn_kernel_name(params, wl)
     return {"attn_us": round(avg * 1e3, 2), "kv_gbs": round(kv / (avg * 1e-3) / 1e9, 2),
             "frac": round(alg / (avg * 1e-3) / 1e9 / peak, 4), "frac_kv": round(kv / (avg * 1e-3) / 1e9 / peak, 4),
             "traffic": recorded_traffic(name, kname), "algorithmic_bytes_per_launch": alg, "kernel": kname,
@@ -977,7 +989,7 @@ def main():
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": sample, "single_thread": {"value": round(gbs1, 4), "sample": sample1}}
 
-    kname = "pva_tc_kernel" if svpa.attn_kernel(st.params) == 2 else "pva_kernel"
+    kname = attn_kernel_name(st.params, wl)
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -1020,14 +1032,14 @@ def main():
                          "traffic": recorded_traffic(args.config, kname),
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s",
-                         "kernel": ("pva_tc_kernel (tcgen05/TMEM)" if kname == "pva_tc_kernel"
-                                    else "pva_kernel (warp-level MMA)"),
+                         "kernel": KERNEL_LABELS[kname],
                          "algorithmic_bytes_per_launch": st.attn_bytes},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4),
                     "copies": "pinned host buffers; the attention's inputs on the step's stream, the "
                               "sampler's rows on two side streams overlapping the attention"},
-            # per step: the attention (1, or 2 with the unit ranking), sampler, commit
+            # per step: the attention (1, or 2 with the unit ranking or the FP8
+            # kernel's block prefix), sampler, commit
             "gpu_launches": (svpa.attn_launches(st.params) + 2) * K,
             "clocks": clk,
             "cpu_baseline": cpu,
