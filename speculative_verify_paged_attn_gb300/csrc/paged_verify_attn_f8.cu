@@ -29,9 +29,15 @@
 // 16 warps; a warp reads the TMEM lanes of quadrant warp % 4 only, and the
 // query rows live in quadrants 0 and 1, so the row-owning warps sit on SM
 // sub-partitions 0 and 1 and everything else on 2 and 3:
-//   warps 0, 1      epilogue (lane quadrants 0, 1): a finished unit's O from
-//                   TMEM to the output, or to a split partial merged by the
-//                   last split's CTA;
+//   warps 0,1 / 4,5 / 8,9 / 12,13
+//                   softmax and epilogue: warp w owns the rows of lane
+//                   quadrant w % 4 and the block's tokens 32 (w / 4) .. + 31;
+//                   the four warps of a quadrant exchange their block maxima
+//                   through shared memory (a bounded mbarrier wait), so that
+//                   all keep one lazy reference maximum per row, and at a
+//                   unit's end their partial row sums, then write their 32
+//                   columns of O (the output, or a piece's partial; the last
+//                   piece of a (sequence, kv head) merges the pieces);
 //   warp 2          producer: walks the CTA's share; each piece's bf16
 //                   query tile into one of two query slots; per 128-token
 //                   block, 8 E4M3 K page tiles (TMA, 128-byte swizzle) and
@@ -39,15 +45,8 @@
 //                   MMA reads directly, and the V page tiles into a 3-deep
 //                   staging ring;
 //   warp 3          MMA issuer (one thread) and TMEM owner: S_j into one of
-//                   two TMEM S buffers, issued ahead of PV_{j-1} when K_j and
-//                   the unit's split queries are ready; O += P_j V_j with P_j
-//                   read from TMEM into one of two TMEM O buffers;
-//   warps 4,5 / 8,9 / 12,13
-//                   softmax: warp w owns the rows of lane quadrant w % 4 and
-//                   the block's tokens 0-63, 64-95 or 96-127 (w / 4 = 1, 2,
-//                   3); the three warps of a quadrant exchange their block
-//                   maxima through shared memory (a bounded mbarrier wait),
-//                   so that all keep one lazy reference maximum per row;
+//                   two TMEM S buffers as soon as K_j and the unit's split
+//                   queries are ready; O += P_j V_j with P_j read from TMEM;
 //   warps 6,7,10,11 V converters: E4M3 -> f16 (exact) in the MMA's tile
 //                   layout, rows past the sequence's end zeroed;
 //   warps 14, 15    query split: one thread per query row turns the landed
@@ -82,12 +81,10 @@ constexpr int kQSlab = 64 * 128;            // one 128-byte column slab of 64 qu
 constexpr int kQSlot = 2 * kQSlab;          // one unit's queries (bf16, then the two E4M3 terms)
 constexpr int kNQScale = 4;                 // query-scale records in flight
 constexpr int kThreads = 512;
-constexpr int kEpiWarps = 2;                // warps 0, 1
 constexpr int kProducerWarp = 2, kMmaWarp = 3;
-constexpr int kSoftWarps = 6;               // 4, 5, 8, 9, 12, 13
+constexpr int kSoftWarps = 8;               // 0, 1, 4, 5, 8, 9, 12, 13 (warp % 4 = quadrant, warp / 4 = column slot)
 constexpr int kConvWarps = 4;               // 6, 7, 10, 11
 constexpr int kPrepWarp0 = 14;              // 14, 15
-constexpr int kBarEpi = 1;                  // named barrier of the two epilogue warps
 // P (at most 2^8 under the lazy maximum) times a V scale stays below the f16
 // maximum 65504
 constexpr float kMaxVScale8 = 255.f;
@@ -117,9 +114,8 @@ struct SmemF8 {
     float ksc[kNMeta][kPB];                   // page scales of the blocks in flight
     float vsc[kNMeta][kPB];
     float qscale[kNQScale][64];               // 2^-e of each query row, per unit in flight
-    float xmax[2][2][3][32];                  // [quadrant][block parity][column slot][lane]
-    float stat_m[64];                         // softmax -> epilogue: reference maximum per row
-    float stat_l[3][64];                      //   and the three partial row sums
+    float xmax[2][2][4][32];                  // [quadrant][block parity][column slot][lane]
+    float lsum[2][4][32];                     // [quadrant][column slot][lane]: partial row sums at a unit's end
     uint64_t k8_full[kNK8], k8_empty[kNK8];
     uint64_t v8_full[kNV8], v8_empty[kNV8];
     uint64_t v_full[kNV], v_empty[kNV];
@@ -128,12 +124,12 @@ struct SmemF8 {
     uint64_t p_full, p_empty;
     uint64_t p_free[2];                       // P[x] read by its P V (PV_j commits to p_free[j & 1])
     uint64_t o_full, o_empty;
-    uint64_t stat_full, stat_empty;
+    uint64_t lbar[2];                         // the quadrant's partial row sums exchanged
+    uint64_t gbar;                            // the eight softmax warps (split pieces' ticket)
     uint64_t xbar[2][2];                      // [quadrant][block parity]
     BlockMeta meta[kNMeta];
     int32_t vid[kNMeta][kPB];                 // page ids of a block, for its V copies
     int32_t q_is_end[2];                      // the producer's end marker on a query slot
-    int32_t ep_b, ep_h, ep_split, ep_nsplit, ep_slot, ep_end;
     uint32_t tmem_base;
     int32_t last;
 };
@@ -291,33 +287,40 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
         : "memory");
 }
 
-// The softmax of one (lane quadrant, column slot): the rows of quadrant
-// `quarter`, the np pages (16 tokens each) of every block from page pg0 on.
-// The six softmax warps share this one body, and its loops over pages are
-// not unrolled: the code stays small enough to remain in the SM
-// sub-partition's instruction cache next to the other roles' code.
-__device__ __noinline__ void softmax_role(SmemF8 &sm, const AttnArgs &a, uint32_t tmem, int quarter, int sl, int pg0,
-                                          int np) {
+// A barrier of the eight softmax warps on an mbarrier: every one of them
+// calls it at the same points in the same order; `phase` (a per-thread
+// counter) numbers those points.  Bounded: false (and SVPA_DEVERR_TIMEOUT)
+// when the wait runs out, after which the caller leaves its loop.
+__device__ __forceinline__ bool soft_sync(uint64_t *bar, uint32_t &phase, int32_t *err) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    const bool ok = wait_phase(bar, phase & 1u, err);
+    ++phase;
+    return ok;
+}
+
+// The softmax, and the epilogue, of one (lane quadrant, column slot): the
+// rows of quadrant `quarter` (TMEM lanes), the 32 columns 32 sl .. of every
+// block (pages 2 sl, 2 sl + 1).  The eight warps share this one body and its
+// code is kept small (one 32-column chunk per block, nothing unrolled twice):
+// every role's hot loop must stay in its SM sub-partition's instruction cache.
+__device__ __noinline__ void softmax_role(SmemF8 &sm, const AttnArgs &a, uint32_t tmem, int quarter, int sl) {
     const int lane = threadIdx.x & 31;
     const int r = quarter * 32 + lane;  // query row == TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int G = a.G;
     const bool live = r < a.M;
-    const int jq = live ? r / a.G : 0;
+    const int jq = live ? r / G : 0;
+    const int gi = r - jq * G;
     const unsigned long long anc = live ? a.anc[jq] : 0ull;
-    const int tok0 = pg0 * 16;
+    const int pg0 = 2 * sl, tok0 = 32 * sl;
     float m_ref = -CUDART_INF_F, l_run = 0.f, rowmul = 0.f;
+    uint32_t gph = 0;  // soft_sync phases passed
     int j = 0, unit = -1;
     while (true) {
         if (!wait_phase(&sm.s_full[j & 1], par_of(j), a.err)) break;
         const BlockMeta md = sm.meta[j % kNMeta];
-        if (md.flags & kFlagEnd) {
-            // tell the epilogue warps there is no further unit
-            if (unit >= 0) wait_phase(&sm.stat_empty, (uint32_t)(unit & 1), a.err);
-            if (quarter == 0 && sl == 0 && lane == 0) sm.ep_end = 1;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.stat_full);
-            break;
-        }
+        if (md.flags & kFlagEnd) break;
         const bool first = (md.flags & kFlagFirst) != 0;
         if (first) {
             ++unit;
@@ -329,16 +332,14 @@ __device__ __noinline__ void softmax_role(SmemF8 &sm, const AttnArgs &a, uint32_
         const uint32_t sa = tmem + kTmemS + (uint32_t)(j & 1) * kNB + lane_off + (uint32_t)tok0;
         // the page scales of this slot's pages came with K_j's staging, which
         // S_j's completion follows
-        const float *kscp = sm.ksc[j % kNMeta] + pg0;
-        const float *vscp = sm.vsc[j % kNMeta] + pg0;
-        // pass 1: the largest scaled score of the slot.  Its (at most 64)
-        // scores are loaded once, 32 columns (two pages) per TMEM load, and
-        // kept for pass 2; a page's K scale multiplies its scores, so the
-        // maximum of the scaled scores is the largest scaled page maximum
-        // (scales are >= 0)
-        uint32_t sc0[32], sc1[32];
-        tmem_ld32(sa, sc0);
-        if (np == 4) tmem_ld32(sa + 32, sc1);
+        const float ka = sm.ksc[j % kNMeta][pg0], kb = sm.ksc[j % kNMeta][pg0 + 1];
+        const float va = sm.vsc[j % kNMeta][pg0], vb = sm.vsc[j % kNMeta][pg0 + 1];
+        if (quarter == 0 && lane == 0 &&
+            (!(ka >= 0.f && ka <= 3.0e38f) || !(kb >= 0.f && kb <= 3.0e38f) || !(va >= 0.f && va <= kMaxVScale8) ||
+             !(vb >= 0.f && vb <= kMaxVScale8)))
+            raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+        uint32_t sc[32];
+        tmem_ld32(sa, sc);
         tmem_ld_wait();
         if (md.pos0 + kNB > md.L || md.ntok < kNB) {
             // only on the blocks that reach the speculative slots or a partial
@@ -356,42 +357,30 @@ __device__ __noinline__ void softmax_role(SmemF8 &sm, const AttnArgs &a, uint32_
             }
             const int nw = min(max(md.ntok - 64 * wv, 0), 64);
             if (nw < 64) vis &= (1ull << nw) - 1ull;
-            vis >>= (tok0 & 63);
-            const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
+            const uint32_t v0 = (uint32_t)(vis >> (tok0 & 63));
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                if (!((v0 >> t) & 1u)) sc0[t] = __float_as_uint(-CUDART_INF_F);
-                if (!((v1 >> t) & 1u)) sc1[t] = __float_as_uint(-CUDART_INF_F);
-            }
+            for (int t = 0; t < 32; ++t)
+                if (!((v0 >> t) & 1u)) sc[t] = __float_as_uint(-CUDART_INF_F);
+        }
+        // the largest scaled score of the slot: a page's K scale multiplies
+        // its scores, so it is the largest scaled page maximum (scales >= 0)
+        float pa = -CUDART_INF_F, pb = -CUDART_INF_F;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            pa = fmaxf(pa, __uint_as_float(sc[t]));
+            pb = fmaxf(pb, __uint_as_float(sc[16 + t]));
         }
         float lm = -CUDART_INF_F;
-        auto chunk_max = [&](const uint32_t(&raw)[32], int c) {
-            float pa = -CUDART_INF_F, pb = -CUDART_INF_F;
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                pa = fmaxf(pa, __uint_as_float(raw[t]));
-                pb = fmaxf(pb, __uint_as_float(raw[16 + t]));
-            }
-            const float ka = kscp[2 * c], kb = kscp[2 * c + 1];
-            if (pa != -CUDART_INF_F) lm = fmaxf(lm, pa * ka);
-            if (pb != -CUDART_INF_F) lm = fmaxf(lm, pb * kb);
-            if (quarter == 0 && lane == 0) {
-                const float va = vscp[2 * c], vb = vscp[2 * c + 1];
-                if (!(ka >= 0.f && ka <= 3.0e38f) || !(kb >= 0.f && kb <= 3.0e38f) ||
-                    !(va >= 0.f && va <= kMaxVScale8) || !(vb >= 0.f && vb <= kMaxVScale8))
-                    raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
-            }
-        };
-        chunk_max(sc0, 0);
-        if (np == 4) chunk_max(sc1, 1);
-        // the quadrant's three warps exchange their maxima
+        if (pa != -CUDART_INF_F) lm = pa * ka;
+        if (pb != -CUDART_INF_F) lm = fmaxf(lm, pb * kb);
+        // the quadrant's four warps exchange their maxima
         sm.xmax[quarter][j & 1][sl][lane] = lm == -CUDART_INF_F ? -CUDART_INF_F : lm * rowmul;
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.xbar[quarter][j & 1]);
         if (!wait_phase(&sm.xbar[quarter][j & 1], par_of(j), a.err)) break;
         const float mx = fmaxf(fmaxf(sm.xmax[quarter][j & 1][0][lane], sm.xmax[quarter][j & 1][1][lane]),
-                               sm.xmax[quarter][j & 1][2][lane]);
-        // the same decision in the three warps of a quadrant: they see the
+                               fmaxf(sm.xmax[quarter][j & 1][2][lane], sm.xmax[quarter][j & 1][3][lane]));
+        // the same decision in the four warps of a quadrant: they see the
         // same maxima and keep the same reference
         float alpha = 1.f;
         bool rescale = false;
@@ -403,64 +392,53 @@ __device__ __noinline__ void softmax_role(SmemF8 &sm, const AttnArgs &a, uint32_
         }
         // (a row past M gets -inf arguments: its P is never read)
         const float neg_m = !live ? -CUDART_INF_F : (m_ref == -CUDART_INF_F ? 0.f : -m_ref);
-        // pass 2, two pages per step: P as f16 pairs into P[j & 1], token t in
-        // column t / 2; each pair of exponents by one ex2.f16x2 on the fp32
-        // arguments rounded to f16 (an argument is at most 8 under the lazy
-        // maximum, where f16 keeps P within ~0.14%); the row sum adds those
-        // f16 values, in f16 within a page (16 values) and in fp32 across
-        // pages; P times the page's V scale is formed in f16.  A page whose K
-        // scale is 0 has scores 0: its multiplier stays positive so masked
-        // columns stay -inf.
-        const uint32_t pt = tmem + kTmemP + (uint32_t)(j & 1) * (kNB / 2) + lane_off + (uint32_t)(tok0 / 2);
+        // P as f16 pairs into P[j & 1], token t in column t / 2: each pair of
+        // exponents by one ex2.f16x2 on the fp32 arguments rounded to f16 (an
+        // argument is at most 8 under the lazy maximum, where f16 keeps P
+        // within ~0.14%); the row sum adds those f16 values, in f16 within a
+        // page (16 values) and in fp32 across pages; P times the page's V
+        // scale is formed in f16.  A page whose K scale is 0 has scores 0:
+        // its multiplier stays positive so masked columns stay -inf.
+        uint32_t w[16];
+        float ls = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float scp = fmaxf(rowmul * (h ? kb : ka), 1e-30f);
+            const float vs = h ? vb : va;
+            const uint32_t v2 = pack_f16x2(vs, vs);
+            uint32_t acc = 0u;  // f16 pair (+0, +0)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = 16 * h + 2 * e;
+                const uint32_t p2 = ex2_f16x2(pack_f16x2(fmaf(__uint_as_float(sc[t]), scp, neg_m),
+                                                         fmaf(__uint_as_float(sc[t + 1]), scp, neg_m)));
+                acc = add_f16x2(acc, p2);
+                w[8 * h + e] = mul_f16x2(p2, v2);
+            }
+            const float2 f = f16x2_to_float2(acc);
+            ls += f.x + f.y;
+        }
         // P[j & 1] held P_{j-2}: its P V must have read it (at block j no later
         // P V on that buffer can have completed, so the parity is unambiguous)
         if (j >= 2) wait_phase(&sm.p_free[j & 1], par_of(j - 2), a.err);
         tc_fence_after();
-        float ls = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < np / 2; ++c) {
-            uint32_t w[16];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float scp = fmaxf(rowmul * kscp[2 * c + h], 1e-30f);
-                const float vs = vscp[2 * c + h];
-                const uint32_t v2 = pack_f16x2(vs, vs);
-                uint32_t acc = 0u;  // f16 pair (+0, +0)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int t = 16 * h + 2 * e;
-                    const float s0 = __uint_as_float(sc0[t]), s1 = __uint_as_float(sc0[t + 1]);
-                    const uint32_t p2 = ex2_f16x2(pack_f16x2(fmaf(s0, scp, neg_m), fmaf(s1, scp, neg_m)));
-                    acc = add_f16x2(acc, p2);
-                    w[8 * h + e] = mul_f16x2(p2, v2);
-                }
-                const float2 f = f16x2_to_float2(acc);
-                ls += f.x + f.y;
-            }
-            tmem_st16(pt + 16 * c, w);
-            // the slot's second chunk moves into place for the next step
-#pragma unroll
-            for (int t = 0; t < 32; ++t) sc0[t] = sc1[t];
-        }
+        tmem_st16(tmem + kTmemP + (uint32_t)(j & 1) * (kNB / 2) + lane_off + (uint32_t)(tok0 / 2), w);
         l_run += ls;
         // TMEM loads and stores are warp-collective: the whole warp takes the
         // rescale path when any of its rows needs it (factor 1 elsewhere); each
-        // warp rescales the O columns of its own token range
+        // warp rescales the O columns of its own slot
         if (__any_sync(0xffffffffu, rescale)) {
             const float f = rescale ? alpha : 1.f;
             // O (TMEM) holds P_{<j} V; PV_{j-1} must have landed first
             wait_phase(&sm.p_empty, (uint32_t)((j - 1) & 1), a.err);
             tc_fence_after();
             const uint32_t oa = tmem + kTmemO + lane_off + (uint32_t)tok0;
-#pragma unroll 1
-            for (int c = 0; c < np / 2; ++c) {
-                uint32_t raw[32];
-                tmem_ld32(oa + c * 32, raw);
-                tmem_ld_wait();
+            uint32_t raw[32];
+            tmem_ld32(oa, raw);
+            tmem_ld_wait();
 #pragma unroll
-                for (int t = 0; t < 32; ++t) raw[t] = __float_as_uint(__uint_as_float(raw[t]) * f);
-                tmem_st32(oa + c * 32, raw);
-            }
+            for (int t = 0; t < 32; ++t) raw[t] = __float_as_uint(__uint_as_float(raw[t]) * f);
+            tmem_st32(oa, raw);
         }
         tmem_st_wait();
         // P_j is published only once PV_{j-1} has completed (PV_j cannot have
@@ -470,24 +448,147 @@ __device__ __noinline__ void softmax_role(SmemF8 &sm, const AttnArgs &a, uint32_
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.p_full);
-        if (md.flags & kFlagLast) {
-            // hand the unit's row statistics to the epilogue warps (one slot:
-            // the previous unit's must have been taken)
-            if (unit >= 1) wait_phase(&sm.stat_empty, (uint32_t)((unit - 1) & 1), a.err);
-            sm.stat_l[sl][r] = l_run;
-            if (sl == 0) sm.stat_m[r] = m_ref;
-            if (quarter == 0 && sl == 0 && lane == 0) {
-                sm.ep_b = md.b;
-                sm.ep_h = md.h;
-                sm.ep_split = md.split;
-                sm.ep_nsplit = md.nsplit;
-                sm.ep_slot = md.slot;
-                sm.ep_end = 0;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.stat_full);
-        }
         ++j;
+        if (!(md.flags & kFlagLast)) continue;
+
+        // ------------------------------------------- the unit's epilogue
+        // the row sum: the quadrant's four partial sums
+        sm.lsum[quarter][sl][lane] = l_run;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.lbar[quarter]);
+        if (!wait_phase(&sm.lbar[quarter], (uint32_t)(unit & 1), a.err)) break;
+        const float l_tot = (sm.lsum[quarter][0][lane] + sm.lsum[quarter][1][lane]) +
+                            (sm.lsum[quarter][2][lane] + sm.lsum[quarter][3][lane]);
+        // this slot's 32 columns of O, once the unit's last P V has landed:
+        // the final output when the unit is a whole (sequence, kv head), else
+        // an fp32 partial in the piece's slot
+        if (!wait_phase(&sm.o_full, (uint32_t)(unit & 1), a.err)) break;
+        tc_fence_after();
+        const int b = md.b, h = md.h, nsplit = md.nsplit;
+        const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
+        const size_t pr_own = (size_t)md.slot * a.M + r;
+        {
+            uint32_t raw[32];
+            tmem_ld32(tmem + kTmemO + lane_off + (uint32_t)tok0, raw);
+            tmem_ld_wait();
+            if (live) {
+                if (nsplit == 1) {
+                    const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+                    uint4 *orow = reinterpret_cast<uint4 *>(a.out + od * kD + tok0);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 0]) * inv, __uint_as_float(raw[c8 * 8 + 1]) * inv);
+                        v.y = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 2]) * inv, __uint_as_float(raw[c8 * 8 + 3]) * inv);
+                        v.z = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 4]) * inv, __uint_as_float(raw[c8 * 8 + 5]) * inv);
+                        v.w = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 6]) * inv, __uint_as_float(raw[c8 * 8 + 7]) * inv);
+                        orow[c8] = v;
+                    }
+                } else {
+                    uint4 *prow4 = reinterpret_cast<uint4 *>(a.sk_acc + pr_own * kD + tok0);
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4)
+                        prow4[c4] = make_uint4(raw[c4 * 4], raw[c4 * 4 + 1], raw[c4 * 4 + 2], raw[c4 * 4 + 3]);
+                }
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.o_empty);
+        if (nsplit == 1) {
+            if (sl == 0 && live && a.lse) a.lse[od] = (m_ref + __log2f(l_tot)) * 0.69314718055994530942f;
+            continue;
+        }
+        if (sl == 0 && live) {
+            a.sk_ml[pr_own * 2] = m_ref;
+            a.sk_ml[pr_own * 2 + 1] = l_tot;
+        }
+        __threadfence();
+        // every softmax warp's part of the piece is written: take a ticket;
+        // the last piece of the (sequence, kv head) merges all of them
+        if (!soft_sync(&sm.gbar, gph, a.err)) break;
+        const int u2 = b * a.Hkv + h;
+        if (quarter == 0 && sl == 0 && lane == 0) {
+            const int t = atomicAdd(&a.tickets[u2], 1);
+            sm.last = (t == nsplit - 1);
+            if (sm.last) a.tickets[u2] = 0;
+        }
+        if (!soft_sync(&sm.gbar, gph, a.err)) break;
+        if (!sm.last) continue;
+        // the merge: an online log-sum-exp merge over the pieces (running
+        // maximum, rescaled sum), one warp per row, 4 columns per lane, four
+        // rows and two pieces per pass so that their loads are in flight
+        // together; the pieces of (b, h) are the CTAs c_first .. c_first +
+        // nsplit - 1, each in its first-piece slot except possibly the first
+        __threadfence();
+        const long long W = a.sk_prefix[a.B];
+        const int nsh = (int)min((long long)gridDim.x, W);  // shares of the work
+        const long long p0 = a.sk_prefix[b];
+        const long long pbh = p0 + (long long)h * ((a.sk_prefix[b + 1] - p0) / a.Hkv);
+        const int c_first = (int)(((pbh + 1) * nsh - 1) / W);
+        const int k_first = ((long long)c_first * W / nsh == pbh) ? 0 : 1;
+        auto slot_of = [&](int i) -> size_t { return (size_t)(2 * (c_first + i) + (i == 0 ? k_first : 0)); };
+        const int ew = sl * 2 + quarter;  // 0..7
+        constexpr int NE = kSoftWarps;
+#pragma unroll 1
+        for (int r0 = ew; r0 < a.M; r0 += 4 * NE) {
+            float mrow[4], lrow[4];
+            float4 o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                mrow[i] = -CUDART_INF_F;
+                lrow[i] = 0.f;
+                o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll 1
+            for (int s0 = 0; s0 < nsplit; s0 += 2) {
+                float2 ml[4][2];
+                float4 v[4][2];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int rr = r0 + NE * i;
+                        if (rr < a.M && s0 + k < nsplit) {
+                            const size_t pr = slot_of(s0 + k) * a.M + rr;
+                            ml[i][k] = __ldcg(reinterpret_cast<const float2 *>(a.sk_ml + pr * 2));
+                            v[i][k] = __ldcg(reinterpret_cast<const float4 *>(a.sk_acc + pr * kD) + lane);
+                        } else {
+                            ml[i][k] = make_float2(-CUDART_INF_F, 0.f);
+                            v[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const float mk = ml[i][k].x;
+                        if (mk == -CUDART_INF_F) continue;  // an empty piece (or none)
+                        const float mn = fmaxf(mrow[i], mk);
+                        const float f_old = ex2_approx(mrow[i] - mn);  // 0 when mrow is -inf
+                        const float f_new = ex2_approx(mk - mn);
+                        lrow[i] = lrow[i] * f_old + ml[i][k].y * f_new;
+                        o[i].x = o[i].x * f_old + v[i][k].x * f_new;
+                        o[i].y = o[i].y * f_old + v[i][k].y * f_new;
+                        o[i].z = o[i].z * f_old + v[i][k].z * f_new;
+                        o[i].w = o[i].w * f_old + v[i][k].w * f_new;
+                        mrow[i] = mn;
+                    }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rr = r0 + NE * i;
+                if (rr >= a.M) break;
+                const float inv2 = lrow[i] > 0.f ? 1.f / lrow[i] : 0.f;
+                const int jq2 = rr / G, gi2 = rr - jq2 * G;
+                const size_t od2 = (((size_t)b * a.n_q + jq2) * a.Hq + (size_t)h * G + gi2);
+                uint2 v2;
+                v2.x = pack_bf16x2(o[i].x * inv2, o[i].y * inv2);
+                v2.y = pack_bf16x2(o[i].z * inv2, o[i].w * inv2);
+                reinterpret_cast<uint2 *>(a.out + od2 * kD)[lane] = v2;
+                if (lane == 0 && a.lse) a.lse[od2] = (mrow[i] + __log2f(lrow[i])) * 0.69314718055994530942f;
+            }
+        }
     }
 }
 
@@ -517,17 +618,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.q_ready[i], 2);
             mbar_init(&sm.q_empty[i], 1);
             mbar_init(&sm.s_full[i], 1);
-            mbar_init(&sm.xbar[i][0], 3);
-            mbar_init(&sm.xbar[i][1], 3);
+            mbar_init(&sm.xbar[i][0], 4);
+            mbar_init(&sm.xbar[i][1], 4);
         }
         mbar_init(&sm.o_full, 1);
-        mbar_init(&sm.o_empty, kEpiWarps);
+        mbar_init(&sm.o_empty, kSoftWarps);
+        mbar_init(&sm.lbar[0], 4);
+        mbar_init(&sm.lbar[1], 4);
+        mbar_init(&sm.gbar, kSoftWarps);
         mbar_init(&sm.p_full, kSoftWarps);
         mbar_init(&sm.p_empty, 1);
         mbar_init(&sm.p_free[0], 1);
         mbar_init(&sm.p_free[1], 1);
-        mbar_init(&sm.stat_full, kSoftWarps);
-        mbar_init(&sm.stat_empty, kEpiWarps);
         fence_mbar_init();
     }
     // query rows past M are never written by the copies: keep them zero
@@ -772,154 +874,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp < kEpiWarps) {
-        // ================================================= epilogue
-        // One thread per query row (TMEM lane) streams a finished unit's O
-        // out of TMEM while the softmax warps already work on the next unit
-        // (O is double-buffered in TMEM).
-        const int quarter = warp;
-        const int r = quarter * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const int G = a.G;
-        const bool live = r < a.M;
-        const int jq = live ? r / G : 0;
-        const int gi = r - jq * G;
-        const int ew = warp;
-        constexpr int NE = kEpiWarps;
-        for (int unit = 0;; ++unit) {
-            if (!wait_phase(&sm.stat_full, (uint32_t)(unit & 1), a.err)) break;
-            if (sm.ep_end) break;
-            const int b = sm.ep_b, h = sm.ep_h, nsplit = sm.ep_nsplit, slot = sm.ep_slot;
-            const float m_ref = sm.stat_m[r];
-            const float l_run = (sm.stat_l[0][r] + sm.stat_l[1][r]) + sm.stat_l[2][r];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.stat_empty);
-            if (!wait_phase(&sm.o_full, (uint32_t)(unit & 1), a.err)) break;
-            tc_fence_after();
-            const uint32_t oa = tmem + kTmemO + lane_off;
-            const int u2 = b * a.Hkv + h;
-            const size_t od = (((size_t)b * a.n_q + jq) * a.Hq + (size_t)h * G + gi);
-            const size_t pr_own = (size_t)slot * a.M + r;
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-#pragma unroll 1
-            for (int c = 0; c < kD / 32; ++c) {
-                uint32_t raw[32];
-                tmem_ld32(oa + c * 32, raw);
-                tmem_ld_wait();
-                if (live) {
-                    if (nsplit == 1) {
-                        uint4 *orow = reinterpret_cast<uint4 *>(a.out + od * kD + c * 32);
-#pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8) {
-                            uint4 v;
-                            v.x = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 0]) * inv, __uint_as_float(raw[c8 * 8 + 1]) * inv);
-                            v.y = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 2]) * inv, __uint_as_float(raw[c8 * 8 + 3]) * inv);
-                            v.z = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 4]) * inv, __uint_as_float(raw[c8 * 8 + 5]) * inv);
-                            v.w = pack_bf16x2(__uint_as_float(raw[c8 * 8 + 6]) * inv, __uint_as_float(raw[c8 * 8 + 7]) * inv);
-                            orow[c8] = v;
-                        }
-                    } else {
-                        uint4 *prow4 = reinterpret_cast<uint4 *>(a.sk_acc + pr_own * kD + c * 32);
-#pragma unroll
-                        for (int c4 = 0; c4 < 8; ++c4)
-                            prow4[c4] = make_uint4(raw[c4 * 4], raw[c4 * 4 + 1], raw[c4 * 4 + 2], raw[c4 * 4 + 3]);
-                    }
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.o_empty);
-            if (nsplit == 1) {
-                if (live && a.lse) a.lse[od] = (m_ref + __log2f(l_run)) * 0.69314718055994530942f;
-                continue;
-            }
-            if (live) {
-                a.sk_ml[pr_own * 2] = m_ref;
-                a.sk_ml[pr_own * 2 + 1] = l_run;
-            }
-            __threadfence();
-            named_barrier_sync(kBarEpi, NE * 32);
-            if (ew == 0 && lane == 0) {
-                const int t = atomicAdd(&a.tickets[u2], 1);
-                sm.last = (t == nsplit - 1);
-                if (sm.last) a.tickets[u2] = 0;
-            }
-            named_barrier_sync(kBarEpi, NE * 32);
-            const int last = sm.last;
-            named_barrier_sync(kBarEpi, NE * 32);
-            if (!last) continue;
-            // the last split's CTA merges every split's partial rows with
-            // log-sum-exp weights (an online merge: running maximum, rescaled
-            // sum): one warp per row, 4 columns per lane, four rows and two
-            // splits per pass so that their loads are in flight together
-            __threadfence();
-            // the pieces of (b, h): the CTAs c_first .. c_first + nsplit - 1,
-            // each in its first-piece slot except possibly the first CTA
-            const long long W = a.sk_prefix[a.B];
-            const int nsh = (int)min((long long)gridDim.x, W);  // shares of the work
-            const long long p0 = a.sk_prefix[b];
-            const long long pbh = p0 + (long long)h * ((a.sk_prefix[b + 1] - p0) / a.Hkv);
-            const int c_first = (int)(((pbh + 1) * nsh - 1) / W);
-            const int k_first = ((long long)c_first * W / nsh == pbh) ? 0 : 1;
-            auto slot_of = [&](int i) -> size_t { return (size_t)(2 * (c_first + i) + (i == 0 ? k_first : 0)); };
-            for (int r0 = ew; r0 < a.M; r0 += 4 * NE) {
-                float mrow[4], lrow[4];
-                float4 o[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    mrow[i] = -CUDART_INF_F;
-                    lrow[i] = 0.f;
-                    o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                for (int s0 = 0; s0 < nsplit; s0 += 2) {
-                    float2 ml[4][2];
-                    float4 v[4][2];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-#pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            const int rr = r0 + NE * i;
-                            if (rr < a.M && s0 + k < nsplit) {
-                                const size_t pr = slot_of(s0 + k) * a.M + rr;
-                                ml[i][k] = __ldcg(reinterpret_cast<const float2 *>(a.sk_ml + pr * 2));
-                                v[i][k] = __ldcg(reinterpret_cast<const float4 *>(a.sk_acc + pr * kD) + lane);
-                            } else {
-                                ml[i][k] = make_float2(-CUDART_INF_F, 0.f);
-                                v[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            }
-                        }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-#pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            const float mk = ml[i][k].x;
-                            if (mk == -CUDART_INF_F) continue;  // an empty split (or none)
-                            const float mn = fmaxf(mrow[i], mk);
-                            const float f_old = ex2_approx(mrow[i] - mn);  // 0 when mrow is -inf
-                            const float f_new = ex2_approx(mk - mn);
-                            lrow[i] = lrow[i] * f_old + ml[i][k].y * f_new;
-                            o[i].x = o[i].x * f_old + v[i][k].x * f_new;
-                            o[i].y = o[i].y * f_old + v[i][k].y * f_new;
-                            o[i].z = o[i].z * f_old + v[i][k].z * f_new;
-                            o[i].w = o[i].w * f_old + v[i][k].w * f_new;
-                            mrow[i] = mn;
-                        }
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int rr = r0 + NE * i;
-                    if (rr >= a.M) break;
-                    const float inv2 = lrow[i] > 0.f ? 1.f / lrow[i] : 0.f;
-                    const int jq2 = rr / G, gi2 = rr - jq2 * G;
-                    const size_t od2 = (((size_t)b * a.n_q + jq2) * a.Hq + (size_t)h * G + gi2);
-                    uint2 v2;
-                    v2.x = pack_bf16x2(o[i].x * inv2, o[i].y * inv2);
-                    v2.y = pack_bf16x2(o[i].z * inv2, o[i].w * inv2);
-                    reinterpret_cast<uint2 *>(a.out + od2 * kD)[lane] = v2;
-                    if (lane == 0 && a.lse) a.lse[od2] = (mrow[i] + __log2f(lrow[i])) * 0.69314718055994530942f;
-                }
-            }
-        }
     } else if (warp >= kPrepWarp0) {
         // ================================================= query split
         // Thread r turns query row r of a landed slot (bf16, two 128-byte
@@ -1000,9 +954,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if ((warp & 3) < 2) {
         // ================================================= softmax
-        // column slot sl: pages 0-3, 4-5 or 6-7 of each block
-        const int quarter = warp & 3, sl = (warp >> 2) - 1;
-        softmax_role(sm, a, tmem, quarter, sl, sl == 0 ? 0 : 2 + 2 * sl, sl == 0 ? 4 : 2);
+        // column slot warp / 4: pages 2 slot, 2 slot + 1 of each block
+        softmax_role(sm, a, tmem, warp & 3, warp >> 2);
     } else {
         // ================================================= V converters
         // Block j's E4M3 V pages -> one f16 tile in the MMA's layout (page p
