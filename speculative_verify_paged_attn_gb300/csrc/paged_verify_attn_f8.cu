@@ -175,6 +175,18 @@ __device__ __forceinline__ bool try_wait_suspend(uint64_t *bar, uint32_t parity)
         : "memory");
     return ok != 0;
 }
+// One probe that suspends the thread for up to `ns` nanoseconds, returning
+// early when the phase completes.
+__device__ __forceinline__ bool try_wait_for(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, int32_t *err) {
     if (try_wait_suspend(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
@@ -823,24 +835,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 {
                     const unsigned long long t0 = global_ns();
                     while (true) {
-                        bool progress = false;
                         if (!next_done &&
                             mbar_test(&sm.k8_full[(j + 1) % kNK8], (uint32_t)(((j + 1) / kNK8) & 1))) {
                             const BlockMeta &mn = sm.meta[(j + 1) % kNMeta];
                             if ((mn.flags & kFlagEnd) || !(mn.flags & kFlagFirst) ||
                                 mbar_test(&sm.q_ready[(unit + 1) & 1], par_of(unit + 1))) {
                                 ok = issue_s(j + 1, unit1, nxt);
-                                next_done = progress = true;
+                                next_done = true;
                                 if (!ok) break;
                             }
                         }
-                        if (mbar_test(&sm.p_full, (uint32_t)(j & 1))) break;
+                        // once S_{j+1} is out, sleep until P_j is published; before,
+                        // wake at least every 0.2 us to look at K_{j+1} again
+                        if (try_wait_for(&sm.p_full, (uint32_t)(j & 1), next_done ? kSuspendNs : 200u)) break;
                         if (global_ns() - t0 > kWaitLimitNs) {
                             raise_error(a.err, SVPA_DEVERR_TIMEOUT);
                             ok = false;
                             break;
                         }
-                        if (!progress) __nanosleep(32);
                     }
                     if (!ok) break;
                 }
