@@ -58,6 +58,7 @@
 
 #include <algorithm>
 #include <cstddef>
+#include <type_traits>
 
 #include "svpa_device.cuh"
 #include "svpa_internal.h"
@@ -73,7 +74,6 @@ constexpr int kRows = 128;                  // MMA M
 constexpr int kPage8 = 16 * 128;            // one E4M3 (page, kv head) tile
 constexpr int kTile8 = kPB * kPage8;        // E4M3 block: 16 KB
 constexpr int kTile16 = kNB * kD * 2;       // f16 V block: 32 KB
-constexpr int kNK8 = 4;                     // K ring (read by the MMA)
 constexpr int kNV8 = 3;                     // V staging ring
 constexpr int kNV = 2;                      // f16 V tiles
 constexpr int kNMeta = 8;                   // block descriptors in flight
@@ -88,9 +88,10 @@ constexpr int kPrepWarp0 = 14;              // 14, 15
 // P (at most 2^8 under the lazy maximum) times a V scale stays below the f16
 // maximum 65504
 constexpr float kMaxVScale8 = 255.f;
-// arrivals that complete a K ring slot: the producer's expect_tx, and one
-// cp.async arrival per page for each of its two page scales
-constexpr uint32_t kStageArrivalsK = 1 + 2 * kPB;
+// V tile scales times 448 stay below the f16 maximum (V is converted to f16
+// with its tile scales)
+constexpr float kMaxTileScale8 = 146.f;
+constexpr int kTileScales = 16 * 2;         // tile scales of one (page, kv head): 16 rows x 2 halves
 constexpr float kRescaleLog2 = 8.f;         // rescale O when a maximum grows by > 2^8
 // TMEM columns: O 0..127 (one buffer: the epilogue drains a unit's O before
 // the next unit's first P V), S[0] 128..255, S[1] 256..383, P[0] 384..447,
@@ -106,9 +107,30 @@ struct BlockMeta {
     int32_t pad[3];
 };
 
+// TILES: one scale per 64-element tile of a row (K and V) instead of one per
+// (page, kv head)
+template <bool TILES>
+struct F8Cfg {
+    static constexpr int kNK8 = TILES ? 3 : 4;  // K ring (read by the MMA)
+    // arrivals that complete a K ring slot: the producer's expect_tx and, with
+    // per-page scales, one cp.async arrival per page for each of its two page
+    // scales (tile scales come by bulk copies counted in the slot's bytes)
+    static constexpr uint32_t kStageArrivalsK = TILES ? 1 : 1 + 2 * kPB;
+};
+
+// tile scales of the blocks in flight: K's by block (the softmax applies them
+// to the scores), V's by staging slot (the converters apply them)
+struct alignas(16) TileScalesF8 {
+    float k[kNMeta][kPB][kTileScales];
+    float v[kNV8][kPB][kTileScales];
+};
+struct NoTileScalesF8 {};
+
+template <bool TILES>
 struct SmemF8 {
+    using C = F8Cfg<TILES>;
     uint8_t q[2][kQSlot];                    // 1024-aligned query slots
-    uint8_t k8[kNK8][kTile8];
+    uint8_t k8[C::kNK8][kTile8];
     uint8_t v8[kNV8][kTile8];
     uint8_t vbuf[kNV][kTile16];
     float ksc[kNMeta][kPB];                   // page scales of the blocks in flight
@@ -116,7 +138,7 @@ struct SmemF8 {
     float qscale[kNQScale][64];               // 2^-e of each query row, per unit in flight
     float xmax[2][2][4][32];                  // [quadrant][block parity][column slot][lane]
     float lsum[2][4][32];                     // [quadrant][column slot][lane]: partial row sums at a unit's end
-    uint64_t k8_full[kNK8], k8_empty[kNK8];
+    uint64_t k8_full[C::kNK8], k8_empty[C::kNK8];
     uint64_t v8_full[kNV8], v8_empty[kNV8];
     uint64_t v_full[kNV], v_empty[kNV];
     uint64_t q_full[2], q_ready[2], q_empty[2];
@@ -127,17 +149,22 @@ struct SmemF8 {
     uint64_t lbar[2];                         // the quadrant's partial row sums exchanged
     uint64_t gbar;                            // the eight softmax warps (split pieces' ticket)
     uint64_t xbar[2][2];                      // [quadrant][block parity]
+    uint64_t s_read;                          // TILES: the softmax has read S (one S buffer)
     BlockMeta meta[kNMeta];
     int32_t vid[kNMeta][kPB];                 // page ids of a block, for its V copies
     int32_t q_is_end[2];                      // the producer's end marker on a query slot
     uint32_t tmem_base;
     int32_t last;
+    typename std::conditional<TILES, TileScalesF8, NoTileScalesF8>::type t64;
 };
 
-static_assert(sizeof(SmemF8) + 1024 <= 232448, "pva_f8_kernel shared memory");
-static_assert(offsetof(SmemF8, k8) % 1024 == 0 && offsetof(SmemF8, v8) % 1024 == 0 &&
-                  offsetof(SmemF8, vbuf) % 1024 == 0,
+static_assert(sizeof(SmemF8<false>) + 1024 <= 232448, "pva_f8_kernel shared memory");
+static_assert(sizeof(SmemF8<true>) + 1024 <= 232448, "pva_f8_kernel shared memory");
+static_assert(offsetof(SmemF8<false>, k8) % 1024 == 0 && offsetof(SmemF8<false>, v8) % 1024 == 0 &&
+                  offsetof(SmemF8<false>, vbuf) % 1024 == 0 && offsetof(SmemF8<true>, v8) % 1024 == 0 &&
+                  offsetof(SmemF8<true>, vbuf) % 1024 == 0,
               "swizzled tiles start on 1024-byte boundaries");
+static_assert(offsetof(SmemF8<true>, t64) % 16 == 0, "bulk copies land on 16-byte boundaries");
 
 // Instruction descriptors: fp32 D; kind::f8f6f4 with A and B E4M3, both
 // K-major; kind::f16 with A and B f16, B MN-major.
@@ -208,17 +235,27 @@ __device__ __forceinline__ uint32_t e4m3x2_of(float lo, float hi) {
 
 // The producer's V copies: V of the oldest block whose K is out, if its
 // staging slot is free (a non-blocking test); warp-collective.
-__device__ __forceinline__ bool producer_try_issue_v(SmemF8 &sm, const CUtensorMap *mvp, uint64_t pol, int &jv, int jk) {
+template <bool TILES>
+__device__ __forceinline__ bool producer_try_issue_v(SmemF8<TILES> &sm, const CUtensorMap *mvp, const float *v_scale,
+                                                     int num_blocks, int Hkv, uint64_t pol, int &jv, int jk) {
     const int lane = threadIdx.x & 31;
     if (jv >= jk) return false;
     const int vs = jv % kNV8;
     int ready = 1;
     if (lane == 0 && jv >= kNV8) ready = mbar_test(&sm.v8_empty[vs], (uint32_t)(((jv / kNV8) & 1) ^ 1));
     if (!__shfl_sync(0xffffffffu, ready, 0)) return false;
-    if (lane == 0) mbar_arrive_expect_tx(&sm.v8_full[vs], kTile8);
+    if (lane == 0) mbar_arrive_expect_tx(&sm.v8_full[vs], kTile8 + (TILES ? kPB * kTileScales * 4 : 0u));
     if (lane < kPB) {
         const int id = sm.vid[jv % kNMeta][lane], hh = sm.meta[jv % kNMeta].h;
         tma_load_4d(sm.v8[vs] + lane * kPage8, mvp, 0, 0, hh, id, &sm.v8_full[vs], pol);
+        if constexpr (TILES) {
+            // the page's 32 tile scales (a missing page takes the block's
+            // first page's: its bytes are zero)
+            const int id0 = __shfl_sync(0x000000ffu, id, 0);
+            const int sid = (id >= 0 && id < num_blocks) ? id : id0;
+            bulk_copy_g2s(sm.t64.v[vs][lane], v_scale + ((size_t)sid * Hkv + hh) * kTileScales, kTileScales * 4,
+                          &sm.v8_full[vs]);
+        }
     }
     __syncwarp();
     ++jv;
@@ -227,15 +264,18 @@ __device__ __forceinline__ bool producer_try_issue_v(SmemF8 &sm, const CUtensorM
 
 // Bounded wait (warp-collective) for phase `parity` of `bar`, issuing V
 // copies meanwhile.
-__device__ __forceinline__ bool producer_wait_issuing_v(SmemF8 &sm, const CUtensorMap *mvp, uint64_t pol, int &jv,
-                                                     int jk, uint64_t *bar, uint32_t parity, int32_t *err) {
+template <bool TILES>
+__device__ __forceinline__ bool producer_wait_issuing_v(SmemF8<TILES> &sm, const CUtensorMap *mvp,
+                                                        const float *v_scale, int num_blocks, int Hkv, uint64_t pol,
+                                                        int &jv, int jk, uint64_t *bar, uint32_t parity,
+                                                        int32_t *err) {
     const int lane = threadIdx.x & 31;
     unsigned long long t0 = 0;
     while (true) {
         int done = 0;
         if (lane == 0) done = mbar_test(bar, parity);
         if (__shfl_sync(0xffffffffu, done, 0)) return true;
-        if (producer_try_issue_v(sm, mvp, pol, jv, jk)) {
+        if (producer_try_issue_v<TILES>(sm, mvp, v_scale, num_blocks, Hkv, pol, jv, jk)) {
             t0 = 0;
             continue;
         }
@@ -257,11 +297,13 @@ __device__ __forceinline__ bool producer_wait_issuing_v(SmemF8 &sm, const CUtens
 // S_jj's TMEM buffer held S_{jj-2}, which the softmax has read once it
 // published P_{jj-2}: the issuer waited for that before P V_{jj-2}, so S_jj
 // needs no further wait (P lives in buffers of its own).
-__device__ __forceinline__ bool mma_issue_s(SmemF8 &sm, int32_t *err, uint32_t tmem, int jj, int &unit_jj,
+template <bool TILES>
+__device__ __forceinline__ bool mma_issue_s(SmemF8<TILES> &sm, int32_t *err, uint32_t tmem, int jj, int &unit_jj,
                                          BlockMeta &m) {
     constexpr uint32_t idS = idesc_e4m3(kRows, kNB);
-    const int ks = jj % kNK8;
-    if (!wait_phase(&sm.k8_full[ks], (uint32_t)((jj / kNK8) & 1), err)) return false;
+    constexpr int NK8 = F8Cfg<TILES>::kNK8;
+    const int ks = jj % NK8;
+    if (!wait_phase(&sm.k8_full[ks], (uint32_t)((jj / NK8) & 1), err)) return false;
     m = sm.meta[jj % kNMeta];
     if (m.flags & kFlagEnd) {
         mbar_arrive(&sm.s_full[jj & 1]);
@@ -271,17 +313,24 @@ __device__ __forceinline__ bool mma_issue_s(SmemF8 &sm, int32_t *err, uint32_t t
         ++unit_jj;
         if (!wait_phase(&sm.q_ready[unit_jj & 1], par_of(unit_jj), err)) return false;
     }
+    // TILES: one S buffer, which the softmax has read for S_{jj-1}
+    if (TILES && jj >= 1 && !wait_phase(&sm.s_read, (uint32_t)((jj - 1) & 1), err)) return false;
     tc_fence_after();
     const uint32_t qa = smem_u32(sm.q[unit_jj & 1]);
     const uint32_t ka = smem_u32(sm.k8[ks]);
-    const uint32_t dS = tmem + kTmemS + (uint32_t)(jj & 1) * kNB;
-    // two query terms x four 32-byte K steps, one accumulation
+    const uint32_t dS = tmem + kTmemS + (TILES ? 0u : (uint32_t)(jj & 1) * kNB);
+    // two query terms x four 32-byte K steps, one accumulation; TILES: the
+    // head dimensions 0-63 (K steps 0, 1) into S0 and 64-127 into S1, the
+    // tile scales of a token's two halves being applied by the softmax
 #pragma unroll
     for (int step = 0; step < 8; ++step) {
         const int term = step >> 2, kk = step & 3;
         const uint64_t ad = umma_desc_sw128(qa + term * kQSlab + kk * 32, 16, 1024);
         const uint64_t bd = umma_desc_sw128(ka + kk * 32, 16, 1024);
-        umma_e4m3(dS, ad, bd, idS, step > 0 ? 1u : 0u);
+        if constexpr (TILES)
+            umma_e4m3(dS + (uint32_t)(kk >> 1) * kNB, ad, bd, idS, (term | (kk & 1)) ? 1u : 0u);
+        else
+            umma_e4m3(dS, ad, bd, idS, step > 0 ? 1u : 0u);
     }
     umma_commit(&sm.k8_empty[ks]);
     umma_commit(&sm.s_full[jj & 1]);
@@ -316,7 +365,8 @@ __device__ __forceinline__ bool soft_sync(uint64_t *bar, uint32_t &phase, int32_
 // block (pages 2 sl, 2 sl + 1).  The eight warps share this one body and its
 // code is kept small (one 32-column chunk per block, nothing unrolled twice):
 // every role's hot loop must stay in its SM sub-partition's instruction cache.
-__device__ __noinline__ void softmax_role(SmemF8 &sm, const AttnArgs &a, uint32_t tmem, int quarter, int sl) {
+template <bool TILES>
+__device__ __noinline__ void softmax_role(SmemF8<TILES> &sm, const AttnArgs &a, uint32_t tmem, int quarter, int sl) {
     const int lane = threadIdx.x & 31;
     const int r = quarter * 32 + lane;  // query row == TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -341,18 +391,52 @@ __device__ __noinline__ void softmax_role(SmemF8 &sm, const AttnArgs &a, uint32_
             rowmul = a.scale_log2 * sm.qscale[unit % kNQScale][r];
         }
         tc_fence_after();
-        const uint32_t sa = tmem + kTmemS + (uint32_t)(j & 1) * kNB + lane_off + (uint32_t)tok0;
+        const uint32_t sa = tmem + kTmemS + (TILES ? 0u : (uint32_t)(j & 1) * kNB) + lane_off + (uint32_t)tok0;
         // the page scales of this slot's pages came with K_j's staging, which
-        // S_j's completion follows
-        const float ka = sm.ksc[j % kNMeta][pg0], kb = sm.ksc[j % kNMeta][pg0 + 1];
-        const float va = sm.vsc[j % kNMeta][pg0], vb = sm.vsc[j % kNMeta][pg0 + 1];
-        if (quarter == 0 && lane == 0 &&
-            (!(ka >= 0.f && ka <= 3.0e38f) || !(kb >= 0.f && kb <= 3.0e38f) || !(va >= 0.f && va <= kMaxVScale8) ||
-             !(vb >= 0.f && vb <= kMaxVScale8)))
-            raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+        // S_j's completion follows (with tile scales the V scales are in the
+        // converted V and the K scales multiply the two halves' scores below)
+        float ka = 1.f, kb = 1.f, va = 1.f, vb = 1.f;
+        if constexpr (!TILES) {
+            ka = sm.ksc[j % kNMeta][pg0];
+            kb = sm.ksc[j % kNMeta][pg0 + 1];
+            va = sm.vsc[j % kNMeta][pg0];
+            vb = sm.vsc[j % kNMeta][pg0 + 1];
+            if (quarter == 0 && lane == 0 &&
+                (!(ka >= 0.f && ka <= 3.0e38f) || !(kb >= 0.f && kb <= 3.0e38f) ||
+                 !(va >= 0.f && va <= kMaxVScale8) || !(vb >= 0.f && vb <= kMaxVScale8)))
+                raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+        }
         uint32_t sc[32];
         tmem_ld32(sa, sc);
-        tmem_ld_wait();
+        if constexpr (TILES) {
+            // the scores of head dimensions 64-127 (S1) too; once both are in
+            // registers the MMA may write the next block's S
+            uint32_t s1[32];
+            tmem_ld32(sa + kNB, s1);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.s_read);
+            // token t of the slot (page pg0 + t / 16, row t % 16): S0 times the
+            // tile scale of its dimensions 0-63 plus S1 times that of 64-127
+            bool bad = false;
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                const float4 *ts = reinterpret_cast<const float4 *>(sm.t64.k[j % kNMeta][pg0 + x]);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 v = ts[q4];  // rows 2 q4, 2 q4 + 1: (half 0, half 1) each
+                    const int t = 16 * x + 2 * q4;
+                    sc[t] = __float_as_uint(fmaf(__uint_as_float(s1[t]), v.y, __uint_as_float(sc[t]) * v.x));
+                    sc[t + 1] = __float_as_uint(fmaf(__uint_as_float(s1[t + 1]), v.w, __uint_as_float(sc[t + 1]) * v.z));
+                    bad |= !(v.x >= 0.f && v.x <= 3.0e38f) || !(v.y >= 0.f && v.y <= 3.0e38f) ||
+                           !(v.z >= 0.f && v.z <= 3.0e38f) || !(v.w >= 0.f && v.w <= 3.0e38f);
+                }
+            }
+            if (bad && quarter == 0 && lane == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+        } else {
+            tmem_ld_wait();
+        }
         if (md.pos0 + kNB > md.L || md.ntok < kNB) {
             // only on the blocks that reach the speculative slots or a partial
             // block: invisible tokens' scores -> -inf.  Visibility of this
@@ -604,13 +688,17 @@ __device__ __noinline__ void softmax_role(SmemF8 &sm, const AttnArgs &a, uint32_
     }
 }
 
+template <bool TILES>
 __global__ void __launch_bounds__(kThreads, 1)
     pva_f8_kernel(const __grid_constant__ CUtensorMap mkp, const __grid_constant__ CUtensorMap mvp,
                   const __grid_constant__ CUtensorMap mq0, const __grid_constant__ CUtensorMap mq1,
                   const __grid_constant__ AttnArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    SmemF8 &sm = *reinterpret_cast<SmemF8 *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SmemF8<TILES> &sm =
+        *reinterpret_cast<SmemF8<TILES> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kNK8 = F8Cfg<TILES>::kNK8;
+    constexpr uint32_t kStageArrivalsK = F8Cfg<TILES>::kStageArrivalsK;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNK8; ++i) {
@@ -642,6 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sm.p_empty, 1);
         mbar_init(&sm.p_free[0], 1);
         mbar_init(&sm.p_free[1], 1);
+        mbar_init(&sm.s_read, kSoftWarps);
         fence_mbar_init();
     }
     // query rows past M are never written by the copies: keep them zero
@@ -677,9 +766,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             cp_async_4(dst, scales + (size_t)sid * a.Hkv + hh);
             cp_async_mbar_arrive_noinc(bar);
         };
-        auto try_issue_v = [&]() -> bool { return producer_try_issue_v(sm, &mvp, pol, jv, jk); };
+        auto try_issue_v = [&]() -> bool {
+            return producer_try_issue_v<TILES>(sm, &mvp, a.v_scale, a.num_blocks, a.Hkv, pol, jv, jk);
+        };
         auto wait_issuing_v = [&](uint64_t *bar, uint32_t parity) -> bool {
-            return producer_wait_issuing_v(sm, &mvp, pol, jv, jk, bar, parity, a.err);
+            return producer_wait_issuing_v<TILES>(sm, &mvp, a.v_scale, a.num_blocks, a.Hkv, pol, jv, jk, bar, parity,
+                                                  a.err);
         };
         // This CTA's share of the work: blocks [xs, xe) of the flat order
         // (sequence, kv head, block), W blocks in all split evenly over the
@@ -759,13 +851,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         m.pos0 = (page0 + i0 + j0) * kBlockSize;
                         m.ntok = min(kPB, n - (i0 + j0)) * kBlockSize;
                         m.flags = (bi == 0 ? kFlagFirst : 0) | (bi == nblk - 1 ? kFlagLast : 0);
-                        mbar_arrive_expect_tx(&sm.k8_full[ks], kTile8);
+                        mbar_arrive_expect_tx(&sm.k8_full[ks], kTile8 + (TILES ? kPB * kTileScales * 4 : 0u));
                     }
                     if (lane < kPB) {
                         sm.vid[jk % kNMeta][lane] = my_id;
                         tma_load_4d(sm.k8[ks] + lane * kPage8, &mkp, 0, 0, h, my_id, &sm.k8_full[ks], pol);
-                        copy_scale(a.k_scale, my_id, h, &sm.ksc[jk % kNMeta][lane], &sm.k8_full[ks]);
-                        copy_scale(a.v_scale, my_id, h, &sm.vsc[jk % kNMeta][lane], &sm.k8_full[ks]);
+                        if constexpr (TILES) {
+                            // the page's 32 K tile scales by a bulk copy counted in the
+                            // slot's bytes (a missing page takes the block's first page's)
+                            const int id0 = __shfl_sync(0x000000ffu, my_id, 0);
+                            const int sid = (my_id >= 0 && my_id < a.num_blocks) ? my_id : id0;
+                            bulk_copy_g2s(sm.t64.k[jk % kNMeta][lane],
+                                          a.k_scale + ((size_t)sid * a.Hkv + h) * kTileScales, kTileScales * 4,
+                                          &sm.k8_full[ks]);
+                        } else {
+                            copy_scale(a.k_scale, my_id, h, &sm.ksc[jk % kNMeta][lane], &sm.k8_full[ks]);
+                            copy_scale(a.v_scale, my_id, h, &sm.vsc[jk % kNMeta][lane], &sm.k8_full[ks]);
+                        }
                     }
                     __syncwarp();
                     ++jk;
@@ -821,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idPV = idesc_f16_bmn(kRows, kD);
             auto issue_s = [&](int jj, int &unit_jj, BlockMeta &m) -> bool {
-                return mma_issue_s(sm, a.err, tmem, jj, unit_jj, m);
+                return mma_issue_s<TILES>(sm, a.err, tmem, jj, unit_jj, m);
             };
             BlockMeta cur, nxt;
             int j = 0, unit = -1;
@@ -835,8 +937,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 {
                     const unsigned long long t0 = global_ns();
                     while (true) {
+                        // (TILES: the one S buffer must have been read, S_j's phase of s_read)
                         if (!next_done &&
-                            mbar_test(&sm.k8_full[(j + 1) % kNK8], (uint32_t)(((j + 1) / kNK8) & 1))) {
+                            mbar_test(&sm.k8_full[(j + 1) % kNK8], (uint32_t)(((j + 1) / kNK8) & 1)) &&
+                            (!TILES || mbar_test(&sm.s_read, (uint32_t)(j & 1)))) {
                             const BlockMeta &mn = sm.meta[(j + 1) % kNMeta];
                             if ((mn.flags & kFlagEnd) || !(mn.flags & kFlagFirst) ||
                                 mbar_test(&sm.q_ready[(unit + 1) & 1], par_of(unit + 1))) {
@@ -967,7 +1071,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if ((warp & 3) < 2) {
         // ================================================= softmax
         // column slot warp / 4: pages 2 slot, 2 slot + 1 of each block
-        softmax_role(sm, a, tmem, warp & 3, warp >> 2);
+        softmax_role<TILES>(sm, a, tmem, warp & 3, warp >> 2);
     } else {
         // ================================================= V converters
         // Block j's E4M3 V pages -> one f16 tile in the MMA's layout (page p
@@ -1011,6 +1115,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     hi.y = e4m3x2_to_f16x2(e[u].z >> 16);
                     hi.z = e4m3x2_to_f16x2(e[u].w & 0xffffu);
                     hi.w = e4m3x2_to_f16x2(e[u].w >> 16);
+                    if constexpr (TILES) {
+                        if (row < t_end) {
+                            // this group's 64-element tile: (page, row, half) of the
+                            // block (rows past the last token keep their zeros)
+                            const float tsc = sm.t64.v[s8][row >> 4][(row & 15) * 2 + (g >> 2)];
+                            if (!(tsc >= 0.f && tsc <= kMaxTileScale8)) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+                            const uint32_t t2 = pack_f16x2(tsc, tsc);
+                            lo.x = mul_f16x2(lo.x, t2);
+                            lo.y = mul_f16x2(lo.y, t2);
+                            lo.z = mul_f16x2(lo.z, t2);
+                            lo.w = mul_f16x2(lo.w, t2);
+                            hi.x = mul_f16x2(hi.x, t2);
+                            hi.y = mul_f16x2(hi.y, t2);
+                            hi.z = mul_f16x2(hi.z, t2);
+                            hi.w = mul_f16x2(hi.w, t2);
+                        }
+                    }
                     const int r8 = row & 7, c0 = (g & 3) * 2;
                     uint8_t *dst = tile + (row >> 3) * 2048 + (g >> 2) * 1024 + r8 * 128;
                     *reinterpret_cast<uint4 *>(dst + ((c0 ^ r8) << 4)) = lo;
@@ -1087,7 +1208,21 @@ __global__ void __launch_bounds__(1024) streamk_prefix_kernel(const int32_t *con
 
 }  // namespace
 
-size_t attn_f8_smem_bytes() { return sizeof(SmemF8) + 1024; }
+namespace {
+template <bool TILES>
+cudaError_t launch_f8(const AttnMaps &m, const AttnArgs &a, int grid, cudaStream_t st) {
+    const size_t smem = sizeof(SmemF8<TILES>) + 1024;
+    static DeviceMemo<int> attr_set;  // the shared-memory opt-in, once per device
+    int done = 0;
+    cudaError_t e = attr_set.get(&done, [&](int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(pva_f8_kernel<TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (e != cudaSuccess) return e;
+    pva_f8_kernel<TILES><<<grid, kThreads, smem, st>>>(m.k[0], m.v[0], m.q[0], m.q[1], a);
+    return cudaGetLastError();
+}
+}  // namespace
 
 cudaError_t launch_streamk_prefix(const int32_t *context_lens, int B, int n_q, int Hkv, int max_blocks,
                                   long long *prefix, int32_t *err, cudaStream_t st) {
@@ -1095,18 +1230,10 @@ cudaError_t launch_streamk_prefix(const int32_t *context_lens, int B, int n_q, i
     return cudaGetLastError();
 }
 
-// FP8 pages with per-(page, kv head) scales, head_dim 128, G * n_q <= 64
+// FP8 pages, head_dim 128, G * n_q <= 64: one scale per (page, kv head), or
+// (scale_tile 64) one per 64-element tile of a row
 cudaError_t launch_paged_verify_attn_f8(const AttnMaps &m, const AttnArgs &a, int grid, cudaStream_t st) {
-    const size_t smem = sizeof(SmemF8) + 1024;
-    static DeviceMemo<int> attr_set;  // the shared-memory opt-in, once per device
-    int done = 0;
-    cudaError_t e = attr_set.get(&done, [&](int *v) {
-        *v = 1;
-        return cudaFuncSetAttribute(pva_f8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    });
-    if (e != cudaSuccess) return e;
-    pva_f8_kernel<<<grid, kThreads, smem, st>>>(m.k[0], m.v[0], m.q[0], m.q[1], a);
-    return cudaGetLastError();
+    return a.scale_tile ? launch_f8<true>(m, a, grid, st) : launch_f8<false>(m, a, grid, st);
 }
 
 }  // namespace svpa

@@ -125,11 +125,11 @@ svpa_status plan_attn(const svpa_attn_params *p, AttnPlan *pl) {
     // unit starts at once and the extra launch buys nothing)
     pl->ordered = pl->max_splits == 1 && p->batch > 1 && p->batch <= kMaxOrderedSeqs &&
                   units > (size_t)pl->grid_slots;
-    // FP8 pages with per-page scales on the tcgen05 kernel: the blocks of all
+    // FP8 pages on the tcgen05 kernel: the blocks of all
     // (sequence, kv head) pairs are split evenly over the grid (no split
     // size, no ordering): [per-sequence block prefix, int64][pieces' (max,
     // sum)][pieces' accumulators], two piece slots per CTA
-    pl->streamk = pl->use_tc && eb == 1 && p->scale_tile == 0;
+    pl->streamk = pl->use_tc && eb == 1;
     if (pl->streamk) {
         pl->ordered = false;
         pl->split_pages = 0;
