@@ -418,8 +418,11 @@ __device__ __noinline__ void softmax_role(SmemF8<TILES> &sm, const AttnArgs &a, 
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.s_read);
             // token t of the slot (page pg0 + t / 16, row t % 16): S0 times the
-            // tile scale of its dimensions 0-63 plus S1 times that of 64-127
-            bool bad = false;
+            // tile scale of its dimensions 0-63 plus S1 times that of 64-127.
+            // Quadrant 0's warps check the scales they use: a finite scale >= 0
+            // is, as an unsigned word, at most 0x7f7fffff (sign bit clear,
+            // exponent below 255).
+            uint32_t worst = 0u;
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
                 const float4 *ts = reinterpret_cast<const float4 *>(sm.t64.k[j % kNMeta][pg0 + x]);
@@ -429,11 +432,12 @@ __device__ __noinline__ void softmax_role(SmemF8<TILES> &sm, const AttnArgs &a, 
                     const int t = 16 * x + 2 * q4;
                     sc[t] = __float_as_uint(fmaf(__uint_as_float(s1[t]), v.y, __uint_as_float(sc[t]) * v.x));
                     sc[t + 1] = __float_as_uint(fmaf(__uint_as_float(s1[t + 1]), v.w, __uint_as_float(sc[t + 1]) * v.z));
-                    bad |= !(v.x >= 0.f && v.x <= 3.0e38f) || !(v.y >= 0.f && v.y <= 3.0e38f) ||
-                           !(v.z >= 0.f && v.z <= 3.0e38f) || !(v.w >= 0.f && v.w <= 3.0e38f);
+                    if (quarter == 0)
+                        worst = max(max(worst, max(__float_as_uint(v.x), __float_as_uint(v.y))),
+                                    max(__float_as_uint(v.z), __float_as_uint(v.w)));
                 }
             }
-            if (bad && quarter == 0 && lane == 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+            if (quarter == 0 && lane == 0 && worst > 0x7f7fffffu) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
         } else {
             tmem_ld_wait();
         }
