@@ -66,11 +66,11 @@ KERNEL_LABELS = {"pva_kernel": "pva_kernel (warp-level MMA)", "pva_tc_kernel": "
 
 def attn_kernel_name(params, wl) -> str:
     """The attention kernel the library runs for these parameters: the warp-level
-    MMA kernel, or on the tcgen05 path the FP8 kernel for pages with one scale
-    per page and the general tcgen05 kernel otherwise."""
+    MMA kernel, or on the tcgen05 path the FP8 kernel for FP8 pages and the
+    bf16 tcgen05 kernel otherwise."""
     if svpa.attn_kernel(params) != 2:
         return "pva_kernel"
-    return "pva_f8_kernel" if wl.kv_fp8 and not wl.scale_tile else "pva_tc_kernel"
+    return "pva_f8_kernel" if wl.kv_fp8 else "pva_tc_kernel"
 SHARED_SOURCES = ["speculative_verify_paged_attn_gb300/csrc/svpa_device.cuh",
                   "speculative_verify_paged_attn_gb300/csrc/svpa_api.cu"]
 

@@ -95,7 +95,7 @@ typedef struct svpa_attn_params {
     float sm_scale;             /* softmax scale, normally 1/sqrt(D)          */
     int32_t split_pages;        /* pages per KV split; 0 = chosen by library
                                    (not used by the tcgen05 kernel for FP8
-                                   pages with one scale per page)              */
+                                   pages)                                      */
     int32_t variant;            /* 0 = chosen by library; 1 = warp-level MMA
                                    kernel; 2 = tcgen05/TMEM kernel (head_dim
                                    128; FP8 pages with Hq / Hkv * n_q <= 64)   */
@@ -165,23 +165,21 @@ svpa_status svpa_attn_workspace_size(const svpa_attn_params *p, size_t *bytes);
  *  lse          fp32 [B, n_q, Hq] natural-log sum of exp(scores), or NULL
  *  workspace    device scratch of at least svpa_attn_workspace_size() bytes
  * Accumulation is fp32; the contraction runs on the tensor cores.  FP8
- * pages on the tcgen05 kernels:
- *  - one scale per page (scale_tile 0): the scores are an E4M3 MMA on the
- *    stored K bytes against each query row split into two E4M3 terms at a
- *    power-of-two scale of its own (any finite |q|); the K scale multiplies
- *    the scores in fp32 (any finite scale >= 0); V is converted exactly to
- *    f16 and P (at most 2^8 under the kernel's lazy maximum) times the V
- *    scale is formed in f16, so a V scale above 255 (or a negative or NaN
- *    K or V scale) raises SVPA_DEVERR_BAD_VALUE.  split_pages is not used:
- *    the blocks of all (sequence, kv head) pairs are split evenly over the
- *    GPU's SMs.
- *  - one scale per 64-element tile (scale_tile 64): K and V are
- *    dequantised to f16 with their tile scales and the queries and P are
- *    f16: a scale above 146 (448 * scale would pass the f16 maximum) or a
- *    negative/NaN scale raises SVPA_DEVERR_BAD_VALUE, and |q| must stay
- *    below 65504.
- * The warp-level kernel (variant 1) applies the scales in fp32 and has
- * none of these limits.  The kernels cannot see the scales before they run,
+ * pages on the tcgen05 kernel: the scores are an E4M3 MMA on the stored K
+ * bytes against each query row split into two E4M3 terms at a power-of-two
+ * scale of its own (any finite |q|); K scales multiply the scores in fp32
+ * (any finite scale >= 0; with tile scales, each 64-dimension half of a
+ * token's scores by its own scale); V is converted exactly to f16 and P
+ * (at most 2^8 under the kernel's lazy maximum) is f16:
+ *  - one scale per page (scale_tile 0): P times the V scale is formed in
+ *    f16, so a V scale above 255 raises SVPA_DEVERR_BAD_VALUE;
+ *  - one scale per 64-element tile (scale_tile 64): V is converted with its
+ *    tile scales, so a V tile scale above 146 (448 * scale would pass the
+ *    f16 maximum) raises SVPA_DEVERR_BAD_VALUE;
+ * a negative or NaN scale raises it too.  split_pages is not used there:
+ * the blocks of all (sequence, kv head) pairs are split evenly over the
+ * GPU's SMs.  The warp-level kernel (variant 1) applies the scales in fp32
+ * and has none of these limits.  The kernels cannot see the scales before they run,
  * so this is the caller's contract: with FP8 pages whose scales may pass
  * those limits, set variant = 1.
  */

@@ -380,7 +380,7 @@ svpa_status svpa_paged_verify_attn(const svpa_attn_params *p, const void *q, con
     }
     if (pl.use_tc) {
         const int grid = std::max(1, std::min(pl.grid_slots, a.total_units));
-        return from_cuda(launch_paged_verify_attn_tc(maps, a, grid, fp8, static_cast<cudaStream_t>(stream)));
+        return from_cuda(launch_paged_verify_attn_tc(maps, a, grid, static_cast<cudaStream_t>(stream)));
     }
     AttnLaunch lp;
     if (attn_plan_launch(D, fp8, pl.M, &lp) != cudaSuccess) return SVPA_ERR_CUDA;

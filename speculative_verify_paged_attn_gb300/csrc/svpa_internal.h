@@ -116,8 +116,7 @@ cudaError_t attn_plan_launch(int head_dim, bool fp8, int M, AttnLaunch *out);
 constexpr int kMaxOrderedSeqs = 4096;
 cudaError_t launch_seq_order(const int32_t *context_lens, int B, int32_t *order, cudaStream_t stream);
 // tcgen05 / TMEM variant (bf16 pages, head_dim 128, one CTA per SM).
-cudaError_t launch_paged_verify_attn_tc(const AttnMaps &maps, const AttnArgs &a, int grid, bool fp8,
-                                        cudaStream_t stream);
+cudaError_t launch_paged_verify_attn_tc(const AttnMaps &maps, const AttnArgs &a, int grid, cudaStream_t stream);
 // tcgen05 / TMEM variant for FP8 pages with one scale per (page, kv head):
 // E4M3 scores MMA on the staged K pages, G * n_q <= 64, one CTA per SM.
 cudaError_t launch_paged_verify_attn_f8(const AttnMaps &maps, const AttnArgs &a, int grid, cudaStream_t stream);
