@@ -75,7 +75,7 @@ constexpr int kPage8 = 16 * 128;            // one E4M3 (page, kv head) tile
 constexpr int kTile8 = kPB * kPage8;        // E4M3 block: 16 KB
 constexpr int kTile16 = kNB * kD * 2;       // f16 V block: 32 KB
 constexpr int kNV8 = 3;                     // V staging ring
-constexpr int kNV = 2;                      // f16 V tiles
+constexpr int kNV = 2;                      // f16 V tiles (tile j & 1; freed by P V_j's p_free signal)
 constexpr int kNMeta = 8;                   // block descriptors in flight
 constexpr int kQSlab = 64 * 128;            // one 128-byte column slab of 64 query rows
 constexpr int kQSlot = 2 * kQSlab;          // one unit's queries (bf16, then the two E4M3 terms)
@@ -140,11 +140,13 @@ struct SmemF8 {
     float lsum[2][4][32];                     // [quadrant][column slot][lane]: partial row sums at a unit's end
     uint64_t k8_full[C::kNK8], k8_empty[C::kNK8];
     uint64_t v8_full[kNV8], v8_empty[kNV8];
-    uint64_t v_full[kNV], v_empty[kNV];
+    uint64_t v_full[kNV];
     uint64_t q_full[2], q_ready[2], q_empty[2];
     uint64_t s_full[2];
-    uint64_t p_full, p_empty;
-    uint64_t p_free[2];                       // P[x] read by its P V (PV_j commits to p_free[j & 1])
+    uint64_t p_full;
+    // P V_j done (its commit arrives on p_free[j & 1]): P[j & 1], the f16 V
+    // tile j & 1 and O's P V_j contribution are then free / complete
+    uint64_t p_free[2];
     uint64_t o_full, o_empty;
     uint64_t lbar[2];                         // the quadrant's partial row sums exchanged
     uint64_t gbar;                            // the eight softmax warps (split pieces' ticket)
@@ -297,31 +299,36 @@ __device__ __forceinline__ bool producer_wait_issuing_v(SmemF8<TILES> &sm, const
 // S_jj's TMEM buffer held S_{jj-2}, which the softmax has read once it
 // published P_{jj-2}: the issuer waited for that before P V_{jj-2}, so S_jj
 // needs no further wait (P lives in buffers of its own).
+// `ready`: the caller has seen K_jj land (and, for a unit's first block, its
+// queries split, and with TILES the one S buffer read) and loaded the block's
+// descriptor into m.
 template <bool TILES>
 __device__ __forceinline__ bool mma_issue_s(SmemF8<TILES> &sm, int32_t *err, uint32_t tmem, int jj, int &unit_jj,
-                                         BlockMeta &m) {
+                                         BlockMeta &m, bool ready) {
     constexpr uint32_t idS = idesc_e4m3(kRows, kNB);
     constexpr int NK8 = F8Cfg<TILES>::kNK8;
     const int ks = jj % NK8;
-    if (!wait_phase(&sm.k8_full[ks], (uint32_t)((jj / NK8) & 1), err)) return false;
-    m = sm.meta[jj % kNMeta];
+    if (!ready) {
+        if (!wait_phase(&sm.k8_full[ks], (uint32_t)((jj / NK8) & 1), err)) return false;
+        m = sm.meta[jj % kNMeta];
+    }
     if (m.flags & kFlagEnd) {
         mbar_arrive(&sm.s_full[jj & 1]);
         return true;
     }
     if (m.flags & kFlagFirst) {
         ++unit_jj;
-        if (!wait_phase(&sm.q_ready[unit_jj & 1], par_of(unit_jj), err)) return false;
+        if (!ready && !wait_phase(&sm.q_ready[unit_jj & 1], par_of(unit_jj), err)) return false;
     }
     // TILES: one S buffer, which the softmax has read for S_{jj-1}
-    if (TILES && jj >= 1 && !wait_phase(&sm.s_read, (uint32_t)((jj - 1) & 1), err)) return false;
+    if (TILES && !ready && jj >= 1 && !wait_phase(&sm.s_read, (uint32_t)((jj - 1) & 1), err)) return false;
     tc_fence_after();
-    const uint32_t qa = smem_u32(sm.q[unit_jj & 1]);
-    const uint32_t ka = smem_u32(sm.k8[ks]);
     const uint32_t dS = tmem + kTmemS + (TILES ? 0u : (uint32_t)(jj & 1) * kNB);
     // two query terms x four 32-byte K steps, one accumulation; TILES: the
     // head dimensions 0-63 (K steps 0, 1) into S0 and 64-127 into S1, the
     // tile scales of a token's two halves being applied by the softmax
+    const uint32_t qa = smem_u32(sm.q[unit_jj & 1]);
+    const uint32_t ka = smem_u32(sm.k8[ks]);
 #pragma unroll
     for (int step = 0; step < 8; ++step) {
         const int term = step >> 2, kk = step & 3;
@@ -530,7 +537,7 @@ __device__ __noinline__ void softmax_role(SmemF8<TILES> &sm, const AttnArgs &a, 
         if (__any_sync(0xffffffffu, rescale)) {
             const float f = rescale ? alpha : 1.f;
             // O (TMEM) holds P_{<j} V; PV_{j-1} must have landed first
-            wait_phase(&sm.p_empty, (uint32_t)((j - 1) & 1), a.err);
+            wait_phase(&sm.p_free[(j - 1) & 1], par_of(j - 1), a.err);
             tc_fence_after();
             const uint32_t oa = tmem + kTmemO + lane_off + (uint32_t)tok0;
             uint32_t raw[32];
@@ -542,9 +549,9 @@ __device__ __noinline__ void softmax_role(SmemF8<TILES> &sm, const AttnArgs &a, 
         }
         tmem_st_wait();
         // P_j is published only once PV_{j-1} has completed (PV_j cannot have
-        // started), which keeps the MMA issuer's p_full and p_empty waits
-        // unambiguous
-        if (j >= 1) wait_phase(&sm.p_empty, (uint32_t)((j - 1) & 1), a.err);
+        // started), which keeps the MMA issuer's p_full wait and every wait on
+        // p_free unambiguous
+        if (j >= 1) wait_phase(&sm.p_free[(j - 1) & 1], par_of(j - 1), a.err);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.p_full);
@@ -715,7 +722,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kNV; ++i) {
             mbar_init(&sm.v_full[i], kConvWarps);
-            mbar_init(&sm.v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.q_full[i], 1);
@@ -731,7 +737,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sm.lbar[1], 4);
         mbar_init(&sm.gbar, kSoftWarps);
         mbar_init(&sm.p_full, kSoftWarps);
-        mbar_init(&sm.p_empty, 1);
         mbar_init(&sm.p_free[0], 1);
         mbar_init(&sm.p_free[1], 1);
         mbar_init(&sm.s_read, kSoftWarps);
@@ -926,12 +931,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================================================= MMA issuer
         if (lane == 0) {
             constexpr uint32_t idPV = idesc_f16_bmn(kRows, kD);
-            auto issue_s = [&](int jj, int &unit_jj, BlockMeta &m) -> bool {
-                return mma_issue_s<TILES>(sm, a.err, tmem, jj, unit_jj, m);
+            auto issue_s = [&](int jj, int &unit_jj, BlockMeta &m, bool ready) -> bool {
+                return mma_issue_s<TILES>(sm, a.err, tmem, jj, unit_jj, m, ready);
             };
             BlockMeta cur, nxt;
             int j = 0, unit = -1;
-            bool ok = issue_s(0, unit, cur);
+            bool ok = issue_s(0, unit, cur, false);
             while (ok && !(cur.flags & kFlagEnd)) {
                 int unit1 = unit;
                 // wait for P_j, issuing S_{j+1} meanwhile as soon as K_{j+1}
@@ -939,16 +944,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // P V_j never waits for the next block's data
                 bool next_done = false;
                 {
-                    const unsigned long long t0 = global_ns();
+                    unsigned long long t0 = 0;  // the wall clock is read only once P_j is waited for
                     while (true) {
                         // (TILES: the one S buffer must have been read, S_j's phase of s_read)
                         if (!next_done &&
                             mbar_test(&sm.k8_full[(j + 1) % kNK8], (uint32_t)(((j + 1) / kNK8) & 1)) &&
                             (!TILES || mbar_test(&sm.s_read, (uint32_t)(j & 1)))) {
-                            const BlockMeta &mn = sm.meta[(j + 1) % kNMeta];
-                            if ((mn.flags & kFlagEnd) || !(mn.flags & kFlagFirst) ||
+                            nxt = sm.meta[(j + 1) % kNMeta];
+                            if ((nxt.flags & kFlagEnd) || !(nxt.flags & kFlagFirst) ||
                                 mbar_test(&sm.q_ready[(unit + 1) & 1], par_of(unit + 1))) {
-                                ok = issue_s(j + 1, unit1, nxt);
+                                ok = issue_s(j + 1, unit1, nxt, true);
                                 next_done = true;
                                 if (!ok) break;
                             }
@@ -956,7 +961,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // once S_{j+1} is out, sleep until P_j is published; before,
                         // wake at least every 0.2 us to look at K_{j+1} again
                         if (try_wait_for(&sm.p_full, (uint32_t)(j & 1), next_done ? kSuspendNs : 200u)) break;
-                        if (global_ns() - t0 > kWaitLimitNs) {
+                        const unsigned long long now = global_ns();
+                        if (t0 == 0) t0 = now;
+                        if (now - t0 > kWaitLimitNs) {
                             raise_error(a.err, SVPA_DEVERR_TIMEOUT);
                             ok = false;
                             break;
@@ -980,12 +987,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bd = umma_desc_sw128(va + kt * 4096, 1024, 2048);
                     umma_bf16_tmem_a(dO, pt + kt * 8, bd, idPV, ((cur.flags & kFlagFirst) && kt == 0) ? 0u : 1u);
                 }
-                umma_commit(&sm.v_empty[vs]);
-                umma_commit(&sm.p_empty);
                 umma_commit(&sm.p_free[j & 1]);
                 if (cur.flags & kFlagLast) umma_commit(&sm.o_full);
                 if (!next_done) {
-                    ok = issue_s(j + 1, unit1, nxt);
+                    ok = issue_s(j + 1, unit1, nxt, false);
                     if (!ok) break;
                 }
                 ++j;
@@ -1088,8 +1093,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0;; ++j) {
             const int s8 = j % kNV8, tb = j % kNV;
             if (!wait_phase(&sm.v8_full[s8], (uint32_t)((j / kNV8) & 1), a.err)) break;
-            // the tile is free once PV of block j - kNV is done
-            if (j >= kNV && !wait_phase(&sm.v_empty[tb], (uint32_t)(((j / kNV) & 1) ^ 1), a.err)) break;
+            // the tile is free once PV of block j - 2 is done
+            if (j >= kNV && !wait_phase(&sm.p_free[tb], par_of(j - 2), a.err)) break;
             const BlockMeta md = sm.meta[j % kNMeta];
             if (md.flags & kFlagEnd) break;
             const uint8_t *src = sm.v8[s8];
