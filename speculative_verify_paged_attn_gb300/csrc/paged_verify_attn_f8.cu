@@ -44,14 +44,17 @@
 //                   both page scales (cp.async) into a 4-deep K ring that the
 //                   MMA reads directly, and the V page tiles into a 3-deep
 //                   staging ring;
-//   warp 3          MMA issuer (one thread) and TMEM owner: S_j into one of
-//                   two TMEM S buffers as soon as K_j and the unit's split
-//                   queries are ready; O += P_j V_j with P_j read from TMEM;
+//   warp 3          P V issuer (one thread) and TMEM owner: O += P_j V_j with
+//                   P_j read from TMEM, once P_j is published and V_j converted;
+//   warp 14         score issuer (one thread): S_j into one of two TMEM S
+//                   buffers as soon as K_j, the unit's split queries and the
+//                   buffer are ready (two issuing threads, so that neither
+//                   chain of waits and issues holds up the other);
 //   warps 6,7,10,11 V converters: E4M3 -> f16 (exact) in the MMA's tile
 //                   layout, rows past the sequence's end zeroed;
-//   warps 14, 15    query split: one thread per query row turns the landed
-//                   bf16 row into its two E4M3 terms in place and records
-//                   its scale.
+//   warp 15         query split: each thread turns two landed bf16 query
+//                   rows into their two E4M3 terms in place and records
+//                   their scales.
 // All waits are bounded; nothing spins forever.
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -81,10 +84,12 @@ constexpr int kQSlab = 64 * 128;            // one 128-byte column slab of 64 qu
 constexpr int kQSlot = 2 * kQSlab;          // one unit's queries (bf16, then the two E4M3 terms)
 constexpr int kNQScale = 4;                 // query-scale records in flight
 constexpr int kThreads = 512;
-constexpr int kProducerWarp = 2, kMmaWarp = 3;
+constexpr int kProducerWarp = 2;
+constexpr int kMmaWarp = 3;                 // P V issuer, TMEM owner
+constexpr int kSWarp = 14;                  // score MMA issuer
 constexpr int kSoftWarps = 8;               // 0, 1, 4, 5, 8, 9, 12, 13 (warp % 4 = quadrant, warp / 4 = column slot)
 constexpr int kConvWarps = 4;               // 6, 7, 10, 11
-constexpr int kPrepWarp0 = 14;              // 14, 15
+constexpr int kPrepWarp = 15;               // query split
 // P (at most 2^8 under the lazy maximum) times a V scale stays below the f16
 // maximum 65504
 constexpr float kMaxVScale8 = 255.f;
@@ -143,7 +148,7 @@ struct SmemF8 {
     uint64_t v_full[kNV];
     uint64_t q_full[2], q_ready[2], q_empty[2];
     uint64_t s_full[2];
-    uint64_t p_full;
+    uint64_t p_full[2];                       // P_j published (p_full[j & 1])
     // P V_j done (its commit arrives on p_free[j & 1]): P[j & 1], the f16 V
     // tile j & 1 and O's P V_j contribution are then free / complete
     uint64_t p_free[2];
@@ -201,18 +206,6 @@ __device__ __forceinline__ bool try_wait_suspend(uint64_t *bar, uint32_t parity)
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
-        : "memory");
-    return ok != 0;
-}
-// One probe that suspends the thread for up to `ns` nanoseconds, returning
-// early when the phase completes.
-__device__ __forceinline__ bool try_wait_for(uint64_t *bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
         : "memory");
     return ok != 0;
 }
@@ -294,34 +287,32 @@ __device__ __forceinline__ bool producer_wait_issuing_v(SmemF8<TILES> &sm, const
     }
 }
 
-// The MMA issuer's S_jj = (Q_hi + Q_lo) K_jj^T once K_jj has landed and, on a
-// unit's first block, its queries are split (or the end marker forwarded).
-// S_jj's TMEM buffer held S_{jj-2}, which the softmax has read once it
-// published P_{jj-2}: the issuer waited for that before P V_{jj-2}, so S_jj
-// needs no further wait (P lives in buffers of its own).
-// `ready`: the caller has seen K_jj land (and, for a unit's first block, its
-// queries split, and with TILES the one S buffer read) and loaded the block's
-// descriptor into m.
+// The score issuer's S_jj = (Q_hi + Q_lo) K_jj^T once K_jj has landed, its
+// TMEM buffer is free and, on a unit's first block, its queries are split (or
+// the end marker forwarded).  Per-page scales: S_jj's buffer held S_{jj-2},
+// which the softmax has read once it published P_{jj-2} (p_full[jj & 1]; P_jj
+// cannot be published before S_jj, so the parity is unambiguous).  Tile
+// scales: the one buffer, read for S_{jj-1} (s_read).  The buffer is waited
+// for before the end marker too, so that the softmax never sees s_full two
+// phases ahead.
 template <bool TILES>
 __device__ __forceinline__ bool mma_issue_s(SmemF8<TILES> &sm, int32_t *err, uint32_t tmem, int jj, int &unit_jj,
-                                         BlockMeta &m, bool ready) {
+                                         BlockMeta &m) {
     constexpr uint32_t idS = idesc_e4m3(kRows, kNB);
     constexpr int NK8 = F8Cfg<TILES>::kNK8;
     const int ks = jj % NK8;
-    if (!ready) {
-        if (!wait_phase(&sm.k8_full[ks], (uint32_t)((jj / NK8) & 1), err)) return false;
-        m = sm.meta[jj % kNMeta];
-    }
+    if (!wait_phase(&sm.k8_full[ks], (uint32_t)((jj / NK8) & 1), err)) return false;
+    m = sm.meta[jj % kNMeta];
+    if (TILES && jj >= 1 && !wait_phase(&sm.s_read, (uint32_t)((jj - 1) & 1), err)) return false;
+    if (!TILES && jj >= 2 && !wait_phase(&sm.p_full[jj & 1], par_of(jj - 2), err)) return false;
     if (m.flags & kFlagEnd) {
         mbar_arrive(&sm.s_full[jj & 1]);
         return true;
     }
     if (m.flags & kFlagFirst) {
         ++unit_jj;
-        if (!ready && !wait_phase(&sm.q_ready[unit_jj & 1], par_of(unit_jj), err)) return false;
+        if (!wait_phase(&sm.q_ready[unit_jj & 1], par_of(unit_jj), err)) return false;
     }
-    // TILES: one S buffer, which the softmax has read for S_{jj-1}
-    if (TILES && !ready && jj >= 1 && !wait_phase(&sm.s_read, (uint32_t)((jj - 1) & 1), err)) return false;
     tc_fence_after();
     const uint32_t dS = tmem + kTmemS + (TILES ? 0u : (uint32_t)(jj & 1) * kNB);
     // two query terms x four 32-byte K steps, one accumulation; TILES: the
@@ -389,7 +380,14 @@ __device__ __noinline__ void softmax_role(SmemF8<TILES> &sm, const AttnArgs &a, 
     while (true) {
         if (!wait_phase(&sm.s_full[j & 1], par_of(j), a.err)) break;
         const BlockMeta md = sm.meta[j % kNMeta];
-        if (md.flags & kFlagEnd) break;
+        if (md.flags & kFlagEnd) {
+            // the end marker, forwarded to the P V issuer on p_full[j & 1] once
+            // P V_{j-2} is done (so that p_full is never two phases ahead of it)
+            if (j >= 2) wait_phase(&sm.p_free[j & 1], par_of(j - 2), a.err);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.p_full[j & 1]);
+            break;
+        }
         const bool first = (md.flags & kFlagFirst) != 0;
         if (first) {
             ++unit;
@@ -536,7 +534,8 @@ __device__ __noinline__ void softmax_role(SmemF8<TILES> &sm, const AttnArgs &a, 
         // warp rescales the O columns of its own slot
         if (__any_sync(0xffffffffu, rescale)) {
             const float f = rescale ? alpha : 1.f;
-            // O (TMEM) holds P_{<j} V; PV_{j-1} must have landed first
+            // O (TMEM) holds P_{<j} V; PV_{j-1} must have landed first (PV_{j-2}
+            // has: P[j & 1] was free above, so the parity is unambiguous)
             wait_phase(&sm.p_free[(j - 1) & 1], par_of(j - 1), a.err);
             tc_fence_after();
             const uint32_t oa = tmem + kTmemO + lane_off + (uint32_t)tok0;
@@ -548,13 +547,9 @@ __device__ __noinline__ void softmax_role(SmemF8<TILES> &sm, const AttnArgs &a, 
             tmem_st32(oa, raw);
         }
         tmem_st_wait();
-        // P_j is published only once PV_{j-1} has completed (PV_j cannot have
-        // started), which keeps the MMA issuer's p_full wait and every wait on
-        // p_free unambiguous
-        if (j >= 1) wait_phase(&sm.p_free[(j - 1) & 1], par_of(j - 1), a.err);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.p_full);
+        if (lane == 0) mbar_arrive(&sm.p_full[j & 1]);
         ++j;
         if (!(md.flags & kFlagLast)) continue;
 
@@ -725,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.q_full[i], 1);
-            mbar_init(&sm.q_ready[i], 2);
+            mbar_init(&sm.q_ready[i], 1);
             mbar_init(&sm.q_empty[i], 1);
             mbar_init(&sm.s_full[i], 1);
             mbar_init(&sm.xbar[i][0], 4);
@@ -736,7 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sm.lbar[0], 4);
         mbar_init(&sm.lbar[1], 4);
         mbar_init(&sm.gbar, kSoftWarps);
-        mbar_init(&sm.p_full, kSoftWarps);
+        mbar_init(&sm.p_full[0], kSoftWarps);
+        mbar_init(&sm.p_full[1], kSoftWarps);
         mbar_init(&sm.p_free[0], 1);
         mbar_init(&sm.p_free[1], 1);
         mbar_init(&sm.s_read, kSoftWarps);
@@ -928,52 +924,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == kMmaWarp) {
-        // ================================================= MMA issuer
+        // ================================================= P V issuer
+        // O += P_j V_j once the softmax has published P_j (or forwarded the end
+        // marker) and V_j is converted; a unit's first P V overwrites O, whose
+        // previous unit must have been drained
         if (lane == 0) {
             constexpr uint32_t idPV = idesc_f16_bmn(kRows, kD);
-            auto issue_s = [&](int jj, int &unit_jj, BlockMeta &m, bool ready) -> bool {
-                return mma_issue_s<TILES>(sm, a.err, tmem, jj, unit_jj, m, ready);
-            };
-            BlockMeta cur, nxt;
-            int j = 0, unit = -1;
-            bool ok = issue_s(0, unit, cur, false);
-            while (ok && !(cur.flags & kFlagEnd)) {
-                int unit1 = unit;
-                // wait for P_j, issuing S_{j+1} meanwhile as soon as K_{j+1}
-                // (and, for a unit's first block, its split queries) are there;
-                // P V_j never waits for the next block's data
-                bool next_done = false;
-                {
-                    unsigned long long t0 = 0;  // the wall clock is read only once P_j is waited for
-                    while (true) {
-                        // (TILES: the one S buffer must have been read, S_j's phase of s_read)
-                        if (!next_done &&
-                            mbar_test(&sm.k8_full[(j + 1) % kNK8], (uint32_t)(((j + 1) / kNK8) & 1)) &&
-                            (!TILES || mbar_test(&sm.s_read, (uint32_t)(j & 1)))) {
-                            nxt = sm.meta[(j + 1) % kNMeta];
-                            if ((nxt.flags & kFlagEnd) || !(nxt.flags & kFlagFirst) ||
-                                mbar_test(&sm.q_ready[(unit + 1) & 1], par_of(unit + 1))) {
-                                ok = issue_s(j + 1, unit1, nxt, true);
-                                next_done = true;
-                                if (!ok) break;
-                            }
-                        }
-                        // once S_{j+1} is out, sleep until P_j is published; before,
-                        // wake at least every 0.2 us to look at K_{j+1} again
-                        if (try_wait_for(&sm.p_full, (uint32_t)(j & 1), next_done ? kSuspendNs : 200u)) break;
-                        const unsigned long long now = global_ns();
-                        if (t0 == 0) t0 = now;
-                        if (now - t0 > kWaitLimitNs) {
-                            raise_error(a.err, SVPA_DEVERR_TIMEOUT);
-                            ok = false;
-                            break;
-                        }
-                    }
-                    if (!ok) break;
+            int unit = -1;
+            for (int j = 0;; ++j) {
+                if (!wait_phase(&sm.p_full[j & 1], par_of(j), a.err)) break;
+                // (block j's descriptor stays until P V_j is done: the producer
+                // reuses its slot only after S_{j+4}, which follows P_{j+2},
+                // which waits for P V_j)
+                const int flags = sm.meta[j % kNMeta].flags;
+                if (flags & kFlagEnd) break;
+                if (flags & kFlagFirst) {
+                    ++unit;
+                    if (unit >= 1 && !wait_phase(&sm.o_empty, (uint32_t)((unit - 1) & 1), a.err)) break;
                 }
-                // a unit's first P V overwrites O: the previous unit's O must be drained
-                if ((cur.flags & kFlagFirst) && unit >= 1 && !wait_phase(&sm.o_empty, (uint32_t)((unit - 1) & 1), a.err))
-                    break;
                 const int vs = j % kNV;
                 if (!wait_phase(&sm.v_full[vs], (uint32_t)((j / kNV) & 1), a.err)) break;
                 tc_fence_after();
@@ -985,34 +953,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kt = 0; kt < kNB / 16; ++kt) {
                     const uint64_t bd = umma_desc_sw128(va + kt * 4096, 1024, 2048);
-                    umma_bf16_tmem_a(dO, pt + kt * 8, bd, idPV, ((cur.flags & kFlagFirst) && kt == 0) ? 0u : 1u);
+                    umma_bf16_tmem_a(dO, pt + kt * 8, bd, idPV, ((flags & kFlagFirst) && kt == 0) ? 0u : 1u);
                 }
                 umma_commit(&sm.p_free[j & 1]);
-                if (cur.flags & kFlagLast) umma_commit(&sm.o_full);
-                if (!next_done) {
-                    ok = issue_s(j + 1, unit1, nxt, false);
-                    if (!ok) break;
-                }
-                ++j;
-                unit = unit1;
-                cur = nxt;
+                if (flags & kFlagLast) umma_commit(&sm.o_full);
             }
         }
         __syncwarp();
-    } else if (warp >= kPrepWarp0) {
+    } else if (warp == kSWarp) {
+        // ================================================= score issuer
+        if (lane == 0) {
+            int unit = -1;
+            for (int jj = 0;; ++jj) {
+                BlockMeta m;
+                if (!mma_issue_s<TILES>(sm, a.err, tmem, jj, unit, m)) break;
+                if (m.flags & kFlagEnd) break;
+            }
+        }
+        __syncwarp();
+    } else if (warp == kPrepWarp) {
         // ================================================= query split
-        // Thread r turns query row r of a landed slot (bf16, two 128-byte
-        // column slabs) into q * 2^e = hi + lo: hi the row rounded to E4M3,
+        // Thread l takes query rows l and l + 32 of a landed slot in turn (bf16,
+        // two 128-byte column slabs), turning row r into q * 2^e = hi + lo: hi
+        // the row rounded to E4M3,
         // lo the remainder rounded to E4M3, with 2^e the power of two that
         // puts the row's largest magnitude in [128, 256) (below the E4M3
         // maximum 448).  hi overwrites slab 0 and lo slab 1 of the same row,
         // each as 128 E4M3 bytes in the 128-byte-swizzled K-major layout the
         // MMA reads; 2^-e goes to the softmax with the unit.
-        const int r = (warp - kPrepWarp0) * 32 + lane;
         for (int nu = 0;; ++nu) {
             const int qs = nu & 1;
             if (!wait_phase(&sm.q_full[qs], par_of(nu), a.err)) break;
             if (sm.q_is_end[qs]) break;
+#pragma unroll 1
+            for (int rr = 0; rr < 2; ++rr) {
+            const int r = rr * 32 + lane;
             float inv_scale = 1.f;
             if (r < a.M) {
                 uint8_t *row0 = &sm.q[qs][r * 128];
@@ -1072,7 +1047,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(row1 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
             }
-            if (r < 64) sm.qscale[nu % kNQScale][r] = inv_scale;
+            sm.qscale[nu % kNQScale][r] = inv_scale;
+            }
             fence_proxy_async_smem();  // the MMA reads the terms through the async proxy
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.q_ready[qs]);
