@@ -709,19 +709,27 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
                      (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
     const bool lead = g.rank == 0 && threadIdx.x == 0;
     cluster_arrive_on_entry();
-    // the row's node tokens and uniforms, and per child of the node being
-    // visited Q(x_c) and P(x_c) (each node is some node's child at most once,
-    // so no entry is rewritten)
+    // the row's node tokens and uniforms, and for every node c > 0 Q(x_c) and
+    // P(x_c) in the rows of its parent (the tree is known up front, so these
+    // gathers are made once, all in flight together, rather than one
+    // dependent round of loads per visited node; parents precede their
+    // children and every parent has a draft row)
     __shared__ int s_x[kMaxNq];
     __shared__ float s_ua[kMaxNq], s_qx[kMaxNq], s_px[kMaxNq];
     if (threadIdx.x < (unsigned)n_nodes) {
-        int x = ntok[threadIdx.x];
+        const int c = (int)threadIdx.x;
+        int x = ntok[c];
         if (x < 0 || x >= V) {
-            if (g.rank == 0 && threadIdx.x > 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
+            if (g.rank == 0 && c > 0) raise_error(a.err, SVPA_DEVERR_BAD_VALUE);
             x = 0;
         }
-        s_x[threadIdx.x] = x;
-        s_ua[threadIdx.x] = __ldg(a.u_acc + (size_t)b * n_nodes + threadIdx.x);
+        s_x[c] = x;
+        s_ua[c] = __ldg(a.u_acc + (size_t)b * n_nodes + c);
+        if (c > 0) {
+            const int pn = a.parent[c];
+            s_qx[c] = __ldg(a.q + ((size_t)b * a.n_internal + a.qrow[pn]) * V + x);
+            s_px[c] = __ldg(a.p + ((size_t)b * n_nodes + pn) * V + x);
+        }
     }
     const float u_s = __ldg(a.u_s + b);
     __syncthreads();
@@ -744,14 +752,6 @@ __global__ void __launch_bounds__(kClThreads, kClCtasPerSm)
             break;
         }
         const float *Qn = a.q + ((size_t)b * a.n_internal + qr) * V;
-        {
-            const int c = node + 1 + (int)threadIdx.x;
-            if (c < n_nodes && a.parent[c] == node) {
-                s_qx[c] = __ldg(Qn + s_x[c]);
-                s_px[c] = __ldg(Pn + s_x[c]);
-            }
-            __syncthreads();
-        }
         double Z = 1.0;
         float rx = 0.f;  // R(x) of the child under test, after a rejection
         int accepted = -1, tested = 0;
