@@ -891,9 +891,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) try_issue_v();
         }
         if (lane == 0) {
-            // end-of-work markers: on the K ring (for the MMA issuer and, through
-            // S, the softmax), the V staging ring (converters) and the next
-            // query slot (query split)
+            // end-of-work markers: on the K ring (for the score issuer and,
+            // through S, the softmax, which forwards it to the P V issuer), the
+            // V staging ring (converters) and the next query slot (query split)
             const int ks = jk % kNK8;
             if (ok && jk >= kNK8) ok = wait_phase(&sm.k8_empty[ks], (uint32_t)(((jk / kNK8) & 1) ^ 1), a.err);
             if (ok) {
@@ -1131,8 +1131,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    // every TMEM user is done (the MMA issuer's last operations were waited
-    // on by the softmax and epilogue warps) before the owner frees it
+    // every TMEM user is done (the issuers' last operations were waited on
+    // by the softmax and epilogue warps) before the owner frees it
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
